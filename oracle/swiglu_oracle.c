@@ -1,0 +1,262 @@
+/*
+ * CPU oracle for the fused SwiGLU up-projection.  TEST INFRASTRUCTURE ONLY.
+ *
+ * Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline / reference
+ * arm may load this library.  The CUDA library never links, includes or calls
+ * it, and this file includes nothing from the CUDA side: its bf16 codec, its
+ * silu and its loops are its own.
+ *
+ * What it computes (plain definitions, fp64 throughout):
+ *
+ *   "Tile-Level Activation Overlap for Efficient LLM Inference", technical
+ *   summary, section "Enonce du probleme": Y = SiLU(A x W1) (.) (A x W2),
+ *   two independent GEMMs followed by an element-wise product.  Here
+ *   A = x [M, d], W1 = W_gate [d, d_ff], W2 = W_up [d, d_ff], Y = h [M, d_ff].
+ *
+ *   "1 . Anatomie d'un transformeur sur GPU", section 1.1 (the layer skeleton,
+ *   "Wgate, Wup -> SwiGLU") and section 1.2 (each projection is a
+ *   (bS x d).(d x d') GEMM; gate and up cost 2 bS d d_ff FLOP each).
+ *
+ *   "Ou part le temps d'un token", section "Un kernel pour les matrices
+ *   etroites": the weight b is indexed (k)*cols + col, i.e. row-major
+ *   [K, N] with N contiguous.  The same section states the comparison rule
+ *   (tolerance scaled by |a|.|b|), which is why this oracle also returns the
+ *   first-order sensitivity s of each output to accumulation error.
+ *
+ * Readings taken where the pages are silent (each is listed in the design doc):
+ *   - SiLU(z) = z * sigma(z) = z / (1 + exp(-z))  (Swish with beta = 1).
+ *   - SiLU applies to x.W_gate; x.W_up enters linearly.
+ *   - g and u are never rounded; only h is rounded (round-to-nearest-even)
+ *     to the output type.
+ *
+ * Every product of two bf16 (8-bit significand) or two f32 (24-bit) values is
+ * exact in fp64 (53-bit significand); each sum runs over k in ascending order.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+
+/* ---- number formats ---------------------------------------------------- */
+
+/* A bf16 value is the upper 16 bits of an IEEE-754 binary32 value. */
+double oracle_bf16_to_f64(uint16_t bits) {
+  uint32_t w = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return (double)f;
+}
+
+static uint16_t f32_bits_hi(float f) {
+  uint32_t w;
+  memcpy(&w, &f, sizeof w);
+  return (uint16_t)(w >> 16);
+}
+
+/*
+ * Round an fp64 value straight to bf16, to nearest, ties to even (one
+ * rounding: no intermediate f32).  bf16 keeps 8 significant bits with the
+ * binary32 exponent range; below 2^-126 the spacing is fixed at 2^-133.
+ */
+uint16_t oracle_f64_to_bf16(double v) {
+  if (isnan(v)) return (uint16_t)0x7FC0;
+  uint16_t sign = signbit(v) ? (uint16_t)0x8000 : (uint16_t)0;
+  double a = fabs(v);
+  if (a == 0.0) return sign;
+  if (isinf(a)) return (uint16_t)(sign | 0x7F80);
+  int ex;
+  frexp(a, &ex);          /* a = m * 2^ex, m in [0.5, 1): a in [2^(ex-1), 2^ex) */
+  int e = ex - 1;         /* a in [2^e, 2^(e+1)) */
+  int q = (e < -126) ? -133 : e - 7; /* exponent of one unit in the last place */
+  double n = nearbyint(ldexp(a, -q)); /* exact scaling; default mode is RNE */
+  double r = ldexp(n, q);
+  const double bf16_max = ldexp(255.0, 120); /* (2 - 2^-7) * 2^127 */
+  if (r > bf16_max) return (uint16_t)(sign | 0x7F80);
+  /* r now has at most 8 significant bits inside the binary32 range, so the
+     conversion to float is exact and the bf16 pattern is its upper half. */
+  return (uint16_t)(sign | (f32_bits_hi((float)r) & 0x7FFF));
+}
+
+static double load_elem(const void* p, int64_t idx, int dtype) {
+  if (dtype == ORACLE_BF16) return oracle_bf16_to_f64(((const uint16_t*)p)[idx]);
+  return (double)((const float*)p)[idx];
+}
+
+static void store_elem(void* p, int64_t idx, int dtype, double v) {
+  if (dtype == ORACLE_BF16)
+    ((uint16_t*)p)[idx] = oracle_f64_to_bf16(v);
+  else
+    ((float*)p)[idx] = (float)v; /* C conversion: round to nearest even */
+}
+
+/* ---- activation -------------------------------------------------------- */
+
+/* SiLU(z) = z * sigma(z) = z / (1 + e^-z).  For z -> -inf the quotient
+   tends to -0 (e^-z overflows to +inf), never NaN. */
+double oracle_silu64(double z) { return z / (1.0 + exp(-z)); }
+
+/* ---- fused definition ---------------------------------------------------- */
+
+typedef struct {
+  const void *x, *wg, *wu;
+  int64_t M, d, d_ff, j0, j1;
+  int dtype;
+  double *h64, *sens;
+  void* h_out;
+  int status;
+} job_t;
+
+/*
+ * For one block of output columns [j0, j1): for every row i, accumulate
+ * g = sum_k x[i,k] Wg[k,j] and u = sum_k x[i,k] Wu[k,j] with k ascending
+ * (the k loop runs outside the j loop only so that W is read along its
+ * contiguous rows; each element's sum still adds its terms in k order),
+ * then h = silu(g) * u.
+ *
+ * s = 1.1 * G * |u| + |silu(g)| * U, with G = sum_k |x||Wg| and
+ * U = sum_k |x||Wu|, bounds to first order how much h moves per unit of
+ * relative accumulation error in g and u (|silu'| <= 1.0999 everywhere).
+ */
+static void* fused_block(void* arg) {
+  job_t* jb = (job_t*)arg;
+  int64_t n = jb->j1 - jb->j0;
+  if (n <= 0) return NULL;
+  double* acc = (double*)malloc((size_t)n * 4 * sizeof(double));
+  if (!acc) { jb->status = 1; return NULL; }
+  double *g = acc, *u = acc + n, *G = acc + 2 * n, *U = acc + 3 * n;
+  for (int64_t i = 0; i < jb->M; ++i) {
+    memset(acc, 0, (size_t)n * 4 * sizeof(double));
+    for (int64_t k = 0; k < jb->d; ++k) {
+      double xv = load_elem(jb->x, i * jb->d + k, jb->dtype);
+      double ax = fabs(xv);
+      int64_t row = k * jb->d_ff + jb->j0;
+      for (int64_t t = 0; t < n; ++t) {
+        double wgv = load_elem(jb->wg, row + t, jb->dtype);
+        double wuv = load_elem(jb->wu, row + t, jb->dtype);
+        g[t] += xv * wgv;
+        u[t] += xv * wuv;
+        G[t] += ax * fabs(wgv);
+        U[t] += ax * fabs(wuv);
+      }
+    }
+    for (int64_t t = 0; t < n; ++t) {
+      double sg = oracle_silu64(g[t]);
+      double hv = sg * u[t];
+      int64_t o = i * jb->d_ff + jb->j0 + t;
+      if (jb->h64) jb->h64[o] = hv;
+      if (jb->sens) jb->sens[o] = 1.1 * G[t] * fabs(u[t]) + fabs(sg) * U[t];
+      if (jb->h_out) store_elem(jb->h_out, o, jb->dtype, hv);
+    }
+  }
+  free(acc);
+  return NULL;
+}
+
+/*
+ * h = silu(x . Wg) (.) (x . Wu) for all M x d_ff outputs.
+ *   x [M, d], Wg/Wu [d, d_ff], row-major, element type `dtype` (0 f32, 1 bf16).
+ *   h64  [M, d_ff] fp64 exact-input result (may be NULL)
+ *   h_out [M, d_ff] in `dtype`, RNE of h64 (may be NULL)
+ *   sens [M, d_ff] sensitivity s defined above (may be NULL)
+ * Column blocks are split across `nthreads` POSIX threads; the arithmetic of
+ * each output does not depend on the split.  Returns 0 on success.
+ */
+int oracle_swiglu_up(const void* x, const void* wg, const void* wu, int64_t M,
+                     int64_t d, int64_t d_ff, int dtype, double* h64,
+                     void* h_out, double* sens, int nthreads) {
+  if (M < 0 || d < 0 || d_ff < 0) return 2;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return 2;
+  if (M == 0 || d_ff == 0) return 0;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > d_ff) nthreads = (int)d_ff;
+  job_t* jobs = (job_t*)calloc((size_t)nthreads, sizeof(job_t));
+  pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  if (!jobs || !th) { free(jobs); free(th); return 1; }
+  for (int t = 0; t < nthreads; ++t) {
+    job_t* jb = &jobs[t];
+    jb->x = x; jb->wg = wg; jb->wu = wu;
+    jb->M = M; jb->d = d; jb->d_ff = d_ff; jb->dtype = dtype;
+    jb->j0 = d_ff * t / nthreads;
+    jb->j1 = d_ff * (t + 1) / nthreads;
+    jb->h64 = h64; jb->sens = sens; jb->h_out = h_out;
+  }
+  int rc = 0;
+  if (nthreads == 1) {
+    fused_block(&jobs[0]);
+  } else {
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+      if (pthread_create(&th[t], NULL, fused_block, &jobs[t]) != 0) { rc = 1; break; }
+      ++started;
+    }
+    for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  }
+  for (int t = 0; t < nthreads; ++t) rc |= jobs[t].status;
+  free(jobs);
+  free(th);
+  return rc;
+}
+
+/*
+ * The same definition evaluated only at n chosen outputs (rows[t], cols[t]),
+ * one k loop per output.  Used for full-size shapes, where every row of h is
+ * independent of the others and each output needs only one row of x and one
+ * column of each weight.
+ */
+int oracle_swiglu_up_at(const void* x, const void* wg, const void* wu, int64_t M,
+                        int64_t d, int64_t d_ff, int dtype, const int64_t* rows,
+                        const int64_t* cols, int64_t n, double* h64,
+                        double* sens) {
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return 2;
+  for (int64_t t = 0; t < n; ++t) {
+    int64_t i = rows[t], j = cols[t];
+    if (i < 0 || i >= M || j < 0 || j >= d_ff) return 2;
+    double g = 0, u = 0, G = 0, U = 0;
+    for (int64_t k = 0; k < d; ++k) {
+      double xv = load_elem(x, i * d + k, dtype);
+      double wgv = load_elem(wg, k * d_ff + j, dtype);
+      double wuv = load_elem(wu, k * d_ff + j, dtype);
+      g += xv * wgv;
+      u += xv * wuv;
+      G += fabs(xv) * fabs(wgv);
+      U += fabs(xv) * fabs(wuv);
+    }
+    double sg = oracle_silu64(g);
+    h64[t] = sg * u;
+    if (sens) sens[t] = 1.1 * G * fabs(u) + fabs(sg) * U;
+  }
+  return 0;
+}
+
+/* ---- unfused composition (the pages' baseline, without its bf16 rounding) */
+
+/* out[i, j] = sum_k a[i, k] * b[k, j], fp64, k ascending.  a [m, kd], b [kd, n]. */
+int oracle_gemm64(const void* a, const void* b, int64_t m, int64_t kd, int64_t n,
+                  int dtype, double* out) {
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return 2;
+  for (int64_t i = 0; i < m; ++i) {
+    double* o = out + i * n;
+    for (int64_t j = 0; j < n; ++j) o[j] = 0.0;
+    for (int64_t k = 0; k < kd; ++k) {
+      double av = load_elem(a, i * kd + k, dtype);
+      for (int64_t j = 0; j < n; ++j) o[j] += av * load_elem(b, k * n + j, dtype);
+    }
+  }
+  return 0;
+}
+
+/* h[t] = silu(g[t]) * u[t] over n elements. */
+void oracle_silu_mul64(const double* g, const double* u, int64_t n, double* h) {
+  for (int64_t t = 0; t < n; ++t) h[t] = oracle_silu64(g[t]) * u[t];
+}
+
+/* Round n fp64 values to `dtype` (RNE), writing the raw output elements. */
+int oracle_round_to_dtype(const double* v, int64_t n, int dtype, void* out) {
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return 2;
+  for (int64_t t = 0; t < n; ++t) store_elem(out, t, dtype, v[t]);
+  return 0;
+}
