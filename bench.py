@@ -1,0 +1,458 @@
+#!/usr/bin/env python
+"""Benchmark of the fused SwiGLU up-projection; prints ONE JSON line.
+
+Workload (one "step"): the bf16 decode sweep -- one call for each
+M in {1, 2, 4, 8, 16} at d=4096, d_ff=14336, weights N(0, 1/d) -- the
+configuration the headline metric (HBM GB/s at M <= 16) is quoted on.
+value = algorithmic bytes of all calls of all ranks / max-over-ranks time.
+Algorithmic bytes per call = 2 (2 d d_ff + M d + M d_ff) (weights read once,
+x read once, h written once).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own replica of the sweep (weak scaling, no
+collective on the data path); the max step time over ranks is reported.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+D, D_FF = 4096, 14336
+SWEEP = (1, 2, 4, 8, 16)
+WORKLOAD = "bf16_decode_d4096 (M in {1,2,4,8,16}, d=4096, d_ff=14336)"
+METRIC = "SwiGLU up-proj: HBM GB/s at M≤16, TFLOP/s at M≥512, % of roofline"
+L2_BYTES = 129 * 2 ** 20          # nominal; the measured value is read from the device
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the secondary per-config measurements")
+    ap.add_argument("--extra-iters", type=int, default=30)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd.insert(1, "--id=" + self.gpu_id)
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1] or self.samples
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i, v in enumerate(s[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_max_mhz": max(s[2] for s in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+def gpu_uuid(dev):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle on the same workload
+# ---------------------------------------------------------------------------
+
+_ORACLE_INPUTS = {}
+
+
+def _oracle_inputs(cols):
+    """Seeded sweep inputs (x per M, first `cols` weight columns), drawn once."""
+    if cols not in _ORACLE_INPUTS:
+        from swiglu_mlp_projection_gb300 import inputs
+        _, wg, wu = inputs.make_inputs(1, D, D_FF, "bf16", seed=0)
+        xs = {M: inputs.raw_bits(inputs.make_inputs(M, D, D_FF, "bf16", seed=0, x_only=True)[0])
+              for M in SWEEP}
+        _ORACLE_INPUTS[cols] = (xs, inputs.raw_bits(wg[:, :cols]), inputs.raw_bits(wu[:, :cols]))
+    return _ORACLE_INPUTS[cols]
+
+
+def oracle_sweep(cols, reps_budget_s):
+    """Time the oracle on the decode sweep restricted to the first `cols`
+    columns (full K); returns (GB/s, seconds, calls, threads)."""
+    import oracle
+    from swiglu_mlp_projection_gb300 import workload
+    xs, wg_s, wu_s = _oracle_inputs(cols)
+    threads = oracle.default_threads()
+    total_bytes, t_total, calls = 0, 0.0, 0
+    while True:
+        for M in SWEEP:
+            t0 = time.perf_counter()
+            oracle.swiglu_up(xs[M], wg_s, wu_s, oracle.BF16, nthreads=threads)
+            t_total += time.perf_counter() - t0
+            total_bytes += workload.algorithmic_bytes(M, D, cols, "bf16")
+            calls += 1
+        if t_total >= reps_budget_s:
+            break
+    return total_bytes / t_total / 1e9, t_total, calls, threads
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    # bounded: about 90 s of CPU work for the whole run, whatever K and W are
+    cols = 256
+    budget = min(2.0, max(0.05, 90.0 / max(args.steps + args.warmup, 1)))
+    for _ in range(args.warmup):
+        oracle_sweep(cols, 0.0)
+    vals, times = [], []
+    for _ in range(args.steps):
+        gbs, t, calls, threads = oracle_sweep(cols, budget)
+        vals.append(gbs)
+        times.append(t)
+    value = statistics.median(vals)
+    sample = ("decode sweep M in {1,2,4,8,16}, d=4096, first %d of 14336 columns, "
+              "repeated for >= %.1f s per step" % (cols, budget))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.median(times), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import swiglu_mlp_projection_gb300 as swg
+    from swiglu_mlp_projection_gb300 import inputs, workload
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    swg._lib.load()
+    peaks = load_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    num_sms = props.multi_processor_count
+    l2 = getattr(props, "L2_cache_size", L2_BYTES) or L2_BYTES
+
+    # weights: enough distinct copies that consecutive calls never find the
+    # previous call's weights in L2 (every copy is larger than L2 already)
+    w_bytes = 2 * D * D_FF * 2
+    n_copies = max(2, math.ceil(3 * l2 / w_bytes))
+    _, wg, wu = inputs.make_inputs(1, D, D_FF, "bf16", seed=0)
+    copies = [(wg.to(dev), wu.to(dev)) for _ in range(n_copies)]
+    xs_host = {M: inputs.make_inputs(M, D, D_FF, "bf16", seed=0, x_only=True)[0] for M in SWEEP}
+    xs = {M: xs_host[M].to(dev) for M in SWEEP}
+    hs = {M: torch.empty(M, D_FF, dtype=torch.bfloat16, device=dev) for M in SWEEP}
+    stream = torch.cuda.current_stream(dev)
+    step_bytes = sum(workload.algorithmic_bytes(M, D, D_FF, "bf16") for M in SWEEP)
+    launches_per_step = sum(swg.plan(M, D, D_FF, "bf16", "auto", num_sms)["launches"] for M in SWEEP)
+    paths = {M: swg.plan(M, D, D_FF, "bf16", "auto", num_sms)["path"] for M in SWEEP}
+
+    counter = [0]
+
+    def step():
+        for M in SWEEP:
+            wgc, wuc = copies[counter[0] % n_copies]
+            counter[0] += 1
+            swg.swiglu_up(xs[M], wgc, wuc, out=hs[M], stream=stream)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(gpu_uuid(dev))
+    sampler.start()
+    for _ in range(max(args.warmup, 3)):
+        step()
+    # keep the GPU busy ~1 s before timing so clock samples reflect load
+    torch.cuda.synchronize(dev)
+    t_settle = time.time()
+    settle_steps = 0
+    while time.time() - t_settle < 1.0:
+        for _ in range(20):
+            step()
+        settle_steps += 20
+        torch.cuda.synchronize(dev)
+
+    # ---- timed region: K steps, per-call events on the launching stream
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(SWEEP) * args.steps)]
+    start_ev, end_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    wall0 = time.time()
+    start_ev.record(stream)
+    i = 0
+    for _ in range(args.steps):
+        for M in SWEEP:
+            wgc, wuc = copies[counter[0] % n_copies]
+            counter[0] += 1
+            ev[i].record(stream)
+            swg.swiglu_up(xs[M], wgc, wuc, out=hs[M], stream=stream)
+            ev[i + 1].record(stream)
+            i += 2
+    end_ev.record(stream)
+    barrier()
+    wall1 = time.time()
+    total_ms = start_ev.elapsed_time(end_ev)
+    per_call_ms = {M: [] for M in SWEEP}
+    i = 0
+    for _ in range(args.steps):
+        for M in SWEEP:
+            per_call_ms[M].append(ev[i].elapsed_time(ev[i + 1]))
+            i += 2
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    kernel_ms = sum(sum(v) for v in per_call_ms.values())
+    achieved = step_bytes * args.steps / (kernel_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with pinned host buffers
+    xs_pin = {M: xs_host[M].pin_memory() for M in SWEEP}
+    hs_pin = {M: torch.empty(M, D_FF, dtype=torch.bfloat16).pin_memory() for M in SWEEP}
+    h2d = sum(M * D * 2 for M in SWEEP)
+    d2h = sum(M * D_FF * 2 for M in SWEEP)
+
+    def e2e_step():
+        for M in SWEEP:
+            wgc, wuc = copies[counter[0] % n_copies]
+            counter[0] += 1
+            xs[M].copy_(xs_pin[M], non_blocking=True)
+            swg.swiglu_up(xs[M], wgc, wuc, out=hs[M], stream=stream)
+            hs_pin[M].copy_(hs[M], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * step_bytes * args.steps / (e2e_ms * 1e-3) / 1e9
+    sampler.stop()
+    clocks = sampler.summary(wall0, wall1)
+
+    sweep = {}
+    for M in SWEEP:
+        ms = statistics.median(per_call_ms[M])
+        b = workload.algorithmic_bytes(M, D, D_FF, "bf16")
+        sweep[str(M)] = {"us": round(ms * 1e3, 2), "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
+                         "frac": round(b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                         "path": paths[M]}
+
+    extra = None
+    if not args.no_extra:
+        extra = other_configs(dev, peaks, l2, args.extra_iters)
+
+    if rank == 0:
+        cpu = cpu_baseline()
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "weights": "N(0,1/d) bf16, seed 0",
+                       "l2": "inputs larger than L2 (235 MB of weights per call) and %d weight "
+                             "copies rotated per call" % n_copies,
+                       "clock_settle_steps": settle_steps},
+            "roofline": {"bound": "hbm", "kernel": "swiglu_up call (%s)" % "+".join(
+                             sorted(set(paths.values()))),
+                         "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                         "peak_source": peaks["source"] + " (hbm_gbs, copy)",
+                         "timing": "CUDA events around each call on its stream"},
+            "sweep": sweep,
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h,
+                    "note": "x copied H2D and h copied D2H every call (pinned host buffers); "
+                            "weights resident in HBM"},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        if extra is not None:
+            line["other_configs"] = extra
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def other_configs(dev, peaks, l2, iters):
+    """Secondary measurements of the other workloads (not the headline)."""
+    import torch
+    import swiglu_mlp_projection_gb300 as swg
+    from swiglu_mlp_projection_gb300 import inputs, workload
+    out = {}
+    for cfg in workload.CONFIGS:
+        if cfg.name == "bf16_decode_d4096":
+            continue
+        _, wg, wu = inputs.make_inputs(1, cfg.d, cfg.d_ff, cfg.dtype, seed=0)
+        w_bytes = 2 * wg.numel() * wg.element_size()
+        n_copies = max(1, math.ceil(3 * l2 / w_bytes)) if w_bytes < 3 * l2 else 1
+        copies = [(wg.to(dev), wu.to(dev)) for _ in range(n_copies)]
+        del wg, wu
+        for M in cfg.Ms:
+            x = inputs.make_inputs(M, cfg.d, cfg.d_ff, cfg.dtype, seed=0, x_only=True)[0].to(dev)
+            h = torch.empty(M, cfg.d_ff, dtype=x.dtype, device=dev)
+            k = [0]
+
+            def call():
+                a, b = copies[k[0] % n_copies]
+                k[0] += 1
+                swg.swiglu_up(x, a, b, out=h)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize(dev)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(iters)]
+            for a, b in evs:
+                a.record()
+                call()
+                b.record()
+            torch.cuda.synchronize(dev)
+            ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+            by = workload.algorithmic_bytes(M, cfg.d, cfg.d_ff, cfg.dtype)
+            fl = workload.flops(M, cfg.d, cfg.d_ff)
+            gbs = by / (ms * 1e-3) / 1e9
+            tfs = fl / (ms * 1e-3) / 1e12
+            key = "%s/M=%d" % (cfg.name, M)
+            entry = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "TFLOP/s": round(tfs, 2),
+                     "path": swg.plan(M, cfg.d, cfg.d_ff, cfg.dtype, "auto")["path"]}
+            if M <= 16 or cfg.dtype == "f32":
+                entry["frac_hbm"] = round(gbs / peaks["hbm_gbs"], 4)
+            else:
+                entry["frac_bf16"] = round(tfs / peaks["bf16_tflops"], 4)
+            out[key] = entry
+            del x, h
+        del copies
+        torch.cuda.empty_cache()
+    return out
+
+
+def cpu_baseline():
+    """The oracle, as it stands, on a bounded sample of the same workload."""
+    try:
+        gbs, t, calls, threads = oracle_sweep(2048, 10.0)
+    except Exception as e:  # the baseline must not sink the GPU measurement
+        return {"value": None, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                "sample": "failed: %s" % e}
+    return {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "decode sweep M in {1,2,4,8,16}, d=4096, first 2048 of 14336 columns, "
+                      "%d calls over %.1f s" % (calls, t)}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,154 @@
+/*
+ * swiglu.h -- C ABI of the GB300 (sm_103a) fused SwiGLU up-projection library.
+ *
+ * The operation ("Tile-Level Activation Overlap for Efficient LLM Inference",
+ * technical summary, section "Enonce du probleme"; "1 . Anatomie d'un
+ * transformeur sur GPU", section 1.1, "Wgate, Wup -> SwiGLU"):
+ *
+ *     h[i, j] = silu(g[i, j]) * u[i, j],   silu(z) = z / (1 + e^-z)
+ *     g = x . W_gate,  u = x . W_up
+ *
+ *     x      [M, d]     row-major, contiguous (activations, one row per token)
+ *     W_gate [d, d_ff]  row-major, contiguous (element (k, j) at k*d_ff + j, the
+ *     W_up   [d, d_ff]  weight layout of "Ou part le temps d'un token", section
+ *                       "Un kernel pour les matrices etroites")
+ *     h      [M, d_ff]  row-major, contiguous
+ *
+ * Arithmetic: products and sums in f32 (bf16 operands are widened exactly);
+ * g and u are never rounded to the operand type; only h is rounded, to
+ * nearest even, to `dtype`.  Partial sums are combined in a fixed order, so a
+ * given call on a given device returns the same bits every time (the
+ * reproducibility argument of "Un kernel pour les matrices etroites").
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library never frees or retains them past the call's stream work.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work; they return before it runs.  Faults inside enqueued work
+ *     surface at the caller's next synchronisation, as for any CUDA library.
+ *   - Argument validation is synchronous and enqueues nothing on failure.
+ *   - The return value is a swiglu_status; swiglu_last_error_string() gives a
+ *     human-readable detail for the calling thread's last failure.
+ *   - h must not overlap x, W_gate, W_up or the workspace.
+ *   - Requirements checked on every call: sizes M, d, d_ff >= 0 (M == 0 or
+ *     d_ff == 0 is a no-op; d == 0 gives h = 0); pointers 16-byte aligned;
+ *     d and d_ff multiples of 8 (bf16) or 4 (f32), so that every row starts on
+ *     a 16-byte boundary for vector loads and TMA; the current device must be
+ *     compute capability 10.3 (sm_103).
+ */
+#ifndef SWIGLU_GB300_H
+#define SWIGLU_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SWIGLU_API __attribute__((visibility("default")))
+#else
+#define SWIGLU_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SWIGLU_F32 = 0, SWIGLU_BF16 = 1 } swiglu_dtype;
+
+typedef enum {
+  SWIGLU_OK = 0,
+  SWIGLU_ERR_INVALID_ARG = 1,   /* null pointer, negative size, unknown dtype/path */
+  SWIGLU_ERR_UNSUPPORTED = 2,   /* valid arguments this build cannot serve      */
+  SWIGLU_ERR_ALIGNMENT = 3,     /* pointer or row stride not 16-byte aligned    */
+  SWIGLU_ERR_OOM = 4,           /* workspace allocation failed                  */
+  SWIGLU_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed            */
+  SWIGLU_ERR_TIMEOUT = 6,       /* a bounded device-side wait gave up           */
+  SWIGLU_ERR_ARCH = 7,          /* current device is not sm_103                 */
+  SWIGLU_ERR_WORKSPACE = 8      /* caller workspace too small or misaligned     */
+} swiglu_status;
+
+/* Which kernels serve a call.  AUTO is the dispatcher (M-based, see below);
+ * the others force one path (tests compare paths against each other). */
+typedef enum {
+  SWIGLU_PATH_AUTO = 0,
+  SWIGLU_PATH_SIMT = 1,     /* split-K CUDA-core GEMV + reduction (f32 and bf16) */
+  SWIGLU_PATH_SKINNY = 2,   /* split-K tcgen05 swap-AB partials + reduction (bf16) */
+  SWIGLU_PATH_TC = 3        /* tcgen05 tile GEMM with the SwiGLU epilogue (bf16)  */
+} swiglu_path;
+
+/*
+ * h = silu(x . W_gate) (.) (x . W_up).
+ *
+ * Dispatch (AUTO): f32 -> SIMT split-K path; bf16 with M <= the skinny limit
+ * (swiglu_plan reports it) -> SKINNY; larger bf16 M -> TC.  The split-K
+ * paths need a workspace for their partial sums; this entry point takes it
+ * from a library-owned, stream-ordered pool (cudaMallocFromPoolAsync /
+ * cudaFreeAsync on `stream`), so calls on different streams never share it.
+ * Errors: SWIGLU_ERR_INVALID_ARG, _ALIGNMENT, _ARCH, _OOM, _CUDA.
+ */
+SWIGLU_API int swiglu_up(const void* x, const void* w_gate, const void* w_up, void* h,
+              int64_t M, int64_t d, int64_t d_ff, int dtype, void* stream);
+
+/*
+ * As swiglu_up, with an explicit path and an optional caller workspace.
+ *   path       a swiglu_path; a forced path that cannot serve the call (e.g.
+ *              SKINNY or TC for f32) returns SWIGLU_ERR_UNSUPPORTED.
+ *   workspace  device buffer, 256-byte aligned, of at least
+ *              swiglu_workspace_bytes(M, d, d_ff, dtype, path) bytes, or NULL
+ *              to use the library pool.  Used only by the enqueued work; the
+ *              caller must keep it alive until that work completes and must
+ *              not share it between calls that may run concurrently.
+ */
+SWIGLU_API int swiglu_up_ex(const void* x, const void* w_gate, const void* w_up, void* h,
+                 int64_t M, int64_t d, int64_t d_ff, int dtype, int path,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes a call with these arguments needs on the current device
+ * (0 for the TC path).  Returns 0 and sets the thread's error string when the
+ * arguments are invalid or no device is current. */
+SWIGLU_API size_t swiglu_workspace_bytes(int64_t M, int64_t d, int64_t d_ff, int dtype,
+                              int path);
+
+/* How a call would be served, for a device with `num_sms` SMs (host-only,
+ * needs no GPU).  Pure function of its arguments. */
+typedef struct {
+  int path;              /* resolved swiglu_path                                */
+  int64_t slices;        /* K slices of the split-K paths (1 for TC)            */
+  int64_t grid;          /* CTAs of the main kernel                              */
+  int64_t row_chunk;     /* rows of x per SIMT pass (SIMT path)                  */
+  int64_t workspace;     /* bytes of partial sums                                */
+  int64_t skinny_max_m;  /* largest bf16 M that AUTO sends to SKINNY            */
+  int64_t launches;      /* kernel launches one call enqueues                   */
+} swiglu_plan_info;
+
+SWIGLU_API int swiglu_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, int path,
+                int num_sms, swiglu_plan_info* out);
+
+/*
+ * The K-slice rule of "Ou part le temps d'un token", section "Un kernel pour
+ * les matrices etroites": split the shared dimension K so that
+ * col_blocks * slices approaches target_blocks, without any slice having
+ * fewer than min_k_per_slice indices (and at least one slice).  Host-only.
+ * Returns the slice count, or -1 on invalid arguments.
+ */
+SWIGLU_API int64_t swiglu_split_k_slices(int64_t K, int64_t col_blocks,
+                              int64_t target_blocks, int64_t min_k_per_slice);
+
+/* Reads and clears the device-side error word that bounded waits inside the
+ * kernels set when they give up.  Synchronises the current device first.
+ * Returns SWIGLU_OK, SWIGLU_ERR_TIMEOUT or SWIGLU_ERR_CUDA. */
+SWIGLU_API int swiglu_check_device_status(void);
+
+/* Text for a swiglu_status value (static storage). */
+SWIGLU_API const char* swiglu_status_string(int status);
+
+/* Detail of the calling thread's most recent failure ("" if none). */
+SWIGLU_API const char* swiglu_last_error_string(void);
+
+/* Library version, as MAJOR*10000 + MINOR*100 + PATCH. */
+SWIGLU_API int swiglu_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWIGLU_GB300_H */

@@ -1,7 +1,112 @@
 """GB300-native fused SwiGLU up-projection: h = silu(x.W_gate) (.) (x.W_up).
 
 The compute path is the CUDA library built from ``csrc/`` (a C ABI declared in
-``include/swiglu.h``); this package only marshals arguments into it.  The
-library is loaded on first use and its absence is an error: there is no CPU
-fallback.
+``include/swiglu.h``); this package only marshals torch tensors (device memory
+and the current stream) into it.  The library is loaded on first use and its
+absence is an error: there is no CPU fallback.
 """
+import ctypes
+
+from . import _lib
+from ._lib import (BF16, F32, PATH_AUTO, PATH_SIMT, PATH_SKINNY, PATH_TC,
+                   SwiGLUError)
+
+PATHS = {"auto": PATH_AUTO, "simt": PATH_SIMT, "skinny": PATH_SKINNY, "tc": PATH_TC}
+PATH_NAMES = {v: k for k, v in PATHS.items()}
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError("swiglu_up supports bfloat16 and float32 tensors, got %s" % t.dtype)
+
+
+def _path_code(path):
+    if isinstance(path, int):
+        return path
+    try:
+        return PATHS[path]
+    except KeyError:
+        raise ValueError("path must be one of %s" % sorted(PATHS)) from None
+
+
+def swiglu_up(x, w_gate, w_up, out=None, path="auto", workspace=None, stream=None):
+    """h = silu(x @ w_gate) * (x @ w_up) on the current CUDA device.
+
+    x [M, d], w_gate / w_up [d, d_ff]: contiguous CUDA tensors of one dtype
+    (bfloat16 or float32).  ``out`` [M, d_ff] is written if given (else
+    allocated).  ``path`` forces a kernel path ("simt", "skinny", "tc");
+    ``workspace`` is an optional uint8 CUDA tensor for split-K partial sums.
+    The call is asynchronous on ``stream`` (default: torch's current stream).
+    """
+    import torch
+    for name, t in (("x", x), ("w_gate", w_gate), ("w_up", w_up)):
+        if not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    if x.dim() != 2 or w_gate.dim() != 2 or w_up.shape != w_gate.shape:
+        raise ValueError("expected x [M, d] and w_gate, w_up [d, d_ff]")
+    M, d = x.shape
+    if w_gate.shape[0] != d:
+        raise ValueError("x has d=%d but w_gate has %d rows" % (d, w_gate.shape[0]))
+    d_ff = w_gate.shape[1]
+    dt = _dtype_code(x)
+    if w_gate.dtype != x.dtype or w_up.dtype != x.dtype:
+        raise TypeError("x, w_gate and w_up must share one dtype")
+    if out is None:
+        out = torch.empty((M, d_ff), dtype=x.dtype, device=x.device)
+    elif out.shape != (M, d_ff) or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, d_ff] tensor of x's dtype")
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    lib = _lib.load()
+    with torch.cuda.device(x.device):
+        st = lib.swiglu_up_ex(x.data_ptr(), w_gate.data_ptr(), w_up.data_ptr(), out.data_ptr(),
+                              M, d, d_ff, dt, _path_code(path), ws_ptr, ws_bytes,
+                              stream.cuda_stream)
+    _lib.check(st)
+    return out
+
+
+def workspace_bytes(M, d, d_ff, dtype="bf16", path="auto"):
+    """Workspace bytes a call needs on the current device (0 for the TC path)."""
+    lib = _lib.load()
+    dt = BF16 if dtype in ("bf16", BF16) else F32
+    return int(lib.swiglu_workspace_bytes(M, d, d_ff, dt, _path_code(path)))
+
+
+def plan(M, d, d_ff, dtype="bf16", path="auto", num_sms=152):
+    """How a call would be served on a GPU with ``num_sms`` SMs (host-only)."""
+    lib = _lib.load()
+    info = _lib.PlanInfo()
+    dt = BF16 if dtype in ("bf16", BF16) else F32
+    _lib.check(lib.swiglu_plan(M, d, d_ff, dt, _path_code(path), num_sms, ctypes.byref(info)))
+    return {"path": PATH_NAMES.get(info.path, info.path), "slices": info.slices,
+            "grid": info.grid, "row_chunk": info.row_chunk,
+            "workspace": info.workspace, "skinny_max_m": info.skinny_max_m,
+            "launches": info.launches}
+
+
+def split_k_slices(K, col_blocks, target_blocks, min_k_per_slice):
+    """The page's K-slice rule (host-only)."""
+    return int(_lib.load().swiglu_split_k_slices(K, col_blocks, target_blocks, min_k_per_slice))
+
+
+def check_device_status():
+    """Synchronise and raise SwiGLUError if a device-side wait timed out."""
+    _lib.check(_lib.load().swiglu_check_device_status())
+
+
+def version():
+    return int(_lib.load().swiglu_version())
+
+
+__all__ = ["swiglu_up", "workspace_bytes", "plan", "split_k_slices",
+           "check_device_status", "version", "SwiGLUError", "PATHS"]

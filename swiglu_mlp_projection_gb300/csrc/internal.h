@@ -1,0 +1,69 @@
+// Internal interfaces between the C-ABI layer and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace swg {
+
+// Partial-sum layout shared by every split-K producer and the reduction:
+//   part[((s * M + m) * 2 + gu) * d_ff + j]   (f32)
+// s = K slice, m = row of x, gu = 0 for x.W_gate, 1 for x.W_up, j = column.
+inline size_t partial_elems(int64_t slices, int64_t M, int64_t d_ff) {
+  return (size_t)slices * (size_t)M * 2u * (size_t)d_ff;
+}
+
+struct SimtPlan {
+  int vec;          // elements per 16-byte load (4 f32, 8 bf16)
+  int cols_per_cta; // 32 lanes x vec
+  int row_chunk;    // rows of x per CTA (1, 2 or 4)
+  int64_t col_blocks, row_chunks, slices, k_per_slice;
+};
+
+SimtPlan plan_simt(int64_t M, int64_t d, int64_t d_ff, int dtype, int num_sms);
+
+// S1 (SIMT): partial sums of x.Wg and x.Wu per K slice.
+cudaError_t launch_simt_partial(const void* x, const void* wg, const void* wu,
+                                float* part, int64_t M, int64_t d, int64_t d_ff,
+                                int dtype, const SimtPlan& p, cudaStream_t st);
+
+// S2: fixed-order sum over slices, then h = silu(g) * u rounded to dtype.
+cudaError_t launch_reduce_swiglu(const float* part, void* h, int64_t M,
+                                 int64_t d_ff, int64_t slices, int dtype,
+                                 int num_sms, cudaStream_t st);
+
+// TMA descriptor of a row-major bf16 matrix [rows, cols], 128-byte swizzle.
+cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                              int box_cols, int box_rows);
+
+// Skinny tensor-core path (bf16, small M): swap-AB split-K over a balanced
+// partition of (64-column block, 64-deep k block) units.
+struct SkinnyPlan {
+  int n_pad;               // M rounded up to the MMA N granule (16..256)
+  int64_t n_cb, n_kb;      // 64-column blocks, 64-deep k blocks
+  int64_t units;           // n_cb * n_kb
+  int grid;                // CTAs (<= SM count)
+  int maxq;                // partial slots per column block
+  size_t counters_bytes;   // arrival counters (zeroed before every launch)
+  size_t part_bytes;       // partial sums
+};
+constexpr int kSkinnyMaxN = 256;
+SkinnyPlan plan_skinny(int64_t M, int64_t d, int64_t d_ff, int num_sms);
+cudaError_t launch_skinny_tc(const void* x, const void* wg, const void* wu, void* h, int64_t M,
+                             int64_t d, int64_t d_ff, const SkinnyPlan& p, void* workspace,
+                             unsigned* status, uint64_t timeout_ns, cudaStream_t st);
+
+// Tile tensor-core path (bf16, large M): 128 x (128 gate + 128 up) output
+// tiles, SwiGLU applied to the accumulator tile before a single bf16 store.
+struct TilePlan {
+  int64_t n_mb, n_nb, tiles;
+  int grid;
+};
+TilePlan plan_tile(int64_t M, int64_t d, int64_t d_ff, int num_sms);
+cudaError_t launch_tile_tc(const void* x, const void* wg, const void* wu, void* h, int64_t M,
+                           int64_t d, int64_t d_ff, const TilePlan& p, unsigned* status,
+                           uint64_t timeout_ns, cudaStream_t st);
+
+}  // namespace swg

@@ -1,0 +1,323 @@
+// C ABI of the SwiGLU up-projection library: validation, dispatch, workspace.
+//
+// Everything a call does on the GPU runs in the kernels of this directory; this
+// file only checks arguments, chooses a path and enqueues the launches on the
+// caller's stream.  See include/swiglu.h for the contract of each entry point.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/swiglu.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace swg {
+
+// Error word written by bounded device-side waits that give up.
+__device__ unsigned g_device_status = 0;
+
+namespace {
+
+thread_local char t_err[512] = "";
+
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof t_err, fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(SWIGLU_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Fills `out` for the current device (cached).  Returns a swiglu_status.
+int current_device(int* dev_out, DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(SWIGLU_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    if ((e = cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    if ((e = cudaDeviceGetAttribute(&di.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(cc major)");
+    if ((e = cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(cc minor)");
+    di.ready = true;
+  }
+  *dev_out = dev;
+  *out = di;
+  if (di.cc_major != 10 || di.cc_minor != 3)
+    return fail(SWIGLU_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103a",
+                dev, di.cc_major, di.cc_minor);
+  return SWIGLU_OK;
+}
+
+// The library's stream-ordered workspace pool for `dev` (created on first use;
+// it keeps freed blocks for reuse instead of returning them to the driver).
+int device_pool(int dev, cudaMemPool_t* pool) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.pool) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaError_t e = cudaMemPoolCreate(&di.pool, &props);
+    if (e != cudaSuccess) { di.pool = nullptr; return cuda_fail(e, "cudaMemPoolCreate"); }
+    uint64_t keep = ~0ull;
+    e = cudaMemPoolSetAttribute(di.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolSetAttribute");
+  }
+  *pool = di.pool;
+  return SWIGLU_OK;
+}
+
+int elem_bytes(int dtype) { return dtype == SWIGLU_BF16 ? 2 : 4; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// Largest M the dispatcher sends to the skinny (split-K) path for bf16.
+constexpr int64_t kSkinnyMaxM = 16;
+// Grid-dimension limits of the SIMT path (gridDim.y/z are 16-bit).
+constexpr int64_t kMaxGridYZ = 65535;
+
+int resolve_path(int64_t M, int dtype, int path, int* out) {
+  if (path < SWIGLU_PATH_AUTO || path > SWIGLU_PATH_TC)
+    return fail(SWIGLU_ERR_INVALID_ARG, "unknown path %d", path);
+  if (path == SWIGLU_PATH_AUTO) {
+    // Tensor-core paths are not part of this build yet: every call is served
+    // by the SIMT split-K path.
+    (void)M;
+    *out = SWIGLU_PATH_SIMT;
+    return SWIGLU_OK;
+  }
+  if (path != SWIGLU_PATH_SIMT)
+    return fail(SWIGLU_ERR_UNSUPPORTED, "path %d is not available in this build", path);
+  (void)dtype;
+  *out = path;
+  return SWIGLU_OK;
+}
+
+int validate(const void* x, const void* wg, const void* wu, const void* h,
+             int64_t M, int64_t d, int64_t d_ff, int dtype) {
+  if (dtype != SWIGLU_F32 && dtype != SWIGLU_BF16)
+    return fail(SWIGLU_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+  if (M < 0 || d < 0 || d_ff < 0)
+    return fail(SWIGLU_ERR_INVALID_ARG, "negative size (M=%lld d=%lld d_ff=%lld)",
+                (long long)M, (long long)d, (long long)d_ff);
+  if (M > INT32_MAX || d > INT32_MAX || d_ff > INT32_MAX)
+    return fail(SWIGLU_ERR_UNSUPPORTED, "a size exceeds 2^31-1");
+  const size_t e = (size_t)elem_bytes(dtype);
+  const size_t nx = (size_t)M * d * e, nw = (size_t)d * d_ff * e, nh = (size_t)M * d_ff * e;
+  if ((nx && !x) || (nw && (!wg || !wu)) || (nh && !h))
+    return fail(SWIGLU_ERR_INVALID_ARG, "null pointer for a non-empty tensor");
+  if ((x && !aligned16(x)) || (wg && !aligned16(wg)) || (wu && !aligned16(wu)) || (h && !aligned16(h)))
+    return fail(SWIGLU_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
+  const int64_t per16 = (int64_t)(16 / e);
+  if (d % per16 != 0 || d_ff % per16 != 0)
+    return fail(SWIGLU_ERR_ALIGNMENT, "d and d_ff must be multiples of %lld for this dtype",
+                (long long)per16);
+  if (overlaps(h, nh, x, nx) || overlaps(h, nh, wg, nw) || overlaps(h, nh, wu, nw))
+    return fail(SWIGLU_ERR_INVALID_ARG, "h overlaps an input");
+  return SWIGLU_OK;
+}
+
+struct Plan {
+  int path;
+  SimtPlan simt;
+  int64_t slices;
+  size_t workspace;
+};
+
+int make_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, int path, int num_sms, Plan* p) {
+  int rp = 0;
+  int st = resolve_path(M, dtype, path, &rp);
+  if (st != SWIGLU_OK) return st;
+  p->path = rp;
+  p->simt = plan_simt(M, d, d_ff, dtype, num_sms);
+  if (p->simt.slices > kMaxGridYZ || p->simt.row_chunks > kMaxGridYZ)
+    return fail(SWIGLU_ERR_UNSUPPORTED, "shape exceeds the grid limits of the SIMT path");
+  p->slices = p->simt.slices;
+  p->workspace = partial_elems(p->slices, M, d_ff) * sizeof(float);
+  p->workspace = (p->workspace + 255) / 256 * 256;
+  return SWIGLU_OK;
+}
+
+int run(const void* x, const void* wg, const void* wu, void* h, int64_t M, int64_t d,
+        int64_t d_ff, int dtype, int path, void* workspace, size_t ws_bytes,
+        cudaStream_t st) {
+  int v = validate(x, wg, wu, h, M, d, d_ff, dtype);
+  if (v != SWIGLU_OK) return v;
+  int dev = 0;
+  DeviceInfo di;
+  if ((v = current_device(&dev, &di)) != SWIGLU_OK) return v;
+  Plan p;
+  if ((v = make_plan(M, d, d_ff, dtype, path, di.num_sms, &p)) != SWIGLU_OK) return v;
+  if (M == 0 || d_ff == 0) return SWIGLU_OK;
+  if (workspace && overlaps(h, (size_t)M * d_ff * elem_bytes(dtype), workspace, ws_bytes))
+    return fail(SWIGLU_ERR_INVALID_ARG, "h overlaps the workspace");
+
+  float* part = (float*)workspace;
+  bool pooled = false;
+  if (p.workspace > 0) {
+    if (workspace) {
+      if (ws_bytes < p.workspace || ((uintptr_t)workspace & 255u))
+        return fail(SWIGLU_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)",
+                    p.workspace, ws_bytes);
+    } else {
+      cudaMemPool_t pool;
+      if ((v = device_pool(dev, &pool)) != SWIGLU_OK) return v;
+      void* ptr = nullptr;
+      cudaError_t e = cudaMallocFromPoolAsync(&ptr, p.workspace, pool, st);
+      if (e != cudaSuccess) {
+        if (e == cudaErrorMemoryAllocation) {
+          cudaGetLastError();
+          return fail(SWIGLU_ERR_OOM, "workspace of %zu bytes: %s", p.workspace, cudaGetErrorString(e));
+        }
+        return cuda_fail(e, "cudaMallocFromPoolAsync");
+      }
+      part = (float*)ptr;
+      pooled = true;
+    }
+  }
+
+  cudaError_t e = cudaSuccess;
+  e = launch_simt_partial(x, wg, wu, part, M, d, d_ff, dtype, p.simt, st);
+  if (e == cudaSuccess) e = launch_reduce_swiglu(part, h, M, d_ff, p.slices, dtype, di.num_sms, st);
+  if (pooled) {
+    cudaError_t ef = cudaFreeAsync(part, st);
+    if (e == cudaSuccess) e = ef;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  t_err[0] = 0;
+  return SWIGLU_OK;
+}
+
+}  // namespace
+
+int64_t split_k_slices(int64_t K, int64_t col_blocks, int64_t target_blocks,
+                       int64_t min_k_per_slice) {
+  if (K < 0 || col_blocks <= 0 || target_blocks <= 0 || min_k_per_slice <= 0) return -1;
+  int64_t want = (target_blocks + col_blocks - 1) / col_blocks;   // slices to reach the target
+  int64_t most = K / min_k_per_slice;                              // keep >= min_k per slice
+  if (most < 1) most = 1;
+  if (want > most) want = most;
+  if (want < 1) want = 1;
+  return want;
+}
+
+}  // namespace swg
+
+using namespace swg;
+
+extern "C" {
+
+int swiglu_up(const void* x, const void* w_gate, const void* w_up, void* h,
+              int64_t M, int64_t d, int64_t d_ff, int dtype, void* stream) {
+  return run(x, w_gate, w_up, h, M, d, d_ff, dtype, SWIGLU_PATH_AUTO, nullptr, 0,
+             (cudaStream_t)stream);
+}
+
+int swiglu_up_ex(const void* x, const void* w_gate, const void* w_up, void* h,
+                 int64_t M, int64_t d, int64_t d_ff, int dtype, int path,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  return run(x, w_gate, w_up, h, M, d, d_ff, dtype, path, workspace, workspace_bytes,
+             (cudaStream_t)stream);
+}
+
+size_t swiglu_workspace_bytes(int64_t M, int64_t d, int64_t d_ff, int dtype, int path) {
+  if (dtype != SWIGLU_F32 && dtype != SWIGLU_BF16) { fail(SWIGLU_ERR_INVALID_ARG, "unknown dtype %d", dtype); return 0; }
+  if (M < 0 || d < 0 || d_ff < 0) { fail(SWIGLU_ERR_INVALID_ARG, "negative size"); return 0; }
+  int dev = 0;
+  DeviceInfo di;
+  if (current_device(&dev, &di) != SWIGLU_OK) return 0;
+  Plan p;
+  if (make_plan(M, d, d_ff, dtype, path, di.num_sms, &p) != SWIGLU_OK) return 0;
+  return p.workspace;
+}
+
+int swiglu_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, int path, int num_sms,
+                swiglu_plan_info* out) {
+  if (!out) return fail(SWIGLU_ERR_INVALID_ARG, "null output");
+  if (dtype != SWIGLU_F32 && dtype != SWIGLU_BF16) return fail(SWIGLU_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+  if (M < 0 || d < 0 || d_ff < 0 || num_sms <= 0) return fail(SWIGLU_ERR_INVALID_ARG, "negative size or SM count");
+  Plan p;
+  int v = make_plan(M, d, d_ff, dtype, path, num_sms, &p);
+  if (v != SWIGLU_OK) return v;
+  out->path = p.path;
+  out->slices = p.slices;
+  out->grid = p.simt.col_blocks * p.simt.slices * p.simt.row_chunks;
+  out->row_chunk = p.simt.row_chunk;
+  out->workspace = (int64_t)p.workspace;
+  out->skinny_max_m = kSkinnyMaxM;
+  out->launches = (M == 0 || d_ff == 0) ? 0 : (p.slices > 0 ? 2 : 1);
+  return SWIGLU_OK;
+}
+
+int64_t swiglu_split_k_slices(int64_t K, int64_t col_blocks, int64_t target_blocks,
+                              int64_t min_k_per_slice) {
+  return split_k_slices(K, col_blocks, target_blocks, min_k_per_slice);
+}
+
+int swiglu_check_device_status(void) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  unsigned word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_device_status, sizeof word);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol");
+  if (word) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
+    return fail(SWIGLU_ERR_TIMEOUT, "a device-side wait gave up (status word 0x%x)", word);
+  }
+  return SWIGLU_OK;
+}
+
+const char* swiglu_status_string(int status) {
+  switch (status) {
+    case SWIGLU_OK: return "ok";
+    case SWIGLU_ERR_INVALID_ARG: return "invalid argument";
+    case SWIGLU_ERR_UNSUPPORTED: return "unsupported";
+    case SWIGLU_ERR_ALIGNMENT: return "misaligned pointer or stride";
+    case SWIGLU_ERR_OOM: return "out of device memory";
+    case SWIGLU_ERR_CUDA: return "CUDA error";
+    case SWIGLU_ERR_TIMEOUT: return "device-side wait timed out";
+    case SWIGLU_ERR_ARCH: return "device is not sm_103";
+    case SWIGLU_ERR_WORKSPACE: return "workspace too small or misaligned";
+    default: return "unknown status";
+  }
+}
+
+const char* swiglu_last_error_string(void) { return t_err; }
+
+int swiglu_version(void) { return 100; }
+
+}  // extern "C"

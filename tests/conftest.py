@@ -20,3 +20,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def cuda_lib():
+    """The CUDA library, built in-tree if it is missing or stale (nvcc is
+    needed; no GPU is needed to build or load it)."""
+    from swiglu_mlp_projection_gb300 import _lib, build
+    build.build()
+    return _lib.load()

@@ -1,0 +1,56 @@
+"""Comparison rule between a GPU result and the oracle's fp64 result.
+
+Tolerances are the ones stated for the method: max relative error 1e-5 for
+the f32 path, 2e-2 for bf16 (bf16 output, f32 accumulation).  "Relative" is
+measured against max(|h64|, phi * s):
+
+  * s (from the oracle) = 1.1 G |u| + |silu(g)| U with G = sum|x||Wg|,
+    U = sum|x||Wu| -- the |a|.|b| scale that "Ou part le temps d'un token"
+    ("Un kernel pour les matrices etroites") ties the tolerance to, because
+    a sum of d terms taken in another order legitimately moves a near-zero
+    result by far more than 1e-5 of itself;
+  * phi = 8 sqrt(d) 2^-24 / tol: an f32 sum of d products carries a
+    rounding error whose size is about 2^-24 sqrt(d) times the sum of the
+    magnitudes, so elements whose |h| is below phi*s are judged on an
+    absolute error of 8x that expected size; all others on plain relative
+    error.
+
+Elements with s == 0 (an exactly zero column) must match exactly.
+"""
+import math
+
+import numpy as np
+
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+
+
+def floor_factor(dtype, d):
+    return 8.0 * math.sqrt(max(d, 1)) * 2.0 ** -24 / TOL[dtype]
+
+
+def compare(h_gpu, h64, sens, dtype, d):
+    """Return a dict of error measures; ``ok`` is the pass/fail verdict."""
+    h_gpu = np.asarray(h_gpu, np.float64)
+    h64 = np.asarray(h64, np.float64)
+    sens = np.asarray(sens, np.float64)
+    diff = np.abs(h_gpu - h64)
+    den = np.maximum(np.abs(h64), floor_factor(dtype, d) * sens)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        err = np.where(den > 0, diff / np.where(den > 0, den, 1.0),
+                       np.where(diff == 0, 0.0, np.inf))
+    finite = bool(np.all(np.isfinite(h_gpu)))
+    max_err = float(err.max()) if err.size else 0.0
+    big = np.abs(h64) >= 1e-3 * (np.abs(h64).max() if h64.size else 0.0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        plain = diff[big] / np.abs(h64[big]) if big.any() else np.zeros(0)
+        rel_all = np.where(np.abs(h64) > 0, diff / np.abs(h64), np.where(diff == 0, 0, np.inf))
+    return {
+        "ok": finite and max_err <= TOL[dtype],
+        "max_err": max_err,
+        "max_plain_rel_above_1e-3max": float(plain.max()) if plain.size else 0.0,
+        "normwise": float(diff.max() / max(np.abs(h64).max(), 1e-300)) if h64.size else 0.0,
+        # share of elements off by more than 1 % of themselves (the SwiGLU
+        # paper's "mismatch" measure, reported, not asserted)
+        "mismatch_pct": float(100.0 * np.mean(rel_all > 0.01)) if h64.size else 0.0,
+        "finite": finite,
+    }

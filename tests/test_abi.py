@@ -1,0 +1,165 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and its host-only logic (slice rule, plans, status strings)
+behaves as documented."""
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from swiglu_mlp_projection_gb300 import _lib, inputs
+import swiglu_mlp_projection_gb300 as swg
+from tests.parity import compare, floor_factor, TOL
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "swiglu.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SWIGLU_API\s+[\w\s\*]+?\b(swiglu_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    syms = declared_symbols()
+    assert "swiglu_up" in syms and "swiglu_up_ex" in syms
+    assert set(syms) == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_library_exports_every_declared_symbol(cuda_lib):
+    for name in declared_symbols():
+        assert hasattr(cuda_lib, name), name
+
+
+def test_status_strings_and_version(cuda_lib):
+    for code in range(9):
+        s = cuda_lib.swiglu_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert cuda_lib.swiglu_status_string(99).decode() == "unknown status"
+    assert swg.version() >= 100
+
+
+def test_split_k_rule_reproduces_the_pages_example(cuda_lib):
+    # 512 x 512 with 32 columns per block: 16 column blocks; aiming at 256
+    # blocks with >= 64 k per slice gives 8 slices and 128 blocks.
+    from tests.test_workload_pins import G
+    col_blocks = int(G["gemv_matrix"] // G["block_cols"])
+    s = swg.split_k_slices(int(G["gemv_matrix"]), col_blocks,
+                           int(G["split_target_blocks"]), int(G["split_min_k"]))
+    assert s == G["split_example_slices"]
+    assert s * col_blocks == G["split_example_blocks"]
+    assert s * col_blocks > G["rtx3090_sms"]
+
+
+def test_split_k_rule_edges(cuda_lib):
+    assert swg.split_k_slices(10, 4, 256, 64) == 1          # K below one slice
+    assert swg.split_k_slices(4096, 1000, 256, 64) == 1     # enough blocks already
+    assert swg.split_k_slices(4096, 1, 608, 64) == 64       # capped by min k
+    assert swg.split_k_slices(0, 4, 256, 64) == 1
+    assert swg.split_k_slices(64, 0, 256, 64) == -1
+    assert swg.split_k_slices(64, 4, 256, 0) == -1
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_plan_covers_all_columns_rows_and_k(cuda_lib, dtype):
+    for (M, d, d_ff) in [(1, 512, 2048), (3, 4096, 14336), (16, 896, 4864), (17, 8, 8),
+                         (5, 1024, 40)]:
+        p = swg.plan(M, d, d_ff, dtype, "simt", 152)
+        assert p["path"] == "simt"
+        vec = 8 if dtype == "bf16" else 4
+        cols = 32 * vec
+        chunks = -(-M // p["row_chunk"])
+        assert p["grid"] == -(-d_ff // cols) * p["slices"] * chunks
+        assert 1 <= p["slices"] <= d
+        assert p["workspace"] >= p["slices"] * M * 2 * d_ff * 4
+        assert p["workspace"] % 256 == 0
+
+
+def test_plan_rejects_bad_arguments(cuda_lib):
+    with pytest.raises(swg.SwiGLUError):
+        swg.plan(-1, 8, 8, "bf16", "auto", 152)
+    with pytest.raises(swg.SwiGLUError):
+        swg.plan(1, 8, 8, "bf16", 17, 152)
+    with pytest.raises(swg.SwiGLUError):
+        swg.plan(1, 8, 8, "bf16", "auto", 0)
+
+
+def test_entry_point_validates_before_touching_the_device(cuda_lib):
+    # Invalid arguments are rejected synchronously, before any device query,
+    # so these run without a GPU.
+    lib = cuda_lib
+    st = lib.swiglu_up(None, None, None, None, -1, 8, 8, _lib.BF16, None)
+    assert st == 1
+    st = lib.swiglu_up(None, None, None, None, 1, 8, 8, 7, None)
+    assert st == 1
+    st = lib.swiglu_up(None, None, None, None, 1, 8, 8, _lib.BF16, None)
+    assert st == 1 and "null" in lib.swiglu_last_error_string().decode()
+    st = lib.swiglu_up(16, 32, 48, 65, 1, 8, 8, _lib.BF16, None)
+    assert st == 3                       # 65 is not 16-byte aligned
+    st = lib.swiglu_up(16, 32, 48, 64, 1, 12, 8, _lib.BF16, None)
+    assert st == 3                       # d not a multiple of 8 for bf16
+    st = lib.swiglu_up(4096, 8192, 12288, 4096, 2, 8, 8, _lib.BF16, None)
+    assert st == 1 and "overlap" in lib.swiglu_last_error_string().decode()
+    st = lib.swiglu_up_ex(16, 32, 48, 64, 1, 8, 8, _lib.BF16, 9, None, 0, None)
+    assert st == 1
+
+
+# --------------------------------------------------------------------------
+# The comparison rule itself (CPU): f32-accumulation noise passes, a planted
+# mistake in the oracle's output fails.
+# --------------------------------------------------------------------------
+
+def _f32_emulation(x, wg, wu, dtype):
+    """An f32-accumulating evaluation in numpy (another summation order)."""
+    x32 = x.to(torch.float32).numpy()
+    g = x32 @ wg.to(torch.float32).numpy()
+    u = x32 @ wu.to(torch.float32).numpy()
+    h = (g / (1 + np.exp(-g.astype(np.float64)))).astype(np.float32) * u
+    if dtype == "bf16":
+        h = torch.from_numpy(h).to(torch.bfloat16).to(torch.float64).numpy()
+    return h
+
+
+@pytest.mark.parametrize("dtype,shape", [("f32", (1, 512, 2048)), ("bf16", (4, 4096, 512)),
+                                         ("bf16", (3, 896, 256))])
+def test_comparison_rule_accepts_f32_accumulation(dtype, shape):
+    M, d, d_ff = shape
+    x, wg, wu = inputs.make_inputs(M, d, d_ff, dtype, seed=21)
+    od = oracle.BF16 if dtype == "bf16" else oracle.F32
+    h64, _, sens = oracle.swiglu_up(inputs.raw_bits(x), inputs.raw_bits(wg), inputs.raw_bits(wu), od)
+    res = compare(_f32_emulation(x, wg, wu, dtype), h64, sens, dtype, d)
+    assert res["ok"], res
+
+
+@pytest.mark.parametrize("dtype,shape", [("f32", (1, 512, 2048)), ("bf16", (4, 4096, 512))])
+def test_comparison_rule_rejects_planted_mistakes(dtype, shape):
+    M, d, d_ff = shape
+    x, wg, wu = inputs.make_inputs(M, d, d_ff, dtype, seed=22)
+    od = oracle.BF16 if dtype == "bf16" else oracle.F32
+    raw = inputs.raw_bits
+    h64, _, sens = oracle.swiglu_up(raw(x), raw(wg), raw(wu), od)
+    # (a) one k term dropped (a slice boundary off by one)
+    bad, _, _ = oracle.swiglu_up(raw(x[:, 1:]), raw(wg[1:]), raw(wu[1:]), od)
+    assert not compare(bad, h64, sens, dtype, d)["ok"]
+    # (b) a 64-wide K tile dropped
+    bad, _, _ = oracle.swiglu_up(raw(x[:, 64:]), raw(wg[64:]), raw(wu[64:]), od)
+    assert not compare(bad, h64, sens, dtype, d)["ok"]
+    # (c) gate and up swapped
+    bad, _, _ = oracle.swiglu_up(raw(x), raw(wu), raw(wg), od)
+    assert not compare(bad, h64, sens, dtype, d)["ok"]
+    # (d) two adjacent output columns exchanged
+    bad = h64.copy()
+    bad[:, [0, 1]] = bad[:, [1, 0]]
+    assert not compare(bad, h64, sens, dtype, d)["ok"]
+    # (e) output rounded to bf16 where f32 was promised
+    if dtype == "f32":
+        bad = torch.from_numpy(h64).to(torch.bfloat16).to(torch.float64).numpy()
+        assert not compare(bad, h64, sens, dtype, d)["ok"]
+
+
+def test_floor_factor_values():
+    assert floor_factor("bf16", 4096) == pytest.approx(8 * 64 * 2 ** -24 / 2e-2)
+    assert floor_factor("f32", 512) == pytest.approx(8 * 512 ** 0.5 * 2 ** -24 / 1e-5)
+    assert TOL == {"f32": 1e-5, "bf16": 2e-2}
