@@ -102,6 +102,40 @@ SWIGLU_API int swiglu_up_ex(const void* x, const void* w_gate, const void* w_up,
                  int64_t M, int64_t d, int64_t d_ff, int dtype, int path,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * As swiglu_up, for callers that cannot allocate device memory.  Some
+ * callers may not call cudaMalloc (or any allocator) while they run this
+ * operation: a host framework that invokes operators from an enqueue
+ * callback in which allocation is forbidden, a process whose device memory is
+ * entirely reserved by another allocator, or a latency-critical loop in which
+ * an allocation or free could block or synchronise the device.  This entry
+ * point allocates nothing: it runs the SIMT split-K path (the per-slice
+ * partial-sum kernel and the reduction kernel) with the partial sums in a
+ * fixed scratch array that the library holds in device memory, of
+ * SWIGLU_NOALLOC_SCRATCH_BYTES bytes on every GPU that loads the library,
+ * until the process exits.  The caller still passes x, the weights and h.
+ * There is no counterpart of this entry point in the pages.
+ *
+ *   - Set-up: the first call on a device, with that device current, looks up
+ *     the scratch array's device address (cudaGetSymbolAddress) and caches
+ *     it; make that first call before any stream capture.
+ *   - Limit: a call whose partial sums need more than
+ *     SWIGLU_NOALLOC_SCRATCH_BYTES returns SWIGLU_ERR_WORKSPACE and enqueues
+ *     nothing.  The need is slices x M x 2 x d_ff x 4 bytes, i.e. the
+ *     `workspace` that swiglu_plan reports for SWIGLU_PATH_SIMT; on a
+ *     152-SM GB300 the d = 4096, d_ff = 14336 decode calls need at most
+ *     7.3 MB (M = 16).
+ *   - Sharing: every call on a device uses the same array, which keeps the
+ *     last call's contents.  Nothing in it needs to start at zero (each call
+ *     writes every partial it later reads), but calls that may overlap on
+ *     the GPU (on different streams, or from different threads without
+ *     ordering) race on it and must be serialised by the caller.
+ *   - Validation and other errors: as swiglu_up.
+ */
+#define SWIGLU_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+SWIGLU_API int swiglu_up_noalloc(const void* x, const void* w_gate, const void* w_up, void* h,
+                                 int64_t M, int64_t d, int64_t d_ff, int dtype, void* stream);
+
 /* Workspace bytes a call with these arguments needs on the current device
  * (0 for the TC path).  Returns 0 and sets the thread's error string when the
  * arguments are invalid or no device is current. */

@@ -233,6 +233,24 @@ int64_t split_k_slices(int64_t K, int64_t col_blocks, int64_t target_blocks,
   return want;
 }
 
+int api_validate(const void* x, const void* wg, const void* wu, const void* h, int64_t M,
+                 int64_t d, int64_t d_ff, int dtype) {
+  return validate(x, wg, wu, h, M, d, d_ff, dtype);
+}
+
+int api_current_device(int* dev, int* num_sms) {
+  DeviceInfo di;
+  int v = current_device(dev, &di);
+  if (v == SWIGLU_OK) *num_sms = di.num_sms;
+  return v;
+}
+
+int api_fail(int status, const char* detail) { return fail(status, "%s", detail); }
+
+int api_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+
+void api_clear_error() { t_err[0] = 0; }
+
 }  // namespace swg
 
 using namespace swg;
