@@ -8,6 +8,7 @@
 #include <mutex>
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "../../include/swiglu.h"
@@ -42,6 +43,7 @@ struct DeviceInfo {
   int num_sms = 0;
   int cc_major = 0, cc_minor = 0;
   cudaMemPool_t pool = nullptr;
+  unsigned* status = nullptr;   // device address of g_device_status
 };
 
 std::mutex g_mu;
@@ -62,6 +64,12 @@ int current_device(int* dev_out, DeviceInfo* out) {
       return cuda_fail(e, "cudaDeviceGetAttribute(cc major)");
     if ((e = cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
       return cuda_fail(e, "cudaDeviceGetAttribute(cc minor)");
+    if (di.cc_major == 10 && di.cc_minor == 3) {
+      void* sp = nullptr;
+      if ((e = cudaGetSymbolAddress(&sp, g_device_status)) != cudaSuccess)
+        return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+      di.status = (unsigned*)sp;
+    }
     di.ready = true;
   }
   *dev_out = dev;
@@ -106,22 +114,35 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 // Largest M the dispatcher sends to the skinny (split-K) path for bf16.
 constexpr int64_t kSkinnyMaxM = 16;
 // Grid-dimension limits of the SIMT path (gridDim.y/z are 16-bit).
-constexpr int64_t kMaxGridYZ = 65535;
+constexpr int64_t kMaxGridYZ = kSimtMaxGridYZ;
 
-int resolve_path(int64_t M, int dtype, int path, int* out) {
+// Bound of every device-side wait, from SWIGLU_WAIT_TIMEOUT_MS (default 2 s).
+uint64_t wait_timeout_ns() {
+  static uint64_t ns = [] {
+    const char* v = getenv("SWIGLU_WAIT_TIMEOUT_MS");
+    long long ms = v ? atoll(v) : 0;
+    if (ms <= 0) ms = 2000;
+    return (uint64_t)ms * 1000000ull;
+  }();
+  return ns;
+}
+
+// AUTO: f32 -> SIMT; bf16 M <= kSkinnyMaxM -> SKINNY; larger bf16 M -> TC.
+// d == 0 (empty sums) always goes to the SIMT path, whose reduction kernel
+// then writes h = silu(0) * 0 = 0.
+int resolve_path(int64_t M, int64_t d, int dtype, int path, int* out) {
   if (path < SWIGLU_PATH_AUTO || path > SWIGLU_PATH_TC)
     return fail(SWIGLU_ERR_INVALID_ARG, "unknown path %d", path);
   if (path == SWIGLU_PATH_AUTO) {
-    // Tensor-core paths are not part of this build yet: every call is served
-    // by the SIMT split-K path.
-    (void)M;
-    *out = SWIGLU_PATH_SIMT;
+    if (dtype == SWIGLU_F32 || d == 0) *out = SWIGLU_PATH_SIMT;
+    else *out = M <= kSkinnyMaxM ? SWIGLU_PATH_SKINNY : SWIGLU_PATH_TC;
     return SWIGLU_OK;
   }
-  if (path != SWIGLU_PATH_SIMT)
-    return fail(SWIGLU_ERR_UNSUPPORTED, "path %d is not available in this build", path);
-  (void)dtype;
-  *out = path;
+  if (path != SWIGLU_PATH_SIMT && dtype != SWIGLU_BF16)
+    return fail(SWIGLU_ERR_UNSUPPORTED, "the tensor-core paths serve bf16 only");
+  if (path == SWIGLU_PATH_SKINNY && M > kSkinnyMaxN)
+    return fail(SWIGLU_ERR_UNSUPPORTED, "the skinny path serves M <= %d", kSkinnyMaxN);
+  *out = d == 0 ? SWIGLU_PATH_SIMT : path;
   return SWIGLU_OK;
 }
 
@@ -152,20 +173,42 @@ int validate(const void* x, const void* wg, const void* wu, const void* h,
 struct Plan {
   int path;
   SimtPlan simt;
+  SkinnyPlan skinny;
+  TilePlan tile;
   int64_t slices;
+  int64_t grid;
+  int64_t launches;   // kernels one call launches
   size_t workspace;
 };
 
 int make_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, int path, int num_sms, Plan* p) {
   int rp = 0;
-  int st = resolve_path(M, dtype, path, &rp);
+  int st = resolve_path(M, d, dtype, path, &rp);
   if (st != SWIGLU_OK) return st;
+  *p = Plan{};
   p->path = rp;
-  p->simt = plan_simt(M, d, d_ff, dtype, num_sms);
-  if (p->simt.slices > kMaxGridYZ || p->simt.row_chunks > kMaxGridYZ)
-    return fail(SWIGLU_ERR_UNSUPPORTED, "shape exceeds the grid limits of the SIMT path");
-  p->slices = p->simt.slices;
-  p->workspace = partial_elems(p->slices, M, d_ff) * sizeof(float);
+  if (rp == SWIGLU_PATH_SIMT) {
+    p->simt = plan_simt(M, d, d_ff, dtype, num_sms);
+    if (p->simt.slices > kMaxGridYZ || p->simt.row_chunks > kMaxGridYZ)
+      return fail(SWIGLU_ERR_UNSUPPORTED, "shape exceeds the grid limits of the SIMT path");
+    p->slices = p->simt.slices;
+    p->grid = p->simt.col_blocks * p->simt.slices * p->simt.row_chunks;
+    p->workspace = partial_elems(p->slices, M, d_ff) * sizeof(float);
+    p->launches = p->slices > 0 ? 2 : 1;
+  } else if (rp == SWIGLU_PATH_SKINNY) {
+    p->skinny = plan_skinny(M, d, d_ff, num_sms);
+    p->slices = p->skinny.maxq;
+    p->grid = p->skinny.grid;
+    p->workspace = p->skinny.counters_bytes + p->skinny.part_bytes;
+    p->launches = 1;
+  } else {
+    p->tile = plan_tile(M, d, d_ff, num_sms);
+    p->slices = 1;
+    p->grid = p->tile.grid;
+    p->workspace = 0;
+    p->launches = 1;
+  }
+  if (M == 0 || d_ff == 0) p->launches = 0;
   p->workspace = (p->workspace + 255) / 256 * 256;
   return SWIGLU_OK;
 }
@@ -209,8 +252,14 @@ int run(const void* x, const void* wg, const void* wu, void* h, int64_t M, int64
   }
 
   cudaError_t e = cudaSuccess;
-  e = launch_simt_partial(x, wg, wu, part, M, d, d_ff, dtype, p.simt, st);
-  if (e == cudaSuccess) e = launch_reduce_swiglu(part, h, M, d_ff, p.slices, dtype, di.num_sms, st);
+  if (p.path == SWIGLU_PATH_SIMT) {
+    e = launch_simt_partial(x, wg, wu, part, M, d, d_ff, dtype, p.simt, st);
+    if (e == cudaSuccess) e = launch_reduce_swiglu(part, h, M, d_ff, p.slices, dtype, di.num_sms, st);
+  } else if (p.path == SWIGLU_PATH_SKINNY) {
+    e = launch_skinny_tc(x, wg, wu, h, M, d, d_ff, p.skinny, part, di.status, wait_timeout_ns(), st);
+  } else {
+    e = launch_tile_tc(x, wg, wu, h, M, d, d_ff, p.tile, di.status, wait_timeout_ns(), st);
+  }
   if (pooled) {
     cudaError_t ef = cudaFreeAsync(part, st);
     if (e == cudaSuccess) e = ef;
@@ -291,11 +340,11 @@ int swiglu_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, int path, int num
   if (v != SWIGLU_OK) return v;
   out->path = p.path;
   out->slices = p.slices;
-  out->grid = p.simt.col_blocks * p.simt.slices * p.simt.row_chunks;
-  out->row_chunk = p.simt.row_chunk;
+  out->grid = p.grid;
+  out->row_chunk = p.path == SWIGLU_PATH_SIMT ? p.simt.row_chunk : 0;
   out->workspace = (int64_t)p.workspace;
   out->skinny_max_m = kSkinnyMaxM;
-  out->launches = (M == 0 || d_ff == 0) ? 0 : (p.slices > 0 ? 2 : 1);
+  out->launches = p.launches;
   return SWIGLU_OK;
 }
 

@@ -1,0 +1,372 @@
+// Skinny-M path on the tensor cores (bf16, M <= 256): one kernel, split-K,
+// deterministic in-kernel reduction, SwiGLU applied after the sums complete.
+//
+// The decode-time product of "Ou part le temps d'un token" ("Un kernel pour
+// les matrices etroites") has too few output rows to fill the GPU, so the
+// work is cut along the weights: the grid is split over (64-column block,
+// 64-deep k block) units of W_gate/W_up, and the shared dimension K is split
+// among CTAs so that every SM streams the same amount of weight bytes.
+// Partial sums of each column block are combined in a fixed order (by k),
+// never with atomics into the output, so a call's result is reproducible bit
+// for bit, as that section requires.  As in its slice-reduction pass
+// ("Deux operations de trop" puts the bias there), the element-wise work --
+// here silu(g) * u -- runs only once the sums are complete.
+//
+// GB300 design (not the page's SIMT kernel):
+//   * swap-AB tcgen05 MMA: A = a 128-row tile made of 64 W_gate columns and
+//     the same 64 W_up columns (the gate/up column interleave of the SwiGLU
+//     paper's Kernel-2, done per 64-column tile while loading, so W_gate and
+//     W_up stay separate row-major arrays), MN-major from shared memory;
+//     B = x^T, K-major, N = M rounded up (rows past M are zero-filled by TMA);
+//     the accumulator D^T [128 x N] f32 lives in TMEM;
+//   * TMA loads into an 8-12 stage shared-memory ring keep ~150-200 KB of
+//     weight reads in flight per SM (Little's law at ~45 GB/s per SM);
+//   * a persistent grid of one CTA per SM gets an equal share of units
+//     (stream-K-style partition), so no SM idles at the tail;
+//   * each CTA writes one f32 partial per column block it touched; the CTA
+//     that finishes a column block last (an arrival counter, no waiting) sums
+//     the partials in contributor order -- i.e. in k order -- applies
+//     silu(g) * u and stores h as bf16.
+//
+// Warp roles (192 threads): warp 0 lane 0 issues TMA, warp 1 lane 0 issues
+// MMAs (warp 1 owns the TMEM allocation), warps 2-5 drain the accumulator.
+// Every mbarrier wait is bounded; on timeout the CTA raises the device error
+// word, stops, lets its in-flight copies and MMAs finish, frees TMEM and exits.
+#include "common.cuh"
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace swg {
+namespace {
+
+using namespace tc;
+
+constexpr int kBK = 64;                               // k per stage (128-byte rows)
+constexpr int kCB = 64;                               // columns per weight per unit
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kChunkBytes = kCB * kBK * 2;       // one 64 x 64 bf16 weight box
+constexpr uint32_t kATileBytes = 2 * kChunkBytes;     // gate chunk + up chunk
+
+template <int N>
+struct SkCfg {
+  static constexpr uint32_t kBTileBytes = (uint32_t)N * kBK * 2;
+  static constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr int kFit = (int)((200u * 1024u) / kStageBytes);
+  static constexpr int kStages = kFit > 12 ? 12 : kFit;
+  static constexpr uint32_t kTmemCols = 2 * N < 32 ? 32 : 2 * N;
+  static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
+};
+
+struct SkArgs {
+  int M, d_ff, n_kb, maxq;
+  int64_t units;
+  int grid;
+  float* part;          // [n_cb][maxq][2][M][64]
+  unsigned* counters;   // [n_cb], zero on entry
+  uint16_t* h;          // [M][d_ff] bf16
+  unsigned* status;
+  uint64_t timeout_ns;
+};
+
+// CTA whose unit range [c U / G, (c+1) U / G) contains unit t.
+__device__ __forceinline__ int64_t cta_of(int64_t t, int64_t U, int64_t G) {
+  return ((t + 1) * G + U - 1) / U - 1;
+}
+
+__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, unsigned* status,
+                                           uint64_t timeout_ns) {
+  int never = 0;
+  return mbar_wait(bar, parity, &never, status, timeout_ns);
+}
+
+template <int N>
+__global__ void __launch_bounds__(kThreads, 1)
+skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+                 const __grid_constant__ CUtensorMap tm_wg,
+                 const __grid_constant__ CUtensorMap tm_wu, const SkArgs a) {
+  using C = SkCfg<N>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* stages = smem_raw + pad;
+  uint64_t* full = reinterpret_cast<uint64_t*>(stages + (size_t)C::kStages * C::kStageBytes);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* tfull = empty + C::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* ticket = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t U = a.units, G = a.grid, c = blockIdx.x;
+  const int64_t u0 = c * U / G, u1 = (c + 1) * U / G;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&tfull[0], 1);
+    mbar_init(&tfull[1], 1);
+    mbar_init(&tempty[0], kEpiThreads);
+    mbar_init(&tempty[1], kEpiThreads);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_wg);
+    tma_prefetch_desc(&tm_wu);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint64_t keep_weights_out = policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int64_t t = u0; t < u1; ++t) {
+        const int cb = (int)(t / a.n_kb), kb = (int)(t - (int64_t)cb * a.n_kb);
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status, a.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = stages + (size_t)stage * C::kStageBytes;
+        mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+        tma_load_2d_hint(st, &tm_wg, &full[stage], cb * kCB, kb * kBK, keep_weights_out);
+        tma_load_2d_hint(st + kChunkBytes, &tm_wu, &full[stage], cb * kCB, kb * kBK,
+                         keep_weights_out);
+        tma_load_2d(st + kATileBytes, &tm_x, &full[stage], kb * kBK, 0);
+        ++issued;
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA's memory goes away
+        const int64_t first = issued > C::kStages ? issued - C::kStages : 0;
+        for (int64_t i = first; i < issued; ++i)
+          wait_drain(&full[i % C::kStages], (uint32_t)((i / C::kStages) & 1), a.status,
+                     a.timeout_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, N, /*a_mn=*/true, /*b_mn=*/false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      int64_t t = u0;
+      while (ok && t < u1) {
+        const int64_t cb = t / a.n_kb;
+        const int64_t seg_end = min(u1, (cb + 1) * (int64_t)a.n_kb);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, a.status, a.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * N);
+        for (int64_t tt = t; tt < seg_end; ++tt) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, a.status, a.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stages + (size_t)stage * C::kStageBytes);
+          const uint32_t b_addr = a_addr + kATileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // A: 16 k-rows further down the MN-major tile (2 swizzle atoms);
+            // B: 32 bytes further along the K-major 128-byte rows.
+            const uint64_t ad = smem_desc_sw128(a_addr + kk * 2048u, kChunkBytes, 1024u);
+            const uint64_t bd = smem_desc_sw128(b_addr + kk * 32u, 16u, 1024u);
+            mma_bf16(d_tmem, ad, bd, idesc, (tt != t || kk != 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+        t = seg_end;
+      }
+      // every MMA this thread issued completes before TMEM is released
+      mma_commit(drain);
+      wait_drain(drain, 0, a.status, a.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: warps 2..5 ----------------
+    const int quarter = warp & 3;          // TMEM lanes this warp may read
+    const int row = quarter * 32 + lane;   // tile row: 0..63 gate, 64..127 up
+    const int gu = row >> 6, j = row & 63;
+    const int et = threadIdx.x - 64;       // 0..127
+    const int64_t Mrow = (int64_t)a.M * kCB;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int64_t t = u0;
+    while (t < u1) {
+      const int64_t cb = t / a.n_kb;
+      const int64_t seg_end = min(u1, (cb + 1) * (int64_t)a.n_kb);
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, a.status, a.timeout_ns)) break;
+      tc_fence_after();
+      const int64_t c_lo = cta_of(cb * a.n_kb, U, G);
+      const int64_t c_hi = cta_of((cb + 1) * a.n_kb - 1, U, G);
+      const int n_contrib = (int)(c_hi - c_lo + 1);
+      float* slot = a.part + ((cb * a.maxq + (c - c_lo)) * 2 + gu) * Mrow;
+#pragma unroll
+      for (int ch = 0; ch < N / 16; ++ch) {
+        uint32_t r[16];
+        tmem_ld_x16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N + ch * 16), r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int m = ch * 16 + i;
+          if (m < a.M) slot[(int64_t)m * kCB + j] = __uint_as_float(r[i]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+      // The CTA that completes column block cb last reduces it.
+      __syncwarp();
+      named_bar_sync(1, kEpiThreads);
+      if (et == 0) {
+        __threadfence();
+        *ticket = (int)atomicAdd(&a.counters[cb], 1u);
+      }
+      __syncwarp();
+      named_bar_sync(1, kEpiThreads);
+      if (*ticket == n_contrib - 1) {
+        __threadfence();
+        const int jj = et & 63, mh = et >> 6;
+        const int64_t col = cb * kCB + jj;
+        if (col < a.d_ff) {
+          const float* pb = a.part + cb * a.maxq * 2 * Mrow + jj;
+          for (int m = mh; m < a.M; m += 2) {
+            float g = 0.f, u = 0.f;
+            for (int q = 0; q < n_contrib; ++q) {
+              g += __ldcg(pb + (int64_t)(2 * q) * Mrow + (int64_t)m * kCB);
+              u += __ldcg(pb + (int64_t)(2 * q + 1) * Mrow + (int64_t)m * kCB);
+            }
+            a.h[(int64_t)m * a.d_ff + col] = (uint16_t)f32_to_bf16_bits(silu_fast(g) * u);
+          }
+        }
+        if (et == 0) a.counters[cb] = 0u;
+      }
+      t = seg_end;
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int N>
+cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mu,
+                     const SkArgs& a, cudaStream_t st) {
+  using C = SkCfg<N>;
+  auto kern = skinny_tc_kernel<N>;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) configured[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  return cudaLaunchKernelEx(&cfg, kern, mx, mg, mu, a);
+}
+
+}  // namespace
+
+SkinnyPlan plan_skinny(int64_t M, int64_t d, int64_t d_ff, int num_sms) {
+  SkinnyPlan p{};
+  int n = 16;
+  while (n < M) n *= 2;
+  p.n_pad = n;
+  p.n_cb = (d_ff + kCB - 1) / kCB;
+  p.n_kb = (d + kBK - 1) / kBK;
+  p.units = p.n_cb * p.n_kb;
+  p.grid = (int)(p.units < num_sms ? p.units : num_sms);
+  if (p.grid < 1) p.grid = 1;
+  const int64_t per = p.units > 0 ? p.units / p.grid : 1;   // fewest units a CTA gets
+  p.maxq = (int)((p.n_kb + per - 1) / (per > 0 ? per : 1) + 1);
+  p.counters_bytes = ((size_t)p.n_cb * sizeof(unsigned) + 255) / 256 * 256;
+  p.part_bytes = (size_t)p.n_cb * p.maxq * 2 * (size_t)M * kCB * sizeof(float);
+  p.part_bytes = (p.part_bytes + 255) / 256 * 256;
+  return p;
+}
+
+cudaError_t launch_skinny_tc(const void* x, const void* wg, const void* wu, void* h, int64_t M,
+                             int64_t d, int64_t d_ff, const SkinnyPlan& p, void* workspace,
+                             unsigned* status, uint64_t timeout_ns, cudaStream_t st) {
+  if (p.units == 0 || M == 0) return cudaSuccess;
+  CUtensorMap mx, mg, mu;
+  cudaError_t e;
+  if ((e = make_tmap_bf16_2d(&mx, x, M, d, kBK, p.n_pad)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_2d(&mg, wg, d, d_ff, kCB, kBK)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_2d(&mu, wu, d, d_ff, kCB, kBK)) != cudaSuccess) return e;
+  unsigned* counters = (unsigned*)workspace;
+  float* part = (float*)((char*)workspace + p.counters_bytes);
+  if ((e = cudaMemsetAsync(counters, 0, (size_t)p.n_cb * sizeof(unsigned), st)) != cudaSuccess)
+    return e;
+  SkArgs a;
+  a.M = (int)M;
+  a.d_ff = (int)d_ff;
+  a.n_kb = (int)p.n_kb;
+  a.maxq = p.maxq;
+  a.units = p.units;
+  a.grid = p.grid;
+  a.part = part;
+  a.counters = counters;
+  a.h = (uint16_t*)h;
+  a.status = status;
+  a.timeout_ns = timeout_ns;
+  switch (p.n_pad) {
+    case 16: return launch_n<16>(mx, mg, mu, a, st);
+    case 32: return launch_n<32>(mx, mg, mu, a, st);
+    case 64: return launch_n<64>(mx, mg, mu, a, st);
+    case 128: return launch_n<128>(mx, mg, mu, a, st);
+    case 256: return launch_n<256>(mx, mg, mu, a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace swg

@@ -1,0 +1,49 @@
+// Host-side creation of TMA tensor maps (cuTensorMapEncodeTiled, reached
+// through the runtime's driver entry-point query so the library does not link
+// libcuda directly).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace swg {
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_once;
+cudaError_t g_init_err = cudaSuccess;
+
+void init_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  g_init_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                cudaEnableDefault, &q);
+  if (g_init_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
+    g_init_err = cudaErrorSymbolNotFound;
+  if (g_init_err == cudaSuccess) g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+}
+}  // namespace
+
+// 2-D bf16 row-major tensor [rows, cols] (cols contiguous) with a box of
+// box_cols x box_rows elements and 128-byte swizzle; out-of-range elements
+// read as zero.  box_cols * 2 must be <= 128.
+cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                              int box_cols, int box_rows) {
+  std::call_once(g_once, init_encode);
+  if (!g_encode) return g_init_err != cudaSuccess ? g_init_err : cudaErrorSymbolNotFound;
+  // A tensor map needs every extent >= 1; callers never ask for empty maps.
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t elem_strides[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace swg

@@ -16,7 +16,7 @@ from tests.parity import TOL, compare
 
 pytestmark = pytest.mark.gpu
 
-PATHS_BY_DTYPE = {"f32": ["simt"], "bf16": ["simt"]}
+PATHS_BY_DTYPE = {"f32": ["simt"], "bf16": ["simt", "skinny", "tc"]}
 
 
 def odt(dtype):
@@ -95,6 +95,33 @@ def test_bf16_prefill_sampled():
 @pytest.mark.parametrize("M", [16, 2048, 8192])
 def test_bf16_large_model_sampled(M):
     sampled_check(M, 8192, 29568, "bf16", "auto", n=2000, seed=M)
+
+
+@pytest.mark.parametrize("M", [17, 64, 256])
+def test_forced_paths_agree(M):
+    # the three kernels serve the same call; each must match the oracle
+    d, d_ff = 640, 1160
+    x, wg, wu = inputs.make_inputs(M, d, d_ff, "bf16", seed=40 + M)
+    raw = inputs.raw_bits
+    h64, _, sens = oracle.swiglu_up(raw(x), raw(wg), raw(wu), oracle.BF16)
+    outs = {}
+    for path in PATHS_BY_DTYPE["bf16"]:
+        outs[path] = to64(gpu_run(x, wg, wu, path))
+        assert compare(outs[path], h64, sens, "bf16", d)["ok"], path
+    for a in outs:
+        for b in outs:
+            assert compare(outs[a], outs[b], sens, "bf16", d)["ok"], (a, b)
+
+
+def test_dispatch_rule():
+    for M, path in [(1, "skinny"), (16, "skinny"), (17, "tc"), (4096, "tc")]:
+        assert swg.plan(M, 4096, 14336, "bf16", "auto", 152)["path"] == path
+    assert swg.plan(1, 512, 2048, "f32", "auto", 152)["path"] == "simt"
+    assert swg.plan(3, 0, 64, "bf16", "auto", 152)["path"] == "simt"
+    with pytest.raises(swg.SwiGLUError):
+        swg.plan(257, 64, 64, "bf16", "skinny", 152)
+    with pytest.raises(swg.SwiGLUError):
+        swg.plan(4, 64, 64, "f32", "tc", 152)
 
 
 # --------------------------------------------------------------------------
@@ -198,23 +225,25 @@ def test_output_guard_band_untouched():
             assert torch.all(buf[:pad] == -3.0) and torch.all(buf[-pad:] == -3.0)
 
 
-def test_caller_workspace_and_errors():
+@pytest.mark.parametrize("path", ["simt", "skinny"])
+def test_caller_workspace_and_errors(path):
     dev = torch.device("cuda", 0)
     M, d, d_ff = 3, 1024, 2048
     x, wg, wu = (t.to(dev) for t in inputs.make_inputs(M, d, d_ff, "bf16", seed=35))
-    need = swg.workspace_bytes(M, d, d_ff, "bf16", "simt")
+    need = swg.workspace_bytes(M, d, d_ff, "bf16", path)
     assert need > 0
-    ws = torch.empty(need + 256, dtype=torch.uint8, device=dev)
-    a = swg.swiglu_up(x, wg, wu, path="simt", workspace=ws[:need])
-    b = swg.swiglu_up(x, wg, wu, path="simt")
+    ws = torch.full((need + 256,), 0xAB, dtype=torch.uint8, device=dev)   # stale contents
+    a = swg.swiglu_up(x, wg, wu, path=path, workspace=ws[:need])
+    b = swg.swiglu_up(x, wg, wu, path=path)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     with pytest.raises(swg.SwiGLUError) as e:
-        swg.swiglu_up(x, wg, wu, path="simt", workspace=ws[:need - 256])
+        swg.swiglu_up(x, wg, wu, path=path, workspace=ws[:need - 256])
     assert e.value.status == 8
     with pytest.raises(swg.SwiGLUError) as e:
-        swg.swiglu_up(x, wg, wu, path="simt", workspace=ws[16:16 + need])
+        swg.swiglu_up(x, wg, wu, path=path, workspace=ws[16:16 + need])
     assert e.value.status == 8
+    assert swg.workspace_bytes(M, d, d_ff, "bf16", "tc") == 0
 
 
 def test_misaligned_pointer_rejected():
