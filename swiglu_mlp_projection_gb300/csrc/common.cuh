@@ -7,7 +7,10 @@
 namespace swg {
 
 // Bits of the device error word (see swiglu_check_device_status).
-enum : unsigned { kStatusTimeout = 1u };
+//   kStatusTimeout: a bounded wait gave up.
+//   kStatusStaleCounter: an arrival counter did not start at zero (left over
+//   by a call that gave up), so a column group was not reduced.
+enum : unsigned { kStatusTimeout = 1u, kStatusStaleCounter = 2u };
 
 // bf16 -> f32 is exact: a bf16 value is the upper half of a binary32.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -47,13 +47,16 @@ constexpr int64_t kSimtMaxGridYZ = 65535;
 
 // TMA descriptor of a row-major bf16 matrix [rows, cols], 128-byte swizzle.
 cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
-                              int box_cols, int box_rows);
+                              int box_cols, int box_rows, int l2_promo_bytes = 256);
 
 // Skinny tensor-core path (bf16, small M): swap-AB split-K over a balanced
 // partition of (64-column block, 64-deep k block) units.
 struct SkinnyPlan {
   int n_pad;               // M rounded up to the MMA N granule (16..256)
-  int64_t n_cb, n_kb;      // 64-column blocks, 64-deep k blocks
+  int nb;                  // 64-column blocks per unit (1, 2 or 4)
+  int l2_promo;            // L2 promotion of the weight loads (bytes, 0 = none)
+  int hint;                // weight-load L2 hint: 0 none, 1 evict_first
+  int64_t n_cb, n_kb;      // units: (nb x 64)-column groups, 64-deep k blocks
   int64_t units;           // n_cb * n_kb
   int grid;                // CTAs (<= SM count)
   int maxq;                // partial slots per column block
@@ -62,9 +65,13 @@ struct SkinnyPlan {
 };
 constexpr int kSkinnyMaxN = 256;
 SkinnyPlan plan_skinny(int64_t M, int64_t d, int64_t d_ff, int num_sms);
+// `clean_counters`: n_cb arrival counters known to be zero (left so by the
+// previous call on the same stream), or null to clear the workspace's own.
 cudaError_t launch_skinny_tc(const void* x, const void* wg, const void* wu, void* h, int64_t M,
                              int64_t d, int64_t d_ff, const SkinnyPlan& p, void* workspace,
-                             unsigned* status, uint64_t timeout_ns, cudaStream_t st);
+                             unsigned* clean_counters, unsigned* status, uint64_t timeout_ns,
+                             cudaStream_t st);
+constexpr size_t kStreamCounterBytes = 64 * 1024;   // per-stream arrival counters
 
 // Tile tensor-core path (bf16, large M): 128 x (128 gate + 128 up) output
 // tiles, SwiGLU applied to the accumulator tile before a single bf16 store.

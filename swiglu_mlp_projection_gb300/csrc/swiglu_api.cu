@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <vector>
 #include <stdarg.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -99,6 +100,70 @@ int device_pool(int dev, cudaMemPool_t* pool) {
   }
   *pool = di.pool;
   return SWIGLU_OK;
+}
+
+// Arrival counters of the skinny kernel, kept per stream.  The kernel leaves
+// every counter it used at zero, so the next call on the same stream (ordered
+// after it) can use them without clearing them first.  Streams are told apart
+// by cudaStreamGetId, which is never reused within a process.  Counters of a
+// call that gave up may be left non-zero: swiglu_check_device_status marks the
+// device's counters dirty and the next call clears them.
+struct StreamCounters {
+  int dev;
+  unsigned long long stream_id;
+  unsigned* counters;
+  bool dirty;
+};
+constexpr size_t kMaxStreamSlots = 256;
+std::vector<StreamCounters> g_stream_counters;   // guarded by g_mu
+
+int device_pool(int dev, cudaMemPool_t* pool);
+
+// Zeroed counters for `st`, or *out = null when the call must clear the
+// workspace's own counters (the per-thread default stream, whose handle is
+// shared by threads that are not ordered with each other; too many streams;
+// or more counters than a slot holds).
+int stream_counters(int dev, cudaStream_t st, size_t need_bytes, unsigned** out) {
+  *out = nullptr;
+  if (st == cudaStreamPerThread || need_bytes > kStreamCounterBytes) return SWIGLU_OK;
+  unsigned long long id = 0;
+  if (cudaStreamGetId(st, &id) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_OK;
+  }
+  cudaMemPool_t pool;
+  int v = device_pool(dev, &pool);
+  if (v != SWIGLU_OK) return v;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& sc : g_stream_counters) {
+    if (sc.dev == dev && sc.stream_id == id) {
+      if (sc.dirty) {
+        cudaError_t e = cudaMemsetAsync(sc.counters, 0, kStreamCounterBytes, st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
+        sc.dirty = false;
+      }
+      *out = sc.counters;
+      return SWIGLU_OK;
+    }
+  }
+  if (g_stream_counters.size() >= kMaxStreamSlots) return SWIGLU_OK;
+  void* p = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&p, kStreamCounterBytes, pool, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_OK;   // fall back to clearing the workspace's counters
+  }
+  e = cudaMemsetAsync(p, 0, kStreamCounterBytes, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
+  g_stream_counters.push_back({dev, id, (unsigned*)p, false});
+  *out = (unsigned*)p;
+  return SWIGLU_OK;
+}
+
+void mark_counters_dirty(int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& sc : g_stream_counters)
+    if (sc.dev == dev) sc.dirty = true;
 }
 
 int elem_bytes(int dtype) { return dtype == SWIGLU_BF16 ? 2 : 4; }
@@ -256,7 +321,13 @@ int run(const void* x, const void* wg, const void* wu, void* h, int64_t M, int64
     e = launch_simt_partial(x, wg, wu, part, M, d, d_ff, dtype, p.simt, st);
     if (e == cudaSuccess) e = launch_reduce_swiglu(part, h, M, d_ff, p.slices, dtype, di.num_sms, st);
   } else if (p.path == SWIGLU_PATH_SKINNY) {
-    e = launch_skinny_tc(x, wg, wu, h, M, d, d_ff, p.skinny, part, di.status, wait_timeout_ns(), st);
+    unsigned* clean = nullptr;
+    if ((v = stream_counters(dev, st, (size_t)p.skinny.n_cb * sizeof(unsigned), &clean)) != SWIGLU_OK) {
+      if (pooled) cudaFreeAsync(part, st);
+      return v;
+    }
+    e = launch_skinny_tc(x, wg, wu, h, M, d, d_ff, p.skinny, part, clean, di.status,
+                         wait_timeout_ns(), st);
   } else {
     e = launch_tile_tc(x, wg, wu, h, M, d, d_ff, p.tile, di.status, wait_timeout_ns(), st);
   }
@@ -363,7 +434,11 @@ int swiglu_check_device_status(void) {
     const unsigned zero = 0;
     e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
-    return fail(SWIGLU_ERR_TIMEOUT, "a device-side wait gave up (status word 0x%x)", word);
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) mark_counters_dirty(dev);
+    return fail(SWIGLU_ERR_TIMEOUT,
+                "a device-side wait gave up or found a stale arrival counter (status word 0x%x)",
+                word);
   }
   return SWIGLU_OK;
 }

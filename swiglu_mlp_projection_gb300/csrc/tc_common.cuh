@@ -78,6 +78,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+
+// Wait until the grids this one depends on (the previous kernel in the stream,
+// when launched with programmatic stream serialization) have completed and
+// their memory is visible.  Everything before this call must touch no global
+// memory that those grids read or write.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next kernel in the stream to be scheduled (it still waits in its
+// own pdl_wait for this grid to finish).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- TMA ----------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -32,6 +32,8 @@
 // MMAs (warp 1 owns the TMEM allocation), warps 2-5 drain the accumulator.
 // Every mbarrier wait is bounded; on timeout the CTA raises the device error
 // word, stops, lets its in-flight copies and MMAs finish, frees TMEM and exits.
+#include <stdlib.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -42,28 +44,40 @@ namespace {
 using namespace tc;
 
 constexpr int kBK = 64;                               // k per stage (128-byte rows)
-constexpr int kCB = 64;                               // columns per weight per unit
+constexpr int kCB = 64;                               // columns of one weight box
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kChunkBytes = kCB * kBK * 2;       // one 64 x 64 bf16 weight box
-constexpr uint32_t kATileBytes = 2 * kChunkBytes;     // gate chunk + up chunk
+constexpr uint32_t kSubBytes = 2 * kChunkBytes;       // gate box + up box = one MMA A tile
 
-template <int N>
+constexpr uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
+  uint32_t r = lo;
+  while (r < v) r *= 2;
+  return r;
+}
+
+// N: MMA N (M of the call rounded up); NB: adjacent 64-column blocks per unit,
+// so every weight row is read in NB x 128-byte contiguous runs per matrix.
+template <int N, int NB>
 struct SkCfg {
   static constexpr uint32_t kBTileBytes = (uint32_t)N * kBK * 2;
-  static constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr uint32_t kStageBytes = NB * kSubBytes + kBTileBytes;
   static constexpr int kFit = (int)((200u * 1024u) / kStageBytes);
   static constexpr int kStages = kFit > 12 ? 12 : kFit;
-  static constexpr uint32_t kTmemCols = 2 * N < 32 ? 32 : 2 * N;
+  static constexpr uint32_t kAccCols = (uint32_t)NB * N;          // one accumulator buffer
+  static constexpr uint32_t kTmemCols = pow2_at_least(2 * kAccCols, 32);
   static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
+  static_assert(2 * kAccCols <= 512, "accumulators exceed TMEM");
+  static_assert(kStages >= 2, "stage too large");
 };
 
 struct SkArgs {
   int M, d_ff, n_kb, maxq;
   int64_t units;
   int grid;
-  float* part;          // [n_cb][maxq][2][M][64]
-  unsigned* counters;   // [n_cb], zero on entry
+  int hint;             // 1: weight loads carry an L2 evict_first hint
+  float* part;          // [n_cg][maxq][NB][2][M][64]
+  unsigned* counters;   // [n_cg], zero on entry, zero again on exit
   uint16_t* h;          // [M][d_ff] bf16
   unsigned* status;
   uint64_t timeout_ns;
@@ -80,12 +94,12 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, unsig
   return mbar_wait(bar, parity, &never, status, timeout_ns);
 }
 
-template <int N>
+template <int N, int NB>
 __global__ void __launch_bounds__(kThreads, 1)
 skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                  const __grid_constant__ CUtensorMap tm_wg,
                  const __grid_constant__ CUtensorMap tm_wu, const SkArgs a) {
-  using C = SkCfg<N>;
+  using C = SkCfg<N, NB>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* stages = smem_raw + pad;
@@ -126,27 +140,40 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Everything above overlaps the previous kernel's tail; from here on the
+  // kernel reads x and the workspace, which that kernel may still be writing.
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      const uint64_t keep_weights_out = policy_evict_first();
+      const uint64_t evict_first = policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
       for (int64_t t = u0; t < u1; ++t) {
-        const int cb = (int)(t / a.n_kb), kb = (int)(t - (int64_t)cb * a.n_kb);
+        const int cg = (int)(t / a.n_kb), kb = (int)(t - (int64_t)cg * a.n_kb);
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status, a.timeout_ns)) {
           ok = false;
           break;
         }
         uint8_t* st = stages + (size_t)stage * C::kStageBytes;
         mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-        tma_load_2d_hint(st, &tm_wg, &full[stage], cb * kCB, kb * kBK, keep_weights_out);
-        tma_load_2d_hint(st + kChunkBytes, &tm_wu, &full[stage], cb * kCB, kb * kBK,
-                         keep_weights_out);
-        tma_load_2d(st + kATileBytes, &tm_x, &full[stage], kb * kBK, 0);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const int col = (cg * NB + b) * kCB;
+          uint8_t* sb = st + b * kSubBytes;
+          if (a.hint) {
+            tma_load_2d_hint(sb, &tm_wg, &full[stage], col, kb * kBK, evict_first);
+            tma_load_2d_hint(sb + kChunkBytes, &tm_wu, &full[stage], col, kb * kBK, evict_first);
+          } else {
+            tma_load_2d(sb, &tm_wg, &full[stage], col, kb * kBK);
+            tma_load_2d(sb + kChunkBytes, &tm_wu, &full[stage], col, kb * kBK);
+          }
+        }
+        tma_load_2d(st + NB * kSubBytes, &tm_x, &full[stage], kb * kBK, 0);
         ++issued;
         if (++stage == C::kStages) {
           stage = 0;
@@ -173,29 +200,33 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
       bool ok = true;
       int64_t t = u0;
       while (ok && t < u1) {
-        const int64_t cb = t / a.n_kb;
-        const int64_t seg_end = min(u1, (cb + 1) * (int64_t)a.n_kb);
+        const int64_t cg = t / a.n_kb;
+        const int64_t seg_end = min(u1, (cg + 1) * (int64_t)a.n_kb);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, a.status, a.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(acc * N);
         for (int64_t tt = t; tt < seg_end; ++tt) {
           if (!mbar_wait(&full[stage], phase, abort_flag, a.status, a.timeout_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(stages + (size_t)stage * C::kStageBytes);
-          const uint32_t b_addr = a_addr + kATileBytes;
+          const uint32_t s_addr = smem_u32(stages + (size_t)stage * C::kStageBytes);
+          const uint32_t b_addr = s_addr + NB * kSubBytes;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            // A: 16 k-rows further down the MN-major tile (2 swizzle atoms);
-            // B: 32 bytes further along the K-major 128-byte rows.
-            const uint64_t ad = smem_desc_sw128(a_addr + kk * 2048u, kChunkBytes, 1024u);
-            const uint64_t bd = smem_desc_sw128(b_addr + kk * 32u, 16u, 1024u);
-            mma_bf16(d_tmem, ad, bd, idesc, (tt != t || kk != 0) ? 1u : 0u);
+          for (int b = 0; b < NB; ++b) {
+            const uint32_t d_tmem = tmem + (uint32_t)(acc * C::kAccCols + b * N);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              // A: 16 k-rows further down the MN-major tile (2 swizzle atoms);
+              // B: 32 bytes further along the K-major 128-byte rows.
+              const uint64_t ad =
+                  smem_desc_sw128(s_addr + b * kSubBytes + kk * 2048u, kChunkBytes, 1024u);
+              const uint64_t bd = smem_desc_sw128(b_addr + kk * 32u, 16u, 1024u);
+              mma_bf16(d_tmem, ad, bd, idesc, (tt != t || kk != 0) ? 1u : 0u);
+            }
           }
           mma_commit(&empty[stage]);
           if (++stage == C::kStages) {
@@ -222,28 +253,34 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     const int row = quarter * 32 + lane;   // tile row: 0..63 gate, 64..127 up
     const int gu = row >> 6, j = row & 63;
     const int et = threadIdx.x - 64;       // 0..127
-    const int64_t Mrow = (int64_t)a.M * kCB;
+    const int64_t Mrow = (int64_t)a.M * kCB;     // floats of one [M][64] partial block
+    constexpr int kGroupCols = NB * kCB;
     int acc = 0;
     uint32_t acc_phase = 0;
     int64_t t = u0;
     while (t < u1) {
-      const int64_t cb = t / a.n_kb;
-      const int64_t seg_end = min(u1, (cb + 1) * (int64_t)a.n_kb);
+      const int64_t cg = t / a.n_kb;
+      const int64_t seg_end = min(u1, (cg + 1) * (int64_t)a.n_kb);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, a.status, a.timeout_ns)) break;
       tc_fence_after();
-      const int64_t c_lo = cta_of(cb * a.n_kb, U, G);
-      const int64_t c_hi = cta_of((cb + 1) * a.n_kb - 1, U, G);
+      const int64_t c_lo = cta_of(cg * a.n_kb, U, G);
+      const int64_t c_hi = cta_of((cg + 1) * a.n_kb - 1, U, G);
       const int n_contrib = (int)(c_hi - c_lo + 1);
-      float* slot = a.part + ((cb * a.maxq + (c - c_lo)) * 2 + gu) * Mrow;
+      float* slot = a.part + (cg * a.maxq + (c - c_lo)) * NB * 2 * Mrow;
 #pragma unroll
-      for (int ch = 0; ch < N / 16; ++ch) {
-        uint32_t r[16];
-        tmem_ld_x16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N + ch * 16), r);
-        tmem_wait_ld();
+      for (int b = 0; b < NB; ++b) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int m = ch * 16 + i;
-          if (m < a.M) slot[(int64_t)m * kCB + j] = __uint_as_float(r[i]);
+        for (int ch = 0; ch < N / 16; ++ch) {
+          uint32_t r[16];
+          tmem_ld_x16(tmem + ((uint32_t)(quarter * 32) << 16) +
+                          (uint32_t)(acc * C::kAccCols + b * N + ch * 16), r);
+          tmem_wait_ld();
+          float* sb = slot + (int64_t)(b * 2 + gu) * Mrow;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int m = ch * 16 + i;
+            if (m < a.M) sb[(int64_t)m * kCB + j] = __uint_as_float(r[i]);
+          }
         }
       }
       tc_fence_before();
@@ -252,31 +289,59 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         acc = 0;
         acc_phase ^= 1u;
       }
-      // The CTA that completes column block cb last reduces it.
+      // The CTA that completes column group cg last reduces it.
       __syncwarp();
       named_bar_sync(1, kEpiThreads);
       if (et == 0) {
         __threadfence();
-        *ticket = (int)atomicAdd(&a.counters[cb], 1u);
+        *ticket = (int)atomicAdd(&a.counters[cg], 1u);
       }
       __syncwarp();
       named_bar_sync(1, kEpiThreads);
-      if (*ticket == n_contrib - 1) {
+      const int tk = *ticket;
+      if (tk == n_contrib - 1) {
         __threadfence();
-        const int jj = et & 63, mh = et >> 6;
-        const int64_t col = cb * kCB + jj;
-        if (col < a.d_ff) {
-          const float* pb = a.part + cb * a.maxq * 2 * Mrow + jj;
-          for (int m = mh; m < a.M; m += 2) {
-            float g = 0.f, u = 0.f;
-            for (int q = 0; q < n_contrib; ++q) {
-              g += __ldcg(pb + (int64_t)(2 * q) * Mrow + (int64_t)m * kCB);
-              u += __ldcg(pb + (int64_t)(2 * q + 1) * Mrow + (int64_t)m * kCB);
+        const float* pg = a.part + cg * a.maxq * NB * 2 * Mrow;
+        const int64_t total = (int64_t)a.M * kGroupCols;
+        constexpr int kBatch = 4;   // outputs per thread in flight
+        for (int64_t base = et; base < total; base += kBatch * kEpiThreads) {
+          float g[kBatch], u[kBatch];
+          const float* pp[kBatch];
+#pragma unroll
+          for (int i = 0; i < kBatch; ++i) {
+            g[i] = u[i] = 0.f;
+            const int64_t idx = base + (int64_t)i * kEpiThreads;
+            const int64_t id = idx < total ? idx : 0;
+            const int m = (int)(id / kGroupCols), cc = (int)(id - (int64_t)m * kGroupCols);
+            const int b = cc / kCB, jj = cc - b * kCB;
+            pp[i] = pg + (int64_t)b * 2 * Mrow + (int64_t)m * kCB + jj;
+          }
+          // slot q holds CTA (c_lo + q)'s sums; adding in q order is k order
+          for (int q = 0; q < n_contrib; ++q) {
+            const int64_t qoff = (int64_t)q * NB * 2 * Mrow;
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+              g[i] += __ldcg(pp[i] + qoff);
+              u[i] += __ldcg(pp[i] + qoff + Mrow);
             }
-            a.h[(int64_t)m * a.d_ff + col] = (uint16_t)f32_to_bf16_bits(silu_fast(g) * u);
+          }
+#pragma unroll
+          for (int i = 0; i < kBatch; ++i) {
+            const int64_t idx = base + (int64_t)i * kEpiThreads;
+            if (idx >= total) continue;
+            const int m = (int)(idx / kGroupCols), cc = (int)(idx - (int64_t)m * kGroupCols);
+            const int64_t col = cg * kGroupCols + cc;
+            if (col < a.d_ff)
+              a.h[(int64_t)m * a.d_ff + col] = (uint16_t)f32_to_bf16_bits(silu_fast(g[i]) * u[i]);
           }
         }
-        if (et == 0) a.counters[cb] = 0u;
+        if (et == 0) a.counters[cg] = 0u;   // ready for the next call
+      } else if (tk >= n_contrib) {
+        // the counter did not start at zero: report it and leave it clean
+        if (et == 0) {
+          atomicOr(a.status, kStatusStaleCounter);
+          a.counters[cg] = 0u;
+        }
       }
       t = seg_end;
     }
@@ -291,11 +356,11 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
   }
 }
 
-template <int N>
+template <int N, int NB>
 cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mu,
                      const SkArgs& a, cudaStream_t st) {
-  using C = SkCfg<N>;
-  auto kern = skinny_tc_kernel<N>;
+  using C = SkCfg<N, NB>;
+  auto kern = skinny_tc_kernel<N, NB>;
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -306,12 +371,35 @@ cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mg, const CUtenso
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = 1;
   }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, mx, mg, mu, a);
+}
+
+template <int N>
+cudaError_t launch_nb(int nb, const CUtensorMap& mx, const CUtensorMap& mg,
+                      const CUtensorMap& mu, const SkArgs& a, cudaStream_t st) {
+  if constexpr (N <= 64) {
+    if (nb == 4) return launch_n<N, 4>(mx, mg, mu, a, st);
+  }
+  if constexpr (N <= 128) {
+    if (nb == 2) return launch_n<N, 2>(mx, mg, mu, a, st);
+  }
+  if (nb == 1) return launch_n<N, 1>(mx, mg, mu, a, st);
+  return cudaErrorInvalidValue;
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  return v ? atoi(v) : dflt;
 }
 
 }  // namespace
@@ -321,7 +409,14 @@ SkinnyPlan plan_skinny(int64_t M, int64_t d, int64_t d_ff, int num_sms) {
   int n = 16;
   while (n < M) n *= 2;
   p.n_pad = n;
-  p.n_cb = (d_ff + kCB - 1) / kCB;
+  int nb = env_int("SWIGLU_SK_NB", 2);
+  if (nb != 1 && nb != 2 && nb != 4) nb = 2;
+  while (nb > 1 && nb * n > 256) nb /= 2;
+  p.nb = nb;
+  p.l2_promo = env_int("SWIGLU_SK_PROMO", 128);
+  p.hint = env_int("SWIGLU_SK_HINT", 1);
+  const int64_t cb = (d_ff + kCB - 1) / kCB;
+  p.n_cb = (cb + nb - 1) / nb;
   p.n_kb = (d + kBK - 1) / kBK;
   p.units = p.n_cb * p.n_kb;
   p.grid = (int)(p.units < num_sms ? p.units : num_sms);
@@ -329,24 +424,31 @@ SkinnyPlan plan_skinny(int64_t M, int64_t d, int64_t d_ff, int num_sms) {
   const int64_t per = p.units > 0 ? p.units / p.grid : 1;   // fewest units a CTA gets
   p.maxq = (int)((p.n_kb + per - 1) / (per > 0 ? per : 1) + 1);
   p.counters_bytes = ((size_t)p.n_cb * sizeof(unsigned) + 255) / 256 * 256;
-  p.part_bytes = (size_t)p.n_cb * p.maxq * 2 * (size_t)M * kCB * sizeof(float);
+  p.part_bytes = (size_t)p.n_cb * p.maxq * nb * 2 * (size_t)M * kCB * sizeof(float);
   p.part_bytes = (p.part_bytes + 255) / 256 * 256;
   return p;
 }
 
 cudaError_t launch_skinny_tc(const void* x, const void* wg, const void* wu, void* h, int64_t M,
                              int64_t d, int64_t d_ff, const SkinnyPlan& p, void* workspace,
-                             unsigned* status, uint64_t timeout_ns, cudaStream_t st) {
+                             unsigned* clean_counters, unsigned* status, uint64_t timeout_ns,
+                             cudaStream_t st) {
   if (p.units == 0 || M == 0) return cudaSuccess;
   CUtensorMap mx, mg, mu;
   cudaError_t e;
   if ((e = make_tmap_bf16_2d(&mx, x, M, d, kBK, p.n_pad)) != cudaSuccess) return e;
-  if ((e = make_tmap_bf16_2d(&mg, wg, d, d_ff, kCB, kBK)) != cudaSuccess) return e;
-  if ((e = make_tmap_bf16_2d(&mu, wu, d, d_ff, kCB, kBK)) != cudaSuccess) return e;
-  unsigned* counters = (unsigned*)workspace;
+  if ((e = make_tmap_bf16_2d(&mg, wg, d, d_ff, kCB, kBK, p.l2_promo)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_2d(&mu, wu, d, d_ff, kCB, kBK, p.l2_promo)) != cudaSuccess) return e;
+  // Arrival counters must be zero on entry.  Counters that the previous call
+  // on this stream left at zero are used as they are; otherwise the
+  // workspace's counter area is cleared first.
+  unsigned* counters = clean_counters;
   float* part = (float*)((char*)workspace + p.counters_bytes);
-  if ((e = cudaMemsetAsync(counters, 0, (size_t)p.n_cb * sizeof(unsigned), st)) != cudaSuccess)
-    return e;
+  if (!counters) {
+    counters = (unsigned*)workspace;
+    if ((e = cudaMemsetAsync(counters, 0, (size_t)p.n_cb * sizeof(unsigned), st)) != cudaSuccess)
+      return e;
+  }
   SkArgs a;
   a.M = (int)M;
   a.d_ff = (int)d_ff;
@@ -354,17 +456,18 @@ cudaError_t launch_skinny_tc(const void* x, const void* wg, const void* wu, void
   a.maxq = p.maxq;
   a.units = p.units;
   a.grid = p.grid;
+  a.hint = p.hint;
   a.part = part;
   a.counters = counters;
   a.h = (uint16_t*)h;
   a.status = status;
   a.timeout_ns = timeout_ns;
   switch (p.n_pad) {
-    case 16: return launch_n<16>(mx, mg, mu, a, st);
-    case 32: return launch_n<32>(mx, mg, mu, a, st);
-    case 64: return launch_n<64>(mx, mg, mu, a, st);
-    case 128: return launch_n<128>(mx, mg, mu, a, st);
-    case 256: return launch_n<256>(mx, mg, mu, a, st);
+    case 16: return launch_nb<16>(p.nb, mx, mg, mu, a, st);
+    case 32: return launch_nb<32>(p.nb, mx, mg, mu, a, st);
+    case 64: return launch_nb<64>(p.nb, mx, mg, mu, a, st);
+    case 128: return launch_nb<128>(p.nb, mx, mg, mu, a, st);
+    case 256: return launch_nb<256>(p.nb, mx, mg, mu, a, st);
     default: return cudaErrorInvalidValue;
   }
 }

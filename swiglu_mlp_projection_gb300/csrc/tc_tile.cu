@@ -101,6 +101,10 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The set-up above overlaps the previous kernel's tail; x and h are touched
+  // only after it has finished.
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -289,11 +293,16 @@ cudaError_t launch_tile_tc(const void* x, const void* wg, const void* wu, void* 
   a.tiles = p.tiles;
   a.status = status;
   a.timeout_ns = timeout_ns;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, tile_tc_kernel, mx, mg, mu, mh, a);
 }
 

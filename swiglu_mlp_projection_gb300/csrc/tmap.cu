@@ -29,9 +29,10 @@ void init_encode() {
 
 // 2-D bf16 row-major tensor [rows, cols] (cols contiguous) with a box of
 // box_cols x box_rows elements and 128-byte swizzle; out-of-range elements
-// read as zero.  box_cols * 2 must be <= 128.
+// read as zero.  box_cols * 2 must be <= 128.  `l2_promo_bytes` (0, 64, 128
+// or 256) is the L2 fill granularity the copies may promote to.
 cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
-                              int box_cols, int box_rows) {
+                              int box_cols, int box_rows, int l2_promo_bytes) {
   std::call_once(g_once, init_encode);
   if (!g_encode) return g_init_err != cudaSuccess ? g_init_err : cudaErrorSymbolNotFound;
   // A tensor map needs every extent >= 1; callers never ask for empty maps.
@@ -39,9 +40,14 @@ cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, 
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
   cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t elem_strides[2] = {1, 1};
+  const CUtensorMapL2promotion promo =
+      l2_promo_bytes >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+      : l2_promo_bytes >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+      : l2_promo_bytes >= 64 ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B
+                             : CU_TENSOR_MAP_L2_PROMOTION_NONE;
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                         strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_SWIZZLE_128B, promo,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
