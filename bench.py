@@ -50,6 +50,29 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def profiled_traffic():
+    """Mean DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, or None when the kernel sources changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "skinny_tc_kernel_decode_sweep_d4096.md")
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if " = " in line and not line.startswith(("#", "|", " ")):
+                    k, v = line.split(" = ", 1)
+                    fields[k.strip()] = v.strip()
+        h = hashlib.sha256()
+        for rel in fields["source_files"].split():
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != fields["source_sha256"]:
+            return None
+        return int(fields["traffic_bytes_per_launch_mean"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -68,41 +91,78 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    """Polls SM clock, max SM clock and clock-event reasons every ~10 ms
+    through NVML (read-only queries, via ctypes); falls back to nvidia-smi."""
 
-    def __init__(self, gpu_id):
-        self.samples = []
-        self.proc = None
-        self.gpu_id = gpu_id
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.samples = []          # (time, sm_mhz, max_mhz, reasons_bitmask)
+        self.stop_evt = threading.Event()
         self.thread = None
+        self.proc = None
+        self.source = None
+
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        if not self.uuid or lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) != 0:
+            if lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+                raise OSError("no NVML device handle")
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, get_reasons
 
     def start(self):
-        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-               "-lms", "200"]
-        if self.gpu_id:
-            cmd.insert(1, "--id=" + self.gpu_id)
+        try:
+            lib, h, get_reasons = self._nvml()
+            self.source = "nvml"
+        except (OSError, AttributeError):
+            return self._start_smi()
+        import ctypes
+
+        def run():
+            clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            while not self.stop_evt.is_set():
+                if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                        get_reasons(h, ctypes.byref(rs)) == 0:
+                    self.samples.append((time.time(), float(clk.value), float(mx.value), rs.value))
+                time.sleep(0.01)
+        self.thread = threading.Thread(target=run, daemon=True)
+        self.thread.start()
+
+    def _start_smi(self):
+        self.source = "nvidia-smi"
+        cmd = ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+               "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            cmd.insert(1, "--id=" + self.uuid)
         try:
             self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
                                          text=True)
         except OSError:
             self.proc = None
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+
+        def read():
+            for line in self.proc.stdout:
+                parts = [p.strip() for p in line.split(",")]
+                try:
+                    self.samples.append((time.time(), float(parts[0]), float(parts[1]),
+                                         int(parts[2], 16)))
+                except (ValueError, IndexError):
+                    continue
+        self.thread = threading.Thread(target=read, daemon=True)
         self.thread.start()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 7:
-                continue
-            try:
-                self.samples.append((time.time(), float(parts[0]), float(parts[1]), parts[3:7]))
-            except ValueError:
-                continue
-
     def stop(self):
+        self.stop_evt.set()
         if self.proc:
             self.proc.terminate()
             try:
@@ -112,15 +172,22 @@ class ClockSampler:
         if self.thread:
             self.thread.join(timeout=5)
 
-    def summary(self, t0, t1):
-        inside = [s for s in self.samples if t0 <= s[0] <= t1] or self.samples
+    def summary(self, t0, t1, settle0):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed"
+        if len(inside) < 3:
+            inside = [s for s in self.samples if settle0 <= s[0] <= t1]
+            window = "settle+timed"
         if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in inside for i, v in enumerate(s[3]) if v == "Active"})
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                    "source": self.source}
+        bits = 0
+        for s in inside:
+            bits |= s[3]
+        reasons = sorted(n for b, n in self.REASONS.items() if bits & b)
         return {"sm_mhz": statistics.median(s[1] for s in inside),
                 "sm_max_mhz": max(s[2] for s in inside), "reasons": reasons,
-                "samples": len(inside)}
+                "samples": len(inside), "window": window, "source": self.source}
 
 
 def gpu_uuid(dev):
@@ -224,8 +291,8 @@ def run_ours(args):
     num_sms = props.multi_processor_count
     l2 = getattr(props, "L2_cache_size", L2_BYTES) or L2_BYTES
 
-    # weights: enough distinct copies that consecutive calls never find the
-    # previous call's weights in L2 (every copy is larger than L2 already)
+    # weights: enough distinct copies that no call finds the previous call's
+    # weights in L2 (each copy, 235 MB, is already larger than L2)
     w_bytes = 2 * D * D_FF * 2
     n_copies = max(2, math.ceil(3 * l2 / w_bytes))
     _, wg, wu = inputs.make_inputs(1, D, D_FF, "bf16", seed=0)
@@ -235,16 +302,19 @@ def run_ours(args):
     hs = {M: torch.empty(M, D_FF, dtype=torch.bfloat16, device=dev) for M in SWEEP}
     stream = torch.cuda.current_stream(dev)
     step_bytes = sum(workload.algorithmic_bytes(M, D, D_FF, "bf16") for M in SWEEP)
-    launches_per_step = sum(swg.plan(M, D, D_FF, "bf16", "auto", num_sms)["launches"] for M in SWEEP)
-    paths = {M: swg.plan(M, D, D_FF, "bf16", "auto", num_sms)["path"] for M in SWEEP}
+    plans = {M: swg.plan(M, D, D_FF, "bf16", "auto", num_sms) for M in SWEEP}
+    launches_per_step = sum(p["launches"] for p in plans.values())
 
     counter = [0]
 
+    def call(M):
+        wgc, wuc = copies[counter[0] % n_copies]
+        counter[0] += 1
+        swg.swiglu_up(xs[M], wgc, wuc, out=hs[M], stream=stream)
+
     def step():
         for M in SWEEP:
-            wgc, wuc = copies[counter[0] % n_copies]
-            counter[0] += 1
-            swg.swiglu_up(xs[M], wgc, wuc, out=hs[M], stream=stream)
+            call(M)
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -259,39 +329,27 @@ def run_ours(args):
         step()
     # keep the GPU busy ~1 s before timing so clock samples reflect load
     torch.cuda.synchronize(dev)
-    t_settle = time.time()
+    settle0 = time.time()
     settle_steps = 0
-    while time.time() - t_settle < 1.0:
+    while time.time() - settle0 < 1.0:
         for _ in range(20):
             step()
         settle_steps += 20
         torch.cuda.synchronize(dev)
 
-    # ---- timed region: K steps, per-call events on the launching stream
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(SWEEP) * args.steps)]
+    # ---- timed region: K steps back to back; events only at its ends.  It
+    # holds only launches of the kernel the sweep dispatches to, so its time
+    # per launch is that kernel's average launch duration.
     start_ev, end_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     wall0 = time.time()
     start_ev.record(stream)
-    i = 0
     for _ in range(args.steps):
-        for M in SWEEP:
-            wgc, wuc = copies[counter[0] % n_copies]
-            counter[0] += 1
-            ev[i].record(stream)
-            swg.swiglu_up(xs[M], wgc, wuc, out=hs[M], stream=stream)
-            ev[i + 1].record(stream)
-            i += 2
+        step()
     end_ev.record(stream)
     barrier()
     wall1 = time.time()
     total_ms = start_ev.elapsed_time(end_ev)
-    per_call_ms = {M: [] for M in SWEEP}
-    i = 0
-    for _ in range(args.steps):
-        for M in SWEEP:
-            per_call_ms[M].append(ev[i].elapsed_time(ev[i + 1]))
-            i += 2
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([total_ms], device=dev)
@@ -299,8 +357,9 @@ def run_ours(args):
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
-    kernel_ms = sum(sum(v) for v in per_call_ms.values())
-    achieved = step_bytes * args.steps / (kernel_ms * 1e-3) / 1e9
+    achieved = step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    avg_launch_us = 1e3 * total_ms / (args.steps * launches_per_step)
+    clocks = sampler.summary(wall0, wall1, settle0)
 
     # ---- end to end through the public API with pinned host buffers
     xs_pin = {M: xs_host[M].pin_memory() for M in SWEEP}
@@ -310,10 +369,8 @@ def run_ours(args):
 
     def e2e_step():
         for M in SWEEP:
-            wgc, wuc = copies[counter[0] % n_copies]
-            counter[0] += 1
             xs[M].copy_(xs_pin[M], non_blocking=True)
-            swg.swiglu_up(xs[M], wgc, wuc, out=hs[M], stream=stream)
+            call(M)
             hs_pin[M].copy_(hs[M], non_blocking=True)
 
     for _ in range(3):
@@ -333,15 +390,33 @@ def run_ours(args):
         e2e_ms = float(t.item())
     e2e_value = world * step_bytes * args.steps / (e2e_ms * 1e-3) / 1e9
     sampler.stop()
-    clocks = sampler.summary(wall0, wall1)
 
+    # ---- per-M breakdown (diagnostic, outside the timed region): each M
+    # back to back, and the latency of one isolated call
     sweep = {}
     for M in SWEEP:
-        ms = statistics.median(per_call_ms[M])
         b = workload.algorithmic_bytes(M, D, D_FF, "bf16")
+        reps = 60
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(reps):
+            call(M)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = a0.elapsed_time(a1) / reps
+        lat = []
+        for _ in range(20):
+            l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            l0.record(stream)
+            call(M)
+            l1.record(stream)
+            torch.cuda.synchronize(dev)
+            lat.append(l0.elapsed_time(l1))
         sweep[str(M)] = {"us": round(ms * 1e3, 2), "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
                          "frac": round(b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                         "path": paths[M]}
+                         "isolated_call_us": round(statistics.median(lat) * 1e3, 2),
+                         "path": plans[M]["path"]}
 
     extra = None
     if not args.no_extra:
@@ -349,6 +424,7 @@ def run_ours(args):
 
     if rank == 0:
         cpu = cpu_baseline()
+        kernels = sorted(set(p["path"] for p in plans.values()))
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -358,12 +434,19 @@ def run_ours(args):
                        "l2": "inputs larger than L2 (235 MB of weights per call) and %d weight "
                              "copies rotated per call" % n_copies,
                        "clock_settle_steps": settle_steps},
-            "roofline": {"bound": "hbm", "kernel": "swiglu_up call (%s)" % "+".join(
-                             sorted(set(paths.values()))),
+            "roofline": {"bound": "hbm",
+                         "kernel": "skinny_tc_kernel" if kernels == ["skinny"] else "+".join(kernels),
                          "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                         "peak_source": peaks["source"] + " (hbm_gbs, copy)",
-                         "timing": "CUDA events around each call on its stream"},
+                         "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "traffic": profiled_traffic() if kernels == ["skinny"] else None,
+                         "traffic_source": "profiles/skinny_tc_kernel_decode_sweep_d4096.md "
+                                           "(mean of the 5 sweep launches; null if the kernel "
+                                           "changed since)",
+                         "algorithmic_bytes_per_launch": step_bytes // launches_per_step,
+                         "avg_launch_us": round(avg_launch_us, 2),
+                         "peak_source": peaks["source"] + " hbm_gbs (copy, burst)",
+                         "timing": "CUDA events on the launching stream around the timed region, "
+                                   "which holds only this kernel's launches"},
             "sweep": sweep,
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
@@ -384,7 +467,9 @@ def run_ours(args):
 
 
 def other_configs(dev, peaks, l2, iters):
-    """Secondary measurements of the other workloads (not the headline)."""
+    """Secondary measurements of the other workloads (not the headline):
+    `iters` calls back to back after 3 warm-up calls, weight copies rotated so
+    that the weights read by each call are not in L2."""
     import torch
     import swiglu_mlp_projection_gb300 as swg
     from swiglu_mlp_projection_gb300 import inputs, workload
@@ -394,7 +479,7 @@ def other_configs(dev, peaks, l2, iters):
             continue
         _, wg, wu = inputs.make_inputs(1, cfg.d, cfg.d_ff, cfg.dtype, seed=0)
         w_bytes = 2 * wg.numel() * wg.element_size()
-        n_copies = max(1, math.ceil(3 * l2 / w_bytes)) if w_bytes < 3 * l2 else 1
+        n_copies = max(2, math.ceil(3 * l2 / w_bytes))
         copies = [(wg.to(dev), wu.to(dev)) for _ in range(n_copies)]
         del wg, wu
         for M in cfg.Ms:
@@ -409,14 +494,13 @@ def other_configs(dev, peaks, l2, iters):
             for _ in range(3):
                 call()
             torch.cuda.synchronize(dev)
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(iters)]
-            for a, b in evs:
-                a.record()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(iters):
                 call()
-                b.record()
+            e1.record()
             torch.cuda.synchronize(dev)
-            ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+            ms = e0.elapsed_time(e1) / iters
             by = workload.algorithmic_bytes(M, cfg.d, cfg.d_ff, cfg.dtype)
             fl = workload.flops(M, cfg.d, cfg.d_ff)
             gbs = by / (ms * 1e-3) / 1e9

@@ -172,6 +172,14 @@ SWIGLU_API int64_t swiglu_split_k_slices(int64_t K, int64_t col_blocks,
  * Returns SWIGLU_OK, SWIGLU_ERR_TIMEOUT or SWIGLU_ERR_CUDA. */
 SWIGLU_API int swiglu_check_device_status(void);
 
+/* Self-test of failure detection: launches one CTA that waits, through the
+ * same bounded wait the tensor-core kernels use, on a barrier that nothing
+ * ever completes.  After `timeout_ms` (1..10000) the wait gives up, raises
+ * the device error word and the kernel returns normally, so the next
+ * swiglu_check_device_status() reports SWIGLU_ERR_TIMEOUT and the CUDA
+ * context stays usable.  No counterpart in the pages. */
+SWIGLU_API int swiglu_selftest_wait_timeout(int timeout_ms, void* stream);
+
 /* Text for a swiglu_status value (static storage). */
 SWIGLU_API const char* swiglu_status_string(int status);
 

@@ -33,21 +33,34 @@ def _path_code(path):
         raise ValueError("path must be one of %s" % sorted(PATHS)) from None
 
 
+_LIB = None
+
+
+def _raw_stream(index):
+    """torch's current stream on device `index`, as a raw cudaStream_t value."""
+    import torch
+    get = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if get is not None:
+        return get(index)
+    return torch.cuda.current_stream(index).cuda_stream
+
+
 def swiglu_up(x, w_gate, w_up, out=None, path="auto", workspace=None, stream=None):
-    """h = silu(x @ w_gate) * (x @ w_up) on the current CUDA device.
+    """h = silu(x @ w_gate) * (x @ w_up) on x's CUDA device.
 
     x [M, d], w_gate / w_up [d, d_ff]: contiguous CUDA tensors of one dtype
     (bfloat16 or float32).  ``out`` [M, d_ff] is written if given (else
     allocated).  ``path`` forces a kernel path ("simt", "skinny", "tc");
     ``workspace`` is an optional uint8 CUDA tensor for split-K partial sums.
-    The call is asynchronous on ``stream`` (default: torch's current stream).
+    The call is asynchronous on ``stream`` (a torch.cuda.Stream; default:
+    torch's current stream on x's device).
     """
+    global _LIB
     import torch
-    for name, t in (("x", x), ("w_gate", w_gate), ("w_up", w_up)):
-        if not t.is_cuda:
-            raise ValueError("%s must be a CUDA tensor" % name)
-        if not t.is_contiguous():
-            raise ValueError("%s must be contiguous" % name)
+    if not (x.is_cuda and w_gate.is_cuda and w_up.is_cuda):
+        raise ValueError("x, w_gate and w_up must be CUDA tensors")
+    if not (x.is_contiguous() and w_gate.is_contiguous() and w_up.is_contiguous()):
+        raise ValueError("x, w_gate and w_up must be contiguous")
     if x.dim() != 2 or w_gate.dim() != 2 or w_up.shape != w_gate.shape:
         raise ValueError("expected x [M, d] and w_gate, w_up [d, d_ff]")
     M, d = x.shape
@@ -61,17 +74,22 @@ def swiglu_up(x, w_gate, w_up, out=None, path="auto", workspace=None, stream=Non
         out = torch.empty((M, d_ff), dtype=x.dtype, device=x.device)
     elif out.shape != (M, d_ff) or out.dtype != x.dtype or not out.is_contiguous():
         raise ValueError("out must be a contiguous [M, d_ff] tensor of x's dtype")
-    if stream is None:
-        stream = torch.cuda.current_stream(x.device)
+    index = x.device.index
+    st = stream.cuda_stream if stream is not None else _raw_stream(index)
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    lib = _lib.load()
-    with torch.cuda.device(x.device):
-        st = lib.swiglu_up_ex(x.data_ptr(), w_gate.data_ptr(), w_up.data_ptr(), out.data_ptr(),
-                              M, d, d_ff, dt, _path_code(path), ws_ptr, ws_bytes,
-                              stream.cuda_stream)
-    _lib.check(st)
+    if _LIB is None:
+        _LIB = _lib.load()
+    args = (x.data_ptr(), w_gate.data_ptr(), w_up.data_ptr(), out.data_ptr(), M, d, d_ff, dt,
+            _path_code(path), ws_ptr, ws_bytes, st)
+    if torch.cuda.current_device() != index:
+        with torch.cuda.device(index):
+            status = _LIB.swiglu_up_ex(*args)
+    else:
+        status = _LIB.swiglu_up_ex(*args)
+    if status:
+        _lib.check(status)
     return out
 
 

@@ -40,6 +40,7 @@ SIGNATURES = {
     "swiglu_plan": ([_i64, _i64, _i64, _int, _int, _int, ctypes.POINTER(PlanInfo)], _int),
     "swiglu_split_k_slices": ([_i64, _i64, _i64, _i64], _i64),
     "swiglu_check_device_status": ([], _int),
+    "swiglu_selftest_wait_timeout": ([_int, _vp], _int),
     "swiglu_status_string": ([_int], ctypes.c_char_p),
     "swiglu_last_error_string": ([], ctypes.c_char_p),
     "swiglu_version": ([], _int),

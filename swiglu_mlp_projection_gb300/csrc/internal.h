@@ -43,6 +43,7 @@ int api_current_device(int* dev, int* num_sms);
 int api_fail(int status, const char* detail);
 int api_cuda_fail(cudaError_t e, const char* what);
 void api_clear_error();
+unsigned* api_status_word(int dev);   // device address of the error word
 constexpr int64_t kSimtMaxGridYZ = 65535;
 
 // TMA descriptor of a row-major bf16 matrix [rows, cols], 128-byte swizzle.
@@ -65,12 +66,12 @@ struct SkinnyPlan {
 };
 constexpr int kSkinnyMaxN = 256;
 SkinnyPlan plan_skinny(int64_t M, int64_t d, int64_t d_ff, int num_sms);
-// `clean_counters`: n_cb arrival counters known to be zero (left so by the
-// previous call on the same stream), or null to clear the workspace's own.
+// `counters`: n_cb arrival counters, zero on entry when `counters_clean`
+// (left so by the previous call on the same stream), else cleared first.
 cudaError_t launch_skinny_tc(const void* x, const void* wg, const void* wu, void* h, int64_t M,
-                             int64_t d, int64_t d_ff, const SkinnyPlan& p, void* workspace,
-                             unsigned* clean_counters, unsigned* status, uint64_t timeout_ns,
-                             cudaStream_t st);
+                             int64_t d, int64_t d_ff, const SkinnyPlan& p, float* part,
+                             unsigned* counters, bool counters_clean, unsigned* status,
+                             uint64_t timeout_ns, cudaStream_t st);
 constexpr size_t kStreamCounterBytes = 64 * 1024;   // per-stream arrival counters
 
 // Tile tensor-core path (bf16, large M): 128 x (128 gate + 128 up) output

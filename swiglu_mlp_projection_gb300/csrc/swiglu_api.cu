@@ -102,30 +102,38 @@ int device_pool(int dev, cudaMemPool_t* pool) {
   return SWIGLU_OK;
 }
 
-// Arrival counters of the skinny kernel, kept per stream.  The kernel leaves
-// every counter it used at zero, so the next call on the same stream (ordered
-// after it) can use them without clearing them first.  Streams are told apart
-// by cudaStreamGetId, which is never reused within a process.  Counters of a
-// call that gave up may be left non-zero: swiglu_check_device_status marks the
-// device's counters dirty and the next call clears them.
-struct StreamCounters {
+// Library-owned workspace, kept per stream.  Layout: kStreamCounterBytes of
+// arrival counters for the skinny kernel, then the partial sums of either
+// split-K path.  Calls on one stream run in stream order, so they can share
+// the buffer; the skinny kernel leaves every counter it used at zero, so the
+// next call needs no clearing.  Streams are told apart by cudaStreamGetId,
+// which is never reused within a process.  Counters of a call that gave up
+// may be left non-zero: swiglu_check_device_status marks the device's
+// buffers dirty and the next call clears their counters.  The buffer grows
+// (stream-ordered free of the old one) when a call needs more.
+struct StreamWorkspace {
   int dev;
   unsigned long long stream_id;
-  unsigned* counters;
+  char* base;
+  size_t part_capacity;
   bool dirty;
 };
 constexpr size_t kMaxStreamSlots = 256;
-std::vector<StreamCounters> g_stream_counters;   // guarded by g_mu
+constexpr size_t kMaxCachedPartBytes = (size_t)256 << 20;
+std::vector<StreamWorkspace> g_stream_ws;   // guarded by g_mu
 
 int device_pool(int dev, cudaMemPool_t* pool);
 
-// Zeroed counters for `st`, or *out = null when the call must clear the
-// workspace's own counters (the per-thread default stream, whose handle is
-// shared by threads that are not ordered with each other; too many streams;
-// or more counters than a slot holds).
-int stream_counters(int dev, cudaStream_t st, size_t need_bytes, unsigned** out) {
-  *out = nullptr;
-  if (st == cudaStreamPerThread || need_bytes > kStreamCounterBytes) return SWIGLU_OK;
+// On success, either *part (and *counters, already zero) point into the
+// stream's buffer, or both are null and the call must bring its own
+// workspace: the per-thread default stream (its handle is shared by threads
+// that are not ordered with each other), a stream without an id, too many
+// streams, or a very large request.
+int stream_workspace(int dev, cudaStream_t st, size_t part_bytes, float** part,
+                     unsigned** counters) {
+  *part = nullptr;
+  *counters = nullptr;
+  if (st == cudaStreamPerThread || part_bytes > kMaxCachedPartBytes) return SWIGLU_OK;
   unsigned long long id = 0;
   if (cudaStreamGetId(st, &id) != cudaSuccess) {
     cudaGetLastError();
@@ -135,35 +143,41 @@ int stream_counters(int dev, cudaStream_t st, size_t need_bytes, unsigned** out)
   int v = device_pool(dev, &pool);
   if (v != SWIGLU_OK) return v;
   std::lock_guard<std::mutex> lk(g_mu);
-  for (auto& sc : g_stream_counters) {
-    if (sc.dev == dev && sc.stream_id == id) {
-      if (sc.dirty) {
-        cudaError_t e = cudaMemsetAsync(sc.counters, 0, kStreamCounterBytes, st);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
-        sc.dirty = false;
-      }
-      *out = sc.counters;
-      return SWIGLU_OK;
+  StreamWorkspace* sw = nullptr;
+  for (auto& e : g_stream_ws)
+    if (e.dev == dev && e.stream_id == id) sw = &e;
+  if (!sw) {
+    if (g_stream_ws.size() >= kMaxStreamSlots) return SWIGLU_OK;
+    g_stream_ws.push_back({dev, id, nullptr, 0, true});
+    sw = &g_stream_ws.back();
+  }
+  if (!sw->base || sw->part_capacity < part_bytes) {
+    const size_t cap = (part_bytes + ((size_t)1 << 20) - 1) & ~(((size_t)1 << 20) - 1);
+    void* p = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&p, kStreamCounterBytes + cap, pool, st);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return SWIGLU_OK;   // the call falls back to a per-call workspace
     }
+    if (sw->base) cudaFreeAsync(sw->base, st);
+    sw->base = (char*)p;
+    sw->part_capacity = cap;
+    sw->dirty = true;
   }
-  if (g_stream_counters.size() >= kMaxStreamSlots) return SWIGLU_OK;
-  void* p = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(&p, kStreamCounterBytes, pool, st);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return SWIGLU_OK;   // fall back to clearing the workspace's counters
+  if (sw->dirty) {
+    cudaError_t e = cudaMemsetAsync(sw->base, 0, kStreamCounterBytes, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
+    sw->dirty = false;
   }
-  e = cudaMemsetAsync(p, 0, kStreamCounterBytes, st);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
-  g_stream_counters.push_back({dev, id, (unsigned*)p, false});
-  *out = (unsigned*)p;
+  *counters = (unsigned*)sw->base;
+  *part = (float*)(sw->base + kStreamCounterBytes);
   return SWIGLU_OK;
 }
 
-void mark_counters_dirty(int dev) {
+void mark_workspaces_dirty(int dev) {
   std::lock_guard<std::mutex> lk(g_mu);
-  for (auto& sc : g_stream_counters)
-    if (sc.dev == dev) sc.dirty = true;
+  for (auto& e : g_stream_ws)
+    if (e.dev == dev) e.dirty = true;
 }
 
 int elem_bytes(int dtype) { return dtype == SWIGLU_BF16 ? 2 : 4; }
@@ -292,27 +306,42 @@ int run(const void* x, const void* wg, const void* wu, void* h, int64_t M, int64
   if (workspace && overlaps(h, (size_t)M * d_ff * elem_bytes(dtype), workspace, ws_bytes))
     return fail(SWIGLU_ERR_INVALID_ARG, "h overlaps the workspace");
 
-  float* part = (float*)workspace;
-  bool pooled = false;
+  // Where the partial sums (and the skinny kernel's counters) live:
+  //   caller workspace -> [counters][partials] inside it, counters cleared;
+  //   else the stream's cached buffer -> counters already zero;
+  //   else a per-call pool allocation -> counters cleared.
+  float* part = nullptr;
+  unsigned* counters = nullptr;
+  bool counters_clean = false;
+  void* pooled = nullptr;
+  const size_t counter_bytes = p.path == SWIGLU_PATH_SKINNY ? p.skinny.counters_bytes : 0;
   if (p.workspace > 0) {
     if (workspace) {
       if (ws_bytes < p.workspace || ((uintptr_t)workspace & 255u))
         return fail(SWIGLU_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)",
                     p.workspace, ws_bytes);
+      counters = (unsigned*)workspace;
+      part = (float*)((char*)workspace + counter_bytes);
     } else {
-      cudaMemPool_t pool;
-      if ((v = device_pool(dev, &pool)) != SWIGLU_OK) return v;
-      void* ptr = nullptr;
-      cudaError_t e = cudaMallocFromPoolAsync(&ptr, p.workspace, pool, st);
-      if (e != cudaSuccess) {
-        if (e == cudaErrorMemoryAllocation) {
-          cudaGetLastError();
-          return fail(SWIGLU_ERR_OOM, "workspace of %zu bytes: %s", p.workspace, cudaGetErrorString(e));
+      if ((v = stream_workspace(dev, st, p.workspace - counter_bytes, &part, &counters)) != SWIGLU_OK)
+        return v;
+      if (part) {
+        counters_clean = true;
+      } else {
+        cudaMemPool_t pool;
+        if ((v = device_pool(dev, &pool)) != SWIGLU_OK) return v;
+        cudaError_t e = cudaMallocFromPoolAsync(&pooled, p.workspace, pool, st);
+        if (e != cudaSuccess) {
+          if (e == cudaErrorMemoryAllocation) {
+            cudaGetLastError();
+            return fail(SWIGLU_ERR_OOM, "workspace of %zu bytes: %s", p.workspace,
+                        cudaGetErrorString(e));
+          }
+          return cuda_fail(e, "cudaMallocFromPoolAsync");
         }
-        return cuda_fail(e, "cudaMallocFromPoolAsync");
+        counters = (unsigned*)pooled;
+        part = (float*)((char*)pooled + counter_bytes);
       }
-      part = (float*)ptr;
-      pooled = true;
     }
   }
 
@@ -321,18 +350,13 @@ int run(const void* x, const void* wg, const void* wu, void* h, int64_t M, int64
     e = launch_simt_partial(x, wg, wu, part, M, d, d_ff, dtype, p.simt, st);
     if (e == cudaSuccess) e = launch_reduce_swiglu(part, h, M, d_ff, p.slices, dtype, di.num_sms, st);
   } else if (p.path == SWIGLU_PATH_SKINNY) {
-    unsigned* clean = nullptr;
-    if ((v = stream_counters(dev, st, (size_t)p.skinny.n_cb * sizeof(unsigned), &clean)) != SWIGLU_OK) {
-      if (pooled) cudaFreeAsync(part, st);
-      return v;
-    }
-    e = launch_skinny_tc(x, wg, wu, h, M, d, d_ff, p.skinny, part, clean, di.status,
-                         wait_timeout_ns(), st);
+    e = launch_skinny_tc(x, wg, wu, h, M, d, d_ff, p.skinny, part, counters, counters_clean,
+                         di.status, wait_timeout_ns(), st);
   } else {
     e = launch_tile_tc(x, wg, wu, h, M, d, d_ff, p.tile, di.status, wait_timeout_ns(), st);
   }
   if (pooled) {
-    cudaError_t ef = cudaFreeAsync(part, st);
+    cudaError_t ef = cudaFreeAsync(pooled, st);
     if (e == cudaSuccess) e = ef;
   }
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
@@ -370,6 +394,12 @@ int api_fail(int status, const char* detail) { return fail(status, "%s", detail)
 int api_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 
 void api_clear_error() { t_err[0] = 0; }
+
+unsigned* api_status_word(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_dev[dev].status;
+}
 
 }  // namespace swg
 
@@ -435,7 +465,7 @@ int swiglu_check_device_status(void) {
     e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
     int dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess) mark_counters_dirty(dev);
+    if (cudaGetDevice(&dev) == cudaSuccess) mark_workspaces_dirty(dev);
     return fail(SWIGLU_ERR_TIMEOUT,
                 "a device-side wait gave up or found a stale arrival counter (status word 0x%x)",
                 word);

@@ -302,34 +302,36 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
       if (tk == n_contrib - 1) {
         __threadfence();
         const float* pg = a.part + cg * a.maxq * NB * 2 * Mrow;
-        const int64_t total = (int64_t)a.M * kGroupCols;
-        constexpr int kBatch = 4;   // outputs per thread in flight
-        for (int64_t base = et; base < total; base += kBatch * kEpiThreads) {
+        const int total = a.M * kGroupCols;
+        constexpr int kBatch = 16;   // outputs per thread with their loads in flight together
+        for (int base = et; base < total; base += kBatch * kEpiThreads) {
           float g[kBatch], u[kBatch];
-          const float* pp[kBatch];
+          int off[kBatch];
 #pragma unroll
           for (int i = 0; i < kBatch; ++i) {
             g[i] = u[i] = 0.f;
-            const int64_t idx = base + (int64_t)i * kEpiThreads;
-            const int64_t id = idx < total ? idx : 0;
-            const int m = (int)(id / kGroupCols), cc = (int)(id - (int64_t)m * kGroupCols);
+            const int idx = base + i * kEpiThreads;
+            const int id = idx < total ? idx : 0;
+            const int m = id / kGroupCols, cc = id - m * kGroupCols;
             const int b = cc / kCB, jj = cc - b * kCB;
-            pp[i] = pg + (int64_t)b * 2 * Mrow + (int64_t)m * kCB + jj;
+            off[i] = b * 2 * (int)Mrow + m * kCB + jj;
           }
           // slot q holds CTA (c_lo + q)'s sums; adding in q order is k order
           for (int q = 0; q < n_contrib; ++q) {
-            const int64_t qoff = (int64_t)q * NB * 2 * Mrow;
+            const float* pq = pg + (int64_t)q * NB * 2 * Mrow;
 #pragma unroll
             for (int i = 0; i < kBatch; ++i) {
-              g[i] += __ldcg(pp[i] + qoff);
-              u[i] += __ldcg(pp[i] + qoff + Mrow);
+              if (base + i * kEpiThreads < total) {
+                g[i] += __ldcg(pq + off[i]);
+                u[i] += __ldcg(pq + off[i] + Mrow);
+              }
             }
           }
 #pragma unroll
           for (int i = 0; i < kBatch; ++i) {
-            const int64_t idx = base + (int64_t)i * kEpiThreads;
+            const int idx = base + i * kEpiThreads;
             if (idx >= total) continue;
-            const int m = (int)(idx / kGroupCols), cc = (int)(idx - (int64_t)m * kGroupCols);
+            const int m = idx / kGroupCols, cc = idx - m * kGroupCols;
             const int64_t col = cg * kGroupCols + cc;
             if (col < a.d_ff)
               a.h[(int64_t)m * a.d_ff + col] = (uint16_t)f32_to_bf16_bits(silu_fast(g[i]) * u[i]);
@@ -430,25 +432,19 @@ SkinnyPlan plan_skinny(int64_t M, int64_t d, int64_t d_ff, int num_sms) {
 }
 
 cudaError_t launch_skinny_tc(const void* x, const void* wg, const void* wu, void* h, int64_t M,
-                             int64_t d, int64_t d_ff, const SkinnyPlan& p, void* workspace,
-                             unsigned* clean_counters, unsigned* status, uint64_t timeout_ns,
-                             cudaStream_t st) {
+                             int64_t d, int64_t d_ff, const SkinnyPlan& p, float* part,
+                             unsigned* counters, bool counters_clean, unsigned* status,
+                             uint64_t timeout_ns, cudaStream_t st) {
   if (p.units == 0 || M == 0) return cudaSuccess;
   CUtensorMap mx, mg, mu;
   cudaError_t e;
   if ((e = make_tmap_bf16_2d(&mx, x, M, d, kBK, p.n_pad)) != cudaSuccess) return e;
   if ((e = make_tmap_bf16_2d(&mg, wg, d, d_ff, kCB, kBK, p.l2_promo)) != cudaSuccess) return e;
   if ((e = make_tmap_bf16_2d(&mu, wu, d, d_ff, kCB, kBK, p.l2_promo)) != cudaSuccess) return e;
-  // Arrival counters must be zero on entry.  Counters that the previous call
-  // on this stream left at zero are used as they are; otherwise the
-  // workspace's counter area is cleared first.
-  unsigned* counters = clean_counters;
-  float* part = (float*)((char*)workspace + p.counters_bytes);
-  if (!counters) {
-    counters = (unsigned*)workspace;
-    if ((e = cudaMemsetAsync(counters, 0, (size_t)p.n_cb * sizeof(unsigned), st)) != cudaSuccess)
-      return e;
-  }
+  // Arrival counters must be zero on entry.
+  if (!counters_clean &&
+      (e = cudaMemsetAsync(counters, 0, (size_t)p.n_cb * sizeof(unsigned), st)) != cudaSuccess)
+    return e;
   SkArgs a;
   a.M = (int)M;
   a.d_ff = (int)d_ff;
