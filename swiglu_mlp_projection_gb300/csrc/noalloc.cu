@@ -8,7 +8,7 @@
 #include <mutex>
 #include <stdio.h>
 
-#include "../../include/swiglu.h"
+#include "swiglu.h"
 #include "internal.h"
 
 // The scratch array.  Every GPU that loads this library holds it until the

@@ -1,5 +1,5 @@
 // Self-test of the bounded device-side waits used by the tensor-core kernels.
-#include "../../include/swiglu.h"
+#include "swiglu.h"
 #include "internal.h"
 #include "tc_common.cuh"
 

@@ -12,7 +12,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-#include "../../include/swiglu.h"
+#include "swiglu.h"
 #include "common.cuh"
 #include "internal.h"
 

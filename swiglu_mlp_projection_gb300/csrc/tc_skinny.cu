@@ -49,6 +49,8 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kChunkBytes = kCB * kBK * 2;       // one 64 x 64 bf16 weight box
 constexpr uint32_t kSubBytes = 2 * kChunkBytes;       // gate box + up box = one MMA A tile
+constexpr int kPrefetchUnits = 16;                    // units prefetched into L2 before the wait
+constexpr uint32_t kRingBudget = 200u * 1024u;        // shared memory for the stage ring
 
 constexpr uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
   uint32_t r = lo;
@@ -62,7 +64,7 @@ template <int N, int NB>
 struct SkCfg {
   static constexpr uint32_t kBTileBytes = (uint32_t)N * kBK * 2;
   static constexpr uint32_t kStageBytes = NB * kSubBytes + kBTileBytes;
-  static constexpr int kFit = (int)((200u * 1024u) / kStageBytes);
+  static constexpr int kFit = (int)(kRingBudget / kStageBytes);
   static constexpr int kStages = kFit > 12 ? 12 : kFit;
   static constexpr uint32_t kAccCols = (uint32_t)NB * N;          // one accumulator buffer
   static constexpr uint32_t kTmemCols = pow2_at_least(2 * kAccCols, 32);
@@ -140,8 +142,22 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // Everything above overlaps the previous kernel's tail; from here on the
-  // kernel reads x and the workspace, which that kernel may still be writing.
+  // Everything above overlaps the previous kernel's tail.  So does an L2
+  // prefetch of this CTA's first weight boxes: a prefetch only reads, and L2
+  // is where every later write lands, so it is safe before the wait.  From
+  // the wait on, the kernel reads x and the workspace, which the previous
+  // kernel may still be writing.
+  if (warp == 0 && lane == 0) {
+    const int64_t pend = min(u1, u0 + (int64_t)kPrefetchUnits);
+    for (int64_t t = u0; t < pend; ++t) {
+      const int cg = (int)(t / a.n_kb), kb = (int)(t - (int64_t)cg * a.n_kb);
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        tma_prefetch_l2_2d(&tm_wg, (cg * NB + b) * kCB, kb * kBK);
+        tma_prefetch_l2_2d(&tm_wu, (cg * NB + b) * kCB, kb * kBK);
+      }
+    }
+  }
   pdl_wait();
   pdl_launch_dependents();
 
@@ -301,29 +317,35 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
       const int tk = *ticket;
       if (tk == n_contrib - 1) {
         __threadfence();
+        // Each thread sums 4 adjacent columns of one row at a time: 16-byte
+        // loads, and the loads of several outputs in flight together.
         const float* pg = a.part + cg * a.maxq * NB * 2 * Mrow;
-        const int total = a.M * kGroupCols;
-        constexpr int kBatch = 16;   // outputs per thread with their loads in flight together
+        constexpr int kChunks = kGroupCols / 4;      // 4-column chunks per row of the group
+        const int total = a.M * kChunks;
+        constexpr int kBatch = 4;
         for (int base = et; base < total; base += kBatch * kEpiThreads) {
-          float g[kBatch], u[kBatch];
+          float4 g[kBatch], u[kBatch];
           int off[kBatch];
 #pragma unroll
           for (int i = 0; i < kBatch; ++i) {
-            g[i] = u[i] = 0.f;
+            g[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            u[i] = g[i];
             const int idx = base + i * kEpiThreads;
             const int id = idx < total ? idx : 0;
-            const int m = id / kGroupCols, cc = id - m * kGroupCols;
-            const int b = cc / kCB, jj = cc - b * kCB;
-            off[i] = b * 2 * (int)Mrow + m * kCB + jj;
+            const int m = id / kChunks, ch = id - m * kChunks;
+            off[i] = (ch >> 4) * 2 * (int)Mrow + m * kCB + (ch & 15) * 4;
           }
           // slot q holds CTA (c_lo + q)'s sums; adding in q order is k order
+#pragma unroll 2
           for (int q = 0; q < n_contrib; ++q) {
             const float* pq = pg + (int64_t)q * NB * 2 * Mrow;
 #pragma unroll
             for (int i = 0; i < kBatch; ++i) {
               if (base + i * kEpiThreads < total) {
-                g[i] += __ldcg(pq + off[i]);
-                u[i] += __ldcg(pq + off[i] + Mrow);
+                const float4 pgv = __ldcg(reinterpret_cast<const float4*>(pq + off[i]));
+                const float4 puv = __ldcg(reinterpret_cast<const float4*>(pq + off[i] + Mrow));
+                g[i].x += pgv.x; g[i].y += pgv.y; g[i].z += pgv.z; g[i].w += pgv.w;
+                u[i].x += puv.x; u[i].y += puv.y; u[i].z += puv.z; u[i].w += puv.w;
               }
             }
           }
@@ -331,10 +353,14 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
           for (int i = 0; i < kBatch; ++i) {
             const int idx = base + i * kEpiThreads;
             if (idx >= total) continue;
-            const int m = idx / kGroupCols, cc = idx - m * kGroupCols;
-            const int64_t col = cg * kGroupCols + cc;
-            if (col < a.d_ff)
-              a.h[(int64_t)m * a.d_ff + col] = (uint16_t)f32_to_bf16_bits(silu_fast(g[i]) * u[i]);
+            const int m = idx / kChunks, ch = idx - m * kChunks;
+            const int64_t col = cg * kGroupCols + ch * 4;
+            if (col < a.d_ff) {   // d_ff is a multiple of 8: a chunk is all in or all out
+              uint2 o;
+              o.x = pack_bf16x2(silu_fast(g[i].x) * u[i].x, silu_fast(g[i].y) * u[i].y);
+              o.y = pack_bf16x2(silu_fast(g[i].z) * u[i].z, silu_fast(g[i].w) * u[i].w);
+              *reinterpret_cast<uint2*>(a.h + (int64_t)m * a.d_ff + col) = o;
+            }
           }
         }
         if (et == 0) a.counters[cg] = 0u;   // ready for the next call
