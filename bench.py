@@ -45,6 +45,17 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(value, world, device=None):
+    """Largest `value` over all ranks (the slowest rank sets the job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -349,12 +360,7 @@ def run_ours(args):
     end_ev.record(stream)
     barrier()
     wall1 = time.time()
-    total_ms = start_ev.elapsed_time(end_ev)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(start_ev.elapsed_time(end_ev), world, dev)
     ms_per_step = total_ms / args.steps
     value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
     achieved = step_bytes * args.steps / (total_ms * 1e-3) / 1e9
@@ -382,12 +388,7 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e_value = world * step_bytes * args.steps / (e2e_ms * 1e-3) / 1e9
     sampler.stop()
 
