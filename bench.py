@@ -502,12 +502,28 @@ def other_configs(dev, peaks, l2, iters):
             e1.record()
             torch.cuda.synchronize(dev)
             ms = e0.elapsed_time(e1) / iters
+            # the same calls captured once into a CUDA graph and replayed:
+            # no host work per call
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(iters):
+                    call()
+            g.replay()
+            torch.cuda.synchronize(dev)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ms_graph = e0.elapsed_time(e1) / iters
+            del g
             by = workload.algorithmic_bytes(M, cfg.d, cfg.d_ff, cfg.dtype)
             fl = workload.flops(M, cfg.d, cfg.d_ff)
             gbs = by / (ms * 1e-3) / 1e9
             tfs = fl / (ms * 1e-3) / 1e12
             key = "%s/M=%d" % (cfg.name, M)
             entry = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "TFLOP/s": round(tfs, 2),
+                     "graph_us": round(ms_graph * 1e3, 2),
+                     "graph_GB/s": round(by / (ms_graph * 1e-3) / 1e9, 1),
                      "path": swg.plan(M, cfg.d, cfg.d_ff, cfg.dtype, "auto")["path"]}
             if M <= 16 or cfg.dtype == "f32":
                 entry["frac_hbm"] = round(gbs / peaks["hbm_gbs"], 4)

@@ -134,6 +134,15 @@ int stream_workspace(int dev, cudaStream_t st, size_t part_bytes, float** part,
   *part = nullptr;
   *counters = nullptr;
   if (st == cudaStreamPerThread || part_bytes > kMaxCachedPartBytes) return SWIGLU_OK;
+  // A call being captured into a CUDA graph gets its own allocation (alloc
+  // and free nodes inside the graph): a replay may run on another stream,
+  // unordered with later calls that would share this stream's buffer.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return SWIGLU_OK;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return SWIGLU_OK;
   unsigned long long id = 0;
   if (cudaStreamGetId(st, &id) != cudaSuccess) {
     cudaGetLastError();
