@@ -11,7 +11,11 @@ Inference", technical summary, "Enonce du probleme" (Y = SiLU(A W1) (.) (A W2));
 layouts per "Ou part le temps d'un token", "Un kernel pour les matrices
 etroites" (row-major weights, (k)*cols + col).
 
-Parity pins (tests/test_oracle.py): exact small-integer brute force, the silu
+The down projection (y = h . W_down + r, the anatomy chapter's kernels #10
+and #11) and the two-operation MLP are evaluated the same way.
+
+Parity pins (tests/test_oracle.py, tests/test_oracle_down.py): exact
+small-integer brute force, the silu
 identities silu(z) - silu(-z) = z and silu(z) = z (1 + tanh(z/2)) / 2,
 high-precision decimal evaluation, one-hot x, zeroed columns, column
 permutation, h(x) + h(-x) = g (.) u, power-of-two scaling, row independence,
@@ -55,6 +59,8 @@ def _load():
         lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
         lib.oracle_round_to_dtype.argtypes = [vp, i64, ip, vp]
         lib.oracle_round_to_dtype.restype = ip
+        lib.oracle_down_proj.argtypes = [vp, vp, vp, i64, i64, i64, ip, vp, vp, vp]
+        lib.oracle_down_proj.restype = ip
         _lib = lib
     return _lib
 
@@ -158,6 +164,38 @@ def swiglu_up_unfused(x, wg, wu, dtype):
     g = gemm64(x, wg, dtype)
     u = gemm64(x, wu, dtype)
     return silu_mul64(g, u)
+
+
+def down_proj(h, wd, dtype, r=None):
+    """y = h . wd (+ r): h [M, K], wd [K, N], r [M, N] or None, raw bits.
+    Returns (y64, y_rounded, sens)."""
+    lib = _load()
+    h, wd = _raw(h, dtype), _raw(wd, dtype)
+    M, K = h.shape
+    K2, N = wd.shape
+    if K2 != K:
+        raise ValueError("shape mismatch")
+    if r is not None:
+        r = _raw(r, dtype)
+        if r.shape != (M, N):
+            raise ValueError("residual shape mismatch")
+    y64 = np.empty((M, N), np.float64)
+    sens = np.empty((M, N), np.float64)
+    yr = np.empty((M, N), np.uint16 if dtype == BF16 else np.float32)
+    rc = lib.oracle_down_proj(_ptr(h), _ptr(wd), _ptr(r) if r is not None else None, M, K, N,
+                              dtype, _ptr(y64), _ptr(yr), _ptr(sens))
+    if rc != 0:
+        raise RuntimeError("oracle_down_proj failed (%d)" % rc)
+    return y64, yr, sens
+
+
+def mlp(x, wg, wu, wd, dtype, r=None, nthreads=None):
+    """The whole MLP as two operations: h = swiglu_up(x) rounded to the
+    operand type (the up-projection's output), then y = h . wd (+ r).
+    Returns (y64, y_rounded, sens, h_rounded)."""
+    _, h, _ = swiglu_up(x, wg, wu, dtype, nthreads=nthreads)
+    y64, yr, sens = down_proj(h, wd, dtype, r)
+    return y64, yr, sens, h
 
 
 def silu64(z):

@@ -260,3 +260,49 @@ int oracle_round_to_dtype(const double* v, int64_t n, int dtype, void* out) {
   for (int64_t t = 0; t < n; ++t) store_elem(out, t, dtype, v[t]);
   return 0;
 }
+
+/* ---- down projection (the MLP's second GEMM, plus the residual) --------- */
+
+/*
+ * y = h . W_down (+ r): "1 . Anatomie d'un transformeur sur GPU", section 1.2
+ * (W_down is a d_ff x d projection, 2 bS d d_ff FLOP) and section 1.6
+ * (kernel #10 "GEMM down", kernel #11 the residual addition).
+ *   h [M, K] (K = d_ff), wd [K, N] (N = d) row-major, r [M, N] or NULL.
+ *   y64 [M, N] fp64 (k ascending, then + r), y_out rounded to `dtype`
+ *   (may be NULL), sens [M, N] = sum_k |h||wd| + |r| (may be NULL): the
+ *   first-order sensitivity of y to relative accumulation error.
+ */
+int oracle_down_proj(const void* h, const void* wd, const void* r, int64_t M, int64_t K,
+                     int64_t N, int dtype, double* y64, void* y_out, double* sens) {
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return 2;
+  if (M < 0 || K < 0 || N < 0) return 2;
+  double* acc = (double*)malloc((size_t)(N > 0 ? N : 1) * 2 * sizeof(double));
+  if (!acc) return 1;
+  double* S = acc + N;
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) acc[j] = S[j] = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      double hv = load_elem(h, i * K + k, dtype);
+      double ah = fabs(hv);
+      for (int64_t j = 0; j < N; ++j) {
+        double wv = load_elem(wd, k * N + j, dtype);
+        acc[j] += hv * wv;
+        S[j] += ah * fabs(wv);
+      }
+    }
+    for (int64_t j = 0; j < N; ++j) {
+      double v = acc[j], s = S[j];
+      if (r) {
+        double rv = load_elem(r, i * N + j, dtype);
+        v += rv;
+        s += fabs(rv);
+      }
+      int64_t o = i * N + j;
+      if (y64) y64[o] = v;
+      if (sens) sens[o] = s;
+      if (y_out) store_elem(y_out, o, dtype, v);
+    }
+  }
+  free(acc);
+  return 0;
+}
