@@ -103,6 +103,49 @@ SWIGLU_API int swiglu_up_ex(const void* x, const void* w_gate, const void* w_up,
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Down projection y = h . W_down (+ residual): the MLP's second GEMM and its
+ * residual addition ("1 . Anatomie d'un transformeur sur GPU", section 1.6,
+ * kernels #10 "GEMM down" and #11 the residual).
+ *
+ *     h        [M, d_ff]  row-major (typically swiglu_up's output)
+ *     w_down   [d_ff, d]  row-major (element (k, j) at k*d + j)
+ *     residual [M, d]     row-major, or NULL for none; it may be y itself
+ *                         (in-place residual update) but must not partially
+ *                         overlap y
+ *     y        [M, d]     row-major output; must not overlap h or w_down
+ *
+ * Sums in f32 over k, the residual added to the f32 sum, one rounding to the
+ * output type.  bf16 only (f32 returns SWIGLU_ERR_UNSUPPORTED), on the
+ * tensor-core paths: M <= 16 -> split-K skinny kernel, larger M -> tile
+ * kernel (SWIGLU_PATH_SIMT is rejected).  d_ff == 0 gives y = residual (or 0).
+ * Workspace, streams, determinism and errors as for swiglu_up.
+ */
+SWIGLU_API int swiglu_down(const void* h, const void* w_down, const void* residual, void* y,
+                           int64_t M, int64_t d_ff, int64_t d, int dtype, void* stream);
+
+/* As swiglu_down, with an explicit path and optional caller workspace (see
+ * swiglu_up_ex; size from swiglu_down_workspace_bytes). */
+SWIGLU_API int swiglu_down_ex(const void* h, const void* w_down, const void* residual, void* y,
+                              int64_t M, int64_t d_ff, int64_t d, int dtype, int path,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of swiglu_down_ex on the current device (0 when invalid). */
+SWIGLU_API size_t swiglu_down_workspace_bytes(int64_t M, int64_t d_ff, int64_t d, int dtype,
+                                              int path);
+
+/*
+ * The whole MLP of "1 . Anatomie d'un transformeur sur GPU", section 1.1,
+ * after its RMSNorm: h = silu(x . W_gate) (.) (x . W_up), then
+ * y = h . W_down (+ residual).  Two kernels on `stream`; h [M, d_ff] is the
+ * caller's buffer and holds the up projection's (bf16-rounded) output
+ * afterwards.  y may be x only when residual is x too.  bf16 only.  All
+ * arguments of both steps are validated before anything is enqueued.
+ */
+SWIGLU_API int swiglu_mlp(const void* x, const void* w_gate, const void* w_up,
+                          const void* w_down, const void* residual, void* h, void* y,
+                          int64_t M, int64_t d, int64_t d_ff, int dtype, void* stream);
+
+/*
  * As swiglu_up, for callers that cannot allocate device memory.  Some
  * callers may not call cudaMalloc (or any allocator) while they run this
  * operation: a host framework that invokes operators from an enqueue
@@ -156,6 +199,10 @@ typedef struct {
 
 SWIGLU_API int swiglu_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, int path,
                 int num_sms, swiglu_plan_info* out);
+
+/* As swiglu_plan, for the down projection y [M, d] = h [M, d_ff] . W_down. */
+SWIGLU_API int swiglu_down_plan(int64_t M, int64_t d_ff, int64_t d, int dtype, int path,
+                                int num_sms, swiglu_plan_info* out);
 
 /*
  * The K-slice rule of "Ou part le temps d'un token", section "Un kernel pour

@@ -93,6 +93,108 @@ def swiglu_up(x, w_gate, w_up, out=None, path="auto", workspace=None, stream=Non
     return out
 
 
+def _check_cuda(**tensors):
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+
+
+def swiglu_down(h, w_down, residual=None, out=None, path="auto", workspace=None, stream=None):
+    """y = h @ w_down (+ residual): the MLP's down projection.
+
+    h [M, d_ff], w_down [d_ff, d], residual [M, d] (or None; may be ``out``):
+    contiguous bfloat16 CUDA tensors.  Returns y [M, d] (``out`` if given).
+    """
+    global _LIB
+    import torch
+    _check_cuda(h=h, w_down=w_down, residual=residual)
+    if h.dim() != 2 or w_down.dim() != 2 or w_down.shape[0] != h.shape[1]:
+        raise ValueError("expected h [M, d_ff] and w_down [d_ff, d]")
+    M, d_ff = h.shape
+    d = w_down.shape[1]
+    dt = _dtype_code(h)
+    if w_down.dtype != h.dtype or (residual is not None and residual.dtype != h.dtype):
+        raise TypeError("h, w_down and residual must share one dtype")
+    if residual is not None and residual.shape != (M, d):
+        raise ValueError("residual must be [M, d]")
+    if out is None:
+        out = torch.empty((M, d), dtype=h.dtype, device=h.device)
+    elif out.shape != (M, d) or out.dtype != h.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, d] tensor of h's dtype")
+    index = h.device.index
+    st = stream.cuda_stream if stream is not None else _raw_stream(index)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    if _LIB is None:
+        _LIB = _lib.load()
+    args = (h.data_ptr(), w_down.data_ptr(), residual.data_ptr() if residual is not None else None,
+            out.data_ptr(), M, d_ff, d, dt, _path_code(path), ws_ptr, ws_bytes, st)
+    if torch.cuda.current_device() != index:
+        with torch.cuda.device(index):
+            status = _LIB.swiglu_down_ex(*args)
+    else:
+        status = _LIB.swiglu_down_ex(*args)
+    if status:
+        _lib.check(status)
+    return out
+
+
+def swiglu_mlp(x, w_gate, w_up, w_down, residual=None, h=None, out=None, stream=None):
+    """y = silu(x @ w_gate) * (x @ w_up) @ w_down (+ residual), as two kernels.
+
+    ``h`` [M, d_ff] receives the intermediate (allocated if None).  Returns
+    (y, h).  bfloat16 only.
+    """
+    global _LIB
+    import torch
+    _check_cuda(x=x, w_gate=w_gate, w_up=w_up, w_down=w_down, residual=residual)
+    M, d = x.shape
+    d_ff = w_gate.shape[1]
+    if w_down.shape != (d_ff, d) or w_gate.shape != (d, d_ff) or w_up.shape != (d, d_ff):
+        raise ValueError("expected x [M, d], w_gate/w_up [d, d_ff], w_down [d_ff, d]")
+    dt = _dtype_code(x)
+    if h is None:
+        h = torch.empty((M, d_ff), dtype=x.dtype, device=x.device)
+    if out is None:
+        out = torch.empty((M, d), dtype=x.dtype, device=x.device)
+    index = x.device.index
+    st = stream.cuda_stream if stream is not None else _raw_stream(index)
+    if _LIB is None:
+        _LIB = _lib.load()
+    args = (x.data_ptr(), w_gate.data_ptr(), w_up.data_ptr(), w_down.data_ptr(),
+            residual.data_ptr() if residual is not None else None, h.data_ptr(),
+            out.data_ptr(), M, d, d_ff, dt, st)
+    if torch.cuda.current_device() != index:
+        with torch.cuda.device(index):
+            status = _LIB.swiglu_mlp(*args)
+    else:
+        status = _LIB.swiglu_mlp(*args)
+    if status:
+        _lib.check(status)
+    return out, h
+
+
+def down_workspace_bytes(M, d_ff, d, dtype="bf16", path="auto"):
+    lib = _lib.load()
+    dt = BF16 if dtype in ("bf16", BF16) else F32
+    return int(lib.swiglu_down_workspace_bytes(M, d_ff, d, dt, _path_code(path)))
+
+
+def down_plan(M, d_ff, d, dtype="bf16", path="auto", num_sms=152):
+    """How a down-projection call would be served (host-only)."""
+    lib = _lib.load()
+    info = _lib.PlanInfo()
+    dt = BF16 if dtype in ("bf16", BF16) else F32
+    _lib.check(lib.swiglu_down_plan(M, d_ff, d, dt, _path_code(path), num_sms, ctypes.byref(info)))
+    return {"path": PATH_NAMES.get(info.path, info.path), "slices": info.slices,
+            "grid": info.grid, "workspace": info.workspace, "launches": info.launches}
+
+
 def workspace_bytes(M, d, d_ff, dtype="bf16", path="auto"):
     """Workspace bytes a call needs on the current device (0 for the TC path)."""
     lib = _lib.load()
@@ -126,5 +228,6 @@ def version():
     return int(_lib.load().swiglu_version())
 
 
-__all__ = ["swiglu_up", "workspace_bytes", "plan", "split_k_slices",
+__all__ = ["swiglu_up", "swiglu_down", "swiglu_mlp", "workspace_bytes",
+           "down_workspace_bytes", "plan", "down_plan", "split_k_slices",
            "check_device_status", "version", "SwiGLUError", "PATHS"]

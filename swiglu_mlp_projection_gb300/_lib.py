@@ -36,6 +36,11 @@ SIGNATURES = {
     "swiglu_up": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp], _int),
     "swiglu_up_ex": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp, _sz, _vp], _int),
     "swiglu_up_noalloc": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp], _int),
+    "swiglu_down": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp], _int),
+    "swiglu_down_ex": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp, _sz, _vp], _int),
+    "swiglu_down_workspace_bytes": ([_i64, _i64, _i64, _int, _int], _sz),
+    "swiglu_mlp": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp], _int),
+    "swiglu_down_plan": ([_i64, _i64, _i64, _int, _int, _int, ctypes.POINTER(PlanInfo)], _int),
     "swiglu_workspace_bytes": ([_i64, _i64, _i64, _int, _int], _sz),
     "swiglu_plan": ([_i64, _i64, _i64, _int, _int, _int, ctypes.POINTER(PlanInfo)], _int),
     "swiglu_split_k_slices": ([_i64, _i64, _i64, _i64], _i64),

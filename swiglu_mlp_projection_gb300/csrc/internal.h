@@ -57,6 +57,7 @@ struct SkinnyPlan {
   int nb;                  // 64-column blocks per unit (1, 2 or 4)
   int l2_promo;            // L2 promotion of the weight loads (bytes, 0 = none)
   int hint;                // weight-load L2 hint: 0 none, 1 evict_first
+  bool plain;              // plain epilogue (down projection) instead of SwiGLU
   int64_t n_cb, n_kb;      // units: (nb x 64)-column groups, 64-deep k blocks
   int64_t units;           // n_cb * n_kb
   int grid;                // CTAs (<= SM count)
@@ -65,24 +66,32 @@ struct SkinnyPlan {
   size_t part_bytes;       // partial sums
 };
 constexpr int kSkinnyMaxN = 256;
-SkinnyPlan plan_skinny(int64_t M, int64_t d, int64_t d_ff, int num_sms);
-// `counters`: n_cb arrival counters, zero on entry when `counters_clean`
-// (left so by the previous call on the same stream), else cleared first.
-cudaError_t launch_skinny_tc(const void* x, const void* wg, const void* wu, void* h, int64_t M,
-                             int64_t d, int64_t d_ff, const SkinnyPlan& p, float* part,
-                             unsigned* counters, bool counters_clean, unsigned* status,
-                             uint64_t timeout_ns, cudaStream_t st);
+// K: shared dimension; n_out: output columns; plain: down-projection mode.
+SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain);
+// out[M][n_out] = silu(x.wa) * (x.wa') (SwiGLU: wa = W_gate, wb = W_up) or
+// x.wa (+ resid) (plain: wa = W_down, wb unused).  `counters`: n_cb arrival
+// counters, zero on entry when `counters_clean` (left so by the previous call
+// on the same stream), else cleared first.
+cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void* out,
+                             const void* resid, int64_t M, int64_t K, int64_t n_out,
+                             const SkinnyPlan& p, float* part, unsigned* counters,
+                             bool counters_clean, unsigned* status, uint64_t timeout_ns,
+                             cudaStream_t st);
 constexpr size_t kStreamCounterBytes = 64 * 1024;   // per-stream arrival counters
 
-// Tile tensor-core path (bf16, large M): 128 x (128 gate + 128 up) output
-// tiles, SwiGLU applied to the accumulator tile before a single bf16 store.
+// Tile tensor-core path (bf16, large M): 128-row output tiles.  SwiGLU:
+// 128 output columns whose gate and up accumulators sit side by side
+// (128 x 256 f32), SwiGLU applied before the bf16 store.  Plain (down
+// projection): 256 output columns, + residual, bf16 store.
 struct TilePlan {
   int64_t n_mb, n_nb, tiles;
   int grid;
+  bool plain;
 };
-TilePlan plan_tile(int64_t M, int64_t d, int64_t d_ff, int num_sms);
-cudaError_t launch_tile_tc(const void* x, const void* wg, const void* wu, void* h, int64_t M,
-                           int64_t d, int64_t d_ff, const TilePlan& p, unsigned* status,
-                           uint64_t timeout_ns, cudaStream_t st);
+TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain);
+cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* out,
+                           const void* resid, int64_t M, int64_t K, int64_t n_out,
+                           const TilePlan& p, unsigned* status, uint64_t timeout_ns,
+                           cudaStream_t st);
 
 }  // namespace swg

@@ -215,14 +215,24 @@ uint64_t wait_timeout_ns() {
   return ns;
 }
 
-// AUTO: f32 -> SIMT; bf16 M <= kSkinnyMaxM -> SKINNY; larger bf16 M -> TC.
-// d == 0 (empty sums) always goes to the SIMT path, whose reduction kernel
-// then writes h = silu(0) * 0 = 0.
-int resolve_path(int64_t M, int64_t d, int dtype, int path, int* out) {
+// The two operations the library serves.
+enum Op { kOpUp = 0, kOpDown = 1 };
+
+// Up projection, AUTO: f32 -> SIMT; bf16 M <= kSkinnyMaxM -> SKINNY; larger
+// bf16 M -> TC.  d == 0 (empty sums) always goes to the SIMT path, whose
+// reduction kernel then writes h = silu(0) * 0 = 0.
+// Down projection: bf16 only, on the tensor-core paths (same M rule).
+int resolve_path(int op, int64_t M, int64_t K, int dtype, int path, int* out) {
   if (path < SWIGLU_PATH_AUTO || path > SWIGLU_PATH_TC)
     return fail(SWIGLU_ERR_INVALID_ARG, "unknown path %d", path);
+  if (op == kOpDown) {
+    if (dtype != SWIGLU_BF16)
+      return fail(SWIGLU_ERR_UNSUPPORTED, "the down projection serves bf16 only");
+    if (path == SWIGLU_PATH_SIMT)
+      return fail(SWIGLU_ERR_UNSUPPORTED, "the down projection has no SIMT path");
+  }
   if (path == SWIGLU_PATH_AUTO) {
-    if (dtype == SWIGLU_F32 || d == 0) *out = SWIGLU_PATH_SIMT;
+    if (op == kOpUp && (dtype == SWIGLU_F32 || K == 0)) *out = SWIGLU_PATH_SIMT;
     else *out = M <= kSkinnyMaxM ? SWIGLU_PATH_SKINNY : SWIGLU_PATH_TC;
     return SWIGLU_OK;
   }
@@ -230,12 +240,11 @@ int resolve_path(int64_t M, int64_t d, int dtype, int path, int* out) {
     return fail(SWIGLU_ERR_UNSUPPORTED, "the tensor-core paths serve bf16 only");
   if (path == SWIGLU_PATH_SKINNY && M > kSkinnyMaxN)
     return fail(SWIGLU_ERR_UNSUPPORTED, "the skinny path serves M <= %d", kSkinnyMaxN);
-  *out = d == 0 ? SWIGLU_PATH_SIMT : path;
+  *out = (op == kOpUp && K == 0) ? SWIGLU_PATH_SIMT : path;
   return SWIGLU_OK;
 }
 
-int validate(const void* x, const void* wg, const void* wu, const void* h,
-             int64_t M, int64_t d, int64_t d_ff, int dtype) {
+int check_sizes(int64_t M, int64_t d, int64_t d_ff, int dtype) {
   if (dtype != SWIGLU_F32 && dtype != SWIGLU_BF16)
     return fail(SWIGLU_ERR_INVALID_ARG, "unknown dtype %d", dtype);
   if (M < 0 || d < 0 || d_ff < 0)
@@ -243,18 +252,44 @@ int validate(const void* x, const void* wg, const void* wu, const void* h,
                 (long long)M, (long long)d, (long long)d_ff);
   if (M > INT32_MAX || d > INT32_MAX || d_ff > INT32_MAX)
     return fail(SWIGLU_ERR_UNSUPPORTED, "a size exceeds 2^31-1");
+  const int64_t per16 = (int64_t)(16 / elem_bytes(dtype));
+  if (d % per16 != 0 || d_ff % per16 != 0)
+    return fail(SWIGLU_ERR_ALIGNMENT, "d and d_ff must be multiples of %lld for this dtype",
+                (long long)per16);
+  return SWIGLU_OK;
+}
+
+int validate(const void* x, const void* wg, const void* wu, const void* h,
+             int64_t M, int64_t d, int64_t d_ff, int dtype) {
+  int v = check_sizes(M, d, d_ff, dtype);
+  if (v != SWIGLU_OK) return v;
   const size_t e = (size_t)elem_bytes(dtype);
   const size_t nx = (size_t)M * d * e, nw = (size_t)d * d_ff * e, nh = (size_t)M * d_ff * e;
   if ((nx && !x) || (nw && (!wg || !wu)) || (nh && !h))
     return fail(SWIGLU_ERR_INVALID_ARG, "null pointer for a non-empty tensor");
   if ((x && !aligned16(x)) || (wg && !aligned16(wg)) || (wu && !aligned16(wu)) || (h && !aligned16(h)))
     return fail(SWIGLU_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
-  const int64_t per16 = (int64_t)(16 / e);
-  if (d % per16 != 0 || d_ff % per16 != 0)
-    return fail(SWIGLU_ERR_ALIGNMENT, "d and d_ff must be multiples of %lld for this dtype",
-                (long long)per16);
   if (overlaps(h, nh, x, nx) || overlaps(h, nh, wg, nw) || overlaps(h, nh, wu, nw))
     return fail(SWIGLU_ERR_INVALID_ARG, "h overlaps an input");
+  return SWIGLU_OK;
+}
+
+// y [M, d] = h [M, d_ff] . W_down [d_ff, d] (+ r [M, d]); r may be y itself.
+int validate_down(const void* h, const void* wd, const void* r, const void* y, int64_t M,
+                  int64_t d_ff, int64_t d, int dtype) {
+  int v = check_sizes(M, d, d_ff, dtype);
+  if (v != SWIGLU_OK) return v;
+  const size_t e = (size_t)elem_bytes(dtype);
+  const size_t nh = (size_t)M * d_ff * e, nw = (size_t)d_ff * d * e, ny = (size_t)M * d * e;
+  if ((nh && !h) || (nw && !wd) || (ny && !y))
+    return fail(SWIGLU_ERR_INVALID_ARG, "null pointer for a non-empty tensor");
+  if ((h && !aligned16(h)) || (wd && !aligned16(wd)) || (r && !aligned16(r)) ||
+      (y && !aligned16(y)))
+    return fail(SWIGLU_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
+  if (overlaps(y, ny, h, nh) || overlaps(y, ny, wd, nw))
+    return fail(SWIGLU_ERR_INVALID_ARG, "y overlaps an input");
+  if (r && r != y && overlaps(y, ny, r, ny))
+    return fail(SWIGLU_ERR_INVALID_ARG, "residual partially overlaps y");
   return SWIGLU_OK;
 }
 
@@ -269,51 +304,79 @@ struct Plan {
   size_t workspace;
 };
 
-int make_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, int path, int num_sms, Plan* p) {
+// K: shared dimension; n_out: output columns (up: d, d_ff; down: d_ff, d).
+int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, int num_sms,
+              Plan* p) {
   int rp = 0;
-  int st = resolve_path(M, d, dtype, path, &rp);
+  int st = resolve_path(op, M, K, dtype, path, &rp);
   if (st != SWIGLU_OK) return st;
   *p = Plan{};
   p->path = rp;
+  const bool plain = op == kOpDown;
   if (rp == SWIGLU_PATH_SIMT) {
-    p->simt = plan_simt(M, d, d_ff, dtype, num_sms);
+    p->simt = plan_simt(M, K, n_out, dtype, num_sms);
     if (p->simt.slices > kMaxGridYZ || p->simt.row_chunks > kMaxGridYZ)
       return fail(SWIGLU_ERR_UNSUPPORTED, "shape exceeds the grid limits of the SIMT path");
     p->slices = p->simt.slices;
     p->grid = p->simt.col_blocks * p->simt.slices * p->simt.row_chunks;
-    p->workspace = partial_elems(p->slices, M, d_ff) * sizeof(float);
+    p->workspace = partial_elems(p->slices, M, n_out) * sizeof(float);
     p->launches = p->slices > 0 ? 2 : 1;
   } else if (rp == SWIGLU_PATH_SKINNY) {
-    p->skinny = plan_skinny(M, d, d_ff, num_sms);
+    p->skinny = plan_skinny(M, K, n_out, num_sms, plain);
     p->slices = p->skinny.maxq;
     p->grid = p->skinny.grid;
     p->workspace = p->skinny.counters_bytes + p->skinny.part_bytes;
     p->launches = 1;
   } else {
-    p->tile = plan_tile(M, d, d_ff, num_sms);
+    p->tile = plan_tile(M, K, n_out, num_sms, plain);
     p->slices = 1;
     p->grid = p->tile.grid;
     p->workspace = 0;
     p->launches = 1;
   }
-  if (M == 0 || d_ff == 0) p->launches = 0;
+  if (M == 0 || n_out == 0) p->launches = 0;
+  if (plain && K == 0) p->launches = 0;
   p->workspace = (p->workspace + 255) / 256 * 256;
   return SWIGLU_OK;
 }
 
-int run(const void* x, const void* wg, const void* wu, void* h, int64_t M, int64_t d,
-        int64_t d_ff, int dtype, int path, void* workspace, size_t ws_bytes,
-        cudaStream_t st) {
-  int v = validate(x, wg, wu, h, M, d, d_ff, dtype);
-  if (v != SWIGLU_OK) return v;
+// One call of either operation: x [M, K] times the weights, into out [M, n_out].
+struct Call {
+  int op;
+  const void *x, *wa, *wb, *resid;
+  void* out;
+  int64_t M, K, n_out;
+  int dtype, path;
+  void* workspace;
+  size_t ws_bytes;
+  cudaStream_t st;
+};
+
+int run(const Call& c) {
+  int v;
   int dev = 0;
   DeviceInfo di;
   if ((v = current_device(&dev, &di)) != SWIGLU_OK) return v;
   Plan p;
-  if ((v = make_plan(M, d, d_ff, dtype, path, di.num_sms, &p)) != SWIGLU_OK) return v;
-  if (M == 0 || d_ff == 0) return SWIGLU_OK;
-  if (workspace && overlaps(h, (size_t)M * d_ff * elem_bytes(dtype), workspace, ws_bytes))
-    return fail(SWIGLU_ERR_INVALID_ARG, "h overlaps the workspace");
+  if ((v = make_plan(c.op, c.M, c.K, c.n_out, c.dtype, c.path, di.num_sms, &p)) != SWIGLU_OK)
+    return v;
+  if (c.M == 0 || c.n_out == 0) {
+    t_err[0] = 0;
+    return SWIGLU_OK;
+  }
+  const size_t out_bytes = (size_t)c.M * c.n_out * elem_bytes(c.dtype);
+  if (c.op == kOpDown && c.K == 0) {
+    // empty sums: y = residual, or 0
+    cudaError_t e = c.resid ? (c.resid == c.out ? cudaSuccess
+                                                : cudaMemcpyAsync(c.out, c.resid, out_bytes,
+                                                                  cudaMemcpyDeviceToDevice, c.st))
+                            : cudaMemsetAsync(c.out, 0, out_bytes, c.st);
+    if (e != cudaSuccess) return cuda_fail(e, "empty-sum fill");
+    t_err[0] = 0;
+    return SWIGLU_OK;
+  }
+  if (c.workspace && overlaps(c.out, out_bytes, c.workspace, c.ws_bytes))
+    return fail(SWIGLU_ERR_INVALID_ARG, "the output overlaps the workspace");
 
   // Where the partial sums (and the skinny kernel's counters) live:
   //   caller workspace -> [counters][partials] inside it, counters cleared;
@@ -324,13 +387,14 @@ int run(const void* x, const void* wg, const void* wu, void* h, int64_t M, int64
   bool counters_clean = false;
   void* pooled = nullptr;
   const size_t counter_bytes = p.path == SWIGLU_PATH_SKINNY ? p.skinny.counters_bytes : 0;
+  cudaStream_t st = c.st;
   if (p.workspace > 0) {
-    if (workspace) {
-      if (ws_bytes < p.workspace || ((uintptr_t)workspace & 255u))
+    if (c.workspace) {
+      if (c.ws_bytes < p.workspace || ((uintptr_t)c.workspace & 255u))
         return fail(SWIGLU_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)",
-                    p.workspace, ws_bytes);
-      counters = (unsigned*)workspace;
-      part = (float*)((char*)workspace + counter_bytes);
+                    p.workspace, c.ws_bytes);
+      counters = (unsigned*)c.workspace;
+      part = (float*)((char*)c.workspace + counter_bytes);
     } else {
       if ((v = stream_workspace(dev, st, p.workspace - counter_bytes, &part, &counters)) != SWIGLU_OK)
         return v;
@@ -356,13 +420,15 @@ int run(const void* x, const void* wg, const void* wu, void* h, int64_t M, int64
 
   cudaError_t e = cudaSuccess;
   if (p.path == SWIGLU_PATH_SIMT) {
-    e = launch_simt_partial(x, wg, wu, part, M, d, d_ff, dtype, p.simt, st);
-    if (e == cudaSuccess) e = launch_reduce_swiglu(part, h, M, d_ff, p.slices, dtype, di.num_sms, st);
+    e = launch_simt_partial(c.x, c.wa, c.wb, part, c.M, c.K, c.n_out, c.dtype, p.simt, st);
+    if (e == cudaSuccess)
+      e = launch_reduce_swiglu(part, c.out, c.M, c.n_out, p.slices, c.dtype, di.num_sms, st);
   } else if (p.path == SWIGLU_PATH_SKINNY) {
-    e = launch_skinny_tc(x, wg, wu, h, M, d, d_ff, p.skinny, part, counters, counters_clean,
-                         di.status, wait_timeout_ns(), st);
+    e = launch_skinny_tc(c.x, c.wa, c.wb, c.out, c.resid, c.M, c.K, c.n_out, p.skinny, part,
+                         counters, counters_clean, di.status, wait_timeout_ns(), st);
   } else {
-    e = launch_tile_tc(x, wg, wu, h, M, d, d_ff, p.tile, di.status, wait_timeout_ns(), st);
+    e = launch_tile_tc(c.x, c.wa, c.wb, c.out, c.resid, c.M, c.K, c.n_out, p.tile, di.status,
+                       wait_timeout_ns(), st);
   }
   if (pooled) {
     cudaError_t ef = cudaFreeAsync(pooled, st);
@@ -371,6 +437,22 @@ int run(const void* x, const void* wg, const void* wu, void* h, int64_t M, int64
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   t_err[0] = 0;
   return SWIGLU_OK;
+}
+
+int run_up(const void* x, const void* wg, const void* wu, void* h, int64_t M, int64_t d,
+           int64_t d_ff, int dtype, int path, void* workspace, size_t ws_bytes,
+           cudaStream_t st) {
+  int v = validate(x, wg, wu, h, M, d, d_ff, dtype);
+  if (v != SWIGLU_OK) return v;
+  return run(Call{kOpUp, x, wg, wu, nullptr, h, M, d, d_ff, dtype, path, workspace, ws_bytes, st});
+}
+
+int run_down(const void* h, const void* wd, const void* r, void* y, int64_t M, int64_t d_ff,
+             int64_t d, int dtype, int path, void* workspace, size_t ws_bytes,
+             cudaStream_t st) {
+  int v = validate_down(h, wd, r, y, M, d_ff, d, dtype);
+  if (v != SWIGLU_OK) return v;
+  return run(Call{kOpDown, h, wd, wd, r, y, M, d_ff, d, dtype, path, workspace, ws_bytes, st});
 }
 
 }  // namespace
@@ -418,35 +500,78 @@ extern "C" {
 
 int swiglu_up(const void* x, const void* w_gate, const void* w_up, void* h,
               int64_t M, int64_t d, int64_t d_ff, int dtype, void* stream) {
-  return run(x, w_gate, w_up, h, M, d, d_ff, dtype, SWIGLU_PATH_AUTO, nullptr, 0,
-             (cudaStream_t)stream);
+  return run_up(x, w_gate, w_up, h, M, d, d_ff, dtype, SWIGLU_PATH_AUTO, nullptr, 0,
+                (cudaStream_t)stream);
 }
 
 int swiglu_up_ex(const void* x, const void* w_gate, const void* w_up, void* h,
                  int64_t M, int64_t d, int64_t d_ff, int dtype, int path,
                  void* workspace, size_t workspace_bytes, void* stream) {
-  return run(x, w_gate, w_up, h, M, d, d_ff, dtype, path, workspace, workspace_bytes,
+  return run_up(x, w_gate, w_up, h, M, d, d_ff, dtype, path, workspace, workspace_bytes,
+                (cudaStream_t)stream);
+}
+
+int swiglu_down(const void* h, const void* w_down, const void* residual, void* y, int64_t M,
+                int64_t d_ff, int64_t d, int dtype, void* stream) {
+  return run_down(h, w_down, residual, y, M, d_ff, d, dtype, SWIGLU_PATH_AUTO, nullptr, 0,
+                  (cudaStream_t)stream);
+}
+
+int swiglu_down_ex(const void* h, const void* w_down, const void* residual, void* y,
+                   int64_t M, int64_t d_ff, int64_t d, int dtype, int path, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  return run_down(h, w_down, residual, y, M, d_ff, d, dtype, path, workspace, workspace_bytes,
+                  (cudaStream_t)stream);
+}
+
+int swiglu_mlp(const void* x, const void* w_gate, const void* w_up, const void* w_down,
+               const void* residual, void* h, void* y, int64_t M, int64_t d, int64_t d_ff,
+               int dtype, void* stream) {
+  // Both steps are validated before either is enqueued.
+  int v = validate(x, w_gate, w_up, h, M, d, d_ff, dtype);
+  if (v != SWIGLU_OK) return v;
+  if ((v = validate_down(h, w_down, residual, y, M, d_ff, d, dtype)) != SWIGLU_OK) return v;
+  if (dtype != SWIGLU_BF16)
+    return fail(SWIGLU_ERR_UNSUPPORTED, "the down projection serves bf16 only");
+  const size_t e = (size_t)elem_bytes(dtype);
+  if (overlaps(y, (size_t)M * d * e, x, (size_t)M * d * e) && y != x)
+    return fail(SWIGLU_ERR_INVALID_ARG, "y partially overlaps x");
+  if (y == x && residual != x)
+    return fail(SWIGLU_ERR_INVALID_ARG, "y may alias x only when x is also the residual");
+  v = run_up(x, w_gate, w_up, h, M, d, d_ff, dtype, SWIGLU_PATH_AUTO, nullptr, 0,
              (cudaStream_t)stream);
+  if (v != SWIGLU_OK) return v;
+  return run_down(h, w_down, residual, y, M, d_ff, d, dtype, SWIGLU_PATH_AUTO, nullptr, 0,
+                  (cudaStream_t)stream);
 }
 
 size_t swiglu_workspace_bytes(int64_t M, int64_t d, int64_t d_ff, int dtype, int path) {
-  if (dtype != SWIGLU_F32 && dtype != SWIGLU_BF16) { fail(SWIGLU_ERR_INVALID_ARG, "unknown dtype %d", dtype); return 0; }
-  if (M < 0 || d < 0 || d_ff < 0) { fail(SWIGLU_ERR_INVALID_ARG, "negative size"); return 0; }
+  if (check_sizes(M < 0 ? -1 : M, d, d_ff, dtype) != SWIGLU_OK) return 0;
   int dev = 0;
   DeviceInfo di;
   if (current_device(&dev, &di) != SWIGLU_OK) return 0;
   Plan p;
-  if (make_plan(M, d, d_ff, dtype, path, di.num_sms, &p) != SWIGLU_OK) return 0;
+  if (make_plan(kOpUp, M, d, d_ff, dtype, path, di.num_sms, &p) != SWIGLU_OK) return 0;
   return p.workspace;
 }
 
-int swiglu_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, int path, int num_sms,
-                swiglu_plan_info* out) {
+size_t swiglu_down_workspace_bytes(int64_t M, int64_t d_ff, int64_t d, int dtype, int path) {
+  if (check_sizes(M < 0 ? -1 : M, d, d_ff, dtype) != SWIGLU_OK) return 0;
+  int dev = 0;
+  DeviceInfo di;
+  if (current_device(&dev, &di) != SWIGLU_OK) return 0;
+  Plan p;
+  if (make_plan(kOpDown, M, d_ff, d, dtype, path, di.num_sms, &p) != SWIGLU_OK) return 0;
+  return p.workspace;
+}
+
+static int plan_common(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path,
+                       int num_sms, swiglu_plan_info* out) {
   if (!out) return fail(SWIGLU_ERR_INVALID_ARG, "null output");
   if (dtype != SWIGLU_F32 && dtype != SWIGLU_BF16) return fail(SWIGLU_ERR_INVALID_ARG, "unknown dtype %d", dtype);
-  if (M < 0 || d < 0 || d_ff < 0 || num_sms <= 0) return fail(SWIGLU_ERR_INVALID_ARG, "negative size or SM count");
+  if (M < 0 || K < 0 || n_out < 0 || num_sms <= 0) return fail(SWIGLU_ERR_INVALID_ARG, "negative size or SM count");
   Plan p;
-  int v = make_plan(M, d, d_ff, dtype, path, num_sms, &p);
+  int v = make_plan(op, M, K, n_out, dtype, path, num_sms, &p);
   if (v != SWIGLU_OK) return v;
   out->path = p.path;
   out->slices = p.slices;
@@ -456,6 +581,16 @@ int swiglu_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, int path, int num
   out->skinny_max_m = kSkinnyMaxM;
   out->launches = p.launches;
   return SWIGLU_OK;
+}
+
+int swiglu_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, int path, int num_sms,
+                swiglu_plan_info* out) {
+  return plan_common(kOpUp, M, d, d_ff, dtype, path, num_sms, out);
+}
+
+int swiglu_down_plan(int64_t M, int64_t d_ff, int64_t d, int dtype, int path, int num_sms,
+                     swiglu_plan_info* out) {
+  return plan_common(kOpDown, M, d_ff, d, dtype, path, num_sms, out);
 }
 
 int64_t swiglu_split_k_slices(int64_t K, int64_t col_blocks, int64_t target_blocks,

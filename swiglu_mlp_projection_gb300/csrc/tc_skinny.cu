@@ -28,6 +28,12 @@
 //     the partials in contributor order -- i.e. in k order -- applies
 //     silu(g) * u and stores h as bf16.
 //
+// The same kernel serves the down projection y = h . W_down (+ residual)
+// ("1 . Anatomie d'un transformeur sur GPU", section 1.6, kernels #10 and
+// #11) in its plain epilogue mode: an MMA tile then holds 128 adjacent W_down
+// columns, and the final reduction adds the residual instead of applying
+// SiLU * up.
+//
 // Warp roles (192 threads): warp 0 lane 0 issues TMA, warp 1 lane 0 issues
 // MMAs (warp 1 owns the TMEM allocation), warps 2-5 drain the accumulator.
 // Every mbarrier wait is bounded; on timeout the CTA raises the device error
@@ -74,16 +80,23 @@ struct SkCfg {
 };
 
 struct SkArgs {
-  int M, d_ff, n_kb, maxq;
+  int M, n_out, n_kb, maxq;   // n_out: output columns (d_ff, or d for the down projection)
   int64_t units;
   int grid;
   int hint;             // 1: weight loads carry an L2 evict_first hint
   float* part;          // [n_cg][maxq][NB][2][M][64]
   unsigned* counters;   // [n_cg], zero on entry, zero again on exit
-  uint16_t* h;          // [M][d_ff] bf16
+  uint16_t* out;        // [M][n_out] bf16
+  const uint16_t* resid;   // plain mode: [M][n_out] bf16 added to the sums, or null
   unsigned* status;
   uint64_t timeout_ns;
 };
+
+// Epilogue modes.  kSwiGLU: A tile = 64 W_gate columns over the same 64 W_up
+// columns, output = silu(g) * u for 64 columns.  kPlain: A tile = 128
+// adjacent columns of one weight, output = sum (+ residual) for 128 columns.
+constexpr int kSwiGLU = 0;
+constexpr int kPlain = 1;
 
 // CTA whose unit range [c U / G, (c+1) U / G) contains unit t.
 __device__ __forceinline__ int64_t cta_of(int64_t t, int64_t U, int64_t G) {
@@ -96,12 +109,18 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, unsig
   return mbar_wait(bar, parity, &never, status, timeout_ns);
 }
 
-template <int N, int NB>
+template <int N, int NB, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                  const __grid_constant__ CUtensorMap tm_wg,
                  const __grid_constant__ CUtensorMap tm_wu, const SkArgs a) {
   using C = SkCfg<N, NB>;
+  // Weight columns of one unit's sub-block, and where its two 64-column
+  // boxes come from: (tm_wg, col) and (tm_wu, col) for SwiGLU, (tm_wg, col)
+  // and (tm_wg, col + 64) for the plain mode.
+  constexpr int kSubCols = MODE == kSwiGLU ? kCB : 2 * kCB;
+  const CUtensorMap* hi_map = MODE == kSwiGLU ? &tm_wu : &tm_wg;
+  constexpr int kHiOff = MODE == kSwiGLU ? 0 : kCB;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* stages = smem_raw + pad;
@@ -153,8 +172,9 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
       const int cg = (int)(t / a.n_kb), kb = (int)(t - (int64_t)cg * a.n_kb);
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
-        tma_prefetch_l2_2d(&tm_wg, (cg * NB + b) * kCB, kb * kBK);
-        tma_prefetch_l2_2d(&tm_wu, (cg * NB + b) * kCB, kb * kBK);
+        const int col = (cg * NB + b) * kSubCols;
+        tma_prefetch_l2_2d(&tm_wg, col, kb * kBK);
+        tma_prefetch_l2_2d(hi_map, col + kHiOff, kb * kBK);
       }
     }
   }
@@ -179,14 +199,15 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-          const int col = (cg * NB + b) * kCB;
+          const int col = (cg * NB + b) * kSubCols;
           uint8_t* sb = st + b * kSubBytes;
           if (a.hint) {
             tma_load_2d_hint(sb, &tm_wg, &full[stage], col, kb * kBK, evict_first);
-            tma_load_2d_hint(sb + kChunkBytes, &tm_wu, &full[stage], col, kb * kBK, evict_first);
+            tma_load_2d_hint(sb + kChunkBytes, hi_map, &full[stage], col + kHiOff, kb * kBK,
+                             evict_first);
           } else {
             tma_load_2d(sb, &tm_wg, &full[stage], col, kb * kBK);
-            tma_load_2d(sb + kChunkBytes, &tm_wu, &full[stage], col, kb * kBK);
+            tma_load_2d(sb + kChunkBytes, hi_map, &full[stage], col + kHiOff, kb * kBK);
           }
         }
         tma_load_2d(st + NB * kSubBytes, &tm_x, &full[stage], kb * kBK, 0);
@@ -270,7 +291,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     const int gu = row >> 6, j = row & 63;
     const int et = threadIdx.x - 64;       // 0..127
     const int64_t Mrow = (int64_t)a.M * kCB;     // floats of one [M][64] partial block
-    constexpr int kGroupCols = NB * kCB;
+    constexpr int kGroupCols = NB * kSubCols;    // output columns of one unit group
     int acc = 0;
     uint32_t acc_phase = 0;
     int64_t t = u0;
@@ -317,8 +338,9 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
       const int tk = *ticket;
       if (tk == n_contrib - 1) {
         __threadfence();
-        // Each thread sums 4 adjacent columns of one row at a time: 16-byte
-        // loads, and the loads of several outputs in flight together.
+        // Each thread sums 4 adjacent output columns of one row at a time:
+        // 16-byte loads, several outputs in flight together.  SwiGLU: gate
+        // and up partials of the same columns; plain: one partial per column.
         const float* pg = a.part + cg * a.maxq * NB * 2 * Mrow;
         constexpr int kChunks = kGroupCols / 4;      // 4-column chunks per row of the group
         const int total = a.M * kChunks;
@@ -333,7 +355,11 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             const int idx = base + i * kEpiThreads;
             const int id = idx < total ? idx : 0;
             const int m = id / kChunks, ch = id - m * kChunks;
-            off[i] = (ch >> 4) * 2 * (int)Mrow + m * kCB + (ch & 15) * 4;
+            // SwiGLU: chunk ch -> sub-block ch/16, gate half; plain: sub-block
+            // ch/32, half (ch/16)&1.  Either way (ch >> 4) picks the [M][64]
+            // partial block in [NB][2] order.
+            const int blk = MODE == kSwiGLU ? (ch >> 4) * 2 : (ch >> 4);
+            off[i] = blk * (int)Mrow + m * kCB + (ch & 15) * 4;
           }
           // slot q holds CTA (c_lo + q)'s sums; adding in q order is k order
 #pragma unroll 2
@@ -343,9 +369,11 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             for (int i = 0; i < kBatch; ++i) {
               if (base + i * kEpiThreads < total) {
                 const float4 pgv = __ldcg(reinterpret_cast<const float4*>(pq + off[i]));
-                const float4 puv = __ldcg(reinterpret_cast<const float4*>(pq + off[i] + Mrow));
                 g[i].x += pgv.x; g[i].y += pgv.y; g[i].z += pgv.z; g[i].w += pgv.w;
-                u[i].x += puv.x; u[i].y += puv.y; u[i].z += puv.z; u[i].w += puv.w;
+                if constexpr (MODE == kSwiGLU) {
+                  const float4 puv = __ldcg(reinterpret_cast<const float4*>(pq + off[i] + Mrow));
+                  u[i].x += puv.x; u[i].y += puv.y; u[i].z += puv.z; u[i].w += puv.w;
+                }
               }
             }
           }
@@ -355,12 +383,22 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             if (idx >= total) continue;
             const int m = idx / kChunks, ch = idx - m * kChunks;
             const int64_t col = cg * kGroupCols + ch * 4;
-            if (col < a.d_ff) {   // d_ff is a multiple of 8: a chunk is all in or all out
-              uint2 o;
-              o.x = pack_bf16x2(silu_fast(g[i].x) * u[i].x, silu_fast(g[i].y) * u[i].y);
-              o.y = pack_bf16x2(silu_fast(g[i].z) * u[i].z, silu_fast(g[i].w) * u[i].w);
-              *reinterpret_cast<uint2*>(a.h + (int64_t)m * a.d_ff + col) = o;
+            if (col >= a.n_out) continue;   // n_out is a multiple of 8: a chunk is all in or out
+            const int64_t o = (int64_t)m * a.n_out + col;
+            uint2 ov;
+            if constexpr (MODE == kSwiGLU) {
+              ov.x = pack_bf16x2(silu_fast(g[i].x) * u[i].x, silu_fast(g[i].y) * u[i].y);
+              ov.y = pack_bf16x2(silu_fast(g[i].z) * u[i].z, silu_fast(g[i].w) * u[i].w);
+            } else {
+              if (a.resid) {
+                const uint2 rv = *reinterpret_cast<const uint2*>(a.resid + o);
+                g[i].x += bf16_lo(rv.x); g[i].y += bf16_hi(rv.x);
+                g[i].z += bf16_lo(rv.y); g[i].w += bf16_hi(rv.y);
+              }
+              ov.x = pack_bf16x2(g[i].x, g[i].y);
+              ov.y = pack_bf16x2(g[i].z, g[i].w);
             }
+            *reinterpret_cast<uint2*>(a.out + o) = ov;
           }
         }
         if (et == 0) a.counters[cg] = 0u;   // ready for the next call
@@ -384,11 +422,11 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
   }
 }
 
-template <int N, int NB>
+template <int N, int NB, int MODE>
 cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mu,
                      const SkArgs& a, cudaStream_t st) {
   using C = SkCfg<N, NB>;
-  auto kern = skinny_tc_kernel<N, NB>;
+  auto kern = skinny_tc_kernel<N, NB, MODE>;
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -412,17 +450,30 @@ cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mg, const CUtenso
   return cudaLaunchKernelEx(&cfg, kern, mx, mg, mu, a);
 }
 
-template <int N>
+template <int N, int MODE>
 cudaError_t launch_nb(int nb, const CUtensorMap& mx, const CUtensorMap& mg,
                       const CUtensorMap& mu, const SkArgs& a, cudaStream_t st) {
   if constexpr (N <= 64) {
-    if (nb == 4) return launch_n<N, 4>(mx, mg, mu, a, st);
+    if (nb == 4) return launch_n<N, 4, MODE>(mx, mg, mu, a, st);
   }
   if constexpr (N <= 128) {
-    if (nb == 2) return launch_n<N, 2>(mx, mg, mu, a, st);
+    if (nb == 2) return launch_n<N, 2, MODE>(mx, mg, mu, a, st);
   }
-  if (nb == 1) return launch_n<N, 1>(mx, mg, mu, a, st);
+  if (nb == 1) return launch_n<N, 1, MODE>(mx, mg, mu, a, st);
   return cudaErrorInvalidValue;
+}
+
+template <int MODE>
+cudaError_t launch_mode(int n_pad, int nb, const CUtensorMap& mx, const CUtensorMap& mg,
+                        const CUtensorMap& mu, const SkArgs& a, cudaStream_t st) {
+  switch (n_pad) {
+    case 16: return launch_nb<16, MODE>(nb, mx, mg, mu, a, st);
+    case 32: return launch_nb<32, MODE>(nb, mx, mg, mu, a, st);
+    case 64: return launch_nb<64, MODE>(nb, mx, mg, mu, a, st);
+    case 128: return launch_nb<128, MODE>(nb, mx, mg, mu, a, st);
+    case 256: return launch_nb<256, MODE>(nb, mx, mg, mu, a, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 int env_int(const char* name, int dflt) {
@@ -432,20 +483,22 @@ int env_int(const char* name, int dflt) {
 
 }  // namespace
 
-SkinnyPlan plan_skinny(int64_t M, int64_t d, int64_t d_ff, int num_sms) {
+SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain) {
   SkinnyPlan p{};
   int n = 16;
   while (n < M) n *= 2;
   p.n_pad = n;
+  p.plain = plain;
   int nb = env_int("SWIGLU_SK_NB", 2);
   if (nb != 1 && nb != 2 && nb != 4) nb = 2;
   while (nb > 1 && nb * n > 256) nb /= 2;
   p.nb = nb;
   p.l2_promo = env_int("SWIGLU_SK_PROMO", 128);
   p.hint = env_int("SWIGLU_SK_HINT", 1);
-  const int64_t cb = (d_ff + kCB - 1) / kCB;
-  p.n_cb = (cb + nb - 1) / nb;
-  p.n_kb = (d + kBK - 1) / kBK;
+  const int64_t sub_cols = plain ? 2 * kCB : kCB;
+  const int64_t subs = (n_out + sub_cols - 1) / sub_cols;
+  p.n_cb = (subs + nb - 1) / nb;
+  p.n_kb = (K + kBK - 1) / kBK;
   p.units = p.n_cb * p.n_kb;
   p.grid = (int)(p.units < num_sms ? p.units : num_sms);
   if (p.grid < 1) p.grid = 1;
@@ -457,23 +510,28 @@ SkinnyPlan plan_skinny(int64_t M, int64_t d, int64_t d_ff, int num_sms) {
   return p;
 }
 
-cudaError_t launch_skinny_tc(const void* x, const void* wg, const void* wu, void* h, int64_t M,
-                             int64_t d, int64_t d_ff, const SkinnyPlan& p, float* part,
-                             unsigned* counters, bool counters_clean, unsigned* status,
-                             uint64_t timeout_ns, cudaStream_t st) {
+cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void* out,
+                             const void* resid, int64_t M, int64_t K, int64_t n_out,
+                             const SkinnyPlan& p, float* part, unsigned* counters,
+                             bool counters_clean, unsigned* status, uint64_t timeout_ns,
+                             cudaStream_t st) {
   if (p.units == 0 || M == 0) return cudaSuccess;
   CUtensorMap mx, mg, mu;
   cudaError_t e;
-  if ((e = make_tmap_bf16_2d(&mx, x, M, d, kBK, p.n_pad)) != cudaSuccess) return e;
-  if ((e = make_tmap_bf16_2d(&mg, wg, d, d_ff, kCB, kBK, p.l2_promo)) != cudaSuccess) return e;
-  if ((e = make_tmap_bf16_2d(&mu, wu, d, d_ff, kCB, kBK, p.l2_promo)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_2d(&mx, x, M, K, kBK, p.n_pad)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_2d(&mg, wa, K, n_out, kCB, kBK, p.l2_promo)) != cudaSuccess) return e;
+  if (p.plain) {
+    mu = mg;
+  } else if ((e = make_tmap_bf16_2d(&mu, wb, K, n_out, kCB, kBK, p.l2_promo)) != cudaSuccess) {
+    return e;
+  }
   // Arrival counters must be zero on entry.
   if (!counters_clean &&
       (e = cudaMemsetAsync(counters, 0, (size_t)p.n_cb * sizeof(unsigned), st)) != cudaSuccess)
     return e;
   SkArgs a;
   a.M = (int)M;
-  a.d_ff = (int)d_ff;
+  a.n_out = (int)n_out;
   a.n_kb = (int)p.n_kb;
   a.maxq = p.maxq;
   a.units = p.units;
@@ -481,17 +539,12 @@ cudaError_t launch_skinny_tc(const void* x, const void* wg, const void* wu, void
   a.hint = p.hint;
   a.part = part;
   a.counters = counters;
-  a.h = (uint16_t*)h;
+  a.out = (uint16_t*)out;
+  a.resid = (const uint16_t*)resid;
   a.status = status;
   a.timeout_ns = timeout_ns;
-  switch (p.n_pad) {
-    case 16: return launch_nb<16>(p.nb, mx, mg, mu, a, st);
-    case 32: return launch_nb<32>(p.nb, mx, mg, mu, a, st);
-    case 64: return launch_nb<64>(p.nb, mx, mg, mu, a, st);
-    case 128: return launch_nb<128>(p.nb, mx, mg, mu, a, st);
-    case 256: return launch_nb<256>(p.nb, mx, mg, mu, a, st);
-    default: return cudaErrorInvalidValue;
-  }
+  return p.plain ? launch_mode<kPlain>(p.n_pad, p.nb, mx, mg, mu, a, st)
+                 : launch_mode<kSwiGLU>(p.n_pad, p.nb, mx, mg, mu, a, st);
 }
 
 }  // namespace swg

@@ -21,6 +21,12 @@
 //     a 128-byte-swizzled staging tile and TMA-stores it.
 // Tiles are visited column-block-major so the CTAs running at the same time
 // share weight columns and x rows through L2.
+//
+// In its plain mode the same kernel computes the down projection
+// y = h . W_down (+ residual) ("1 . Anatomie d'un transformeur sur GPU",
+// section 1.6, kernels #10 and #11): the 256 accumulator columns are 256
+// adjacent output columns, and the epilogue adds the residual and stores
+// them in two 128-column passes.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -46,11 +52,16 @@ constexpr uint32_t kTmemCols = 512;             // two 128 x 256 f32 accumulator
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kStagingBytes + 256;
 
 struct TileArgs {
-  int n_mb, n_nb, n_kb, d_ff;
+  int n_mb, n_nb, n_kb, n_out;   // n_out: output columns
+  int M;
   int64_t tiles;
+  const uint16_t* resid;         // plain mode: [M][n_out] added to the sums, or null
   unsigned* status;
   uint64_t timeout_ns;
 };
+
+constexpr int kSwiGLU = 0;       // accumulator = 128 gate columns | 128 up columns
+constexpr int kPlain = 1;        // accumulator = 256 adjacent output columns
 
 __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, unsigned* status,
                                            uint64_t timeout_ns) {
@@ -58,10 +69,13 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, unsig
   return mbar_wait(bar, parity, &never, status, timeout_ns);
 }
 
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wg,
                const __grid_constant__ CUtensorMap tm_wu, const __grid_constant__ CUtensorMap tm_h,
                const TileArgs a) {
+  // output columns per tile, and where the four 64-column B boxes come from
+  constexpr int kOutCols = MODE == kSwiGLU ? kBN : 2 * kBN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* stages = smem_raw + pad;
@@ -124,10 +138,17 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
           uint8_t* sb = st + kABytes;
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
           tma_load_2d(st, &tm_x, &full[stage], kb * kBK, mb * kBM);
-          tma_load_2d(sb, &tm_wg, &full[stage], nb * kBN, kb * kBK);
-          tma_load_2d(sb + kChunkBytes, &tm_wg, &full[stage], nb * kBN + 64, kb * kBK);
-          tma_load_2d(sb + 2 * kChunkBytes, &tm_wu, &full[stage], nb * kBN, kb * kBK);
-          tma_load_2d(sb + 3 * kChunkBytes, &tm_wu, &full[stage], nb * kBN + 64, kb * kBK);
+          if constexpr (MODE == kSwiGLU) {
+            tma_load_2d(sb, &tm_wg, &full[stage], nb * kBN, kb * kBK);
+            tma_load_2d(sb + kChunkBytes, &tm_wg, &full[stage], nb * kBN + 64, kb * kBK);
+            tma_load_2d(sb + 2 * kChunkBytes, &tm_wu, &full[stage], nb * kBN, kb * kBK);
+            tma_load_2d(sb + 3 * kChunkBytes, &tm_wu, &full[stage], nb * kBN + 64, kb * kBK);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              tma_load_2d(sb + q * kChunkBytes, &tm_wg, &full[stage], nb * kOutCols + 64 * q,
+                          kb * kBK);
+          }
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -195,50 +216,82 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     const int row = quarter * 32 + lane;   // accumulator row = output row in the tile
     const int et = threadIdx.x - 64;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    constexpr int kPasses = MODE == kSwiGLU ? 1 : 2;   // 128 output columns per pass
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < a.tiles; t += gridDim.x) {
+    bool ok = true;
+    for (int64_t t = blockIdx.x; ok && t < a.tiles; t += gridDim.x) {
       const int mb = (int)(t % a.n_mb), nb = (int)(t / a.n_mb);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, a.status, a.timeout_ns)) break;
       tc_fence_after();
-      if (et == 0) bulk_wait_read0();   // the previous tile's store has read the staging tile
-      __syncwarp();
-      named_bar_sync(1, kEpiThreads);
+      const int64_t grow = (int64_t)mb * kBM + row;       // output row of this thread
+      for (int pass = 0; pass < kPasses; ++pass) {
+        if (et == 0) bulk_wait_read0();   // the previous store has read the staging tile
+        __syncwarp();
+        named_bar_sync(1, kEpiThreads);
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t g[32], u[32];
-        const uint32_t col0 = (uint32_t)(acc * 2 * kBN + ch * 32);
-        tmem_ld_x32(tmem + lane_off + col0, g);
-        tmem_ld_x32(tmem + lane_off + col0 + kBN, u);
-        tmem_wait_ld();
-        uint8_t* rowp = staging + (ch >> 1) * kStagingHalf + row * 128;
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t g[32], u[32];
+          const uint32_t col0 = (uint32_t)(acc * 2 * kBN + pass * kBN + ch * 32);
+          tmem_ld_x32(tmem + lane_off + col0, g);
+          if constexpr (MODE == kSwiGLU) tmem_ld_x32(tmem + lane_off + col0 + kBN, u);
+          tmem_wait_ld();
+          float rv[32];
+          if constexpr (MODE == kPlain) {
+            // residual row segment: 32 bf16 of this output row
+            const int64_t c0 = (int64_t)nb * kOutCols + pass * kBN + ch * 32;
+            const bool has = a.resid && grow < a.M && c0 < a.n_out;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 v;
-          uint32_t* w = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int q = 8 * i + 2 * e;
-            w[e] = pack_bf16x2(silu_fast(__uint_as_float(g[q])) * __uint_as_float(u[q]),
-                               silu_fast(__uint_as_float(g[q + 1])) * __uint_as_float(u[q + 1]));
+            for (int v = 0; v < 4; ++v) {
+              uint4 w = make_uint4(0u, 0u, 0u, 0u);
+              if (has && c0 + 8 * v < a.n_out)
+                w = *reinterpret_cast<const uint4*>(a.resid + grow * a.n_out + c0 + 8 * v);
+              rv[8 * v + 0] = bf16_lo(w.x); rv[8 * v + 1] = bf16_hi(w.x);
+              rv[8 * v + 2] = bf16_lo(w.y); rv[8 * v + 3] = bf16_hi(w.y);
+              rv[8 * v + 4] = bf16_lo(w.z); rv[8 * v + 5] = bf16_hi(w.z);
+              rv[8 * v + 6] = bf16_lo(w.w); rv[8 * v + 7] = bf16_hi(w.w);
+            }
           }
-          const int chunk = ((ch & 1) * 4 + i) ^ (row & 7);   // 128-byte swizzle
-          *reinterpret_cast<uint4*>(rowp + chunk * 16) = v;
+          uint8_t* rowp = staging + (ch >> 1) * kStagingHalf + row * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 v;
+            uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int q = 8 * i + 2 * e;
+              float o0, o1;
+              if constexpr (MODE == kSwiGLU) {
+                o0 = silu_fast(__uint_as_float(g[q])) * __uint_as_float(u[q]);
+                o1 = silu_fast(__uint_as_float(g[q + 1])) * __uint_as_float(u[q + 1]);
+              } else {
+                o0 = __uint_as_float(g[q]) + rv[q];
+                o1 = __uint_as_float(g[q + 1]) + rv[q + 1];
+              }
+              w[e] = pack_bf16x2(o0, o1);
+            }
+            const int chunk = ((ch & 1) * 4 + i) ^ (row & 7);   // 128-byte swizzle
+            *reinterpret_cast<uint4*>(rowp + chunk * 16) = v;
+          }
+        }
+        if (pass == kPasses - 1) {
+          // every accumulator column of this buffer has been read
+          tc_fence_before();
+          mbar_arrive(&tempty[acc]);
+        }
+        fence_async_smem();
+        __syncwarp();
+        named_bar_sync(1, kEpiThreads);
+        if (et == 0) {
+          const int c0 = nb * kOutCols + pass * kBN;
+          if (c0 < a.n_out) tma_store_2d(&tm_h, staging, c0, mb * kBM);
+          if (c0 + 64 < a.n_out) tma_store_2d(&tm_h, staging + kStagingHalf, c0 + 64, mb * kBM);
+          bulk_commit();
         }
       }
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
-      }
-      fence_async_smem();
-      __syncwarp();
-      named_bar_sync(1, kEpiThreads);
-      if (et == 0) {
-        tma_store_2d(&tm_h, staging, nb * kBN, mb * kBM);
-        if (nb * kBN + 64 < a.d_ff) tma_store_2d(&tm_h, staging + kStagingHalf, nb * kBN + 64, mb * kBM);
-        bulk_commit();
       }
     }
     if (et == 0) bulk_wait0();
@@ -255,55 +308,72 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 
 }  // namespace
 
-TilePlan plan_tile(int64_t M, int64_t d, int64_t d_ff, int num_sms) {
-  (void)d;
+TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain) {
+  (void)K;
   TilePlan p{};
+  const int64_t cols = plain ? 2 * kBN : kBN;
+  p.plain = plain;
   p.n_mb = (M + kBM - 1) / kBM;
-  p.n_nb = (d_ff + kBN - 1) / kBN;
+  p.n_nb = (n_out + cols - 1) / cols;
   p.tiles = p.n_mb * p.n_nb;
   p.grid = (int)(p.tiles < num_sms ? p.tiles : num_sms);
   if (p.grid < 1) p.grid = 1;
   return p;
 }
 
-cudaError_t launch_tile_tc(const void* x, const void* wg, const void* wu, void* h, int64_t M,
-                           int64_t d, int64_t d_ff, const TilePlan& p, unsigned* status,
-                           uint64_t timeout_ns, cudaStream_t st) {
-  if (p.tiles == 0 || d == 0) return cudaSuccess;
-  CUtensorMap mx, mg, mu, mh;
-  cudaError_t e;
-  if ((e = make_tmap_bf16_2d(&mx, x, M, d, kBK, kBM)) != cudaSuccess) return e;
-  if ((e = make_tmap_bf16_2d(&mg, wg, d, d_ff, 64, kBK)) != cudaSuccess) return e;
-  if ((e = make_tmap_bf16_2d(&mu, wu, d, d_ff, 64, kBK)) != cudaSuccess) return e;
-  if ((e = make_tmap_bf16_2d(&mh, h, M, d_ff, 64, kBM)) != cudaSuccess) return e;
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mu,
+                        const CUtensorMap& mh, const TileArgs& a, int grid, cudaStream_t st) {
+  auto kern = tile_tc_kernel<MODE>;
   static int configured[64] = {0};
   int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
   if (dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(tile_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = 1;
   }
-  TileArgs a;
-  a.n_mb = (int)p.n_mb;
-  a.n_nb = (int)p.n_nb;
-  a.n_kb = (int)((d + kBK - 1) / kBK);
-  a.d_ff = (int)d_ff;
-  a.tiles = p.tiles;
-  a.status = status;
-  a.timeout_ns = timeout_ns;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.grid);
+  cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tile_tc_kernel, mx, mg, mu, mh, a);
+  return cudaLaunchKernelEx(&cfg, kern, mx, mg, mu, mh, a);
+}
+
+cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* out,
+                           const void* resid, int64_t M, int64_t K, int64_t n_out,
+                           const TilePlan& p, unsigned* status, uint64_t timeout_ns,
+                           cudaStream_t st) {
+  if (p.tiles == 0 || K == 0) return cudaSuccess;
+  CUtensorMap mx, mg, mu, mh;
+  cudaError_t e;
+  if ((e = make_tmap_bf16_2d(&mx, x, M, K, kBK, kBM)) != cudaSuccess) return e;
+  if ((e = make_tmap_bf16_2d(&mg, wa, K, n_out, 64, kBK)) != cudaSuccess) return e;
+  if (p.plain) {
+    mu = mg;
+  } else if ((e = make_tmap_bf16_2d(&mu, wb, K, n_out, 64, kBK)) != cudaSuccess) {
+    return e;
+  }
+  if ((e = make_tmap_bf16_2d(&mh, out, M, n_out, 64, kBM)) != cudaSuccess) return e;
+  TileArgs a;
+  a.n_mb = (int)p.n_mb;
+  a.n_nb = (int)p.n_nb;
+  a.n_kb = (int)((K + kBK - 1) / kBK);
+  a.n_out = (int)n_out;
+  a.M = (int)M;
+  a.tiles = p.tiles;
+  a.resid = (const uint16_t*)resid;
+  a.status = status;
+  a.timeout_ns = timeout_ns;
+  return p.plain ? launch_mode<kPlain>(mx, mg, mu, mh, a, p.grid, st)
+                 : launch_mode<kSwiGLU>(mx, mg, mu, mh, a, p.grid, st);
 }
 
 }  // namespace swg
