@@ -419,9 +419,10 @@ def run_ours(args):
                          "isolated_call_us": round(statistics.median(lat) * 1e3, 2),
                          "path": plans[M]["path"]}
 
-    extra = None
+    extra = next_rows = None
     if not args.no_extra:
         extra = other_configs(dev, peaks, l2, args.extra_iters)
+        next_rows = down_and_mlp(dev, peaks, l2, args.extra_iters)
 
     if rank == 0:
         cpu = cpu_baseline()
@@ -459,6 +460,8 @@ def run_ours(args):
         }
         if extra is not None:
             line["other_configs"] = extra
+        if next_rows is not None:
+            line["down_and_mlp"] = next_rows
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -533,6 +536,66 @@ def other_configs(dev, peaks, l2, iters):
             del x, h
         del copies
         torch.cuda.empty_cache()
+    return out
+
+
+def down_and_mlp(dev, peaks, l2, iters):
+    """The down projection y = h.W_down + r and the two-kernel MLP at the
+    decode and prefill shapes of d=4096, d_ff=14336 (back to back)."""
+    import torch
+    import swiglu_mlp_projection_gb300 as swg
+    from swiglu_mlp_projection_gb300 import inputs, workload
+    d, d_ff = D, D_FF
+    _, wd, _ = inputs.make_inputs(1, d_ff, d, "bf16", seed=1)
+    _, wg, wu = inputs.make_inputs(1, d, d_ff, "bf16", seed=0)
+    n_copies = 2
+    wds = [wd.to(dev) for _ in range(n_copies)]
+    wgs = [(wg.to(dev), wu.to(dev)) for _ in range(n_copies)]
+    del wd, wg, wu
+    out = {}
+
+    def timed(fn):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(iters):
+            fn(i)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / iters
+
+    for M in (1, 16, 4096):
+        h = inputs.make_inputs(M, d_ff, 8, "bf16", seed=2, x_only=True)[0].to(dev)
+        x = inputs.make_inputs(M, d, 8, "bf16", seed=3, x_only=True)[0].to(dev)
+        y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+        hb = torch.empty(M, d_ff, dtype=torch.bfloat16, device=dev)
+        ms = timed(lambda i: swg.swiglu_down(h, wds[i % n_copies], residual=x, out=y))
+        by = workload.down_bytes(M, d_ff, d, "bf16")
+        fl = workload.down_flops(M, d_ff, d)
+        e = {"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
+             "TFLOP/s": round(fl / ms / 1e9, 2),
+             "path": swg.down_plan(M, d_ff, d, "bf16", "auto")["path"]}
+        if M <= 16:
+            e["frac_hbm"] = round(by / ms / 1e6 / peaks["hbm_gbs"], 4)
+        else:
+            e["frac_bf16"] = round(fl / ms / 1e9 / peaks["bf16_tflops"], 4)
+        out["down_d4096/M=%d" % M] = e
+        ms = timed(lambda i: swg.swiglu_mlp(x, wgs[i % n_copies][0], wgs[i % n_copies][1],
+                                             wds[i % n_copies], residual=x, h=hb, out=y))
+        by = workload.algorithmic_bytes(M, d, d_ff, "bf16") + workload.down_bytes(M, d_ff, d, "bf16")
+        fl = workload.flops(M, d, d_ff) + workload.down_flops(M, d_ff, d)
+        e = {"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
+             "TFLOP/s": round(fl / ms / 1e9, 2)}
+        if M <= 16:
+            e["frac_hbm"] = round(by / ms / 1e6 / peaks["hbm_gbs"], 4)
+        else:
+            e["frac_bf16"] = round(fl / ms / 1e9 / peaks["bf16_tflops"], 4)
+        out["mlp_d4096/M=%d" % M] = e
+        del h, x, y, hb
+    del wds, wgs
+    torch.cuda.empty_cache()
     return out
 
 

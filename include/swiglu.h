@@ -134,6 +134,24 @@ SWIGLU_API size_t swiglu_down_workspace_bytes(int64_t M, int64_t d_ff, int64_t d
                                               int path);
 
 /*
+ * As swiglu_up_ex and swiglu_down_ex, for weights stored with the shared
+ * dimension contiguous -- the layout of torch.nn.Linear.weight:
+ *     w_gate_nk, w_up_nk [d_ff, d]   (element (j, k) at j*d + k)
+ *     w_down_nk          [d, d_ff]   (element (j, k) at j*d_ff + k)
+ * No copy or transpose is made: the kernels read these weights directly
+ * (the decode article's "TransposedMatmul" point, "Deux operations de trop":
+ * a . b^T without copying b).  bf16 on the tensor-core paths only;
+ * SWIGLU_PATH_SIMT and f32 return SWIGLU_ERR_UNSUPPORTED.  Workspace sizes
+ * are those of the [K, N] entry points.
+ */
+SWIGLU_API int swiglu_up_nk(const void* x, const void* w_gate_nk, const void* w_up_nk, void* h,
+                            int64_t M, int64_t d, int64_t d_ff, int dtype, int path,
+                            void* workspace, size_t workspace_bytes, void* stream);
+SWIGLU_API int swiglu_down_nk(const void* h, const void* w_down_nk, const void* residual, void* y,
+                              int64_t M, int64_t d_ff, int64_t d, int dtype, int path,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * The whole MLP of "1 . Anatomie d'un transformeur sur GPU", section 1.1,
  * after its RMSNorm: h = silu(x . W_gate) (.) (x . W_up), then
  * y = h . W_down (+ residual).  Two kernels on `stream`; h [M, d_ff] is the

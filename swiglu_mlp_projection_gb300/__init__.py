@@ -45,11 +45,13 @@ def _raw_stream(index):
     return torch.cuda.current_stream(index).cuda_stream
 
 
-def swiglu_up(x, w_gate, w_up, out=None, path="auto", workspace=None, stream=None):
+def swiglu_up(x, w_gate, w_up, out=None, path="auto", workspace=None, stream=None,
+              layout="kn"):
     """h = silu(x @ w_gate) * (x @ w_up) on x's CUDA device.
 
-    x [M, d], w_gate / w_up [d, d_ff]: contiguous CUDA tensors of one dtype
-    (bfloat16 or float32).  ``out`` [M, d_ff] is written if given (else
+    x [M, d], w_gate / w_up [d, d_ff] (layout "kn") or [d_ff, d] (layout "nk",
+    the torch.nn.Linear.weight layout; then h = silu(x @ w_gate.T) * ...):
+    contiguous CUDA tensors of one dtype (bfloat16 or float32).  ``out`` [M, d_ff] is written if given (else
     allocated).  ``path`` forces a kernel path ("simt", "skinny", "tc");
     ``workspace`` is an optional uint8 CUDA tensor for split-K partial sums.
     The call is asynchronous on ``stream`` (a torch.cuda.Stream; default:
@@ -62,11 +64,14 @@ def swiglu_up(x, w_gate, w_up, out=None, path="auto", workspace=None, stream=Non
     if not (x.is_contiguous() and w_gate.is_contiguous() and w_up.is_contiguous()):
         raise ValueError("x, w_gate and w_up must be contiguous")
     if x.dim() != 2 or w_gate.dim() != 2 or w_up.shape != w_gate.shape:
-        raise ValueError("expected x [M, d] and w_gate, w_up [d, d_ff]")
+        raise ValueError("expected x [M, d] and w_gate, w_up [d, d_ff] or [d_ff, d]")
+    if layout not in ("kn", "nk"):
+        raise ValueError("layout must be 'kn' or 'nk'")
     M, d = x.shape
-    if w_gate.shape[0] != d:
-        raise ValueError("x has d=%d but w_gate has %d rows" % (d, w_gate.shape[0]))
-    d_ff = w_gate.shape[1]
+    kdim = 0 if layout == "kn" else 1
+    if w_gate.shape[kdim] != d:
+        raise ValueError("x has d=%d but w_gate is %s (layout %s)" % (d, tuple(w_gate.shape), layout))
+    d_ff = w_gate.shape[1 - kdim]
     dt = _dtype_code(x)
     if w_gate.dtype != x.dtype or w_up.dtype != x.dtype:
         raise TypeError("x, w_gate and w_up must share one dtype")
@@ -83,11 +88,12 @@ def swiglu_up(x, w_gate, w_up, out=None, path="auto", workspace=None, stream=Non
         _LIB = _lib.load()
     args = (x.data_ptr(), w_gate.data_ptr(), w_up.data_ptr(), out.data_ptr(), M, d, d_ff, dt,
             _path_code(path), ws_ptr, ws_bytes, st)
+    fn = _LIB.swiglu_up_ex if layout == "kn" else _LIB.swiglu_up_nk
     if torch.cuda.current_device() != index:
         with torch.cuda.device(index):
-            status = _LIB.swiglu_up_ex(*args)
+            status = fn(*args)
     else:
-        status = _LIB.swiglu_up_ex(*args)
+        status = fn(*args)
     if status:
         _lib.check(status)
     return out
@@ -103,19 +109,24 @@ def _check_cuda(**tensors):
             raise ValueError("%s must be contiguous" % name)
 
 
-def swiglu_down(h, w_down, residual=None, out=None, path="auto", workspace=None, stream=None):
+def swiglu_down(h, w_down, residual=None, out=None, path="auto", workspace=None, stream=None,
+                layout="kn"):
     """y = h @ w_down (+ residual): the MLP's down projection.
 
-    h [M, d_ff], w_down [d_ff, d], residual [M, d] (or None; may be ``out``):
+    h [M, d_ff], w_down [d_ff, d] (layout "kn") or [d, d_ff] (layout "nk",
+    torch.nn.Linear.weight), residual [M, d] (or None; may be ``out``):
     contiguous bfloat16 CUDA tensors.  Returns y [M, d] (``out`` if given).
     """
     global _LIB
     import torch
     _check_cuda(h=h, w_down=w_down, residual=residual)
-    if h.dim() != 2 or w_down.dim() != 2 or w_down.shape[0] != h.shape[1]:
-        raise ValueError("expected h [M, d_ff] and w_down [d_ff, d]")
+    if layout not in ("kn", "nk"):
+        raise ValueError("layout must be 'kn' or 'nk'")
+    kdim = 0 if layout == "kn" else 1
+    if h.dim() != 2 or w_down.dim() != 2 or w_down.shape[kdim] != h.shape[1]:
+        raise ValueError("expected h [M, d_ff] and w_down [d_ff, d] (kn) or [d, d_ff] (nk)")
     M, d_ff = h.shape
-    d = w_down.shape[1]
+    d = w_down.shape[1 - kdim]
     dt = _dtype_code(h)
     if w_down.dtype != h.dtype or (residual is not None and residual.dtype != h.dtype):
         raise TypeError("h, w_down and residual must share one dtype")
@@ -134,11 +145,12 @@ def swiglu_down(h, w_down, residual=None, out=None, path="auto", workspace=None,
         _LIB = _lib.load()
     args = (h.data_ptr(), w_down.data_ptr(), residual.data_ptr() if residual is not None else None,
             out.data_ptr(), M, d_ff, d, dt, _path_code(path), ws_ptr, ws_bytes, st)
+    fn = _LIB.swiglu_down_ex if layout == "kn" else _LIB.swiglu_down_nk
     if torch.cuda.current_device() != index:
         with torch.cuda.device(index):
-            status = _LIB.swiglu_down_ex(*args)
+            status = fn(*args)
     else:
-        status = _LIB.swiglu_down_ex(*args)
+        status = fn(*args)
     if status:
         _lib.check(status)
     return out

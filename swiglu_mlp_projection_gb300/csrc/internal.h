@@ -72,11 +72,13 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
 // x.wa (+ resid) (plain: wa = W_down, wb unused).  `counters`: n_cb arrival
 // counters, zero on entry when `counters_clean` (left so by the previous call
 // on the same stream), else cleared first.
+// w_kmajor: weights stored [n_out, K] (K contiguous, torch.nn.Linear.weight)
+// instead of [K, n_out].
 cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void* out,
                              const void* resid, int64_t M, int64_t K, int64_t n_out,
-                             const SkinnyPlan& p, float* part, unsigned* counters,
-                             bool counters_clean, unsigned* status, uint64_t timeout_ns,
-                             cudaStream_t st);
+                             bool w_kmajor, const SkinnyPlan& p, float* part,
+                             unsigned* counters, bool counters_clean, unsigned* status,
+                             uint64_t timeout_ns, cudaStream_t st);
 constexpr size_t kStreamCounterBytes = 64 * 1024;   // per-stream arrival counters
 
 // Tile tensor-core path (bf16, large M): 128-row output tiles.  SwiGLU:
@@ -91,7 +93,7 @@ struct TilePlan {
 TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain);
 cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* out,
                            const void* resid, int64_t M, int64_t K, int64_t n_out,
-                           const TilePlan& p, unsigned* status, uint64_t timeout_ns,
-                           cudaStream_t st);
+                           bool w_kmajor, const TilePlan& p, unsigned* status,
+                           uint64_t timeout_ns, cudaStream_t st);
 
 }  // namespace swg

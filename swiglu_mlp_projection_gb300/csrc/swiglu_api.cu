@@ -350,6 +350,7 @@ struct Call {
   void* workspace;
   size_t ws_bytes;
   cudaStream_t st;
+  bool kmajor;   // weights stored [n_out, K] (torch.nn.Linear.weight) instead of [K, n_out]
 };
 
 int run(const Call& c) {
@@ -360,6 +361,9 @@ int run(const Call& c) {
   Plan p;
   if ((v = make_plan(c.op, c.M, c.K, c.n_out, c.dtype, c.path, di.num_sms, &p)) != SWIGLU_OK)
     return v;
+  if (c.kmajor && p.path == SWIGLU_PATH_SIMT && c.K > 0)
+    return fail(SWIGLU_ERR_UNSUPPORTED,
+                "[N, K] weights are served by the tensor-core paths (bf16) only");
   if (c.M == 0 || c.n_out == 0) {
     t_err[0] = 0;
     return SWIGLU_OK;
@@ -424,11 +428,11 @@ int run(const Call& c) {
     if (e == cudaSuccess)
       e = launch_reduce_swiglu(part, c.out, c.M, c.n_out, p.slices, c.dtype, di.num_sms, st);
   } else if (p.path == SWIGLU_PATH_SKINNY) {
-    e = launch_skinny_tc(c.x, c.wa, c.wb, c.out, c.resid, c.M, c.K, c.n_out, p.skinny, part,
-                         counters, counters_clean, di.status, wait_timeout_ns(), st);
+    e = launch_skinny_tc(c.x, c.wa, c.wb, c.out, c.resid, c.M, c.K, c.n_out, c.kmajor, p.skinny,
+                         part, counters, counters_clean, di.status, wait_timeout_ns(), st);
   } else {
-    e = launch_tile_tc(c.x, c.wa, c.wb, c.out, c.resid, c.M, c.K, c.n_out, p.tile, di.status,
-                       wait_timeout_ns(), st);
+    e = launch_tile_tc(c.x, c.wa, c.wb, c.out, c.resid, c.M, c.K, c.n_out, c.kmajor, p.tile,
+                       di.status, wait_timeout_ns(), st);
   }
   if (pooled) {
     cudaError_t ef = cudaFreeAsync(pooled, st);
@@ -441,18 +445,20 @@ int run(const Call& c) {
 
 int run_up(const void* x, const void* wg, const void* wu, void* h, int64_t M, int64_t d,
            int64_t d_ff, int dtype, int path, void* workspace, size_t ws_bytes,
-           cudaStream_t st) {
+           cudaStream_t st, bool kmajor = false) {
   int v = validate(x, wg, wu, h, M, d, d_ff, dtype);
   if (v != SWIGLU_OK) return v;
-  return run(Call{kOpUp, x, wg, wu, nullptr, h, M, d, d_ff, dtype, path, workspace, ws_bytes, st});
+  return run(Call{kOpUp, x, wg, wu, nullptr, h, M, d, d_ff, dtype, path, workspace, ws_bytes, st,
+                  kmajor});
 }
 
 int run_down(const void* h, const void* wd, const void* r, void* y, int64_t M, int64_t d_ff,
              int64_t d, int dtype, int path, void* workspace, size_t ws_bytes,
-             cudaStream_t st) {
+             cudaStream_t st, bool kmajor = false) {
   int v = validate_down(h, wd, r, y, M, d_ff, d, dtype);
   if (v != SWIGLU_OK) return v;
-  return run(Call{kOpDown, h, wd, wd, r, y, M, d_ff, d, dtype, path, workspace, ws_bytes, st});
+  return run(Call{kOpDown, h, wd, wd, r, y, M, d_ff, d, dtype, path, workspace, ws_bytes, st,
+                  kmajor});
 }
 
 }  // namespace
@@ -522,6 +528,20 @@ int swiglu_down_ex(const void* h, const void* w_down, const void* residual, void
                    size_t workspace_bytes, void* stream) {
   return run_down(h, w_down, residual, y, M, d_ff, d, dtype, path, workspace, workspace_bytes,
                   (cudaStream_t)stream);
+}
+
+int swiglu_up_nk(const void* x, const void* w_gate_nk, const void* w_up_nk, void* h, int64_t M,
+                 int64_t d, int64_t d_ff, int dtype, int path, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  return run_up(x, w_gate_nk, w_up_nk, h, M, d, d_ff, dtype, path, workspace, workspace_bytes,
+                (cudaStream_t)stream, true);
+}
+
+int swiglu_down_nk(const void* h, const void* w_down_nk, const void* residual, void* y,
+                   int64_t M, int64_t d_ff, int64_t d, int dtype, int path, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  return run_down(h, w_down_nk, residual, y, M, d_ff, d, dtype, path, workspace,
+                  workspace_bytes, (cudaStream_t)stream, true);
 }
 
 int swiglu_mlp(const void* x, const void* w_gate, const void* w_up, const void* w_down,

@@ -84,6 +84,7 @@ struct SkArgs {
   int64_t units;
   int grid;
   int hint;             // 1: weight loads carry an L2 evict_first hint
+  int kmajor;           // weights stored [n_out, K] (K contiguous) instead of [K, n_out]
   float* part;          // [n_cg][maxq][NB][2][M][64]
   unsigned* counters;   // [n_cg], zero on entry, zero again on exit
   uint16_t* out;        // [M][n_out] bf16
@@ -173,8 +174,13 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         const int col = (cg * NB + b) * kSubCols;
-        tma_prefetch_l2_2d(&tm_wg, col, kb * kBK);
-        tma_prefetch_l2_2d(hi_map, col + kHiOff, kb * kBK);
+        if (a.kmajor) {
+          tma_prefetch_l2_2d(&tm_wg, kb * kBK, col);
+          tma_prefetch_l2_2d(hi_map, kb * kBK, col + kHiOff);
+        } else {
+          tma_prefetch_l2_2d(&tm_wg, col, kb * kBK);
+          tma_prefetch_l2_2d(hi_map, col + kHiOff, kb * kBK);
+        }
       }
     }
   }
@@ -201,13 +207,15 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         for (int b = 0; b < NB; ++b) {
           const int col = (cg * NB + b) * kSubCols;
           uint8_t* sb = st + b * kSubBytes;
+          // [K, n_out] weights: box (col, k); [n_out, K] weights: box (k, col).
+          const int c0 = a.kmajor ? kb * kBK : col, c1 = a.kmajor ? col : kb * kBK;
+          const int h0 = a.kmajor ? kb * kBK : col + kHiOff, h1 = a.kmajor ? col + kHiOff : kb * kBK;
           if (a.hint) {
-            tma_load_2d_hint(sb, &tm_wg, &full[stage], col, kb * kBK, evict_first);
-            tma_load_2d_hint(sb + kChunkBytes, hi_map, &full[stage], col + kHiOff, kb * kBK,
-                             evict_first);
+            tma_load_2d_hint(sb, &tm_wg, &full[stage], c0, c1, evict_first);
+            tma_load_2d_hint(sb + kChunkBytes, hi_map, &full[stage], h0, h1, evict_first);
           } else {
-            tma_load_2d(sb, &tm_wg, &full[stage], col, kb * kBK);
-            tma_load_2d(sb + kChunkBytes, hi_map, &full[stage], col + kHiOff, kb * kBK);
+            tma_load_2d(sb, &tm_wg, &full[stage], c0, c1);
+            tma_load_2d(sb + kChunkBytes, hi_map, &full[stage], h0, h1);
           }
         }
         tma_load_2d(st + NB * kSubBytes, &tm_x, &full[stage], kb * kBK, 0);
@@ -229,7 +237,15 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, N, /*a_mn=*/true, /*b_mn=*/false);
+      // A (the weight tile) is MN-major for [K, n_out] weights, K-major for
+      // [n_out, K] weights; B (x^T) is always K-major.
+      const uint32_t idesc = a.kmajor ? idesc_bf16_f32(128, N, false, false)
+                                      : idesc_bf16_f32(128, N, true, false);
+      // per 16-deep k step: MN-major tiles advance 16 rows of 128 bytes (two
+      // swizzle atoms; the two 64-column boxes are kChunkBytes apart), K-major
+      // tiles 32 bytes along their 128-byte rows (8-row groups 1024 B apart).
+      const uint32_t a_step = a.kmajor ? 32u : 2048u;
+      const uint32_t a_lbo = a.kmajor ? 16u : kChunkBytes;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -260,7 +276,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
               // A: 16 k-rows further down the MN-major tile (2 swizzle atoms);
               // B: 32 bytes further along the K-major 128-byte rows.
               const uint64_t ad =
-                  smem_desc_sw128(s_addr + b * kSubBytes + kk * 2048u, kChunkBytes, 1024u);
+                  smem_desc_sw128(s_addr + b * kSubBytes + kk * a_step, a_lbo, 1024u);
               const uint64_t bd = smem_desc_sw128(b_addr + kk * 32u, 16u, 1024u);
               mma_bf16(d_tmem, ad, bd, idesc, (tt != t || kk != 0) ? 1u : 0u);
             }
@@ -512,17 +528,19 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
 
 cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void* out,
                              const void* resid, int64_t M, int64_t K, int64_t n_out,
-                             const SkinnyPlan& p, float* part, unsigned* counters,
-                             bool counters_clean, unsigned* status, uint64_t timeout_ns,
-                             cudaStream_t st) {
+                             bool w_kmajor, const SkinnyPlan& p, float* part,
+                             unsigned* counters, bool counters_clean, unsigned* status,
+                             uint64_t timeout_ns, cudaStream_t st) {
   if (p.units == 0 || M == 0) return cudaSuccess;
   CUtensorMap mx, mg, mu;
   cudaError_t e;
   if ((e = make_tmap_bf16_2d(&mx, x, M, K, kBK, p.n_pad)) != cudaSuccess) return e;
-  if ((e = make_tmap_bf16_2d(&mg, wa, K, n_out, kCB, kBK, p.l2_promo)) != cudaSuccess) return e;
+  // weights as [K, n_out] (boxes 64 columns x 64 k) or [n_out, K] (64 k x 64 rows)
+  const int64_t wr = w_kmajor ? n_out : K, wc = w_kmajor ? K : n_out;
+  if ((e = make_tmap_bf16_2d(&mg, wa, wr, wc, 64, 64, p.l2_promo)) != cudaSuccess) return e;
   if (p.plain) {
     mu = mg;
-  } else if ((e = make_tmap_bf16_2d(&mu, wb, K, n_out, kCB, kBK, p.l2_promo)) != cudaSuccess) {
+  } else if ((e = make_tmap_bf16_2d(&mu, wb, wr, wc, 64, 64, p.l2_promo)) != cudaSuccess) {
     return e;
   }
   // Arrival counters must be zero on entry.
@@ -537,6 +555,7 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   a.units = p.units;
   a.grid = p.grid;
   a.hint = p.hint;
+  a.kmajor = w_kmajor ? 1 : 0;
   a.part = part;
   a.counters = counters;
   a.out = (uint16_t*)out;

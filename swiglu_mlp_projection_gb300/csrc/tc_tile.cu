@@ -56,6 +56,7 @@ struct TileArgs {
   int M;
   int64_t tiles;
   const uint16_t* resid;         // plain mode: [M][n_out] added to the sums, or null
+  int kmajor;                    // weights stored [n_out, K] instead of [K, n_out]
   unsigned* status;
   uint64_t timeout_ns;
 };
@@ -138,16 +139,16 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
           uint8_t* sb = st + kABytes;
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
           tma_load_2d(st, &tm_x, &full[stage], kb * kBK, mb * kBM);
-          if constexpr (MODE == kSwiGLU) {
-            tma_load_2d(sb, &tm_wg, &full[stage], nb * kBN, kb * kBK);
-            tma_load_2d(sb + kChunkBytes, &tm_wg, &full[stage], nb * kBN + 64, kb * kBK);
-            tma_load_2d(sb + 2 * kChunkBytes, &tm_wu, &full[stage], nb * kBN, kb * kBK);
-            tma_load_2d(sb + 3 * kChunkBytes, &tm_wu, &full[stage], nb * kBN + 64, kb * kBK);
-          } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              tma_load_2d(sb + q * kChunkBytes, &tm_wg, &full[stage], nb * kOutCols + 64 * q,
-                          kb * kBK);
+          for (int q = 0; q < 4; ++q) {
+            // box q of the B tile: SwiGLU -> gate 0-63, gate 64-127, up 0-63,
+            // up 64-127 of this tile's columns; plain -> 4 x 64 adjacent columns
+            const CUtensorMap* m = (MODE == kSwiGLU && q >= 2) ? &tm_wu : &tm_wg;
+            const int col = MODE == kSwiGLU ? nb * kBN + 64 * (q & 1) : nb * kOutCols + 64 * q;
+            if (a.kmajor)
+              tma_load_2d(sb + q * kChunkBytes, m, &full[stage], kb * kBK, col);
+            else
+              tma_load_2d(sb + q * kChunkBytes, m, &full[stage], col, kb * kBK);
           }
           ++issued;
           if (++stage == kStages) {
@@ -166,7 +167,12 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, 2 * kBN, /*a_mn=*/false, /*b_mn=*/true);
+      // A (x) is K-major; B (the weights) MN-major for [K, n_out] weights,
+      // K-major for [n_out, K] weights.
+      const uint32_t idesc = a.kmajor ? idesc_bf16_f32(kBM, 2 * kBN, false, false)
+                                      : idesc_bf16_f32(kBM, 2 * kBN, false, true);
+      const uint32_t b_step = a.kmajor ? 32u : 2048u;
+      const uint32_t b_lbo = a.kmajor ? 16u : kChunkBytes;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -190,7 +196,7 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = smem_desc_sw128(a_addr + kk * 32u, 16u, 1024u);
-            const uint64_t bd = smem_desc_sw128(b_addr + kk * 2048u, kChunkBytes, 1024u);
+            const uint64_t bd = smem_desc_sw128(b_addr + kk * b_step, b_lbo, 1024u);
             mma_bf16(d_tmem, ad, bd, idesc, (kb != 0 || kk != 0) ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
@@ -349,16 +355,17 @@ cudaError_t launch_mode(const CUtensorMap& mx, const CUtensorMap& mg, const CUte
 
 cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* out,
                            const void* resid, int64_t M, int64_t K, int64_t n_out,
-                           const TilePlan& p, unsigned* status, uint64_t timeout_ns,
-                           cudaStream_t st) {
+                           bool w_kmajor, const TilePlan& p, unsigned* status,
+                           uint64_t timeout_ns, cudaStream_t st) {
   if (p.tiles == 0 || K == 0) return cudaSuccess;
   CUtensorMap mx, mg, mu, mh;
   cudaError_t e;
   if ((e = make_tmap_bf16_2d(&mx, x, M, K, kBK, kBM)) != cudaSuccess) return e;
-  if ((e = make_tmap_bf16_2d(&mg, wa, K, n_out, 64, kBK)) != cudaSuccess) return e;
+  const int64_t wr = w_kmajor ? n_out : K, wc = w_kmajor ? K : n_out;
+  if ((e = make_tmap_bf16_2d(&mg, wa, wr, wc, 64, 64)) != cudaSuccess) return e;
   if (p.plain) {
     mu = mg;
-  } else if ((e = make_tmap_bf16_2d(&mu, wb, K, n_out, 64, kBK)) != cudaSuccess) {
+  } else if ((e = make_tmap_bf16_2d(&mu, wb, wr, wc, 64, 64)) != cudaSuccess) {
     return e;
   }
   if ((e = make_tmap_bf16_2d(&mh, out, M, n_out, 64, kBM)) != cudaSuccess) return e;
@@ -370,6 +377,7 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
   a.M = (int)M;
   a.tiles = p.tiles;
   a.resid = (const uint16_t*)resid;
+  a.kmajor = w_kmajor ? 1 : 0;
   a.status = status;
   a.timeout_ns = timeout_ns;
   return p.plain ? launch_mode<kPlain>(mx, mg, mu, mh, a, p.grid, st)

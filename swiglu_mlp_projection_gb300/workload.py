@@ -27,6 +27,17 @@ def algorithmic_bytes(M, d, d_ff, dtype):
     return e * (2 * d * d_ff + M * d + M * d_ff)
 
 
+def down_flops(M, d_ff, d):
+    """FLOP of the down projection: 2 M d_ff d (the residual add is not counted)."""
+    return 2 * M * d_ff * d
+
+
+def down_bytes(M, d_ff, d, dtype, residual=True):
+    """W_down and h read once, the residual read once, y written once."""
+    e = ELEM_BYTES[dtype]
+    return e * (d_ff * d + M * d_ff + M * d * (2 if residual else 1))
+
+
 def arithmetic_intensity(M, d, d_ff, dtype):
     return flops(M, d, d_ff) / algorithmic_bytes(M, d, d_ff, dtype)
 
