@@ -10,6 +10,7 @@
 // g and u exist only as f32 partials and are combined only once complete.
 #include "common.cuh"
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace swg {
 
@@ -21,6 +22,11 @@ template <bool BF16>
 __global__ void __launch_bounds__(kThreads)
 reduce_swiglu_kernel(const float* __restrict__ part, void* __restrict__ h,
                      int64_t M, int64_t d_ff, int slices) {
+  // Launched with programmatic stream serialisation behind the partial-sum
+  // kernel: its launch overlaps that kernel, and it reads the partial sums
+  // only once that kernel has finished and its writes are visible.
+  tc::pdl_wait();
+  tc::pdl_launch_dependents();
   // One thread = 4 adjacent outputs of one row (d_ff is a multiple of 4).
   const int64_t groups = d_ff >> 2;
   const int64_t total = M * groups;
@@ -62,10 +68,15 @@ cudaError_t launch_reduce_swiglu(const float* part, void* h, int64_t M,
   int64_t blocks = (total + kThreads - 1) / kThreads;
   const int64_t cap = (int64_t)num_sms * 16;
   if (blocks > cap) blocks = cap;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(kThreads);
   cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (dtype == 1)
     return cudaLaunchKernelEx(&cfg, reduce_swiglu_kernel<true>, part, h, M, d_ff, (int)slices);
   return cudaLaunchKernelEx(&cfg, reduce_swiglu_kernel<false>, part, h, M, d_ff, (int)slices);

@@ -20,6 +20,7 @@
 // serve bf16 by default.
 #include "common.cuh"
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace swg {
 
@@ -64,6 +65,11 @@ simt_partial_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
   const int kn = k1 - k0;
   const int col = blockIdx.x * C + lane * VEC;
   const bool valid = col < d_ff;
+  // Launched with programmatic stream serialisation: wait for the previous
+  // kernel before touching x or the partial-sum buffer, then let the
+  // reduction kernel be scheduled.
+  tc::pdl_wait();
+  tc::pdl_launch_dependents();
 
   // Stage x[row0 : row0+RC, k0 : k1] in shared memory as f32 (rows past M are 0).
   for (int t = threadIdx.x; t < RC * kn; t += kThreads) {
@@ -168,11 +174,16 @@ cudaError_t launch_one(const void* x, const void* wg, const void* wu, float* par
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = 1;
   }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.col_blocks, (unsigned)p.slices, (unsigned)p.row_chunks);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, x, wg, wu, part, (int)M, (int)d, (int)d_ff,
                             (int)p.k_per_slice);
 }

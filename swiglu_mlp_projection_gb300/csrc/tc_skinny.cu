@@ -55,7 +55,7 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kChunkBytes = kCB * kBK * 2;       // one 64 x 64 bf16 weight box
 constexpr uint32_t kSubBytes = 2 * kChunkBytes;       // gate box + up box = one MMA A tile
-constexpr int kPrefetchUnits = 16;                    // units prefetched into L2 before the wait
+constexpr uint32_t kPrefetchBytes = 512u * 1024u;     // weight bytes per CTA prefetched before the wait
 constexpr uint32_t kRingBudget = 200u * 1024u;        // shared memory for the stage ring
 
 constexpr uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
@@ -85,6 +85,7 @@ struct SkArgs {
   int grid;
   int hint;             // 1: weight loads carry an L2 evict_first hint
   int kmajor;           // weights stored [n_out, K] (K contiguous) instead of [K, n_out]
+  int prefetch_units;   // units each CTA prefetches into L2 before the dependency wait
   float* part;          // [n_cg][maxq][NB][2][M][64]
   unsigned* counters;   // [n_cg], zero on entry, zero again on exit
   uint16_t* out;        // [M][n_out] bf16
@@ -168,7 +169,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
   // the wait on, the kernel reads x and the workspace, which the previous
   // kernel may still be writing.
   if (warp == 0 && lane == 0) {
-    const int64_t pend = min(u1, u0 + (int64_t)kPrefetchUnits);
+    const int64_t pend = min(u1, u0 + (int64_t)a.prefetch_units);
     for (int64_t t = u0; t < pend; ++t) {
       const int cg = (int)(t / a.n_kb), kb = (int)(t - (int64_t)cg * a.n_kb);
 #pragma unroll
@@ -511,6 +512,13 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   p.nb = nb;
   p.l2_promo = env_int("SWIGLU_SK_PROMO", 128);
   p.hint = env_int("SWIGLU_SK_HINT", 1);
+  // L2 prefetch budget per CTA (measured): 512 KB for SwiGLU; 256 KB for the
+  // down projection, whose column groups collect ~10 partial sums each (K is
+  // long), so the previous call's final reductions run longer and a larger
+  // prefetch slows them (512 KB measured ~5 % slower, none ~13 % slower).
+  const uint32_t pf_bytes = plain ? kPrefetchBytes / 2 : kPrefetchBytes;
+  p.prefetch_units = env_int("SWIGLU_SK_PREFETCH_UNITS",
+                             (int)(pf_bytes / ((uint32_t)nb * kSubBytes)));
   const int64_t sub_cols = plain ? 2 * kCB : kCB;
   const int64_t subs = (n_out + sub_cols - 1) / sub_cols;
   p.n_cb = (subs + nb - 1) / nb;
@@ -556,6 +564,7 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   a.grid = p.grid;
   a.hint = p.hint;
   a.kmajor = w_kmajor ? 1 : 0;
+  a.prefetch_units = p.prefetch_units;
   a.part = part;
   a.counters = counters;
   a.out = (uint16_t*)out;
