@@ -59,6 +59,7 @@ struct SkinnyPlan {
   int hint;                // weight-load L2 hint: 0 none, 1 evict_first
   bool plain;              // plain epilogue (down projection) instead of SwiGLU
   int prefetch_units;      // units each CTA prefetches into L2 before its dependency wait
+  int cluster;             // cluster mode: CTAs per column group (0: stream-K)
   int64_t n_cb, n_kb;      // units: (nb x 64)-column groups, 64-deep k blocks
   int64_t units;           // n_cb * n_kb
   int grid;                // CTAs (<= SM count)

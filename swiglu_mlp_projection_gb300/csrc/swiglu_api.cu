@@ -323,7 +323,8 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
     p->launches = p->slices > 0 ? 2 : 1;
   } else if (rp == SWIGLU_PATH_SKINNY) {
     p->skinny = plan_skinny(M, K, n_out, num_sms, plain);
-    p->slices = p->skinny.maxq;
+    // K slices per column group: the cluster size, or (stream-K) at most maxq
+    p->slices = p->skinny.cluster ? p->skinny.cluster : p->skinny.maxq;
     p->grid = p->skinny.grid;
     p->workspace = p->skinny.counters_bytes + p->skinny.part_bytes;
     p->launches = 1;

@@ -28,6 +28,16 @@
 //     the partials in contributor order -- i.e. in k order -- applies
 //     silu(g) * u and stores h as bf16.
 //
+// Cluster mode, for problems with few column groups (at most half as many as
+// SMs, e.g. d = 896, d_ff = 4864): each column group is one thread-block
+// cluster of S CTAs that split K evenly.  Every CTA stages its finished
+// accumulator in its own shared memory; after a cluster barrier the CTA of
+// rank 0 reads the S partial sums through distributed shared memory, adds them
+// in rank order (= k order, so the result is reproducible), applies the
+// epilogue and stores.  No global workspace, no counters, no memset: the
+// reduction never leaves the chip, which shortens the per-call critical path
+// that dominates such small calls.
+//
 // The same kernel serves the down projection y = h . W_down (+ residual)
 // ("1 . Anatomie d'un transformeur sur GPU", section 1.6, kernels #10 and
 // #11) in its plain epilogue mode: an MMA tile then holds 128 adjacent W_down
@@ -76,6 +86,8 @@ struct SkCfg {
   static constexpr uint32_t kTmemCols = pow2_at_least(2 * kAccCols, 32);
   static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 256;
   static_assert(2 * kAccCols <= 512, "accumulators exceed TMEM");
+  // cluster mode stages one accumulator (NB x N x 128 f32) in the idle ring
+  static_assert((size_t)NB * N * 128 * 4 <= (size_t)kStages * kStageBytes, "ring too small");
   static_assert(kStages >= 2, "stage too large");
 };
 
@@ -86,6 +98,7 @@ struct SkArgs {
   int hint;             // 1: weight loads carry an L2 evict_first hint
   int kmajor;           // weights stored [n_out, K] (K contiguous) instead of [K, n_out]
   int prefetch_units;   // units each CTA prefetches into L2 before the dependency wait
+  int cluster;          // cluster mode: CTAs per column group (0: stream-K mode)
   float* part;          // [n_cg][maxq][NB][2][M][64]
   unsigned* counters;   // [n_cg], zero on entry, zero again on exit
   uint16_t* out;        // [M][n_out] bf16
@@ -137,7 +150,17 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t U = a.units, G = a.grid, c = blockIdx.x;
-  const int64_t u0 = c * U / G, u1 = (c + 1) * U / G;
+  // Stream-K mode: an even share of the (group, k-block) units.  Cluster mode:
+  // CTA rank r of cluster g takes k-blocks [r n_kb / S, (r+1) n_kb / S) of
+  // column group g (S <= n_kb, so every CTA has at least one).
+  int64_t u0 = c * U / G, u1 = (c + 1) * U / G;
+  const int S = a.cluster;
+  const int64_t cgroup = S ? c / S : 0;
+  const int crank = S ? (int)(c % S) : 0;
+  if (S) {
+    u0 = cgroup * a.n_kb + (int64_t)crank * a.n_kb / S;
+    u1 = cgroup * a.n_kb + (int64_t)(crank + 1) * a.n_kb / S;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -301,6 +324,30 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
       wait_drain(drain, 0, a.status, a.timeout_ns);
     }
     __syncwarp();
+  } else if (S) {
+    // ---------------- cluster mode: stage this CTA's sums ----------------
+    // The accumulator is complete once tfull fires; every MMA has then read
+    // its operands, so the ring is idle and holds the sums as P[b][m][row].
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    float* xb = reinterpret_cast<float*>(stages);
+    if (mbar_wait(&tfull[0], 0, abort_flag, a.status, a.timeout_ns)) {
+      tc_fence_after();
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+#pragma unroll
+        for (int ch = 0; ch < N / 16; ++ch) {
+          uint32_t r[16];
+          tmem_ld_x16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * N + ch * 16), r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            xb[(size_t)(b * N + ch * 16 + i) * 128 + row] = __uint_as_float(r[i]);
+        }
+      }
+      tc_fence_before();
+    }
+    __syncwarp();
   } else {
     // ---------------- epilogue: warps 2..5 ----------------
     const int quarter = warp & 3;          // TMEM lanes this warp may read
@@ -431,6 +478,62 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     __syncwarp();
   }
 
+  if (S) {
+    // ---------------- cluster mode: rank 0 reduces over the cluster ----------------
+    cluster_sync_all();   // every CTA's sums are staged
+    if (crank == 0 && warp >= 2 && !*abort_flag) {
+      constexpr int kSubCols2 = MODE == kSwiGLU ? kCB : 2 * kCB;
+      constexpr int kGroupCols = NB * kSubCols2;
+      constexpr int kChunks = kGroupCols / 4;
+      constexpr int kMaxS = 8;
+      const int et = threadIdx.x - 64;
+      uint32_t base[kMaxS];
+      const uint32_t local = smem_u32(stages);
+#pragma unroll
+      for (int r = 0; r < kMaxS; ++r) base[r] = r < S ? mapa_shared(local, (uint32_t)r) : 0u;
+      const int total = a.M * kChunks;
+      for (int idx = et; idx < total; idx += kEpiThreads) {
+        const int m = idx / kChunks, ch = idx - m * kChunks;
+        // SwiGLU: 16 chunks per 64-column sub-block, gate rows ch*4.., up rows
+        // 64 + ch*4..; plain: 32 chunks per 128-column sub-block, rows ch*4..
+        const int b = MODE == kSwiGLU ? (ch >> 4) : (ch >> 5);
+        const int r0 = MODE == kSwiGLU ? (ch & 15) * 4 : (ch & 31) * 4;
+        const uint32_t off = (uint32_t)(((b * N + m) * 128 + r0) * 4);
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+#pragma unroll
+        for (int r = 0; r < kMaxS; ++r) {   // rank order = k order
+          if (r < S) {
+            const float4 pv = ld_shared_cluster_v4(base[r] + off);
+            g.x += pv.x; g.y += pv.y; g.z += pv.z; g.w += pv.w;
+            if constexpr (MODE == kSwiGLU) {
+              const float4 qv = ld_shared_cluster_v4(base[r] + off + 64 * 4);
+              u.x += qv.x; u.y += qv.y; u.z += qv.z; u.w += qv.w;
+            }
+          }
+        }
+        const int64_t col = cgroup * kGroupCols + ch * 4;
+        if (col >= a.n_out) continue;   // n_out is a multiple of 8
+        const int64_t o = (int64_t)m * a.n_out + col;
+        uint2 ov;
+        if constexpr (MODE == kSwiGLU) {
+          ov.x = pack_bf16x2(silu_fast(g.x) * u.x, silu_fast(g.y) * u.y);
+          ov.y = pack_bf16x2(silu_fast(g.z) * u.z, silu_fast(g.w) * u.w);
+        } else {
+          if (a.resid) {
+            const uint2 rv = *reinterpret_cast<const uint2*>(a.resid + o);
+            g.x += bf16_lo(rv.x); g.y += bf16_hi(rv.x);
+            g.z += bf16_lo(rv.y); g.w += bf16_hi(rv.y);
+          }
+          ov.x = pack_bf16x2(g.x, g.y);
+          ov.y = pack_bf16x2(g.z, g.w);
+        }
+        *reinterpret_cast<uint2*>(a.out + o) = ov;
+      }
+    }
+    __syncwarp();
+    cluster_sync_all();   // peers keep their shared memory until rank 0 is done
+  }
+
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -454,16 +557,20 @@ cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mg, const CUtenso
     if (e != cudaSuccess) return e;
     if (dev < 64) configured[dev] = 1;
   }
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = a.cluster ? (unsigned)a.cluster : 1u;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.cluster ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, mx, mg, mu, a);
 }
 
@@ -526,11 +633,31 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   p.units = p.n_cb * p.n_kb;
   p.grid = (int)(p.units < num_sms ? p.units : num_sms);
   if (p.grid < 1) p.grid = 1;
+  // Cluster mode (measured): it wins when stream-K would spread each column
+  // group over many CTAs (>= 8 partial sums to reduce through global memory)
+  // and the weights are small enough that the call is latency-bound (<= 32 MB;
+  // e.g. the d = 896 down projection: 38 partials per group in stream-K mode,
+  // 1.4-3x slower than 8-CTA clusters).  Elsewhere stream-K is as fast or
+  // faster (larger clusters leave SMs idle and schedule later).  S = the
+  // largest power of two <= 8 with n_cb * S <= SMs and S <= n_kb.
+  // SWIGLU_SK_CLUSTER overrides (0 = stream-K, 1/2/4/8 = that cluster size).
+  int S = 1;
+  while (S < 8 && p.n_cb * (2 * S) <= num_sms && 2 * S <= p.n_kb) S *= 2;
+  const int64_t per_cta = p.units / p.grid;                       // stream-K units per CTA
+  const int64_t sk_partials = per_cta > 0 ? (p.n_kb + per_cta - 1) / per_cta : p.n_kb;
+  const int64_t weight_bytes = (plain ? 1 : 2) * K * n_out * 2;
+  p.cluster = (S >= 2 && sk_partials >= 8 && weight_bytes <= ((int64_t)32 << 20)) ? S : 0;
+  const int forced = env_int("SWIGLU_SK_CLUSTER", -1);
+  if (forced == 0) p.cluster = 0;
+  if (forced == 1 || forced == 2 || forced == 4 || forced == 8)
+    p.cluster = p.n_kb >= forced ? forced : 0;
+  if (p.cluster) p.grid = (int)(p.n_cb * p.cluster);
   const int64_t per = p.units > 0 ? p.units / p.grid : 1;   // fewest units a CTA gets
   p.maxq = (int)((p.n_kb + per - 1) / (per > 0 ? per : 1) + 1);
   p.counters_bytes = ((size_t)p.n_cb * sizeof(unsigned) + 255) / 256 * 256;
   p.part_bytes = (size_t)p.n_cb * p.maxq * nb * 2 * (size_t)M * kCB * sizeof(float);
   p.part_bytes = (p.part_bytes + 255) / 256 * 256;
+  if (p.cluster) p.counters_bytes = p.part_bytes = 0;   // the reduction stays on chip
   return p;
 }
 
@@ -551,8 +678,8 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   } else if ((e = make_tmap_bf16_2d(&mu, wb, wr, wc, 64, 64, p.l2_promo)) != cudaSuccess) {
     return e;
   }
-  // Arrival counters must be zero on entry.
-  if (!counters_clean &&
+  // Arrival counters must be zero on entry (stream-K mode only).
+  if (!p.cluster && !counters_clean &&
       (e = cudaMemsetAsync(counters, 0, (size_t)p.n_cb * sizeof(unsigned), st)) != cudaSuccess)
     return e;
   SkArgs a;
@@ -565,6 +692,7 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   a.hint = p.hint;
   a.kmajor = w_kmajor ? 1 : 0;
   a.prefetch_units = p.prefetch_units;
+  a.cluster = p.cluster;
   a.part = part;
   a.counters = counters;
   a.out = (uint16_t*)out;

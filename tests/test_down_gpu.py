@@ -53,6 +53,13 @@ def test_ragged(shape, path):
     check(M, d_ff, d, path, seed=M + d + 7, with_resid=False)
 
 
+@pytest.mark.parametrize("cluster", ["0", "4", "8"])
+def test_skinny_plain_cluster_modes(cluster, monkeypatch):
+    monkeypatch.setenv("SWIGLU_SK_CLUSTER", cluster)
+    for shape in [(1, 4864, 896), (16, 1032, 520), (7, 520, 1032)]:
+        check(*shape, "skinny", seed=int(cluster) + shape[0])
+
+
 @pytest.mark.parametrize("M", [1, 4, 16])
 def test_decode_shape_full(M):
     # d_ff=14336 -> d=4096

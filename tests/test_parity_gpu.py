@@ -113,6 +113,26 @@ def test_forced_paths_agree(M):
             assert compare(outs[a], outs[b], sens, "bf16", d)["ok"], (a, b)
 
 
+@pytest.mark.parametrize("cluster", ["0", "2", "4", "8"])
+def test_skinny_cluster_and_stream_k_modes(cluster, monkeypatch):
+    # the skinny kernel's two reductions: stream-K (global partials, last
+    # arriver) and cluster mode (on-chip, through distributed shared memory)
+    monkeypatch.setenv("SWIGLU_SK_CLUSTER", cluster)
+    for (M, d, d_ff) in [(1, 896, 4864), (16, 896, 4864), (3, 520, 264), (40, 1024, 1032),
+                         (130, 640, 520)]:
+        full_check(M, d, d_ff, "bf16", "skinny", seed=M + int(cluster))
+
+
+def test_cluster_mode_selection():
+    # the small model's down projection (38 partials per group in stream-K
+    # mode) runs in 8-CTA clusters with no workspace; the up projections stay
+    # on stream-K
+    p = swg.down_plan(1, 4864, 896, "bf16", "auto", 152)
+    assert p["path"] == "skinny" and p["workspace"] == 0 and p["grid"] == 4 * 8
+    assert swg.plan(1, 896, 4864, "bf16", "auto", 152)["workspace"] > 0
+    assert swg.plan(16, 4096, 14336, "bf16", "auto", 152)["workspace"] > 0
+
+
 def test_dispatch_rule():
     for M, path in [(1, "skinny"), (16, "skinny"), (17, "tc"), (4096, "tc")]:
         assert swg.plan(M, 4096, 14336, "bf16", "auto", 152)["path"] == path
@@ -226,7 +246,8 @@ def test_output_guard_band_untouched():
 
 
 @pytest.mark.parametrize("path", ["simt", "skinny"])
-def test_caller_workspace_and_errors(path):
+def test_caller_workspace_and_errors(path, monkeypatch):
+    monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")     # the split-K workspace of stream-K mode
     dev = torch.device("cuda", 0)
     M, d, d_ff = 3, 1024, 2048
     x, wg, wu = (t.to(dev) for t in inputs.make_inputs(M, d, d_ff, "bf16", seed=35))
