@@ -213,6 +213,9 @@ typedef struct {
   int64_t workspace;     /* bytes of partial sums                                */
   int64_t skinny_max_m;  /* largest bf16 M that AUTO sends to SKINNY            */
   int64_t launches;      /* kernel launches one call enqueues                   */
+  int64_t cluster;       /* CTAs per thread-block cluster of the main kernel
+                            (1: none; 2-8: the skinny kernel's split-K
+                            clusters; 2: the TC path's CTA pairs)            */
 } swiglu_plan_info;
 
 SWIGLU_API int swiglu_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, int path,

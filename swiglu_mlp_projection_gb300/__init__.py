@@ -204,7 +204,8 @@ def down_plan(M, d_ff, d, dtype="bf16", path="auto", num_sms=152):
     dt = BF16 if dtype in ("bf16", BF16) else F32
     _lib.check(lib.swiglu_down_plan(M, d_ff, d, dt, _path_code(path), num_sms, ctypes.byref(info)))
     return {"path": PATH_NAMES.get(info.path, info.path), "slices": info.slices,
-            "grid": info.grid, "workspace": info.workspace, "launches": info.launches}
+            "grid": info.grid, "workspace": info.workspace, "launches": info.launches,
+            "cluster": info.cluster}
 
 
 def workspace_bytes(M, d, d_ff, dtype="bf16", path="auto"):
@@ -223,7 +224,7 @@ def plan(M, d, d_ff, dtype="bf16", path="auto", num_sms=152):
     return {"path": PATH_NAMES.get(info.path, info.path), "slices": info.slices,
             "grid": info.grid, "row_chunk": info.row_chunk,
             "workspace": info.workspace, "skinny_max_m": info.skinny_max_m,
-            "launches": info.launches}
+            "launches": info.launches, "cluster": info.cluster}
 
 
 def split_k_slices(K, col_blocks, target_blocks, min_k_per_slice):

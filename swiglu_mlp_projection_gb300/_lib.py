@@ -29,7 +29,7 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("slices", ctypes.c_int64),
                 ("grid", ctypes.c_int64), ("row_chunk", ctypes.c_int64),
                 ("workspace", ctypes.c_int64), ("skinny_max_m", ctypes.c_int64),
-                ("launches", ctypes.c_int64)]
+                ("launches", ctypes.c_int64), ("cluster", ctypes.c_int64)]
 
 
 SIGNATURES = {

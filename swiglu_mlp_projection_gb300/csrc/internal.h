@@ -87,10 +87,13 @@ constexpr size_t kStreamCounterBytes = 64 * 1024;   // per-stream arrival counte
 // 128 output columns whose gate and up accumulators sit side by side
 // (128 x 256 f32), SwiGLU applied before the bf16 store.  Plain (down
 // projection): 256 output columns, + residual, bf16 store.
+// With `pair`, a tile is 256 rows computed by a 2-CTA cluster (cta_group::2
+// MMAs); n_mb then counts 256-row blocks and grid is even.
 struct TilePlan {
   int64_t n_mb, n_nb, tiles;
   int grid;
   bool plain;
+  bool pair;
 };
 TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain);
 cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* out,

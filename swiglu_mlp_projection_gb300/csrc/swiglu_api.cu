@@ -301,6 +301,7 @@ struct Plan {
   int64_t slices;
   int64_t grid;
   int64_t launches;   // kernels one call launches
+  int64_t cluster;    // CTAs per cluster of the main kernel (1 = none)
   size_t workspace;
 };
 
@@ -312,6 +313,7 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
   if (st != SWIGLU_OK) return st;
   *p = Plan{};
   p->path = rp;
+  p->cluster = 1;
   const bool plain = op == kOpDown;
   if (rp == SWIGLU_PATH_SIMT) {
     p->simt = plan_simt(M, K, n_out, dtype, num_sms);
@@ -328,12 +330,14 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
     p->grid = p->skinny.grid;
     p->workspace = p->skinny.counters_bytes + p->skinny.part_bytes;
     p->launches = 1;
+    p->cluster = p->skinny.cluster ? p->skinny.cluster : 1;
   } else {
     p->tile = plan_tile(M, K, n_out, num_sms, plain);
     p->slices = 1;
     p->grid = p->tile.grid;
     p->workspace = 0;
     p->launches = 1;
+    p->cluster = p->tile.pair ? 2 : 1;
   }
   if (M == 0 || n_out == 0) p->launches = 0;
   if (plain && K == 0) p->launches = 0;
@@ -601,6 +605,7 @@ static int plan_common(int op, int64_t M, int64_t K, int64_t n_out, int dtype, i
   out->workspace = (int64_t)p.workspace;
   out->skinny_max_m = kSkinnyMaxM;
   out->launches = p.launches;
+  out->cluster = p.cluster;
   return SWIGLU_OK;
 }
 
@@ -632,7 +637,8 @@ int swiglu_check_device_status(void) {
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) mark_workspaces_dirty(dev);
     return fail(SWIGLU_ERR_TIMEOUT,
-                "a device-side wait gave up or found a stale arrival counter (status word 0x%x)",
+                "a device-side wait gave up, found a stale arrival counter or a CTA pair's "
+                "TMEM allocations disagreed (status word 0x%x)",
                 word);
   }
   return SWIGLU_OK;
@@ -655,6 +661,6 @@ const char* swiglu_status_string(int status) {
 
 const char* swiglu_last_error_string(void) { return t_err; }
 
-int swiglu_version(void) { return 100; }
+int swiglu_version(void) { return 200; }
 
 }  // extern "C"

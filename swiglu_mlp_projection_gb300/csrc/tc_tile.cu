@@ -12,7 +12,8 @@
 //     the same 128 output columns (the interleave happens per 64-column TMA
 //     box while loading; W_gate and W_up stay separate row-major arrays);
 //   * A = x tile (K-major), B = the four weight boxes (MN-major, read straight
-//     from the row-major weights), both TMA-staged in a 4-stage ring;
+//     from the row-major weights), both TMA-staged in a 4-stage ring
+//     (6 stages on a CTA pair);
 //   * one thread issues tcgen05.mma (M=128, N=256, K=16) into one of two TMEM
 //     accumulators, so the epilogue of tile i overlaps the MMAs of tile i+1
 //     (the overlap the paper gets from ping-pong warp groups);
@@ -22,6 +23,13 @@
 // Tiles are visited column-block-major so the CTAs running at the same time
 // share weight columns and x rows through L2.
 //
+// Above 128 rows the kernel runs on CTA pairs (2-CTA clusters, tcgen05
+// cta_group::2): a tile is 256 rows, each CTA loads its 128 rows of x and
+// half of the weight boxes (gate in rank 0, up in rank 1), and one M = 256
+// MMA stream fills both CTAs' TMEM.  Per CTA and k-block that is 32 KB of
+// operands instead of 48 KB, so six stages fit and the L2 -> SM bytes per
+// FLOP fall by a third (measured: prefill 480 vs 549 us per call).
+//
 // In its plain mode the same kernel computes the down projection
 // y = h . W_down (+ residual) ("1 . Anatomie d'un transformeur sur GPU",
 // section 1.6, kernels #10 and #11): the 256 accumulator columns are 256
@@ -30,29 +38,44 @@
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
+#include "tc_pair.cuh"
 
 namespace swg {
 namespace {
 
 using namespace tc;
 
-constexpr int kBM = 128;                        // output rows per tile
+constexpr int kBM = 128;                        // output rows per CTA and tile
 constexpr int kBN = 128;                        // output columns per tile
 constexpr int kBK = 64;
-constexpr int kStages = 4;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kABytes = kBM * kBK * 2;     // 16 KB
 constexpr uint32_t kChunkBytes = 64 * kBK * 2;  // 8 KB: one 64-column weight box
-constexpr uint32_t kBBytes = 4 * kChunkBytes;   // gate 0-63, gate 64-127, up 0-63, up 64-127
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kStagingHalf = kBM * 128;    // 128 rows x 64 bf16
 constexpr uint32_t kStagingBytes = 2 * kStagingHalf;
 constexpr uint32_t kTmemCols = 512;             // two 128 x 256 f32 accumulators
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kStagingBytes + 256;
+
+// One CTA per tile (PAIR = false), or a 2-CTA cluster per 256-row tile whose
+// MMAs run as cta_group::2 (PAIR = true).  A pair tile gives each CTA 128 rows
+// of x and half of the 256 weight columns, so a CTA stages 32 KB per k-block
+// instead of 48 KB: more stages fit, and the L2 -> SM bytes per FLOP drop by
+// a third.
+template <bool PAIR>
+struct TileCfg {
+  static constexpr int kBoxes = PAIR ? 2 : 4;   // 64-column weight boxes per CTA and k-block
+  static constexpr uint32_t kBBytes = kBoxes * kChunkBytes;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kTileRows = PAIR ? 2 * kBM : kBM;
+  static constexpr size_t kSmemBytes =
+      1024 + (size_t)kStages * kStageBytes + kStagingBytes + 256;
+};
+static_assert(TileCfg<true>::kSmemBytes <= 232448, "pair tile exceeds shared memory");
+static_assert(TileCfg<false>::kSmemBytes <= 232448, "tile exceeds shared memory");
 
 struct TileArgs {
-  int n_mb, n_nb, n_kb, n_out;   // n_out: output columns
+  int n_mb, n_nb, n_kb, n_out;   // n_mb: row blocks of the tile height; n_out: output columns
   int M;
   int64_t tiles;
   const uint16_t* resid;         // plain mode: [M][n_out] added to the sums, or null
@@ -70,17 +93,19 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, unsig
   return mbar_wait(bar, parity, &never, status, timeout_ns);
 }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
 tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wg,
                const __grid_constant__ CUtensorMap tm_wu, const __grid_constant__ CUtensorMap tm_h,
                const TileArgs a) {
-  // output columns per tile, and where the four 64-column B boxes come from
+  using C = TileCfg<PAIR>;
+  constexpr int kStages = C::kStages;
+  // output columns per tile, and where the 64-column B boxes come from
   constexpr int kOutCols = MODE == kSwiGLU ? kBN : 2 * kBN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* stages = smem_raw + pad;
-  uint8_t* staging = stages + (size_t)kStages * kStageBytes;
+  uint8_t* staging = stages + (size_t)kStages * C::kStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(staging + kStagingBytes);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
@@ -90,16 +115,25 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // In a pair, rank 0 issues the MMAs for both CTAs; each CTA loads its own
+  // 128 rows of x and its half of the weight columns and runs its own
+  // epilogue on the 128 accumulator rows in its TMEM.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int64_t unit = PAIR ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
+  const int64_t n_units = PAIR ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+      // rank 0's stage is full once its own bytes have landed and rank 1 has
+      // relayed that its half has landed too
+      mbar_init(&full[s], (PAIR && rank == 0) ? 2 : 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(&tfull[0], 1);
     mbar_init(&tfull[1], 1);
-    mbar_init(&tempty[0], kEpiThreads);
-    mbar_init(&tempty[1], kEpiThreads);
+    // a pair's accumulator is free once both CTAs' epilogues have read it
+    mbar_init(&tempty[0], PAIR ? 2 * kEpiThreads : kEpiThreads);
+    mbar_init(&tempty[1], PAIR ? 2 * kEpiThreads : kEpiThreads);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -109,42 +143,66 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     tma_prefetch_desc(&tm_h);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();   // both CTAs' barriers and TMEM are ready
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The pair's MMAs address both TMEMs with one column address; if the two
+  // allocations disagree, neither CTA does any work.
+  bool skip = false;
+  if constexpr (PAIR) {
+    skip = ld_shared_cluster_u32(mapa_shared(smem_u32(tmem_slot), rank ^ 1u)) != tmem;
+    if (skip && threadIdx.x == 0) atomicOr(a.status, kStatusPairTmem);
+  }
   // The set-up above overlaps the previous kernel's tail; x and h are touched
   // only after it has finished.
   pdl_wait();
   pdl_launch_dependents();
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer (each CTA) ----------------
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
-      bool ok = true;
-      for (int64_t t = blockIdx.x; ok && t < a.tiles; t += gridDim.x) {
+      bool ok = !skip;
+      for (int64_t t = unit; ok && t < a.tiles; t += n_units) {
         const int mb = (int)(t % a.n_mb), nb = (int)(t / a.n_mb);
+        const int row0 = mb * C::kTileRows + (int)rank * kBM;
         for (int kb = 0; kb < a.n_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status, a.timeout_ns)) {
             ok = false;
             break;
           }
-          uint8_t* st = stages + (size_t)stage * kStageBytes;
+          uint8_t* st = stages + (size_t)stage * C::kStageBytes;
           uint8_t* sb = st + kABytes;
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          tma_load_2d(st, &tm_x, &full[stage], kb * kBK, mb * kBM);
+          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+          tma_load_2d(st, &tm_x, &full[stage], kb * kBK, row0);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            // box q of the B tile: SwiGLU -> gate 0-63, gate 64-127, up 0-63,
-            // up 64-127 of this tile's columns; plain -> 4 x 64 adjacent columns
-            const CUtensorMap* m = (MODE == kSwiGLU && q >= 2) ? &tm_wu : &tm_wg;
-            const int col = MODE == kSwiGLU ? nb * kBN + 64 * (q & 1) : nb * kOutCols + 64 * q;
+          for (int q = 0; q < C::kBoxes; ++q) {
+            // B boxes.  One CTA: SwiGLU -> gate 0-63, gate 64-127, up 0-63,
+            // up 64-127 of the tile's columns; plain -> 4 x 64 adjacent
+            // columns.  Pair: rank 0 holds accumulator columns 0-127 (gate,
+            // or output columns 0-127), rank 1 columns 128-255 (up, or
+            // output columns 128-255).
+            const CUtensorMap* m;
+            int col;
+            if constexpr (PAIR) {
+              m = (MODE == kSwiGLU && rank == 1) ? &tm_wu : &tm_wg;
+              col = MODE == kSwiGLU ? nb * kBN + 64 * q : nb * kOutCols + (int)rank * kBN + 64 * q;
+            } else {
+              m = (MODE == kSwiGLU && q >= 2) ? &tm_wu : &tm_wg;
+              col = MODE == kSwiGLU ? nb * kBN + 64 * (q & 1) : nb * kOutCols + 64 * q;
+            }
             if (a.kmajor)
               tma_load_2d(sb + q * kChunkBytes, m, &full[stage], kb * kBK, col);
             else
@@ -157,28 +215,30 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
           }
         }
       }
-      if (!ok) {
+      if (issued > 0 && !ok) {
+        // let the loads still in flight land before the CTA can exit
         const int64_t first = issued > kStages ? issued - kStages : 0;
         for (int64_t i = first; i < issued; ++i)
           wait_drain(&full[i % kStages], (uint32_t)((i / kStages) & 1), a.status, a.timeout_ns);
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 1 && (!PAIR || rank == 0)) {
+    // ---------------- MMA issuer (the CTA, or rank 0 of the pair) ----------------
     if (lane == 0) {
       // A (x) is K-major; B (the weights) MN-major for [K, n_out] weights,
       // K-major for [n_out, K] weights.
-      const uint32_t idesc = a.kmajor ? idesc_bf16_f32(kBM, 2 * kBN, false, false)
-                                      : idesc_bf16_f32(kBM, 2 * kBN, false, true);
+      constexpr int kMmaM = PAIR ? 2 * kBM : kBM;
+      const uint32_t idesc = a.kmajor ? idesc_bf16_f32(kMmaM, 2 * kBN, false, false)
+                                      : idesc_bf16_f32(kMmaM, 2 * kBN, false, true);
       const uint32_t b_step = a.kmajor ? 32u : 2048u;
       const uint32_t b_lbo = a.kmajor ? 16u : kChunkBytes;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      bool ok = true;
-      for (int64_t t = blockIdx.x; ok && t < a.tiles; t += gridDim.x) {
+      bool ok = !skip;
+      for (int64_t t = unit; ok && t < a.tiles; t += n_units) {
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, a.status, a.timeout_ns)) {
           ok = false;
           break;
@@ -191,46 +251,88 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(stages + (size_t)stage * kStageBytes);
+          const uint32_t a_addr = smem_u32(stages + (size_t)stage * C::kStageBytes);
           const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = smem_desc_sw128(a_addr + kk * 32u, 16u, 1024u);
             const uint64_t bd = smem_desc_sw128(b_addr + kk * b_step, b_lbo, 1024u);
-            mma_bf16(d_tmem, ad, bd, idesc, (kb != 0 || kk != 0) ? 1u : 0u);
+            const uint32_t accumulate = (kb != 0 || kk != 0) ? 1u : 0u;
+            if constexpr (PAIR)
+              mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+            else
+              mma_bf16(d_tmem, ad, bd, idesc, accumulate);
           }
-          mma_commit(&empty[stage]);
+          // the stage is free again in both CTAs once these MMAs are done
+          if constexpr (PAIR)
+            mma_commit_pair_mc(&empty[stage], (uint16_t)0x3);
+          else
+            mma_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);
+        if constexpr (PAIR)
+          mma_commit_pair_mc(&tfull[acc], (uint16_t)0x3);
+        else
+          mma_commit(&tfull[acc]);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
-      mma_commit(drain);
+      if constexpr (PAIR)
+        mma_commit_pair(drain);
+      else
+        mma_commit(drain);
       wait_drain(drain, 0, a.status, a.timeout_ns);
     }
     __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- rank 1 of a pair: relay ----------------
+    // Tell rank 0 when this CTA's half of each stage has landed.
+    if constexpr (PAIR) {
+      if (lane == 0) {
+        const uint32_t full0 = mapa_shared(smem_u32(full), 0u);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = !skip;
+        for (int64_t t = unit; ok && t < a.tiles; t += n_units) {
+          for (int kb = 0; kb < a.n_kb; ++kb) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, a.status, a.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_remote(full0 + (uint32_t)stage * 8u);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
   } else {
-    // ---------------- epilogue: warps 2..5 ----------------
+    // ---------------- epilogue: warps 2..5 (each CTA) ----------------
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;   // accumulator row = output row in the tile
+    const int row = quarter * 32 + lane;   // accumulator row = output row in this CTA's rows
     const int et = threadIdx.x - 64;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     constexpr int kPasses = MODE == kSwiGLU ? 1 : 2;   // 128 output columns per pass
+    // rank 1 tells rank 0's MMA issuer that an accumulator has been read
+    const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(tempty), 0u) : 0u;
     int acc = 0;
     uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int64_t t = blockIdx.x; ok && t < a.tiles; t += gridDim.x) {
+    bool ok = !skip;
+    for (int64_t t = unit; ok && t < a.tiles; t += n_units) {
       const int mb = (int)(t % a.n_mb), nb = (int)(t / a.n_mb);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, a.status, a.timeout_ns)) break;
       tc_fence_after();
-      const int64_t grow = (int64_t)mb * kBM + row;       // output row of this thread
+      const int row_base = mb * C::kTileRows + (int)rank * kBM;
+      const int64_t grow = (int64_t)row_base + row;       // output row of this thread
       for (int pass = 0; pass < kPasses; ++pass) {
         if (et == 0) bulk_wait_read0();   // the previous store has read the staging tile
         __syncwarp();
@@ -283,15 +385,23 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         if (pass == kPasses - 1) {
           // every accumulator column of this buffer has been read
           tc_fence_before();
-          mbar_arrive(&tempty[acc]);
+          if (PAIR && rank == 1)
+            mbar_arrive_remote(tempty0 + (uint32_t)acc * 8u);
+          else
+            mbar_arrive(&tempty[acc]);
         }
         fence_async_smem();
         __syncwarp();
         named_bar_sync(1, kEpiThreads);
         if (et == 0) {
+          // (rank 1 of a pair whose 256-row tile sticks out past M may have
+          // no rows to store)
           const int c0 = nb * kOutCols + pass * kBN;
-          if (c0 < a.n_out) tma_store_2d(&tm_h, staging, c0, mb * kBM);
-          if (c0 + 64 < a.n_out) tma_store_2d(&tm_h, staging + kStagingHalf, c0 + 64, mb * kBM);
+          if (row_base < a.M) {
+            if (c0 < a.n_out) tma_store_2d(&tm_h, staging, c0, row_base);
+            if (c0 + 64 < a.n_out)
+              tma_store_2d(&tm_h, staging + kStagingHalf, c0 + 64, row_base);
+          }
           bulk_commit();
         }
       }
@@ -306,10 +416,21 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 
   tc_fence_before();
   __syncthreads();
+  // Neither CTA of a pair leaves (or frees its TMEM) while the other may still
+  // signal its barriers or read its shared memory.
+  if constexpr (PAIR) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+int tile_env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  return v ? atoi(v) : dflt;
 }
 
 }  // namespace
@@ -319,39 +440,73 @@ TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain)
   TilePlan p{};
   const int64_t cols = plain ? 2 * kBN : kBN;
   p.plain = plain;
-  p.n_mb = (M + kBM - 1) / kBM;
+  // 2-CTA tiles wherever there is more than one 128-row block;
+  // SWIGLU_TILE_PAIR = 0 / 1 forces one mode.
+  const int forced = tile_env_int("SWIGLU_TILE_PAIR", -1);
+  p.pair = forced >= 0 ? forced != 0 : M > kBM;
+  if (num_sms < 2) p.pair = false;
+  const int64_t rows = p.pair ? 2 * kBM : kBM;
+  p.n_mb = (M + rows - 1) / rows;
   p.n_nb = (n_out + cols - 1) / cols;
   p.tiles = p.n_mb * p.n_nb;
-  p.grid = (int)(p.tiles < num_sms ? p.tiles : num_sms);
-  if (p.grid < 1) p.grid = 1;
+  const int64_t units = p.pair ? num_sms / 2 : num_sms;   // CTAs or CTA pairs at once
+  int64_t g = p.tiles < units ? p.tiles : units;
+  if (g < 1) g = 1;
+  p.grid = (int)(p.pair ? 2 * g : g);
   return p;
 }
 
-template <int MODE>
+namespace {
+
+template <int MODE, bool PAIR>
 cudaError_t launch_mode(const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mu,
                         const CUtensorMap& mh, const TileArgs& a, int grid, cudaStream_t st) {
-  auto kern = tile_tc_kernel<MODE>;
+  using C = TileCfg<PAIR>;
+  auto kern = tile_tc_kernel<MODE, PAIR>;
   static int configured[64] = {0};
+  static int max_clusters[64] = {0};   // co-resident CTA pairs, per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) configured[dev] = 1;
-  }
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = PAIR ? 2 : 1;
+  if (dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    int mc = 0;
+    if (PAIR) {
+      // The persistent grid takes no more pairs than can run at once (pairs
+      // need both SMs of a cluster slot, so this may be below SMs / 2).
+      e = cudaOccupancyMaxActiveClusters(&mc, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (mc < 1) return cudaErrorInvalidConfiguration;
+    }
+    if (dev < 64) {
+      max_clusters[dev] = mc;
+      configured[dev] = 1;
+    } else if (PAIR && grid > 2 * mc) {
+      cfg.gridDim = dim3((unsigned)(2 * mc));
+    }
+  }
+  if (PAIR && dev < 64 && grid > 2 * max_clusters[dev])
+    cfg.gridDim = dim3((unsigned)(2 * max_clusters[dev]));
   return cudaLaunchKernelEx(&cfg, kern, mx, mg, mu, mh, a);
 }
+
+}  // namespace
 
 cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* out,
                            const void* resid, int64_t M, int64_t K, int64_t n_out,
@@ -380,8 +535,11 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
   a.kmajor = w_kmajor ? 1 : 0;
   a.status = status;
   a.timeout_ns = timeout_ns;
-  return p.plain ? launch_mode<kPlain>(mx, mg, mu, mh, a, p.grid, st)
-                 : launch_mode<kSwiGLU>(mx, mg, mu, mh, a, p.grid, st);
+  if (p.pair)
+    return p.plain ? launch_mode<kPlain, true>(mx, mg, mu, mh, a, p.grid, st)
+                   : launch_mode<kSwiGLU, true>(mx, mg, mu, mh, a, p.grid, st);
+  return p.plain ? launch_mode<kPlain, false>(mx, mg, mu, mh, a, p.grid, st)
+                 : launch_mode<kSwiGLU, false>(mx, mg, mu, mh, a, p.grid, st);
 }
 
 }  // namespace swg

@@ -77,6 +77,22 @@ def test_plan_covers_all_columns_rows_and_k(cuda_lib, dtype):
         assert p["workspace"] % 256 == 0
 
 
+def test_plan_reports_cluster_size(cuda_lib):
+    # TC path: CTA pairs above one 128-row block, single CTAs below
+    p = swg.plan(4096, 4096, 14336, "bf16", "auto", 152)
+    assert p["path"] == "tc" and p["cluster"] == 2 and p["grid"] == 152
+    p = swg.plan(64, 896, 4864, "bf16", "tc", 152)
+    assert p["cluster"] == 1 and p["grid"] == 38
+    p = swg.plan(300, 4096, 14336, "bf16", "tc", 152)
+    assert p["cluster"] == 2 and p["grid"] == 152      # 2 x 112 pair tiles > 76 pairs
+    p = swg.plan(300, 520, 264, "bf16", "tc", 152)
+    assert p["cluster"] == 2 and p["grid"] == 2 * 2 * 3
+    # skinny path: split-K clusters for the small down projection only
+    assert swg.down_plan(1, 4864, 896, "bf16", "auto", 152)["cluster"] == 8
+    assert swg.plan(1, 4096, 14336, "bf16", "auto", 152)["cluster"] == 1
+    assert swg.plan(1, 512, 2048, "f32", "auto", 152)["cluster"] == 1
+
+
 def test_plan_rejects_bad_arguments(cuda_lib):
     with pytest.raises(swg.SwiGLUError):
         swg.plan(-1, 8, 8, "bf16", "auto", 152)
