@@ -80,7 +80,8 @@ typedef enum {
  *
  * Dispatch (AUTO): f32 -> SIMT split-K path; bf16 with M <= the skinny limit
  * (swiglu_plan reports it) -> SKINNY; larger bf16 M -> TC.  The split-K
- * paths need a workspace for their partial sums; this entry point takes it
+ * paths, and the TC path where it splits its last wave of tiles along K
+ * (stream-K), need a workspace for their partial sums; this entry point takes it
  * from a library-owned, stream-ordered pool (cudaMallocFromPoolAsync /
  * cudaFreeAsync on `stream`), so calls on different streams never share it.
  * Errors: SWIGLU_ERR_INVALID_ARG, _ALIGNMENT, _ARCH, _OOM, _CUDA.
@@ -198,8 +199,9 @@ SWIGLU_API int swiglu_up_noalloc(const void* x, const void* w_gate, const void* 
                                  int64_t M, int64_t d, int64_t d_ff, int dtype, void* stream);
 
 /* Workspace bytes a call with these arguments needs on the current device
- * (0 for the TC path).  Returns 0 and sets the thread's error string when the
- * arguments are invalid or no device is current. */
+ * (0 for TC calls whose tiles fill whole waves of the GPU).  Returns 0 and sets
+ * the thread's error string when the arguments are invalid or no device is
+ * current. */
 SWIGLU_API size_t swiglu_workspace_bytes(int64_t M, int64_t d, int64_t d_ff, int dtype,
                               int path);
 

@@ -209,7 +209,8 @@ def down_plan(M, d_ff, d, dtype="bf16", path="auto", num_sms=152):
 
 
 def workspace_bytes(M, d, d_ff, dtype="bf16", path="auto"):
-    """Workspace bytes a call needs on the current device (0 for the TC path)."""
+    """Workspace bytes a call needs on the current device (0 for TC calls
+    whose tiles fill whole waves)."""
     lib = _lib.load()
     dt = BF16 if dtype in ("bf16", BF16) else F32
     return int(lib.swiglu_workspace_bytes(M, d, d_ff, dt, _path_code(path)))

@@ -88,17 +88,26 @@ constexpr size_t kStreamCounterBytes = 64 * 1024;   // per-stream arrival counte
 // (128 x 256 f32), SwiGLU applied before the bf16 store.  Plain (down
 // projection): 256 output columns, + residual, bf16 store.
 // With `pair`, a tile is 256 rows computed by a 2-CTA cluster (cta_group::2
-// MMAs); n_mb then counts 256-row blocks and grid is even.
+// MMAs); n_mb then counts 256-row blocks and grid is even.  Tiles from
+// dp_tiles on form a stream-K tail (sk_iters > 0): their (tile, k-block)
+// iterations are shared out evenly over the grid's units, and partial tiles
+// meet in `part_bytes` of f32 slots with `counters_bytes` of arrival counters.
 struct TilePlan {
-  int64_t n_mb, n_nb, tiles;
+  int64_t n_mb, n_nb, n_kb, tiles;
   int grid;
   bool plain;
   bool pair;
+  int64_t dp_tiles, sk_iters, sk_q, sk_r;
+  size_t counters_bytes, part_bytes;
 };
-TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain);
+// max_pairs: 2-CTA clusters of the tile kernel that fit on the device at once.
+TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
+                   int max_pairs);
+cudaError_t tile_max_pairs(int* pairs);
 cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* out,
                            const void* resid, int64_t M, int64_t K, int64_t n_out,
-                           bool w_kmajor, const TilePlan& p, unsigned* status,
-                           uint64_t timeout_ns, cudaStream_t st);
+                           bool w_kmajor, const TilePlan& p, float* part, unsigned* counters,
+                           bool counters_clean, unsigned* status, uint64_t timeout_ns,
+                           cudaStream_t st);
 
 }  // namespace swg

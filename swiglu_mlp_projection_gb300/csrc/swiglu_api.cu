@@ -42,6 +42,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
+  int max_pairs = 0;            // 2-CTA clusters of the tile kernel that fit at once
   int cc_major = 0, cc_minor = 0;
   cudaMemPool_t pool = nullptr;
   unsigned* status = nullptr;   // device address of g_device_status
@@ -70,6 +71,8 @@ int current_device(int* dev_out, DeviceInfo* out) {
       if ((e = cudaGetSymbolAddress(&sp, g_device_status)) != cudaSuccess)
         return cuda_fail(e, "cudaGetSymbolAddress(status word)");
       di.status = (unsigned*)sp;
+      if ((e = tile_max_pairs(&di.max_pairs)) != cudaSuccess)
+        return cuda_fail(e, "cudaOccupancyMaxActiveClusters(tile kernel)");
     }
     di.ready = true;
   }
@@ -306,8 +309,10 @@ struct Plan {
 };
 
 // K: shared dimension; n_out: output columns (up: d, d_ff; down: d_ff, d).
+// max_pairs: 2-CTA clusters that fit on the device at once (num_sms / 2 when
+// planning without a device).
 int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, int num_sms,
-              Plan* p) {
+              int max_pairs, Plan* p) {
   int rp = 0;
   int st = resolve_path(op, M, K, dtype, path, &rp);
   if (st != SWIGLU_OK) return st;
@@ -332,10 +337,10 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
     p->launches = 1;
     p->cluster = p->skinny.cluster ? p->skinny.cluster : 1;
   } else {
-    p->tile = plan_tile(M, K, n_out, num_sms, plain);
+    p->tile = plan_tile(M, K, n_out, num_sms, plain, max_pairs);
     p->slices = 1;
     p->grid = p->tile.grid;
-    p->workspace = 0;
+    p->workspace = p->tile.counters_bytes + p->tile.part_bytes;
     p->launches = 1;
     p->cluster = p->tile.pair ? 2 : 1;
   }
@@ -364,7 +369,8 @@ int run(const Call& c) {
   DeviceInfo di;
   if ((v = current_device(&dev, &di)) != SWIGLU_OK) return v;
   Plan p;
-  if ((v = make_plan(c.op, c.M, c.K, c.n_out, c.dtype, c.path, di.num_sms, &p)) != SWIGLU_OK)
+  if ((v = make_plan(c.op, c.M, c.K, c.n_out, c.dtype, c.path, di.num_sms, di.max_pairs, &p)) !=
+      SWIGLU_OK)
     return v;
   if (c.kmajor && p.path == SWIGLU_PATH_SIMT && c.K > 0)
     return fail(SWIGLU_ERR_UNSUPPORTED,
@@ -395,7 +401,9 @@ int run(const Call& c) {
   unsigned* counters = nullptr;
   bool counters_clean = false;
   void* pooled = nullptr;
-  const size_t counter_bytes = p.path == SWIGLU_PATH_SKINNY ? p.skinny.counters_bytes : 0;
+  const size_t counter_bytes = p.path == SWIGLU_PATH_SKINNY ? p.skinny.counters_bytes
+                               : p.path == SWIGLU_PATH_TC   ? p.tile.counters_bytes
+                                                            : 0;
   cudaStream_t st = c.st;
   if (p.workspace > 0) {
     if (c.workspace) {
@@ -437,7 +445,7 @@ int run(const Call& c) {
                          part, counters, counters_clean, di.status, wait_timeout_ns(), st);
   } else {
     e = launch_tile_tc(c.x, c.wa, c.wb, c.out, c.resid, c.M, c.K, c.n_out, c.kmajor, p.tile,
-                       di.status, wait_timeout_ns(), st);
+                       part, counters, counters_clean, di.status, wait_timeout_ns(), st);
   }
   if (pooled) {
     cudaError_t ef = cudaFreeAsync(pooled, st);
@@ -576,7 +584,8 @@ size_t swiglu_workspace_bytes(int64_t M, int64_t d, int64_t d_ff, int dtype, int
   DeviceInfo di;
   if (current_device(&dev, &di) != SWIGLU_OK) return 0;
   Plan p;
-  if (make_plan(kOpUp, M, d, d_ff, dtype, path, di.num_sms, &p) != SWIGLU_OK) return 0;
+  if (make_plan(kOpUp, M, d, d_ff, dtype, path, di.num_sms, di.max_pairs, &p) != SWIGLU_OK)
+    return 0;
   return p.workspace;
 }
 
@@ -586,7 +595,8 @@ size_t swiglu_down_workspace_bytes(int64_t M, int64_t d_ff, int64_t d, int dtype
   DeviceInfo di;
   if (current_device(&dev, &di) != SWIGLU_OK) return 0;
   Plan p;
-  if (make_plan(kOpDown, M, d_ff, d, dtype, path, di.num_sms, &p) != SWIGLU_OK) return 0;
+  if (make_plan(kOpDown, M, d_ff, d, dtype, path, di.num_sms, di.max_pairs, &p) != SWIGLU_OK)
+    return 0;
   return p.workspace;
 }
 
@@ -596,7 +606,7 @@ static int plan_common(int op, int64_t M, int64_t K, int64_t n_out, int dtype, i
   if (dtype != SWIGLU_F32 && dtype != SWIGLU_BF16) return fail(SWIGLU_ERR_INVALID_ARG, "unknown dtype %d", dtype);
   if (M < 0 || K < 0 || n_out < 0 || num_sms <= 0) return fail(SWIGLU_ERR_INVALID_ARG, "negative size or SM count");
   Plan p;
-  int v = make_plan(op, M, K, n_out, dtype, path, num_sms, &p);
+  int v = make_plan(op, M, K, n_out, dtype, path, num_sms, num_sms / 2, &p);
   if (v != SWIGLU_OK) return v;
   out->path = p.path;
   out->slices = p.slices;

@@ -82,6 +82,56 @@ struct TileArgs {
   int kmajor;                    // weights stored [n_out, K] instead of [K, n_out]
   unsigned* status;
   uint64_t timeout_ns;
+  // Stream-K tail.  Tiles [0, dp_tiles) are done whole, round-robin over the
+  // units (CTAs, or CTA pairs).  The k-blocks of the tiles after them form one
+  // iteration space of sk_iters = (tiles - dp_tiles) * n_kb, cut into
+  // contiguous ranges: sk_q + 1 iterations for each of the first sk_r units,
+  // sk_q for the rest.
+  int64_t dp_tiles, sk_iters, sk_q, sk_r;
+  float* part;                   // partial tiles: slot (tile - dp_tiles + unit), rank, 8 x 8 x 128 x 4 f32
+  unsigned* counters;            // arrivals per stream-K tile and rank; left at zero
+};
+
+constexpr int kPartFloats = kBM * 2 * kBN;   // one CTA's 128 x 256 f32 accumulator
+
+// First stream-K iteration of unit u.
+__device__ __forceinline__ int64_t sk_begin(const TileArgs& a, int64_t u) {
+  return u * a.sk_q + (u < a.sk_r ? u : a.sk_r);
+}
+
+// Unit whose range holds stream-K iteration i.
+__device__ __forceinline__ int64_t sk_unit_of(const TileArgs& a, int64_t i) {
+  const int64_t big = a.sk_r * (a.sk_q + 1);
+  return i < big ? i / (a.sk_q + 1) : a.sk_r + (i - big) / a.sk_q;
+}
+
+// The work items of one unit, in order: its whole tiles, then its stream-K
+// range cut at tile boundaries.  An item is a tile and a k-block range.
+struct WorkIter {
+  int64_t t_dp, it, it_end;
+  __device__ WorkIter(const TileArgs& a, int64_t unit) : t_dp(unit) {
+    it = a.sk_iters ? sk_begin(a, unit) : 0;
+    it_end = a.sk_iters ? sk_begin(a, unit + 1) : 0;
+  }
+  __device__ bool next(const TileArgs& a, int64_t n_units, int64_t& t, int& kb0, int& kb1) {
+    if (t_dp < a.dp_tiles) {
+      t = t_dp;
+      kb0 = 0;
+      kb1 = a.n_kb;
+      t_dp += n_units;
+      return true;
+    }
+    if (it < it_end) {
+      const int64_t rel = it / a.n_kb;
+      const int64_t stop = (rel + 1) * a.n_kb < it_end ? (rel + 1) * a.n_kb : it_end;
+      t = a.dp_tiles + rel;
+      kb0 = (int)(it - rel * a.n_kb);
+      kb1 = (int)(stop - rel * a.n_kb);
+      it = stop;
+      return true;
+    }
+    return false;
+  }
 };
 
 constexpr int kSwiGLU = 0;       // accumulator = 128 gate columns | 128 up columns
@@ -113,6 +163,7 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile unsigned* ticket_slot = reinterpret_cast<volatile unsigned*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // In a pair, rank 0 issues the MMAs for both CTAs; each CTA loads its own
@@ -175,10 +226,13 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = !skip;
-      for (int64_t t = unit; ok && t < a.tiles; t += n_units) {
+      WorkIter w(a, unit);
+      int64_t t;
+      int kb0, kb1;
+      while (ok && w.next(a, n_units, t, kb0, kb1)) {
         const int mb = (int)(t % a.n_mb), nb = (int)(t / a.n_mb);
         const int row0 = mb * C::kTileRows + (int)rank * kBM;
-        for (int kb = 0; kb < a.n_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status, a.timeout_ns)) {
             ok = false;
             break;
@@ -238,14 +292,17 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = !skip;
-      for (int64_t t = unit; ok && t < a.tiles; t += n_units) {
+      WorkIter w(a, unit);
+      int64_t t;
+      int kb0, kb1;
+      while (ok && w.next(a, n_units, t, kb0, kb1)) {
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, a.status, a.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(acc * 2 * kBN);
-        for (int kb = 0; kb < a.n_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, a.status, a.timeout_ns)) {
             ok = false;
             break;
@@ -257,7 +314,7 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = smem_desc_sw128(a_addr + kk * 32u, 16u, 1024u);
             const uint64_t bd = smem_desc_sw128(b_addr + kk * b_step, b_lbo, 1024u);
-            const uint32_t accumulate = (kb != 0 || kk != 0) ? 1u : 0u;
+            const uint32_t accumulate = (kb != kb0 || kk != 0) ? 1u : 0u;
             if constexpr (PAIR)
               mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
             else
@@ -299,8 +356,11 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         int stage = 0;
         uint32_t phase = 0;
         bool ok = !skip;
-        for (int64_t t = unit; ok && t < a.tiles; t += n_units) {
-          for (int kb = 0; kb < a.n_kb; ++kb) {
+        WorkIter w(a, unit);
+        int64_t t;
+        int kb0, kb1;
+        while (ok && w.next(a, n_units, t, kb0, kb1)) {
+          for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(&full[stage], phase, abort_flag, a.status, a.timeout_ns)) {
               ok = false;
               break;
@@ -324,15 +384,69 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     constexpr int kPasses = MODE == kSwiGLU ? 1 : 2;   // 128 output columns per pass
     // rank 1 tells rank 0's MMA issuer that an accumulator has been read
     const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(tempty), 0u) : 0u;
+    constexpr int kRanks = PAIR ? 2 : 1;
     int acc = 0;
     uint32_t acc_phase = 0;
-    bool ok = !skip;
-    for (int64_t t = unit; ok && t < a.tiles; t += n_units) {
+    WorkIter w(a, unit);
+    int64_t t;
+    int kb0, kb1;
+    while (!skip && w.next(a, n_units, t, kb0, kb1)) {
       const int mb = (int)(t % a.n_mb), nb = (int)(t / a.n_mb);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, a.status, a.timeout_ns)) break;
       tc_fence_after();
       const int row_base = mb * C::kTileRows + (int)rank * kBM;
       const int64_t grow = (int64_t)row_base + row;       // output row of this thread
+      const uint32_t acc_col = (uint32_t)(acc * 2 * kBN);
+      // A stream-K item holds part of the tile's k range.  This CTA stores its
+      // partial accumulator in its slot (slot = tile - dp_tiles + unit, so the
+      // units of one tile have consecutive slots), frees the accumulator and
+      // takes a ticket; the last of the tile's units to arrive adds all the
+      // partials in k order and runs the epilogue on the sum.
+      const bool whole = kb0 == 0 && kb1 == a.n_kb;
+      const float* seg0 = nullptr;
+      int nseg = 0;
+      if (!whole) {
+        const int64_t rel = t - a.dp_tiles;
+        float* mine = a.part + ((rel + unit) * kRanks + rank) * (int64_t)kPartFloats;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          tmem_ld_x32(tmem + lane_off + acc_col + (uint32_t)(c * 32), v);
+          tmem_wait_ld();
+          // slot layout [32-column chunk][4-column group][row][4]: a warp's
+          // store covers 512 contiguous bytes
+          float4* dst = reinterpret_cast<float4*>(mine + ((int64_t)c * 8 * kBM + row) * 4);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            __stcg(dst + i * kBM, make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                        __uint_as_float(v[4 * i + 2]),
+                                        __uint_as_float(v[4 * i + 3])));
+        }
+        tc_fence_before();
+        if (PAIR && rank == 1)
+          mbar_arrive_remote(tempty0 + (uint32_t)acc * 8u);
+        else
+          mbar_arrive(&tempty[acc]);
+        __threadfence();
+        named_bar_sync(1, kEpiThreads);
+        if (et == 0) *ticket_slot = atomicAdd(a.counters + rel * kRanks + rank, 1u);
+        named_bar_sync(1, kEpiThreads);
+        const unsigned ticket = *ticket_slot;
+        const int64_t u_first = sk_unit_of(a, rel * a.n_kb);
+        nseg = (int)(sk_unit_of(a, rel * a.n_kb + a.n_kb - 1) - u_first + 1);
+        if (ticket + 1u != (unsigned)nseg) {
+          // not the last (or a counter left over by a call that gave up)
+          if (ticket >= (unsigned)nseg && et == 0) atomicOr(a.status, kStatusStaleCounter);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+          continue;
+        }
+        __threadfence();
+        if (et == 0) a.counters[rel * kRanks + rank] = 0u;   // left at zero for the next call
+        seg0 = a.part + ((rel + u_first) * kRanks + rank) * (int64_t)kPartFloats;
+      }
       for (int pass = 0; pass < kPasses; ++pass) {
         if (et == 0) bulk_wait_read0();   // the previous store has read the staging tile
         __syncwarp();
@@ -340,10 +454,43 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t g[32], u[32];
-          const uint32_t col0 = (uint32_t)(acc * 2 * kBN + pass * kBN + ch * 32);
-          tmem_ld_x32(tmem + lane_off + col0, g);
-          if constexpr (MODE == kSwiGLU) tmem_ld_x32(tmem + lane_off + col0 + kBN, u);
-          tmem_wait_ld();
+          if (whole) {
+            const uint32_t col0 = acc_col + (uint32_t)(pass * kBN + ch * 32);
+            tmem_ld_x32(tmem + lane_off + col0, g);
+            if constexpr (MODE == kSwiGLU) tmem_ld_x32(tmem + lane_off + col0 + kBN, u);
+            tmem_wait_ld();
+          } else {
+            // sum of the tile's partials, in k order
+            float gs[32], us[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) gs[i] = us[i] = 0.f;
+            const int cg = pass * 4 + ch;   // 32-column chunk of the gate (or output) columns
+#pragma unroll 1
+            for (int sg = 0; sg < nseg; ++sg) {
+              const float* sp = seg0 + (int64_t)sg * kRanks * kPartFloats;
+              const float4* pg =
+                  reinterpret_cast<const float4*>(sp + ((int64_t)cg * 8 * kBM + row) * 4);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 q = __ldcg(pg + i * kBM);
+                gs[4 * i] += q.x; gs[4 * i + 1] += q.y; gs[4 * i + 2] += q.z; gs[4 * i + 3] += q.w;
+              }
+              if constexpr (MODE == kSwiGLU) {
+                const float4* pu =
+                    reinterpret_cast<const float4*>(sp + ((int64_t)(cg + 4) * 8 * kBM + row) * 4);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float4 q = __ldcg(pu + i * kBM);
+                  us[4 * i] += q.x; us[4 * i + 1] += q.y; us[4 * i + 2] += q.z; us[4 * i + 3] += q.w;
+                }
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              g[i] = __float_as_uint(gs[i]);
+              u[i] = __float_as_uint(us[i]);
+            }
+          }
           float rv[32];
           if constexpr (MODE == kPlain) {
             // residual row segment: 32 bf16 of this output row
@@ -382,7 +529,7 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             *reinterpret_cast<uint4*>(rowp + chunk * 16) = v;
           }
         }
-        if (pass == kPasses - 1) {
+        if (whole && pass == kPasses - 1) {
           // every accumulator column of this buffer has been read
           tc_fence_before();
           if (PAIR && rank == 1)
@@ -435,8 +582,8 @@ int tile_env_int(const char* name, int dflt) {
 
 }  // namespace
 
-TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain) {
-  (void)K;
+TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
+                   int max_pairs) {
   TilePlan p{};
   const int64_t cols = plain ? 2 * kBN : kBN;
   p.plain = plain;
@@ -444,16 +591,81 @@ TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain)
   // SWIGLU_TILE_PAIR = 0 / 1 forces one mode.
   const int forced = tile_env_int("SWIGLU_TILE_PAIR", -1);
   p.pair = forced >= 0 ? forced != 0 : M > kBM;
-  if (num_sms < 2) p.pair = false;
+  if (num_sms < 2 || max_pairs < 1) p.pair = false;
   const int64_t rows = p.pair ? 2 * kBM : kBM;
   p.n_mb = (M + rows - 1) / rows;
   p.n_nb = (n_out + cols - 1) / cols;
+  p.n_kb = (K + kBK - 1) / kBK;
   p.tiles = p.n_mb * p.n_nb;
-  const int64_t units = p.pair ? num_sms / 2 : num_sms;   // CTAs or CTA pairs at once
-  int64_t g = p.tiles < units ? p.tiles : units;
-  if (g < 1) g = 1;
-  p.grid = (int)(p.pair ? 2 * g : g);
+  // units: CTAs, or CTA pairs, that run at once
+  int64_t units = p.pair ? (num_sms / 2 < max_pairs ? num_sms / 2 : max_pairs) : num_sms;
+  if (units < 1) units = 1;
+  p.dp_tiles = p.tiles;
+  // Stream-K tail.  With W full waves and a partial one, the last wave plus
+  // one full wave (all tiles if W = 0) are split along K over the units, in
+  // equal contiguous shares of (tile, k-block) iterations; the rest are done
+  // whole.  With W = 0 a tile is split over at most 4 units
+  // (SWIGLU_TILE_SK_SPLIT), which bounds the partials its final reduction
+  // reads.  Measured on GB300, it pays only where whole tiles would leave
+  // most units idle: the down projection at d = 4096 with M = 64 / 256 (16
+  // tiles) ran in 48 / 52 us instead of 97 / 84 us.  Where the tiles fill
+  // >= 3/4 of a wave or more than one wave it was 4-35 % slower: units at
+  // different k offsets no longer share weight and x tiles through L2, so
+  // operands are re-read from DRAM.  So it is used when whole tiles keep
+  // < 30 % of the units busy and each unit gets >= 4 k-blocks.
+  // SWIGLU_TILE_SK = 0 / 1 forces it off / on (on: wherever there is a
+  // partial wave).
+  const int forced_sk = tile_env_int("SWIGLU_TILE_SK", -1);
+  int max_split = tile_env_int("SWIGLU_TILE_SK_SPLIT", 4);
+  if (max_split < 2) max_split = 2;
+  const int64_t waves = p.tiles / units, rem = p.tiles % units;
+  if (p.tiles > 0 && p.n_kb > 0 && rem != 0 && forced_sk != 0) {
+    const int64_t sk_tiles = waves >= 1 ? units + rem : p.tiles;
+    int64_t g = units;
+    if (waves == 0 && p.tiles * max_split < g) g = p.tiles * max_split;
+    const int64_t iters = sk_tiles * p.n_kb;
+    const int64_t q = iters / g;
+    const double busy = (double)p.tiles / (double)((waves + 1) * units);
+    const bool want = forced_sk == 1 ? q >= 1 : (busy < 0.3 && q >= 4);
+    if (want && g > 1) {
+      units = g;
+      p.dp_tiles = p.tiles - sk_tiles;
+      p.sk_iters = iters;
+      p.sk_q = q;
+      p.sk_r = iters % g;
+    }
+  }
+  int64_t gu = p.sk_iters ? units : (p.tiles < units ? p.tiles : units);
+  if (gu < 1) gu = 1;
+  p.grid = (int)(p.pair ? 2 * gu : gu);
+  if (p.sk_iters) {
+    const int64_t ranks = p.pair ? 2 : 1;
+    const int64_t sk_tiles = p.tiles - p.dp_tiles;
+    p.counters_bytes = ((size_t)(sk_tiles * ranks) * sizeof(unsigned) + 255) / 256 * 256;
+    // one slot per (stream-K tile, unit) pair that shares a tile: at most
+    // sk_tiles + units slots (slot = tile - dp_tiles + unit)
+    p.part_bytes = (size_t)((sk_tiles + gu) * ranks) * kPartFloats * sizeof(float);
+  }
   return p;
+}
+
+cudaError_t tile_max_pairs(int* pairs) {
+  auto kern = tile_tc_kernel<kSwiGLU, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)TileCfg<true>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = TileCfg<true>::kSmemBytes;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(pairs, kern, &cfg);
 }
 
 namespace {
@@ -464,10 +676,17 @@ cudaError_t launch_mode(const CUtensorMap& mx, const CUtensorMap& mg, const CUte
   using C = TileCfg<PAIR>;
   auto kern = tile_tc_kernel<MODE, PAIR>;
   static int configured[64] = {0};
-  static int max_clusters[64] = {0};   // co-resident CTA pairs, per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) configured[dev] = 1;
+  }
+  // The grid is the plan's: the stream-K shares assume exactly this many
+  // units (the plan already caps pairs at what can run at once).
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -482,27 +701,6 @@ cudaError_t launch_mode(const CUtensorMap& mx, const CUtensorMap& mg, const CUte
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 2 : 1;
-  if (dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    int mc = 0;
-    if (PAIR) {
-      // The persistent grid takes no more pairs than can run at once (pairs
-      // need both SMs of a cluster slot, so this may be below SMs / 2).
-      e = cudaOccupancyMaxActiveClusters(&mc, kern, &cfg);
-      if (e != cudaSuccess) return e;
-      if (mc < 1) return cudaErrorInvalidConfiguration;
-    }
-    if (dev < 64) {
-      max_clusters[dev] = mc;
-      configured[dev] = 1;
-    } else if (PAIR && grid > 2 * mc) {
-      cfg.gridDim = dim3((unsigned)(2 * mc));
-    }
-  }
-  if (PAIR && dev < 64 && grid > 2 * max_clusters[dev])
-    cfg.gridDim = dim3((unsigned)(2 * max_clusters[dev]));
   return cudaLaunchKernelEx(&cfg, kern, mx, mg, mu, mh, a);
 }
 
@@ -510,9 +708,11 @@ cudaError_t launch_mode(const CUtensorMap& mx, const CUtensorMap& mg, const CUte
 
 cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* out,
                            const void* resid, int64_t M, int64_t K, int64_t n_out,
-                           bool w_kmajor, const TilePlan& p, unsigned* status,
-                           uint64_t timeout_ns, cudaStream_t st) {
+                           bool w_kmajor, const TilePlan& p, float* part, unsigned* counters,
+                           bool counters_clean, unsigned* status, uint64_t timeout_ns,
+                           cudaStream_t st) {
   if (p.tiles == 0 || K == 0) return cudaSuccess;
+  if (p.sk_iters && (!part || !counters)) return cudaErrorInvalidValue;
   CUtensorMap mx, mg, mu, mh;
   cudaError_t e;
   if ((e = make_tmap_bf16_2d(&mx, x, M, K, kBK, kBM)) != cudaSuccess) return e;
@@ -535,6 +735,16 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
   a.kmajor = w_kmajor ? 1 : 0;
   a.status = status;
   a.timeout_ns = timeout_ns;
+  a.dp_tiles = p.dp_tiles;
+  a.sk_iters = p.sk_iters;
+  a.sk_q = p.sk_q;
+  a.sk_r = p.sk_r;
+  a.part = part;
+  a.counters = counters;
+  // Stream-K arrival counters must be zero on entry.
+  if (p.sk_iters && !counters_clean &&
+      (e = cudaMemsetAsync(counters, 0, p.counters_bytes, st)) != cudaSuccess)
+    return e;
   if (p.pair)
     return p.plain ? launch_mode<kPlain, true>(mx, mg, mu, mh, a, p.grid, st)
                    : launch_mode<kSwiGLU, true>(mx, mg, mu, mh, a, p.grid, st);

@@ -264,7 +264,10 @@ def test_caller_workspace_and_errors(path, monkeypatch):
     with pytest.raises(swg.SwiGLUError) as e:
         swg.swiglu_up(x, wg, wu, path=path, workspace=ws[16:16 + need])
     assert e.value.status == 8
-    assert swg.workspace_bytes(M, d, d_ff, "bf16", "tc") == 0
+    # tc: M = 3 is one 128-row tile per 128 columns, 16 tiles < SMs: stream-K
+    assert swg.workspace_bytes(M, d, d_ff, "bf16", "tc") > 0
+    # whole waves (prefill shape, 1792 pair tiles) need none
+    assert swg.workspace_bytes(4096, 4096, 14336, "bf16", "tc") == 0
 
 
 def test_misaligned_pointer_rejected():
