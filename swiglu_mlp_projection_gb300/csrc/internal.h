@@ -20,14 +20,20 @@ struct SimtPlan {
   int cols_per_cta; // 32 lanes x vec
   int row_chunk;    // rows of x per CTA (1, 2 or 4)
   int64_t col_blocks, row_chunks, slices, k_per_slice;
+  bool fused;       // single launch: the last slice of a column block reduces
+  size_t counters_bytes;   // arrival counters of the single launch
 };
 
 SimtPlan plan_simt(int64_t M, int64_t d, int64_t d_ff, int dtype, int num_sms);
 
-// S1 (SIMT): partial sums of x.Wg and x.Wu per K slice.
+// S1 (SIMT): partial sums of x.Wg and x.Wu per K slice.  With `counters`
+// (p.fused plans; zero on entry unless !counters_clean, left at zero) the
+// same launch also reduces them and writes h: no S2 launch follows.
 cudaError_t launch_simt_partial(const void* x, const void* wg, const void* wu,
                                 float* part, int64_t M, int64_t d, int64_t d_ff,
-                                int dtype, const SimtPlan& p, cudaStream_t st);
+                                int dtype, const SimtPlan& p, cudaStream_t st,
+                                unsigned* counters = nullptr, bool counters_clean = false,
+                                void* h = nullptr);
 
 // S2: fixed-order sum over slices, then h = silu(g) * u rounded to dtype.
 cudaError_t launch_reduce_swiglu(const float* part, void* h, int64_t M,

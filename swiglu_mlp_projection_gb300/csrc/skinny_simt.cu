@@ -9,8 +9,13 @@
 // takes every 8th k of the slice.  Each thread keeps 4 k-rows of both
 // matrices in flight before using them.  The 8 warp sums are combined through
 // shared memory in warp order, and each slice writes its partial sum; the
-// reduction kernel (reduce_swiglu.cu) adds the slices in slice order, so the
-// result does not depend on CTA scheduling.
+// slices are then added in slice order, so the result does not depend on CTA
+// scheduling.  That sum and the SwiGLU epilogue run either in the reduction
+// kernel (reduce_swiglu.cu) or, in the single-launch form, in this kernel:
+// the last CTA of a column block to finish (an atomic ticket; nothing waits)
+// adds the slices, exactly as the reduction kernel does, and stores h.  The
+// page's "Ce qui reste : les lancements" finds the second launch to be a
+// large part of a small product's time.
 //
 // Differences from the page's design, for GB300: 16-byte loads (4 f32 or
 // 8 bf16 per lane instead of one f32), both weight matrices streamed by the
@@ -18,6 +23,8 @@
 // the slice target scaled to this GPU's SM count.  This path serves f32 (all
 // M) and is the CUDA-core reference path for bf16; the tensor-core paths
 // serve bf16 by default.
+#include <stdlib.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -46,11 +53,15 @@ __device__ __forceinline__ void unpack16(const uint4& v, float* f) {
   }
 }
 
+// counters == null: write the partial sums only.  Otherwise (single launch)
+// counters holds one arrival counter per (column block, row chunk), zero on
+// entry and left at zero, and the last CTA of each writes h.
 template <bool BF16, int RC>
 __global__ void __launch_bounds__(kThreads)
 simt_partial_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
                     const void* __restrict__ wu_, float* __restrict__ part,
-                    int M, int d, int d_ff, int ks) {
+                    int M, int d, int d_ff, int ks, unsigned* __restrict__ counters,
+                    void* __restrict__ h) {
   constexpr int VEC = BF16 ? 8 : 4;
   constexpr int C = 32 * VEC;
   constexpr int ES = BF16 ? 2 : 4;
@@ -149,12 +160,50 @@ simt_partial_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
       part[(((size_t)s * M + row) * 2 + gu) * d_ff + j] = sum;
     }
   }
+  if (!counters) return;
+
+  // Single launch: the last slice of this column block and row chunk to
+  // arrive sums the slices in slice order and applies the epilogue.
+  __shared__ unsigned ticket;
+  __threadfence();
+  __syncthreads();
+  unsigned* ctr = counters + (size_t)blockIdx.z * gridDim.x + blockIdx.x;
+  if (threadIdx.x == 0) ticket = atomicAdd(ctr, 1u);
+  __syncthreads();
+  if (ticket + 1u != gridDim.y) return;
+  __threadfence();
+  // one thread = 4 adjacent outputs of one row (d_ff is a multiple of 4),
+  // the same sums and rounding as the reduction kernel
+  for (int t = threadIdx.x; t < RC * (C / 4); t += kThreads) {
+    const int r = t / (C / 4), row = row0 + r;
+    const int j = blockIdx.x * C + (t - r * (C / 4)) * 4;
+    if (row >= M || j >= d_ff) continue;
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+    for (int q = 0; q < (int)gridDim.y; ++q) {
+      const float* pg = part + (((size_t)q * M + row) * 2) * d_ff + j;
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(pg));
+      const float4 b = __ldcg(reinterpret_cast<const float4*>(pg + d_ff));
+      g.x += a.x; g.y += a.y; g.z += a.z; g.w += a.w;
+      u.x += b.x; u.y += b.y; u.z += b.z; u.w += b.w;
+    }
+    if constexpr (BF16) {
+      uint2 o;
+      o.x = pack_bf16x2(silu_fast(g.x) * u.x, silu_fast(g.y) * u.y);
+      o.y = pack_bf16x2(silu_fast(g.z) * u.z, silu_fast(g.w) * u.w);
+      *reinterpret_cast<uint2*>((uint16_t*)h + (size_t)row * d_ff + j) = o;
+    } else {
+      *reinterpret_cast<float4*>((float*)h + (size_t)row * d_ff + j) =
+          make_float4(silu_accurate(g.x) * u.x, silu_accurate(g.y) * u.y,
+                      silu_accurate(g.z) * u.z, silu_accurate(g.w) * u.w);
+    }
+  }
+  if (threadIdx.x == 0) *ctr = 0u;   // left at zero for the next call
 }
 
 template <bool BF16, int RC>
 cudaError_t launch_one(const void* x, const void* wg, const void* wu, float* part,
                        int64_t M, int64_t d, int64_t d_ff, const SimtPlan& p,
-                       cudaStream_t st) {
+                       unsigned* counters, void* h, cudaStream_t st) {
   constexpr int VEC = BF16 ? 8 : 4;
   constexpr int C = 32 * VEC;
   const size_t x_bytes = (size_t)RC * p.k_per_slice * sizeof(float);
@@ -185,7 +234,7 @@ cudaError_t launch_one(const void* x, const void* wg, const void* wu, float* par
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, x, wg, wu, part, (int)M, (int)d, (int)d_ff,
-                            (int)p.k_per_slice);
+                            (int)p.k_per_slice, counters, h);
 }
 
 }  // namespace
@@ -213,21 +262,33 @@ SimtPlan plan_simt(int64_t M, int64_t d, int64_t d_ff, int dtype, int num_sms) {
   ks = (ks + 7) / 8 * 8;
   p.k_per_slice = ks;
   p.slices = (d + ks - 1) / ks;
+  // Single launch wherever the arrival counters fit the per-stream counter
+  // region (every decode shape); SWIGLU_SIMT_FUSED = 0 keeps two launches.
+  const char* env = getenv("SWIGLU_SIMT_FUSED");
+  const int64_t n_ctr = p.col_blocks * p.row_chunks;
+  p.fused = (!env || atoi(env) != 0) && n_ctr * (int64_t)sizeof(unsigned) <= (int64_t)kStreamCounterBytes;
+  p.counters_bytes = p.fused ? ((size_t)n_ctr * sizeof(unsigned) + 255) / 256 * 256 : 0;
   return p;
 }
 
 cudaError_t launch_simt_partial(const void* x, const void* wg, const void* wu,
                                 float* part, int64_t M, int64_t d, int64_t d_ff,
-                                int dtype, const SimtPlan& p, cudaStream_t st) {
+                                int dtype, const SimtPlan& p, cudaStream_t st,
+                                unsigned* counters, bool counters_clean, void* h) {
   if (p.slices == 0) return cudaSuccess;
+  if (counters && !counters_clean) {
+    cudaError_t e = cudaMemsetAsync(counters, 0, p.counters_bytes, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (!counters) h = nullptr;
   const bool bf16 = dtype == 1;
   switch (p.row_chunk) {
-    case 1: return bf16 ? launch_one<true, 1>(x, wg, wu, part, M, d, d_ff, p, st)
-                        : launch_one<false, 1>(x, wg, wu, part, M, d, d_ff, p, st);
-    case 2: return bf16 ? launch_one<true, 2>(x, wg, wu, part, M, d, d_ff, p, st)
-                        : launch_one<false, 2>(x, wg, wu, part, M, d, d_ff, p, st);
-    default: return bf16 ? launch_one<true, 4>(x, wg, wu, part, M, d, d_ff, p, st)
-                         : launch_one<false, 4>(x, wg, wu, part, M, d, d_ff, p, st);
+    case 1: return bf16 ? launch_one<true, 1>(x, wg, wu, part, M, d, d_ff, p, counters, h, st)
+                        : launch_one<false, 1>(x, wg, wu, part, M, d, d_ff, p, counters, h, st);
+    case 2: return bf16 ? launch_one<true, 2>(x, wg, wu, part, M, d, d_ff, p, counters, h, st)
+                        : launch_one<false, 2>(x, wg, wu, part, M, d, d_ff, p, counters, h, st);
+    default: return bf16 ? launch_one<true, 4>(x, wg, wu, part, M, d, d_ff, p, counters, h, st)
+                         : launch_one<false, 4>(x, wg, wu, part, M, d, d_ff, p, counters, h, st);
   }
 }
 

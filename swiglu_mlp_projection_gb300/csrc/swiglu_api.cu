@@ -326,8 +326,8 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
       return fail(SWIGLU_ERR_UNSUPPORTED, "shape exceeds the grid limits of the SIMT path");
     p->slices = p->simt.slices;
     p->grid = p->simt.col_blocks * p->simt.slices * p->simt.row_chunks;
-    p->workspace = partial_elems(p->slices, M, n_out) * sizeof(float);
-    p->launches = p->slices > 0 ? 2 : 1;
+    p->workspace = p->simt.counters_bytes + partial_elems(p->slices, M, n_out) * sizeof(float);
+    p->launches = p->slices > 0 && !p->simt.fused ? 2 : 1;
   } else if (rp == SWIGLU_PATH_SKINNY) {
     p->skinny = plan_skinny(M, K, n_out, num_sms, plain);
     // K slices per column group: the cluster size, or (stream-K) at most maxq
@@ -375,6 +375,19 @@ int run(const Call& c) {
   if (c.kmajor && p.path == SWIGLU_PATH_SIMT && c.K > 0)
     return fail(SWIGLU_ERR_UNSUPPORTED,
                 "[N, K] weights are served by the tensor-core paths (bf16) only");
+  if (p.path == SWIGLU_PATH_SIMT && p.simt.fused) {
+    // Inside a CUDA graph the workspace is a fresh allocation per call whose
+    // counters would need a memset node; two kernel nodes cost less.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(c.st, &cs) != cudaSuccess) {
+      cudaGetLastError();
+    } else if (cs != cudaStreamCaptureStatusNone) {
+      p.simt.fused = false;
+      p.simt.counters_bytes = 0;
+      p.workspace = (partial_elems(p.slices, c.M, c.n_out) * sizeof(float) + 255) / 256 * 256;
+      p.launches = 2;
+    }
+  }
   if (c.M == 0 || c.n_out == 0) {
     t_err[0] = 0;
     return SWIGLU_OK;
@@ -403,7 +416,7 @@ int run(const Call& c) {
   void* pooled = nullptr;
   const size_t counter_bytes = p.path == SWIGLU_PATH_SKINNY ? p.skinny.counters_bytes
                                : p.path == SWIGLU_PATH_TC   ? p.tile.counters_bytes
-                                                            : 0;
+                                                            : p.simt.counters_bytes;
   cudaStream_t st = c.st;
   if (p.workspace > 0) {
     if (c.workspace) {
@@ -436,7 +449,10 @@ int run(const Call& c) {
   }
 
   cudaError_t e = cudaSuccess;
-  if (p.path == SWIGLU_PATH_SIMT) {
+  if (p.path == SWIGLU_PATH_SIMT && p.simt.fused) {
+    e = launch_simt_partial(c.x, c.wa, c.wb, part, c.M, c.K, c.n_out, c.dtype, p.simt, st,
+                            counters, counters_clean, c.out);
+  } else if (p.path == SWIGLU_PATH_SIMT) {
     e = launch_simt_partial(c.x, c.wa, c.wb, part, c.M, c.K, c.n_out, c.dtype, p.simt, st);
     if (e == cudaSuccess)
       e = launch_reduce_swiglu(part, c.out, c.M, c.n_out, p.slices, c.dtype, di.num_sms, st);

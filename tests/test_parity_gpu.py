@@ -297,3 +297,24 @@ def test_non_default_stream_and_raw_abi():
     h64, _, sens = oracle.swiglu_up(raw(x), raw(wg), raw(wu), oracle.BF16)
     assert compare(to64(h), h64, sens, "bf16", d)["ok"]
     swg.check_device_status()
+
+
+@pytest.mark.parametrize("dtype,shape", [("f32", (1, 512, 2048)), ("f32", (5, 1000, 1032)),
+                                         ("bf16", (3, 520, 264)), ("f32", (17, 64, 2056))])
+def test_simt_single_launch_matches_two_launches(dtype, shape, monkeypatch):
+    # The SIMT path reduces its K slices either in a second kernel or, in one
+    # launch, in the last CTA of each column block; both add the slices in
+    # the same order, so the results are bit-identical.
+    M, d, d_ff = shape
+    dev = torch.device("cuda", 0)
+    x, wg, wu = (t.to(dev) for t in inputs.make_inputs(M, d, d_ff, dtype, seed=M + d))
+    out = {}
+    for fused in ("0", "1"):
+        monkeypatch.setenv("SWIGLU_SIMT_FUSED", fused)
+        assert swg.plan(M, d, d_ff, dtype, "simt", 152)["launches"] == (1 if fused == "1" else 2)
+        out[fused] = swg.swiglu_up(x, wg, wu, path="simt")
+        swg.swiglu_up(x, wg, wu, path="simt", out=out[fused])   # counters left at zero
+    torch.cuda.synchronize()
+    view = torch.int32 if dtype == "f32" else torch.int16
+    assert torch.equal(out["0"].view(view), out["1"].view(view))
+    full_check(M, d, d_ff, dtype, "simt", seed=M + d)
