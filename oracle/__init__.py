@@ -12,14 +12,17 @@ layouts per "Ou part le temps d'un token", "Un kernel pour les matrices
 etroites" (row-major weights, (k)*cols + col).
 
 The down projection (y = h . W_down + r, the anatomy chapter's kernels #10
-and #11) and the two-operation MLP are evaluated the same way.
+and #11) and the two-operation MLP are evaluated the same way.  ``pack``
+writes the gate/up-interleaved weight matrix of the SwiGLU paper's Kernel-2
+(64-column blocks), a copy of element bits.
 
 Parity pins (tests/test_oracle.py, tests/test_oracle_down.py): exact
 small-integer brute force, the silu
 identities silu(z) - silu(-z) = z and silu(z) = z (1 + tanh(z/2)) / 2,
 high-precision decimal evaluation, one-hot x, zeroed columns, column
 permutation, h(x) + h(-x) = g (.) u, power-of-two scaling, row independence,
-numpy fp64 matmul at realistic sizes, and torch's bf16 rounding.  Every oracle
+numpy fp64 matmul at realistic sizes, and torch's bf16 rounding; the packing
+against a reshape-based unpacking and a worked example (tests/test_oracle_pack.py).  Every oracle
 function is pinned; none is marked "parity unpinned".
 """
 import ctypes
@@ -61,6 +64,8 @@ def _load():
         lib.oracle_round_to_dtype.restype = ip
         lib.oracle_down_proj.argtypes = [vp, vp, vp, i64, i64, i64, ip, vp, vp, vp]
         lib.oracle_down_proj.restype = ip
+        lib.oracle_pack.argtypes = [vp, vp, i64, i64, ip, vp]
+        lib.oracle_pack.restype = ip
         _lib = lib
     return _lib
 
@@ -187,6 +192,22 @@ def down_proj(h, wd, dtype, r=None):
     if rc != 0:
         raise RuntimeError("oracle_down_proj failed (%d)" % rc)
     return y64, yr, sens
+
+
+def pack(wg, wu, dtype):
+    """Step a0: the packed weight matrix [d, 2P] (P = d_ff rounded up to 64),
+    64-column blocks of Wg and Wu alternating, zero past d_ff; raw bits."""
+    lib = _load()
+    wg, wu = _raw(wg, dtype), _raw(wu, dtype)
+    if wg.shape != wu.shape:
+        raise ValueError("shape mismatch")
+    d, d_ff = wg.shape
+    width = 2 * 64 * ((d_ff + 63) // 64)
+    out = np.empty((d, width), wg.dtype)
+    rc = lib.oracle_pack(_ptr(wg), _ptr(wu), d, d_ff, dtype, _ptr(out))
+    if rc != 0:
+        raise RuntimeError("oracle_pack failed (%d)" % rc)
+    return out
 
 
 def mlp(x, wg, wu, wd, dtype, r=None, nthreads=None):

@@ -306,3 +306,47 @@ int oracle_down_proj(const void* h, const void* wd, const void* r, int64_t M, in
   free(acc);
   return 0;
 }
+
+/* ---- weight packing (step a0) ------------------------------------------- */
+
+/*
+ * "Tile-Level Activation Overlap for Efficient LLM Inference", Kernel-2:
+ * the gate and up weight columns are interleaved once, before any GEMM, so
+ * that one tile of the packed matrix holds matching gate and up columns.
+ * The interleave unit here is a block of 64 columns.  With
+ * P = ceil(d_ff / 64) * 64, packed row k (2P elements) is
+ *     Wg[k, 0:64] | Wu[k, 0:64] | Wg[k, 64:128] | Wu[k, 64:128] | ...
+ * and an element whose column j = 64 t + i is >= d_ff is zero.  The packing
+ * is a copy of element bits: nothing is rounded.
+ *   wg, wu  [d, d_ff] row-major, element type `dtype`
+ *   packed  [d, 2P], same element type
+ * Returns 0 on success.
+ */
+int oracle_pack(const void* wg, const void* wu, int64_t d, int64_t d_ff, int dtype,
+                void* packed) {
+  if (d < 0 || d_ff < 0) return 2;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return 2;
+  const size_t es = dtype == ORACLE_BF16 ? 2 : 4;
+  const int64_t tiles = (d_ff + 63) / 64, width = 2 * 64 * tiles;
+  const unsigned char* g = (const unsigned char*)wg;
+  const unsigned char* u = (const unsigned char*)wu;
+  unsigned char* out = (unsigned char*)packed;
+  for (int64_t k = 0; k < d; ++k) {
+    for (int64_t t = 0; t < tiles; ++t) {
+      for (int64_t i = 0; i < 64; ++i) {
+        const int64_t j = 64 * t + i;
+        unsigned char* dg = out + ((size_t)(k * width + 128 * t + i)) * es;
+        unsigned char* du = out + ((size_t)(k * width + 128 * t + 64 + i)) * es;
+        if (j < d_ff) {
+          memcpy(dg, g + (size_t)(k * d_ff + j) * es, es);
+          memcpy(du, u + (size_t)(k * d_ff + j) * es, es);
+        } else {
+          memset(dg, 0, es);
+          memset(du, 0, es);
+        }
+      }
+    }
+  }
+  return 0;
+}
+
