@@ -153,6 +153,37 @@ SWIGLU_API int swiglu_down_nk(const void* h, const void* w_down_nk, const void* 
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Weight packing (step a0).  "Tile-Level Activation Overlap for Efficient
+ * LLM Inference", Kernel-2, interleaves the gate and up weight columns once,
+ * before any GEMM, so that one tile of the packed matrix holds matching gate
+ * and up columns.  Here the interleave unit is a block of 64 columns:
+ *
+ *     w_packed [d, 2P], P = ceil(d_ff / 64) * 64, row k =
+ *         W_gate[k, 0:64] | W_up[k, 0:64] | W_gate[k, 64:128] | W_up[k, 64:128] | ...
+ *
+ * with zeros where a column index reaches d_ff.  The packing copies element
+ * bits (nothing is rounded) and is done once per weight set, off the
+ * per-call path.
+ *
+ * swiglu_packed_weight_bytes: size of w_packed (d * 2P * element size), or 0
+ *   for invalid sizes.  Host-only.
+ * swiglu_pack_weights: writes w_packed from w_gate and w_up (both [d, d_ff]
+ *   row-major), asynchronously on `stream`.  w_packed is caller-owned device
+ *   memory of swiglu_packed_weight_bytes bytes, 16-byte aligned, overlapping
+ *   neither input.  Errors: SWIGLU_ERR_INVALID_ARG, _ALIGNMENT, _ARCH, _CUDA.
+ * swiglu_up_packed: as swiglu_up_ex, reading both weight matrices from
+ *   w_packed; every path and dtype of swiglu_up_ex is served, and workspace
+ *   sizes are those of swiglu_workspace_bytes.  h [M, d_ff] must not overlap
+ *   x or w_packed.
+ */
+SWIGLU_API size_t swiglu_packed_weight_bytes(int64_t d, int64_t d_ff, int dtype);
+SWIGLU_API int swiglu_pack_weights(const void* w_gate, const void* w_up, void* w_packed,
+                                   int64_t d, int64_t d_ff, int dtype, void* stream);
+SWIGLU_API int swiglu_up_packed(const void* x, const void* w_packed, void* h, int64_t M,
+                                int64_t d, int64_t d_ff, int dtype, int path, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
  * The whole MLP of "1 . Anatomie d'un transformeur sur GPU", section 1.1,
  * after its RMSNorm: h = silu(x . W_gate) (.) (x . W_up), then
  * y = h . W_down (+ residual).  Two kernels on `stream`; h [M, d_ff] is the

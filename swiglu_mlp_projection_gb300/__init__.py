@@ -99,6 +99,82 @@ def swiglu_up(x, w_gate, w_up, out=None, path="auto", workspace=None, stream=Non
     return out
 
 
+def _call(index, fn, *args):
+    import torch
+    if torch.cuda.current_device() != index:
+        with torch.cuda.device(index):
+            status = fn(*args)
+    else:
+        status = fn(*args)
+    if status:
+        _lib.check(status)
+
+
+def packed_weight_bytes(d, d_ff, dtype="bf16"):
+    """Bytes of the packed gate/up matrix for [d, d_ff] weights (host-only)."""
+    dt = BF16 if dtype in ("bf16", BF16) else F32
+    n = int(_lib.load().swiglu_packed_weight_bytes(d, d_ff, dt))
+    if n == 0 and d * d_ff > 0:
+        _lib.check(1)   # invalid sizes (detail in the library's error string)
+    return n
+
+
+def pack_weights(w_gate, w_up, out=None, stream=None):
+    """Step a0: pack w_gate and w_up ([d, d_ff], contiguous CUDA tensors of one
+    dtype) into one [d, 2 P] matrix (P = d_ff rounded up to 64) whose 64-column
+    blocks alternate gate, up (zero past d_ff).  The copy runs on the current
+    (or given) stream; returns the packed tensor (``out`` if given)."""
+    global _LIB
+    import torch
+    _check_cuda(w_gate=w_gate, w_up=w_up)
+    if w_gate.dim() != 2 or w_up.shape != w_gate.shape or w_up.dtype != w_gate.dtype:
+        raise ValueError("expected w_gate and w_up of one shape [d, d_ff] and dtype")
+    d, d_ff = w_gate.shape
+    width = 128 * ((d_ff + 63) // 64)
+    if out is None:
+        out = torch.empty((d, width), dtype=w_gate.dtype, device=w_gate.device)
+    elif out.shape != (d, width) or out.dtype != w_gate.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [d, %d] tensor of the weights' dtype" % width)
+    index = w_gate.device.index
+    st = stream.cuda_stream if stream is not None else _raw_stream(index)
+    if _LIB is None:
+        _LIB = _lib.load()
+    _call(index, _LIB.swiglu_pack_weights, w_gate.data_ptr(), w_up.data_ptr(), out.data_ptr(),
+          d, d_ff, _dtype_code(w_gate), st)
+    return out
+
+
+def swiglu_up_packed(x, w_packed, d_ff, out=None, path="auto", workspace=None, stream=None):
+    """h = silu(x @ W_gate) * (x @ W_up) with both weights read from the packed
+    matrix of ``pack_weights`` (w_packed [d, 2 P]); d_ff is the unpadded
+    output width.  Arguments and result otherwise as ``swiglu_up``."""
+    global _LIB
+    import torch
+    _check_cuda(x=x, w_packed=w_packed)
+    if x.dim() != 2 or w_packed.dim() != 2 or w_packed.shape[0] != x.shape[1]:
+        raise ValueError("expected x [M, d] and w_packed [d, 2P]")
+    if w_packed.shape[1] != 128 * ((d_ff + 63) // 64):
+        raise ValueError("w_packed has %d columns; d_ff=%d needs %d"
+                         % (w_packed.shape[1], d_ff, 128 * ((d_ff + 63) // 64)))
+    if w_packed.dtype != x.dtype:
+        raise TypeError("x and w_packed must share one dtype")
+    M, d = x.shape
+    if out is None:
+        out = torch.empty((M, d_ff), dtype=x.dtype, device=x.device)
+    elif out.shape != (M, d_ff) or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, d_ff] tensor of x's dtype")
+    index = x.device.index
+    st = stream.cuda_stream if stream is not None else _raw_stream(index)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    if _LIB is None:
+        _LIB = _lib.load()
+    _call(index, _LIB.swiglu_up_packed, x.data_ptr(), w_packed.data_ptr(), out.data_ptr(), M, d,
+          d_ff, _dtype_code(x), _path_code(path), ws_ptr, ws_bytes, st)
+    return out
+
+
 def _check_cuda(**tensors):
     for name, t in tensors.items():
         if t is None:

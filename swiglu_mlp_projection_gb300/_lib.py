@@ -41,6 +41,9 @@ SIGNATURES = {
     "swiglu_down_workspace_bytes": ([_i64, _i64, _i64, _int, _int], _sz),
     "swiglu_up_nk": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp, _sz, _vp], _int),
     "swiglu_down_nk": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp, _sz, _vp], _int),
+    "swiglu_packed_weight_bytes": ([_i64, _i64, _int], _sz),
+    "swiglu_pack_weights": ([_vp, _vp, _vp, _i64, _i64, _int, _vp], _int),
+    "swiglu_up_packed": ([_vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp, _sz, _vp], _int),
     "swiglu_mlp": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp], _int),
     "swiglu_down_plan": ([_i64, _i64, _i64, _int, _int, _int, ctypes.POINTER(PlanInfo)], _int),
     "swiglu_workspace_bytes": ([_i64, _i64, _i64, _int, _int], _sz),

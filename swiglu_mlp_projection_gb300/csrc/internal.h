@@ -29,11 +29,27 @@ SimtPlan plan_simt(int64_t M, int64_t d, int64_t d_ff, int dtype, int num_sms);
 // S1 (SIMT): partial sums of x.Wg and x.Wu per K slice.  With `counters`
 // (p.fused plans; zero on entry unless !counters_clean, left at zero) the
 // same launch also reduces them and writes h: no S2 launch follows.
+// `packed`: wg (= wu) is a packed weight matrix (kWeightsPacked).
 cudaError_t launch_simt_partial(const void* x, const void* wg, const void* wu,
                                 float* part, int64_t M, int64_t d, int64_t d_ff,
                                 int dtype, const SimtPlan& p, cudaStream_t st,
                                 unsigned* counters = nullptr, bool counters_clean = false,
-                                void* h = nullptr);
+                                void* h = nullptr, bool packed = false);
+
+// How the weights are stored:
+//   kWeightsKN      [K, n_out] row-major (the default);
+//   kWeightsNK      [n_out, K], K contiguous (torch.nn.Linear.weight);
+//   kWeightsPacked  one [K, packed_cols(n_out)] matrix for W_gate and W_up
+//                   (up projection only), see launch_pack.
+enum WeightLayout : int { kWeightsKN = 0, kWeightsNK = 1, kWeightsPacked = 2 };
+
+// Step a0: packed weights [d, packed_cols(d_ff)], 64-column blocks of W_gate
+// and W_up alternating (zero past d_ff).  A packed matrix is read by the
+// up-projection kernels with gate block b at packed column 128 b and up
+// block b at 128 b + 64.
+int64_t packed_cols(int64_t d_ff);
+cudaError_t launch_pack(const void* wg, const void* wu, void* out, int64_t d, int64_t d_ff,
+                        int dtype, int num_sms, cudaStream_t st);
 
 // S2: fixed-order sum over slices, then h = silu(g) * u rounded to dtype.
 cudaError_t launch_reduce_swiglu(const float* part, void* h, int64_t M,
@@ -80,11 +96,10 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
 // x.wa (+ resid) (plain: wa = W_down, wb unused).  `counters`: n_cb arrival
 // counters, zero on entry when `counters_clean` (left so by the previous call
 // on the same stream), else cleared first.
-// w_kmajor: weights stored [n_out, K] (K contiguous, torch.nn.Linear.weight)
-// instead of [K, n_out].
+// wlayout: a WeightLayout.
 cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void* out,
                              const void* resid, int64_t M, int64_t K, int64_t n_out,
-                             bool w_kmajor, const SkinnyPlan& p, float* part,
+                             int wlayout, const SkinnyPlan& p, float* part,
                              unsigned* counters, bool counters_clean, unsigned* status,
                              uint64_t timeout_ns, cudaStream_t st);
 constexpr size_t kStreamCounterBytes = 64 * 1024;   // per-stream arrival counters
@@ -112,7 +127,7 @@ TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
 cudaError_t tile_max_pairs(int* pairs);
 cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* out,
                            const void* resid, int64_t M, int64_t K, int64_t n_out,
-                           bool w_kmajor, const TilePlan& p, float* part, unsigned* counters,
+                           int wlayout, const TilePlan& p, float* part, unsigned* counters,
                            bool counters_clean, unsigned* status, uint64_t timeout_ns,
                            cudaStream_t st);
 

@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kThreads)
 simt_partial_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
                     const void* __restrict__ wu_, float* __restrict__ part,
                     int M, int d, int d_ff, int ks, unsigned* __restrict__ counters,
-                    void* __restrict__ h) {
+                    void* __restrict__ h, int packed) {
   constexpr int VEC = BF16 ? 8 : 4;
   constexpr int C = 32 * VEC;
   constexpr int ES = BF16 ? 2 : 4;
@@ -104,9 +104,13 @@ simt_partial_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
     for (int v = 0; v < VEC; ++v) accg[r][v] = accu[r][v] = 0.f;
 
   if (valid) {
-    const char* wg = (const char*)wg_ + (size_t)col * ES;
-    const char* wu = (const char*)wu_ + (size_t)col * ES;
-    const size_t row_bytes = (size_t)d_ff * ES;
+    // packed weights: gate block b of 64 columns at packed column 128 b, up at
+    // 128 b + 64 (a lane's VEC columns never straddle a block)
+    const int gcol = packed ? col + (col & ~63) : col;
+    const int ucol = packed ? gcol + 64 : col;
+    const char* wg = (const char*)wg_ + (size_t)gcol * ES;
+    const char* wu = (const char*)wu_ + (size_t)ucol * ES;
+    const size_t row_bytes = (size_t)(packed ? 128 * ((d_ff + 63) / 64) : d_ff) * ES;
     for (int k = k0 + warp; k < k1; k += kWarps * kUnroll) {
       uint4 vg[kUnroll], vu[kUnroll];
 #pragma unroll
@@ -203,7 +207,7 @@ simt_partial_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
 template <bool BF16, int RC>
 cudaError_t launch_one(const void* x, const void* wg, const void* wu, float* part,
                        int64_t M, int64_t d, int64_t d_ff, const SimtPlan& p,
-                       unsigned* counters, void* h, cudaStream_t st) {
+                       unsigned* counters, void* h, bool packed, cudaStream_t st) {
   constexpr int VEC = BF16 ? 8 : 4;
   constexpr int C = 32 * VEC;
   const size_t x_bytes = (size_t)RC * p.k_per_slice * sizeof(float);
@@ -234,7 +238,7 @@ cudaError_t launch_one(const void* x, const void* wg, const void* wu, float* par
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, x, wg, wu, part, (int)M, (int)d, (int)d_ff,
-                            (int)p.k_per_slice, counters, h);
+                            (int)p.k_per_slice, counters, h, packed ? 1 : 0);
 }
 
 }  // namespace
@@ -274,7 +278,8 @@ SimtPlan plan_simt(int64_t M, int64_t d, int64_t d_ff, int dtype, int num_sms) {
 cudaError_t launch_simt_partial(const void* x, const void* wg, const void* wu,
                                 float* part, int64_t M, int64_t d, int64_t d_ff,
                                 int dtype, const SimtPlan& p, cudaStream_t st,
-                                unsigned* counters, bool counters_clean, void* h) {
+                                unsigned* counters, bool counters_clean, void* h,
+                                bool packed) {
   if (p.slices == 0) return cudaSuccess;
   if (counters && !counters_clean) {
     cudaError_t e = cudaMemsetAsync(counters, 0, p.counters_bytes, st);
@@ -283,12 +288,12 @@ cudaError_t launch_simt_partial(const void* x, const void* wg, const void* wu,
   if (!counters) h = nullptr;
   const bool bf16 = dtype == 1;
   switch (p.row_chunk) {
-    case 1: return bf16 ? launch_one<true, 1>(x, wg, wu, part, M, d, d_ff, p, counters, h, st)
-                        : launch_one<false, 1>(x, wg, wu, part, M, d, d_ff, p, counters, h, st);
-    case 2: return bf16 ? launch_one<true, 2>(x, wg, wu, part, M, d, d_ff, p, counters, h, st)
-                        : launch_one<false, 2>(x, wg, wu, part, M, d, d_ff, p, counters, h, st);
-    default: return bf16 ? launch_one<true, 4>(x, wg, wu, part, M, d, d_ff, p, counters, h, st)
-                         : launch_one<false, 4>(x, wg, wu, part, M, d, d_ff, p, counters, h, st);
+    case 1: return bf16 ? launch_one<true, 1>(x, wg, wu, part, M, d, d_ff, p, counters, h, packed, st)
+                        : launch_one<false, 1>(x, wg, wu, part, M, d, d_ff, p, counters, h, packed, st);
+    case 2: return bf16 ? launch_one<true, 2>(x, wg, wu, part, M, d, d_ff, p, counters, h, packed, st)
+                        : launch_one<false, 2>(x, wg, wu, part, M, d, d_ff, p, counters, h, packed, st);
+    default: return bf16 ? launch_one<true, 4>(x, wg, wu, part, M, d, d_ff, p, counters, h, packed, st)
+                         : launch_one<false, 4>(x, wg, wu, part, M, d, d_ff, p, counters, h, packed, st);
   }
 }
 

@@ -360,7 +360,7 @@ struct Call {
   void* workspace;
   size_t ws_bytes;
   cudaStream_t st;
-  bool kmajor;   // weights stored [n_out, K] (torch.nn.Linear.weight) instead of [K, n_out]
+  int wlayout;   // a WeightLayout: [K, n_out], [n_out, K] (torch.nn.Linear.weight) or packed
 };
 
 int run(const Call& c) {
@@ -372,7 +372,7 @@ int run(const Call& c) {
   if ((v = make_plan(c.op, c.M, c.K, c.n_out, c.dtype, c.path, di.num_sms, di.max_pairs, &p)) !=
       SWIGLU_OK)
     return v;
-  if (c.kmajor && p.path == SWIGLU_PATH_SIMT && c.K > 0)
+  if (c.wlayout == kWeightsNK && p.path == SWIGLU_PATH_SIMT && c.K > 0)
     return fail(SWIGLU_ERR_UNSUPPORTED,
                 "[N, K] weights are served by the tensor-core paths (bf16) only");
   if (p.path == SWIGLU_PATH_SIMT && p.simt.fused) {
@@ -451,16 +451,17 @@ int run(const Call& c) {
   cudaError_t e = cudaSuccess;
   if (p.path == SWIGLU_PATH_SIMT && p.simt.fused) {
     e = launch_simt_partial(c.x, c.wa, c.wb, part, c.M, c.K, c.n_out, c.dtype, p.simt, st,
-                            counters, counters_clean, c.out);
+                            counters, counters_clean, c.out, c.wlayout == kWeightsPacked);
   } else if (p.path == SWIGLU_PATH_SIMT) {
-    e = launch_simt_partial(c.x, c.wa, c.wb, part, c.M, c.K, c.n_out, c.dtype, p.simt, st);
+    e = launch_simt_partial(c.x, c.wa, c.wb, part, c.M, c.K, c.n_out, c.dtype, p.simt, st,
+                            nullptr, false, nullptr, c.wlayout == kWeightsPacked);
     if (e == cudaSuccess)
       e = launch_reduce_swiglu(part, c.out, c.M, c.n_out, p.slices, c.dtype, di.num_sms, st);
   } else if (p.path == SWIGLU_PATH_SKINNY) {
-    e = launch_skinny_tc(c.x, c.wa, c.wb, c.out, c.resid, c.M, c.K, c.n_out, c.kmajor, p.skinny,
+    e = launch_skinny_tc(c.x, c.wa, c.wb, c.out, c.resid, c.M, c.K, c.n_out, c.wlayout, p.skinny,
                          part, counters, counters_clean, di.status, wait_timeout_ns(), st);
   } else {
-    e = launch_tile_tc(c.x, c.wa, c.wb, c.out, c.resid, c.M, c.K, c.n_out, c.kmajor, p.tile,
+    e = launch_tile_tc(c.x, c.wa, c.wb, c.out, c.resid, c.M, c.K, c.n_out, c.wlayout, p.tile,
                        part, counters, counters_clean, di.status, wait_timeout_ns(), st);
   }
   if (pooled) {
@@ -474,20 +475,37 @@ int run(const Call& c) {
 
 int run_up(const void* x, const void* wg, const void* wu, void* h, int64_t M, int64_t d,
            int64_t d_ff, int dtype, int path, void* workspace, size_t ws_bytes,
-           cudaStream_t st, bool kmajor = false) {
+           cudaStream_t st, int wlayout = kWeightsKN) {
   int v = validate(x, wg, wu, h, M, d, d_ff, dtype);
   if (v != SWIGLU_OK) return v;
   return run(Call{kOpUp, x, wg, wu, nullptr, h, M, d, d_ff, dtype, path, workspace, ws_bytes, st,
-                  kmajor});
+                  wlayout});
+}
+
+// x [M, d], w_packed [d, packed_cols(d_ff)] (launch_pack's layout), h [M, d_ff].
+int validate_packed(const void* x, const void* wp, const void* h, int64_t M, int64_t d,
+                    int64_t d_ff, int dtype) {
+  int v = check_sizes(M, d, d_ff, dtype);
+  if (v != SWIGLU_OK) return v;
+  const size_t e = (size_t)elem_bytes(dtype);
+  const size_t nx = (size_t)M * d * e, nw = (size_t)d * packed_cols(d_ff) * e;
+  const size_t nh = (size_t)M * d_ff * e;
+  if ((nx && !x) || (nw && !wp) || (nh && !h))
+    return fail(SWIGLU_ERR_INVALID_ARG, "null pointer for a non-empty tensor");
+  if ((x && !aligned16(x)) || (wp && !aligned16(wp)) || (h && !aligned16(h)))
+    return fail(SWIGLU_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
+  if (overlaps(h, nh, x, nx) || overlaps(h, nh, wp, nw))
+    return fail(SWIGLU_ERR_INVALID_ARG, "h overlaps an input");
+  return SWIGLU_OK;
 }
 
 int run_down(const void* h, const void* wd, const void* r, void* y, int64_t M, int64_t d_ff,
              int64_t d, int dtype, int path, void* workspace, size_t ws_bytes,
-             cudaStream_t st, bool kmajor = false) {
+             cudaStream_t st, int wlayout = kWeightsKN) {
   int v = validate_down(h, wd, r, y, M, d_ff, d, dtype);
   if (v != SWIGLU_OK) return v;
   return run(Call{kOpDown, h, wd, wd, r, y, M, d_ff, d, dtype, path, workspace, ws_bytes, st,
-                  kmajor});
+                  wlayout});
 }
 
 }  // namespace
@@ -563,14 +581,56 @@ int swiglu_up_nk(const void* x, const void* w_gate_nk, const void* w_up_nk, void
                  int64_t d, int64_t d_ff, int dtype, int path, void* workspace,
                  size_t workspace_bytes, void* stream) {
   return run_up(x, w_gate_nk, w_up_nk, h, M, d, d_ff, dtype, path, workspace, workspace_bytes,
-                (cudaStream_t)stream, true);
+                (cudaStream_t)stream, kWeightsNK);
+}
+
+size_t swiglu_packed_weight_bytes(int64_t d, int64_t d_ff, int dtype) {
+  if (check_sizes(0, d, d_ff, dtype) != SWIGLU_OK) return 0;
+  t_err[0] = 0;
+  return (size_t)d * (size_t)packed_cols(d_ff) * (size_t)elem_bytes(dtype);
+}
+
+int swiglu_pack_weights(const void* w_gate, const void* w_up, void* w_packed, int64_t d,
+                        int64_t d_ff, int dtype, void* stream) {
+  int v = check_sizes(0, d, d_ff, dtype);
+  if (v != SWIGLU_OK) return v;
+  const size_t e = (size_t)elem_bytes(dtype);
+  const size_t nw = (size_t)d * d_ff * e, np = (size_t)d * packed_cols(d_ff) * e;
+  if (nw && (!w_gate || !w_up || !w_packed))
+    return fail(SWIGLU_ERR_INVALID_ARG, "null pointer for a non-empty tensor");
+  if ((w_gate && !aligned16(w_gate)) || (w_up && !aligned16(w_up)) ||
+      (w_packed && !aligned16(w_packed)))
+    return fail(SWIGLU_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
+  if (overlaps(w_packed, np, w_gate, nw) || overlaps(w_packed, np, w_up, nw))
+    return fail(SWIGLU_ERR_INVALID_ARG, "the packed matrix overlaps an input");
+  int dev = 0;
+  DeviceInfo di;
+  if ((v = current_device(&dev, &di)) != SWIGLU_OK) return v;
+  if (nw == 0) {
+    t_err[0] = 0;
+    return SWIGLU_OK;
+  }
+  cudaError_t e2 = launch_pack(w_gate, w_up, w_packed, d, d_ff, dtype, di.num_sms,
+                               (cudaStream_t)stream);
+  if (e2 != cudaSuccess) return cuda_fail(e2, "kernel launch");
+  t_err[0] = 0;
+  return SWIGLU_OK;
+}
+
+int swiglu_up_packed(const void* x, const void* w_packed, void* h, int64_t M, int64_t d,
+                     int64_t d_ff, int dtype, int path, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  int v = validate_packed(x, w_packed, h, M, d, d_ff, dtype);
+  if (v != SWIGLU_OK) return v;
+  return run(Call{kOpUp, x, w_packed, w_packed, nullptr, h, M, d, d_ff, dtype, path, workspace,
+                  workspace_bytes, (cudaStream_t)stream, kWeightsPacked});
 }
 
 int swiglu_down_nk(const void* h, const void* w_down_nk, const void* residual, void* y,
                    int64_t M, int64_t d_ff, int64_t d, int dtype, int path, void* workspace,
                    size_t workspace_bytes, void* stream) {
   return run_down(h, w_down_nk, residual, y, M, d_ff, d, dtype, path, workspace,
-                  workspace_bytes, (cudaStream_t)stream, true);
+                  workspace_bytes, (cudaStream_t)stream, kWeightsNK);
 }
 
 int swiglu_mlp(const void* x, const void* w_gate, const void* w_up, const void* w_down,

@@ -97,6 +97,7 @@ struct SkArgs {
   int grid;
   int hint;             // 1: weight loads carry an L2 evict_first hint
   int kmajor;           // weights stored [n_out, K] (K contiguous) instead of [K, n_out]
+  int packed;           // SwiGLU: one packed gate/up matrix (tm_wg = tm_wu)
   int prefetch_units;   // units each CTA prefetches into L2 before the dependency wait
   int cluster;          // cluster mode: CTAs per column group (0: stream-K mode)
   float* part;          // [n_cg][maxq][NB][2][M][64]
@@ -133,9 +134,13 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
   // Weight columns of one unit's sub-block, and where its two 64-column
   // boxes come from: (tm_wg, col) and (tm_wu, col) for SwiGLU, (tm_wg, col)
   // and (tm_wg, col + 64) for the plain mode.
+  // A packed gate/up matrix holds gate block b at column 2 col and up block
+  // b at 2 col + 64, both in tm_wg (the plain mode's pattern at twice the
+  // column).
   constexpr int kSubCols = MODE == kSwiGLU ? kCB : 2 * kCB;
-  const CUtensorMap* hi_map = MODE == kSwiGLU ? &tm_wu : &tm_wg;
-  constexpr int kHiOff = MODE == kSwiGLU ? 0 : kCB;
+  const CUtensorMap* hi_map = (MODE == kSwiGLU && !a.packed) ? &tm_wu : &tm_wg;
+  const int kHiOff = (MODE == kSwiGLU && !a.packed) ? 0 : kCB;
+  const int col_mul = (MODE == kSwiGLU && a.packed) ? 2 : 1;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* stages = smem_raw + pad;
@@ -197,7 +202,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
       const int cg = (int)(t / a.n_kb), kb = (int)(t - (int64_t)cg * a.n_kb);
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
-        const int col = (cg * NB + b) * kSubCols;
+        const int col = (cg * NB + b) * kSubCols * col_mul;
         if (a.kmajor) {
           tma_prefetch_l2_2d(&tm_wg, kb * kBK, col);
           tma_prefetch_l2_2d(hi_map, kb * kBK, col + kHiOff);
@@ -229,7 +234,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-          const int col = (cg * NB + b) * kSubCols;
+          const int col = (cg * NB + b) * kSubCols * col_mul;
           uint8_t* sb = st + b * kSubBytes;
           // [K, n_out] weights: box (col, k); [n_out, K] weights: box (k, col).
           const int c0 = a.kmajor ? kb * kBK : col, c1 = a.kmajor ? col : kb * kBK;
@@ -663,7 +668,7 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
 
 cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void* out,
                              const void* resid, int64_t M, int64_t K, int64_t n_out,
-                             bool w_kmajor, const SkinnyPlan& p, float* part,
+                             int wlayout, const SkinnyPlan& p, float* part,
                              unsigned* counters, bool counters_clean, unsigned* status,
                              uint64_t timeout_ns, cudaStream_t st) {
   if (p.units == 0 || M == 0) return cudaSuccess;
@@ -671,9 +676,12 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   cudaError_t e;
   if ((e = make_tmap_bf16_2d(&mx, x, M, K, kBK, p.n_pad)) != cudaSuccess) return e;
   // weights as [K, n_out] (boxes 64 columns x 64 k) or [n_out, K] (64 k x 64 rows)
-  const int64_t wr = w_kmajor ? n_out : K, wc = w_kmajor ? K : n_out;
+  const bool w_kmajor = wlayout == kWeightsNK, packed = wlayout == kWeightsPacked;
+  if (packed && p.plain) return cudaErrorInvalidValue;
+  const int64_t wr = w_kmajor ? n_out : K;
+  const int64_t wc = w_kmajor ? K : (packed ? packed_cols(n_out) : n_out);
   if ((e = make_tmap_bf16_2d(&mg, wa, wr, wc, 64, 64, p.l2_promo)) != cudaSuccess) return e;
-  if (p.plain) {
+  if (p.plain || packed) {
     mu = mg;
   } else if ((e = make_tmap_bf16_2d(&mu, wb, wr, wc, 64, 64, p.l2_promo)) != cudaSuccess) {
     return e;
@@ -691,6 +699,7 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   a.grid = p.grid;
   a.hint = p.hint;
   a.kmajor = w_kmajor ? 1 : 0;
+  a.packed = packed ? 1 : 0;
   a.prefetch_units = p.prefetch_units;
   a.cluster = p.cluster;
   a.part = part;

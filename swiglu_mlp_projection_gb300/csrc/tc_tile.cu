@@ -80,6 +80,7 @@ struct TileArgs {
   int64_t tiles;
   const uint16_t* resid;         // plain mode: [M][n_out] added to the sums, or null
   int kmajor;                    // weights stored [n_out, K] instead of [K, n_out]
+  int packed;                    // SwiGLU: one packed gate/up matrix (tm_wg = tm_wu)
   unsigned* status;
   uint64_t timeout_ns;
   // Stream-K tail.  Tiles [0, dp_tiles) are done whole, round-robin over the
@@ -257,6 +258,9 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
               m = (MODE == kSwiGLU && q >= 2) ? &tm_wu : &tm_wg;
               col = MODE == kSwiGLU ? nb * kBN + 64 * (q & 1) : nb * kOutCols + 64 * q;
             }
+            // packed gate/up matrix: gate block at 2 col, up block at 2 col + 64
+            if (MODE == kSwiGLU && a.packed)
+              col = 2 * col + ((PAIR ? rank == 1 : q >= 2) ? 64 : 0);
             if (a.kmajor)
               tma_load_2d(sb + q * kChunkBytes, m, &full[stage], kb * kBK, col);
             else
@@ -708,7 +712,7 @@ cudaError_t launch_mode(const CUtensorMap& mx, const CUtensorMap& mg, const CUte
 
 cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* out,
                            const void* resid, int64_t M, int64_t K, int64_t n_out,
-                           bool w_kmajor, const TilePlan& p, float* part, unsigned* counters,
+                           int wlayout, const TilePlan& p, float* part, unsigned* counters,
                            bool counters_clean, unsigned* status, uint64_t timeout_ns,
                            cudaStream_t st) {
   if (p.tiles == 0 || K == 0) return cudaSuccess;
@@ -716,9 +720,12 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
   CUtensorMap mx, mg, mu, mh;
   cudaError_t e;
   if ((e = make_tmap_bf16_2d(&mx, x, M, K, kBK, kBM)) != cudaSuccess) return e;
-  const int64_t wr = w_kmajor ? n_out : K, wc = w_kmajor ? K : n_out;
+  const bool w_kmajor = wlayout == kWeightsNK, packed = wlayout == kWeightsPacked;
+  if (packed && p.plain) return cudaErrorInvalidValue;
+  const int64_t wr = w_kmajor ? n_out : K;
+  const int64_t wc = w_kmajor ? K : (packed ? packed_cols(n_out) : n_out);
   if ((e = make_tmap_bf16_2d(&mg, wa, wr, wc, 64, 64)) != cudaSuccess) return e;
-  if (p.plain) {
+  if (p.plain || packed) {
     mu = mg;
   } else if ((e = make_tmap_bf16_2d(&mu, wb, wr, wc, 64, 64)) != cudaSuccess) {
     return e;
@@ -733,6 +740,7 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
   a.tiles = p.tiles;
   a.resid = (const uint16_t*)resid;
   a.kmajor = w_kmajor ? 1 : 0;
+  a.packed = packed ? 1 : 0;
   a.status = status;
   a.timeout_ns = timeout_ns;
   a.dp_tiles = p.dp_tiles;

@@ -93,6 +93,15 @@ def test_plan_reports_cluster_size(cuda_lib):
     assert swg.plan(1, 512, 2048, "f32", "auto", 152)["cluster"] == 1
 
 
+def test_packed_weight_bytes(cuda_lib):
+    # 64-column blocks of gate and up alternate; d_ff is padded to 64
+    assert swg.packed_weight_bytes(4096, 14336, "bf16") == 4096 * 2 * 14336 * 2
+    assert swg.packed_weight_bytes(8, 200, "bf16") == 8 * 2 * 256 * 2
+    assert swg.packed_weight_bytes(4, 1032, "f32") == 4 * 2 * 1088 * 4
+    assert swg.packed_weight_bytes(0, 64, "bf16") == 0
+    assert cuda_lib.swiglu_packed_weight_bytes(8, 12, _lib.BF16) == 0   # d_ff % 8 != 0
+
+
 def test_plan_rejects_bad_arguments(cuda_lib):
     with pytest.raises(swg.SwiGLUError):
         swg.plan(-1, 8, 8, "bf16", "auto", 152)
