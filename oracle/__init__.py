@@ -14,7 +14,9 @@ etroites" (row-major weights, (k)*cols + col).
 The down projection (y = h . W_down + r, the anatomy chapter's kernels #10
 and #11) and the two-operation MLP are evaluated the same way.  ``pack``
 writes the gate/up-interleaved weight matrix of the SwiGLU paper's Kernel-2
-(64-column blocks), a copy of element bits.
+(64-column blocks), a copy of element bits.  The FP8 functions (e4m3 codec,
+per-row / per-column quantizers, dequantization) define the FP8 path: its
+result is the fused definition on the dequantized operands, in fp64.
 
 Parity pins (tests/test_oracle.py, tests/test_oracle_down.py): exact
 small-integer brute force, the silu
@@ -22,7 +24,10 @@ identities silu(z) - silu(-z) = z and silu(z) = z (1 + tanh(z/2)) / 2,
 high-precision decimal evaluation, one-hot x, zeroed columns, column
 permutation, h(x) + h(-x) = g (.) u, power-of-two scaling, row independence,
 numpy fp64 matmul at realistic sizes, and torch's bf16 rounding; the packing
-against a reshape-based unpacking and a worked example (tests/test_oracle_pack.py).  Every oracle
+against a reshape-based unpacking and a worked example (tests/test_oracle_pack.py);
+the e4m3 codec against torch's float8_e4m3fn on all codes and 90,000 values,
+and the FP8 path against the bf16 definition on exactly representable inputs
+(tests/test_oracle_fp8.py).  Every oracle
 function is pinned; none is marked "parity unpinned".
 """
 import ctypes
@@ -34,6 +39,7 @@ from . import build as _build
 
 F32 = 0
 BF16 = 1
+F64 = 2   # operands already dequantized to fp64 (the FP8 path)
 
 _lib = None
 
@@ -66,6 +72,16 @@ def _load():
         lib.oracle_down_proj.restype = ip
         lib.oracle_pack.argtypes = [vp, vp, i64, i64, ip, vp]
         lib.oracle_pack.restype = ip
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = ctypes.c_double
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_quantize_rows_e4m3.argtypes = [vp, i64, i64, vp, vp]
+        lib.oracle_quantize_rows_e4m3.restype = ip
+        lib.oracle_quantize_cols_e4m3.argtypes = [vp, i64, i64, vp, vp]
+        lib.oracle_quantize_cols_e4m3.restype = ip
+        lib.oracle_dequant_rows_e4m3.argtypes = [vp, vp, i64, i64, vp]
+        lib.oracle_dequant_rows_e4m3.restype = ip
         _lib = lib
     return _lib
 
@@ -73,7 +89,10 @@ def _load():
 def _raw(a, dtype):
     """Return a C-contiguous numpy array holding the raw element bits."""
     a = np.ascontiguousarray(a)
-    if dtype == BF16:
+    if dtype == F64:
+        if a.dtype != np.float64:
+            raise TypeError("dequantized operands are passed as float64")
+    elif dtype == BF16:
         if a.dtype != np.uint16:
             raise TypeError("bf16 operands are passed as uint16 bit patterns")
     elif dtype == F32:
@@ -107,7 +126,7 @@ def swiglu_up(x, wg, wu, dtype, nthreads=None, want_rounded=True):
         raise ValueError("shape mismatch")
     h64 = np.empty((M, d_ff), np.float64)
     sens = np.empty((M, d_ff), np.float64)
-    hr = np.empty((M, d_ff), np.uint16 if dtype == BF16 else np.float32)
+    hr = np.empty((M, d_ff), {BF16: np.uint16, F32: np.float32, F64: np.float64}[dtype])
     rc = lib.oracle_swiglu_up(_ptr(x), _ptr(wg), _ptr(wu), M, d, d_ff, dtype,
                               _ptr(h64), _ptr(hr) if want_rounded else None,
                               _ptr(sens), nthreads or default_threads())
@@ -251,3 +270,76 @@ def to_f64(a, dtype):
         # the decoder is a bit shift; vectorised form of oracle_bf16_to_f64
         return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     return np.asarray(a, np.float32).astype(np.float64)
+
+
+# ---- FP8 (e4m3) ----------------------------------------------------------
+
+def e4m3_decode(codes):
+    """Values of e4m3 codes (uint8 array) as float64."""
+    lib = _load()
+    c = np.ascontiguousarray(codes, np.uint8)
+    return np.array([lib.oracle_e4m3_decode(int(v)) for v in c.ravel()]).reshape(c.shape)
+
+
+def e4m3_encode(values):
+    """float32 values -> e4m3 codes (round to nearest even, saturating)."""
+    lib = _load()
+    v = np.ascontiguousarray(values, np.float32)
+    return np.array([lib.oracle_e4m3_encode(float(x)) for x in v.ravel()],
+                    np.uint8).reshape(v.shape)
+
+
+def quantize_rows_e4m3(a):
+    """Per-row e4m3 quantization of bf16 bits a [R, K]: (codes [R, K], scales [R] f32)."""
+    lib = _load()
+    a = _raw(a, BF16)
+    R, K = a.shape
+    codes = np.empty((R, K), np.uint8)
+    scales = np.empty(R, np.float32)
+    rc = lib.oracle_quantize_rows_e4m3(_ptr(a), R, K, _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise RuntimeError("oracle_quantize_rows_e4m3 failed (%d)" % rc)
+    return codes, scales
+
+
+def quantize_cols_e4m3(w):
+    """Per-column e4m3 quantization of bf16 bits w [K, N], codes transposed:
+    (codes [N, K], scales [N] f32)."""
+    lib = _load()
+    w = _raw(w, BF16)
+    K, N = w.shape
+    codes = np.empty((N, K), np.uint8)
+    scales = np.empty(N, np.float32)
+    rc = lib.oracle_quantize_cols_e4m3(_ptr(w), K, N, _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise RuntimeError("oracle_quantize_cols_e4m3 failed (%d)" % rc)
+    return codes, scales
+
+
+def dequant_rows_e4m3(codes, scales):
+    """decode(codes[r, k]) * scales[r] as float64 [R, K]."""
+    lib = _load()
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.float32)
+    R, K = codes.shape
+    out = np.empty((R, K), np.float64)
+    rc = lib.oracle_dequant_rows_e4m3(_ptr(codes), _ptr(scales), R, K, _ptr(out))
+    if rc != 0:
+        raise RuntimeError("oracle_dequant_rows_e4m3 failed (%d)" % rc)
+    return out
+
+
+def swiglu_up_fp8(x, wg, wu, nthreads=None):
+    """The FP8 path's definition: x (bf16 bits [M, d]) quantized per row,
+    wg/wu (bf16 bits [d, d_ff]) per column, then the fused definition on the
+    dequantized operands in fp64.  Returns (h64, sens, q) with q the dict of
+    codes and scales (x8, sx, wg8 [d_ff, d], sg, wu8, su)."""
+    x8, sx = quantize_rows_e4m3(x)
+    g8, sg = quantize_cols_e4m3(wg)
+    u8, su = quantize_cols_e4m3(wu)
+    xd = dequant_rows_e4m3(x8, sx)
+    gd = np.ascontiguousarray(dequant_rows_e4m3(g8, sg).T)
+    ud = np.ascontiguousarray(dequant_rows_e4m3(u8, su).T)
+    h64, _, sens = swiglu_up(xd, gd, ud, F64, nthreads=nthreads, want_rounded=False)
+    return h64, sens, {"x8": x8, "sx": sx, "wg8": g8, "sg": sg, "wu8": u8, "su": su}
+

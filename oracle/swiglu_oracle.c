@@ -40,6 +40,7 @@
 
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
+#define ORACLE_F64 2   /* operands already dequantized to fp64 (the FP8 path) */
 
 /* ---- number formats ---------------------------------------------------- */
 
@@ -83,12 +84,15 @@ uint16_t oracle_f64_to_bf16(double v) {
 
 static double load_elem(const void* p, int64_t idx, int dtype) {
   if (dtype == ORACLE_BF16) return oracle_bf16_to_f64(((const uint16_t*)p)[idx]);
+  if (dtype == ORACLE_F64) return ((const double*)p)[idx];
   return (double)((const float*)p)[idx];
 }
 
 static void store_elem(void* p, int64_t idx, int dtype, double v) {
   if (dtype == ORACLE_BF16)
     ((uint16_t*)p)[idx] = oracle_f64_to_bf16(v);
+  else if (dtype == ORACLE_F64)
+    ((double*)p)[idx] = v;
   else
     ((float*)p)[idx] = (float)v; /* C conversion: round to nearest even */
 }
@@ -169,7 +173,7 @@ int oracle_swiglu_up(const void* x, const void* wg, const void* wu, int64_t M,
                      int64_t d, int64_t d_ff, int dtype, double* h64,
                      void* h_out, double* sens, int nthreads) {
   if (M < 0 || d < 0 || d_ff < 0) return 2;
-  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return 2;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64) return 2;
   if (M == 0 || d_ff == 0) return 0;
   if (nthreads < 1) nthreads = 1;
   if (nthreads > d_ff) nthreads = (int)d_ff;
@@ -211,7 +215,7 @@ int oracle_swiglu_up_at(const void* x, const void* wg, const void* wu, int64_t M
                         int64_t d, int64_t d_ff, int dtype, const int64_t* rows,
                         const int64_t* cols, int64_t n, double* h64,
                         double* sens) {
-  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return 2;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64) return 2;
   for (int64_t t = 0; t < n; ++t) {
     int64_t i = rows[t], j = cols[t];
     if (i < 0 || i >= M || j < 0 || j >= d_ff) return 2;
@@ -347,6 +351,126 @@ int oracle_pack(const void* wg, const void* wu, int64_t d, int64_t d_ff, int dty
       }
     }
   }
+  return 0;
+}
+
+/* ---- FP8 (e4m3) weights and activations ---------------------------------- */
+
+/*
+ * The e4m3 format (the "FP8 E4M3" of the OCP 8-bit floating-point
+ * specification, the type tcgen05 kind::f8f6f4 reads as E4M3): 1 sign bit,
+ * 4 exponent bits with bias 7, 3 mantissa bits, no infinities.  Code
+ * s.eeee.mmm is (-1)^s (1 + m/8) 2^(e-7) for e >= 1, (-1)^s (m/8) 2^-6 for
+ * e = 0, and NaN for e = 15, m = 7; the largest finite magnitude is 448.
+ */
+double oracle_e4m3_decode(uint8_t c) {
+  const int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+  return sgn ? -v : v;
+}
+
+/* Round-half-to-even of a non-negative double that holds few bits (exact). */
+static double rne_nonneg(double q) {
+  const double n = floor(q), r = q - n;
+  if (r > 0.5 || (r == 0.5 && fmod(n, 2.0) != 0.0)) return n + 1.0;
+  return n;
+}
+
+/*
+ * f32 -> e4m3, round to nearest (ties to even), finite results saturated to
+ * +-448 (values past the largest finite magnitude, which would round to the
+ * NaN pattern or beyond, become +-448); NaN -> 0x7F.
+ */
+uint8_t oracle_e4m3_encode(float f) {
+  if (isnan(f)) return 0x7F;
+  const uint8_t sgn = signbit(f) ? 0x80 : 0x00;
+  const double a = fabs((double)f);
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal range: multiples of 2^-9; rounding up to 8 gives the
+       smallest normal, code 0x08 */
+    const double n = rne_nonneg(ldexp(a, 9));
+    return (uint8_t)(sgn | (uint8_t)n);
+  }
+  int ex = 0;
+  (void)frexp(a, &ex);          /* a = fr 2^ex, fr in [0.5, 1) */
+  int E = ex - 1;                /* a in [2^E, 2^(E+1)) */
+  double n = rne_nonneg((ldexp(a, -E) - 1.0) * 8.0);
+  if (n == 8.0) { n = 0.0; ++E; }
+  const int biased = E + 7;
+  if (biased > 15 || (biased == 15 && n == 7.0)) return (uint8_t)(sgn | 0x7E);
+  return (uint8_t)(sgn | (biased << 3) | (int)n);
+}
+
+/* amax -> (multiplier 448 / amax, dequantization scale amax / 448), both in
+   f32 arithmetic; an all-zero vector gets 0 and 0. */
+static void e4m3_scale(float amax, float* inv, float* scale) {
+  *inv = amax > 0.0f ? 448.0f / amax : 0.0f;
+  *scale = amax > 0.0f ? amax / 448.0f : 0.0f;
+}
+
+/*
+ * Per-row e4m3 quantization of a bf16 [R, K] matrix (the activations x):
+ * for each row, amax = max |a| (exact in f32), then every element's code is
+ * e4m3(f32(a) * (448 / amax)) with the product rounded to f32 first, and the
+ * row's dequantization scale is amax / 448 (f32).
+ *   codes [R, K], scales [R]
+ */
+int oracle_quantize_rows_e4m3(const uint16_t* a, int64_t R, int64_t K, uint8_t* codes,
+                              float* scales) {
+  if (R < 0 || K < 0) return 2;
+  for (int64_t r = 0; r < R; ++r) {
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      const float v = fabsf((float)oracle_bf16_to_f64(a[r * K + k]));
+      if (v > amax) amax = v;
+    }
+    float inv, sc;
+    e4m3_scale(amax, &inv, &sc);
+    for (int64_t k = 0; k < K; ++k) {
+      const float v = (float)oracle_bf16_to_f64(a[r * K + k]);
+      const float q = v * inv;
+      codes[r * K + k] = oracle_e4m3_encode(q);
+    }
+    scales[r] = sc;
+  }
+  return 0;
+}
+
+/*
+ * Per-column e4m3 quantization of a bf16 [K, N] weight matrix, as the rows
+ * above but over each column j, with the codes written transposed:
+ *   codes_nk [N, K] (code of w[k, j] at j * K + k), scales [N]
+ */
+int oracle_quantize_cols_e4m3(const uint16_t* w, int64_t K, int64_t N, uint8_t* codes_nk,
+                              float* scales) {
+  if (K < 0 || N < 0) return 2;
+  for (int64_t j = 0; j < N; ++j) {
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+      const float v = fabsf((float)oracle_bf16_to_f64(w[k * N + j]));
+      if (v > amax) amax = v;
+    }
+    float inv, sc;
+    e4m3_scale(amax, &inv, &sc);
+    for (int64_t k = 0; k < K; ++k) {
+      const float v = (float)oracle_bf16_to_f64(w[k * N + j]);
+      const float q = v * inv;
+      codes_nk[j * K + k] = oracle_e4m3_encode(q);
+    }
+    scales[j] = sc;
+  }
+  return 0;
+}
+
+/* out[r, k] = decode(codes[r, k]) * scales[r], exactly (a 4-bit significand
+   times a 24-bit one fits a double). */
+int oracle_dequant_rows_e4m3(const uint8_t* codes, const float* scales, int64_t R, int64_t K,
+                             double* out) {
+  if (R < 0 || K < 0) return 2;
+  for (int64_t r = 0; r < R; ++r)
+    for (int64_t k = 0; k < K; ++k)
+      out[r * K + k] = oracle_e4m3_decode(codes[r * K + k]) * (double)scales[r];
   return 0;
 }
 
