@@ -184,6 +184,48 @@ SWIGLU_API int swiglu_up_packed(const void* x, const void* w_packed, void* h, in
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * FP8 weights (e4m3) on the tcgen05 kind::f8f6f4 tensor cores.  "Tile-Level
+ * Activation Overlap for Efficient LLM Inference" (problem statement)
+ * observes that quantization shrinks the GEMM's share of the time and so
+ * raises the activation's; this is the up projection with 8-bit operands and
+ * the same fused epilogue.
+ *
+ * Numerical contract.  Weights are quantized once, per output column:
+ * amax_j = max_k |W[k, j]|, code = e4m3(f32(W[k, j]) * f32(448 / amax_j)),
+ * scale_j = f32(amax_j / 448) (e4m3: 1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits, largest finite value 448; conversion rounds to nearest even
+ * and saturates).  Each call quantizes x per row the same way (into the
+ * workspace), sums code products in f32 on the tensor cores, multiplies each
+ * sum by scale_x[i] * scale_w[j], and applies h = silu(g) * u to the scaled
+ * f32 sums; h is bf16.  An all-zero row or column gets scale 0.  The result
+ * is the fused definition evaluated on the dequantized operands (code value
+ * times scale), within the bf16 tolerance.
+ *
+ * swiglu_quantize_weights_fp8: w_gate, w_up bf16 [d, d_ff] row-major ->
+ *   w8_gate, w8_up: e4m3 codes [d_ff, d] (the shared dimension contiguous,
+ *   as tcgen05 reads 8-bit operands), s_gate, s_up: f32 [d_ff].  All
+ *   caller-owned device memory, 16-byte aligned; the outputs overlap neither
+ *   each other nor the inputs.  Asynchronous on `stream`; uses a short-lived
+ *   d_ff * 4-byte allocation from the library's stream-ordered pool.
+ * swiglu_up_fp8: x bf16 [M, d], the codes and scales above, h bf16 [M, d_ff].
+ *   Paths: AUTO (SKINNY for M <= the skinny limit, else TC), SKINNY, TC;
+ *   SIMT returns SWIGLU_ERR_UNSUPPORTED.  Workspace as swiglu_up_ex, sized by
+ *   swiglu_fp8_workspace_bytes.  It also holds x's codes and row scales: in
+ *   a caller workspace, after the call, bytes [0, M d) are x's e4m3 codes
+ *   [M, d] and the M f32 row scales start at byte M d rounded up to 256.
+ * Both need d a multiple of 16 and d_ff a multiple of 8
+ * (SWIGLU_ERR_ALIGNMENT); other errors as swiglu_up_ex.
+ */
+SWIGLU_API int swiglu_quantize_weights_fp8(const void* w_gate, const void* w_up, void* w8_gate,
+                                           void* w8_up, float* s_gate, float* s_up, int64_t d,
+                                           int64_t d_ff, void* stream);
+SWIGLU_API int swiglu_up_fp8(const void* x, const void* w8_gate, const void* w8_up,
+                             const float* s_gate, const float* s_up, void* h, int64_t M,
+                             int64_t d, int64_t d_ff, int path, void* workspace,
+                             size_t workspace_bytes, void* stream);
+SWIGLU_API size_t swiglu_fp8_workspace_bytes(int64_t M, int64_t d, int64_t d_ff, int path);
+
+/*
  * The whole MLP of "1 . Anatomie d'un transformeur sur GPU", section 1.1,
  * after its RMSNorm: h = silu(x . W_gate) (.) (x . W_up), then
  * y = h . W_down (+ residual).  Two kernels on `stream`; h [M, d_ff] is the

@@ -175,6 +175,74 @@ def swiglu_up_packed(x, w_packed, d_ff, out=None, path="auto", workspace=None, s
     return out
 
 
+class Fp8Weights:
+    """W_gate and W_up quantized to e4m3 per output column: codes [d_ff, d]
+    (uint8, the shared dimension contiguous) and f32 scales [d_ff]."""
+
+    def __init__(self, w8_gate, w8_up, s_gate, s_up):
+        self.w8_gate, self.w8_up, self.s_gate, self.s_up = w8_gate, w8_up, s_gate, s_up
+        self.d_ff, self.d = w8_gate.shape
+
+
+def quantize_weights_fp8(w_gate, w_up, stream=None):
+    """Quantize bf16 w_gate, w_up [d, d_ff] to e4m3 per output column (see
+    swiglu_quantize_weights_fp8); returns an Fp8Weights."""
+    global _LIB
+    import torch
+    _check_cuda(w_gate=w_gate, w_up=w_up)
+    if w_gate.dtype != torch.bfloat16 or w_up.dtype != torch.bfloat16:
+        raise TypeError("w_gate and w_up must be bfloat16")
+    if w_gate.dim() != 2 or w_up.shape != w_gate.shape:
+        raise ValueError("expected w_gate and w_up of one shape [d, d_ff]")
+    d, d_ff = w_gate.shape
+    dev = w_gate.device
+    w8g = torch.empty((d_ff, d), dtype=torch.uint8, device=dev)
+    w8u = torch.empty((d_ff, d), dtype=torch.uint8, device=dev)
+    sg = torch.empty(d_ff, dtype=torch.float32, device=dev)
+    su = torch.empty(d_ff, dtype=torch.float32, device=dev)
+    st = stream.cuda_stream if stream is not None else _raw_stream(dev.index)
+    if _LIB is None:
+        _LIB = _lib.load()
+    _call(dev.index, _LIB.swiglu_quantize_weights_fp8, w_gate.data_ptr(), w_up.data_ptr(),
+          w8g.data_ptr(), w8u.data_ptr(), sg.data_ptr(), su.data_ptr(), d, d_ff, st)
+    return Fp8Weights(w8g, w8u, sg, su)
+
+
+def fp8_workspace_bytes(M, d, d_ff, path="auto"):
+    """Workspace bytes an FP8 call needs on the current device."""
+    n = int(_lib.load().swiglu_fp8_workspace_bytes(M, d, d_ff, _path_code(path)))
+    if n == 0:
+        _lib.check(1)
+    return n
+
+
+def swiglu_up_fp8(x, w, out=None, path="auto", workspace=None, stream=None):
+    """h = silu(x @ W_gate) * (x @ W_up) with e4m3 weights ``w`` (an
+    Fp8Weights) and x quantized per row to e4m3 inside the call; x [M, d] and
+    the result [M, d_ff] are bfloat16."""
+    global _LIB
+    import torch
+    _check_cuda(x=x)
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != w.d:
+        raise ValueError("expected bfloat16 x [M, %d]" % w.d)
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, w.d_ff), dtype=x.dtype, device=x.device)
+    elif out.shape != (M, w.d_ff) or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bfloat16 [M, d_ff] tensor")
+    index = x.device.index
+    st = stream.cuda_stream if stream is not None else _raw_stream(index)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    if _LIB is None:
+        _LIB = _lib.load()
+    _call(index, _LIB.swiglu_up_fp8, x.data_ptr(), w.w8_gate.data_ptr(), w.w8_up.data_ptr(),
+          w.s_gate.data_ptr(), w.s_up.data_ptr(), out.data_ptr(), M, w.d, w.d_ff,
+          _path_code(path), ws_ptr, ws_bytes, st)
+    return out
+
+
 def _check_cuda(**tensors):
     for name, t in tensors.items():
         if t is None:

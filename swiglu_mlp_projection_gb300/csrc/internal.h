@@ -96,12 +96,24 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
 // x.wa (+ resid) (plain: wa = W_down, wb unused).  `counters`: n_cb arrival
 // counters, zero on entry when `counters_clean` (left so by the previous call
 // on the same stream), else cleared first.
-// wlayout: a WeightLayout.
+// The FP8 up projection: x and the weights are e4m3 codes (the weights
+// [n_out, K], kWeightsNK), and each f32 sum (row i, column j) is multiplied by
+// sx[i] * sw_a[j] (gate) or sx[i] * sw_b[j] (up).  The tensor maps view each
+// 8-bit matrix as a 16-bit one of half the columns, so K is passed as the
+// number of byte pairs (a 128-byte k-block holds 128 e4m3 values).
+struct Fp8Scales {
+  const float* sx;     // [M]
+  const float* sw_a;   // [n_out], gate
+  const float* sw_b;   // [n_out], up
+};
+
+// wlayout: a WeightLayout.  fp8: null, or the FP8 scales (SwiGLU mode only).
 cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void* out,
                              const void* resid, int64_t M, int64_t K, int64_t n_out,
                              int wlayout, const SkinnyPlan& p, float* part,
                              unsigned* counters, bool counters_clean, unsigned* status,
-                             uint64_t timeout_ns, cudaStream_t st);
+                             uint64_t timeout_ns, cudaStream_t st,
+                             const Fp8Scales* fp8 = nullptr);
 constexpr size_t kStreamCounterBytes = 64 * 1024;   // per-stream arrival counters
 
 // Tile tensor-core path (bf16, large M): 128-row output tiles.  SwiGLU:
@@ -129,6 +141,15 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
                            const void* resid, int64_t M, int64_t K, int64_t n_out,
                            int wlayout, const TilePlan& p, float* part, unsigned* counters,
                            bool counters_clean, unsigned* status, uint64_t timeout_ns,
-                           cudaStream_t st);
+                           cudaStream_t st, const Fp8Scales* fp8 = nullptr);
+
+// FP8 quantization (e4m3; multiplier 448 / amax, scale amax / 448):
+// x [M, K] bf16 -> codes [M, K] and per-row scales; w [K, N] bf16 -> codes
+// [N, K] (transposed) and per-column scales (amax_scratch: N unsigned).
+cudaError_t launch_quantize_rows_fp8(const void* x, void* codes, float* scales, int64_t M,
+                                     int64_t K, cudaStream_t st);
+cudaError_t launch_quantize_cols_fp8(const void* w, void* codes_nk, float* scales,
+                                     unsigned* amax_scratch, int64_t K, int64_t N,
+                                     int num_sms, cudaStream_t st);
 
 }  // namespace swg

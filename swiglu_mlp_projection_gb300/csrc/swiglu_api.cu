@@ -361,7 +361,17 @@ struct Call {
   size_t ws_bytes;
   cudaStream_t st;
   int wlayout;   // a WeightLayout: [K, n_out], [n_out, K] (torch.nn.Linear.weight) or packed
+  // FP8 up projection: x is bf16 and is quantized per row to e4m3 in the
+  // workspace; wa, wb are e4m3 codes [n_out, K] with column scales sw_a, sw_b.
+  bool fp8 = false;
+  const float* sw_a = nullptr;
+  const float* sw_b = nullptr;
 };
+
+// Bytes an FP8 call keeps ahead of its partial sums: x's codes and row scales.
+size_t fp8_prefix_bytes(int64_t M, int64_t K) {
+  return ((size_t)M * K + 255) / 256 * 256 + ((size_t)M * 4 + 255) / 256 * 256;
+}
 
 int run(const Call& c) {
   int v;
@@ -369,9 +379,15 @@ int run(const Call& c) {
   DeviceInfo di;
   if ((v = current_device(&dev, &di)) != SWIGLU_OK) return v;
   Plan p;
-  if ((v = make_plan(c.op, c.M, c.K, c.n_out, c.dtype, c.path, di.num_sms, di.max_pairs, &p)) !=
+  // FP8: the GEMM kernels see each row of e4m3 codes as K / 2 byte pairs
+  const int64_t Kg = c.fp8 ? c.K / 2 : c.K;
+  if ((v = make_plan(c.op, c.M, Kg, c.n_out, c.dtype, c.path, di.num_sms, di.max_pairs, &p)) !=
       SWIGLU_OK)
     return v;
+  if (c.fp8 && p.path == SWIGLU_PATH_SIMT && c.K > 0)
+    return fail(SWIGLU_ERR_UNSUPPORTED, "FP8 weights are served by the tensor-core paths only");
+  const size_t fp8_prefix = c.fp8 && p.path != SWIGLU_PATH_SIMT ? fp8_prefix_bytes(c.M, c.K) : 0;
+  p.workspace += fp8_prefix;
   if (c.wlayout == kWeightsNK && p.path == SWIGLU_PATH_SIMT && c.K > 0)
     return fail(SWIGLU_ERR_UNSUPPORTED,
                 "[N, K] weights are served by the tensor-core paths (bf16) only");
@@ -406,10 +422,14 @@ int run(const Call& c) {
   if (c.workspace && overlaps(c.out, out_bytes, c.workspace, c.ws_bytes))
     return fail(SWIGLU_ERR_INVALID_ARG, "the output overlaps the workspace");
 
-  // Where the partial sums (and the skinny kernel's counters) live:
+  // Where the partial sums (and the arrival counters) live:
   //   caller workspace -> [counters][partials] inside it, counters cleared;
   //   else the stream's cached buffer -> counters already zero;
   //   else a per-call pool allocation -> counters cleared.
+  // An FP8 call keeps x's codes and row scales ahead of them: at the start
+  // of a caller workspace (a documented layout), else at the start of the
+  // partial-sum region.
+  char* fp8_base = nullptr;
   float* part = nullptr;
   unsigned* counters = nullptr;
   bool counters_clean = false;
@@ -423,13 +443,16 @@ int run(const Call& c) {
       if (c.ws_bytes < p.workspace || ((uintptr_t)c.workspace & 255u))
         return fail(SWIGLU_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)",
                     p.workspace, c.ws_bytes);
-      counters = (unsigned*)c.workspace;
-      part = (float*)((char*)c.workspace + counter_bytes);
+      fp8_base = (char*)c.workspace;
+      counters = (unsigned*)((char*)c.workspace + fp8_prefix);
+      part = (float*)((char*)c.workspace + fp8_prefix + counter_bytes);
     } else {
       if ((v = stream_workspace(dev, st, p.workspace - counter_bytes, &part, &counters)) != SWIGLU_OK)
         return v;
       if (part) {
         counters_clean = true;
+        fp8_base = (char*)part;
+        part = (float*)((char*)part + fp8_prefix);
       } else {
         cudaMemPool_t pool;
         if ((v = device_pool(dev, &pool)) != SWIGLU_OK) return v;
@@ -443,12 +466,24 @@ int run(const Call& c) {
           return cuda_fail(e, "cudaMallocFromPoolAsync");
         }
         counters = (unsigned*)pooled;
-        part = (float*)((char*)pooled + counter_bytes);
+        fp8_base = (char*)pooled + counter_bytes;
+        part = (float*)(fp8_base + fp8_prefix);
       }
     }
   }
 
   cudaError_t e = cudaSuccess;
+  const void* xg = c.x;   // what the GEMM kernels read as x
+  Fp8Scales fs{nullptr, c.sw_a, c.sw_b};
+  if (fp8_prefix) {
+    uint8_t* x8 = (uint8_t*)fp8_base;
+    float* sx = (float*)(x8 + ((size_t)c.M * c.K + 255) / 256 * 256);
+    e = launch_quantize_rows_fp8(c.x, x8, sx, c.M, c.K, st);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    xg = x8;
+    fs.sx = sx;
+  }
+  const Fp8Scales* fsp = fp8_prefix ? &fs : nullptr;
   if (p.path == SWIGLU_PATH_SIMT && p.simt.fused) {
     e = launch_simt_partial(c.x, c.wa, c.wb, part, c.M, c.K, c.n_out, c.dtype, p.simt, st,
                             counters, counters_clean, c.out, c.wlayout == kWeightsPacked);
@@ -458,11 +493,11 @@ int run(const Call& c) {
     if (e == cudaSuccess)
       e = launch_reduce_swiglu(part, c.out, c.M, c.n_out, p.slices, c.dtype, di.num_sms, st);
   } else if (p.path == SWIGLU_PATH_SKINNY) {
-    e = launch_skinny_tc(c.x, c.wa, c.wb, c.out, c.resid, c.M, c.K, c.n_out, c.wlayout, p.skinny,
-                         part, counters, counters_clean, di.status, wait_timeout_ns(), st);
+    e = launch_skinny_tc(xg, c.wa, c.wb, c.out, c.resid, c.M, Kg, c.n_out, c.wlayout, p.skinny,
+                         part, counters, counters_clean, di.status, wait_timeout_ns(), st, fsp);
   } else {
-    e = launch_tile_tc(c.x, c.wa, c.wb, c.out, c.resid, c.M, c.K, c.n_out, c.wlayout, p.tile,
-                       part, counters, counters_clean, di.status, wait_timeout_ns(), st);
+    e = launch_tile_tc(xg, c.wa, c.wb, c.out, c.resid, c.M, Kg, c.n_out, c.wlayout, p.tile,
+                       part, counters, counters_clean, di.status, wait_timeout_ns(), st, fsp);
   }
   if (pooled) {
     cudaError_t ef = cudaFreeAsync(pooled, st);
@@ -495,6 +530,26 @@ int validate_packed(const void* x, const void* wp, const void* h, int64_t M, int
   if ((x && !aligned16(x)) || (wp && !aligned16(wp)) || (h && !aligned16(h)))
     return fail(SWIGLU_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
   if (overlaps(h, nh, x, nx) || overlaps(h, nh, wp, nw))
+    return fail(SWIGLU_ERR_INVALID_ARG, "h overlaps an input");
+  return SWIGLU_OK;
+}
+
+// x [M, d] bf16, w8 [d_ff, d] e4m3 codes (x2), scales [d_ff] f32 (x2), h [M, d_ff] bf16.
+int validate_fp8(const void* x, const void* w8g, const void* w8u, const float* sg,
+                 const float* su, const void* h, int64_t M, int64_t d, int64_t d_ff) {
+  int v = check_sizes(M, d, d_ff, SWIGLU_BF16);
+  if (v != SWIGLU_OK) return v;
+  if (d % 16 != 0)
+    return fail(SWIGLU_ERR_ALIGNMENT, "d must be a multiple of 16 for e4m3 rows");
+  const size_t nx = (size_t)M * d * 2, nw = (size_t)d * d_ff, ns = (size_t)d_ff * 4;
+  const size_t nh = (size_t)M * d_ff * 2;
+  if ((nx && !x) || (nw && (!w8g || !w8u || !sg || !su)) || (nh && !h))
+    return fail(SWIGLU_ERR_INVALID_ARG, "null pointer for a non-empty tensor");
+  if ((x && !aligned16(x)) || (w8g && !aligned16(w8g)) || (w8u && !aligned16(w8u)) ||
+      (sg && !aligned16(sg)) || (su && !aligned16(su)) || (h && !aligned16(h)))
+    return fail(SWIGLU_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
+  if (overlaps(h, nh, x, nx) || overlaps(h, nh, w8g, nw) || overlaps(h, nh, w8u, nw) ||
+      overlaps(h, nh, sg, ns) || overlaps(h, nh, su, ns))
     return fail(SWIGLU_ERR_INVALID_ARG, "h overlaps an input");
   return SWIGLU_OK;
 }
@@ -615,6 +670,89 @@ int swiglu_pack_weights(const void* w_gate, const void* w_up, void* w_packed, in
   if (e2 != cudaSuccess) return cuda_fail(e2, "kernel launch");
   t_err[0] = 0;
   return SWIGLU_OK;
+}
+
+int swiglu_quantize_weights_fp8(const void* w_gate, const void* w_up, void* w8_gate,
+                                void* w8_up, float* s_gate, float* s_up, int64_t d,
+                                int64_t d_ff, void* stream) {
+  int v = check_sizes(0, d, d_ff, SWIGLU_BF16);
+  if (v != SWIGLU_OK) return v;
+  if (d % 16 != 0)
+    return fail(SWIGLU_ERR_ALIGNMENT, "d must be a multiple of 16 for e4m3 rows");
+  const size_t nw = (size_t)d * d_ff * 2, n8 = (size_t)d * d_ff, ns = (size_t)d_ff * 4;
+  if (n8 && (!w_gate || !w_up || !w8_gate || !w8_up || !s_gate || !s_up))
+    return fail(SWIGLU_ERR_INVALID_ARG, "null pointer for a non-empty tensor");
+  const void* ptrs[6] = {w_gate, w_up, w8_gate, w8_up, s_gate, s_up};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return fail(SWIGLU_ERR_ALIGNMENT, "pointers must be 16-byte aligned");
+  const void* outs[4] = {w8_gate, w8_up, s_gate, s_up};
+  const size_t out_n[4] = {n8, n8, ns, ns};
+  for (int i = 0; i < 4; ++i) {
+    if (overlaps(outs[i], out_n[i], w_gate, nw) || overlaps(outs[i], out_n[i], w_up, nw))
+      return fail(SWIGLU_ERR_INVALID_ARG, "an output overlaps an input");
+    for (int j = 0; j < i; ++j)
+      if (overlaps(outs[i], out_n[i], outs[j], out_n[j]))
+        return fail(SWIGLU_ERR_INVALID_ARG, "outputs overlap");
+  }
+  int dev = 0;
+  DeviceInfo di;
+  if ((v = current_device(&dev, &di)) != SWIGLU_OK) return v;
+  if (n8 == 0) {
+    t_err[0] = 0;
+    return SWIGLU_OK;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaMemPool_t pool;
+  if ((v = device_pool(dev, &pool)) != SWIGLU_OK) return v;
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&scratch, (size_t)d_ff * sizeof(unsigned), pool, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(SWIGLU_ERR_OOM, "column maxima: %s", cudaGetErrorString(e));
+  }
+  e = launch_quantize_cols_fp8(w_gate, w8_gate, s_gate, (unsigned*)scratch, d, d_ff,
+                               di.num_sms, st);
+  if (e == cudaSuccess)
+    e = launch_quantize_cols_fp8(w_up, w8_up, s_up, (unsigned*)scratch, d, d_ff, di.num_sms, st);
+  const cudaError_t ef = cudaFreeAsync(scratch, st);
+  if (e == cudaSuccess) e = ef;
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  t_err[0] = 0;
+  return SWIGLU_OK;
+}
+
+int swiglu_up_fp8(const void* x, const void* w8_gate, const void* w8_up, const float* s_gate,
+                  const float* s_up, void* h, int64_t M, int64_t d, int64_t d_ff, int path,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  int v = validate_fp8(x, w8_gate, w8_up, s_gate, s_up, h, M, d, d_ff);
+  if (v != SWIGLU_OK) return v;
+  Call c{kOpUp, x, w8_gate, w8_up, nullptr, h, M, d, d_ff, SWIGLU_BF16, path, workspace,
+         workspace_bytes, (cudaStream_t)stream, kWeightsNK};
+  c.fp8 = true;
+  c.sw_a = s_gate;
+  c.sw_b = s_up;
+  return run(c);
+}
+
+size_t swiglu_fp8_workspace_bytes(int64_t M, int64_t d, int64_t d_ff, int path) {
+  if (check_sizes(M < 0 ? -1 : M, d, d_ff, SWIGLU_BF16) != SWIGLU_OK) return 0;
+  if (d % 16 != 0) {
+    fail(SWIGLU_ERR_ALIGNMENT, "d must be a multiple of 16 for e4m3 rows");
+    return 0;
+  }
+  int dev = 0;
+  DeviceInfo di;
+  if (current_device(&dev, &di) != SWIGLU_OK) return 0;
+  Plan p;
+  if (make_plan(kOpUp, M, d / 2, d_ff, SWIGLU_BF16, path, di.num_sms, di.max_pairs, &p) !=
+      SWIGLU_OK)
+    return 0;
+  if (p.path == SWIGLU_PATH_SIMT && d > 0) {
+    fail(SWIGLU_ERR_UNSUPPORTED, "FP8 weights are served by the tensor-core paths only");
+    return 0;
+  }
+  t_err[0] = 0;
+  return p.workspace + (p.path != SWIGLU_PATH_SIMT ? fp8_prefix_bytes(M, d) : 0);
 }
 
 int swiglu_up_packed(const void* x, const void* w_packed, void* h, int64_t M, int64_t d,

@@ -98,6 +98,10 @@ struct SkArgs {
   int hint;             // 1: weight loads carry an L2 evict_first hint
   int kmajor;           // weights stored [n_out, K] (K contiguous) instead of [K, n_out]
   int packed;           // SwiGLU: one packed gate/up matrix (tm_wg = tm_wu)
+  int fp8;              // SwiGLU on e4m3 codes (K-major weights): sums scaled by sx sw
+  const float* sx;      // fp8: [M] row scales of x
+  const float* sw_a;    // fp8: [n_out] column scales of W_gate
+  const float* sw_b;    // fp8: [n_out] column scales of W_up
   int prefetch_units;   // units each CTA prefetches into L2 before the dependency wait
   int cluster;          // cluster mode: CTAs per column group (0: stream-K mode)
   float* part;          // [n_cg][maxq][NB][2][M][64]
@@ -117,6 +121,16 @@ constexpr int kPlain = 1;
 // CTA whose unit range [c U / G, (c+1) U / G) contains unit t.
 __device__ __forceinline__ int64_t cta_of(int64_t t, int64_t U, int64_t G) {
   return ((t + 1) * G + U - 1) / U - 1;
+}
+
+// FP8: the sums of row m, columns col..col+3 times sx[m] sw[col..].
+__device__ __forceinline__ void fp8_scale(float4& g, float4& u, const SkArgs& a, int m,
+                                          int64_t col) {
+  const float sxm = a.sx[m];
+  const float4 sg = *reinterpret_cast<const float4*>(a.sw_a + col);
+  const float4 su = *reinterpret_cast<const float4*>(a.sw_b + col);
+  g.x *= sxm * sg.x; g.y *= sxm * sg.y; g.z *= sxm * sg.z; g.w *= sxm * sg.w;
+  u.x *= sxm * su.x; u.y *= sxm * su.y; u.z *= sxm * su.z; u.w *= sxm * su.w;
 }
 
 __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, unsigned* status,
@@ -268,8 +282,10 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     if (lane == 0) {
       // A (the weight tile) is MN-major for [K, n_out] weights, K-major for
       // [n_out, K] weights; B (x^T) is always K-major.
-      const uint32_t idesc = a.kmajor ? idesc_bf16_f32(128, N, false, false)
-                                      : idesc_bf16_f32(128, N, true, false);
+      // (FP8: e4m3 codes, K-major; one MMA takes 32 of them, the same 32 bytes)
+      const uint32_t idesc = a.fp8      ? idesc_e4m3_f32(128, N)
+                             : a.kmajor ? idesc_bf16_f32(128, N, false, false)
+                                        : idesc_bf16_f32(128, N, true, false);
       // per 16-deep k step: MN-major tiles advance 16 rows of 128 bytes (two
       // swizzle atoms; the two 64-column boxes are kChunkBytes apart), K-major
       // tiles 32 bytes along their 128-byte rows (8-row groups 1024 B apart).
@@ -307,7 +323,11 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
               const uint64_t ad =
                   smem_desc_sw128(s_addr + b * kSubBytes + kk * a_step, a_lbo, 1024u);
               const uint64_t bd = smem_desc_sw128(b_addr + kk * 32u, 16u, 1024u);
-              mma_bf16(d_tmem, ad, bd, idesc, (tt != t || kk != 0) ? 1u : 0u);
+              const uint32_t accum = (tt != t || kk != 0) ? 1u : 0u;
+              if (a.fp8)
+                mma_e4m3(d_tmem, ad, bd, idesc, accum);
+              else
+                mma_bf16(d_tmem, ad, bd, idesc, accum);
             }
           }
           mma_commit(&empty[stage]);
@@ -456,6 +476,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             const int64_t o = (int64_t)m * a.n_out + col;
             uint2 ov;
             if constexpr (MODE == kSwiGLU) {
+              if (a.fp8) fp8_scale(g[i], u[i], a, m, col);
               ov.x = pack_bf16x2(silu_fast(g[i].x) * u[i].x, silu_fast(g[i].y) * u[i].y);
               ov.y = pack_bf16x2(silu_fast(g[i].z) * u[i].z, silu_fast(g[i].w) * u[i].w);
             } else {
@@ -521,6 +542,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         const int64_t o = (int64_t)m * a.n_out + col;
         uint2 ov;
         if constexpr (MODE == kSwiGLU) {
+          if (a.fp8) fp8_scale(g, u, a, m, col);
           ov.x = pack_bf16x2(silu_fast(g.x) * u.x, silu_fast(g.y) * u.y);
           ov.y = pack_bf16x2(silu_fast(g.z) * u.z, silu_fast(g.w) * u.w);
         } else {
@@ -670,8 +692,9 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
                              const void* resid, int64_t M, int64_t K, int64_t n_out,
                              int wlayout, const SkinnyPlan& p, float* part,
                              unsigned* counters, bool counters_clean, unsigned* status,
-                             uint64_t timeout_ns, cudaStream_t st) {
+                             uint64_t timeout_ns, cudaStream_t st, const Fp8Scales* fp8) {
   if (p.units == 0 || M == 0) return cudaSuccess;
+  if (fp8 && (p.plain || wlayout != kWeightsNK)) return cudaErrorInvalidValue;
   CUtensorMap mx, mg, mu;
   cudaError_t e;
   if ((e = make_tmap_bf16_2d(&mx, x, M, K, kBK, p.n_pad)) != cudaSuccess) return e;
@@ -700,6 +723,10 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   a.hint = p.hint;
   a.kmajor = w_kmajor ? 1 : 0;
   a.packed = packed ? 1 : 0;
+  a.fp8 = fp8 ? 1 : 0;
+  a.sx = fp8 ? fp8->sx : nullptr;
+  a.sw_a = fp8 ? fp8->sw_a : nullptr;
+  a.sw_b = fp8 ? fp8->sw_b : nullptr;
   a.prefetch_units = p.prefetch_units;
   a.cluster = p.cluster;
   a.part = part;

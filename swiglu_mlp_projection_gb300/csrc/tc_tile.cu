@@ -81,6 +81,10 @@ struct TileArgs {
   const uint16_t* resid;         // plain mode: [M][n_out] added to the sums, or null
   int kmajor;                    // weights stored [n_out, K] instead of [K, n_out]
   int packed;                    // SwiGLU: one packed gate/up matrix (tm_wg = tm_wu)
+  int fp8;                       // SwiGLU on e4m3 codes (K-major weights): sums scaled by sx sw
+  const float* sx;               // fp8: [M] row scales of x
+  const float* sw_a;             // fp8: [n_out] column scales of W_gate
+  const float* sw_b;             // fp8: [n_out] column scales of W_up
   unsigned* status;
   uint64_t timeout_ns;
   // Stream-K tail.  Tiles [0, dp_tiles) are done whole, round-robin over the
@@ -286,9 +290,11 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     if (lane == 0) {
       // A (x) is K-major; B (the weights) MN-major for [K, n_out] weights,
       // K-major for [n_out, K] weights.
+      // (FP8: e4m3 codes, K-major; one MMA takes 32 of them, the same 32 bytes)
       constexpr int kMmaM = PAIR ? 2 * kBM : kBM;
-      const uint32_t idesc = a.kmajor ? idesc_bf16_f32(kMmaM, 2 * kBN, false, false)
-                                      : idesc_bf16_f32(kMmaM, 2 * kBN, false, true);
+      const uint32_t idesc = a.fp8      ? idesc_e4m3_f32(kMmaM, 2 * kBN)
+                             : a.kmajor ? idesc_bf16_f32(kMmaM, 2 * kBN, false, false)
+                                        : idesc_bf16_f32(kMmaM, 2 * kBN, false, true);
       const uint32_t b_step = a.kmajor ? 32u : 2048u;
       const uint32_t b_lbo = a.kmajor ? 16u : kChunkBytes;
       int stage = 0;
@@ -319,10 +325,17 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const uint64_t ad = smem_desc_sw128(a_addr + kk * 32u, 16u, 1024u);
             const uint64_t bd = smem_desc_sw128(b_addr + kk * b_step, b_lbo, 1024u);
             const uint32_t accumulate = (kb != kb0 || kk != 0) ? 1u : 0u;
-            if constexpr (PAIR)
-              mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
-            else
-              mma_bf16(d_tmem, ad, bd, idesc, accumulate);
+            if constexpr (PAIR) {
+              if (a.fp8)
+                mma_e4m3_pair(d_tmem, ad, bd, idesc, accumulate);
+              else
+                mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+            } else {
+              if (a.fp8)
+                mma_e4m3(d_tmem, ad, bd, idesc, accumulate);
+              else
+                mma_bf16(d_tmem, ad, bd, idesc, accumulate);
+            }
           }
           // the stage is free again in both CTAs once these MMAs are done
           if constexpr (PAIR)
@@ -493,6 +506,25 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             for (int i = 0; i < 32; ++i) {
               g[i] = __float_as_uint(gs[i]);
               u[i] = __float_as_uint(us[i]);
+            }
+          }
+          if (MODE == kSwiGLU && a.fp8) {
+            // FP8: the sums times sx[row] sw[column]
+            const float sxm = grow < a.M ? a.sx[grow] : 0.f;
+            const int64_t c0 = (int64_t)nb * kOutCols + pass * kBN + ch * 32;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              float4 sg = make_float4(0.f, 0.f, 0.f, 0.f), su = sg;
+              if (c0 + 4 * v < a.n_out) {   // n_out is a multiple of 8
+                sg = reinterpret_cast<const float4*>(a.sw_a + c0)[v];
+                su = reinterpret_cast<const float4*>(a.sw_b + c0)[v];
+              }
+              const float sgv[4] = {sg.x, sg.y, sg.z, sg.w}, suv[4] = {su.x, su.y, su.z, su.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                g[4 * v + e] = __float_as_uint(__uint_as_float(g[4 * v + e]) * (sxm * sgv[e]));
+                u[4 * v + e] = __float_as_uint(__uint_as_float(u[4 * v + e]) * (sxm * suv[e]));
+              }
             }
           }
           float rv[32];
@@ -714,9 +746,10 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
                            const void* resid, int64_t M, int64_t K, int64_t n_out,
                            int wlayout, const TilePlan& p, float* part, unsigned* counters,
                            bool counters_clean, unsigned* status, uint64_t timeout_ns,
-                           cudaStream_t st) {
+                           cudaStream_t st, const Fp8Scales* fp8) {
   if (p.tiles == 0 || K == 0) return cudaSuccess;
   if (p.sk_iters && (!part || !counters)) return cudaErrorInvalidValue;
+  if (fp8 && (p.plain || wlayout != kWeightsNK)) return cudaErrorInvalidValue;
   CUtensorMap mx, mg, mu, mh;
   cudaError_t e;
   if ((e = make_tmap_bf16_2d(&mx, x, M, K, kBK, kBM)) != cudaSuccess) return e;
@@ -741,6 +774,10 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
   a.resid = (const uint16_t*)resid;
   a.kmajor = w_kmajor ? 1 : 0;
   a.packed = packed ? 1 : 0;
+  a.fp8 = fp8 ? 1 : 0;
+  a.sx = fp8 ? fp8->sx : nullptr;
+  a.sw_a = fp8 ? fp8->sw_a : nullptr;
+  a.sw_b = fp8 ? fp8->sw_b : nullptr;
   a.status = status;
   a.timeout_ns = timeout_ns;
   a.dp_tiles = p.dp_tiles;

@@ -102,6 +102,18 @@ def test_packed_weight_bytes(cuda_lib):
     assert cuda_lib.swiglu_packed_weight_bytes(8, 12, _lib.BF16) == 0   # d_ff % 8 != 0
 
 
+def test_fp8_entry_points_validate_before_touching_the_device(cuda_lib):
+    lib = cuda_lib
+    # d not a multiple of 16 (e4m3 rows must be 16-byte multiples)
+    assert lib.swiglu_up_fp8(16, 32, 48, 64, 80, 96, 1, 24, 8, 0, None, 0, None) == 3
+    assert lib.swiglu_quantize_weights_fp8(16, 32, 48, 64, 80, 96, 24, 8, None) == 3
+    # null weights
+    assert lib.swiglu_up_fp8(16, None, 48, 64, 80, 96, 1, 16, 8, 0, None, 0, None) == 1
+    # h overlapping a scale vector
+    assert lib.swiglu_up_fp8(4096, 8192, 12288, 16384, 20480, 20480, 1, 16, 8, 0, None, 0,
+                             None) == 1
+
+
 def test_plan_rejects_bad_arguments(cuda_lib):
     with pytest.raises(swg.SwiGLUError):
         swg.plan(-1, 8, 8, "bf16", "auto", 152)

@@ -1,0 +1,144 @@
+"""The FP8 up projection (e4m3 weights per output column, e4m3 activations
+per row, tcgen05 kind::f8f6f4, scaled f32 sums, SwiGLU epilogue): the
+quantizers against the oracle bit for bit, and h against the oracle's FP8
+definition (the fused definition on the dequantized operands) on every
+tensor-core path and mode."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import swiglu_mlp_projection_gb300 as swg
+from swiglu_mlp_projection_gb300 import _lib, inputs
+from tests.parity import compare
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+RAW = inputs.raw_bits
+
+
+def to64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def make(M, d, d_ff, seed):
+    x, wg, wu = inputs.make_inputs(M, d, d_ff, "bf16", seed=seed)
+    return x, wg, wu
+
+
+@pytest.mark.parametrize("shape", [(64, 136), (1040, 264), (16, 8)])
+def test_weight_quantizer_bitwise(shape):
+    d, d_ff = shape
+    _, wg, wu = make(1, d, d_ff, seed=d)
+    w = swg.quantize_weights_fp8(wg.to(DEV), wu.to(DEV))
+    torch.cuda.synchronize()
+    for got8, gots, ref in ((w.w8_gate, w.s_gate, wg), (w.w8_up, w.s_up, wu)):
+        c, s = oracle.quantize_cols_e4m3(RAW(ref))
+        assert np.array_equal(got8.cpu().numpy(), c)
+        assert np.array_equal(gots.cpu().numpy().view(np.uint32), s.view(np.uint32))
+
+
+def test_activation_quantizer_bitwise_through_the_workspace():
+    # a caller workspace holds x's codes [M, d] at offset 0 and the row scales
+    # from byte M d rounded up to 256
+    M, d, d_ff = 5, 1040, 264
+    x, wg, wu = make(M, d, d_ff, seed=3)
+    xb = RAW(x)
+    xb[4] = 0                                    # an all-zero row: scale 0
+    xd = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(DEV)
+    w = swg.quantize_weights_fp8(wg.to(DEV), wu.to(DEV))
+    for path in ("skinny", "tc"):
+        need = swg.fp8_workspace_bytes(M, d, d_ff, path)
+        ws = torch.full((need,), 0xCD, dtype=torch.uint8, device=DEV)
+        swg.swiglu_up_fp8(xd, w, path=path, workspace=ws)
+        torch.cuda.synchronize()
+        c, s = oracle.quantize_rows_e4m3(xb)
+        off = -(-M * d // 256) * 256
+        wsn = ws.cpu().numpy()
+        assert np.array_equal(wsn[:M * d].reshape(M, d), c), path
+        assert np.array_equal(wsn[off:off + 4 * M].view(np.float32), s), path
+
+
+def check(M, d, d_ff, path, seed=0, **env):
+    x, wg, wu = make(M, d, d_ff, seed)
+    h64, sens, _ = oracle.swiglu_up_fp8(RAW(x), RAW(wg), RAW(wu))
+    w = swg.quantize_weights_fp8(wg.to(DEV), wu.to(DEV))
+    h = swg.swiglu_up_fp8(x.to(DEV), w, path=path)
+    torch.cuda.synchronize()
+    res = compare(to64(h), h64, sens, "bf16", d)
+    assert res["ok"], (M, d, d_ff, path, res)
+    return h
+
+
+SHAPES = [(1, 64, 136), (3, 528, 264), (16, 1040, 520), (17, 256, 1032), (200, 528, 392),
+          (300, 1040, 200)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("path", ["skinny", "tc", "auto"])
+def test_fp8_matches_oracle(shape, path):
+    if path == "skinny" and shape[0] > 256:
+        pytest.skip("skinny path serves M <= 256")
+    check(*shape, path, seed=sum(shape))
+
+
+@pytest.mark.parametrize("env,path,shape", [
+    (("SWIGLU_TILE_PAIR", "0"), "tc", (300, 528, 392)),
+    (("SWIGLU_TILE_PAIR", "1"), "tc", (300, 528, 392)),
+    (("SWIGLU_TILE_SK", "1"), "tc", (40, 1040, 520)),
+    (("SWIGLU_SK_CLUSTER", "4"), "skinny", (7, 1040, 1032)),
+    (("SWIGLU_SK_CLUSTER", "0"), "skinny", (7, 1040, 1032))])
+def test_fp8_kernel_modes(env, path, shape, monkeypatch):
+    monkeypatch.setenv(*env)
+    check(*shape, path, seed=7)
+
+
+def test_fp8_deterministic_and_errors():
+    M, d, d_ff = 9, 1040, 520
+    x, wg, wu = make(M, d, d_ff, seed=1)
+    w = swg.quantize_weights_fp8(wg.to(DEV), wu.to(DEV))
+    xd = x.to(DEV)
+    a = swg.swiglu_up_fp8(xd, w)
+    b = swg.swiglu_up_fp8(xd, w)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    with pytest.raises(swg.SwiGLUError) as e:
+        swg.swiglu_up_fp8(xd, w, path="simt")
+    assert e.value.status == 2
+    lib = _lib.load()
+    h = torch.empty(M, d_ff, dtype=torch.bfloat16, device=DEV)
+    st = lib.swiglu_up_fp8(xd.data_ptr(), w.w8_gate.data_ptr(), w.w8_up.data_ptr(),
+                           w.s_gate.data_ptr(), w.s_up.data_ptr(), h.data_ptr(), M, 1032,
+                           d_ff, 0, None, 0, None)
+    assert st == 3                                   # d not a multiple of 16
+    st = lib.swiglu_up_fp8(xd.data_ptr(), w.w8_gate.data_ptr(), w.w8_up.data_ptr(),
+                           w.s_gate.data_ptr() + 4, w.s_up.data_ptr(), h.data_ptr(), M, d,
+                           d_ff, 0, None, 0, None)
+    assert st == 3                                   # scales not 16-byte aligned
+    swg.check_device_status()
+
+
+@pytest.mark.parametrize("M", [1, 16, 4096])
+def test_fp8_full_size_sampled(M):
+    # d = 4096, d_ff = 14336: the weight codes are checked against the oracle
+    # on sampled columns, and h on those columns for sampled rows
+    d, d_ff = 4096, 14336
+    x, wg, wu = make(M, d, d_ff, seed=M)
+    w = swg.quantize_weights_fp8(wg.to(DEV), wu.to(DEV))
+    h = swg.swiglu_up_fp8(x.to(DEV), w)
+    torch.cuda.synchronize()
+    cols = np.arange(3, d_ff, 211)
+    rows = np.unique(np.linspace(0, M - 1, min(M, 6)).astype(int))
+    gsub, usub = RAW(wg)[:, cols].copy(), RAW(wu)[:, cols].copy()
+    cg, sg = oracle.quantize_cols_e4m3(gsub)
+    cu, su = oracle.quantize_cols_e4m3(usub)
+    assert np.array_equal(w.w8_gate[cols].cpu().numpy(), cg)
+    assert np.array_equal(w.w8_up[cols].cpu().numpy(), cu)
+    x8, sx = oracle.quantize_rows_e4m3(RAW(x)[rows].copy())
+    xdq = oracle.dequant_rows_e4m3(x8, sx)
+    gdq = np.ascontiguousarray(oracle.dequant_rows_e4m3(cg, sg).T)
+    udq = np.ascontiguousarray(oracle.dequant_rows_e4m3(cu, su).T)
+    h64, _, sens = oracle.swiglu_up(xdq, gdq, udq, oracle.F64, want_rounded=False)
+    res = compare(to64(h)[np.ix_(rows, cols)], h64, sens, "bf16", d)
+    assert res["ok"], (M, res)
+    swg.check_device_status()
