@@ -458,10 +458,11 @@ def run_ours(args):
                          "isolated_call_us": round(statistics.median(lat) * 1e3, 2),
                          "path": plans[M]["path"]}
 
-    extra = next_rows = None
+    extra = next_rows = fp8_rows = None
     if not args.no_extra:
         extra = other_configs(dev, peaks, l2, args.extra_iters)
         next_rows = down_and_mlp(dev, peaks, l2, args.extra_iters)
+        fp8_rows = fp8_configs(dev, peaks, args.extra_iters)
 
     if rank == 0:
         cpu = cpu_baseline()
@@ -503,6 +504,8 @@ def run_ours(args):
             line["other_configs"] = extra
         if next_rows is not None:
             line["down_and_mlp"] = next_rows
+        if fp8_rows is not None:
+            line["fp8"] = fp8_rows
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -580,6 +583,52 @@ def other_configs(dev, peaks, l2, iters):
             del x, h
         del copies
         torch.cuda.empty_cache()
+    return out
+
+
+def fp8_configs(dev, peaks, iters):
+    """The FP8 (e4m3) up projection at d=4096, d_ff=14336: the decode sweep
+    and the prefill call, back to back with 2 weight copies (117 MB each,
+    larger than L2).  GB/s counts fp8_bytes; TFLOP/s is against the FP8
+    dense peak taken as 2x the measured bf16 peak (the nominal FP8 : BF16
+    ratio, 4.5 : 2.25 PFLOP/s)."""
+    import torch
+    import swiglu_mlp_projection_gb300 as swg
+    from swiglu_mlp_projection_gb300 import inputs, workload
+    d, d_ff = D, D_FF
+    _, wg, wu = inputs.make_inputs(1, d, d_ff, "bf16", seed=0)
+    wgd, wud = wg.to(dev), wu.to(dev)
+    qs = [swg.quantize_weights_fp8(wgd, wud) for _ in range(2)]
+    del wg, wu, wgd, wud
+    torch.cuda.synchronize(dev)
+    out = {}
+    fp8_peak = 2 * peaks["bf16_tflops"]
+    for M in SWEEP + (4096,):
+        x = inputs.make_inputs(M, d, 8, "bf16", seed=M, x_only=True)[0].to(dev)
+        h = torch.empty(M, d_ff, dtype=torch.bfloat16, device=dev)
+        for i in range(3):
+            swg.swiglu_up_fp8(x, qs[i % 2], out=h)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(iters):
+            swg.swiglu_up_fp8(x, qs[i % 2], out=h)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / iters
+        by = workload.fp8_bytes(M, d, d_ff)
+        fl = workload.flops(M, d, d_ff)
+        e = {"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
+             "TFLOP/s": round(fl / ms / 1e9, 2), "path": swg.plan(M, d, d_ff)["path"],
+             "launches": 2}
+        if M <= 16:
+            e["frac_hbm"] = round(by / ms / 1e6 / peaks["hbm_gbs"], 4)
+        else:
+            e["frac_fp8"] = round(fl / ms / 1e9 / fp8_peak, 4)
+        out["fp8_d4096/M=%d" % M] = e
+        del x, h
+    del qs
+    torch.cuda.empty_cache()
     return out
 
 

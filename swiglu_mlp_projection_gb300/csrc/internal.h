@@ -91,7 +91,8 @@ struct SkinnyPlan {
 };
 constexpr int kSkinnyMaxN = 256;
 // K: shared dimension; n_out: output columns; plain: down-projection mode.
-SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain);
+SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
+                       bool fp8 = false);
 // out[M][n_out] = silu(x.wa) * (x.wa') (SwiGLU: wa = W_gate, wb = W_up) or
 // x.wa (+ resid) (plain: wa = W_down, wb unused).  `counters`: n_cb arrival
 // counters, zero on entry when `counters_clean` (left so by the previous call

@@ -312,7 +312,7 @@ struct Plan {
 // max_pairs: 2-CTA clusters that fit on the device at once (num_sms / 2 when
 // planning without a device).
 int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, int num_sms,
-              int max_pairs, Plan* p) {
+              int max_pairs, Plan* p, bool fp8 = false) {
   int rp = 0;
   int st = resolve_path(op, M, K, dtype, path, &rp);
   if (st != SWIGLU_OK) return st;
@@ -329,7 +329,7 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
     p->workspace = p->simt.counters_bytes + partial_elems(p->slices, M, n_out) * sizeof(float);
     p->launches = p->slices > 0 && !p->simt.fused ? 2 : 1;
   } else if (rp == SWIGLU_PATH_SKINNY) {
-    p->skinny = plan_skinny(M, K, n_out, num_sms, plain);
+    p->skinny = plan_skinny(M, K, n_out, num_sms, plain, fp8);
     // K slices per column group: the cluster size, or (stream-K) at most maxq
     p->slices = p->skinny.cluster ? p->skinny.cluster : p->skinny.maxq;
     p->grid = p->skinny.grid;
@@ -381,8 +381,8 @@ int run(const Call& c) {
   Plan p;
   // FP8: the GEMM kernels see each row of e4m3 codes as K / 2 byte pairs
   const int64_t Kg = c.fp8 ? c.K / 2 : c.K;
-  if ((v = make_plan(c.op, c.M, Kg, c.n_out, c.dtype, c.path, di.num_sms, di.max_pairs, &p)) !=
-      SWIGLU_OK)
+  if ((v = make_plan(c.op, c.M, Kg, c.n_out, c.dtype, c.path, di.num_sms, di.max_pairs, &p,
+                     c.fp8)) != SWIGLU_OK)
     return v;
   if (c.fp8 && p.path == SWIGLU_PATH_SIMT && c.K > 0)
     return fail(SWIGLU_ERR_UNSUPPORTED, "FP8 weights are served by the tensor-core paths only");
@@ -744,7 +744,7 @@ size_t swiglu_fp8_workspace_bytes(int64_t M, int64_t d, int64_t d_ff, int path) 
   DeviceInfo di;
   if (current_device(&dev, &di) != SWIGLU_OK) return 0;
   Plan p;
-  if (make_plan(kOpUp, M, d / 2, d_ff, SWIGLU_BF16, path, di.num_sms, di.max_pairs, &p) !=
+  if (make_plan(kOpUp, M, d / 2, d_ff, SWIGLU_BF16, path, di.num_sms, di.max_pairs, &p, true) !=
       SWIGLU_OK)
     return 0;
   if (p.path == SWIGLU_PATH_SIMT && d > 0) {

@@ -98,7 +98,6 @@ struct SkArgs {
   int hint;             // 1: weight loads carry an L2 evict_first hint
   int kmajor;           // weights stored [n_out, K] (K contiguous) instead of [K, n_out]
   int packed;           // SwiGLU: one packed gate/up matrix (tm_wg = tm_wu)
-  int fp8;              // SwiGLU on e4m3 codes (K-major weights): sums scaled by sx sw
   const float* sx;      // fp8: [M] row scales of x
   const float* sw_a;    // fp8: [n_out] column scales of W_gate
   const float* sw_b;    // fp8: [n_out] column scales of W_up
@@ -139,7 +138,10 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, unsig
   return mbar_wait(bar, parity, &never, status, timeout_ns);
 }
 
-template <int N, int NB, int MODE>
+// FP8: e4m3 operands (kind::f8f6f4) and scaled sums.  A compile-time choice:
+// one kernel issuing MMAs of two kinds behind a runtime branch measured
+// 20-40 % slower on its bf16 work.
+template <int N, int NB, int MODE, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                  const __grid_constant__ CUtensorMap tm_wg,
@@ -283,7 +285,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
       // A (the weight tile) is MN-major for [K, n_out] weights, K-major for
       // [n_out, K] weights; B (x^T) is always K-major.
       // (FP8: e4m3 codes, K-major; one MMA takes 32 of them, the same 32 bytes)
-      const uint32_t idesc = a.fp8      ? idesc_e4m3_f32(128, N)
+      const uint32_t idesc = FP8        ? idesc_e4m3_f32(128, N)
                              : a.kmajor ? idesc_bf16_f32(128, N, false, false)
                                         : idesc_bf16_f32(128, N, true, false);
       // per 16-deep k step: MN-major tiles advance 16 rows of 128 bytes (two
@@ -324,7 +326,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                   smem_desc_sw128(s_addr + b * kSubBytes + kk * a_step, a_lbo, 1024u);
               const uint64_t bd = smem_desc_sw128(b_addr + kk * 32u, 16u, 1024u);
               const uint32_t accum = (tt != t || kk != 0) ? 1u : 0u;
-              if (a.fp8)
+              if constexpr (FP8)
                 mma_e4m3(d_tmem, ad, bd, idesc, accum);
               else
                 mma_bf16(d_tmem, ad, bd, idesc, accum);
@@ -476,7 +478,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             const int64_t o = (int64_t)m * a.n_out + col;
             uint2 ov;
             if constexpr (MODE == kSwiGLU) {
-              if (a.fp8) fp8_scale(g[i], u[i], a, m, col);
+              if constexpr (FP8) fp8_scale(g[i], u[i], a, m, col);
               ov.x = pack_bf16x2(silu_fast(g[i].x) * u[i].x, silu_fast(g[i].y) * u[i].y);
               ov.y = pack_bf16x2(silu_fast(g[i].z) * u[i].z, silu_fast(g[i].w) * u[i].w);
             } else {
@@ -542,7 +544,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         const int64_t o = (int64_t)m * a.n_out + col;
         uint2 ov;
         if constexpr (MODE == kSwiGLU) {
-          if (a.fp8) fp8_scale(g, u, a, m, col);
+          if constexpr (FP8) fp8_scale(g, u, a, m, col);
           ov.x = pack_bf16x2(silu_fast(g.x) * u.x, silu_fast(g.y) * u.y);
           ov.y = pack_bf16x2(silu_fast(g.z) * u.z, silu_fast(g.w) * u.w);
         } else {
@@ -569,11 +571,11 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
   }
 }
 
-template <int N, int NB, int MODE>
+template <int N, int NB, int MODE, bool FP8>
 cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mu,
                      const SkArgs& a, cudaStream_t st) {
   using C = SkCfg<N, NB>;
-  auto kern = skinny_tc_kernel<N, NB, MODE>;
+  auto kern = skinny_tc_kernel<N, NB, MODE, FP8>;
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -601,28 +603,28 @@ cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mg, const CUtenso
   return cudaLaunchKernelEx(&cfg, kern, mx, mg, mu, a);
 }
 
-template <int N, int MODE>
+template <int N, int MODE, bool FP8>
 cudaError_t launch_nb(int nb, const CUtensorMap& mx, const CUtensorMap& mg,
                       const CUtensorMap& mu, const SkArgs& a, cudaStream_t st) {
   if constexpr (N <= 64) {
-    if (nb == 4) return launch_n<N, 4, MODE>(mx, mg, mu, a, st);
+    if (nb == 4) return launch_n<N, 4, MODE, FP8>(mx, mg, mu, a, st);
   }
   if constexpr (N <= 128) {
-    if (nb == 2) return launch_n<N, 2, MODE>(mx, mg, mu, a, st);
+    if (nb == 2) return launch_n<N, 2, MODE, FP8>(mx, mg, mu, a, st);
   }
-  if (nb == 1) return launch_n<N, 1, MODE>(mx, mg, mu, a, st);
+  if (nb == 1) return launch_n<N, 1, MODE, FP8>(mx, mg, mu, a, st);
   return cudaErrorInvalidValue;
 }
 
-template <int MODE>
+template <int MODE, bool FP8>
 cudaError_t launch_mode(int n_pad, int nb, const CUtensorMap& mx, const CUtensorMap& mg,
                         const CUtensorMap& mu, const SkArgs& a, cudaStream_t st) {
   switch (n_pad) {
-    case 16: return launch_nb<16, MODE>(nb, mx, mg, mu, a, st);
-    case 32: return launch_nb<32, MODE>(nb, mx, mg, mu, a, st);
-    case 64: return launch_nb<64, MODE>(nb, mx, mg, mu, a, st);
-    case 128: return launch_nb<128, MODE>(nb, mx, mg, mu, a, st);
-    case 256: return launch_nb<256, MODE>(nb, mx, mg, mu, a, st);
+    case 16: return launch_nb<16, MODE, FP8>(nb, mx, mg, mu, a, st);
+    case 32: return launch_nb<32, MODE, FP8>(nb, mx, mg, mu, a, st);
+    case 64: return launch_nb<64, MODE, FP8>(nb, mx, mg, mu, a, st);
+    case 128: return launch_nb<128, MODE, FP8>(nb, mx, mg, mu, a, st);
+    case 256: return launch_nb<256, MODE, FP8>(nb, mx, mg, mu, a, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -634,7 +636,8 @@ int env_int(const char* name, int dflt) {
 
 }  // namespace
 
-SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain) {
+SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
+                       bool fp8) {
   SkinnyPlan p{};
   int n = 16;
   while (n < M) n *= 2;
@@ -649,8 +652,10 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   // L2 prefetch budget per CTA (measured): 512 KB for SwiGLU; 256 KB for the
   // down projection, whose column groups collect ~10 partial sums each (K is
   // long), so the previous call's final reductions run longer and a larger
-  // prefetch slows them (512 KB measured ~5 % slower, none ~13 % slower).
-  const uint32_t pf_bytes = plain ? kPrefetchBytes / 2 : kPrefetchBytes;
+  // prefetch slows them (512 KB measured ~5 % slower, none ~13 % slower);
+  // 256 KB for FP8 weights, where 512 KB is most of a CTA's share of the
+  // call (d = 4096, M = 1: 26.8 us at 256 KB, 29.4 us at 512 KB).
+  const uint32_t pf_bytes = (plain || fp8) ? kPrefetchBytes / 2 : kPrefetchBytes;
   p.prefetch_units = env_int("SWIGLU_SK_PREFETCH_UNITS",
                              (int)(pf_bytes / ((uint32_t)nb * kSubBytes)));
   const int64_t sub_cols = plain ? 2 * kCB : kCB;
@@ -723,7 +728,6 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   a.hint = p.hint;
   a.kmajor = w_kmajor ? 1 : 0;
   a.packed = packed ? 1 : 0;
-  a.fp8 = fp8 ? 1 : 0;
   a.sx = fp8 ? fp8->sx : nullptr;
   a.sw_a = fp8 ? fp8->sw_a : nullptr;
   a.sw_b = fp8 ? fp8->sw_b : nullptr;
@@ -735,8 +739,9 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   a.resid = (const uint16_t*)resid;
   a.status = status;
   a.timeout_ns = timeout_ns;
-  return p.plain ? launch_mode<kPlain>(p.n_pad, p.nb, mx, mg, mu, a, st)
-                 : launch_mode<kSwiGLU>(p.n_pad, p.nb, mx, mg, mu, a, st);
+  if (p.plain) return launch_mode<kPlain, false>(p.n_pad, p.nb, mx, mg, mu, a, st);
+  return fp8 ? launch_mode<kSwiGLU, true>(p.n_pad, p.nb, mx, mg, mu, a, st)
+             : launch_mode<kSwiGLU, false>(p.n_pad, p.nb, mx, mg, mu, a, st);
 }
 
 }  // namespace swg

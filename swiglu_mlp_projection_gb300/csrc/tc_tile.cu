@@ -81,7 +81,6 @@ struct TileArgs {
   const uint16_t* resid;         // plain mode: [M][n_out] added to the sums, or null
   int kmajor;                    // weights stored [n_out, K] instead of [K, n_out]
   int packed;                    // SwiGLU: one packed gate/up matrix (tm_wg = tm_wu)
-  int fp8;                       // SwiGLU on e4m3 codes (K-major weights): sums scaled by sx sw
   const float* sx;               // fp8: [M] row scales of x
   const float* sw_a;             // fp8: [n_out] column scales of W_gate
   const float* sw_b;             // fp8: [n_out] column scales of W_up
@@ -148,7 +147,10 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, unsig
   return mbar_wait(bar, parity, &never, status, timeout_ns);
 }
 
-template <int MODE, bool PAIR>
+// FP8: e4m3 operands (kind::f8f6f4) and scaled sums.  A compile-time choice:
+// one kernel issuing MMAs of two kinds behind a runtime branch measured
+// 20-40 % slower on its bf16 work.
+template <int MODE, bool PAIR, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
 tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wg,
                const __grid_constant__ CUtensorMap tm_wu, const __grid_constant__ CUtensorMap tm_h,
@@ -292,7 +294,7 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
       // K-major for [n_out, K] weights.
       // (FP8: e4m3 codes, K-major; one MMA takes 32 of them, the same 32 bytes)
       constexpr int kMmaM = PAIR ? 2 * kBM : kBM;
-      const uint32_t idesc = a.fp8      ? idesc_e4m3_f32(kMmaM, 2 * kBN)
+      const uint32_t idesc = FP8        ? idesc_e4m3_f32(kMmaM, 2 * kBN)
                              : a.kmajor ? idesc_bf16_f32(kMmaM, 2 * kBN, false, false)
                                         : idesc_bf16_f32(kMmaM, 2 * kBN, false, true);
       const uint32_t b_step = a.kmajor ? 32u : 2048u;
@@ -325,17 +327,14 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const uint64_t ad = smem_desc_sw128(a_addr + kk * 32u, 16u, 1024u);
             const uint64_t bd = smem_desc_sw128(b_addr + kk * b_step, b_lbo, 1024u);
             const uint32_t accumulate = (kb != kb0 || kk != 0) ? 1u : 0u;
-            if constexpr (PAIR) {
-              if (a.fp8)
-                mma_e4m3_pair(d_tmem, ad, bd, idesc, accumulate);
-              else
-                mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
-            } else {
-              if (a.fp8)
-                mma_e4m3(d_tmem, ad, bd, idesc, accumulate);
-              else
-                mma_bf16(d_tmem, ad, bd, idesc, accumulate);
-            }
+            if constexpr (PAIR && FP8)
+              mma_e4m3_pair(d_tmem, ad, bd, idesc, accumulate);
+            else if constexpr (PAIR)
+              mma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+            else if constexpr (FP8)
+              mma_e4m3(d_tmem, ad, bd, idesc, accumulate);
+            else
+              mma_bf16(d_tmem, ad, bd, idesc, accumulate);
           }
           // the stage is free again in both CTAs once these MMAs are done
           if constexpr (PAIR)
@@ -508,7 +507,7 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
               u[i] = __float_as_uint(us[i]);
             }
           }
-          if (MODE == kSwiGLU && a.fp8) {
+          if constexpr (MODE == kSwiGLU && FP8) {
             // FP8: the sums times sx[row] sw[column]
             const float sxm = grow < a.M ? a.sx[grow] : 0.f;
             const int64_t c0 = (int64_t)nb * kOutCols + pass * kBN + ch * 32;
@@ -686,7 +685,7 @@ TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
 }
 
 cudaError_t tile_max_pairs(int* pairs) {
-  auto kern = tile_tc_kernel<kSwiGLU, true>;
+  auto kern = tile_tc_kernel<kSwiGLU, true, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)TileCfg<true>::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -706,11 +705,11 @@ cudaError_t tile_max_pairs(int* pairs) {
 
 namespace {
 
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIR, bool FP8>
 cudaError_t launch_mode(const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mu,
                         const CUtensorMap& mh, const TileArgs& a, int grid, cudaStream_t st) {
   using C = TileCfg<PAIR>;
-  auto kern = tile_tc_kernel<MODE, PAIR>;
+  auto kern = tile_tc_kernel<MODE, PAIR, FP8>;
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -774,7 +773,6 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
   a.resid = (const uint16_t*)resid;
   a.kmajor = w_kmajor ? 1 : 0;
   a.packed = packed ? 1 : 0;
-  a.fp8 = fp8 ? 1 : 0;
   a.sx = fp8 ? fp8->sx : nullptr;
   a.sw_a = fp8 ? fp8->sw_a : nullptr;
   a.sw_b = fp8 ? fp8->sw_b : nullptr;
@@ -790,11 +788,14 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
   if (p.sk_iters && !counters_clean &&
       (e = cudaMemsetAsync(counters, 0, p.counters_bytes, st)) != cudaSuccess)
     return e;
+  if (fp8)
+    return p.pair ? launch_mode<kSwiGLU, true, true>(mx, mg, mu, mh, a, p.grid, st)
+                  : launch_mode<kSwiGLU, false, true>(mx, mg, mu, mh, a, p.grid, st);
   if (p.pair)
-    return p.plain ? launch_mode<kPlain, true>(mx, mg, mu, mh, a, p.grid, st)
-                   : launch_mode<kSwiGLU, true>(mx, mg, mu, mh, a, p.grid, st);
-  return p.plain ? launch_mode<kPlain, false>(mx, mg, mu, mh, a, p.grid, st)
-                 : launch_mode<kSwiGLU, false>(mx, mg, mu, mh, a, p.grid, st);
+    return p.plain ? launch_mode<kPlain, true, false>(mx, mg, mu, mh, a, p.grid, st)
+                   : launch_mode<kSwiGLU, true, false>(mx, mg, mu, mh, a, p.grid, st);
+  return p.plain ? launch_mode<kPlain, false, false>(mx, mg, mu, mh, a, p.grid, st)
+                 : launch_mode<kSwiGLU, false, false>(mx, mg, mu, mh, a, p.grid, st);
 }
 
 }  // namespace swg

@@ -27,6 +27,13 @@ def algorithmic_bytes(M, d, d_ff, dtype):
     return e * (2 * d * d_ff + M * d + M * d_ff)
 
 
+def fp8_bytes(M, d, d_ff):
+    """Bytes an FP8 call must move at least: the two e4m3 weight matrices and
+    their f32 column scales read once, x (bf16) read once, h (bf16) written
+    once.  (x's e4m3 codes are an intermediate of M d bytes, not counted.)"""
+    return 2 * d * d_ff + 2 * 4 * d_ff + 2 * M * d + 2 * M * d_ff
+
+
 def down_flops(M, d_ff, d):
     """FLOP of the down projection: 2 M d_ff d (the residual add is not counted)."""
     return 2 * M * d_ff * d
