@@ -131,6 +131,7 @@ struct TilePlan {
   int grid;
   bool plain;
   bool pair;
+  bool seq;    // SwiGLU: gate then up k loops (N = 128 each) instead of one N = 256 loop
   int64_t dp_tiles, sk_iters, sk_q, sk_r;
   size_t counters_bytes, part_bytes;
 };

@@ -81,6 +81,7 @@ struct TileArgs {
   const uint16_t* resid;         // plain mode: [M][n_out] added to the sums, or null
   int kmajor;                    // weights stored [n_out, K] instead of [K, n_out]
   int packed;                    // SwiGLU: one packed gate/up matrix (tm_wg = tm_wu)
+  int seq;                       // SwiGLU, one CTA: gate then up, each an N = 128 k loop
   const float* sx;               // fp8: [M] row scales of x
   const float* sw_a;             // fp8: [n_out] column scales of W_gate
   const float* sw_b;             // fp8: [n_out] column scales of W_up
@@ -236,9 +237,15 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
       WorkIter w(a, unit);
       int64_t t;
       int kb0, kb1;
+      // Sequential order (seq): the tile's k loop runs twice, first with
+      // only the two gate boxes per stage, then with only the two up boxes.
+      const int n_ph = (MODE == kSwiGLU && !PAIR && !FP8 && a.seq) ? 2 : 1;
+      const int n_box = n_ph == 2 ? 2 : C::kBoxes;
+      const uint32_t stage_tx = kABytes + (uint32_t)n_box * kChunkBytes;
       while (ok && w.next(a, n_units, t, kb0, kb1)) {
         const int mb = (int)(t % a.n_mb), nb = (int)(t / a.n_mb);
         const int row0 = mb * C::kTileRows + (int)rank * kBM;
+        for (int ph = 0; ok && ph < n_ph; ++ph)
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status, a.timeout_ns)) {
             ok = false;
@@ -246,7 +253,7 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
           }
           uint8_t* st = stages + (size_t)stage * C::kStageBytes;
           uint8_t* sb = st + kABytes;
-          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+          mbar_arrive_expect_tx(&full[stage], stage_tx);
           tma_load_2d(st, &tm_x, &full[stage], kb * kBK, row0);
 #pragma unroll
           for (int q = 0; q < C::kBoxes; ++q) {
@@ -254,23 +261,24 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             // up 64-127 of the tile's columns; plain -> 4 x 64 adjacent
             // columns.  Pair: rank 0 holds accumulator columns 0-127 (gate,
             // or output columns 0-127), rank 1 columns 128-255 (up, or
-            // output columns 128-255).
-            const CUtensorMap* m;
+            // output columns 128-255).  Sequential order: the two boxes of
+            // this phase's matrix only.
+            const bool up = PAIR ? rank == 1 : (n_ph == 2 ? ph == 1 : q >= 2);
+            const CUtensorMap* m = (MODE == kSwiGLU && up) ? &tm_wu : &tm_wg;
             int col;
-            if constexpr (PAIR) {
-              m = (MODE == kSwiGLU && rank == 1) ? &tm_wu : &tm_wg;
+            if constexpr (PAIR)
               col = MODE == kSwiGLU ? nb * kBN + 64 * q : nb * kOutCols + (int)rank * kBN + 64 * q;
-            } else {
-              m = (MODE == kSwiGLU && q >= 2) ? &tm_wu : &tm_wg;
-              col = MODE == kSwiGLU ? nb * kBN + 64 * (q & 1) : nb * kOutCols + 64 * q;
-            }
-            // packed gate/up matrix: gate block at 2 col, up block at 2 col + 64
-            if (MODE == kSwiGLU && a.packed)
-              col = 2 * col + ((PAIR ? rank == 1 : q >= 2) ? 64 : 0);
-            if (a.kmajor)
-              tma_load_2d(sb + q * kChunkBytes, m, &full[stage], kb * kBK, col);
             else
-              tma_load_2d(sb + q * kChunkBytes, m, &full[stage], col, kb * kBK);
+              col = MODE == kSwiGLU ? nb * kBN + 64 * (q & 1) : nb * kOutCols + 64 * q;
+            // packed gate/up matrix: gate block at 2 col, up block at 2 col + 64
+            if (MODE == kSwiGLU && a.packed) col = 2 * col + (up ? 64 : 0);
+            uint8_t* dst = sb + q * kChunkBytes;
+            if (q < n_box) {
+              if (a.kmajor)
+                tma_load_2d(dst, m, &full[stage], kb * kBK, col);
+              else
+                tma_load_2d(dst, m, &full[stage], col, kb * kBK);
+            }
           }
           ++issued;
           if (++stage == kStages) {
@@ -299,6 +307,11 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                                         : idesc_bf16_f32(kMmaM, 2 * kBN, false, true);
       const uint32_t b_step = a.kmajor ? 32u : 2048u;
       const uint32_t b_lbo = a.kmajor ? 16u : kChunkBytes;
+      // sequential order: two N = 128 k loops per tile (gate into accumulator
+      // columns 0-127, then up into 128-255)
+      const int n_ph = (MODE == kSwiGLU && !PAIR && !FP8 && a.seq) ? 2 : 1;
+      const uint32_t idesc_mma =
+          n_ph == 2 ? idesc_bf16_f32(kMmaM, kBN, false, a.kmajor == 0) : idesc;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -313,8 +326,9 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(acc * 2 * kBN);
+        for (int ph = 0; ok && ph < n_ph; ++ph)
         for (int kb = kb0; kb < kb1; ++kb) {
+          const uint32_t d_tmem = tmem + (uint32_t)(acc * 2 * kBN + ph * kBN);
           if (!mbar_wait(&full[stage], phase, abort_flag, a.status, a.timeout_ns)) {
             ok = false;
             break;
@@ -334,7 +348,7 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             else if constexpr (FP8)
               mma_e4m3(d_tmem, ad, bd, idesc, accumulate);
             else
-              mma_bf16(d_tmem, ad, bd, idesc, accumulate);
+              mma_bf16(d_tmem, ad, bd, idesc_mma, accumulate);
           }
           // the stage is free again in both CTAs once these MMAs are done
           if constexpr (PAIR)
@@ -627,6 +641,12 @@ TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
   const int forced = tile_env_int("SWIGLU_TILE_PAIR", -1);
   p.pair = forced >= 0 ? forced != 0 : M > kBM;
   if (num_sms < 2 || max_pairs < 1) p.pair = false;
+  // The SwiGLU paper's Kernel-1 order (gate tile, then up tile, instead of
+  // the interleaved gate|up accumulator): kept to compare the two, never
+  // chosen by default (measured slower); SWIGLU_TILE_SEQ = 1 selects it, on
+  // single-CTA tiles.
+  p.seq = !plain && tile_env_int("SWIGLU_TILE_SEQ", 0) == 1;
+  if (p.seq) p.pair = false;
   const int64_t rows = p.pair ? 2 * kBM : kBM;
   p.n_mb = (M + rows - 1) / rows;
   p.n_nb = (n_out + cols - 1) / cols;
@@ -773,6 +793,7 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
   a.resid = (const uint16_t*)resid;
   a.kmajor = w_kmajor ? 1 : 0;
   a.packed = packed ? 1 : 0;
+  a.seq = p.seq ? 1 : 0;
   a.sx = fp8 ? fp8->sx : nullptr;
   a.sw_a = fp8 ? fp8->sw_a : nullptr;
   a.sw_b = fp8 ? fp8->sw_b : nullptr;

@@ -90,3 +90,26 @@ def test_pair_tiles_at_prefill_size_sampled_rows():
     res = compare(to64(h)[rows], h64, s, "bf16", d)
     assert res["ok"], res
     swg.check_device_status()
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk", "packed"])
+@pytest.mark.parametrize("shape", [(17, 264, 520), (300, 520, 392), (513, 1032, 136)])
+def test_sequential_gate_then_up_order(shape, layout, monkeypatch):
+    # The SwiGLU paper's Kernel-1 order: per tile, a k loop over W_gate, then
+    # one over W_up (each N = 128), instead of one interleaved N = 256 loop.
+    monkeypatch.setenv("SWIGLU_TILE_SEQ", "1")
+    M, d, d_ff = shape
+    assert swg.plan(M, d, d_ff, "bf16", "tc")["cluster"] == 1     # single-CTA tiles
+    x, wg, wu = inputs.make_inputs(M, d, d_ff, "bf16", seed=M + 3)
+    xd = x.to(DEV)
+    if layout == "nk":
+        h = swg.swiglu_up(xd, wg.t().contiguous().to(DEV), wu.t().contiguous().to(DEV),
+                          path="tc", layout="nk")
+    elif layout == "packed":
+        h = swg.swiglu_up_packed(xd, swg.pack_weights(wg.to(DEV), wu.to(DEV)), d_ff, path="tc")
+    else:
+        h = swg.swiglu_up(xd, wg.to(DEV), wu.to(DEV), path="tc")
+    torch.cuda.synchronize()
+    h64, _, s = oracle.swiglu_up(RAW(x), RAW(wg), RAW(wu), oracle.BF16)
+    res = compare(to64(h), h64, s, "bf16", d)
+    assert res["ok"], (shape, layout, res)
