@@ -51,10 +51,14 @@ __global__ void __launch_bounds__(kThreads)
 quantize_rows_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ codes,
                      float* __restrict__ scales, int64_t K) {
   __shared__ float red[kThreads / 32];
-  // launched with programmatic serialisation: x may still be written by the
-  // previous kernel, and the previous GEMM may still read codes / scales
-  tc::pdl_wait();
+  // Launched with programmatic serialisation: x may still be written by the
+  // previous kernel, and the previous GEMM may still read codes / scales, so
+  // everything waits.  The GEMM that follows may launch at once: it prefetches
+  // its weights into L2 while the previous GEMM finishes, and its own
+  // dependency wait covers this kernel (which completes only after the
+  // previous one has).
   tc::pdl_launch_dependents();
+  tc::pdl_wait();
   const int64_t r = blockIdx.x;
   const uint4* src = reinterpret_cast<const uint4*>(x + r * K);
   const int64_t n8 = K / 8;
