@@ -91,8 +91,11 @@ struct SkinnyPlan {
 };
 constexpr int kSkinnyMaxN = 256;
 // K: shared dimension; n_out: output columns; plain: down-projection mode.
+// cluster_caps[lg]: thread-block clusters of 2^lg CTAs of the skinny kernel
+// that fit on the device at once (lg = 1..3), or null (an estimate from num_sms).
 SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
-                       bool fp8 = false);
+                       bool fp8 = false, const int* cluster_caps = nullptr);
+cudaError_t skinny_cluster_caps(int caps[4]);
 // out[M][n_out] = silu(x.wa) * (x.wa') (SwiGLU: wa = W_gate, wb = W_up) or
 // x.wa (+ resid) (plain: wa = W_down, wb unused).  `counters`: n_cb arrival
 // counters, zero on entry when `counters_clean` (left so by the previous call

@@ -43,6 +43,7 @@ struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
   int max_pairs = 0;            // 2-CTA clusters of the tile kernel that fit at once
+  int sk_caps[4] = {0, 0, 0, 0};   // clusters of 2, 4, 8 skinny CTAs that fit at once
   int cc_major = 0, cc_minor = 0;
   cudaMemPool_t pool = nullptr;
   unsigned* status = nullptr;   // device address of g_device_status
@@ -73,6 +74,8 @@ int current_device(int* dev_out, DeviceInfo* out) {
       di.status = (unsigned*)sp;
       if ((e = tile_max_pairs(&di.max_pairs)) != cudaSuccess)
         return cuda_fail(e, "cudaOccupancyMaxActiveClusters(tile kernel)");
+      if ((e = skinny_cluster_caps(di.sk_caps)) != cudaSuccess)
+        return cuda_fail(e, "cudaOccupancyMaxActiveClusters(skinny kernel)");
     }
     di.ready = true;
   }
@@ -312,7 +315,7 @@ struct Plan {
 // max_pairs: 2-CTA clusters that fit on the device at once (num_sms / 2 when
 // planning without a device).
 int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, int num_sms,
-              int max_pairs, Plan* p, bool fp8 = false) {
+              int max_pairs, Plan* p, bool fp8 = false, const int* sk_caps = nullptr) {
   int rp = 0;
   int st = resolve_path(op, M, K, dtype, path, &rp);
   if (st != SWIGLU_OK) return st;
@@ -329,7 +332,7 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
     p->workspace = p->simt.counters_bytes + partial_elems(p->slices, M, n_out) * sizeof(float);
     p->launches = p->slices > 0 && !p->simt.fused ? 2 : 1;
   } else if (rp == SWIGLU_PATH_SKINNY) {
-    p->skinny = plan_skinny(M, K, n_out, num_sms, plain, fp8);
+    p->skinny = plan_skinny(M, K, n_out, num_sms, plain, fp8, sk_caps);
     // K slices per column group: the cluster size, or (stream-K) at most maxq
     p->slices = p->skinny.cluster ? p->skinny.cluster : p->skinny.maxq;
     p->grid = p->skinny.grid;
@@ -382,7 +385,7 @@ int run(const Call& c) {
   // FP8: the GEMM kernels see each row of e4m3 codes as K / 2 byte pairs
   const int64_t Kg = c.fp8 ? c.K / 2 : c.K;
   if ((v = make_plan(c.op, c.M, Kg, c.n_out, c.dtype, c.path, di.num_sms, di.max_pairs, &p,
-                     c.fp8)) != SWIGLU_OK)
+                     c.fp8, di.sk_caps)) != SWIGLU_OK)
     return v;
   if (c.fp8 && p.path == SWIGLU_PATH_SIMT && c.K > 0)
     return fail(SWIGLU_ERR_UNSUPPORTED, "FP8 weights are served by the tensor-core paths only");
@@ -744,8 +747,8 @@ size_t swiglu_fp8_workspace_bytes(int64_t M, int64_t d, int64_t d_ff, int path) 
   DeviceInfo di;
   if (current_device(&dev, &di) != SWIGLU_OK) return 0;
   Plan p;
-  if (make_plan(kOpUp, M, d / 2, d_ff, SWIGLU_BF16, path, di.num_sms, di.max_pairs, &p, true) !=
-      SWIGLU_OK)
+  if (make_plan(kOpUp, M, d / 2, d_ff, SWIGLU_BF16, path, di.num_sms, di.max_pairs, &p, true,
+                di.sk_caps) != SWIGLU_OK)
     return 0;
   if (p.path == SWIGLU_PATH_SIMT && d > 0) {
     fail(SWIGLU_ERR_UNSUPPORTED, "FP8 weights are served by the tensor-core paths only");
@@ -798,7 +801,8 @@ size_t swiglu_workspace_bytes(int64_t M, int64_t d, int64_t d_ff, int dtype, int
   DeviceInfo di;
   if (current_device(&dev, &di) != SWIGLU_OK) return 0;
   Plan p;
-  if (make_plan(kOpUp, M, d, d_ff, dtype, path, di.num_sms, di.max_pairs, &p) != SWIGLU_OK)
+  if (make_plan(kOpUp, M, d, d_ff, dtype, path, di.num_sms, di.max_pairs, &p, false,
+                di.sk_caps) != SWIGLU_OK)
     return 0;
   return p.workspace;
 }
@@ -809,7 +813,8 @@ size_t swiglu_down_workspace_bytes(int64_t M, int64_t d_ff, int64_t d, int dtype
   DeviceInfo di;
   if (current_device(&dev, &di) != SWIGLU_OK) return 0;
   Plan p;
-  if (make_plan(kOpDown, M, d_ff, d, dtype, path, di.num_sms, di.max_pairs, &p) != SWIGLU_OK)
+  if (make_plan(kOpDown, M, d_ff, d, dtype, path, di.num_sms, di.max_pairs, &p, false,
+                di.sk_caps) != SWIGLU_OK)
     return 0;
   return p.workspace;
 }

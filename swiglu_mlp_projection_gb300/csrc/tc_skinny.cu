@@ -637,7 +637,7 @@ int env_int(const char* name, int dflt) {
 }  // namespace
 
 SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
-                       bool fp8) {
+                       bool fp8, const int* cluster_caps) {
   SkinnyPlan p{};
   int n = 16;
   while (n < M) n *= 2;
@@ -665,20 +665,29 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   p.units = p.n_cb * p.n_kb;
   p.grid = (int)(p.units < num_sms ? p.units : num_sms);
   if (p.grid < 1) p.grid = 1;
-  // Cluster mode (measured): it wins when stream-K would spread each column
-  // group over many CTAs (>= 8 partial sums to reduce through global memory)
-  // and the weights are small enough that the call is latency-bound (<= 32 MB;
-  // e.g. the d = 896 down projection: 38 partials per group in stream-K mode,
-  // 1.4-3x slower than 8-CTA clusters).  Elsewhere stream-K is as fast or
-  // faster (larger clusters leave SMs idle and schedule later).  S = the
-  // largest power of two <= 8 with n_cb * S <= SMs and S <= n_kb.
-  // SWIGLU_SK_CLUSTER overrides (0 = stream-K, 1/2/4/8 = that cluster size).
+  // Cluster mode (measured): it wins when the weights are small enough that
+  // the call is latency-bound (<= 32 MB), with the largest cluster size S
+  // (<= 8, <= n_kb) whose n_cb clusters all run at once (cluster_caps[log2 S]
+  // clusters of S fit on the GPU: 76 / 36 / 15 for S = 2 / 4 / 8 on GB300;
+  // planning without a device assumes the same fractions of num_sms / S,
+  // 1, 0.95 and 0.8, as clusters of 4 and 8 must fit whole GPCs).  d = 896: up projection in
+  // 2-CTA clusters 8.3 us vs 9.2 us stream-K (4-CTA clusters, which need a
+  // second wave, 12.8 us), 7.0 vs 12.5 us inside a CUDA graph (no workspace
+  // to allocate and clear); down projection in 8-CTA clusters 8.6 vs 11.8 us.
+  // With large weights stream-K is as fast or faster.  SWIGLU_SK_CLUSTER
+  // overrides (0 = stream-K, 1/2/4/8 = that cluster size).
   int S = 1;
-  while (S < 8 && p.n_cb * (2 * S) <= num_sms && 2 * S <= p.n_kb) S *= 2;
-  const int64_t per_cta = p.units / p.grid;                       // stream-K units per CTA
-  const int64_t sk_partials = per_cta > 0 ? (p.n_kb + per_cta - 1) / per_cta : p.n_kb;
+  for (int s = 8; s >= 2; s /= 2) {
+    const int lg = s == 8 ? 3 : (s == 4 ? 2 : 1);
+    const int64_t cap = cluster_caps ? cluster_caps[lg]
+                                     : (int64_t)(num_sms / s * (s == 2 ? 1.0 : s == 4 ? 0.95 : 0.8));
+    if (s <= p.n_kb && p.n_cb <= cap) {
+      S = s;
+      break;
+    }
+  }
   const int64_t weight_bytes = (plain ? 1 : 2) * K * n_out * 2;
-  p.cluster = (S >= 2 && sk_partials >= 8 && weight_bytes <= ((int64_t)32 << 20)) ? S : 0;
+  p.cluster = (S >= 2 && weight_bytes <= ((int64_t)32 << 20)) ? S : 0;
   const int forced = env_int("SWIGLU_SK_CLUSTER", -1);
   if (forced == 0) p.cluster = 0;
   if (forced == 1 || forced == 2 || forced == 4 || forced == 8)
@@ -691,6 +700,30 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   p.part_bytes = (p.part_bytes + 255) / 256 * 256;
   if (p.cluster) p.counters_bytes = p.part_bytes = 0;   // the reduction stays on chip
   return p;
+}
+
+cudaError_t skinny_cluster_caps(int caps[4]) {
+  using C = SkCfg<16, 2>;
+  auto kern = skinny_tc_kernel<16, 2, kSwiGLU, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  caps[0] = 0;
+  for (int lg = 1; lg <= 3; ++lg) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1u << lg;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1u << lg);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaOccupancyMaxActiveClusters(&caps[lg], kern, &cfg)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void* out,
