@@ -129,6 +129,8 @@ constexpr size_t kStreamCounterBytes = 64 * 1024;   // per-stream arrival counte
 // dp_tiles on form a stream-K tail (sk_iters > 0): their (tile, k-block)
 // iterations are shared out evenly over the grid's units, and partial tiles
 // meet in `part_bytes` of f32 slots with `counters_bytes` of arrival counters.
+// With `seq` (single-CTA SwiGLU tiles only), a tile runs a k loop over W_gate
+// and then one over W_up, each of N = 128.
 struct TilePlan {
   int64_t n_mb, n_nb, n_kb, tiles;
   int grid;

@@ -28,15 +28,20 @@
 //     the partials in contributor order -- i.e. in k order -- applies
 //     silu(g) * u and stores h as bf16.
 //
-// Cluster mode, for problems with few column groups (at most half as many as
-// SMs, e.g. d = 896, d_ff = 4864): each column group is one thread-block
-// cluster of S CTAs that split K evenly.  Every CTA stages its finished
+// Cluster mode, for small weights (at most 32 MB, e.g. d = 896, d_ff = 4864):
+// each column group is one thread-block cluster of S CTAs that split K
+// evenly, S the largest size whose clusters all run at once.  Every CTA stages its finished
 // accumulator in its own shared memory; after a cluster barrier the CTA of
 // rank 0 reads the S partial sums through distributed shared memory, adds them
 // in rank order (= k order, so the result is reproducible), applies the
 // epilogue and stores.  No global workspace, no counters, no memset: the
 // reduction never leaves the chip, which shortens the per-call critical path
 // that dominates such small calls.
+//
+// Variants of the same kernel: the plain epilogue (down projection, plus the
+// residual); [n_out, K] weights (the A operand K-major); a packed gate/up
+// matrix (other box columns); and e4m3 operands (FP8: kind::f8f6f4 MMAs and
+// scaled sums, a template parameter).
 //
 // The same kernel serves the down projection y = h . W_down (+ residual)
 // ("1 . Anatomie d'un transformeur sur GPU", section 1.6, kernels #10 and
