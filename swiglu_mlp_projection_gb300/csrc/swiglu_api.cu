@@ -205,8 +205,16 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return a0 < b0 + nb && b0 < a0 + na;
 }
 
-// Largest M the dispatcher sends to the skinny (split-K) path for bf16.
-constexpr int64_t kSkinnyMaxM = 16;
+// Largest M the dispatcher sends to the skinny (split-K) path for bf16.  The
+// decode article serves at most 16 rows with its skinny kernel; measured on
+// GB300 (both paths forced, back to back), the skinny tcgen05 kernel stays
+// ahead of the tile kernel up to M = 32 for the up projection at d = 896,
+// 4096 and 8192 (d = 4096: 39.4 vs 40.2 us at M = 32, 42.8 vs 40.4 at 48),
+// and up to M = 64 for the down projection, whose few output tiles leave the
+// tile kernel short of parallelism (d = 4096: 40.6 vs 42.1 us at M = 64,
+// 49.8 vs 42.4 at 96; d = 896: 21.7 vs 27.3 us at M = 64).
+constexpr int64_t kSkinnyMaxM = 32;
+constexpr int64_t kSkinnyMaxMDown = 64;
 // Grid-dimension limits of the SIMT path (gridDim.y/z are 16-bit).
 constexpr int64_t kMaxGridYZ = kSimtMaxGridYZ;
 
@@ -227,7 +235,8 @@ enum Op { kOpUp = 0, kOpDown = 1 };
 // Up projection, AUTO: f32 -> SIMT; bf16 M <= kSkinnyMaxM -> SKINNY; larger
 // bf16 M -> TC.  d == 0 (empty sums) always goes to the SIMT path, whose
 // reduction kernel then writes h = silu(0) * 0 = 0.
-// Down projection: bf16 only, on the tensor-core paths (same M rule).
+// Down projection: bf16 only, on the tensor-core paths (M <= kSkinnyMaxMDown
+// -> SKINNY).
 int resolve_path(int op, int64_t M, int64_t K, int dtype, int path, int* out) {
   if (path < SWIGLU_PATH_AUTO || path > SWIGLU_PATH_TC)
     return fail(SWIGLU_ERR_INVALID_ARG, "unknown path %d", path);
@@ -239,7 +248,8 @@ int resolve_path(int op, int64_t M, int64_t K, int dtype, int path, int* out) {
   }
   if (path == SWIGLU_PATH_AUTO) {
     if (op == kOpUp && (dtype == SWIGLU_F32 || K == 0)) *out = SWIGLU_PATH_SIMT;
-    else *out = M <= kSkinnyMaxM ? SWIGLU_PATH_SKINNY : SWIGLU_PATH_TC;
+    else *out = M <= (op == kOpDown ? kSkinnyMaxMDown : kSkinnyMaxM) ? SWIGLU_PATH_SKINNY
+                                                                      : SWIGLU_PATH_TC;
     return SWIGLU_OK;
   }
   if (path != SWIGLU_PATH_SIMT && dtype != SWIGLU_BF16)
@@ -832,7 +842,7 @@ static int plan_common(int op, int64_t M, int64_t K, int64_t n_out, int dtype, i
   out->grid = p.grid;
   out->row_chunk = p.path == SWIGLU_PATH_SIMT ? p.simt.row_chunk : 0;
   out->workspace = (int64_t)p.workspace;
-  out->skinny_max_m = kSkinnyMaxM;
+  out->skinny_max_m = op == kOpDown ? kSkinnyMaxMDown : kSkinnyMaxM;
   out->launches = p.launches;
   out->cluster = p.cluster;
   return SWIGLU_OK;
