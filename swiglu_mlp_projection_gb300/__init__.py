@@ -211,7 +211,7 @@ def quantize_weights_fp8(w_gate, w_up, stream=None):
 def fp8_workspace_bytes(M, d, d_ff, path="auto"):
     """Workspace bytes an FP8 call needs on the current device."""
     n = int(_lib.load().swiglu_fp8_workspace_bytes(M, d, d_ff, _path_code(path)))
-    if n == 0:
+    if n == 0 and M > 0 and d > 0:   # a call with rows and a shared dimension needs some
         _lib.check(1)
     return n
 
