@@ -24,7 +24,20 @@ struct SimtPlan {
   size_t counters_bytes;   // arrival counters of the single launch
 };
 
-SimtPlan plan_simt(int64_t M, int64_t d, int64_t d_ff, int dtype, int num_sms);
+// Tuning overrides from the environment (SWIGLU_SK_NB, SWIGLU_SK_PROMO,
+// SWIGLU_SK_HINT, SWIGLU_SK_PREFETCH_UNITS, SWIGLU_SK_CLUSTER, SWIGLU_TILE_PAIR,
+// SWIGLU_TILE_SK, SWIGLU_TILE_SK_SPLIT, SWIGLU_TILE_SEQ, SWIGLU_SIMT_FUSED),
+// read in one pass over the environment for every planned call, so a process
+// may change them between calls.  -1: not set (the measured default applies).
+struct Tuning {
+  int sk_nb = -1, sk_promo = -1, sk_hint = -1, sk_prefetch_units = -1, sk_cluster = -1;
+  int tile_pair = -1, tile_sk = -1, tile_sk_split = -1, tile_seq = -1;
+  int simt_fused = -1;
+};
+Tuning read_tuning();
+
+SimtPlan plan_simt(int64_t M, int64_t d, int64_t d_ff, int dtype, int num_sms,
+                   const Tuning& tn = Tuning{});
 
 // S1 (SIMT): partial sums of x.Wg and x.Wu per K slice.  With `counters`
 // (p.fused plans; zero on entry unless !counters_clean, left at zero) the
@@ -94,7 +107,8 @@ constexpr int kSkinnyMaxN = 256;
 // cluster_caps[lg]: thread-block clusters of 2^lg CTAs of the skinny kernel
 // that fit on the device at once (lg = 1..3), or null (an estimate from num_sms).
 SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
-                       bool fp8 = false, const int* cluster_caps = nullptr);
+                       bool fp8 = false, const int* cluster_caps = nullptr,
+                       const Tuning& tn = Tuning{});
 cudaError_t skinny_cluster_caps(int caps[4]);
 // out[M][n_out] = silu(x.wa) * (x.wa') (SwiGLU: wa = W_gate, wb = W_up) or
 // x.wa (+ resid) (plain: wa = W_down, wb unused).  `counters`: n_cb arrival
@@ -142,7 +156,7 @@ struct TilePlan {
 };
 // max_pairs: 2-CTA clusters of the tile kernel that fit on the device at once.
 TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
-                   int max_pairs);
+                   int max_pairs, const Tuning& tn = Tuning{});
 cudaError_t tile_max_pairs(int* pairs);
 cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* out,
                            const void* resid, int64_t M, int64_t K, int64_t n_out,

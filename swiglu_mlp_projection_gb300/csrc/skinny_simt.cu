@@ -246,7 +246,8 @@ cudaError_t launch_one(const void* x, const void* wg, const void* wu, float* par
 int64_t split_k_slices(int64_t K, int64_t col_blocks, int64_t target_blocks,
                        int64_t min_k_per_slice);
 
-SimtPlan plan_simt(int64_t M, int64_t d, int64_t d_ff, int dtype, int num_sms) {
+SimtPlan plan_simt(int64_t M, int64_t d, int64_t d_ff, int dtype, int num_sms,
+                   const Tuning& tn) {
   SimtPlan p{};
   p.vec = dtype == 1 ? 8 : 4;
   p.cols_per_cta = 32 * p.vec;
@@ -268,9 +269,8 @@ SimtPlan plan_simt(int64_t M, int64_t d, int64_t d_ff, int dtype, int num_sms) {
   p.slices = (d + ks - 1) / ks;
   // Single launch wherever the arrival counters fit the per-stream counter
   // region (every decode shape); SWIGLU_SIMT_FUSED = 0 keeps two launches.
-  const char* env = getenv("SWIGLU_SIMT_FUSED");
   const int64_t n_ctr = p.col_blocks * p.row_chunks;
-  p.fused = (!env || atoi(env) != 0) && n_ctr * (int64_t)sizeof(unsigned) <= (int64_t)kStreamCounterBytes;
+  p.fused = tn.simt_fused != 0 && n_ctr * (int64_t)sizeof(unsigned) <= (int64_t)kStreamCounterBytes;
   p.counters_bytes = p.fused ? ((size_t)n_ctr * sizeof(unsigned) + 255) / 256 * 256 : 0;
   return p;
 }

@@ -11,6 +11,7 @@
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
+#include <unistd.h>   // environ
 
 #include "swiglu.h"
 #include "common.cuh"
@@ -232,6 +233,37 @@ uint64_t wait_timeout_ns() {
 // The two operations the library serves.
 enum Op { kOpUp = 0, kOpDown = 1 };
 
+}  // namespace
+
+Tuning read_tuning() {
+  Tuning t;
+  for (char** e = environ; e && *e; ++e) {
+    const char* s = *e;
+    if (strncmp(s, "SWIGLU_", 7) != 0) continue;
+    const char* eq = strchr(s, '=');
+    if (!eq) continue;
+    const char* name = s + 7;
+    const size_t n = (size_t)(eq - name);
+    const int v = atoi(eq + 1);
+    struct Knob { const char* key; int* dst; };
+    const Knob knobs[] = {{"SK_NB", &t.sk_nb},
+                          {"SK_PROMO", &t.sk_promo},
+                          {"SK_HINT", &t.sk_hint},
+                          {"SK_PREFETCH_UNITS", &t.sk_prefetch_units},
+                          {"SK_CLUSTER", &t.sk_cluster},
+                          {"TILE_PAIR", &t.tile_pair},
+                          {"TILE_SK", &t.tile_sk},
+                          {"TILE_SK_SPLIT", &t.tile_sk_split},
+                          {"TILE_SEQ", &t.tile_seq},
+                          {"SIMT_FUSED", &t.simt_fused}};
+    for (const Knob& k : knobs)
+      if (strlen(k.key) == n && strncmp(k.key, name, n) == 0) *k.dst = v;
+  }
+  return t;
+}
+
+namespace {
+
 // Up projection, AUTO: f32 -> SIMT; bf16 M <= kSkinnyMaxM -> SKINNY; larger
 // bf16 M -> TC.  d == 0 (empty sums) always goes to the SIMT path, whose
 // reduction kernel then writes h = silu(0) * 0 = 0.
@@ -333,8 +365,9 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
   p->path = rp;
   p->cluster = 1;
   const bool plain = op == kOpDown;
+  const Tuning tn = read_tuning();
   if (rp == SWIGLU_PATH_SIMT) {
-    p->simt = plan_simt(M, K, n_out, dtype, num_sms);
+    p->simt = plan_simt(M, K, n_out, dtype, num_sms, tn);
     if (p->simt.slices > kMaxGridYZ || p->simt.row_chunks > kMaxGridYZ)
       return fail(SWIGLU_ERR_UNSUPPORTED, "shape exceeds the grid limits of the SIMT path");
     p->slices = p->simt.slices;
@@ -342,7 +375,7 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
     p->workspace = p->simt.counters_bytes + partial_elems(p->slices, M, n_out) * sizeof(float);
     p->launches = p->slices > 0 && !p->simt.fused ? 2 : 1;
   } else if (rp == SWIGLU_PATH_SKINNY) {
-    p->skinny = plan_skinny(M, K, n_out, num_sms, plain, fp8, sk_caps);
+    p->skinny = plan_skinny(M, K, n_out, num_sms, plain, fp8, sk_caps, tn);
     // K slices per column group: the cluster size, or (stream-K) at most maxq
     p->slices = p->skinny.cluster ? p->skinny.cluster : p->skinny.maxq;
     p->grid = p->skinny.grid;
@@ -350,7 +383,7 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
     p->launches = 1;
     p->cluster = p->skinny.cluster ? p->skinny.cluster : 1;
   } else {
-    p->tile = plan_tile(M, K, n_out, num_sms, plain, max_pairs);
+    p->tile = plan_tile(M, K, n_out, num_sms, plain, max_pairs, tn);
     p->slices = 1;
     p->grid = p->tile.grid;
     p->workspace = p->tile.counters_bytes + p->tile.part_bytes;

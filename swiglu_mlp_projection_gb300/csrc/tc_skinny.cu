@@ -634,26 +634,22 @@ cudaError_t launch_mode(int n_pad, int nb, const CUtensorMap& mx, const CUtensor
   }
 }
 
-int env_int(const char* name, int dflt) {
-  const char* v = getenv(name);
-  return v ? atoi(v) : dflt;
-}
 
 }  // namespace
 
 SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
-                       bool fp8, const int* cluster_caps) {
+                       bool fp8, const int* cluster_caps, const Tuning& tn) {
   SkinnyPlan p{};
   int n = 16;
   while (n < M) n *= 2;
   p.n_pad = n;
   p.plain = plain;
-  int nb = env_int("SWIGLU_SK_NB", 2);
+  int nb = tn.sk_nb >= 0 ? tn.sk_nb : 2;
   if (nb != 1 && nb != 2 && nb != 4) nb = 2;
   while (nb > 1 && nb * n > 256) nb /= 2;
   p.nb = nb;
-  p.l2_promo = env_int("SWIGLU_SK_PROMO", 128);
-  p.hint = env_int("SWIGLU_SK_HINT", 1);
+  p.l2_promo = tn.sk_promo >= 0 ? tn.sk_promo : 128;
+  p.hint = tn.sk_hint >= 0 ? tn.sk_hint : 1;
   // L2 prefetch budget per CTA (measured): 512 KB for SwiGLU; 256 KB for the
   // down projection, whose column groups collect ~10 partial sums each (K is
   // long), so the previous call's final reductions run longer and a larger
@@ -661,8 +657,8 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   // 256 KB for FP8 weights, where 512 KB is most of a CTA's share of the
   // call (d = 4096, M = 1: 26.8 us at 256 KB, 29.4 us at 512 KB).
   const uint32_t pf_bytes = (plain || fp8) ? kPrefetchBytes / 2 : kPrefetchBytes;
-  p.prefetch_units = env_int("SWIGLU_SK_PREFETCH_UNITS",
-                             (int)(pf_bytes / ((uint32_t)nb * kSubBytes)));
+  p.prefetch_units = tn.sk_prefetch_units >= 0 ? tn.sk_prefetch_units
+                                               : (int)(pf_bytes / ((uint32_t)nb * kSubBytes));
   const int64_t sub_cols = plain ? 2 * kCB : kCB;
   const int64_t subs = (n_out + sub_cols - 1) / sub_cols;
   p.n_cb = (subs + nb - 1) / nb;
@@ -693,7 +689,7 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   }
   const int64_t weight_bytes = (plain ? 1 : 2) * K * n_out * 2;
   p.cluster = (S >= 2 && weight_bytes <= ((int64_t)32 << 20)) ? S : 0;
-  const int forced = env_int("SWIGLU_SK_CLUSTER", -1);
+  const int forced = tn.sk_cluster;
   if (forced == 0) p.cluster = 0;
   if (forced == 1 || forced == 2 || forced == 4 || forced == 8)
     p.cluster = p.n_kb >= forced ? forced : 0;

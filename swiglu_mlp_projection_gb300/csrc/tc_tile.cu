@@ -624,28 +624,24 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
   }
 }
 
-int tile_env_int(const char* name, int dflt) {
-  const char* v = getenv(name);
-  return v ? atoi(v) : dflt;
-}
 
 }  // namespace
 
 TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
-                   int max_pairs) {
+                   int max_pairs, const Tuning& tn) {
   TilePlan p{};
   const int64_t cols = plain ? 2 * kBN : kBN;
   p.plain = plain;
   // 2-CTA tiles wherever there is more than one 128-row block;
   // SWIGLU_TILE_PAIR = 0 / 1 forces one mode.
-  const int forced = tile_env_int("SWIGLU_TILE_PAIR", -1);
+  const int forced = tn.tile_pair;
   p.pair = forced >= 0 ? forced != 0 : M > kBM;
   if (num_sms < 2 || max_pairs < 1) p.pair = false;
   // The SwiGLU paper's Kernel-1 order (gate tile, then up tile, instead of
   // the interleaved gate|up accumulator): kept to compare the two, never
   // chosen by default (measured slower); SWIGLU_TILE_SEQ = 1 selects it, on
   // single-CTA tiles.
-  p.seq = !plain && tile_env_int("SWIGLU_TILE_SEQ", 0) == 1;
+  p.seq = !plain && tn.tile_seq == 1;
   if (p.seq) p.pair = false;
   const int64_t rows = p.pair ? 2 * kBM : kBM;
   p.n_mb = (M + rows - 1) / rows;
@@ -670,8 +666,8 @@ TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
   // < 30 % of the units busy and each unit gets >= 4 k-blocks.
   // SWIGLU_TILE_SK = 0 / 1 forces it off / on (on: wherever there is a
   // partial wave).
-  const int forced_sk = tile_env_int("SWIGLU_TILE_SK", -1);
-  int max_split = tile_env_int("SWIGLU_TILE_SK_SPLIT", 4);
+  const int forced_sk = tn.tile_sk;
+  int max_split = tn.tile_sk_split >= 0 ? tn.tile_sk_split : 4;
   if (max_split < 2) max_split = 2;
   const int64_t waves = p.tiles / units, rem = p.tiles % units;
   if (p.tiles > 0 && p.n_kb > 0 && rem != 0 && forced_sk != 0) {
