@@ -205,7 +205,7 @@ def down_proj(h, wd, dtype, r=None):
             raise ValueError("residual shape mismatch")
     y64 = np.empty((M, N), np.float64)
     sens = np.empty((M, N), np.float64)
-    yr = np.empty((M, N), np.uint16 if dtype == BF16 else np.float32)
+    yr = np.empty((M, N), {BF16: np.uint16, F32: np.float32, F64: np.float64}[dtype])
     rc = lib.oracle_down_proj(_ptr(h), _ptr(wd), _ptr(r) if r is not None else None, M, K, N,
                               dtype, _ptr(y64), _ptr(yr), _ptr(sens))
     if rc != 0:
@@ -342,4 +342,18 @@ def swiglu_up_fp8(x, wg, wu, nthreads=None):
     ud = np.ascontiguousarray(dequant_rows_e4m3(u8, su).T)
     h64, _, sens = swiglu_up(xd, gd, ud, F64, nthreads=nthreads, want_rounded=False)
     return h64, sens, {"x8": x8, "sx": sx, "wg8": g8, "sg": sg, "wu8": u8, "su": su}
+
+
+def down_proj_fp8(h, wd, r=None):
+    """The FP8 down projection's definition: h (bf16 bits [M, d_ff]) quantized
+    per row, wd (bf16 bits [d_ff, d]) per column, then y = h . wd (+ r) in
+    fp64 on the dequantized operands (r, bf16 bits, exact).  Returns
+    (y64, sens)."""
+    h8, sh = quantize_rows_e4m3(h)
+    w8, sw = quantize_cols_e4m3(wd)
+    hd = dequant_rows_e4m3(h8, sh)
+    wdd = np.ascontiguousarray(dequant_rows_e4m3(w8, sw).T)
+    rd = bf16_to_f64(_raw(r, BF16)) if r is not None else None
+    y64, _, sens = down_proj(hd, wdd, F64, rd)
+    return y64, sens
 

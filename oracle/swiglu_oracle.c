@@ -278,7 +278,7 @@ int oracle_round_to_dtype(const double* v, int64_t n, int dtype, void* out) {
  */
 int oracle_down_proj(const void* h, const void* wd, const void* r, int64_t M, int64_t K,
                      int64_t N, int dtype, double* y64, void* y_out, double* sens) {
-  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return 2;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64) return 2;
   if (M < 0 || K < 0 || N < 0) return 2;
   double* acc = (double*)malloc((size_t)(N > 0 ? N : 1) * 2 * sizeof(double));
   if (!acc) return 1;

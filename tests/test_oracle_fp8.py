@@ -89,3 +89,21 @@ def test_fp8_definition_equals_bf16_oracle_on_exact_inputs():
     assert np.all(q["sx"] == 1) and np.all(q["sg"] == 1) and np.all(q["su"] == 1)
     h64, _, s = oracle.swiglu_up(xb, gb, ub, oracle.BF16)
     assert np.array_equal(h8, h64) and np.array_equal(s8, s)
+
+
+def test_fp8_down_definition_equals_bf16_oracle_on_exact_inputs():
+    # the down projection's FP8 definition, on inputs e4m3 holds exactly with
+    # scales 1, is the bf16 down projection to the last bit
+    rng = np.random.default_rng(2)
+    grid = np.array([0, 1, 2, 3, 4, 6, 8, 12, 16, 24, 448], np.float32)
+    M, d_ff, d = 3, 32, 16
+    h = rng.choice(grid, (M, d_ff)) * rng.choice([-1, 1], (M, d_ff))
+    wd = rng.choice(grid, (d_ff, d)) * rng.choice([-1, 1], (d_ff, d))
+    r = rng.choice(grid, (M, d)) * rng.choice([-1, 1], (M, d))
+    h[:, 0] = 448
+    wd[0, :] = 448
+    to_bits = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    hb, wb, rb = to_bits(h), to_bits(wd), to_bits(r)
+    y8, s8 = oracle.down_proj_fp8(hb, wb, rb)
+    y64, _, s = oracle.down_proj(hb, wb, oracle.BF16, rb)
+    assert np.array_equal(y8, y64) and np.array_equal(s8, s)
