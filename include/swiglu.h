@@ -226,6 +226,31 @@ SWIGLU_API int swiglu_up_fp8(const void* x, const void* w8_gate, const void* w8_
 SWIGLU_API size_t swiglu_fp8_workspace_bytes(int64_t M, int64_t d, int64_t d_ff, int path);
 
 /*
+ * The same FP8 contract for the down projection y = h . W_down (+ residual)
+ * ("1 . Anatomie d'un transformeur sur GPU", section 1.6, kernels #10 and
+ * #11): h [M, d_ff] bf16 is quantized per row inside the call, W_down once
+ * per output column, and each f32 sum is scaled by scale_h[i] * scale_w[j]
+ * before the residual (bf16 [M, d], may be y itself) is added and y [M, d]
+ * is rounded to bf16.
+ *
+ * swiglu_quantize_weight_fp8: one bf16 matrix w [K, N] row-major -> e4m3
+ *   codes w8 [N, K] (K contiguous) and f32 column scales s [N]; for the down
+ *   projection K = d_ff, N = d.  Needs K a multiple of 16.  As
+ *   swiglu_quantize_weights_fp8 otherwise.
+ * swiglu_down_fp8: paths AUTO (SKINNY for M <= its skinny limit, else TC),
+ *   SKINNY, TC; needs d_ff a multiple of 16.  Workspace sized by
+ *   swiglu_down_fp8_workspace_bytes (h's codes and row scales first, as in
+ *   swiglu_up_fp8).  Other errors as swiglu_down_ex.
+ */
+SWIGLU_API int swiglu_quantize_weight_fp8(const void* w, void* w8, float* s, int64_t K,
+                                          int64_t N, void* stream);
+SWIGLU_API int swiglu_down_fp8(const void* h, const void* w8_down, const float* s_down,
+                               const void* residual, void* y, int64_t M, int64_t d_ff,
+                               int64_t d, int path, void* workspace, size_t workspace_bytes,
+                               void* stream);
+SWIGLU_API size_t swiglu_down_fp8_workspace_bytes(int64_t M, int64_t d_ff, int64_t d, int path);
+
+/*
  * The whole MLP of "1 . Anatomie d'un transformeur sur GPU", section 1.1,
  * after its RMSNorm: h = silu(x . W_gate) (.) (x . W_up), then
  * y = h . W_down (+ residual).  Two kernels on `stream`; h [M, d_ff] is the

@@ -208,6 +208,63 @@ def quantize_weights_fp8(w_gate, w_up, stream=None):
     return Fp8Weights(w8g, w8u, sg, su)
 
 
+class Fp8Matrix:
+    """One weight matrix quantized to e4m3 per output column: codes [N, K]
+    (uint8, K contiguous) and f32 scales [N]."""
+
+    def __init__(self, w8, s):
+        self.w8, self.s = w8, s
+        self.N, self.K = w8.shape
+
+
+def quantize_weight_fp8(w, stream=None):
+    """Quantize one bf16 matrix w [K, N] (e.g. W_down [d_ff, d]) to e4m3 per
+    output column; returns an Fp8Matrix."""
+    global _LIB
+    import torch
+    _check_cuda(w=w)
+    if w.dtype != torch.bfloat16 or w.dim() != 2:
+        raise ValueError("expected a bfloat16 matrix [K, N]")
+    K, N = w.shape
+    w8 = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    s = torch.empty(N, dtype=torch.float32, device=w.device)
+    st = stream.cuda_stream if stream is not None else _raw_stream(w.device.index)
+    if _LIB is None:
+        _LIB = _lib.load()
+    _call(w.device.index, _LIB.swiglu_quantize_weight_fp8, w.data_ptr(), w8.data_ptr(),
+          s.data_ptr(), K, N, st)
+    return Fp8Matrix(w8, s)
+
+
+def swiglu_down_fp8(h, w, residual=None, out=None, path="auto", workspace=None, stream=None):
+    """y = h @ W_down (+ residual) with e4m3 weights ``w`` (an Fp8Matrix of
+    W_down) and h quantized per row inside the call; h [M, d_ff], residual and
+    the result [M, d] are bfloat16."""
+    global _LIB
+    import torch
+    _check_cuda(h=h, residual=residual)
+    if h.dtype != torch.bfloat16 or h.dim() != 2 or h.shape[1] != w.K:
+        raise ValueError("expected bfloat16 h [M, %d]" % w.K)
+    M, d = h.shape[0], w.N
+    if residual is not None and (residual.shape != (M, d) or residual.dtype != h.dtype):
+        raise ValueError("residual must be a bfloat16 [M, d] tensor")
+    if out is None:
+        out = torch.empty((M, d), dtype=h.dtype, device=h.device)
+    elif out.shape != (M, d) or out.dtype != h.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bfloat16 [M, d] tensor")
+    index = h.device.index
+    st = stream.cuda_stream if stream is not None else _raw_stream(index)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    if _LIB is None:
+        _LIB = _lib.load()
+    _call(index, _LIB.swiglu_down_fp8, h.data_ptr(), w.w8.data_ptr(), w.s.data_ptr(),
+          residual.data_ptr() if residual is not None else None, out.data_ptr(), M, w.K, d,
+          _path_code(path), ws_ptr, ws_bytes, st)
+    return out
+
+
 def fp8_workspace_bytes(M, d, d_ff, path="auto"):
     """Workspace bytes an FP8 call needs on the current device."""
     n = int(_lib.load().swiglu_fp8_workspace_bytes(M, d, d_ff, _path_code(path)))

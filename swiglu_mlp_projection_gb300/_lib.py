@@ -45,6 +45,9 @@ SIGNATURES = {
     "swiglu_quantize_weights_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp], _int),
     "swiglu_up_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp], _int),
     "swiglu_fp8_workspace_bytes": ([_i64, _i64, _i64, _int], _sz),
+    "swiglu_quantize_weight_fp8": ([_vp, _vp, _vp, _i64, _i64, _vp], _int),
+    "swiglu_down_fp8": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp], _int),
+    "swiglu_down_fp8_workspace_bytes": ([_i64, _i64, _i64, _int], _sz),
     "swiglu_pack_weights": ([_vp, _vp, _vp, _i64, _i64, _int, _vp], _int),
     "swiglu_up_packed": ([_vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _vp, _sz, _vp], _int),
     "swiglu_mlp": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp], _int),

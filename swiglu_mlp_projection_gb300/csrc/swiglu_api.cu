@@ -767,6 +767,86 @@ int swiglu_quantize_weights_fp8(const void* w_gate, const void* w_up, void* w8_g
   return SWIGLU_OK;
 }
 
+int swiglu_quantize_weight_fp8(const void* w, void* w8, float* s, int64_t K, int64_t N,
+                               void* stream) {
+  int v = check_sizes(0, K, N, SWIGLU_BF16);
+  if (v != SWIGLU_OK) return v;
+  if (K % 16 != 0)
+    return fail(SWIGLU_ERR_ALIGNMENT, "K must be a multiple of 16 for e4m3 rows");
+  const size_t nw = (size_t)K * N * 2, n8 = (size_t)K * N, ns = (size_t)N * 4;
+  if (n8 && (!w || !w8 || !s)) return fail(SWIGLU_ERR_INVALID_ARG, "null pointer for a non-empty tensor");
+  if ((w && !aligned16(w)) || (w8 && !aligned16(w8)) || (s && !aligned16(s)))
+    return fail(SWIGLU_ERR_ALIGNMENT, "pointers must be 16-byte aligned");
+  if (overlaps(w8, n8, w, nw) || overlaps(s, ns, w, nw) || overlaps(s, ns, w8, n8))
+    return fail(SWIGLU_ERR_INVALID_ARG, "an output overlaps an input or the other output");
+  int dev = 0;
+  DeviceInfo di;
+  if ((v = current_device(&dev, &di)) != SWIGLU_OK) return v;
+  if (n8 == 0) {
+    t_err[0] = 0;
+    return SWIGLU_OK;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaMemPool_t pool;
+  if ((v = device_pool(dev, &pool)) != SWIGLU_OK) return v;
+  void* scratch = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&scratch, (size_t)N * sizeof(unsigned), pool, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(SWIGLU_ERR_OOM, "column maxima: %s", cudaGetErrorString(e));
+  }
+  e = launch_quantize_cols_fp8(w, w8, s, (unsigned*)scratch, K, N, di.num_sms, st);
+  const cudaError_t ef = cudaFreeAsync(scratch, st);
+  if (e == cudaSuccess) e = ef;
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  t_err[0] = 0;
+  return SWIGLU_OK;
+}
+
+int swiglu_down_fp8(const void* h, const void* w8_down, const float* s_down,
+                    const void* residual, void* y, int64_t M, int64_t d_ff, int64_t d, int path,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  // As validate_down, with 1-byte weight codes and the scale vector.
+  int v = check_sizes(M, d, d_ff, SWIGLU_BF16);
+  if (v != SWIGLU_OK) return v;
+  if (d_ff % 16 != 0)
+    return fail(SWIGLU_ERR_ALIGNMENT, "d_ff must be a multiple of 16 for e4m3 rows");
+  const size_t nh = (size_t)M * d_ff * 2, nw = (size_t)d_ff * d, ns = (size_t)d * 4;
+  const size_t ny = (size_t)M * d * 2;
+  if ((nh && !h) || (nw && (!w8_down || !s_down)) || (ny && !y))
+    return fail(SWIGLU_ERR_INVALID_ARG, "null pointer for a non-empty tensor");
+  if ((h && !aligned16(h)) || (w8_down && !aligned16(w8_down)) || (s_down && !aligned16(s_down)) ||
+      (residual && !aligned16(residual)) || (y && !aligned16(y)))
+    return fail(SWIGLU_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
+  if (overlaps(y, ny, h, nh) || overlaps(y, ny, w8_down, nw) || overlaps(y, ny, s_down, ns))
+    return fail(SWIGLU_ERR_INVALID_ARG, "y overlaps an input");
+  if (residual && residual != y && overlaps(y, ny, residual, ny))
+    return fail(SWIGLU_ERR_INVALID_ARG, "residual partially overlaps y");
+  Call c{kOpDown, h, w8_down, w8_down, residual, y, M, d_ff, d, SWIGLU_BF16, path, workspace,
+         workspace_bytes, (cudaStream_t)stream, kWeightsNK};
+  c.fp8 = true;
+  c.sw_a = s_down;
+  c.sw_b = s_down;
+  return run(c);
+}
+
+size_t swiglu_down_fp8_workspace_bytes(int64_t M, int64_t d_ff, int64_t d, int path) {
+  if (check_sizes(M < 0 ? -1 : M, d, d_ff, SWIGLU_BF16) != SWIGLU_OK) return 0;
+  if (d_ff % 16 != 0) {
+    fail(SWIGLU_ERR_ALIGNMENT, "d_ff must be a multiple of 16 for e4m3 rows");
+    return 0;
+  }
+  int dev = 0;
+  DeviceInfo di;
+  if (current_device(&dev, &di) != SWIGLU_OK) return 0;
+  Plan p;
+  if (make_plan(kOpDown, M, d_ff / 2, d, SWIGLU_BF16, path, di.num_sms, di.max_pairs, &p, true,
+                di.sk_caps) != SWIGLU_OK)
+    return 0;
+  t_err[0] = 0;
+  return p.workspace + fp8_prefix_bytes(M, d_ff);
+}
+
 int swiglu_up_fp8(const void* x, const void* w8_gate, const void* w8_up, const float* s_gate,
                   const float* s_up, void* h, int64_t M, int64_t d, int64_t d_ff, int path,
                   void* workspace, size_t workspace_bytes, void* stream) {

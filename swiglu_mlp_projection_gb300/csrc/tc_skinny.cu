@@ -127,6 +127,13 @@ __device__ __forceinline__ int64_t cta_of(int64_t t, int64_t U, int64_t G) {
   return ((t + 1) * G + U - 1) / U - 1;
 }
 
+// FP8, plain mode: the sums of row m, columns col..col+3 times sx[m] sw[col..].
+__device__ __forceinline__ void fp8_scale1(float4& g, const SkArgs& a, int m, int64_t col) {
+  const float sxm = a.sx[m];
+  const float4 sw = *reinterpret_cast<const float4*>(a.sw_a + col);
+  g.x *= sxm * sw.x; g.y *= sxm * sw.y; g.z *= sxm * sw.z; g.w *= sxm * sw.w;
+}
+
 // FP8: the sums of row m, columns col..col+3 times sx[m] sw[col..].
 __device__ __forceinline__ void fp8_scale(float4& g, float4& u, const SkArgs& a, int m,
                                           int64_t col) {
@@ -487,6 +494,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
               ov.x = pack_bf16x2(silu_fast(g[i].x) * u[i].x, silu_fast(g[i].y) * u[i].y);
               ov.y = pack_bf16x2(silu_fast(g[i].z) * u[i].z, silu_fast(g[i].w) * u[i].w);
             } else {
+              if constexpr (FP8) fp8_scale1(g[i], a, m, col);
               if (a.resid) {
                 const uint2 rv = *reinterpret_cast<const uint2*>(a.resid + o);
                 g[i].x += bf16_lo(rv.x); g[i].y += bf16_hi(rv.x);
@@ -553,6 +561,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
           ov.x = pack_bf16x2(silu_fast(g.x) * u.x, silu_fast(g.y) * u.y);
           ov.y = pack_bf16x2(silu_fast(g.z) * u.z, silu_fast(g.w) * u.w);
         } else {
+          if constexpr (FP8) fp8_scale1(g, a, m, col);
           if (a.resid) {
             const uint2 rv = *reinterpret_cast<const uint2*>(a.resid + o);
             g.x += bf16_lo(rv.x); g.y += bf16_hi(rv.x);
@@ -733,7 +742,7 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
                              unsigned* counters, bool counters_clean, unsigned* status,
                              uint64_t timeout_ns, cudaStream_t st, const Fp8Scales* fp8) {
   if (p.units == 0 || M == 0) return cudaSuccess;
-  if (fp8 && (p.plain || wlayout != kWeightsNK)) return cudaErrorInvalidValue;
+  if (fp8 && wlayout != kWeightsNK) return cudaErrorInvalidValue;
   CUtensorMap mx, mg, mu;
   cudaError_t e;
   if ((e = make_tmap_bf16_2d(&mx, x, M, K, kBK, p.n_pad)) != cudaSuccess) return e;
@@ -773,7 +782,9 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   a.resid = (const uint16_t*)resid;
   a.status = status;
   a.timeout_ns = timeout_ns;
-  if (p.plain) return launch_mode<kPlain, false>(p.n_pad, p.nb, mx, mg, mu, a, st);
+  if (p.plain)
+    return fp8 ? launch_mode<kPlain, true>(p.n_pad, p.nb, mx, mg, mu, a, st)
+               : launch_mode<kPlain, false>(p.n_pad, p.nb, mx, mg, mu, a, st);
   return fp8 ? launch_mode<kSwiGLU, true>(p.n_pad, p.nb, mx, mg, mu, a, st)
              : launch_mode<kSwiGLU, false>(p.n_pad, p.nb, mx, mg, mu, a, st);
 }

@@ -521,8 +521,9 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
               u[i] = __float_as_uint(us[i]);
             }
           }
-          if constexpr (MODE == kSwiGLU && FP8) {
-            // FP8: the sums times sx[row] sw[column]
+          if constexpr (FP8) {
+            // FP8: the sums times sx[row] sw[column] (gate / output columns
+            // from sw_a, up columns from sw_b)
             const float sxm = grow < a.M ? a.sx[grow] : 0.f;
             const int64_t c0 = (int64_t)nb * kOutCols + pass * kBN + ch * 32;
 #pragma unroll
@@ -530,13 +531,14 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
               float4 sg = make_float4(0.f, 0.f, 0.f, 0.f), su = sg;
               if (c0 + 4 * v < a.n_out) {   // n_out is a multiple of 8
                 sg = reinterpret_cast<const float4*>(a.sw_a + c0)[v];
-                su = reinterpret_cast<const float4*>(a.sw_b + c0)[v];
+                if constexpr (MODE == kSwiGLU) su = reinterpret_cast<const float4*>(a.sw_b + c0)[v];
               }
               const float sgv[4] = {sg.x, sg.y, sg.z, sg.w}, suv[4] = {su.x, su.y, su.z, su.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 g[4 * v + e] = __float_as_uint(__uint_as_float(g[4 * v + e]) * (sxm * sgv[e]));
-                u[4 * v + e] = __float_as_uint(__uint_as_float(u[4 * v + e]) * (sxm * suv[e]));
+                if constexpr (MODE == kSwiGLU)
+                  u[4 * v + e] = __float_as_uint(__uint_as_float(u[4 * v + e]) * (sxm * suv[e]));
               }
             }
           }
@@ -764,7 +766,7 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
                            cudaStream_t st, const Fp8Scales* fp8) {
   if (p.tiles == 0 || K == 0) return cudaSuccess;
   if (p.sk_iters && (!part || !counters)) return cudaErrorInvalidValue;
-  if (fp8 && (p.plain || wlayout != kWeightsNK)) return cudaErrorInvalidValue;
+  if (fp8 && wlayout != kWeightsNK) return cudaErrorInvalidValue;
   CUtensorMap mx, mg, mu, mh;
   cudaError_t e;
   if ((e = make_tmap_bf16_2d(&mx, x, M, K, kBK, kBM)) != cudaSuccess) return e;
@@ -805,6 +807,9 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
   if (p.sk_iters && !counters_clean &&
       (e = cudaMemsetAsync(counters, 0, p.counters_bytes, st)) != cudaSuccess)
     return e;
+  if (fp8 && p.plain)
+    return p.pair ? launch_mode<kPlain, true, true>(mx, mg, mu, mh, a, p.grid, st)
+                  : launch_mode<kPlain, false, true>(mx, mg, mu, mh, a, p.grid, st);
   if (fp8)
     return p.pair ? launch_mode<kSwiGLU, true, true>(mx, mg, mu, mh, a, p.grid, st)
                   : launch_mode<kSwiGLU, false, true>(mx, mg, mu, mh, a, p.grid, st);

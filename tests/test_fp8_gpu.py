@@ -142,3 +142,50 @@ def test_fp8_full_size_sampled(M):
     res = compare(to64(h)[np.ix_(rows, cols)], h64, sens, "bf16", d)
     assert res["ok"], (M, res)
     swg.check_device_status()
+
+
+# ---------------------------------------------------------------------------
+# The FP8 down projection
+# ---------------------------------------------------------------------------
+
+def down_check(M, d_ff, d, path, seed=0, rows=None):
+    h = inputs.make_inputs(M, d_ff, 8, "bf16", seed=seed, x_only=True)[0]
+    _, wd, _ = inputs.make_inputs(1, d_ff, d, "bf16", seed=seed + 1)
+    r = inputs.make_inputs(M, d, 8, "bf16", seed=seed + 2, x_only=True)[0]
+    w8 = swg.quantize_weight_fp8(wd.to(DEV))
+    y = swg.swiglu_down_fp8(h.to(DEV), w8, residual=r.to(DEV), path=path)
+    torch.cuda.synchronize()
+    sel = slice(None) if rows is None else rows
+    y64, sens = oracle.down_proj_fp8(RAW(h[sel].contiguous()), RAW(wd), RAW(r[sel].contiguous()))
+    res = compare(to64(y)[sel], y64, sens, "bf16", d_ff)
+    assert res["ok"], (M, d_ff, d, path, res)
+    return w8, wd
+
+
+@pytest.mark.parametrize("shape", [(1, 528, 136), (16, 1040, 264), (65, 528, 520),
+                                   (300, 1040, 392)])
+@pytest.mark.parametrize("path", ["skinny", "tc", "auto"])
+def test_fp8_down_matches_oracle(shape, path):
+    if path == "skinny" and shape[0] > 256:
+        pytest.skip("skinny path serves M <= 256")
+    w8, wd = down_check(*shape, path, seed=sum(shape))
+    c, s = oracle.quantize_cols_e4m3(RAW(wd))
+    assert np.array_equal(w8.w8.cpu().numpy(), c)
+    assert np.array_equal(w8.s.cpu().numpy().view(np.uint32), s.view(np.uint32))
+
+
+@pytest.mark.parametrize("env,path,shape", [
+    (("SWIGLU_TILE_PAIR", "0"), "tc", (300, 528, 392)),
+    (("SWIGLU_TILE_SK", "1"), "tc", (40, 1040, 520)),
+    (("SWIGLU_SK_CLUSTER", "8"), "skinny", (3, 4864, 896)),
+    (("SWIGLU_SK_CLUSTER", "0"), "skinny", (3, 4864, 896))])
+def test_fp8_down_kernel_modes(env, path, shape, monkeypatch):
+    monkeypatch.setenv(*env)
+    down_check(*shape, path, seed=9)
+
+
+def test_fp8_down_full_size_sampled():
+    # d = 4096, d_ff = 14336 at decode and prefill sizes, sampled rows
+    for M, rows in ((16, [0, 15]), (4096, [0, 255, 4095])):
+        down_check(M, 14336, 4096, "auto", seed=M, rows=rows)
+    swg.check_device_status()
