@@ -589,7 +589,8 @@ def other_configs(dev, peaks, l2, iters):
 def fp8_configs(dev, peaks, iters):
     """The FP8 (e4m3) up projection at d=4096, d_ff=14336: the decode sweep
     and the prefill call, back to back with 2 weight copies (117 MB each,
-    larger than L2).  GB/s counts fp8_bytes; TFLOP/s is against the FP8
+    larger than L2); then the FP8 down projection and the FP8 MLP (both
+    projections, with the residual) at M = 1, 16, 4096.  GB/s counts fp8_bytes; TFLOP/s is against the FP8
     dense peak taken as 2x the measured bf16 peak (the nominal FP8 : BF16
     ratio, 4.5 : 2.25 PFLOP/s)."""
     import torch
@@ -627,7 +628,42 @@ def fp8_configs(dev, peaks, iters):
             e["frac_fp8"] = round(fl / ms / 1e9 / fp8_peak, 4)
         out["fp8_d4096/M=%d" % M] = e
         del x, h
-    del qs
+    # the FP8 down projection and the whole FP8 MLP (both projections e4m3)
+    _, wd, _ = inputs.make_inputs(1, d_ff, d, "bf16", seed=1)
+    wdd = wd.to(dev)
+    qds = [swg.quantize_weight_fp8(wdd) for _ in range(2)]
+    del wd, wdd
+    for M in (1, 16, 4096):
+        x = inputs.make_inputs(M, d, 8, "bf16", seed=M, x_only=True)[0].to(dev)
+        hb = torch.empty(M, d_ff, dtype=torch.bfloat16, device=dev)
+        y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+        swg.swiglu_up_fp8(x, qs[0], out=hb)
+        for name, fn, by, fl in (
+                ("fp8_down_d4096", lambda i: swg.swiglu_down_fp8(hb, qds[i % 2], residual=x, out=y),
+                 d_ff * d + 4 * d + 2 * M * d_ff + 4 * M * d, workload.down_flops(M, d_ff, d)),
+                ("fp8_mlp_d4096", lambda i: (swg.swiglu_up_fp8(x, qs[i % 2], out=hb),
+                                             swg.swiglu_down_fp8(hb, qds[i % 2], residual=x, out=y)),
+                 workload.fp8_bytes(M, d, d_ff) + d_ff * d + 4 * d + 2 * M * d_ff + 4 * M * d,
+                 workload.flops(M, d, d_ff) + workload.down_flops(M, d_ff, d))):
+            for i in range(3):
+                fn(i)
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for i in range(iters):
+                fn(i)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1) / iters
+            e = {"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
+                 "TFLOP/s": round(fl / ms / 1e9, 2)}
+            if M <= 16:
+                e["frac_hbm"] = round(by / ms / 1e6 / peaks["hbm_gbs"], 4)
+            else:
+                e["frac_fp8"] = round(fl / ms / 1e9 / fp8_peak, 4)
+            out["%s/M=%d" % (name, M)] = e
+        del x, hb, y
+    del qs, qds
     torch.cuda.empty_cache()
     return out
 
