@@ -196,6 +196,55 @@ void mark_workspaces_dirty(int dev) {
     if (e.dev == dev) e.dirty = true;
 }
 
+// Arrival counters for calls captured into CUDA graphs.  A captured call's
+// workspace is a graph allocation whose contents are undefined on every
+// replay, so its counters would need a memset node, which costs ~5 us per
+// d = 4096 decode call and breaks the programmatic overlap with the previous
+// kernel.  Instead each captured call takes its own counters, once, from a
+// per-device region zeroed when it was created; the kernels leave them at
+// zero, so every replay finds them clean.  Slices are never reused: graphs
+// replay independently of each other (a graph exec never overlaps itself).
+// The region is created by the first non-captured call that uses counters
+// (one synchronisation of that call's stream); captures made before it, or
+// after it fills up, fall back to allocating and clearing.
+struct GraphCounters {
+  char* base = nullptr;
+  size_t cap = 0, used = 0;
+  bool tried = false;
+};
+GraphCounters g_gctr[kMaxDevices];   // guarded by g_mu
+constexpr size_t kGraphCounterBytes = (size_t)4 << 20;
+
+void ensure_graph_counters(int dev, cudaStream_t st) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_gctr[dev].tried) return;
+    g_gctr[dev].tried = true;
+  }
+  cudaMemPool_t pool;
+  if (device_pool(dev, &pool) != SWIGLU_OK) return;
+  void* p = nullptr;
+  if (cudaMallocFromPoolAsync(&p, kGraphCounterBytes, pool, st) != cudaSuccess ||
+      cudaMemsetAsync(p, 0, kGraphCounterBytes, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_gctr[dev].base = (char*)p;
+  g_gctr[dev].cap = kGraphCounterBytes;
+}
+
+unsigned* take_graph_counters(int dev, size_t bytes) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  GraphCounters& g = g_gctr[dev];
+  bytes = (bytes + 255) / 256 * 256;
+  if (!g.base || g.used + bytes > g.cap) return nullptr;
+  unsigned* r = (unsigned*)(g.base + g.used);
+  g.used += bytes;
+  return r;
+}
+
 int elem_bytes(int dtype) { return dtype == SWIGLU_BF16 ? 2 : 4; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -499,20 +548,36 @@ int run(const Call& c) {
         counters_clean = true;
         fp8_base = (char*)part;
         part = (float*)((char*)part + fp8_prefix);
+        if (counter_bytes) ensure_graph_counters(dev, st);
       } else {
-        cudaMemPool_t pool;
-        if ((v = device_pool(dev, &pool)) != SWIGLU_OK) return v;
-        cudaError_t e = cudaMallocFromPoolAsync(&pooled, p.workspace, pool, st);
-        if (e != cudaSuccess) {
-          if (e == cudaErrorMemoryAllocation) {
-            cudaGetLastError();
-            return fail(SWIGLU_ERR_OOM, "workspace of %zu bytes: %s", p.workspace,
-                        cudaGetErrorString(e));
+        // A captured call takes clean counters from the graph-counter region
+        // when it can (see GraphCounters) and allocates only the rest.
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (counter_bytes && cudaStreamIsCapturing(st, &cs) == cudaSuccess &&
+            cs != cudaStreamCaptureStatusNone)
+          counters = take_graph_counters(dev, counter_bytes);
+        cudaGetLastError();
+        const size_t own = counters ? p.workspace - counter_bytes : p.workspace;
+        if (own > 0) {
+          cudaMemPool_t pool;
+          if ((v = device_pool(dev, &pool)) != SWIGLU_OK) return v;
+          cudaError_t e = cudaMallocFromPoolAsync(&pooled, own, pool, st);
+          if (e != cudaSuccess) {
+            if (e == cudaErrorMemoryAllocation) {
+              cudaGetLastError();
+              return fail(SWIGLU_ERR_OOM, "workspace of %zu bytes: %s", own,
+                          cudaGetErrorString(e));
+            }
+            return cuda_fail(e, "cudaMallocFromPoolAsync");
           }
-          return cuda_fail(e, "cudaMallocFromPoolAsync");
         }
-        counters = (unsigned*)pooled;
-        fp8_base = (char*)pooled + counter_bytes;
+        if (counters) {
+          counters_clean = true;
+          fp8_base = (char*)pooled;
+        } else {
+          counters = (unsigned*)pooled;
+          fp8_base = (char*)pooled + counter_bytes;
+        }
         part = (float*)(fp8_base + fp8_prefix);
       }
     }

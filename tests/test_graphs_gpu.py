@@ -50,3 +50,67 @@ def test_capture_and_replay(case):
     assert torch.equal(h2.view(torch.int16 if dtype == "bf16" else torch.int32),
                        hs.view(torch.int16 if dtype == "bf16" else torch.int32))
     swg.check_device_status()
+
+
+@pytest.mark.parametrize("env,path,shape", [
+    (("SWIGLU_SK_CLUSTER", "0"), "skinny", (4, 512, 1032)),    # stream-K: arrival counters
+    (("SWIGLU_TILE_SK", "1"), "tc", (40, 1040, 520)),           # tile stream-K tail
+    (None, "auto", (16, 4096, 14336))])                         # the decode shape
+def test_graphs_with_arrival_counters(env, path, shape, monkeypatch):
+    # Captured calls whose kernels count arrivals take their counters from a
+    # region that stays zero between replays; two graphs of the same call,
+    # replayed alternately, each keep their own.
+    if env:
+        monkeypatch.setenv(*env)
+    M, d, d_ff = shape
+    dev = torch.device("cuda", 0)
+    x0, wg, wu = inputs.make_inputs(M, d, d_ff, "bf16", seed=60)
+    xs, wgs, wus = x0.to(dev), wg.to(dev), wu.to(dev)
+    ha = torch.empty(M, d_ff, dtype=xs.dtype, device=dev)
+    hb = torch.empty(M, d_ff, dtype=xs.dtype, device=dev)
+    swg.swiglu_up(xs, wgs, wus, out=ha, path=path)          # outside capture first
+    torch.cuda.synchronize()
+    graphs = []
+    for h in (ha, hb):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(2):
+                swg.swiglu_up(xs, wgs, wus, out=h, path=path)
+        graphs.append(g)
+    for rep, seed in enumerate((61, 62, 63)):
+        xn = inputs.make_inputs(M, d, d_ff, "bf16", seed=seed, x_only=True)[0]
+        xs.copy_(xn.to(dev))
+        for g in graphs:
+            g.replay()
+        torch.cuda.synchronize()
+        for h in (ha, hb):
+            if M * d_ff <= 2 ** 16:
+                res = _check(h, xn, wg, wu, "bf16", d)
+                assert res["ok"], (shape, rep, res)
+        assert torch.equal(ha.view(torch.int16), hb.view(torch.int16))
+    ref = swg.swiglu_up(xs, wgs, wus, path=path)
+    torch.cuda.synchronize()
+    assert torch.equal(ref.view(torch.int16), ha.view(torch.int16))
+    swg.check_device_status()
+
+
+def test_fp8_call_in_a_graph():
+    M, d, d_ff = 8, 1040, 1032
+    dev = torch.device("cuda", 0)
+    x0, wg, wu = inputs.make_inputs(M, d, d_ff, "bf16", seed=70)
+    w8 = swg.quantize_weights_fp8(wg.to(dev), wu.to(dev))
+    xs = x0.to(dev)
+    h = torch.empty(M, d_ff, dtype=xs.dtype, device=dev)
+    swg.swiglu_up_fp8(xs, w8, out=h)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        swg.swiglu_up_fp8(xs, w8, out=h)
+    xn = inputs.make_inputs(M, d, d_ff, "bf16", seed=71, x_only=True)[0]
+    xs.copy_(xn.to(dev))
+    g.replay()
+    torch.cuda.synchronize()
+    raw = inputs.raw_bits
+    h64, sens, _ = oracle.swiglu_up_fp8(raw(xn), raw(wg), raw(wu))
+    res = compare(h.to("cpu", torch.float64).numpy(), h64, sens, "bf16", d)
+    assert res["ok"], res
