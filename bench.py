@@ -324,10 +324,10 @@ def run_ours(args):
 
     counter = [0]
 
-    def call(M):
+    def call(M, st=None):
         wgc, wuc = copies[counter[0] % n_copies]
         counter[0] += 1
-        swg.swiglu_up(xs[M], wgc, wuc, out=hs[M], stream=stream)
+        swg.swiglu_up(xs[M], wgc, wuc, out=hs[M], stream=st if st is not None else stream)
 
     def step():
         for M in SWEEP:
@@ -453,9 +453,31 @@ def run_ours(args):
             l1.record(stream)
             torch.cuda.synchronize(dev)
             lat.append(l0.elapsed_time(l1))
+        # the same calls captured into a CUDA graph (as a serving loop would
+        # replay them), on a side stream
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gs):
+            call(M, gs)
+            with torch.cuda.graph(graph, stream=gs):
+                for _ in range(20):
+                    call(M, gs)
+        stream.wait_stream(gs)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(3):
+            graph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        graph_ms = g0.elapsed_time(g1) / 60
+        del graph
         sweep[str(M)] = {"us": round(ms * 1e3, 2), "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
                          "frac": round(b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                          "isolated_call_us": round(statistics.median(lat) * 1e3, 2),
+                         "graph_us": round(graph_ms * 1e3, 2),
                          "path": plans[M]["path"]}
 
     extra = next_rows = fp8_rows = None
