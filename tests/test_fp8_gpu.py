@@ -118,16 +118,17 @@ def test_fp8_deterministic_and_errors():
     swg.check_device_status()
 
 
-@pytest.mark.parametrize("M", [1, 16, 4096])
-def test_fp8_full_size_sampled(M):
-    # d = 4096, d_ff = 14336: the weight codes are checked against the oracle
-    # on sampled columns, and h on those columns for sampled rows
-    d, d_ff = 4096, 14336
+@pytest.mark.parametrize("M,d,d_ff", [(1, 4096, 14336), (16, 4096, 14336), (4096, 4096, 14336),
+                                       (16, 8192, 29568), (2048, 8192, 29568)])
+def test_fp8_full_size_sampled(M, d, d_ff):
+    # the decode, prefill and large-model shapes: the weight codes are checked
+    # against the oracle on sampled columns, and h on those columns for
+    # sampled rows
     x, wg, wu = make(M, d, d_ff, seed=M)
     w = swg.quantize_weights_fp8(wg.to(DEV), wu.to(DEV))
     h = swg.swiglu_up_fp8(x.to(DEV), w)
     torch.cuda.synchronize()
-    cols = np.arange(3, d_ff, 211)
+    cols = np.arange(3, d_ff, 211 if d_ff < 20000 else 421)
     rows = np.unique(np.linspace(0, M - 1, min(M, 6)).astype(int))
     gsub, usub = RAW(wg)[:, cols].copy(), RAW(wu)[:, cols].copy()
     cg, sg = oracle.quantize_cols_e4m3(gsub)
