@@ -783,24 +783,34 @@ int swiglu_pack_weights(const void* w_gate, const void* w_up, void* w_packed, in
   return SWIGLU_OK;
 }
 
-int swiglu_quantize_weights_fp8(const void* w_gate, const void* w_up, void* w8_gate,
-                                void* w8_up, float* s_gate, float* s_up, int64_t d,
-                                int64_t d_ff, void* stream) {
-  int v = check_sizes(0, d, d_ff, SWIGLU_BF16);
+// The weight quantizers: `n` bf16 matrices w[i] [K, N] row-major -> e4m3
+// codes w8[i] [N, K] and f32 column scales s[i] [N], all checked first (sizes,
+// null pointers, 16-byte alignment, no output overlapping an input or another
+// output), with one short-lived N * 4-byte pool allocation for the column
+// maxima.
+static int quantize_weights(int n, const void* const* w, void* const* w8, float* const* s,
+                            int64_t K, int64_t N, const char* kname, cudaStream_t st) {
+  int v = check_sizes(0, K, N, SWIGLU_BF16);
   if (v != SWIGLU_OK) return v;
-  if (d % 16 != 0)
-    return fail(SWIGLU_ERR_ALIGNMENT, "d must be a multiple of 16 for e4m3 rows");
-  const size_t nw = (size_t)d * d_ff * 2, n8 = (size_t)d * d_ff, ns = (size_t)d_ff * 4;
-  if (n8 && (!w_gate || !w_up || !w8_gate || !w8_up || !s_gate || !s_up))
-    return fail(SWIGLU_ERR_INVALID_ARG, "null pointer for a non-empty tensor");
-  const void* ptrs[6] = {w_gate, w_up, w8_gate, w8_up, s_gate, s_up};
-  for (const void* q : ptrs)
-    if (q && !aligned16(q)) return fail(SWIGLU_ERR_ALIGNMENT, "pointers must be 16-byte aligned");
-  const void* outs[4] = {w8_gate, w8_up, s_gate, s_up};
-  const size_t out_n[4] = {n8, n8, ns, ns};
-  for (int i = 0; i < 4; ++i) {
-    if (overlaps(outs[i], out_n[i], w_gate, nw) || overlaps(outs[i], out_n[i], w_up, nw))
-      return fail(SWIGLU_ERR_INVALID_ARG, "an output overlaps an input");
+  if (K % 16 != 0)
+    return fail(SWIGLU_ERR_ALIGNMENT, "%s must be a multiple of 16 for e4m3 rows", kname);
+  const size_t nw = (size_t)K * N * 2, n8 = (size_t)K * N, ns = (size_t)N * 4;
+  const void* outs[4];
+  size_t out_n[4];
+  for (int i = 0; i < n; ++i) {
+    if (n8 && (!w[i] || !w8[i] || !s[i]))
+      return fail(SWIGLU_ERR_INVALID_ARG, "null pointer for a non-empty tensor");
+    if ((w[i] && !aligned16(w[i])) || (w8[i] && !aligned16(w8[i])) || (s[i] && !aligned16(s[i])))
+      return fail(SWIGLU_ERR_ALIGNMENT, "pointers must be 16-byte aligned");
+    outs[2 * i] = w8[i];
+    out_n[2 * i] = n8;
+    outs[2 * i + 1] = s[i];
+    out_n[2 * i + 1] = ns;
+  }
+  for (int i = 0; i < 2 * n; ++i) {
+    for (int j = 0; j < n; ++j)
+      if (overlaps(outs[i], out_n[i], w[j], nw))
+        return fail(SWIGLU_ERR_INVALID_ARG, "an output overlaps an input");
     for (int j = 0; j < i; ++j)
       if (overlaps(outs[i], out_n[i], outs[j], out_n[j]))
         return fail(SWIGLU_ERR_INVALID_ARG, "outputs overlap");
@@ -812,46 +822,6 @@ int swiglu_quantize_weights_fp8(const void* w_gate, const void* w_up, void* w8_g
     t_err[0] = 0;
     return SWIGLU_OK;
   }
-  cudaStream_t st = (cudaStream_t)stream;
-  cudaMemPool_t pool;
-  if ((v = device_pool(dev, &pool)) != SWIGLU_OK) return v;
-  void* scratch = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(&scratch, (size_t)d_ff * sizeof(unsigned), pool, st);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return fail(SWIGLU_ERR_OOM, "column maxima: %s", cudaGetErrorString(e));
-  }
-  e = launch_quantize_cols_fp8(w_gate, w8_gate, s_gate, (unsigned*)scratch, d, d_ff,
-                               di.num_sms, st);
-  if (e == cudaSuccess)
-    e = launch_quantize_cols_fp8(w_up, w8_up, s_up, (unsigned*)scratch, d, d_ff, di.num_sms, st);
-  const cudaError_t ef = cudaFreeAsync(scratch, st);
-  if (e == cudaSuccess) e = ef;
-  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
-  t_err[0] = 0;
-  return SWIGLU_OK;
-}
-
-int swiglu_quantize_weight_fp8(const void* w, void* w8, float* s, int64_t K, int64_t N,
-                               void* stream) {
-  int v = check_sizes(0, K, N, SWIGLU_BF16);
-  if (v != SWIGLU_OK) return v;
-  if (K % 16 != 0)
-    return fail(SWIGLU_ERR_ALIGNMENT, "K must be a multiple of 16 for e4m3 rows");
-  const size_t nw = (size_t)K * N * 2, n8 = (size_t)K * N, ns = (size_t)N * 4;
-  if (n8 && (!w || !w8 || !s)) return fail(SWIGLU_ERR_INVALID_ARG, "null pointer for a non-empty tensor");
-  if ((w && !aligned16(w)) || (w8 && !aligned16(w8)) || (s && !aligned16(s)))
-    return fail(SWIGLU_ERR_ALIGNMENT, "pointers must be 16-byte aligned");
-  if (overlaps(w8, n8, w, nw) || overlaps(s, ns, w, nw) || overlaps(s, ns, w8, n8))
-    return fail(SWIGLU_ERR_INVALID_ARG, "an output overlaps an input or the other output");
-  int dev = 0;
-  DeviceInfo di;
-  if ((v = current_device(&dev, &di)) != SWIGLU_OK) return v;
-  if (n8 == 0) {
-    t_err[0] = 0;
-    return SWIGLU_OK;
-  }
-  cudaStream_t st = (cudaStream_t)stream;
   cudaMemPool_t pool;
   if ((v = device_pool(dev, &pool)) != SWIGLU_OK) return v;
   void* scratch = nullptr;
@@ -860,12 +830,27 @@ int swiglu_quantize_weight_fp8(const void* w, void* w8, float* s, int64_t K, int
     cudaGetLastError();
     return fail(SWIGLU_ERR_OOM, "column maxima: %s", cudaGetErrorString(e));
   }
-  e = launch_quantize_cols_fp8(w, w8, s, (unsigned*)scratch, K, N, di.num_sms, st);
+  for (int i = 0; i < n && e == cudaSuccess; ++i)
+    e = launch_quantize_cols_fp8(w[i], w8[i], s[i], (unsigned*)scratch, K, N, di.num_sms, st);
   const cudaError_t ef = cudaFreeAsync(scratch, st);
   if (e == cudaSuccess) e = ef;
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   t_err[0] = 0;
   return SWIGLU_OK;
+}
+
+int swiglu_quantize_weights_fp8(const void* w_gate, const void* w_up, void* w8_gate,
+                                void* w8_up, float* s_gate, float* s_up, int64_t d,
+                                int64_t d_ff, void* stream) {
+  const void* w[2] = {w_gate, w_up};
+  void* w8[2] = {w8_gate, w8_up};
+  float* s[2] = {s_gate, s_up};
+  return quantize_weights(2, w, w8, s, d, d_ff, "d", (cudaStream_t)stream);
+}
+
+int swiglu_quantize_weight_fp8(const void* w, void* w8, float* s, int64_t K, int64_t N,
+                               void* stream) {
+  return quantize_weights(1, &w, &w8, &s, K, N, "K", (cudaStream_t)stream);
 }
 
 int swiglu_down_fp8(const void* h, const void* w8_down, const float* s_down,

@@ -75,9 +75,9 @@ static_assert(TileCfg<true>::kSmemBytes <= 232448, "pair tile exceeds shared mem
 static_assert(TileCfg<false>::kSmemBytes <= 232448, "tile exceeds shared memory");
 
 struct TileArgs {
-  int n_mb, n_nb, n_kb, n_out;   // n_mb: row blocks of the tile height; n_out: output columns
+  int n_mb, n_kb, n_out;         // n_mb: row blocks of the tile height (tile t: row block
+                                 // t % n_mb, column block t / n_mb); n_out: output columns
   int M;
-  int64_t tiles;
   const uint16_t* resid;         // plain mode: [M][n_out] added to the sums, or null
   int kmajor;                    // weights stored [n_out, K] instead of [K, n_out]
   int packed;                    // SwiGLU: one packed gate/up matrix (tm_wg = tm_wu)
@@ -783,11 +783,9 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
   if ((e = make_tmap_bf16_2d(&mh, out, M, n_out, 64, kBM)) != cudaSuccess) return e;
   TileArgs a;
   a.n_mb = (int)p.n_mb;
-  a.n_nb = (int)p.n_nb;
   a.n_kb = (int)((K + kBK - 1) / kBK);
   a.n_out = (int)n_out;
   a.M = (int)M;
-  a.tiles = p.tiles;
   a.resid = (const uint16_t*)resid;
   a.kmajor = w_kmajor ? 1 : 0;
   a.packed = packed ? 1 : 0;
