@@ -445,9 +445,14 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         // 16-byte loads, several outputs in flight together.  SwiGLU: gate
         // and up partials of the same columns; plain: one partial per column.
         const float* pg = a.part + cg * a.maxq * NB * 2 * Mrow;
+        const int64_t q_stride = (int64_t)NB * 2 * Mrow;   // floats of one slot
         constexpr int kChunks = kGroupCols / 4;      // 4-column chunks per row of the group
         const int total = a.M * kChunks;
+        // The sums are bound by L2 latency, not bandwidth: each round of loads
+        // waits one L2 round trip.  So a round loads kQ slots' partials of
+        // kBatch chunks (twice that for SwiGLU) before it adds any of them.
         constexpr int kBatch = 4;
+        constexpr int kQ = MODE == kSwiGLU ? 2 : 4;
         for (int base = et; base < total; base += kBatch * kEpiThreads) {
           float4 g[kBatch], u[kBatch];
           int off[kBatch];
@@ -456,7 +461,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             g[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             u[i] = g[i];
             const int idx = base + i * kEpiThreads;
-            const int id = idx < total ? idx : 0;
+            const int id = idx < total ? idx : 0;    // a chunk past the end reads chunk 0, unused
             const int m = id / kChunks, ch = id - m * kChunks;
             // SwiGLU: chunk ch -> sub-block ch/16, gate half; plain: sub-block
             // ch/32, half (ch/16)&1.  Either way (ch >> 4) picks the [M][64]
@@ -465,17 +470,32 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             off[i] = blk * (int)Mrow + m * kCB + (ch & 15) * 4;
           }
           // slot q holds CTA (c_lo + q)'s sums; adding in q order is k order
-#pragma unroll 2
-          for (int q = 0; q < n_contrib; ++q) {
-            const float* pq = pg + (int64_t)q * NB * 2 * Mrow;
+          for (int q0 = 0; q0 < n_contrib; q0 += kQ) {
+            float4 vg[kQ][kBatch], vu[kQ][kBatch];
 #pragma unroll
-            for (int i = 0; i < kBatch; ++i) {
-              if (base + i * kEpiThreads < total) {
-                const float4 pgv = __ldcg(reinterpret_cast<const float4*>(pq + off[i]));
-                g[i].x += pgv.x; g[i].y += pgv.y; g[i].z += pgv.z; g[i].w += pgv.w;
-                if constexpr (MODE == kSwiGLU) {
-                  const float4 puv = __ldcg(reinterpret_cast<const float4*>(pq + off[i] + Mrow));
-                  u[i].x += puv.x; u[i].y += puv.y; u[i].z += puv.z; u[i].w += puv.w;
+            for (int j = 0; j < kQ; ++j) {
+              const bool have = q0 + j < n_contrib;
+              const float* pq = pg + (int64_t)(q0 + j) * q_stride;
+#pragma unroll
+              for (int i = 0; i < kBatch; ++i) {
+                vg[j][i] = have ? __ldcg(reinterpret_cast<const float4*>(pq + off[i]))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                if constexpr (MODE == kSwiGLU)
+                  vu[j][i] = have ? __ldcg(reinterpret_cast<const float4*>(pq + off[i] + Mrow))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < kQ; ++j) {
+              if (q0 + j < n_contrib) {
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i) {
+                  g[i].x += vg[j][i].x; g[i].y += vg[j][i].y;
+                  g[i].z += vg[j][i].z; g[i].w += vg[j][i].w;
+                  if constexpr (MODE == kSwiGLU) {
+                    u[i].x += vu[j][i].x; u[i].y += vu[j][i].y;
+                    u[i].z += vu[j][i].z; u[i].w += vu[j][i].w;
+                  }
                 }
               }
             }
