@@ -311,7 +311,9 @@ typedef struct {
   int64_t grid;          /* CTAs of the main kernel                              */
   int64_t row_chunk;     /* rows of x per SIMT pass (SIMT path)                  */
   int64_t workspace;     /* bytes of partial sums                                */
-  int64_t skinny_max_m;  /* largest bf16 M that AUTO sends to SKINNY            */
+  int64_t skinny_max_m;  /* largest bf16 M that AUTO sends to SKINNY at these
+                            weight sizes: 32 (up projection); 128 (down
+                            projection, weights above 32 MB) or 64 (smaller)  */
   int64_t launches;      /* kernel launches one call enqueues                   */
   int64_t cluster;       /* CTAs per thread-block cluster of the main kernel
                             (1: none; 2-8: the skinny kernel's split-K

@@ -404,9 +404,7 @@ def down_plan(M, d_ff, d, dtype="bf16", path="auto", num_sms=152):
     info = _lib.PlanInfo()
     dt = BF16 if dtype in ("bf16", BF16) else F32
     _lib.check(lib.swiglu_down_plan(M, d_ff, d, dt, _path_code(path), num_sms, ctypes.byref(info)))
-    return {"path": PATH_NAMES.get(info.path, info.path), "slices": info.slices,
-            "grid": info.grid, "workspace": info.workspace, "launches": info.launches,
-            "cluster": info.cluster}
+    return _plan_dict(info)
 
 
 def workspace_bytes(M, d, d_ff, dtype="bf16", path="auto"):
@@ -423,6 +421,10 @@ def plan(M, d, d_ff, dtype="bf16", path="auto", num_sms=152):
     info = _lib.PlanInfo()
     dt = BF16 if dtype in ("bf16", BF16) else F32
     _lib.check(lib.swiglu_plan(M, d, d_ff, dt, _path_code(path), num_sms, ctypes.byref(info)))
+    return _plan_dict(info)
+
+
+def _plan_dict(info):
     return {"path": PATH_NAMES.get(info.path, info.path), "slices": info.slices,
             "grid": info.grid, "row_chunk": info.row_chunk,
             "workspace": info.workspace, "skinny_max_m": info.skinny_max_m,

@@ -103,6 +103,9 @@ struct SkinnyPlan {
   size_t part_bytes;       // partial sums
 };
 constexpr int kSkinnyMaxN = 256;
+// Weights up to this size (bytes of the matrices one call streams) run the
+// skinny kernel in cluster mode, larger ones in stream-K mode.
+constexpr int64_t kSkinnyClusterMaxWeightBytes = (int64_t)32 << 20;
 // K: shared dimension; n_out: output columns; plain: down-projection mode.
 // cluster_caps[lg]: thread-block clusters of 2^lg CTAs of the skinny kernel
 // that fit on the device at once (lg = 1..3), or null (an estimate from num_sms).

@@ -263,8 +263,14 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 // and up to M = 64 for the down projection, whose few output tiles leave the
 // tile kernel short of parallelism (d = 4096: 40.6 vs 42.1 us at M = 64,
 // 49.8 vs 42.4 at 96; d = 896: 21.7 vs 27.3 us at M = 64).
+// Largest bf16 M that AUTO sends to the skinny kernel, by operation and by
+// whether the weights stream in stream-K mode (above 32 MB) or in cluster
+// mode (the skinny kernel's two modes).
 constexpr int64_t kSkinnyMaxM = 32;
-constexpr int64_t kSkinnyMaxMDown = 64;
+constexpr int64_t kSkinnyMaxMSmall = 64;
+constexpr int64_t kSkinnyMaxMDown = 128;
+constexpr int64_t kSkinnyMaxMDownSmall = 256;
+
 // Grid-dimension limits of the SIMT path (gridDim.y/z are 16-bit).
 constexpr int64_t kMaxGridYZ = kSimtMaxGridYZ;
 
@@ -281,6 +287,19 @@ uint64_t wait_timeout_ns() {
 
 // The two operations the library serves.
 enum Op { kOpUp = 0, kOpDown = 1 };
+
+// The measured crossovers (both paths forced, calls back to back, residual
+// included).  Stream-K mode: up projection 32 at d = 4096 and 8192 (d =
+// 4096: 39.4 vs 40.2 us at M = 32, 42.8 vs 40.4 at 48); down projection 128
+// (d = 4096: 44.6 vs 48.9 us at M = 128, 58.3 vs 49.4 at 192; d = 8192:
+// 94.9 vs 109 at 128).  Cluster mode, d = 896: up projection 64 (10.0 vs
+// 10.4 us at M = 64, 11.7 vs 10.5 at 96); down projection all M the kernel
+// serves (13.9 vs 27.3 us at M = 256).  FP8 calls measure alike.
+int64_t skinny_max_m(int op, int64_t K, int64_t n_out) {
+  const bool small = (op == kOpDown ? 1 : 2) * K * n_out * 2 <= kSkinnyClusterMaxWeightBytes;
+  if (op == kOpDown) return small ? kSkinnyMaxMDownSmall : kSkinnyMaxMDown;
+  return small ? kSkinnyMaxMSmall : kSkinnyMaxM;
+}
 
 }  // namespace
 
@@ -313,12 +332,12 @@ Tuning read_tuning() {
 
 namespace {
 
-// Up projection, AUTO: f32 -> SIMT; bf16 M <= kSkinnyMaxM -> SKINNY; larger
+// Up projection, AUTO: f32 -> SIMT; bf16 M <= skinny_max_m -> SKINNY; larger
 // bf16 M -> TC.  d == 0 (empty sums) always goes to the SIMT path, whose
 // reduction kernel then writes h = silu(0) * 0 = 0.
-// Down projection: bf16 only, on the tensor-core paths (M <= kSkinnyMaxMDown
+// Down projection: bf16 only, on the tensor-core paths (M <= skinny_max_m
 // -> SKINNY).
-int resolve_path(int op, int64_t M, int64_t K, int dtype, int path, int* out) {
+int resolve_path(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, int* out) {
   if (path < SWIGLU_PATH_AUTO || path > SWIGLU_PATH_TC)
     return fail(SWIGLU_ERR_INVALID_ARG, "unknown path %d", path);
   if (op == kOpDown) {
@@ -329,8 +348,7 @@ int resolve_path(int op, int64_t M, int64_t K, int dtype, int path, int* out) {
   }
   if (path == SWIGLU_PATH_AUTO) {
     if (op == kOpUp && (dtype == SWIGLU_F32 || K == 0)) *out = SWIGLU_PATH_SIMT;
-    else *out = M <= (op == kOpDown ? kSkinnyMaxMDown : kSkinnyMaxM) ? SWIGLU_PATH_SKINNY
-                                                                      : SWIGLU_PATH_TC;
+    else *out = M <= skinny_max_m(op, K, n_out) ? SWIGLU_PATH_SKINNY : SWIGLU_PATH_TC;
     return SWIGLU_OK;
   }
   if (path != SWIGLU_PATH_SIMT && dtype != SWIGLU_BF16)
@@ -408,7 +426,7 @@ struct Plan {
 int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, int num_sms,
               int max_pairs, Plan* p, bool fp8 = false, const int* sk_caps = nullptr) {
   int rp = 0;
-  int st = resolve_path(op, M, K, dtype, path, &rp);
+  int st = resolve_path(op, M, K, n_out, dtype, path, &rp);
   if (st != SWIGLU_OK) return st;
   *p = Plan{};
   p->path = rp;
@@ -1005,7 +1023,7 @@ static int plan_common(int op, int64_t M, int64_t K, int64_t n_out, int dtype, i
   out->grid = p.grid;
   out->row_chunk = p.path == SWIGLU_PATH_SIMT ? p.simt.row_chunk : 0;
   out->workspace = (int64_t)p.workspace;
-  out->skinny_max_m = op == kOpDown ? kSkinnyMaxMDown : kSkinnyMaxM;
+  out->skinny_max_m = skinny_max_m(op, K, n_out);
   out->launches = p.launches;
   out->cluster = p.cluster;
   return SWIGLU_OK;

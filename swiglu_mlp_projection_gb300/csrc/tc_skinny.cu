@@ -31,10 +31,10 @@
 // Cluster mode, for small weights (at most 32 MB, e.g. d = 896, d_ff = 4864):
 // each column group is one thread-block cluster of S CTAs that split K
 // evenly, S the largest size whose clusters all run at once.  Every CTA stages its finished
-// accumulator in its own shared memory; after a cluster barrier the CTA of
-// rank 0 reads the S partial sums through distributed shared memory, adds them
-// in rank order (= k order, so the result is reproducible), applies the
-// epilogue and stores.  No global workspace, no counters, no memset: the
+// accumulator in its own shared memory; after a cluster barrier the CTAs
+// split the outputs, and each reads the S partial sums of its share through
+// distributed shared memory, adds them in rank order (= k order, so the
+// result is reproducible), applies the epilogue and stores.  No global workspace, no counters, no memset: the
 // reduction never leaves the chip, which shortens the per-call critical path
 // that dominates such small calls.
 //
@@ -540,9 +540,14 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
   }
 
   if (S) {
-    // ---------------- cluster mode: rank 0 reduces over the cluster ----------------
+    // ---------------- cluster mode: the cluster reduces ----------------
+    // The CTAs split the group's outputs (contiguous chunk ranges) and each
+    // sums its share over the S staged accumulators, so they read distributed
+    // shared memory side by side instead of one CTA reading it all (d = 896
+    // down projection, M = 16 / 64 / 96: 12.8 / 26.4 / 35.2 us with rank 0
+    // alone, 9.4 / 11.8 / 13.5 us shared).
     cluster_sync_all();   // every CTA's sums are staged
-    if (crank == 0 && warp >= 2 && !*abort_flag) {
+    if (warp >= 2 && !*abort_flag) {
       constexpr int kSubCols2 = MODE == kSwiGLU ? kCB : 2 * kCB;
       constexpr int kGroupCols = NB * kSubCols2;
       constexpr int kChunks = kGroupCols / 4;
@@ -553,7 +558,13 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
 #pragma unroll
       for (int r = 0; r < kMaxS; ++r) base[r] = r < S ? mapa_shared(local, (uint32_t)r) : 0u;
       const int total = a.M * kChunks;
-      for (int idx = et; idx < total; idx += kEpiThreads) {
+      // R CTAs share the chunks: no more than one pass of 128 threads' worth
+      // each (a call whose chunks fit one pass stays on rank 0: d = 896, up
+      // projection, M = 1 measured 7.4 us that way, 7.7 us split in two).
+      const int R = min(S, (total + kEpiThreads - 1) / kEpiThreads);
+      const int lo = crank < R ? (int)((int64_t)crank * total / R) : 0;
+      const int hi = crank < R ? (int)((int64_t)(crank + 1) * total / R) : 0;
+      for (int idx = lo + et; idx < hi; idx += kEpiThreads) {
         const int m = idx / kChunks, ch = idx - m * kChunks;
         // SwiGLU: 16 chunks per 64-column sub-block, gate rows ch*4.., up rows
         // 64 + ch*4..; plain: 32 chunks per 128-column sub-block, rows ch*4..
@@ -594,7 +605,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
       }
     }
     __syncwarp();
-    cluster_sync_all();   // peers keep their shared memory until rank 0 is done
+    cluster_sync_all();   // each CTA keeps its shared memory until all peers are done
   }
 
   tc_fence_before();
@@ -675,6 +686,27 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   p.plain = plain;
   int nb = tn.sk_nb >= 0 ? tn.sk_nb : 2;
   if (nb != 1 && nb != 2 && nb != 4) nb = 2;
+  const int64_t weight_bytes = (plain ? 1 : 2) * K * n_out * 2;
+  if (plain && tn.sk_nb < 0 && weight_bytes > kSkinnyClusterMaxWeightBytes) {
+    // The down projection's K is long and its output narrow, so each column
+    // group collects many partial sums (stream-K mode), and the CTA that
+    // completes a group adds them all while the call's other CTAs are already
+    // done.  Past
+    // about 256 KB of partials per group (with 256-column groups: slots x
+    // 256 columns x M rows x 4 B), 128-column groups finish first, although
+    // they stream the weights in shorter runs.  Measured, residual included:
+    // d = 4096: 24.5 vs 26.7 us at M = 16 (180 KB), 30.4 vs 29.0 at 32
+    // (360 KB), 43.5 vs 33.9 at 64; d = 8192: 79.2 vs 81.1 at M = 32
+    // (196 KB), 90.2 vs 85.5 at 64.  FP8 weights stream in half the time,
+    // so there the limit is half (FP8 d = 4096, M = 16: 20.6 vs 19.3 us).
+    const int64_t n_kb2 = (K + kBK - 1) / kBK, n_cb2 = (n_out + 4 * kCB - 1) / (4 * kCB);
+    const int64_t units2 = n_cb2 * n_kb2;
+    const int64_t grid2 = units2 < num_sms ? units2 : num_sms;
+    const int64_t per2 = grid2 > 0 ? units2 / grid2 : 1;
+    const int64_t slots2 = per2 > 0 ? (n_kb2 + per2 - 1) / per2 + 1 : 1;
+    const int64_t limit = fp8 ? (int64_t)128 << 10 : (int64_t)256 << 10;
+    if (slots2 * 4 * kCB * 4 * M > limit) nb = 1;
+  }
   while (nb > 1 && nb * n > 256) nb /= 2;
   p.nb = nb;
   p.l2_promo = tn.sk_promo >= 0 ? tn.sk_promo : 128;
@@ -716,8 +748,7 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
       break;
     }
   }
-  const int64_t weight_bytes = (plain ? 1 : 2) * K * n_out * 2;
-  p.cluster = (S >= 2 && weight_bytes <= ((int64_t)32 << 20)) ? S : 0;
+  p.cluster = (S >= 2 && weight_bytes <= kSkinnyClusterMaxWeightBytes) ? S : 0;
   const int forced = tn.sk_cluster;
   if (forced == 0) p.cluster = 0;
   if (forced == 1 || forced == 2 || forced == 4 || forced == 8)

@@ -60,10 +60,24 @@ def test_skinny_plain_cluster_modes(cluster, monkeypatch):
         check(*shape, "skinny", seed=int(cluster) + shape[0])
 
 
-@pytest.mark.parametrize("M", [1, 4, 16])
+@pytest.mark.parametrize("M", [1, 4, 16, 48])
 def test_decode_shape_full(M):
-    # d_ff=14336 -> d=4096
+    # d_ff=14336 -> d=4096; M = 48 takes 128-column groups (large partials)
     check(M, 14336, 4096, "auto", seed=M)
+
+
+@pytest.mark.parametrize("M", [1, 96, 256])
+def test_small_model_full(M):
+    # d_ff = 4864 -> d = 896 (8.7 MB of weights): AUTO serves every M up to
+    # 256 on the skinny kernel's cluster mode
+    assert swg.down_plan(M, 4864, 896)["path"] == "skinny"
+    check(M, 4864, 896, "auto", seed=M + 5)
+
+
+def test_skinny_up_to_128_rows_sampled():
+    # AUTO serves M = 128 on the skinny kernel at d = 4096 (128-column groups)
+    assert swg.down_plan(128, 14336, 4096)["path"] == "skinny"
+    check(128, 14336, 4096, "auto", seed=128, rows=np.array([0, 1, 63, 127]))
 
 
 def test_prefill_shape_sampled_rows():

@@ -187,6 +187,6 @@ def test_fp8_down_kernel_modes(env, path, shape, monkeypatch):
 
 def test_fp8_down_full_size_sampled():
     # d = 4096, d_ff = 14336 at decode and prefill sizes, sampled rows
-    for M, rows in ((16, [0, 15]), (4096, [0, 255, 4095])):
+    for M, rows in ((16, [0, 15]), (128, [0, 127]), (4096, [0, 255, 4095])):
         down_check(M, 14336, 4096, "auto", seed=M, rows=rows)
     swg.check_device_status()
