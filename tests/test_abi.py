@@ -93,6 +93,45 @@ def test_plan_reports_cluster_size(cuda_lib):
     assert swg.plan(1, 512, 2048, "f32", "auto", 152)["cluster"] == 1
 
 
+def test_dispatch_rule(cuda_lib):
+    # measured thresholds, weights above 32 MB (stream-K mode): skinny up to
+    # M = 32 (up) and 128 (down); smaller weights (cluster mode): 64 (up) and
+    # every M the skinny kernel serves (down)
+    for M, path in [(1, "skinny"), (16, "skinny"), (32, "skinny"), (33, "tc"), (4096, "tc")]:
+        assert swg.plan(M, 4096, 14336, "bf16", "auto", 152)["path"] == path
+    for M, path in [(1, "skinny"), (64, "skinny"), (65, "tc"), (512, "tc")]:
+        assert swg.plan(M, 896, 4864, "bf16", "auto", 152)["path"] == path
+    for M, path in [(1, "skinny"), (64, "skinny"), (128, "skinny"), (129, "tc"), (4096, "tc")]:
+        assert swg.down_plan(M, 14336, 4096, "bf16", "auto", 152)["path"] == path
+    for M, path in [(1, "skinny"), (256, "skinny"), (257, "tc")]:
+        assert swg.down_plan(M, 4864, 896, "bf16", "auto", 152)["path"] == path
+    assert swg.plan(1, 4096, 14336, "bf16", "auto", 152)["skinny_max_m"] == 32
+    assert swg.plan(1, 896, 4864, "bf16", "auto", 152)["skinny_max_m"] == 64
+    assert swg.down_plan(1, 14336, 4096, "bf16", "auto", 152)["skinny_max_m"] == 128
+    assert swg.down_plan(1, 4864, 896, "bf16", "auto", 152)["skinny_max_m"] == 256
+    assert swg.plan(1, 512, 2048, "f32", "auto", 152)["path"] == "simt"
+    assert swg.plan(3, 0, 64, "bf16", "auto", 152)["path"] == "simt"
+    with pytest.raises(swg.SwiGLUError):
+        swg.plan(257, 64, 64, "bf16", "skinny", 152)
+    with pytest.raises(swg.SwiGLUError):
+        swg.plan(4, 64, 64, "f32", "tc", 152)
+
+
+def test_down_projection_column_groups(cuda_lib, monkeypatch):
+    # 256-column groups (11 partial slots at d = 4096) until their partial
+    # sums pass 256 KB per group, then 128-column groups (6 slots)
+    assert swg.down_plan(16, 14336, 4096, "bf16", "skinny", 152)["slices"] == 11
+    assert swg.down_plan(64, 14336, 4096, "bf16", "skinny", 152)["slices"] == 6
+    assert swg.down_plan(32, 29568, 8192, "bf16", "skinny", 152)["slices"] == 6
+    assert swg.down_plan(64, 29568, 8192, "bf16", "skinny", 152)["slices"] == 4
+    # small weights stay in cluster mode; the up projection keeps its groups
+    assert swg.down_plan(256, 4864, 896, "bf16", "skinny", 152)["cluster"] == 8
+    assert swg.plan(32, 4096, 14336, "bf16", "skinny", 152)["slices"] == 3
+    # SWIGLU_SK_NB overrides the rule
+    monkeypatch.setenv("SWIGLU_SK_NB", "2")
+    assert swg.down_plan(64, 14336, 4096, "bf16", "skinny", 152)["slices"] == 11
+
+
 def test_packed_weight_bytes(cuda_lib):
     # 64-column blocks of gate and up alternate; d_ff is padded to 64
     assert swg.packed_weight_bytes(4096, 14336, "bf16") == 4096 * 2 * 14336 * 2

@@ -141,30 +141,6 @@ def test_cluster_mode_selection():
     assert swg.workspace_bytes(16, 4096, 14336, "bf16", "auto") > 0
 
 
-def test_dispatch_rule():
-    # measured thresholds, weights above 32 MB (stream-K mode): skinny up to
-    # M = 32 (up) and 128 (down); smaller weights (cluster mode): 64 (up) and
-    # every M the skinny kernel serves (down)
-    for M, path in [(1, "skinny"), (16, "skinny"), (32, "skinny"), (33, "tc"), (4096, "tc")]:
-        assert swg.plan(M, 4096, 14336, "bf16", "auto", 152)["path"] == path
-    for M, path in [(1, "skinny"), (64, "skinny"), (65, "tc"), (512, "tc")]:
-        assert swg.plan(M, 896, 4864, "bf16", "auto", 152)["path"] == path
-    for M, path in [(1, "skinny"), (64, "skinny"), (128, "skinny"), (129, "tc"), (4096, "tc")]:
-        assert swg.down_plan(M, 14336, 4096, "bf16", "auto", 152)["path"] == path
-    for M, path in [(1, "skinny"), (256, "skinny"), (257, "tc")]:
-        assert swg.down_plan(M, 4864, 896, "bf16", "auto", 152)["path"] == path
-    assert swg.plan(1, 4096, 14336, "bf16", "auto", 152)["skinny_max_m"] == 32
-    assert swg.plan(1, 896, 4864, "bf16", "auto", 152)["skinny_max_m"] == 64
-    assert swg.down_plan(1, 14336, 4096, "bf16", "auto", 152)["skinny_max_m"] == 128
-    assert swg.down_plan(1, 4864, 896, "bf16", "auto", 152)["skinny_max_m"] == 256
-    assert swg.plan(1, 512, 2048, "f32", "auto", 152)["path"] == "simt"
-    assert swg.plan(3, 0, 64, "bf16", "auto", 152)["path"] == "simt"
-    with pytest.raises(swg.SwiGLUError):
-        swg.plan(257, 64, 64, "bf16", "skinny", 152)
-    with pytest.raises(swg.SwiGLUError):
-        swg.plan(4, 64, 64, "f32", "tc", 152)
-
-
 # --------------------------------------------------------------------------
 # Invariants and edge cases
 # --------------------------------------------------------------------------
