@@ -662,10 +662,10 @@ def fp8_configs(dev, peaks, iters):
         swg.swiglu_up_fp8(x, qs[0], out=hb)
         for name, fn, by, fl in (
                 ("fp8_down_d4096", lambda i: swg.swiglu_down_fp8(hb, qds[i % 2], residual=x, out=y),
-                 d_ff * d + 4 * d + 2 * M * d_ff + 4 * M * d, workload.down_flops(M, d_ff, d)),
+                 workload.fp8_down_bytes(M, d_ff, d), workload.down_flops(M, d_ff, d)),
                 ("fp8_mlp_d4096", lambda i: (swg.swiglu_up_fp8(x, qs[i % 2], out=hb),
                                              swg.swiglu_down_fp8(hb, qds[i % 2], residual=x, out=y)),
-                 workload.fp8_bytes(M, d, d_ff) + d_ff * d + 4 * d + 2 * M * d_ff + 4 * M * d,
+                 workload.fp8_bytes(M, d, d_ff) + workload.fp8_down_bytes(M, d_ff, d),
                  workload.flops(M, d, d_ff) + workload.down_flops(M, d_ff, d))):
             for i in range(3):
                 fn(i)

@@ -45,6 +45,13 @@ def down_bytes(M, d_ff, d, dtype, residual=True):
     return e * (d_ff * d + M * d_ff + M * d * (2 if residual else 1))
 
 
+def fp8_down_bytes(M, d_ff, d, residual=True):
+    """Bytes an FP8 down projection must move at least: W_down's e4m3 codes
+    and f32 column scales, h (bf16) read once, the residual (bf16) read once,
+    y (bf16) written once."""
+    return d_ff * d + 4 * d + 2 * M * d_ff + 2 * M * d * (2 if residual else 1)
+
+
 def arithmetic_intensity(M, d, d_ff, dtype):
     return flops(M, d, d_ff) / algorithmic_bytes(M, d, d_ff, dtype)
 

@@ -81,3 +81,12 @@ def test_config_work_counts():
     assert workload.algorithmic_bytes(16, 4096, 14336, "bf16") == 235_470_848
     assert workload.algorithmic_bytes(1, 512, 2048, "f32") == 8_398_848
     assert workload.algorithmic_bytes(0, 4096, 14336, "bf16") == 234_881_024
+
+
+def test_down_projection_work_counts():
+    # d = 4096, d_ff = 14336, M = 16: W_down 14336 x 4096 (bf16: 2 B, e4m3:
+    # 1 B plus 4 B per column scale), h 16 x 14336, residual and y 16 x 4096
+    assert workload.down_flops(16, 14336, 4096) == 1_879_048_192
+    assert workload.down_bytes(16, 14336, 4096, "bf16") == 118_161_408
+    assert workload.fp8_down_bytes(16, 14336, 4096) == 59_457_536
+    assert workload.fp8_down_bytes(16, 14336, 4096, residual=False) == 59_326_464
