@@ -144,6 +144,31 @@ __device__ __forceinline__ void fp8_scale(float4& g, float4& u, const SkArgs& a,
   u.x *= sxm * su.x; u.y *= sxm * su.y; u.z *= sxm * su.z; u.w *= sxm * su.w;
 }
 
+// Output columns col..col+3 of row m from their finished sums g (and u):
+// FP8 sums scaled first; then silu(g) * u (SwiGLU) or g + residual (plain);
+// stored as bf16.
+template <int MODE, bool FP8>
+__device__ __forceinline__ void store_chunk(const SkArgs& a, float4 g, float4 u, int m,
+                                            int64_t col) {
+  const int64_t o = (int64_t)m * a.n_out + col;
+  uint2 ov;
+  if constexpr (MODE == kSwiGLU) {
+    if constexpr (FP8) fp8_scale(g, u, a, m, col);
+    ov.x = pack_bf16x2(silu_fast(g.x) * u.x, silu_fast(g.y) * u.y);
+    ov.y = pack_bf16x2(silu_fast(g.z) * u.z, silu_fast(g.w) * u.w);
+  } else {
+    if constexpr (FP8) fp8_scale1(g, a, m, col);
+    if (a.resid) {
+      const uint2 rv = *reinterpret_cast<const uint2*>(a.resid + o);
+      g.x += bf16_lo(rv.x); g.y += bf16_hi(rv.x);
+      g.z += bf16_lo(rv.y); g.w += bf16_hi(rv.y);
+    }
+    ov.x = pack_bf16x2(g.x, g.y);
+    ov.y = pack_bf16x2(g.z, g.w);
+  }
+  *reinterpret_cast<uint2*>(a.out + o) = ov;
+}
+
 __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, unsigned* status,
                                            uint64_t timeout_ns) {
   int never = 0;
@@ -506,24 +531,8 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             if (idx >= total) continue;
             const int m = idx / kChunks, ch = idx - m * kChunks;
             const int64_t col = cg * kGroupCols + ch * 4;
-            if (col >= a.n_out) continue;   // n_out is a multiple of 8: a chunk is all in or out
-            const int64_t o = (int64_t)m * a.n_out + col;
-            uint2 ov;
-            if constexpr (MODE == kSwiGLU) {
-              if constexpr (FP8) fp8_scale(g[i], u[i], a, m, col);
-              ov.x = pack_bf16x2(silu_fast(g[i].x) * u[i].x, silu_fast(g[i].y) * u[i].y);
-              ov.y = pack_bf16x2(silu_fast(g[i].z) * u[i].z, silu_fast(g[i].w) * u[i].w);
-            } else {
-              if constexpr (FP8) fp8_scale1(g[i], a, m, col);
-              if (a.resid) {
-                const uint2 rv = *reinterpret_cast<const uint2*>(a.resid + o);
-                g[i].x += bf16_lo(rv.x); g[i].y += bf16_hi(rv.x);
-                g[i].z += bf16_lo(rv.y); g[i].w += bf16_hi(rv.y);
-              }
-              ov.x = pack_bf16x2(g[i].x, g[i].y);
-              ov.y = pack_bf16x2(g[i].z, g[i].w);
-            }
-            *reinterpret_cast<uint2*>(a.out + o) = ov;
+            // n_out is a multiple of 8: a chunk is all in or all out
+            if (col < a.n_out) store_chunk<MODE, FP8>(a, g[i], u[i], m, col);
           }
         }
         if (et == 0) a.counters[cg] = 0u;   // ready for the next call
@@ -584,24 +593,7 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
           }
         }
         const int64_t col = cgroup * kGroupCols + ch * 4;
-        if (col >= a.n_out) continue;   // n_out is a multiple of 8
-        const int64_t o = (int64_t)m * a.n_out + col;
-        uint2 ov;
-        if constexpr (MODE == kSwiGLU) {
-          if constexpr (FP8) fp8_scale(g, u, a, m, col);
-          ov.x = pack_bf16x2(silu_fast(g.x) * u.x, silu_fast(g.y) * u.y);
-          ov.y = pack_bf16x2(silu_fast(g.z) * u.z, silu_fast(g.w) * u.w);
-        } else {
-          if constexpr (FP8) fp8_scale1(g, a, m, col);
-          if (a.resid) {
-            const uint2 rv = *reinterpret_cast<const uint2*>(a.resid + o);
-            g.x += bf16_lo(rv.x); g.y += bf16_hi(rv.x);
-            g.z += bf16_lo(rv.y); g.w += bf16_hi(rv.y);
-          }
-          ov.x = pack_bf16x2(g.x, g.y);
-          ov.y = pack_bf16x2(g.z, g.w);
-        }
-        *reinterpret_cast<uint2*>(a.out + o) = ov;
+        if (col < a.n_out) store_chunk<MODE, FP8>(a, g, u, m, col);   // n_out: a multiple of 8
       }
     }
     __syncwarp();
