@@ -692,7 +692,8 @@ def fp8_configs(dev, peaks, iters):
 
 def down_and_mlp(dev, peaks, l2, iters):
     """The down projection y = h.W_down + r and the two-kernel MLP at the
-    decode and prefill shapes of d=4096, d_ff=14336 (back to back)."""
+    decode and prefill shapes of d=4096, d_ff=14336 (back to back); the down
+    projection also at M = 64 and 128, which its skinny path serves."""
     import torch
     import swiglu_mlp_projection_gb300 as swg
     from swiglu_mlp_projection_gb300 import inputs, workload
@@ -717,7 +718,7 @@ def down_and_mlp(dev, peaks, l2, iters):
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) / iters
 
-    for M in (1, 16, 4096):
+    for M in (1, 16, 64, 128, 4096):
         h = inputs.make_inputs(M, d_ff, 8, "bf16", seed=2, x_only=True)[0].to(dev)
         x = inputs.make_inputs(M, d, 8, "bf16", seed=3, x_only=True)[0].to(dev)
         y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
@@ -728,12 +729,15 @@ def down_and_mlp(dev, peaks, l2, iters):
         e = {"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
              "TFLOP/s": round(fl / ms / 1e9, 2),
              "path": swg.down_plan(M, d_ff, d, "bf16", "auto")["path"]}
-        if M <= 16:
+        if e["path"] == "skinny":   # M FLOP per weight byte: below the ridge, HBM-bound
             e["frac_hbm"] = round(by / ms / 1e6 / peaks["hbm_gbs"], 4)
         else:
             e["frac_bf16"] = round(fl / ms / 1e9 / peaks["bf16_tflops"], 4)
             e["frac_bf16_sustained"] = round(fl / ms / 1e9 / peaks["bf16_tflops_sustained"], 4)
         out["down_d4096/M=%d" % M] = e
+        if M not in (1, 16, 4096):
+            del h, x, y, hb
+            continue
         ms = timed(lambda i: swg.swiglu_mlp(x, wgs[i % n_copies][0], wgs[i % n_copies][1],
                                              wds[i % n_copies], residual=x, h=hb, out=y))
         by = workload.algorithmic_bytes(M, d, d_ff, "bf16") + workload.down_bytes(M, d_ff, d, "bf16")
