@@ -23,7 +23,7 @@
  *   (tolerance scaled by |a|.|b|), which is why this oracle also returns the
  *   first-order sensitivity s of each output to accumulation error.
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - SiLU(z) = z * sigma(z) = z / (1 + exp(-z))  (Swish with beta = 1).
  *   - SiLU applies to x.W_gate; x.W_up enters linearly.
  *   - g and u are never rounded; only h is rounded (round-to-nearest-even)
