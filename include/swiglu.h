@@ -57,7 +57,7 @@ typedef enum { SWIGLU_F32 = 0, SWIGLU_BF16 = 1 } swiglu_dtype;
 typedef enum {
   SWIGLU_OK = 0,
   SWIGLU_ERR_INVALID_ARG = 1,   /* null pointer, negative size, unknown dtype/path */
-  SWIGLU_ERR_UNSUPPORTED = 2,   /* valid arguments this build cannot serve      */
+  SWIGLU_ERR_UNSUPPORTED = 2,   /* valid arguments the library does not serve  */
   SWIGLU_ERR_ALIGNMENT = 3,     /* pointer or row stride not 16-byte aligned    */
   SWIGLU_ERR_OOM = 4,           /* workspace allocation failed                  */
   SWIGLU_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed            */
