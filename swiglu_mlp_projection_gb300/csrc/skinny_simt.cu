@@ -23,6 +23,7 @@
 // the slice target scaled to this GPU's SM count.  This path serves f32 (all
 // M) and is the CUDA-core reference path for bf16; the tensor-core paths
 // serve bf16 by default.
+#include <atomic>
 #include <stdlib.h>
 
 #include "common.cuh"
@@ -216,16 +217,16 @@ cudaError_t launch_one(const void* x, const void* wg, const void* wu, float* par
   auto kern = simt_partial_kernel<BF16, RC>;
   // The opt-in shared-memory limit is a per-function, per-device attribute:
   // set it once per device to the largest size this instantiation can use.
-  static int configured[64] = {0};
+  static std::atomic<int> configured[64];   // zero: not yet set on that device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !configured[dev]) {
+  if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     const size_t most = (size_t)RC * kMaxKPerSlice * sizeof(float) > red_bytes
                             ? (size_t)RC * kMaxKPerSlice * sizeof(float) : red_bytes;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
     if (e != cudaSuccess) return e;
-    if (dev < 64) configured[dev] = 1;
+    if (dev < 64) configured[dev].store(1, std::memory_order_release);
   }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -53,6 +53,7 @@
 // MMAs (warp 1 owns the TMEM allocation), warps 2-5 drain the accumulator.
 // Every mbarrier wait is bounded; on timeout the CTA raises the device error
 // word, stops, lets its in-flight copies and MMAs finish, frees TMEM and exits.
+#include <atomic>
 #include <stdlib.h>
 
 #include "common.cuh"
@@ -613,15 +614,15 @@ cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mg, const CUtenso
                      const SkArgs& a, cudaStream_t st) {
   using C = SkCfg<N, NB>;
   auto kern = skinny_tc_kernel<N, NB, MODE, FP8>;
-  static int configured[64] = {0};
+  static std::atomic<int> configured[64];   // zero: not yet set on that device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !configured[dev]) {
+  if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    if (dev < 64) configured[dev] = 1;
+    if (dev < 64) configured[dev].store(1, std::memory_order_release);
   }
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

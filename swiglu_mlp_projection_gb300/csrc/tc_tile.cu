@@ -35,6 +35,7 @@
 // section 1.6, kernels #10 and #11): the 256 accumulator columns are 256
 // adjacent output columns, and the epilogue adds the residual and stores
 // them in two 128-column passes.
+#include <atomic>
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -728,15 +729,15 @@ cudaError_t launch_mode(const CUtensorMap& mx, const CUtensorMap& mg, const CUte
                         const CUtensorMap& mh, const TileArgs& a, int grid, cudaStream_t st) {
   using C = TileCfg<PAIR>;
   auto kern = tile_tc_kernel<MODE, PAIR, FP8>;
-  static int configured[64] = {0};
+  static std::atomic<int> configured[64];   // zero: not yet set on that device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !configured[dev]) {
+  if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    if (dev < 64) configured[dev] = 1;
+    if (dev < 64) configured[dev].store(1, std::memory_order_release);
   }
   // The grid is the plan's: the stream-K shares assume exactly this many
   // units (the plan already caps pairs at what can run at once).
