@@ -239,3 +239,22 @@ def test_floor_factor_values():
     assert floor_factor("bf16", 4096) == pytest.approx(8 * 64 * 2 ** -24 / 2e-2)
     assert floor_factor("f32", 512) == pytest.approx(8 * 512 ** 0.5 * 2 ** -24 / 1e-5)
     assert TOL == {"f32": 1e-5, "bf16": 2e-2}
+
+
+def test_no_cpu_fallback_for_host_tensors(cuda_lib):
+    # Every compute entry point of the binding refuses host tensors instead of
+    # computing on the CPU: the only compute path is the CUDA library.
+    import torch
+    x = torch.randn(2, 64).to(torch.bfloat16)
+    w = torch.randn(64, 64).to(torch.bfloat16)
+    calls = {
+        "swiglu_up": lambda: swg.swiglu_up(x, w, w),
+        "swiglu_down": lambda: swg.swiglu_down(x, w),
+        "swiglu_mlp": lambda: swg.swiglu_mlp(x, w, w, w),
+        "pack_weights": lambda: swg.pack_weights(w, w),
+        "quantize_weights_fp8": lambda: swg.quantize_weights_fp8(w, w),
+        "quantize_weight_fp8": lambda: swg.quantize_weight_fp8(w),
+    }
+    for name, call in calls.items():
+        with pytest.raises(ValueError, match="CUDA"):
+            call()
