@@ -38,7 +38,7 @@ constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kUnroll = 4;          // k rows in flight per thread per matrix
 constexpr int kMaxKPerSlice = 1024; // bounds the staged slice of x
-constexpr int kMinKPerSlice = 64;   // "never fewer than 64 indices per slice"
+constexpr int kMinKPerSlice = 64;   // minimum slice depth ("Ou part le temps d'un token", "Un kernel pour les matrices etroites")
 constexpr int kCtasPerSmTarget = 4;
 
 template <bool BF16>

@@ -54,3 +54,25 @@ def compare(h_gpu, h64, sens, dtype, d):
         "mismatch_pct": float(100.0 * np.mean(rel_all > 0.01)) if h64.size else 0.0,
         "finite": finite,
     }
+
+
+def tile_rows(M, seed=0, per_block=2):
+    """Rows that reach every output tile of an M-row call: ``per_block`` rows
+    from each 128-row block (one CTA's rows in both the single-CTA and the
+    CTA-pair tiles), taken from different 32-row quarters (the four epilogue
+    warps' rows), the quarters rotating from block to block, plus the first and
+    the last row.  Every column of these rows is compared, so every column tile
+    of every row block is checked, whichever CTA, TMEM buffer or wave
+    computed it.  Rows of h are independent, so the check of a row is exact.
+    """
+    rng = np.random.default_rng(seed)
+    rows = {0, M - 1}
+    for b in range((M + 127) // 128):
+        for q in range(per_block):
+            quarter = (b + 2 * q) % 4
+            lo = b * 128 + 32 * quarter
+            if lo >= M:
+                lo = b * 128
+            hi = min(lo + 32, M)
+            rows.add(int(rng.integers(lo, hi)))
+    return np.array(sorted(rows), dtype=np.int64)

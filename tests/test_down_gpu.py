@@ -8,7 +8,7 @@ import torch
 import oracle
 import swiglu_mlp_projection_gb300 as swg
 from swiglu_mlp_projection_gb300 import inputs
-from tests.parity import compare
+from tests.parity import compare, tile_rows
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
@@ -80,9 +80,10 @@ def test_skinny_up_to_128_rows_sampled():
     check(128, 14336, 4096, "auto", seed=128, rows=np.array([0, 1, 63, 127]))
 
 
-def test_prefill_shape_sampled_rows():
-    rows = np.array([0, 1, 127, 128, 2047, 4095])
-    check(4096, 14336, 4096, "auto", seed=9, rows=rows)
+def test_prefill_shape_tile_rows():
+    # M = 4096 (16 row blocks of CTA-pair tiles): every column of 2 rows of
+    # every 128-row block, so every 256-column output tile is reached
+    check(4096, 14336, 4096, "auto", seed=9, rows=tile_rows(4096, seed=9))
 
 
 def test_in_place_residual_and_paths_agree():

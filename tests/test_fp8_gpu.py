@@ -10,7 +10,7 @@ import torch
 import oracle
 import swiglu_mlp_projection_gb300 as swg
 from swiglu_mlp_projection_gb300 import _lib, inputs
-from tests.parity import compare
+from tests.parity import compare, tile_rows
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
@@ -145,6 +145,30 @@ def test_fp8_full_size_sampled(M, d, d_ff):
     swg.check_device_status()
 
 
+def test_fp8_prefill_tile_rows():
+    # M = 4096, d = 4096, d_ff = 14336 on the FP8 tile kernel (CTA pairs):
+    # every column of 2 rows of every 128-row block, against the oracle's
+    # quantization and fp64 definition on the dequantized operands
+    M, d, d_ff = 4096, 4096, 14336
+    x, wg, wu = make(M, d, d_ff, seed=11)
+    w = swg.quantize_weights_fp8(wg.to(DEV), wu.to(DEV))
+    h = swg.swiglu_up_fp8(x.to(DEV), w)
+    torch.cuda.synchronize()
+    rows = tile_rows(M, seed=11)
+    cg, sg = oracle.quantize_cols_e4m3(RAW(wg))
+    cu, su = oracle.quantize_cols_e4m3(RAW(wu))
+    assert np.array_equal(w.w8_gate.cpu().numpy(), cg)
+    assert np.array_equal(w.w8_up.cpu().numpy(), cu)
+    x8, sx = oracle.quantize_rows_e4m3(RAW(x)[rows].copy())
+    xdq = oracle.dequant_rows_e4m3(x8, sx)
+    gdq = np.ascontiguousarray(oracle.dequant_rows_e4m3(cg, sg).T)
+    udq = np.ascontiguousarray(oracle.dequant_rows_e4m3(cu, su).T)
+    h64, _, sens = oracle.swiglu_up(xdq, gdq, udq, oracle.F64, want_rounded=False)
+    res = compare(to64(h)[rows], h64, sens, "bf16", d)
+    assert res["ok"], res
+    swg.check_device_status()
+
+
 # ---------------------------------------------------------------------------
 # The FP8 down projection
 # ---------------------------------------------------------------------------
@@ -185,8 +209,9 @@ def test_fp8_down_kernel_modes(env, path, shape, monkeypatch):
     down_check(*shape, path, seed=9)
 
 
-def test_fp8_down_full_size_sampled():
-    # d = 4096, d_ff = 14336 at decode and prefill sizes, sampled rows
-    for M, rows in ((16, [0, 15]), (128, [0, 127]), (4096, [0, 255, 4095])):
+def test_fp8_down_full_size_rows():
+    # d = 4096, d_ff = 14336 at decode and prefill sizes: every column of the
+    # chosen rows (at M = 4096, 2 rows of every 128-row block)
+    for M, rows in ((16, np.arange(16)), (128, [0, 63, 127]), (4096, tile_rows(4096, seed=4))):
         down_check(M, 14336, 4096, "auto", seed=M, rows=rows)
     swg.check_device_status()

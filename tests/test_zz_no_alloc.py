@@ -4,10 +4,11 @@ allocation, a process whose device memory another allocator has reserved, a
 latency-critical loop that must not block on cudaMalloc/cudaFree).  It uses
 a fixed scratch array held by the library instead of a workspace.
 
-The test calls it through the C ABI and checks it against the regular
-swiglu_up entry point, within the tolerance the parity tests use, on two
-calls in a row with different shapes and inputs (the scratch keeps the first
-call's contents when the second one runs).  This file sorts last so that a
+The test calls it through the C ABI and checks every output against the CPU
+oracle's fp64 result, within the tolerance the parity tests use, and also
+against the regular swiglu_up entry point, on two calls in a row with
+different shapes and inputs (the scratch keeps the first call's contents when
+the second one runs).  This file sorts last so that a
 run stopping at the first failure has run every other test before it.
 """
 import numpy as np
@@ -53,9 +54,12 @@ def test_noalloc_matches_swiglu_up_on_two_calls(cuda_lib, dtype):
         assert st == 0, cuda_lib.swiglu_last_error_string()
         torch.cuda.synchronize()
         raw = inputs.raw_bits
-        _, _, sens = oracle.swiglu_up(raw(x), raw(wg), raw(wu), od)
-        res = compare(_to64(out), _to64(ref), sens, dtype, d)
+        h64, _, sens = oracle.swiglu_up(raw(x), raw(wg), raw(wu), od)
+        res = compare(_to64(out), h64, sens, dtype, d)
         assert res["ok"], (M, d, d_ff, dtype, res)
+        # and within the same tolerance of the regular entry point
+        res = compare(_to64(out), _to64(ref), sens, dtype, d)
+        assert res["ok"], (M, d, d_ff, dtype, "vs swiglu_up", res)
     swg.check_device_status()
 
 
@@ -64,7 +68,10 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(cuda_lib):
     M, d, d_ff = 256, 4096, 14336          # needs far more than the fixed scratch
     x = torch.zeros(M, d, dtype=torch.bfloat16, device=dev)
     w = torch.zeros(d, d_ff, dtype=torch.bfloat16, device=dev)
-    h = torch.empty(M, d_ff, dtype=torch.bfloat16, device=dev)
+    h = torch.full((M, d_ff), 3.0, dtype=torch.bfloat16, device=dev)
     st = _noalloc(cuda_lib, x, w, w, h, _lib.BF16)
     assert st == 8
     assert b"scratch" in cuda_lib.swiglu_last_error_string()
+    # a rejected call enqueues nothing: h keeps its contents
+    torch.cuda.synchronize()
+    assert bool((h == 3.0).all())
