@@ -84,6 +84,12 @@ typedef enum {
  * (stream-K), need a workspace for their partial sums; this entry point takes it
  * from a library-owned, stream-ordered pool (cudaMallocFromPoolAsync /
  * cudaFreeAsync on `stream`), so calls on different streams never share it.
+ * The buffer is cached per stream (up to 256 streams, 256 MB of partial sums
+ * each) and reused by the stream's later calls; swiglu_release_stream_workspace
+ * and swiglu_release_workspaces give it back.  The first call on a device
+ * that uses arrival counters outside a CUDA-graph capture also creates a
+ * 4 MB region of zeroed counters for captured calls, and waits for `stream`
+ * once to do so.
  * Errors: SWIGLU_ERR_INVALID_ARG, _ALIGNMENT, _ARCH, _OOM, _CUDA.
  */
 SWIGLU_API int swiglu_up(const void* x, const void* w_gate, const void* w_up, void* h,
@@ -117,8 +123,10 @@ SWIGLU_API int swiglu_up_ex(const void* x, const void* w_gate, const void* w_up,
  *
  * Sums in f32 over k, the residual added to the f32 sum, one rounding to the
  * output type.  bf16 only (f32 returns SWIGLU_ERR_UNSUPPORTED), on the
- * tensor-core paths: M <= 16 -> split-K skinny kernel, larger M -> tile
- * kernel (SWIGLU_PATH_SIMT is rejected).  d_ff == 0 gives y = residual (or 0).
+ * tensor-core paths: M up to the skinny limit that swiglu_down_plan reports
+ * (128 for weights above 32 MB, 256 for smaller ones) -> split-K skinny
+ * kernel, larger M -> tile kernel (SWIGLU_PATH_SIMT is rejected).
+ * d_ff == 0 gives y = residual (or 0).
  * Workspace, streams, determinism and errors as for swiglu_up.
  */
 SWIGLU_API int swiglu_down(const void* h, const void* w_down, const void* residual, void* y,
@@ -336,6 +344,31 @@ SWIGLU_API int swiglu_down_plan(int64_t M, int64_t d_ff, int64_t d, int dtype, i
  */
 SWIGLU_API int64_t swiglu_split_k_slices(int64_t K, int64_t col_blocks,
                               int64_t target_blocks, int64_t min_k_per_slice);
+
+/*
+ * Workspace cache management (the per-stream buffers swiglu_up, swiglu_down
+ * and the FP8 entry points keep when they run without a caller workspace).
+ * The workspace serves the split-K reductions of "Ou part le temps d'un
+ * token", section "Un kernel pour les matrices etroites".
+ *
+ * swiglu_release_stream_workspace: frees the buffer cached for `stream` on
+ *   the current device, stream-ordered (cudaFreeAsync on `stream`, after the
+ *   work already enqueued there).  Call it before destroying a stream that
+ *   made calls; a later call on the stream allocates a new buffer.  NULL is
+ *   the legacy default stream.  Returns SWIGLU_OK (also when nothing was
+ *   cached) or SWIGLU_ERR_CUDA.
+ * swiglu_release_workspaces: waits for the current device to finish its
+ *   work (cudaDeviceSynchronize), frees every buffer cached on it, including
+ *   those of streams already destroyed, and returns the library pool's unused
+ *   memory to the driver.  Returns SWIGLU_OK or SWIGLU_ERR_CUDA.
+ * swiglu_cached_workspace_bytes: bytes the cache holds on the current
+ *   device (0 when no device is current).
+ * Neither release call may run while another thread enqueues calls of this
+ * library on the same stream (release_stream) or device (release).
+ */
+SWIGLU_API int swiglu_release_stream_workspace(void* stream);
+SWIGLU_API int swiglu_release_workspaces(void);
+SWIGLU_API size_t swiglu_cached_workspace_bytes(void);
 
 /* Reads and clears the device-side error word that bounded waits inside the
  * kernels set when they give up.  Synchronises the current device first.

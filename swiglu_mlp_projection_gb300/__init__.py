@@ -441,10 +441,31 @@ def check_device_status():
     _lib.check(_lib.load().swiglu_check_device_status())
 
 
+def release_stream_workspace(stream=None):
+    """Free the workspace the library caches for ``stream`` (torch's current
+    stream by default), stream-ordered; call before dropping a stream."""
+    import torch
+    dev = torch.cuda.current_device()
+    raw = stream.cuda_stream if stream is not None else _raw_stream(dev)
+    _call(dev, _lib.load().swiglu_release_stream_workspace, raw)
+
+
+def release_workspaces():
+    """Wait for the current device, then free every workspace the library
+    caches on it and trim its pool."""
+    _lib.check(_lib.load().swiglu_release_workspaces())
+
+
+def cached_workspace_bytes():
+    """Bytes of workspace the library caches on the current device."""
+    return int(_lib.load().swiglu_cached_workspace_bytes())
+
+
 def version():
     return int(_lib.load().swiglu_version())
 
 
 __all__ = ["swiglu_up", "swiglu_down", "swiglu_mlp", "workspace_bytes",
            "down_workspace_bytes", "plan", "down_plan", "split_k_slices",
-           "check_device_status", "version", "SwiGLUError", "PATHS"]
+           "check_device_status", "release_stream_workspace", "release_workspaces",
+           "cached_workspace_bytes", "version", "SwiGLUError", "PATHS"]

@@ -56,6 +56,9 @@ SIGNATURES = {
     "swiglu_plan": ([_i64, _i64, _i64, _int, _int, _int, ctypes.POINTER(PlanInfo)], _int),
     "swiglu_split_k_slices": ([_i64, _i64, _i64, _i64], _i64),
     "swiglu_check_device_status": ([], _int),
+    "swiglu_release_stream_workspace": ([_vp], _int),
+    "swiglu_release_workspaces": ([], _int),
+    "swiglu_cached_workspace_bytes": ([], _sz),
     "swiglu_selftest_wait_timeout": ([_int, _vp], _int),
     "swiglu_status_string": ([_int], ctypes.c_char_p),
     "swiglu_last_error_string": ([], ctypes.c_char_p),

@@ -33,6 +33,11 @@ struct Tuning {
   int sk_nb = -1, sk_promo = -1, sk_hint = -1, sk_prefetch_units = -1, sk_cluster = -1;
   int tile_pair = -1, tile_sk = -1, tile_sk_split = -1, tile_seq = -1;
   int simt_fused = -1;
+  // Test hook (SWIGLU_INJECT_OOM=1): every workspace the library would take
+  // from its pool or its per-stream cache fails to allocate, so the call
+  // returns SWIGLU_ERR_OOM having enqueued nothing.  Caller workspaces and
+  // calls that need none are unaffected.
+  int inject_oom = 0;
 };
 Tuning read_tuning();
 

@@ -196,6 +196,58 @@ void mark_workspaces_dirty(int dev) {
     if (e.dev == dev) e.dirty = true;
 }
 
+// Drops the cached buffer of stream `st` on `dev`: a stream-ordered free on
+// `st` itself, after the work already enqueued there.
+int release_stream_workspace(int dev, cudaStream_t st) {
+  if (st == cudaStreamPerThread) return SWIGLU_OK;   // never cached
+  unsigned long long id = 0;
+  cudaError_t e = cudaStreamGetId(st, &id);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetId");
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (size_t i = 0; i < g_stream_ws.size(); ++i) {
+    StreamWorkspace& w = g_stream_ws[i];
+    if (w.dev != dev || w.stream_id != id) continue;
+    if (w.base && (e = cudaFreeAsync(w.base, st)) != cudaSuccess)
+      return cuda_fail(e, "cudaFreeAsync(stream workspace)");
+    g_stream_ws.erase(g_stream_ws.begin() + (ptrdiff_t)i);
+    break;
+  }
+  return SWIGLU_OK;
+}
+
+// Drops every cached buffer of `dev` once the device is idle, and returns the
+// pool's unused memory to the driver.  Buffers of streams the caller has
+// destroyed are freed too: no stream handle is needed.
+int release_device_workspaces(int dev) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  cudaMemPool_t pool = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (size_t i = 0; i < g_stream_ws.size();) {
+      StreamWorkspace& w = g_stream_ws[i];
+      if (w.dev != dev) { ++i; continue; }
+      if (w.base && (e = cudaFreeAsync(w.base, cudaStreamLegacy)) != cudaSuccess)
+        return cuda_fail(e, "cudaFreeAsync(stream workspace)");
+      g_stream_ws.erase(g_stream_ws.begin() + (ptrdiff_t)i);
+    }
+    pool = g_dev[dev].pool;
+  }
+  if ((e = cudaStreamSynchronize(cudaStreamLegacy)) != cudaSuccess)
+    return cuda_fail(e, "cudaStreamSynchronize");
+  if (pool && (e = cudaMemPoolTrimTo(pool, 0)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemPoolTrimTo");
+  return SWIGLU_OK;
+}
+
+size_t cached_workspace_bytes(int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  size_t n = 0;
+  for (const auto& w : g_stream_ws)
+    if (w.dev == dev && w.base) n += kStreamCounterBytes + w.part_capacity;
+  return n;
+}
+
 // Arrival counters for calls captured into CUDA graphs.  A captured call's
 // workspace is a graph allocation whose contents are undefined on every
 // replay, so its counters would need a memset node, which costs ~5 us per
@@ -323,7 +375,8 @@ Tuning read_tuning() {
                           {"TILE_SK", &t.tile_sk},
                           {"TILE_SK_SPLIT", &t.tile_sk_split},
                           {"TILE_SEQ", &t.tile_seq},
-                          {"SIMT_FUSED", &t.simt_fused}};
+                          {"SIMT_FUSED", &t.simt_fused},
+                          {"INJECT_OOM", &t.inject_oom}};
     for (const Knob& k : knobs)
       if (strlen(k.key) == n && strncmp(k.key, name, n) == 0) *k.dst = v;
   }
@@ -418,6 +471,7 @@ struct Plan {
   int64_t launches;   // kernels one call launches
   int64_t cluster;    // CTAs per cluster of the main kernel (1 = none)
   size_t workspace;
+  bool inject_oom;    // the SWIGLU_INJECT_OOM test hook is set
 };
 
 // K: shared dimension; n_out: output columns (up: d, d_ff; down: d_ff, d).
@@ -433,6 +487,7 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
   p->cluster = 1;
   const bool plain = op == kOpDown;
   const Tuning tn = read_tuning();
+  p->inject_oom = tn.inject_oom != 0;
   if (rp == SWIGLU_PATH_SIMT) {
     p->simt = plan_simt(M, K, n_out, dtype, num_sms, tn);
     if (p->simt.slices > kMaxGridYZ || p->simt.row_chunks > kMaxGridYZ)
@@ -560,7 +615,8 @@ int run(const Call& c) {
       counters = (unsigned*)((char*)c.workspace + fp8_prefix);
       part = (float*)((char*)c.workspace + fp8_prefix + counter_bytes);
     } else {
-      if ((v = stream_workspace(dev, st, p.workspace - counter_bytes, &part, &counters)) != SWIGLU_OK)
+      if (!p.inject_oom &&
+          (v = stream_workspace(dev, st, p.workspace - counter_bytes, &part, &counters)) != SWIGLU_OK)
         return v;
       if (part) {
         counters_clean = true;
@@ -571,11 +627,14 @@ int run(const Call& c) {
         // A captured call takes clean counters from the graph-counter region
         // when it can (see GraphCounters) and allocates only the rest.
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        if (counter_bytes && cudaStreamIsCapturing(st, &cs) == cudaSuccess &&
+        if (counter_bytes && !p.inject_oom && cudaStreamIsCapturing(st, &cs) == cudaSuccess &&
             cs != cudaStreamCaptureStatusNone)
           counters = take_graph_counters(dev, counter_bytes);
         cudaGetLastError();
         const size_t own = counters ? p.workspace - counter_bytes : p.workspace;
+        if (own > 0 && p.inject_oom)
+          return fail(SWIGLU_ERR_OOM, "workspace of %zu bytes: allocation failure injected "
+                      "(SWIGLU_INJECT_OOM)", own);
         if (own > 0) {
           cudaMemPool_t pool;
           if ((v = device_pool(dev, &pool)) != SWIGLU_OK) return v;
@@ -1062,6 +1121,35 @@ int swiglu_check_device_status(void) {
                 word);
   }
   return SWIGLU_OK;
+}
+
+int swiglu_release_stream_workspace(void* stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(SWIGLU_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  int v = release_stream_workspace(dev, (cudaStream_t)stream);
+  if (v == SWIGLU_OK) t_err[0] = 0;
+  return v;
+}
+
+int swiglu_release_workspaces(void) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(SWIGLU_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  int v = release_device_workspaces(dev);
+  if (v == SWIGLU_OK) t_err[0] = 0;
+  return v;
+}
+
+size_t swiglu_cached_workspace_bytes(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return 0;
+  }
+  return cached_workspace_bytes(dev);
 }
 
 const char* swiglu_status_string(int status) {
