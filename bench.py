@@ -9,8 +9,19 @@ Algorithmic bytes per call = 2 (2 d d_ff + M d + M d_ff) (weights read once,
 x read once, h written once).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-Under torchrun each rank runs its own replica of the sweep (weak scaling, no
-collective on the data path); the max step time over ranks is reported.
+                       [--split replicas|columns]
+With --gpus N > 1 outside torchrun the script re-launches itself under
+torch.distributed.run with N local ranks.  Each rank runs its own replica of
+the sweep (weak scaling, no collective on the data path), or with
+--split columns its 64-aligned share of the d_ff columns of both weight
+matrices (strong scaling, still no collective); the max time over ranks is
+reported.
+
+Besides the GPU timings, rank 0 runs the CPU oracle on bounded samples: the
+headline cpu_baseline (all host cores and one core) and, for every timed
+up-projection configuration, the oracle on a set of rows of the same call,
+whose time is extrapolated to the whole call and whose result checks the GPU
+output of the timed call (max error, normwise error, mismatch %).
 """
 import argparse
 import json
@@ -42,7 +53,41 @@ def parse():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the secondary per-config measurements")
     ap.add_argument("--extra-iters", type=int, default=30)
+    ap.add_argument("--split", choices=["replicas", "columns"], default="replicas",
+                    help="multi-rank data path: a replica of the sweep per rank, or each "
+                         "rank's share of the d_ff columns")
+    ap.add_argument("--no-oracle", action="store_true",
+                    help="skip the CPU oracle leg (baseline timings and accuracy)")
     return ap.parse_args()
+
+
+def quantiles(xs):
+    """Median, 10th and 90th percentile of a list of times (nearest rank)."""
+    xs = sorted(xs)
+    if not xs:
+        return {"median": None, "p10": None, "p90": None}
+    pick = lambda q: xs[min(len(xs) - 1, max(0, int(round(q * (len(xs) - 1)))))]
+    return {"median": statistics.median(xs), "p10": pick(0.10), "p90": pick(0.90)}
+
+
+def bench_config():
+    """The `config` both arms print (identical, so the two lines describe the
+    same workload)."""
+    return {"workload": WORKLOAD, "weights": "N(0,1/d) bf16, seed 0",
+            "l2": "inputs larger than L2: 235 MB of weights per call, and distinct weight "
+                  "copies rotated per call"}
+
+
+def torchrun_argv(args, argv):
+    """Command that re-runs this script under torch.distributed.run with
+    args.gpus local ranks (used when --gpus N > 1 is given outside torchrun)."""
+    import socket
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            "--nproc-per-node", str(args.gpus), "--master-addr", "127.0.0.1",
+            "--master-port", str(port), os.path.abspath(__file__)] + list(argv)
 
 
 def max_over_ranks(value, world, device=None):
@@ -61,26 +106,24 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+TRAFFIC_FILE = os.path.join("profiles", "skinny_decode_traffic.json")
+
+
 def profiled_traffic():
     """Mean DRAM bytes per launch of the decode kernel from the committed ncu
-    summary, or None when the kernel sources changed since that capture."""
+    capture, or None when the kernel sources changed since that capture."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "skinny_tc_kernel_decode_sweep_d4096.md")
     try:
-        fields = {}
-        with open(path) as f:
-            for line in f:
-                if " = " in line and not line.startswith(("#", "|", " ")):
-                    k, v = line.split(" = ", 1)
-                    fields[k.strip()] = v.strip()
+        with open(os.path.join(ROOT, TRAFFIC_FILE)) as f:
+            rec = json.load(f)
         h = hashlib.sha256()
-        for rel in fields["source_files"].split():
+        for rel in rec["source_files"]:
             with open(os.path.join(ROOT, rel), "rb") as f:
                 h.update(f.read())
-        if h.hexdigest() != fields["source_sha256"]:
+        if h.hexdigest() != rec["source_sha256"]:
             return None
-        return int(fields["traffic_bytes_per_launch_mean"])
-    except (OSError, KeyError, ValueError):
+        return int(rec["traffic_bytes_per_launch_mean"])
+    except (OSError, KeyError, ValueError, TypeError):
         return None
 
 
@@ -228,13 +271,17 @@ def _oracle_inputs(cols):
     return _ORACLE_INPUTS[cols]
 
 
-def oracle_sweep(cols, reps_budget_s):
+ORACLE_COLS = 2048     # columns of the decode sweep in the oracle's timed sample
+
+
+def oracle_sweep(cols, reps_budget_s, threads=None):
     """Time the oracle on the decode sweep restricted to the first `cols`
-    columns (full K); returns (GB/s, seconds, calls, threads)."""
+    columns (full K), repeated until `reps_budget_s` seconds have been spent;
+    returns (GB/s, seconds, calls, threads)."""
     import oracle
     from swiglu_mlp_projection_gb300 import workload
     xs, wg_s, wu_s = _oracle_inputs(cols)
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     total_bytes, t_total, calls = 0, 0.0, 0
     while True:
         for M in SWEEP:
@@ -248,12 +295,18 @@ def oracle_sweep(cols, reps_budget_s):
     return total_bytes / t_total / 1e9, t_total, calls, threads
 
 
+def oracle_sample_text(cols, budget_s):
+    return ("decode sweep M in {1,2,4,8,16}, d=4096, first %d of 14336 columns (all K), "
+            "repeated for >= %.1f s" % (cols, budget_s))
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    # bounded: about 90 s of CPU work for the whole run, whatever K and W are
-    cols = 256
+    # bounded: about 90 s of CPU work for the whole run, whatever K and W are;
+    # the same sample (columns of the sweep) as our arm's cpu_baseline
+    cols = ORACLE_COLS
     budget = min(2.0, max(0.05, 90.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):
         oracle_sweep(cols, 0.0)
@@ -263,18 +316,18 @@ def run_reference(args):
         vals.append(gbs)
         times.append(t)
     value = statistics.median(vals)
-    sample = ("decode sweep M in {1,2,4,8,16}, d=4096, first %d of 14336 columns, "
-              "repeated for >= %.1f s per step" % (cols, budget))
+    sample = oracle_sample_text(cols, budget) + " per step"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * statistics.median(times), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample": sample},
+        "config": bench_config(),
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
+        "step_GB/s": {k: round(v, 3) for k, v in quantiles(vals).items()},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -287,7 +340,7 @@ def run_reference(args):
 def run_ours(args):
     import torch
     import swiglu_mlp_projection_gb300 as swg
-    from swiglu_mlp_projection_gb300 import inputs, workload
+    from swiglu_mlp_projection_gb300 import inputs, sharding, workload
 
     rank, world, local_rank = dist_env()
     if world > 1:
@@ -301,25 +354,31 @@ def run_ours(args):
     props = torch.cuda.get_device_properties(dev)
     num_sms = props.multi_processor_count
     l2 = getattr(props, "L2_cache_size", L2_BYTES) or L2_BYTES
+    oracle_leg = rank == 0 and not args.no_oracle
 
+    # this rank's columns of both weight matrices: all of them (a replica of
+    # the sweep per rank), or its 64-aligned share (--split columns)
+    c0, c1 = (0, D_FF) if args.split == "replicas" else sharding.column_range(D_FF, rank, world)
+    n_cols = c1 - c0
     # weights: enough distinct copies that no call finds the previous call's
-    # weights in L2 (each copy, 235 MB, is already larger than L2)
-    w_bytes = 2 * D * D_FF * 2
+    # weights in L2 (each copy of the full matrices, 235 MB, is already larger)
+    w_bytes = 2 * D * max(n_cols, 1) * 2
     n_copies = max(2, math.ceil(3 * l2 / w_bytes))
-    _, wg, wu = inputs.make_inputs(1, D, D_FF, "bf16", seed=0)
-    copies = [(wg.to(dev), wu.to(dev)) for _ in range(n_copies)]
+    _, wg_h, wu_h = inputs.make_inputs(1, D, D_FF, "bf16", seed=0)
+    wg_s, wu_s = wg_h[:, c0:c1].contiguous(), wu_h[:, c0:c1].contiguous()
+    copies = [(wg_s.to(dev), wu_s.to(dev)) for _ in range(n_copies)]
     # one step's activations and outputs, each as one contiguous buffer with a
     # view per call (so the end-to-end loop moves them in one copy each way)
     xs_host = {M: inputs.make_inputs(M, D, D_FF, "bf16", seed=0, x_only=True)[0] for M in SWEEP}
     x_all_host = torch.cat([xs_host[M] for M in SWEEP], 0)
     x_all = x_all_host.to(dev)
-    h_all = torch.empty(sum(SWEEP), D_FF, dtype=torch.bfloat16, device=dev)
+    h_all = torch.empty(sum(SWEEP), n_cols, dtype=torch.bfloat16, device=dev)
     offs = {M: sum(SWEEP[:i]) for i, M in enumerate(SWEEP)}
     xs = {M: x_all[offs[M]:offs[M] + M] for M in SWEEP}
     hs = {M: h_all[offs[M]:offs[M] + M] for M in SWEEP}
     stream = torch.cuda.current_stream(dev)
-    step_bytes = sum(workload.algorithmic_bytes(M, D, D_FF, "bf16") for M in SWEEP)
-    plans = {M: swg.plan(M, D, D_FF, "bf16", "auto", num_sms) for M in SWEEP}
+    step_bytes = sum(workload.algorithmic_bytes(M, D, n_cols, "bf16") for M in SWEEP)
+    plans = {M: swg.plan(M, D, n_cols, "bf16", "auto", num_sms) for M in SWEEP}
     launches_per_step = sum(p["launches"] for p in plans.values())
 
     counter = [0]
@@ -368,10 +427,22 @@ def run_ours(args):
     wall1 = time.time()
     total_ms = max_over_ranks(start_ev.elapsed_time(end_ev), world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    # the job's bytes: every rank's algorithmic bytes (with --split columns
+    # each rank reads x and its share of the weights, and writes its share of h)
+    job_bytes = sum(workload.algorithmic_bytes(M, D, hi - lo, "bf16")
+                    for r in range(world) for M in SWEEP
+                    for lo, hi in [(0, D_FF) if args.split == "replicas"
+                                   else sharding.column_range(D_FF, r, world)])
+    value = job_bytes / (ms_per_step * 1e-3) / 1e9
     achieved = step_bytes * args.steps / (total_ms * 1e-3) / 1e9
     avg_launch_us = 1e3 * total_ms / (args.steps * launches_per_step)
     clocks = sampler.summary(wall0, wall1, settle0)
+
+    # ---- distribution of the step time (outside the timed region above,
+    # whose value is taken with events at its two ends only): 30 repetitions
+    # of 10 steps back to back, an event at each repetition's boundary, so
+    # the calls inside a repetition overlap as in the timed region
+    step_ms = quantiles(timed_reps(lambda i: step(), 10, 30, stream))
 
     # ---- end to end through the public API with pinned host buffers.  Every
     # step copies its inputs (x for every M) host->device in one copy, makes
@@ -381,7 +452,7 @@ def run_ours(args):
     # i+1's inputs and the download of step i-1's results; every copy of
     # every step is inside the timed region.
     x_pin = [x_all_host.pin_memory() for _ in range(2)]
-    h_pin = [torch.empty(sum(SWEEP), D_FF, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    h_pin = [torch.empty(sum(SWEEP), n_cols, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     h2d = x_pin[0].numel() * 2
     d2h = h_pin[0].numel() * 2
     xb = [x_all, torch.empty_like(x_all)]
@@ -428,22 +499,18 @@ def run_ours(args):
     e1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    e2e_value = world * step_bytes * args.steps / (e2e_ms * 1e-3) / 1e9
+    e2e_value = job_bytes * args.steps / (e2e_ms * 1e-3) / 1e9
     sampler.stop()
 
     # ---- per-M breakdown (diagnostic, outside the timed region): each M
-    # back to back, and the latency of one isolated call
+    # back to back, per-call times, the latency of one isolated call, and
+    # CUDA-graph replay
     sweep = {}
     for M in SWEEP:
-        b = workload.algorithmic_bytes(M, D, D_FF, "bf16")
-        reps = 60
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for _ in range(reps):
-            call(M)
-        a1.record(stream)
-        torch.cuda.synchronize(dev)
-        ms = a0.elapsed_time(a1) / reps
+        b = workload.algorithmic_bytes(M, D, n_cols, "bf16")
+        per = timed_reps(lambda i: call(M), 20, 10, stream)
+        ms = sum(per) / len(per)
+        q = quantiles(per)
         lat = []
         for _ in range(20):
             l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -476,36 +543,55 @@ def run_ours(args):
         del graph
         sweep[str(M)] = {"us": round(ms * 1e3, 2), "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
                          "frac": round(b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                         "us_median": round(q["median"] * 1e3, 2),
+                         "us_p10": round(q["p10"] * 1e3, 2), "us_p90": round(q["p90"] * 1e3, 2),
                          "isolated_call_us": round(statistics.median(lat) * 1e3, 2),
                          "graph_us": round(graph_ms * 1e3, 2),
                          "path": plans[M]["path"]}
 
+    # ---- oracle leg on the sweep's own outputs (every output of every M,
+    # this rank's columns), outside every timed region
+    if oracle_leg:
+        torch.cuda.synchronize(dev)
+        for M in SWEEP:
+            chk = oracle_check(xs_host[M], wg_s, wu_s, hs[M].cpu(), list(range(M)), "bf16",
+                               M, D, n_cols)
+            sweep[str(M)]["accuracy"] = chk["accuracy"]
+            sweep[str(M)]["oracle"] = chk["oracle"]
+    del wg_h, wu_h
+
     extra = next_rows = fp8_rows = None
     if not args.no_extra:
-        extra = other_configs(dev, peaks, l2, args.extra_iters)
+        xs_sampler = ClockSampler(gpu_uuid(dev))
+        xs_sampler.start()
+        extra = other_configs(dev, peaks, l2, args.extra_iters, oracle_leg, xs_sampler)
         next_rows = down_and_mlp(dev, peaks, l2, args.extra_iters)
         fp8_rows = fp8_configs(dev, peaks, args.extra_iters)
+        xs_sampler.stop()
 
     if rank == 0:
-        cpu = cpu_baseline()
+        cpu = cpu_baseline() if oracle_leg else None
         kernels = sorted(set(p["path"] for p in plans.values()))
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": {"workload": WORKLOAD, "weights": "N(0,1/d) bf16, seed 0",
-                       "l2": "inputs larger than L2 (235 MB of weights per call) and %d weight "
-                             "copies rotated per call" % n_copies,
-                       "clock_settle_steps": settle_steps},
+            "higher_is_better": True, "scaling": "weak" if args.split == "replicas" else "strong",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": bench_config(),
+            "split": args.split if world > 1 else None,
+            "weight_copies": n_copies, "clock_settle_steps": settle_steps,
+            "step_ms": {k: round(v, 5) for k, v in step_ms.items()},
+            "step_ms_note": "median / p10 / p90 of the mean step time of 30 repetitions of 10 "
+                            "steps back to back (after the timed region; ms_per_step is the "
+                            "timed region's mean)",
             "roofline": {"bound": "hbm",
                          "kernel": "skinny_tc_kernel" if kernels == ["skinny"] else "+".join(kernels),
                          "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / peaks["hbm_gbs"], 4),
-                         "traffic": profiled_traffic() if kernels == ["skinny"] else None,
-                         "traffic_source": "profiles/skinny_tc_kernel_decode_sweep_d4096.md "
-                                           "(mean of the 5 sweep launches; null if the kernel "
-                                           "changed since)",
+                         "traffic": profiled_traffic() if kernels == ["skinny"] and n_cols == D_FF
+                         else None,
+                         "traffic_source": TRAFFIC_FILE + " (ncu, mean of the 5 sweep "
+                                           "launches; null if the kernel changed since)",
                          "algorithmic_bytes_per_launch": step_bytes // launches_per_step,
                          "avg_launch_us": round(avg_launch_us, 2),
                          "peak_source": peaks["source"] + " hbm_gbs (copy, burst)",
@@ -536,10 +622,41 @@ def run_ours(args):
     return 0
 
 
-def other_configs(dev, peaks, l2, iters):
+def timed_reps(fn, iters, reps=10, stream=None):
+    """Mean per-call time (ms) of each of `reps` repetitions of `iters` calls
+    back to back, with events only at the repetitions' boundaries (an event
+    between two calls would cut the programmatic overlap of one call's set-up
+    with the previous call's tail, and for calls of a few microseconds it
+    would time the host); for the median / p10 / p90 of a configuration."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    evs[0].record(stream)
+    k = 0
+    for r in range(reps):
+        for _ in range(iters):
+            fn(k)
+            k += 1
+        evs[r + 1].record(stream)
+    torch.cuda.synchronize()
+    return [evs[r].elapsed_time(evs[r + 1]) / iters for r in range(reps)]
+
+
+def add_quantiles(entry, per_ms):
+    q = quantiles(per_ms)
+    entry["us_median"] = round(q["median"] * 1e3, 2)
+    entry["us_p10"] = round(q["p10"] * 1e3, 2)
+    entry["us_p90"] = round(q["p90"] * 1e3, 2)
+    return entry
+
+
+def other_configs(dev, peaks, l2, iters, oracle_leg=False, sampler=None):
     """Secondary measurements of the other workloads (not the headline):
     `iters` calls back to back after 3 warm-up calls, weight copies rotated so
-    that the weights read by each call are not in L2."""
+    that the weights read by each call are not in L2 (mean from events at the
+    two ends; median / p10 / p90 from a second pass with an event per call);
+    then the same calls replayed from a CUDA graph.  With `oracle_leg`, the
+    oracle evaluates rows of each call (check_rows) and the GPU's output of
+    the timed calls is compared with it."""
     import torch
     import swiglu_mlp_projection_gb300 as swg
     from swiglu_mlp_projection_gb300 import inputs, workload
@@ -551,9 +668,9 @@ def other_configs(dev, peaks, l2, iters):
         w_bytes = 2 * wg.numel() * wg.element_size()
         n_copies = max(2, math.ceil(3 * l2 / w_bytes))
         copies = [(wg.to(dev), wu.to(dev)) for _ in range(n_copies)]
-        del wg, wu
         for M in cfg.Ms:
-            x = inputs.make_inputs(M, cfg.d, cfg.d_ff, cfg.dtype, seed=0, x_only=True)[0].to(dev)
+            x_h = inputs.make_inputs(M, cfg.d, cfg.d_ff, cfg.dtype, seed=0, x_only=True)[0]
+            x = x_h.to(dev)
             h = torch.empty(M, cfg.d_ff, dtype=x.dtype, device=dev)
             k = [0]
 
@@ -565,12 +682,15 @@ def other_configs(dev, peaks, l2, iters):
                 call()
             torch.cuda.synchronize(dev)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            w0 = time.time()
             e0.record()
             for _ in range(iters):
                 call()
             e1.record()
             torch.cuda.synchronize(dev)
             ms = e0.elapsed_time(e1) / iters
+            per = timed_reps(lambda i: call(), iters)
+            w1 = time.time()
             # the same calls captured once into a CUDA graph and replayed:
             # no host work per call
             g = torch.cuda.CUDAGraph()
@@ -594,6 +714,19 @@ def other_configs(dev, peaks, l2, iters):
                      "graph_us": round(ms_graph * 1e3, 2),
                      "graph_GB/s": round(by / (ms_graph * 1e-3) / 1e9, 1),
                      "path": swg.plan(M, cfg.d, cfg.d_ff, cfg.dtype, "auto")["path"]}
+            add_quantiles(entry, per)
+            if sampler is not None:
+                # SM clock while this configuration ran (both timing passes):
+                # calls of milliseconds of dense tensor work run under the
+                # power cap at lower clocks
+                cs = sampler.summary(w0, w1, w0)
+                entry["clocks"] = {"sm_mhz": cs["sm_mhz"], "reasons": cs["reasons"],
+                                   "samples": cs.get("samples", 0)}
+            if oracle_leg:
+                rows = check_rows(M, cfg.d, cfg.d_ff)
+                torch.cuda.synchronize(dev)
+                entry.update(oracle_check(x_h, wg, wu, h[rows].cpu(), rows, cfg.dtype,
+                                          M, cfg.d, cfg.d_ff))
             if M <= 16 or cfg.dtype == "f32":
                 entry["frac_hbm"] = round(gbs / peaks["hbm_gbs"], 4)
             else:
@@ -602,8 +735,8 @@ def other_configs(dev, peaks, l2, iters):
                 # the sustained (seconds-long cuBLAS loop) peak
                 entry["frac_bf16_sustained"] = round(tfs / peaks["bf16_tflops_sustained"], 4)
             out[key] = entry
-            del x, h
-        del copies
+            del x, x_h, h
+        del copies, wg, wu
         torch.cuda.empty_cache()
     return out
 
@@ -639,11 +772,13 @@ def fp8_configs(dev, peaks, iters):
         e1.record()
         torch.cuda.synchronize(dev)
         ms = e0.elapsed_time(e1) / iters
+        per = timed_reps(lambda i: swg.swiglu_up_fp8(x, qs[i % 2], out=h), iters)
         by = workload.fp8_bytes(M, d, d_ff)
         fl = workload.flops(M, d, d_ff)
         e = {"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
              "TFLOP/s": round(fl / ms / 1e9, 2), "path": swg.plan(M, d, d_ff)["path"],
              "launches": 2}
+        add_quantiles(e, per)
         if M <= 16:
             e["frac_hbm"] = round(by / ms / 1e6 / peaks["hbm_gbs"], 4)
         else:
@@ -677,8 +812,8 @@ def fp8_configs(dev, peaks, iters):
             e1.record()
             torch.cuda.synchronize(dev)
             ms = e0.elapsed_time(e1) / iters
-            e = {"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
-                 "TFLOP/s": round(fl / ms / 1e9, 2)}
+            e = add_quantiles({"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
+                               "TFLOP/s": round(fl / ms / 1e9, 2)}, timed_reps(fn, iters))
             if M <= 16:
                 e["frac_hbm"] = round(by / ms / 1e6 / peaks["hbm_gbs"], 4)
             else:
@@ -705,6 +840,7 @@ def down_and_mlp(dev, peaks, l2, iters):
     wgs = [(wg.to(dev), wu.to(dev)) for _ in range(n_copies)]
     del wd, wg, wu
     out = {}
+    per_call = []
 
     def timed(fn):
         for i in range(3):
@@ -716,6 +852,7 @@ def down_and_mlp(dev, peaks, l2, iters):
             fn(i)
         e1.record()
         torch.cuda.synchronize(dev)
+        per_call.append(timed_reps(fn, iters))
         return e0.elapsed_time(e1) / iters
 
     for M in (1, 16, 64, 128, 4096):
@@ -729,6 +866,7 @@ def down_and_mlp(dev, peaks, l2, iters):
         e = {"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
              "TFLOP/s": round(fl / ms / 1e9, 2),
              "path": swg.down_plan(M, d_ff, d, "bf16", "auto")["path"]}
+        add_quantiles(e, per_call[-1])
         if e["path"] == "skinny":   # M FLOP per weight byte: below the ridge, HBM-bound
             e["frac_hbm"] = round(by / ms / 1e6 / peaks["hbm_gbs"], 4)
         else:
@@ -742,8 +880,8 @@ def down_and_mlp(dev, peaks, l2, iters):
                                              wds[i % n_copies], residual=x, h=hb, out=y))
         by = workload.algorithmic_bytes(M, d, d_ff, "bf16") + workload.down_bytes(M, d_ff, d, "bf16")
         fl = workload.flops(M, d, d_ff) + workload.down_flops(M, d_ff, d)
-        e = {"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
-             "TFLOP/s": round(fl / ms / 1e9, 2)}
+        e = add_quantiles({"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
+                           "TFLOP/s": round(fl / ms / 1e9, 2)}, per_call[-1])
         if M <= 16:
             e["frac_hbm"] = round(by / ms / 1e6 / peaks["hbm_gbs"], 4)
         else:
@@ -757,19 +895,85 @@ def down_and_mlp(dev, peaks, l2, iters):
 
 
 def cpu_baseline():
-    """The oracle, as it stands, on a bounded sample of the same workload."""
+    """The oracle, as it stands, on a bounded sample of the headline workload
+    (the same sample as the reference arm): on all host cores, then on one."""
+    import oracle
     try:
-        gbs, t, calls, threads = oracle_sweep(2048, 10.0)
+        gbs, t, calls, threads = oracle_sweep(ORACLE_COLS, 10.0)
+        gbs1, t1, calls1, _ = oracle_sweep(ORACLE_COLS, 5.0, threads=1)
     except Exception as e:  # the baseline must not sink the GPU measurement
         return {"value": None, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
                 "sample": "failed: %s" % e}
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": "decode sweep M in {1,2,4,8,16}, d=4096, first 2048 of 14336 columns, "
-                      "%d calls over %.1f s" % (calls, t)}
+            "sample": oracle_sample_text(ORACLE_COLS, 10.0) + ": %d calls over %.1f s" % (calls, t),
+            "single_thread": {"value": round(gbs1, 3), "unit": "GB/s", "cores": 1,
+                              "sample": oracle_sample_text(ORACLE_COLS, 5.0) +
+                              ": %d calls over %.1f s" % (calls1, t1)},
+            "host_cores": os.cpu_count(), "oracle_threads_default": oracle.default_threads()}
+
+
+def check_rows(M, d=0, d_ff=0):
+    """Rows of an M-row call the oracle leg evaluates: all of them up to 64
+    rows or 4e9 multiply-adds per matrix, else 8 rows from different 128-row
+    blocks and 32-row quarters, including the first and the last row."""
+    if M <= 64 or M * d * d_ff <= 4e9:
+        return list(range(M))
+    blocks = (M + 127) // 128
+    picks = {0, M - 1}
+    for i, frac in enumerate((0.0, 0.2, 0.4, 0.6, 0.8, 1.0)):
+        b = min(blocks - 1, int(frac * (blocks - 1)))
+        picks.add(min(M - 1, b * 128 + 32 * (i % 4) + 5 * i))
+    return sorted(picks)
+
+
+def oracle_check(x, wg, wu, h_rows, rows, dtype, M, d, d_ff):
+    """The oracle leg for one timed call: the oracle on `rows` of x (timed on
+    all host cores; the time is extrapolated linearly in M to the whole call,
+    rows being independent), and the GPU's h on those rows compared with it.
+    x, wg, wu: the call's host inputs; h_rows: the GPU result on `rows`."""
+    import numpy as np
+    import oracle
+    import torch
+    from swiglu_mlp_projection_gb300 import inputs, workload
+    from tests.parity import compare
+    raw = inputs.raw_bits
+    od = oracle.BF16 if dtype == "bf16" else oracle.F32
+    xr = x[rows].contiguous()
+    t0 = time.perf_counter()
+    h64, _, sens = oracle.swiglu_up(raw(xr), raw(wg), raw(wu), od)
+    t = time.perf_counter() - t0
+    res = compare(h_rows.to(torch.float64).numpy(), h64, sens, dtype, d)
+    full_s = t * M / len(rows)
+    by = workload.algorithmic_bytes(M, d, d_ff, dtype)
+    fl = workload.flops(M, d, d_ff)
+    return {
+        "accuracy": {"rows_checked": len(rows), "all_rows": len(rows) == M, "ok": res["ok"],
+                     "max_err": float("%.3g" % res["max_err"]),
+                     "normwise": float("%.3g" % res["normwise"]),
+                     "mismatch_pct": round(res["mismatch_pct"], 4),
+                     "mismatch_pct_above_1e-3max": round(res["mismatch_pct_above_1e-3max"], 4)},
+        "oracle": {"rows": len(rows), "s": round(t, 3), "threads": oracle.default_threads(),
+                   "call_s": round(full_s, 3),
+                   "GB/s": round(by / full_s / 1e9, 4), "TFLOP/s": round(fl / full_s / 1e12, 6),
+                   "extrapolated": len(rows) != M},
+    }
 
 
 def main():
     args = parse()
+    rank, world, _ = dist_env()
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # one process per GPU: re-run under torch.distributed.run
+        if args.impl == "ours":
+            import torch
+            if torch.cuda.device_count() < args.gpus:
+                print("bench.py: --gpus %d asked for, %d CUDA devices visible"
+                      % (args.gpus, torch.cuda.device_count()), file=sys.stderr)
+                return 2
+        return subprocess.call(torchrun_argv(args, sys.argv[1:]))
+    if world != args.gpus:
+        print("bench.py: --gpus %d but WORLD_SIZE=%d" % (args.gpus, world), file=sys.stderr)
+        return 2
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
