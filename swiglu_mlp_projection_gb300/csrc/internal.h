@@ -22,6 +22,7 @@ struct SimtPlan {
   int64_t col_blocks, row_chunks, slices, k_per_slice;
   bool fused;       // single launch: the last slice of a column block reduces
   size_t counters_bytes;   // arrival counters of the single launch
+  int cluster = 0;  // > 0: the cluster form (simt_cluster.cu) with this many K slices
 };
 
 // Tuning overrides from the environment (SWIGLU_SK_NB, SWIGLU_SK_PROMO,
@@ -31,8 +32,10 @@ struct SimtPlan {
 // may change them between calls.  -1: not set (the measured default applies).
 struct Tuning {
   int sk_nb = -1, sk_promo = -1, sk_hint = -1, sk_prefetch_units = -1, sk_cluster = -1;
-  int tile_pair = -1, tile_sk = -1, tile_sk_split = -1, tile_seq = -1;
+  int tile_pair = -1, tile_sk = -1, tile_sk_split = -1, tile_seq = -1, tile_band = -1;
   int simt_fused = -1;
+  int sk_bulk = -1;   // skinny stream-K final sums staged by bulk copies (default on)
+  int simt_cluster = -1;   // 0: never use the cluster form of the SIMT path
   // Test hook (SWIGLU_INJECT_OOM=1): every workspace the library would take
   // from its pool or its per-stream cache fails to allocate, so the call
   // returns SWIGLU_ERR_OOM having enqueued nothing.  Caller workspaces and
@@ -53,6 +56,15 @@ cudaError_t launch_simt_partial(const void* x, const void* wg, const void* wu,
                                 int dtype, const SimtPlan& p, cudaStream_t st,
                                 unsigned* counters = nullptr, bool counters_clean = false,
                                 void* h = nullptr, bool packed = false);
+
+// The cluster form of the SIMT path (M = 1, weights <= 32 MB, d <= 2048):
+// the K slices of a column block are one thread-block cluster that adds them
+// in distributed shared memory, in one launch with no workspace.  Returns the
+// cluster size (the K slices) for a call it serves, else 0.
+int simt_cluster_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, const Tuning& tn);
+cudaError_t launch_simt_cluster(const void* x, const void* wg, const void* wu, void* h,
+                                int64_t M, int64_t d, int64_t d_ff, int dtype, bool packed,
+                                cudaStream_t st);
 
 // How the weights are stored:
 //   kWeightsKN      [K, n_out] row-major (the default);
@@ -100,6 +112,7 @@ struct SkinnyPlan {
   bool plain;              // plain epilogue (down projection) instead of SwiGLU
   int prefetch_units;      // units each CTA prefetches into L2 before its dependency wait
   int cluster;             // cluster mode: CTAs per column group (0: stream-K)
+  int bulk;                // stream-K: stage the final sums by bulk copies when possible
   int64_t n_cb, n_kb;      // units: (nb x 64)-column groups, 64-deep k blocks
   int64_t units;           // n_cb * n_kb
   int grid;                // CTAs (<= SM count)
@@ -159,6 +172,7 @@ struct TilePlan {
   bool plain;
   bool pair;
   bool seq;    // SwiGLU: gate then up k loops (N = 128 each) instead of one N = 256 loop
+  int64_t band;   // row blocks per band of the tile order (n_mb: one band)
   int64_t dp_tiles, sk_iters, sk_q, sk_r;
   size_t counters_bytes, part_bytes;
 };

@@ -1,0 +1,267 @@
+// Cluster form of the SIMT path, for the smallest calls: one row of x on
+// small weights (at most 32 MB, d <= 2048, e.g. the f32 decode step at
+// d = 512), where a call moves a few MB and its time is set by latency, not
+// by bandwidth.
+//
+// It computes the same sums as the split-K kernel of "Ou part le temps d'un
+// token" (section "Un kernel pour les matrices etroites": the grid is cut
+// along the weights, and the K slices of a column block are added in a fixed
+// order), and applies SiLU * up only once they are complete, as that page's
+// slice-reduction pass does.  What changes is where the slices meet:
+//   * the S = 8 K slices of a column block are one thread-block cluster, and
+//     each CTA leaves its partial sums in its own shared memory; after a
+//     cluster barrier the CTAs split the block's outputs, read the S partials
+//     through distributed shared memory and add them in rank (= k) order.
+//     No workspace, no arrival counter, no second pass through L2 -- the
+//     page's "Ce qui reste : les lancements" finds such fixed costs to be
+//     most of a small product's time;
+//   * a column block is 128 bytes wide (32 f32 or 64 bf16 columns), so the
+//     grid holds 4-8 CTAs per SM, and every thread issues all of its weight
+//     loads (at most 8 rows of both matrices, 16 bytes each) before it uses
+//     any: the whole call is in flight at once.  Eight lanes cover one 128-byte
+//     row segment, so each warp load reads four full 128-byte lines.
+// Sums per thread in k order, then across the four row groups of a warp
+// (a fixed shuffle tree), across the 8 warps in warp order and across the
+// cluster in rank order: the result is the same bits on every run.
+#include "common.cuh"
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace swg {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kLanesPerRow = 8;                       // 8 x 16 B = one 128-byte row segment
+constexpr int kGroups = kThreads / kLanesPerRow;      // 32 rows of W in flight per pass
+constexpr int kMaxRows = 8;                           // k rows per thread and matrix, at most
+constexpr int kMaxK = kGroups * kMaxRows;             // 256 k per CTA at most
+constexpr int kS = 8;                                 // CTAs per cluster (K slices)
+constexpr int64_t kMaxWeightBytes = (int64_t)32 << 20;
+
+template <bool BF16>
+__device__ __forceinline__ void unpack16(const uint4& v, float* f) {
+  if constexpr (BF16) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+  } else {
+    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+  }
+}
+
+// grid.x = column blocks x kS (a cluster = the kS K slices of one column
+// block), grid.y = chunks of RC rows of x.  ROWS: k rows of W per thread
+// (kn <= 32 ROWS), all in flight at once.  One row of x keeps 4 CTAs (1024
+// threads) resident per SM, so that a call of 4 CTAs per SM runs in one wave.
+template <bool BF16, int RC, int ROWS>
+__global__ void __launch_bounds__(kThreads, (RC == 1 && ROWS <= 4) ? 4 : 2)
+simt_cluster_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
+                    const void* __restrict__ wu_, void* __restrict__ h_, int M, int d,
+                    int d_ff, int packed) {
+  constexpr int VEC = BF16 ? 8 : 4;
+  constexpr int C = kLanesPerRow * VEC;   // columns of a block
+  constexpr int ES = BF16 ? 2 : 4;
+  __shared__ float xs[RC][kMaxK];
+  __shared__ float red[kThreads / 32][RC][2][C];
+  __shared__ __align__(16) float part[RC][2][C];   // this slice's sums, read by the cluster
+
+  const int rank = (int)tc::cluster_ctarank();        // = blockIdx.x % kS
+  const int cb = blockIdx.x / kS;
+  const int row0 = blockIdx.y * RC;
+  const int k0 = (int)((int64_t)rank * d / kS), k1 = (int)((int64_t)(rank + 1) * d / kS);
+  const int kn = k1 - k0;
+  const int l8 = threadIdx.x & 7, grp = threadIdx.x >> 3;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = cb * C + l8 * VEC;
+  const bool valid = col < d_ff;
+
+  // Launched with programmatic stream serialisation: x and h may belong to
+  // the previous kernel until this wait.
+  tc::pdl_wait();
+  tc::pdl_launch_dependents();
+
+  // All weight loads first: rows k0 + grp + 32 i of both matrices.
+  uint4 vg[ROWS], vu[ROWS];
+  if (valid) {
+    // packed weights: gate block b of 64 columns at packed column 128 b, up
+    // at 128 b + 64 (a block of 32 or 64 columns never straddles two)
+    const int gcol = packed ? col + (col & ~63) : col;
+    const int ucol = packed ? gcol + 64 : col;
+    const char* wg = (const char*)wg_ + (size_t)gcol * ES;
+    const char* wu = (const char*)wu_ + (size_t)ucol * ES;
+    const size_t row_bytes = (size_t)(packed ? 128 * ((d_ff + 63) / 64) : d_ff) * ES;
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i) {
+      const int kk = k0 + grp + kGroups * i;
+      if (kk < k1) {
+        vg[i] = ldg_stream_v4(wg + (size_t)kk * row_bytes);
+        vu[i] = ldg_stream_v4(wu + (size_t)kk * row_bytes);
+      }
+    }
+  }
+  // x[row0 : row0 + RC, k0 : k1] as f32 (rows past M are 0) while they land
+  for (int t = threadIdx.x; t < RC * kn; t += kThreads) {
+    const int r = t / kn, k = t - r * kn, row = row0 + r;
+    float v = 0.f;
+    if (row < M) {
+      const size_t idx = (size_t)row * d + k0 + k;
+      if constexpr (BF16)
+        v = bf16_lo(((const uint16_t*)x_)[idx]);
+      else
+        v = ((const float*)x_)[idx];
+    }
+    xs[r][k] = v;
+  }
+  __syncthreads();
+
+  float accg[RC][VEC], accu[RC][VEC];
+#pragma unroll
+  for (int r = 0; r < RC; ++r)
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) accg[r][v] = accu[r][v] = 0.f;
+  if (valid) {
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i) {
+      const int kk = k0 + grp + kGroups * i;
+      if (kk < k1) {
+        float fg[VEC], fu[VEC];
+        unpack16<BF16>(vg[i], fg);
+        unpack16<BF16>(vu[i], fu);
+#pragma unroll
+        for (int r = 0; r < RC; ++r) {
+          const float xv = xs[r][kk - k0];
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) {
+            accg[r][v] = fmaf(xv, fg[v], accg[r][v]);
+            accu[r][v] = fmaf(xv, fu[v], accu[r][v]);
+          }
+        }
+      }
+    }
+  }
+  // The four row groups of a warp hold the same columns: lanes l, l^8, l^16,
+  // l^24.  A fixed two-step tree leaves the same sum in all four.
+#pragma unroll
+  for (int r = 0; r < RC; ++r)
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+      accg[r][v] += __shfl_xor_sync(0xffffffffu, accg[r][v], 8);
+      accu[r][v] += __shfl_xor_sync(0xffffffffu, accu[r][v], 8);
+      accg[r][v] += __shfl_xor_sync(0xffffffffu, accg[r][v], 16);
+      accu[r][v] += __shfl_xor_sync(0xffffffffu, accu[r][v], 16);
+    }
+  if (lane < kLanesPerRow) {
+#pragma unroll
+    for (int r = 0; r < RC; ++r)
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) {
+        red[warp][r][0][l8 * VEC + v] = accg[r][v];
+        red[warp][r][1][l8 * VEC + v] = accu[r][v];
+      }
+  }
+  __syncthreads();
+  // this slice's sums over the 8 warps, in warp order
+  for (int t = threadIdx.x; t < RC * 2 * C; t += kThreads) {
+    const int c = t % C, gu = (t / C) & 1, r = t / (2 * C);
+    float s = red[0][r][gu][c];
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w) s += red[w][r][gu][c];
+    part[r][gu][c] = s;
+  }
+  tc::cluster_sync_all();   // every slice's sums are in place
+
+  // The kS CTAs split the block's 4-column chunks; each adds the kS slices
+  // of its chunks in rank order and applies the epilogue.
+  constexpr int kChunks = RC * C / 4;
+  const int per = (kChunks + kS - 1) / kS;
+  for (int t = threadIdx.x; t < per; t += kThreads) {
+    const int q = rank * per + t;
+    if (q >= kChunks) break;
+    const int r = q / (C / 4), c = (q - r * (C / 4)) * 4;
+    const int row = row0 + r, j = cb * C + c;
+    if (row >= M || j >= d_ff) continue;   // d_ff is a multiple of 4: chunks are whole
+    const uint32_t gl = tc::smem_u32(&part[r][0][c]), ul = tc::smem_u32(&part[r][1][c]);
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+#pragma unroll
+    for (int s = 0; s < kS; ++s) {
+      const float4 a = tc::ld_shared_cluster_v4(tc::mapa_shared(gl, (uint32_t)s));
+      const float4 b = tc::ld_shared_cluster_v4(tc::mapa_shared(ul, (uint32_t)s));
+      g.x += a.x; g.y += a.y; g.z += a.z; g.w += a.w;
+      u.x += b.x; u.y += b.y; u.z += b.z; u.w += b.w;
+    }
+    if constexpr (BF16) {
+      uint2 o;
+      o.x = pack_bf16x2(silu_fast(g.x) * u.x, silu_fast(g.y) * u.y);
+      o.y = pack_bf16x2(silu_fast(g.z) * u.z, silu_fast(g.w) * u.w);
+      *reinterpret_cast<uint2*>((uint16_t*)h_ + (size_t)row * d_ff + j) = o;
+    } else {
+      *reinterpret_cast<float4*>((float*)h_ + (size_t)row * d_ff + j) =
+          make_float4(silu_accurate(g.x) * u.x, silu_accurate(g.y) * u.y,
+                      silu_accurate(g.z) * u.z, silu_accurate(g.w) * u.w);
+    }
+  }
+  tc::cluster_sync_all();   // each CTA's sums stay readable until all peers are done
+}
+
+template <bool BF16, int RC, int ROWS>
+cudaError_t launch_rows(const void* x, const void* wg, const void* wu, void* h, int64_t M,
+                        int64_t d, int64_t d_ff, bool packed, cudaStream_t st) {
+  constexpr int C = kLanesPerRow * (BF16 ? 8 : 4);
+  const int64_t n_cb = (d_ff + C - 1) / C;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kS;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(n_cb * kS), (unsigned)((M + RC - 1) / RC));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, simt_cluster_kernel<BF16, RC, ROWS>, x, wg, wu, h, (int)M,
+                            (int)d, (int)d_ff, packed ? 1 : 0);
+}
+
+template <bool BF16, int RC>
+cudaError_t launch_rc(const void* x, const void* wg, const void* wu, void* h, int64_t M,
+                      int64_t d, int64_t d_ff, bool packed, cudaStream_t st) {
+  const int64_t kn = (d + kS - 1) / kS;    // k of the largest slice
+  if (kn <= 2 * kGroups) return launch_rows<BF16, RC, 2>(x, wg, wu, h, M, d, d_ff, packed, st);
+  if (kn <= 4 * kGroups) return launch_rows<BF16, RC, 4>(x, wg, wu, h, M, d, d_ff, packed, st);
+  return launch_rows<BF16, RC, 8>(x, wg, wu, h, M, d, d_ff, packed, st);
+}
+
+}  // namespace
+
+int simt_cluster_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, const Tuning& tn) {
+  if (tn.simt_cluster == 0) return 0;
+  const int64_t e = dtype == 1 ? 2 : 4;
+  const int C = kLanesPerRow * (dtype == 1 ? 8 : 4);
+  // One row only (measured, graph replay): the f32 decode step d = 512,
+  // d_ff = 2048 takes 4.6 us against 7.1 us on the split-K kernel.  Two or
+  // four rows double or quadruple the accumulators, which halves the CTAs an
+  // SM holds, and the call then needs two waves (bf16 d = 896: 12.4 / 15.4
+  // us at M = 2 / 4 against 8.1 at M = 1).
+  const bool fits = M == 1 && d >= kS && (d + kS - 1) / kS <= kMaxK && d_ff > 0 &&
+                    2 * d * d_ff * e <= kMaxWeightBytes &&
+                    (d_ff + C - 1) / C * kS <= (int64_t)INT32_MAX;
+  return fits ? kS : 0;
+}
+
+cudaError_t launch_simt_cluster(const void* x, const void* wg, const void* wu, void* h,
+                                int64_t M, int64_t d, int64_t d_ff, int dtype, bool packed,
+                                cudaStream_t st) {
+  if (M == 0 || d_ff == 0) return cudaSuccess;
+  if (M != 1) return cudaErrorInvalidValue;   // simt_cluster_plan serves one row
+  return dtype == 1 ? launch_rc<true, 1>(x, wg, wu, h, M, d, d_ff, packed, st)
+                    : launch_rc<false, 1>(x, wg, wu, h, M, d, d_ff, packed, st);
+}
+
+}  // namespace swg

@@ -375,7 +375,10 @@ Tuning read_tuning() {
                           {"TILE_SK", &t.tile_sk},
                           {"TILE_SK_SPLIT", &t.tile_sk_split},
                           {"TILE_SEQ", &t.tile_seq},
+                          {"TILE_BAND", &t.tile_band},
                           {"SIMT_FUSED", &t.simt_fused},
+                          {"SK_BULK", &t.sk_bulk},
+                          {"SIMT_CLUSTER", &t.simt_cluster},
                           {"INJECT_OOM", &t.inject_oom}};
     for (const Knob& k : knobs)
       if (strlen(k.key) == n && strncmp(k.key, name, n) == 0) *k.dst = v;
@@ -492,10 +495,23 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
     p->simt = plan_simt(M, K, n_out, dtype, num_sms, tn);
     if (p->simt.slices > kMaxGridYZ || p->simt.row_chunks > kMaxGridYZ)
       return fail(SWIGLU_ERR_UNSUPPORTED, "shape exceeds the grid limits of the SIMT path");
-    p->slices = p->simt.slices;
-    p->grid = p->simt.col_blocks * p->simt.slices * p->simt.row_chunks;
-    p->workspace = p->simt.counters_bytes + partial_elems(p->slices, M, n_out) * sizeof(float);
-    p->launches = p->slices > 0 && !p->simt.fused ? 2 : 1;
+    p->simt.cluster = simt_cluster_plan(M, K, n_out, dtype, tn);
+    if (p->simt.cluster) {
+      // one launch: K slices in clusters of CTAs, no workspace
+      const int64_t cols = dtype == SWIGLU_BF16 ? 64 : 32;
+      p->simt.fused = false;
+      p->simt.counters_bytes = 0;
+      p->slices = p->simt.cluster;
+      p->grid = (n_out + cols - 1) / cols * p->slices;
+      p->workspace = 0;
+      p->launches = 1;
+      p->cluster = p->simt.cluster;
+    } else {
+      p->slices = p->simt.slices;
+      p->grid = p->simt.col_blocks * p->simt.slices * p->simt.row_chunks;
+      p->workspace = p->simt.counters_bytes + partial_elems(p->slices, M, n_out) * sizeof(float);
+      p->launches = p->slices > 0 && !p->simt.fused ? 2 : 1;
+    }
   } else if (rp == SWIGLU_PATH_SKINNY) {
     p->skinny = plan_skinny(M, K, n_out, num_sms, plain, fp8, sk_caps, tn);
     // K slices per column group: the cluster size, or (stream-K) at most maxq
@@ -672,7 +688,10 @@ int run(const Call& c) {
     fs.sx = sx;
   }
   const Fp8Scales* fsp = fp8_prefix ? &fs : nullptr;
-  if (p.path == SWIGLU_PATH_SIMT && p.simt.fused) {
+  if (p.path == SWIGLU_PATH_SIMT && p.simt.cluster) {
+    e = launch_simt_cluster(c.x, c.wa, c.wb, c.out, c.M, c.K, c.n_out, c.dtype,
+                            c.wlayout == kWeightsPacked, st);
+  } else if (p.path == SWIGLU_PATH_SIMT && p.simt.fused) {
     e = launch_simt_partial(c.x, c.wa, c.wb, part, c.M, c.K, c.n_out, c.dtype, p.simt, st,
                             counters, counters_clean, c.out, c.wlayout == kWeightsPacked);
   } else if (p.path == SWIGLU_PATH_SIMT) {

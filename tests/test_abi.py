@@ -69,12 +69,37 @@ def test_plan_covers_all_columns_rows_and_k(cuda_lib, dtype):
         p = swg.plan(M, d, d_ff, dtype, "simt", 152)
         assert p["path"] == "simt"
         vec = 8 if dtype == "bf16" else 4
+        e = 2 if dtype == "bf16" else 4
+        if p["cluster"] > 1:
+            # the cluster form: 8 K slices per cluster, 128-byte column
+            # blocks, one launch, no workspace
+            assert M == 1 and 8 <= d <= 2048 and 2 * d * d_ff * e <= 32 << 20
+            assert p["slices"] == p["cluster"] == 8
+            assert p["grid"] == -(-d_ff // (8 * vec)) * 8
+            assert p["workspace"] == 0 and p["launches"] == 1
+            continue
         cols = 32 * vec
         chunks = -(-M // p["row_chunk"])
         assert p["grid"] == -(-d_ff // cols) * p["slices"] * chunks
         assert 1 <= p["slices"] <= d
         assert p["workspace"] >= p["slices"] * M * 2 * d_ff * 4
         assert p["workspace"] % 256 == 0
+
+
+def test_simt_cluster_form_selection(cuda_lib, monkeypatch):
+    # M = 1, d <= 2048 and weights <= 32 MB take the cluster form of the SIMT
+    # path; SWIGLU_SIMT_CLUSTER=0 keeps the split-K kernel with its workspace
+    for (M, d, d_ff, dtype, yes) in [(1, 512, 2048, "f32", True), (1, 896, 4864, "bf16", True),
+                                     (2, 896, 4864, "bf16", False),
+                                     (1, 4096, 14336, "bf16", False),
+                                     (1, 2048, 4096, "f32", False),   # 64 MB of weights
+                                     (1, 2056, 1024, "bf16", False),  # d above 2048
+                                     (1, 8, 8, "f32", True), (1, 0, 8, "f32", False)]:
+        p = swg.plan(M, d, d_ff, dtype, "simt", 152)
+        assert (p["cluster"] == 8) == yes, (M, d, d_ff, dtype, p)
+    monkeypatch.setenv("SWIGLU_SIMT_CLUSTER", "0")
+    p = swg.plan(1, 512, 2048, "f32", "simt", 152)
+    assert p["cluster"] == 1 and p["workspace"] > 0
 
 
 def test_plan_reports_cluster_size(cuda_lib):
@@ -90,7 +115,7 @@ def test_plan_reports_cluster_size(cuda_lib):
     # skinny path: split-K clusters for the small down projection only
     assert swg.down_plan(1, 4864, 896, "bf16", "auto", 152)["cluster"] == 8
     assert swg.plan(1, 4096, 14336, "bf16", "auto", 152)["cluster"] == 1
-    assert swg.plan(1, 512, 2048, "f32", "auto", 152)["cluster"] == 1
+    assert swg.plan(1, 512, 2048, "f32", "auto", 152)["cluster"] == 8   # SIMT cluster form
 
 
 def test_dispatch_rule(cuda_lib):

@@ -136,3 +136,27 @@ def test_mlp_matches_oracle(M):
     y64, _, ys = oracle.down_proj(inputs.raw_bits(h.cpu()), raw(wd), oracle.BF16, raw(x))
     assert compare(to64(y), y64, ys, "bf16", d_ff)["ok"]
     swg.check_device_status()
+
+
+@pytest.mark.parametrize("shape", [(16, 14336, 4096), (64, 14336, 4096), (128, 14336, 4096),
+                                   (40, 4104, 1032), (200, 2056, 520)])
+def test_bulk_staged_final_sums_equal_l2_sums(shape, monkeypatch):
+    # The skinny kernel's final sums, staged in shared memory by bulk copies
+    # (SWIGLU_SK_BULK=1, the default) or read from L2 (0), add the same
+    # partials in the same order: the bits must agree, and match the oracle.
+    M, d_ff, d = shape
+    h, wd, r = make(M, d_ff, d, seed=M + 1)
+    outs = []
+    for bulk in ("1", "0"):
+        monkeypatch.setenv("SWIGLU_SK_BULK", bulk)
+        monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")
+        y = swg.swiglu_down(h.to(DEV), wd.to(DEV), r.to(DEV), path="skinny")
+        torch.cuda.synchronize()
+        outs.append(y)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    raw = inputs.raw_bits
+    rows = np.unique(np.linspace(0, M - 1, min(M, 8)).astype(int))
+    y64, _, s = oracle.down_proj(raw(h[rows].contiguous()), raw(wd), oracle.BF16,
+                                 raw(r[rows].contiguous()))
+    assert compare(to64(outs[0])[rows], y64, s, "bf16", d_ff)["ok"]
+    swg.check_device_status()

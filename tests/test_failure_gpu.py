@@ -53,7 +53,7 @@ def _check(h, x, wg, wu, d):
 
 
 @pytest.mark.parametrize("case", [("bf16", "auto", 16, 4096, 14336),   # skinny, stream-K
-                                  ("f32", "auto", 1, 512, 2048),       # SIMT
+                                  ("f32", "auto", 5, 512, 2048),       # SIMT split-K (M > 4)
                                   ("bf16", "tc", 64, 4096, 1032)])     # tile, stream-K tail
 def test_injected_workspace_oom_enqueues_nothing(case, monkeypatch):
     # SWIGLU_INJECT_OOM=1 makes every library-owned workspace allocation fail:

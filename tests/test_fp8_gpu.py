@@ -215,3 +215,21 @@ def test_fp8_down_full_size_rows():
     for M, rows in ((16, np.arange(16)), (128, [0, 63, 127]), (4096, tile_rows(4096, seed=4))):
         down_check(M, 14336, 4096, "auto", seed=M, rows=rows)
     swg.check_device_status()
+
+
+@pytest.mark.parametrize("M", [16, 64])
+def test_fp8_down_bulk_staged_final_sums(M, monkeypatch):
+    # FP8 down projection (stream-K at d = 4096): both final-sum routes agree
+    h = inputs.make_inputs(M, 14336, 8, "bf16", seed=M, x_only=True)[0]
+    _, wd, _ = inputs.make_inputs(1, 14336, 4096, "bf16", seed=M + 1)
+    r = inputs.make_inputs(M, 4096, 8, "bf16", seed=M + 2, x_only=True)[0]
+    w8 = swg.quantize_weight_fp8(wd.to(DEV))
+    outs = []
+    for bulk in ("1", "0"):
+        monkeypatch.setenv("SWIGLU_SK_BULK", bulk)
+        outs.append(swg.swiglu_down_fp8(h.to(DEV), w8, residual=r.to(DEV), path="skinny"))
+        torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    rows = [0, M - 1]
+    y64, sens = oracle.down_proj_fp8(RAW(h[rows].contiguous()), RAW(wd), RAW(r[rows].contiguous()))
+    assert compare(to64(outs[0])[rows], y64, sens, "bf16", 14336)["ok"]

@@ -254,6 +254,7 @@ def test_output_guard_band_untouched():
 @pytest.mark.parametrize("path", ["simt", "skinny"])
 def test_caller_workspace_and_errors(path, monkeypatch):
     monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")     # the split-K workspace of stream-K mode
+    monkeypatch.setenv("SWIGLU_SIMT_CLUSTER", "0")   # (the SIMT path's cluster form has none)
     dev = torch.device("cuda", 0)
     M, d, d_ff = 3, 1024, 2048
     x, wg, wu = (t.to(dev) for t in inputs.make_inputs(M, d, d_ff, "bf16", seed=35))
@@ -312,6 +313,7 @@ def test_simt_single_launch_matches_two_launches(dtype, shape, monkeypatch):
     # launch, in the last CTA of each column block; both add the slices in
     # the same order, so the results are bit-identical.
     M, d, d_ff = shape
+    monkeypatch.setenv("SWIGLU_SIMT_CLUSTER", "0")   # the split-K form's two reductions
     dev = torch.device("cuda", 0)
     x, wg, wu = (t.to(dev) for t in inputs.make_inputs(M, d, d_ff, dtype, seed=M + d))
     out = {}
@@ -324,3 +326,19 @@ def test_simt_single_launch_matches_two_launches(dtype, shape, monkeypatch):
     view = torch.int32 if dtype == "f32" else torch.int16
     assert torch.equal(out["0"].view(view), out["1"].view(view))
     full_check(M, d, d_ff, dtype, "simt", seed=M + d)
+
+
+@pytest.mark.parametrize("M,d,d_ff", [(16, 4096, 14336), (32, 4096, 14336), (130, 640, 1032),
+                                      (7, 1024, 4104)])
+def test_skinny_bulk_staged_final_sums_equal_l2_sums(M, d, d_ff, monkeypatch):
+    # the up projection's final sums by either route: identical bits
+    x, wg, wu = inputs.make_inputs(M, d, d_ff, "bf16", seed=M + 2)
+    outs = []
+    for bulk in ("1", "0"):
+        monkeypatch.setenv("SWIGLU_SK_BULK", bulk)
+        monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")
+        outs.append(gpu_run(x, wg, wu, "skinny"))
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    raw = inputs.raw_bits
+    h64, _, sens = oracle.swiglu_up(raw(x), raw(wg), raw(wu), oracle.BF16)
+    assert compare(to64(outs[0]), h64, sens, "bf16", d)["ok"]
