@@ -565,8 +565,8 @@ def run_ours(args):
         xs_sampler = ClockSampler(gpu_uuid(dev))
         xs_sampler.start()
         extra = other_configs(dev, peaks, l2, args.extra_iters, oracle_leg, xs_sampler)
-        next_rows = down_and_mlp(dev, peaks, l2, args.extra_iters)
-        fp8_rows = fp8_configs(dev, peaks, args.extra_iters)
+        next_rows = down_and_mlp(dev, peaks, l2, args.extra_iters, xs_sampler)
+        fp8_rows = fp8_configs(dev, peaks, args.extra_iters, xs_sampler)
         xs_sampler.stop()
 
     if rank == 0:
@@ -741,7 +741,15 @@ def other_configs(dev, peaks, l2, iters, oracle_leg=False, sampler=None):
     return out
 
 
-def fp8_configs(dev, peaks, iters):
+def clocks_of(sampler, w0, w1):
+    """Median SM clock and throttle reasons sampled between wall times w0, w1."""
+    if sampler is None:
+        return None
+    cs = sampler.summary(w0, w1, w0)
+    return {"sm_mhz": cs["sm_mhz"], "reasons": cs["reasons"], "samples": cs.get("samples", 0)}
+
+
+def fp8_configs(dev, peaks, iters, sampler=None):
     """The FP8 (e4m3) up projection at d=4096, d_ff=14336: the decode sweep
     and the prefill call, back to back with 2 weight copies (117 MB each,
     larger than L2); then the FP8 down projection and the FP8 MLP (both
@@ -765,6 +773,7 @@ def fp8_configs(dev, peaks, iters):
         for i in range(3):
             swg.swiglu_up_fp8(x, qs[i % 2], out=h)
         torch.cuda.synchronize(dev)
+        w0 = time.time()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for i in range(iters):
@@ -773,12 +782,14 @@ def fp8_configs(dev, peaks, iters):
         torch.cuda.synchronize(dev)
         ms = e0.elapsed_time(e1) / iters
         per = timed_reps(lambda i: swg.swiglu_up_fp8(x, qs[i % 2], out=h), iters)
+        w1 = time.time()
         by = workload.fp8_bytes(M, d, d_ff)
         fl = workload.flops(M, d, d_ff)
         e = {"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
              "TFLOP/s": round(fl / ms / 1e9, 2), "path": swg.plan(M, d, d_ff)["path"],
              "launches": 2}
         add_quantiles(e, per)
+        e["clocks"] = clocks_of(sampler, w0, w1)
         if M <= 16:
             e["frac_hbm"] = round(by / ms / 1e6 / peaks["hbm_gbs"], 4)
         else:
@@ -805,6 +816,7 @@ def fp8_configs(dev, peaks, iters):
             for i in range(3):
                 fn(i)
             torch.cuda.synchronize(dev)
+            w0 = time.time()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             for i in range(iters):
@@ -814,6 +826,7 @@ def fp8_configs(dev, peaks, iters):
             ms = e0.elapsed_time(e1) / iters
             e = add_quantiles({"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
                                "TFLOP/s": round(fl / ms / 1e9, 2)}, timed_reps(fn, iters))
+            e["clocks"] = clocks_of(sampler, w0, time.time())
             if M <= 16:
                 e["frac_hbm"] = round(by / ms / 1e6 / peaks["hbm_gbs"], 4)
             else:
@@ -825,7 +838,7 @@ def fp8_configs(dev, peaks, iters):
     return out
 
 
-def down_and_mlp(dev, peaks, l2, iters):
+def down_and_mlp(dev, peaks, l2, iters, sampler=None):
     """The down projection y = h.W_down + r and the two-kernel MLP at the
     decode and prefill shapes of d=4096, d_ff=14336 (back to back); the down
     projection also at M = 64 and 128, which its skinny path serves."""
@@ -841,11 +854,13 @@ def down_and_mlp(dev, peaks, l2, iters):
     del wd, wg, wu
     out = {}
     per_call = []
+    walls = []
 
     def timed(fn):
         for i in range(3):
             fn(i)
         torch.cuda.synchronize(dev)
+        walls.append(time.time())
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for i in range(iters):
@@ -853,6 +868,7 @@ def down_and_mlp(dev, peaks, l2, iters):
         e1.record()
         torch.cuda.synchronize(dev)
         per_call.append(timed_reps(fn, iters))
+        walls.append(time.time())
         return e0.elapsed_time(e1) / iters
 
     for M in (1, 16, 64, 128, 4096):
@@ -867,6 +883,7 @@ def down_and_mlp(dev, peaks, l2, iters):
              "TFLOP/s": round(fl / ms / 1e9, 2),
              "path": swg.down_plan(M, d_ff, d, "bf16", "auto")["path"]}
         add_quantiles(e, per_call[-1])
+        e["clocks"] = clocks_of(sampler, walls[-2], walls[-1])
         if e["path"] == "skinny":   # M FLOP per weight byte: below the ridge, HBM-bound
             e["frac_hbm"] = round(by / ms / 1e6 / peaks["hbm_gbs"], 4)
         else:
@@ -882,6 +899,7 @@ def down_and_mlp(dev, peaks, l2, iters):
         fl = workload.flops(M, d, d_ff) + workload.down_flops(M, d_ff, d)
         e = add_quantiles({"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
                            "TFLOP/s": round(fl / ms / 1e9, 2)}, per_call[-1])
+        e["clocks"] = clocks_of(sampler, walls[-2], walls[-1])
         if M <= 16:
             e["frac_hbm"] = round(by / ms / 1e6 / peaks["hbm_gbs"], 4)
         else:

@@ -124,6 +124,10 @@ constexpr int kSkinnyMaxN = 256;
 // Weights up to this size (bytes of the matrices one call streams) run the
 // skinny kernel in cluster mode, larger ones in stream-K mode.
 constexpr int64_t kSkinnyClusterMaxWeightBytes = (int64_t)32 << 20;
+// Whether a down projection's 128-column groups fit as 4-CTA clusters all at
+// once (cluster_caps: clusters of 2 / 4 / 8 skinny CTAs that fit, or null to
+// assume 0.95 num_sms / 4 of them).
+bool skinny_plain_cluster4_fits(int64_t K, int64_t n_out, int num_sms, const int* cluster_caps);
 // K: shared dimension; n_out: output columns; plain: down-projection mode.
 // cluster_caps[lg]: thread-block clusters of 2^lg CTAs of the skinny kernel
 // that fit on the device at once (lg = 1..3), or null (an estimate from num_sms).

@@ -307,21 +307,16 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return a0 < b0 + nb && b0 < a0 + na;
 }
 
-// Largest M the dispatcher sends to the skinny (split-K) path for bf16.  The
-// decode article serves at most 16 rows with its skinny kernel; measured on
-// GB300 (both paths forced, back to back), the skinny tcgen05 kernel stays
-// ahead of the tile kernel up to M = 32 for the up projection at d = 896,
-// 4096 and 8192 (d = 4096: 39.4 vs 40.2 us at M = 32, 42.8 vs 40.4 at 48),
-// and up to M = 64 for the down projection, whose few output tiles leave the
-// tile kernel short of parallelism (d = 4096: 40.6 vs 42.1 us at M = 64,
-// 49.8 vs 42.4 at 96; d = 896: 21.7 vs 27.3 us at M = 64).
 // Largest bf16 M that AUTO sends to the skinny kernel, by operation and by
-// whether the weights stream in stream-K mode (above 32 MB) or in cluster
-// mode (the skinny kernel's two modes).
+// the skinny kernel's mode for the weights: cluster mode (at most 32 MB),
+// stream-K, or, for the down projection above 32 MB whose 128-column groups
+// fit as 4-CTA clusters, that cluster mode.  The decode article serves at
+// most 16 rows with its skinny kernel; the tcgen05 skinny kernel pays longer.
 constexpr int64_t kSkinnyMaxM = 32;
 constexpr int64_t kSkinnyMaxMSmall = 64;
 constexpr int64_t kSkinnyMaxMDown = 128;
 constexpr int64_t kSkinnyMaxMDownSmall = 256;
+constexpr int64_t kSkinnyMaxMDownCluster4 = 256;
 
 // Grid-dimension limits of the SIMT path (gridDim.y/z are 16-bit).
 constexpr int64_t kMaxGridYZ = kSimtMaxGridYZ;
@@ -346,10 +341,17 @@ enum Op { kOpUp = 0, kOpDown = 1 };
 // (d = 4096: 44.6 vs 48.9 us at M = 128, 58.3 vs 49.4 at 192; d = 8192:
 // 94.9 vs 109 at 128).  Cluster mode, d = 896: up projection 64 (10.0 vs
 // 10.4 us at M = 64, 11.7 vs 10.5 at 96); down projection all M the kernel
-// serves (13.9 vs 27.3 us at M = 256).  FP8 calls measure alike.
-int64_t skinny_max_m(int op, int64_t K, int64_t n_out) {
+// serves (13.9 vs 27.3 us at M = 256).  Down projection in 4-CTA clusters of
+// 128-column groups (d_ff = 14336 -> d = 4096): the skinny kernel leads up to
+// the 256 rows it serves (37.3 vs 49.6 us at M = 256; FP8 32.4 vs 46.7).
+// FP8 calls measure alike otherwise.
+int64_t skinny_max_m(int op, int64_t K, int64_t n_out, int num_sms, const int* sk_caps) {
   const bool small = (op == kOpDown ? 1 : 2) * K * n_out * 2 <= kSkinnyClusterMaxWeightBytes;
-  if (op == kOpDown) return small ? kSkinnyMaxMDownSmall : kSkinnyMaxMDown;
+  if (op == kOpDown) {
+    if (small) return kSkinnyMaxMDownSmall;
+    return skinny_plain_cluster4_fits(K, n_out, num_sms, sk_caps) ? kSkinnyMaxMDownCluster4
+                                                                  : kSkinnyMaxMDown;
+  }
   return small ? kSkinnyMaxMSmall : kSkinnyMaxM;
 }
 
@@ -393,7 +395,8 @@ namespace {
 // reduction kernel then writes h = silu(0) * 0 = 0.
 // Down projection: bf16 only, on the tensor-core paths (M <= skinny_max_m
 // -> SKINNY).
-int resolve_path(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, int* out) {
+int resolve_path(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, int* out,
+                 int num_sms, const int* sk_caps) {
   if (path < SWIGLU_PATH_AUTO || path > SWIGLU_PATH_TC)
     return fail(SWIGLU_ERR_INVALID_ARG, "unknown path %d", path);
   if (op == kOpDown) {
@@ -404,7 +407,9 @@ int resolve_path(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int pat
   }
   if (path == SWIGLU_PATH_AUTO) {
     if (op == kOpUp && (dtype == SWIGLU_F32 || K == 0)) *out = SWIGLU_PATH_SIMT;
-    else *out = M <= skinny_max_m(op, K, n_out) ? SWIGLU_PATH_SKINNY : SWIGLU_PATH_TC;
+    else
+      *out = M <= skinny_max_m(op, K, n_out, num_sms, sk_caps) ? SWIGLU_PATH_SKINNY
+                                                                : SWIGLU_PATH_TC;
     return SWIGLU_OK;
   }
   if (path != SWIGLU_PATH_SIMT && dtype != SWIGLU_BF16)
@@ -483,7 +488,7 @@ struct Plan {
 int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, int num_sms,
               int max_pairs, Plan* p, bool fp8 = false, const int* sk_caps = nullptr) {
   int rp = 0;
-  int st = resolve_path(op, M, K, n_out, dtype, path, &rp);
+  int st = resolve_path(op, M, K, n_out, dtype, path, &rp, num_sms, sk_caps);
   if (st != SWIGLU_OK) return st;
   *p = Plan{};
   p->path = rp;
@@ -1101,7 +1106,7 @@ static int plan_common(int op, int64_t M, int64_t K, int64_t n_out, int dtype, i
   out->grid = p.grid;
   out->row_chunk = p.path == SWIGLU_PATH_SIMT ? p.simt.row_chunk : 0;
   out->workspace = (int64_t)p.workspace;
-  out->skinny_max_m = skinny_max_m(op, K, n_out);
+  out->skinny_max_m = skinny_max_m(op, K, n_out, num_sms, nullptr);
   out->launches = p.launches;
   out->cluster = p.cluster;
   return SWIGLU_OK;

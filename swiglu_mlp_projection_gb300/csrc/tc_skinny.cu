@@ -73,6 +73,7 @@ constexpr uint32_t kChunkBytes = kCB * kBK * 2;       // one 64 x 64 bf16 weight
 constexpr uint32_t kSubBytes = 2 * kChunkBytes;       // gate box + up box = one MMA A tile
 constexpr uint32_t kPrefetchBytes = 512u * 1024u;     // weight bytes per CTA prefetched before the wait
 constexpr uint32_t kRingBudget = 200u * 1024u;        // shared memory for the stage ring
+constexpr int64_t kPlainCluster4MinM = 32;            // see plan_skinny (FP8: 16)
 
 constexpr uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
   uint32_t r = lo;
@@ -789,6 +790,12 @@ cudaError_t launch_mode(int n_pad, int nb, const CUtensorMap& mx, const CUtensor
 
 }  // namespace
 
+bool skinny_plain_cluster4_fits(int64_t K, int64_t n_out, int num_sms, const int* cluster_caps) {
+  const int64_t groups = (n_out + 2 * kCB - 1) / (2 * kCB);   // 128-column groups
+  const int64_t cap4 = cluster_caps ? cluster_caps[2] : (int64_t)(num_sms / 4 * 0.95);
+  return groups >= 1 && groups <= cap4 && (K + kBK - 1) / kBK >= 4;
+}
+
 SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
                        bool fp8, const int* cluster_caps, const Tuning& tn) {
   SkinnyPlan p{};
@@ -818,6 +825,22 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
     const int64_t slots2 = per2 > 0 ? (n_kb2 + per2 - 1) / per2 + 1 : 1;
     const int64_t limit = fp8 ? (int64_t)128 << 10 : (int64_t)256 << 10;
     if (slots2 * 4 * kCB * 4 * M > limit) nb = 1;
+  }
+  // Large down projections from kPlainCluster4MinM rows on (FP8: 16): 4-CTA
+  // clusters of 128-column groups, when all the groups' clusters fit at once
+  // (n_out up to 36 x 128 on GB300).  The group's four K quarters then meet
+  // in distributed shared memory instead of ~5 partial slots in L2 that one
+  // CTA adds after everyone else is done, a tail that grows with M.
+  // Measured, d_ff = 14336 -> d = 4096, calls back to back, stream-K vs
+  // 4-CTA clusters: M = 16: 25.2 / 27.8 us; 32: 29.0 / 28.4; 64: 33.5 /
+  // 29.7; 128: 42.3 / 31.9; 256: 62.6 / 37.3.  FP8: M = 16: 19.6 / 18.5;
+  // 64: 27.3 / 20.9.  (d = 8192 needs 64 groups, more than fit: stream-K.)
+  bool plain_cluster4 = false;
+  if (plain && weight_bytes > kSkinnyClusterMaxWeightBytes &&
+      M >= (fp8 ? kPlainCluster4MinM / 2 : kPlainCluster4MinM) && tn.sk_nb < 0 &&
+      tn.sk_cluster < 0 && skinny_plain_cluster4_fits(K, n_out, num_sms, cluster_caps)) {
+    nb = 1;
+    plain_cluster4 = true;
   }
   while (nb > 1 && nb * n > 256) nb /= 2;
   p.nb = nb;
@@ -866,6 +889,7 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
     }
   }
   p.cluster = (S >= 2 && weight_bytes <= kSkinnyClusterMaxWeightBytes) ? S : 0;
+  if (plain_cluster4) p.cluster = 4;
   const int forced = tn.sk_cluster;
   if (forced == 0) p.cluster = 0;
   if (forced == 1 || forced == 2 || forced == 4 || forced == 8)

@@ -20,8 +20,9 @@
 //   * the epilogue (4 warps, one accumulator row per thread) reads gate and up
 //     columns with tcgen05.ld, computes silu(g) * u in f32, rounds to bf16 into
 //     a 128-byte-swizzled staging tile and TMA-stores it.
-// Tiles are visited column-block-major so the CTAs running at the same time
-// share weight columns and x rows through L2.
+// Tiles are visited band by band (a band = a few 128/256-row blocks),
+// column-block-major inside a band, so the CTAs running at the same time
+// share weight columns and x rows through L2 (tile_coords).
 //
 // Above 128 rows the kernel runs on CTA pairs (2-CTA clusters, tcgen05
 // cta_group::2): a tile is 256 rows, each CTA loads its 128 rows of x and
@@ -76,8 +77,8 @@ static_assert(TileCfg<true>::kSmemBytes <= 232448, "pair tile exceeds shared mem
 static_assert(TileCfg<false>::kSmemBytes <= 232448, "tile exceeds shared memory");
 
 struct TileArgs {
-  int n_mb, n_kb, n_out;         // n_mb: row blocks of the tile height (tile t: row block
-                                 // t % n_mb, column block t / n_mb); n_out: output columns
+  int n_mb, n_kb, n_out;         // n_mb: row blocks of the tile height; n_out: output columns
+  int n_nb, band;                // column blocks; row blocks per band (tile_coords)
   int M;
   const uint16_t* resid;         // plain mode: [M][n_out] added to the sums, or null
   int kmajor;                    // weights stored [n_out, K] instead of [K, n_out]
@@ -99,6 +100,26 @@ struct TileArgs {
 };
 
 constexpr int kPartFloats = kBM * 2 * kBN;   // one CTA's 128 x 256 f32 accumulator
+
+// Row block mb and column block nb of tile t.  The row blocks are cut into
+// bands of `band` (the last band may be shorter); tiles run band by band,
+// column-block-major inside a band, so the tiles in flight at once share the
+// x rows of one band and a few weight columns through L2.  With one band
+// (band = n_mb) this is the plain column-block-major order.
+__device__ __forceinline__ void tile_coords(const TileArgs& a, int64_t t, int& mb, int& nb) {
+  const int64_t full = (int64_t)(a.n_mb / a.band) * a.band * a.n_nb;   // tiles in full bands
+  if (t < full) {
+    const int64_t per = (int64_t)a.band * a.n_nb;
+    const int64_t b = t / per, l = t - b * per;
+    nb = (int)(l / a.band);
+    mb = (int)(b * a.band + (l - (int64_t)nb * a.band));
+  } else {
+    const int64_t rows = a.n_mb - (int64_t)(a.n_mb / a.band) * a.band;
+    const int64_t l = t - full;
+    nb = (int)(l / rows);
+    mb = (int)((int64_t)(a.n_mb / a.band) * a.band + (l - (int64_t)nb * rows));
+  }
+}
 
 // First stream-K iteration of unit u.
 __device__ __forceinline__ int64_t sk_begin(const TileArgs& a, int64_t u) {
@@ -244,7 +265,8 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
       const int n_box = n_ph == 2 ? 2 : C::kBoxes;
       const uint32_t stage_tx = kABytes + (uint32_t)n_box * kChunkBytes;
       while (ok && w.next(a, n_units, t, kb0, kb1)) {
-        const int mb = (int)(t % a.n_mb), nb = (int)(t / a.n_mb);
+        int mb, nb;
+        tile_coords(a, t, mb, nb);
         const int row0 = mb * C::kTileRows + (int)rank * kBM;
         for (int ph = 0; ok && ph < n_ph; ++ph)
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -422,7 +444,8 @@ tile_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     int64_t t;
     int kb0, kb1;
     while (!skip && w.next(a, n_units, t, kb0, kb1)) {
-      const int mb = (int)(t % a.n_mb), nb = (int)(t / a.n_mb);
+      int mb, nb;
+      tile_coords(a, t, mb, nb);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, a.status, a.timeout_ns)) break;
       tc_fence_after();
       const int row_base = mb * C::kTileRows + (int)rank * kBM;
@@ -654,6 +677,29 @@ TilePlan plan_tile(int64_t M, int64_t K, int64_t n_out, int num_sms, bool plain,
   // units: CTAs, or CTA pairs, that run at once
   int64_t units = p.pair ? (num_sms / 2 < max_pairs ? num_sms / 2 : max_pairs) : num_sms;
   if (units < 1) units = 1;
+  // Banded tile order.  The tiles in flight at once (one per unit) share the
+  // x rows of one band, which every wave of the band reads again, while each
+  // weight column block is used by one wave only.  So a band holds as many
+  // row blocks as keep its x rows within a quarter of L2 (32 MB), evened
+  // out over the bands.  Measured at d = 8192, d_ff = 29568, M = 8192 (32
+  // row blocks of 4 MB; calls back to back): one band 5148 us (x re-read
+  // from DRAM for every wave: 16.75 GB of DRAM reads per call against
+  // 1.59 GB of algorithmic bytes), bands of 16 / 11 / 8 row blocks 4731 /
+  // 4569 / 4413 us.  Prefill (d = 4096, 16 row blocks of 2 MB) and d = 8192,
+  // M = 2048 keep one band, their fastest.  SWIGLU_TILE_BAND overrides.
+  {
+    const int64_t xr = rows * K * 2;   // bytes of x per row block
+    const int64_t budget = (int64_t)32 << 20;
+    int64_t band = xr > 0 ? budget / xr : p.n_mb;
+    if (band < 1) band = 1;
+    if (band > p.n_mb) band = p.n_mb;
+    if (band > 0) {
+      const int64_t nbands = (p.n_mb + band - 1) / band;
+      band = (p.n_mb + nbands - 1) / nbands;
+    }
+    if (tn.tile_band > 0) band = tn.tile_band < p.n_mb ? tn.tile_band : p.n_mb;
+    p.band = band > 0 ? band : 1;
+  }
   p.dp_tiles = p.tiles;
   // Stream-K tail.  With W full waves and a partial one, the last wave plus
   // one full wave (all tiles if W = 0) are split along K over the units, in
@@ -784,6 +830,8 @@ cudaError_t launch_tile_tc(const void* x, const void* wa, const void* wb, void* 
   if ((e = make_tmap_bf16_2d(&mh, out, M, n_out, 64, kBM)) != cudaSuccess) return e;
   TileArgs a;
   a.n_mb = (int)p.n_mb;
+  a.n_nb = (int)p.n_nb;
+  a.band = (int)p.band;
   a.n_kb = (int)((K + kBK - 1) / kBK);
   a.n_out = (int)n_out;
   a.M = (int)M;

@@ -121,19 +121,28 @@ def test_plan_reports_cluster_size(cuda_lib):
 def test_dispatch_rule(cuda_lib):
     # measured thresholds, weights above 32 MB (stream-K mode): skinny up to
     # M = 32 (up) and 128 (down); smaller weights (cluster mode): 64 (up) and
-    # every M the skinny kernel serves (down)
+    # every M the skinny kernel serves (down); a down projection whose
+    # 128-column groups fit as 4-CTA clusters (d = 4096): every M it serves
     for M, path in [(1, "skinny"), (16, "skinny"), (32, "skinny"), (33, "tc"), (4096, "tc")]:
         assert swg.plan(M, 4096, 14336, "bf16", "auto", 152)["path"] == path
     for M, path in [(1, "skinny"), (64, "skinny"), (65, "tc"), (512, "tc")]:
         assert swg.plan(M, 896, 4864, "bf16", "auto", 152)["path"] == path
-    for M, path in [(1, "skinny"), (64, "skinny"), (128, "skinny"), (129, "tc"), (4096, "tc")]:
+    for M, path in [(1, "skinny"), (64, "skinny"), (256, "skinny"), (257, "tc"), (4096, "tc")]:
         assert swg.down_plan(M, 14336, 4096, "bf16", "auto", 152)["path"] == path
+    for M, path in [(1, "skinny"), (128, "skinny"), (129, "tc"), (4096, "tc")]:
+        assert swg.down_plan(M, 29568, 8192, "bf16", "auto", 152)["path"] == path
     for M, path in [(1, "skinny"), (256, "skinny"), (257, "tc")]:
         assert swg.down_plan(M, 4864, 896, "bf16", "auto", 152)["path"] == path
     assert swg.plan(1, 4096, 14336, "bf16", "auto", 152)["skinny_max_m"] == 32
     assert swg.plan(1, 896, 4864, "bf16", "auto", 152)["skinny_max_m"] == 64
-    assert swg.down_plan(1, 14336, 4096, "bf16", "auto", 152)["skinny_max_m"] == 128
+    assert swg.down_plan(1, 14336, 4096, "bf16", "auto", 152)["skinny_max_m"] == 256
+    assert swg.down_plan(1, 29568, 8192, "bf16", "auto", 152)["skinny_max_m"] == 128
     assert swg.down_plan(1, 4864, 896, "bf16", "auto", 152)["skinny_max_m"] == 256
+    # the down projection at d = 4096: stream-K up to 31 rows, 4-CTA clusters
+    # of 128-column groups from 32 on
+    for M, cl in [(16, 1), (31, 1), (32, 4), (256, 4)]:
+        p = swg.down_plan(M, 14336, 4096, "bf16", "auto", 152)
+        assert p["cluster"] == cl and (cl == 1) == (p["workspace"] > 0), (M, p)
     assert swg.plan(1, 512, 2048, "f32", "auto", 152)["path"] == "simt"
     assert swg.plan(3, 0, 64, "bf16", "auto", 152)["path"] == "simt"
     with pytest.raises(swg.SwiGLUError):
@@ -145,16 +154,21 @@ def test_dispatch_rule(cuda_lib):
 def test_down_projection_column_groups(cuda_lib, monkeypatch):
     # 256-column groups (11 partial slots at d = 4096) until their partial
     # sums pass 256 KB per group, then 128-column groups (6 slots)
+    # (stream-K mode forced: at d = 4096 the down projection takes 4-CTA
+    # clusters from M = 32 on)
+    monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")
     assert swg.down_plan(16, 14336, 4096, "bf16", "skinny", 152)["slices"] == 11
     assert swg.down_plan(64, 14336, 4096, "bf16", "skinny", 152)["slices"] == 6
+    monkeypatch.delenv("SWIGLU_SK_CLUSTER")
     assert swg.down_plan(32, 29568, 8192, "bf16", "skinny", 152)["slices"] == 6
     assert swg.down_plan(64, 29568, 8192, "bf16", "skinny", 152)["slices"] == 4
     # small weights stay in cluster mode; the up projection keeps its groups
     assert swg.down_plan(256, 4864, 896, "bf16", "skinny", 152)["cluster"] == 8
     assert swg.plan(32, 4096, 14336, "bf16", "skinny", 152)["slices"] == 3
-    # SWIGLU_SK_NB overrides the rule
+    # SWIGLU_SK_NB overrides the rule (and keeps stream-K mode)
     monkeypatch.setenv("SWIGLU_SK_NB", "2")
     assert swg.down_plan(64, 14336, 4096, "bf16", "skinny", 152)["slices"] == 11
+    assert swg.down_plan(64, 14336, 4096, "bf16", "skinny", 152)["cluster"] == 1
 
 
 def test_packed_weight_bytes(cuda_lib):

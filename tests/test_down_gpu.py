@@ -62,7 +62,7 @@ def test_skinny_plain_cluster_modes(cluster, monkeypatch):
 
 @pytest.mark.parametrize("M", [1, 4, 16, 48])
 def test_decode_shape_full(M):
-    # d_ff=14336 -> d=4096; M = 48 takes 128-column groups (large partials)
+    # d_ff=14336 -> d=4096; M = 48 takes 4-CTA clusters of 128-column groups
     check(M, 14336, 4096, "auto", seed=M)
 
 
@@ -74,10 +74,31 @@ def test_small_model_full(M):
     check(M, 4864, 896, "auto", seed=M + 5)
 
 
-def test_skinny_up_to_128_rows_sampled():
-    # AUTO serves M = 128 on the skinny kernel at d = 4096 (128-column groups)
-    assert swg.down_plan(128, 14336, 4096)["path"] == "skinny"
-    check(128, 14336, 4096, "auto", seed=128, rows=np.array([0, 1, 63, 127]))
+@pytest.mark.parametrize("M", [32, 128, 256])
+def test_skinny_cluster4_rows(M):
+    # AUTO serves M = 32 .. 256 at d = 4096 on the skinny kernel in 4-CTA
+    # clusters of 128-column groups (the K quarters meet on chip)
+    p = swg.down_plan(M, 14336, 4096)
+    assert p["path"] == "skinny" and p["cluster"] == 4 and p["workspace"] == 0
+    check(M, 14336, 4096, "auto", seed=M, rows=tile_rows(M, seed=M))
+
+
+def test_cluster4_and_stream_k_agree(monkeypatch):
+    # both modes of the skinny kernel serve the same call
+    M, d_ff, d = 40, 14336, 4096
+    h, wd, r = make(M, d_ff, d, seed=77)
+    outs = {}
+    for mode in ("0", "4"):
+        monkeypatch.setenv("SWIGLU_SK_CLUSTER", mode)
+        monkeypatch.setenv("SWIGLU_SK_NB", "1")
+        assert swg.down_plan(M, d_ff, d, "bf16", "skinny")["cluster"] == (4 if mode == "4" else 1)
+        y = swg.swiglu_down(h.to(DEV), wd.to(DEV), r.to(DEV), path="skinny")
+        torch.cuda.synchronize()
+        outs[mode] = to64(y)
+    raw = inputs.raw_bits
+    y64, _, s = oracle.down_proj(raw(h), raw(wd), oracle.BF16, raw(r))
+    for mode, y in outs.items():
+        assert compare(y, y64, s, "bf16", d_ff)["ok"], mode
 
 
 def test_prefill_shape_tile_rows():

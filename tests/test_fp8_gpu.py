@@ -233,3 +233,10 @@ def test_fp8_down_bulk_staged_final_sums(M, monkeypatch):
     rows = [0, M - 1]
     y64, sens = oracle.down_proj_fp8(RAW(h[rows].contiguous()), RAW(wd), RAW(r[rows].contiguous()))
     assert compare(to64(outs[0])[rows], y64, sens, "bf16", 14336)["ok"]
+
+
+@pytest.mark.parametrize("M", [16, 64, 256])
+def test_fp8_down_cluster4(M):
+    # FP8 down projection at d = 4096: 4-CTA clusters of 128-column groups
+    # from M = 16 on; every column of rows of every 128-row block
+    down_check(M, 14336, 4096, "auto", seed=M + 9, rows=tile_rows(M, seed=M))

@@ -113,3 +113,30 @@ def test_sequential_gate_then_up_order(shape, layout, monkeypatch):
     h64, _, s = oracle.swiglu_up(RAW(x), RAW(wg), RAW(wu), oracle.BF16)
     res = compare(to64(h), h64, s, "bf16", d)
     assert res["ok"], (shape, layout, res)
+
+
+@pytest.mark.parametrize("band", ["1", "2", "3"])
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_banded_tile_order(band, pair, monkeypatch):
+    # tiles run in bands of row blocks (the last band shorter when the band
+    # does not divide the row blocks); every tile is computed exactly once
+    monkeypatch.setenv("SWIGLU_TILE_BAND", band)
+    monkeypatch.setenv("SWIGLU_TILE_PAIR", pair)
+    monkeypatch.setenv("SWIGLU_TILE_SK", "0")
+    M, d, d_ff = 1100, 264, 904          # 9 / 5 row blocks, 8 column blocks
+    x, wg, wu = inputs.make_inputs(M, d, d_ff, "bf16", seed=int(band) + 10 * int(pair))
+    buf = torch.full(((M + 40) * d_ff,), 7.0, dtype=torch.bfloat16, device=DEV)
+    h = buf[: M * d_ff].view(M, d_ff)
+    swg.swiglu_up(x.to(DEV), wg.to(DEV), wu.to(DEV), out=h, path="tc")
+    torch.cuda.synchronize()
+    assert bool((buf[M * d_ff:] == 7.0).all())
+    h64, _, s = oracle.swiglu_up(RAW(x), RAW(wg), RAW(wu), oracle.BF16)
+    res = compare(to64(h), h64, s, "bf16", d)
+    assert res["ok"], (band, pair, res)
+    # the down projection's plain tiles too
+    _, wd, _ = inputs.make_inputs(1, d_ff, d, "bf16", seed=3)
+    hb = h[:, :].contiguous()
+    y = swg.swiglu_down(hb, wd.to(DEV), path="tc")
+    torch.cuda.synchronize()
+    y64, _, ys = oracle.down_proj(RAW(hb.cpu()), RAW(wd), oracle.BF16)
+    assert compare(to64(y), y64, ys, "bf16", d_ff)["ok"]
