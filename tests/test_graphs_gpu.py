@@ -114,3 +114,37 @@ def test_fp8_call_in_a_graph():
     h64, sens, _ = oracle.swiglu_up_fp8(raw(xn), raw(wg), raw(wu))
     res = compare(h.to("cpu", torch.float64).numpy(), h64, sens, "bf16", d)
     assert res["ok"], res
+
+
+@pytest.mark.parametrize("M", [16, 64])
+def test_down_projection_in_a_graph(M):
+    # d_ff = 14336 -> d = 4096: stream-K (M = 16, arrival counters from the
+    # graph-counter region) and 4-CTA clusters (M = 64, no workspace);
+    # replays with a new h match the oracle and the direct call bit for bit
+    d_ff, d = 14336, 4096
+    dev = torch.device("cuda", 0)
+    h0 = inputs.make_inputs(M, d_ff, 8, "bf16", seed=80, x_only=True)[0]
+    _, wd, _ = inputs.make_inputs(1, d_ff, d, "bf16", seed=81)
+    r = inputs.make_inputs(M, d, 8, "bf16", seed=82, x_only=True)[0]
+    hs, wds, rs = h0.to(dev), wd.to(dev), r.to(dev)
+    y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+    assert swg.down_plan(M, d_ff, d)["cluster"] == (4 if M >= 32 else 1)
+    swg.swiglu_down(hs, wds, residual=rs, out=y)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        swg.swiglu_down(hs, wds, residual=rs, out=y)
+    hn = inputs.make_inputs(M, d_ff, 8, "bf16", seed=83, x_only=True)[0]
+    hs.copy_(hn.to(dev))
+    g.replay()
+    torch.cuda.synchronize()
+    raw = inputs.raw_bits
+    rows = np.unique(np.linspace(0, M - 1, 4).astype(int))
+    y64, _, s = oracle.down_proj(raw(hn[rows].contiguous()), raw(wd), oracle.BF16,
+                                 raw(r[rows].contiguous()))
+    res = compare(y.to("cpu", torch.float64).numpy()[rows], y64, s, "bf16", d_ff)
+    assert res["ok"], (M, res)
+    ref = swg.swiglu_down(hs, wds, residual=rs)
+    torch.cuda.synchronize()
+    assert torch.equal(ref.view(torch.int16), y.view(torch.int16))
+    swg.check_device_status()
