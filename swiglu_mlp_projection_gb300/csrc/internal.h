@@ -62,6 +62,9 @@ cudaError_t launch_simt_partial(const void* x, const void* wg, const void* wu,
 // in distributed shared memory, in one launch with no workspace.  Returns the
 // cluster size (the K slices) for a call it serves, else 0.
 int simt_cluster_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, const Tuning& tn);
+// Largest d for which AUTO prefers the cluster form for bf16 (at most 4 rows
+// of W per thread, so 4 CTAs fit per SM).
+constexpr int64_t kSimtClusterPreferMaxK = 1024;
 cudaError_t launch_simt_cluster(const void* x, const void* wg, const void* wu, void* h,
                                 int64_t M, int64_t d, int64_t d_ff, int dtype, bool packed,
                                 cudaStream_t st);

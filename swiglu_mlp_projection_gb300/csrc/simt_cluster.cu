@@ -8,17 +8,18 @@
 // along the weights, and the K slices of a column block are added in a fixed
 // order), and applies SiLU * up only once they are complete, as that page's
 // slice-reduction pass does.  What changes is where the slices meet:
-//   * the S = 8 K slices of a column block are one thread-block cluster, and
-//     each CTA leaves its partial sums in its own shared memory; after a
-//     cluster barrier the CTAs split the block's outputs, read the S partials
-//     through distributed shared memory and add them in rank (= k) order.
-//     No workspace, no arrival counter, no second pass through L2 -- the
+//   * the S = 8 K slices of a column block are one thread-block cluster; each
+//     CTA stores its partial sums into the shared memory of the cluster's
+//     rank 0 (distributed shared memory), and after one cluster barrier rank
+//     0 adds the S partials in rank (= k) order and applies the epilogue;
+//     the other CTAs exit at the barrier, since nobody reads their shared
+//     memory.  No workspace, no arrival counter, no second pass through L2 -- the
 //     page's "Ce qui reste : les lancements" finds such fixed costs to be
 //     most of a small product's time;
 //   * a column block is 128 bytes wide (32 f32 or 64 bf16 columns), so the
 //     grid holds 4-8 CTAs per SM, and every thread issues all of its weight
-//     loads (at most 8 rows of both matrices, 16 bytes each) before it uses
-//     any: the whole call is in flight at once.  Eight lanes cover one 128-byte
+//     loads (at most 8 rows of both matrices, 16 bytes each) and the x values
+//     of those rows before it uses any: the whole call is in flight at once.  Eight lanes cover one 128-byte
 //     row segment, so each warp load reads four full 128-byte lines.
 // Sums per thread in k order, then across the four row groups of a warp
 // (a fixed shuffle tree), across the 8 warps in warp order and across the
@@ -35,7 +36,7 @@ constexpr int kThreads = 256;
 constexpr int kLanesPerRow = 8;                       // 8 x 16 B = one 128-byte row segment
 constexpr int kGroups = kThreads / kLanesPerRow;      // 32 rows of W in flight per pass
 constexpr int kMaxRows = 8;                           // k rows per thread and matrix, at most
-constexpr int kMaxK = kGroups * kMaxRows;             // 256 k per CTA at most
+constexpr int kMaxK = kGroups * kMaxRows;             // 256 k per CTA at most (d <= 2048)
 constexpr int kS = 8;                                 // CTAs per cluster (K slices)
 constexpr int64_t kMaxWeightBytes = (int64_t)32 << 20;
 
@@ -64,15 +65,15 @@ simt_cluster_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
   constexpr int VEC = BF16 ? 8 : 4;
   constexpr int C = kLanesPerRow * VEC;   // columns of a block
   constexpr int ES = BF16 ? 2 : 4;
-  __shared__ float xs[RC][kMaxK];
   __shared__ float red[kThreads / 32][RC][2][C];
-  __shared__ __align__(16) float part[RC][2][C];   // this slice's sums, read by the cluster
+  // rank 0 only: every slice's sums, written by their CTAs through
+  // distributed shared memory
+  __shared__ __align__(16) float part[kS][RC][2][C];
 
   const int rank = (int)tc::cluster_ctarank();        // = blockIdx.x % kS
   const int cb = blockIdx.x / kS;
   const int row0 = blockIdx.y * RC;
   const int k0 = (int)((int64_t)rank * d / kS), k1 = (int)((int64_t)(rank + 1) * d / kS);
-  const int kn = k1 - k0;
   const int l8 = threadIdx.x & 7, grp = threadIdx.x >> 3;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int col = cb * C + l8 * VEC;
@@ -83,8 +84,10 @@ simt_cluster_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
   tc::pdl_wait();
   tc::pdl_launch_dependents();
 
-  // All weight loads first: rows k0 + grp + 32 i of both matrices.
+  // All loads first: rows k0 + grp + 32 i of both matrices, and the x values
+  // of those rows (rows of x past M read as 0).
   uint4 vg[ROWS], vu[ROWS];
+  float xv[ROWS][RC];
   if (valid) {
     // packed weights: gate block b of 64 columns at packed column 128 b, up
     // at 128 b + 64 (a block of 32 or 64 columns never straddles two)
@@ -101,21 +104,23 @@ simt_cluster_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
         vu[i] = ldg_stream_v4(wu + (size_t)kk * row_bytes);
       }
     }
-  }
-  // x[row0 : row0 + RC, k0 : k1] as f32 (rows past M are 0) while they land
-  for (int t = threadIdx.x; t < RC * kn; t += kThreads) {
-    const int r = t / kn, k = t - r * kn, row = row0 + r;
-    float v = 0.f;
-    if (row < M) {
-      const size_t idx = (size_t)row * d + k0 + k;
-      if constexpr (BF16)
-        v = bf16_lo(((const uint16_t*)x_)[idx]);
-      else
-        v = ((const float*)x_)[idx];
+#pragma unroll
+    for (int i = 0; i < ROWS; ++i) {
+      const int kk = k0 + grp + kGroups * i;
+#pragma unroll
+      for (int r = 0; r < RC; ++r) {
+        float v = 0.f;
+        if (kk < k1 && row0 + r < M) {
+          const size_t idx = (size_t)(row0 + r) * d + kk;
+          if constexpr (BF16)
+            v = bf16_lo(__ldg((const unsigned short*)x_ + idx));
+          else
+            v = __ldg((const float*)x_ + idx);
+        }
+        xv[i][r] = v;
+      }
     }
-    xs[r][k] = v;
   }
-  __syncthreads();
 
   float accg[RC][VEC], accu[RC][VEC];
 #pragma unroll
@@ -132,11 +137,10 @@ simt_cluster_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
         unpack16<BF16>(vu[i], fu);
 #pragma unroll
         for (int r = 0; r < RC; ++r) {
-          const float xv = xs[r][kk - k0];
 #pragma unroll
           for (int v = 0; v < VEC; ++v) {
-            accg[r][v] = fmaf(xv, fg[v], accg[r][v]);
-            accu[r][v] = fmaf(xv, fu[v], accu[r][v]);
+            accg[r][v] = fmaf(xv[i][r], fg[v], accg[r][v]);
+            accu[r][v] = fmaf(xv[i][r], fu[v], accu[r][v]);
           }
         }
       }
@@ -163,32 +167,30 @@ simt_cluster_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
       }
   }
   __syncthreads();
-  // this slice's sums over the 8 warps, in warp order
+  // this slice's sums over the 8 warps, in warp order, stored into rank 0's
+  // shared memory (slot `rank`)
+  const uint32_t part0 = tc::mapa_shared(tc::smem_u32(&part[rank][0][0][0]), 0u);
   for (int t = threadIdx.x; t < RC * 2 * C; t += kThreads) {
     const int c = t % C, gu = (t / C) & 1, r = t / (2 * C);
     float s = red[0][r][gu][c];
 #pragma unroll
     for (int w = 1; w < kThreads / 32; ++w) s += red[w][r][gu][c];
-    part[r][gu][c] = s;
+    tc::st_shared_cluster_f32(part0 + (uint32_t)(((r * 2 + gu) * C + c) * 4), s);
   }
-  tc::cluster_sync_all();   // every slice's sums are in place
+  tc::cluster_sync_all();   // every slice's sums are in rank 0's shared memory
+  if (rank != 0) return;    // nobody reads the other CTAs' shared memory
 
-  // The kS CTAs split the block's 4-column chunks; each adds the kS slices
-  // of its chunks in rank order and applies the epilogue.
+  // Rank 0 adds the kS slices in rank (= k) order and applies the epilogue.
   constexpr int kChunks = RC * C / 4;
-  const int per = (kChunks + kS - 1) / kS;
-  for (int t = threadIdx.x; t < per; t += kThreads) {
-    const int q = rank * per + t;
-    if (q >= kChunks) break;
+  for (int q = threadIdx.x; q < kChunks; q += kThreads) {
     const int r = q / (C / 4), c = (q - r * (C / 4)) * 4;
     const int row = row0 + r, j = cb * C + c;
     if (row >= M || j >= d_ff) continue;   // d_ff is a multiple of 4: chunks are whole
-    const uint32_t gl = tc::smem_u32(&part[r][0][c]), ul = tc::smem_u32(&part[r][1][c]);
     float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
 #pragma unroll
     for (int s = 0; s < kS; ++s) {
-      const float4 a = tc::ld_shared_cluster_v4(tc::mapa_shared(gl, (uint32_t)s));
-      const float4 b = tc::ld_shared_cluster_v4(tc::mapa_shared(ul, (uint32_t)s));
+      const float4 a = *reinterpret_cast<const float4*>(&part[s][r][0][c]);
+      const float4 b = *reinterpret_cast<const float4*>(&part[s][r][1][c]);
       g.x += a.x; g.y += a.y; g.z += a.z; g.w += a.w;
       u.x += b.x; u.y += b.y; u.z += b.z; u.w += b.w;
     }
@@ -203,7 +205,6 @@ simt_cluster_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
                       silu_accurate(g.z) * u.z, silu_accurate(g.w) * u.w);
     }
   }
-  tc::cluster_sync_all();   // each CTA's sums stay readable until all peers are done
 }
 
 template <bool BF16, int RC, int ROWS>

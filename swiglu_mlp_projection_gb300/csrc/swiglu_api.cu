@@ -485,16 +485,25 @@ struct Plan {
 // K: shared dimension; n_out: output columns (up: d, d_ff; down: d_ff, d).
 // max_pairs: 2-CTA clusters that fit on the device at once (num_sms / 2 when
 // planning without a device).
+// nk: the weights are [n_out, K] (served by the tensor-core paths only).
 int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, int num_sms,
-              int max_pairs, Plan* p, bool fp8 = false, const int* sk_caps = nullptr) {
+              int max_pairs, Plan* p, bool fp8 = false, const int* sk_caps = nullptr,
+              bool nk = false) {
   int rp = 0;
   int st = resolve_path(op, M, K, n_out, dtype, path, &rp, num_sms, sk_caps);
   if (st != SWIGLU_OK) return st;
+  const Tuning tn = read_tuning();
+  // AUTO, bf16, one row on small weights: the SIMT path's cluster form
+  // (measured, graph replay, against the skinny tcgen05 kernel: d = 512 /
+  // 896 / 1024 at M = 1: 3.2 / 6.6 / 4.6 us against 4.2 / 7.0 / 6.4 us; at
+  // d = 2048 it trails, 10.2 against 9.8 us).
+  if (path == SWIGLU_PATH_AUTO && op == kOpUp && dtype == SWIGLU_BF16 && !fp8 && !nk &&
+      simt_cluster_plan(M, K, n_out, dtype, tn) && K <= kSimtClusterPreferMaxK)
+    rp = SWIGLU_PATH_SIMT;
   *p = Plan{};
   p->path = rp;
   p->cluster = 1;
   const bool plain = op == kOpDown;
-  const Tuning tn = read_tuning();
   p->inject_oom = tn.inject_oom != 0;
   if (rp == SWIGLU_PATH_SIMT) {
     p->simt = plan_simt(M, K, n_out, dtype, num_sms, tn);
@@ -571,7 +580,7 @@ int run(const Call& c) {
   // FP8: the GEMM kernels see each row of e4m3 codes as K / 2 byte pairs
   const int64_t Kg = c.fp8 ? c.K / 2 : c.K;
   if ((v = make_plan(c.op, c.M, Kg, c.n_out, c.dtype, c.path, di.num_sms, di.max_pairs, &p,
-                     c.fp8, di.sk_caps)) != SWIGLU_OK)
+                     c.fp8, di.sk_caps, c.wlayout == kWeightsNK)) != SWIGLU_OK)
     return v;
   if (c.fp8 && p.path == SWIGLU_PATH_SIMT && c.K > 0)
     return fail(SWIGLU_ERR_UNSUPPORTED, "FP8 weights are served by the tensor-core paths only");

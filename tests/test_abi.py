@@ -125,8 +125,10 @@ def test_dispatch_rule(cuda_lib):
     # 128-column groups fit as 4-CTA clusters (d = 4096): every M it serves
     for M, path in [(1, "skinny"), (16, "skinny"), (32, "skinny"), (33, "tc"), (4096, "tc")]:
         assert swg.plan(M, 4096, 14336, "bf16", "auto", 152)["path"] == path
-    for M, path in [(1, "skinny"), (64, "skinny"), (65, "tc"), (512, "tc")]:
+    # (one row on small weights with d <= 1024: the SIMT path's cluster form)
+    for M, path in [(1, "simt"), (2, "skinny"), (64, "skinny"), (65, "tc"), (512, "tc")]:
         assert swg.plan(M, 896, 4864, "bf16", "auto", 152)["path"] == path
+    assert swg.plan(1, 2048, 3584, "bf16", "auto", 152)["path"] == "skinny"
     for M, path in [(1, "skinny"), (64, "skinny"), (256, "skinny"), (257, "tc"), (4096, "tc")]:
         assert swg.down_plan(M, 14336, 4096, "bf16", "auto", 152)["path"] == path
     for M, path in [(1, "skinny"), (128, "skinny"), (129, "tc"), (4096, "tc")]:
