@@ -78,8 +78,10 @@ typedef enum {
 /*
  * h = silu(x . W_gate) (.) (x . W_up).
  *
- * Dispatch (AUTO): f32 -> SIMT split-K path; bf16 with M <= the skinny limit
- * (swiglu_plan reports it) -> SKINNY; larger bf16 M -> TC.  The split-K
+ * Dispatch (AUTO): f32 -> SIMT path; bf16 with M <= the skinny limit
+ * (swiglu_plan reports it) -> SKINNY; larger bf16 M -> TC.  One row on
+ * weights of 32 MB or less with d <= 2048 (f32) or d <= 1024 (bf16) takes
+ * the SIMT path's cluster form (one launch, no workspace).  The split-K
  * paths, and the TC path where it splits its last wave of tiles along K
  * (stream-K), need a workspace for their partial sums; this entry point takes it
  * from a library-owned, stream-ordered pool (cudaMallocFromPoolAsync /
@@ -320,12 +322,17 @@ typedef struct {
   int64_t row_chunk;     /* rows of x per SIMT pass (SIMT path)                  */
   int64_t workspace;     /* bytes of partial sums                                */
   int64_t skinny_max_m;  /* largest bf16 M that AUTO sends to SKINNY at these
-                            weight sizes: 32 (up projection); 128 (down
-                            projection, weights above 32 MB) or 64 (smaller)  */
+                            weight sizes.  Up projection: 32, or 128 for
+                            weights of 32 MB or less (where one row may take
+                            the SIMT path's cluster form instead).  Down
+                            projection: 128, or 256 for weights of 32 MB or
+                            less and where 128-column groups fit as 4-CTA
+                            clusters                                         */
   int64_t launches;      /* kernel launches one call enqueues                   */
   int64_t cluster;       /* CTAs per thread-block cluster of the main kernel
                             (1: none; 2-8: the skinny kernel's split-K
-                            clusters; 2: the TC path's CTA pairs)            */
+                            clusters; 8: the SIMT path's cluster form;
+                            2: the TC path's CTA pairs)                      */
 } swiglu_plan_info;
 
 SWIGLU_API int swiglu_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, int path,

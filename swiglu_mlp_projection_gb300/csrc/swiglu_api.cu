@@ -313,7 +313,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 // fit as 4-CTA clusters, that cluster mode.  The decode article serves at
 // most 16 rows with its skinny kernel; the tcgen05 skinny kernel pays longer.
 constexpr int64_t kSkinnyMaxM = 32;
-constexpr int64_t kSkinnyMaxMSmall = 64;
+constexpr int64_t kSkinnyMaxMSmall = 128;
 constexpr int64_t kSkinnyMaxMDown = 128;
 constexpr int64_t kSkinnyMaxMDownSmall = 256;
 constexpr int64_t kSkinnyMaxMDownCluster4 = 256;
@@ -339,8 +339,9 @@ enum Op { kOpUp = 0, kOpDown = 1 };
 // included).  Stream-K mode: up projection 32 at d = 4096 and 8192 (d =
 // 4096: 39.4 vs 40.2 us at M = 32, 42.8 vs 40.4 at 48); down projection 128
 // (d = 4096: 44.6 vs 48.9 us at M = 128, 58.3 vs 49.4 at 192; d = 8192:
-// 94.9 vs 109 at 128).  Cluster mode, d = 896: up projection 64 (10.0 vs
-// 10.4 us at M = 64, 11.7 vs 10.5 at 96); down projection all M the kernel
+// 94.9 vs 109 at 128).  Cluster mode, d = 896 (graph replay; 64-column
+// groups from 16 rows): up projection 128 (9.97 vs 10.67 us at M = 128,
+// 11.84 vs 10.39 at 192); down projection all M the kernel
 // serves (13.9 vs 27.3 us at M = 256).  Down projection in 4-CTA clusters of
 // 128-column groups (d_ff = 14336 -> d = 4096): the skinny kernel leads up to
 // the 256 rows it serves (37.3 vs 49.6 us at M = 256; FP8 32.4 vs 46.7).

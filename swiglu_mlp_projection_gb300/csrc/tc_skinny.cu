@@ -842,6 +842,16 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
     nb = 1;
     plain_cluster4 = true;
   }
+  // Small weights, up projection, from 16 rows: single 64-column units, when
+  // their twice as many column groups still fit as 2-CTA clusters at once
+  // (measured, graph replay, d = 896, d_ff = 4864: M = 16 / 64 take 7.2 /
+  // 8.5 us against 7.3 / 9.7 us in 128-column groups).
+  if (!plain && weight_bytes <= kSkinnyClusterMaxWeightBytes && M >= 16 && tn.sk_nb < 0 &&
+      tn.sk_cluster < 0) {
+    const int64_t groups1 = (n_out + kCB - 1) / kCB;
+    const int64_t cap2 = cluster_caps ? cluster_caps[1] : (int64_t)(num_sms / 2);
+    if (groups1 <= cap2 && (K + kBK - 1) / kBK >= 2) nb = 1;
+  }
   while (nb > 1 && nb * n > 256) nb /= 2;
   p.nb = nb;
   p.l2_promo = tn.sk_promo >= 0 ? tn.sk_promo : 128;
@@ -895,6 +905,11 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   if (forced == 1 || forced == 2 || forced == 4 || forced == 8)
     p.cluster = p.n_kb >= forced ? forced : 0;
   if (p.cluster) p.grid = (int)(p.n_cb * p.cluster);
+  // Cluster mode, up projection: no L2 prefetch before the dependency wait.
+  // With a few MB per call the prefetch only delays the first loads
+  // (measured, graph replay, d = 896: 6.8 / 9.7 us at M = 1 / 64 without it,
+  // 7.1 / 9.8 us with it).
+  if (p.cluster && !plain && tn.sk_prefetch_units < 0) p.prefetch_units = 0;
   const int64_t per = p.units > 0 ? p.units / p.grid : 1;   // fewest units a CTA gets
   p.maxq = (int)((p.n_kb + per - 1) / (per > 0 ? per : 1) + 1);
   p.counters_bytes = ((size_t)p.n_cb * sizeof(unsigned) + 255) / 256 * 256;

@@ -120,13 +120,14 @@ def test_plan_reports_cluster_size(cuda_lib):
 
 def test_dispatch_rule(cuda_lib):
     # measured thresholds, weights above 32 MB (stream-K mode): skinny up to
-    # M = 32 (up) and 128 (down); smaller weights (cluster mode): 64 (up) and
+    # M = 32 (up) and 128 (down); smaller weights (cluster mode): 128 (up) and
     # every M the skinny kernel serves (down); a down projection whose
     # 128-column groups fit as 4-CTA clusters (d = 4096): every M it serves
     for M, path in [(1, "skinny"), (16, "skinny"), (32, "skinny"), (33, "tc"), (4096, "tc")]:
         assert swg.plan(M, 4096, 14336, "bf16", "auto", 152)["path"] == path
     # (one row on small weights with d <= 1024: the SIMT path's cluster form)
-    for M, path in [(1, "simt"), (2, "skinny"), (64, "skinny"), (65, "tc"), (512, "tc")]:
+    for M, path in [(1, "simt"), (2, "skinny"), (64, "skinny"), (128, "skinny"), (129, "tc"),
+                    (512, "tc")]:
         assert swg.plan(M, 896, 4864, "bf16", "auto", 152)["path"] == path
     assert swg.plan(1, 2048, 3584, "bf16", "auto", 152)["path"] == "skinny"
     for M, path in [(1, "skinny"), (64, "skinny"), (256, "skinny"), (257, "tc"), (4096, "tc")]:
@@ -136,7 +137,7 @@ def test_dispatch_rule(cuda_lib):
     for M, path in [(1, "skinny"), (256, "skinny"), (257, "tc")]:
         assert swg.down_plan(M, 4864, 896, "bf16", "auto", 152)["path"] == path
     assert swg.plan(1, 4096, 14336, "bf16", "auto", 152)["skinny_max_m"] == 32
-    assert swg.plan(1, 896, 4864, "bf16", "auto", 152)["skinny_max_m"] == 64
+    assert swg.plan(1, 896, 4864, "bf16", "auto", 152)["skinny_max_m"] == 128
     assert swg.down_plan(1, 14336, 4096, "bf16", "auto", 152)["skinny_max_m"] == 256
     assert swg.down_plan(1, 29568, 8192, "bf16", "auto", 152)["skinny_max_m"] == 128
     assert swg.down_plan(1, 4864, 896, "bf16", "auto", 152)["skinny_max_m"] == 256

@@ -136,15 +136,17 @@ def test_cluster_mode_selection():
     # Small weights (<= 32 MB) run the skinny kernel in the largest clusters
     # that all fit at once, with no workspace: the small model's down
     # projection in 8-CTA clusters (4 of them), its up projection in 2-CTA
-    # clusters (38 groups: too many for one wave of 4-CTA clusters).  The
-    # d = 4096 decode stays on stream-K.
+    # clusters (38 or 76 groups: too many for one wave of 4-CTA clusters).
+    # The d = 4096 decode stays on stream-K.
     for M in (1, 16):
         p = swg.down_plan(M, 4864, 896, "bf16", "auto", 152)
         assert p["path"] == "skinny" and p["workspace"] == 0 and p["grid"] == 4 * 8
         assert p["cluster"] == 8
         assert swg.down_workspace_bytes(M, 4864, 896, "bf16", "auto") == 0
+        # (from 16 rows in 64-column groups: 76 clusters of 2)
         p = swg.plan(M, 896, 4864, "bf16", "skinny", 152)
-        assert p["cluster"] == 2 and p["grid"] == 38 * 2 and p["workspace"] == 0
+        assert p["cluster"] == 2 and p["grid"] == (76 if M >= 16 else 38) * 2
+        assert p["workspace"] == 0
         assert swg.workspace_bytes(M, 896, 4864, "bf16", "skinny") == 0
     # AUTO: one row takes the SIMT path's cluster form (8 K slices, no workspace)
     p = swg.plan(1, 896, 4864, "bf16", "auto", 152)
