@@ -842,6 +842,11 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
     nb = 1;
     plain_cluster4 = true;
   }
+  // Small weights, down projection: single 128-column groups, so twice as
+  // many clusters stream the weights (measured, graph replay, d_ff = 4864 ->
+  // d = 896, 8-CTA clusters: M = 1 / 16 / 64 / 128 take 7.1 / 7.5 / 8.5 /
+  // 10.0 us in 7 groups against 8.3 / 8.8 / 10.9 / 14.2 us in 4).
+  if (plain && weight_bytes <= kSkinnyClusterMaxWeightBytes && tn.sk_nb < 0) nb = 1;
   // Small weights, up projection, from 16 rows: single 64-column units, when
   // their twice as many column groups still fit as 2-CTA clusters at once
   // (measured, graph replay, d = 896, d_ff = 4864: M = 16 / 64 take 7.2 /

@@ -135,12 +135,12 @@ def test_skinny_cluster_and_stream_k_modes(cluster, monkeypatch):
 def test_cluster_mode_selection():
     # Small weights (<= 32 MB) run the skinny kernel in the largest clusters
     # that all fit at once, with no workspace: the small model's down
-    # projection in 8-CTA clusters (4 of them), its up projection in 2-CTA
+    # projection in 8-CTA clusters (7 groups of 128 columns), its up projection in 2-CTA
     # clusters (38 or 76 groups: too many for one wave of 4-CTA clusters).
     # The d = 4096 decode stays on stream-K.
     for M in (1, 16):
         p = swg.down_plan(M, 4864, 896, "bf16", "auto", 152)
-        assert p["path"] == "skinny" and p["workspace"] == 0 and p["grid"] == 4 * 8
+        assert p["path"] == "skinny" and p["workspace"] == 0 and p["grid"] == 7 * 8
         assert p["cluster"] == 8
         assert swg.down_workspace_bytes(M, 4864, 896, "bf16", "auto") == 0
         # (from 16 rows in 64-column groups: 76 clusters of 2)
