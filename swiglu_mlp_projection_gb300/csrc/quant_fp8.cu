@@ -46,6 +46,28 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return r;
 }
 
+// Eight bf16 -> eight e4m3 codes of v * inv.
+__device__ __forceinline__ uint2 quant8(const uint4& v, float inv) {
+  uint2 o;
+  o.x = e4m3x2(bf16_lo(v.x) * inv, bf16_hi(v.x) * inv) |
+        (e4m3x2(bf16_lo(v.y) * inv, bf16_hi(v.y) * inv) << 16);
+  o.y = e4m3x2(bf16_lo(v.z) * inv, bf16_hi(v.z) * inv) |
+        (e4m3x2(bf16_lo(v.w) * inv, bf16_hi(v.w) * inv) << 16);
+  return o;
+}
+
+__device__ __forceinline__ float amax8(const uint4& v, float m) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
+  return m;
+}
+
+// A row of up to kThreads * kRowItems groups of 8 values is held in registers:
+// every load of the row is issued before any is used, and the codes are made
+// from the same registers (K up to 16384 here).
+constexpr int kRowItems = 8;
+
 // One CTA per row of x [M, K] (bf16, K a multiple of 16): codes [M, K], scales [M].
 __global__ void __launch_bounds__(kThreads)
 quantize_rows_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ codes,
@@ -61,26 +83,31 @@ quantize_rows_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ codes
   tc::pdl_wait();
   const int64_t r = blockIdx.x;
   const uint4* src = reinterpret_cast<const uint4*>(x + r * K);
+  uint2* dst = reinterpret_cast<uint2*>(codes + r * K);
   const int64_t n8 = K / 8;
   float amax = 0.f;
-  for (int64_t i = threadIdx.x; i < n8; i += kThreads) {
-    const uint4 v = src[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if (n8 <= (int64_t)kThreads * kRowItems) {
+    uint4 v[kRowItems];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[q])), fabsf(bf16_hi(w[q]))));
-  }
-  amax = block_max(amax, red);
-  const float inv = amax > 0.f ? 448.0f / amax : 0.f;
-  uint2* dst = reinterpret_cast<uint2*>(codes + r * K);
-  for (int64_t i = threadIdx.x; i < n8; i += kThreads) {
-    const uint4 v = src[i];
-    uint2 o;
-    o.x = e4m3x2(bf16_lo(v.x) * inv, bf16_hi(v.x) * inv) |
-          (e4m3x2(bf16_lo(v.y) * inv, bf16_hi(v.y) * inv) << 16);
-    o.y = e4m3x2(bf16_lo(v.z) * inv, bf16_hi(v.z) * inv) |
-          (e4m3x2(bf16_lo(v.w) * inv, bf16_hi(v.w) * inv) << 16);
-    dst[i] = o;
+    for (int j = 0; j < kRowItems; ++j) {
+      const int64_t i = threadIdx.x + (int64_t)j * kThreads;
+      if (i < n8) v[j] = src[i];
+    }
+#pragma unroll
+    for (int j = 0; j < kRowItems; ++j)
+      if (threadIdx.x + (int64_t)j * kThreads < n8) amax = amax8(v[j], amax);
+    amax = block_max(amax, red);
+    const float inv = amax > 0.f ? 448.0f / amax : 0.f;
+#pragma unroll
+    for (int j = 0; j < kRowItems; ++j) {
+      const int64_t i = threadIdx.x + (int64_t)j * kThreads;
+      if (i < n8) dst[i] = quant8(v[j], inv);
+    }
+  } else {
+    for (int64_t i = threadIdx.x; i < n8; i += kThreads) amax = amax8(src[i], amax);
+    amax = block_max(amax, red);
+    const float inv = amax > 0.f ? 448.0f / amax : 0.f;
+    for (int64_t i = threadIdx.x; i < n8; i += kThreads) dst[i] = quant8(src[i], inv);
   }
   if (threadIdx.x == 0) scales[r] = amax > 0.f ? amax / 448.0f : 0.f;
 }
