@@ -73,7 +73,8 @@ constexpr uint32_t kChunkBytes = kCB * kBK * 2;       // one 64 x 64 bf16 weight
 constexpr uint32_t kSubBytes = 2 * kChunkBytes;       // gate box + up box = one MMA A tile
 constexpr uint32_t kPrefetchBytes = 512u * 1024u;     // weight bytes per CTA prefetched before the wait
 constexpr uint32_t kRingBudget = 200u * 1024u;        // shared memory for the stage ring
-constexpr int64_t kPlainCluster4MinM = 32;            // see plan_skinny (FP8: 16)
+constexpr int64_t kPlainCluster4MinM = 24;            // see plan_skinny
+constexpr int64_t kPlainCluster4MinMFp8 = 16;
 
 constexpr uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
   uint32_t r = lo;
@@ -832,12 +833,13 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   // in distributed shared memory instead of ~5 partial slots in L2 that one
   // CTA adds after everyone else is done, a tail that grows with M.
   // Measured, d_ff = 14336 -> d = 4096, calls back to back, stream-K vs
-  // 4-CTA clusters: M = 16: 25.2 / 27.8 us; 32: 29.0 / 28.4; 64: 33.5 /
-  // 29.7; 128: 42.3 / 31.9; 256: 62.6 / 37.3.  FP8: M = 16: 19.6 / 18.5;
-  // 64: 27.3 / 20.9.  (d = 8192 needs 64 groups, more than fit: stream-K.)
+  // 4-CTA clusters (without the pre-wait prefetch, below): M = 16: 25.3 /
+  // 25.4 us; 24: 28.2 / 25.9; 32: 29.1 / 26.1; 64: 33.5 / 27.3; 128: 42.4 /
+  // 29.7; 256: 62.7 / 35.8.  FP8: M = 16: 18.8 / 17.8; 64: 26.6 / 20.4.
+  // (d = 8192 needs 64 groups, more than fit: stream-K.)
   bool plain_cluster4 = false;
   if (plain && weight_bytes > kSkinnyClusterMaxWeightBytes &&
-      M >= (fp8 ? kPlainCluster4MinM / 2 : kPlainCluster4MinM) && tn.sk_nb < 0 &&
+      M >= (fp8 ? kPlainCluster4MinMFp8 : kPlainCluster4MinM) && tn.sk_nb < 0 &&
       tn.sk_cluster < 0 && skinny_plain_cluster4_fits(K, n_out, num_sms, cluster_caps)) {
     nb = 1;
     plain_cluster4 = true;
@@ -910,11 +912,12 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   if (forced == 1 || forced == 2 || forced == 4 || forced == 8)
     p.cluster = p.n_kb >= forced ? forced : 0;
   if (p.cluster) p.grid = (int)(p.n_cb * p.cluster);
-  // Cluster mode, up projection: no L2 prefetch before the dependency wait.
-  // With a few MB per call the prefetch only delays the first loads
-  // (measured, graph replay, d = 896: 6.8 / 9.7 us at M = 1 / 64 without it,
-  // 7.1 / 9.8 us with it).
-  if (p.cluster && !plain && tn.sk_prefetch_units < 0) p.prefetch_units = 0;
+  // Cluster mode: no L2 prefetch before the dependency wait (measured: the
+  // d = 896 up projection, graph replay, 6.8 / 9.7 us at M = 1 / 64 without
+  // it, 7.1 / 9.8 us with it; the d = 4096 down projection in 4-CTA
+  // clusters, back to back, 27.3 / 29.7 us at M = 64 / 128 without it, 29.8 /
+  // 31.9 us with it).
+  if (p.cluster && tn.sk_prefetch_units < 0) p.prefetch_units = 0;
   const int64_t per = p.units > 0 ? p.units / p.grid : 1;   // fewest units a CTA gets
   p.maxq = (int)((p.n_kb + per - 1) / (per > 0 ? per : 1) + 1);
   p.counters_bytes = ((size_t)p.n_cb * sizeof(unsigned) + 255) / 256 * 256;

@@ -141,9 +141,9 @@ def test_dispatch_rule(cuda_lib):
     assert swg.down_plan(1, 14336, 4096, "bf16", "auto", 152)["skinny_max_m"] == 256
     assert swg.down_plan(1, 29568, 8192, "bf16", "auto", 152)["skinny_max_m"] == 128
     assert swg.down_plan(1, 4864, 896, "bf16", "auto", 152)["skinny_max_m"] == 256
-    # the down projection at d = 4096: stream-K up to 31 rows, 4-CTA clusters
-    # of 128-column groups from 32 on
-    for M, cl in [(16, 1), (31, 1), (32, 4), (256, 4)]:
+    # the down projection at d = 4096: stream-K up to 23 rows, 4-CTA clusters
+    # of 128-column groups from 24 on
+    for M, cl in [(16, 1), (23, 1), (24, 4), (256, 4)]:
         p = swg.down_plan(M, 14336, 4096, "bf16", "auto", 152)
         assert p["cluster"] == cl and (cl == 1) == (p["workspace"] > 0), (M, p)
     assert swg.plan(1, 512, 2048, "f32", "auto", 152)["path"] == "simt"
@@ -158,7 +158,7 @@ def test_down_projection_column_groups(cuda_lib, monkeypatch):
     # 256-column groups (11 partial slots at d = 4096) until their partial
     # sums pass 256 KB per group, then 128-column groups (6 slots)
     # (stream-K mode forced: at d = 4096 the down projection takes 4-CTA
-    # clusters from M = 32 on)
+    # clusters from M = 24 on)
     monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")
     assert swg.down_plan(16, 14336, 4096, "bf16", "skinny", 152)["slices"] == 11
     assert swg.down_plan(64, 14336, 4096, "bf16", "skinny", 152)["slices"] == 6

@@ -91,9 +91,9 @@ def test_down_projection_column_group_rule(cuda_lib):
         for d, d_ff in ((4096, 14336), (8192, 29568)):
             p = swg.down_plan(M, d_ff, d, "bf16", "skinny", 152)
             if p["cluster"] == 4:
-                # d = 4096 from M = 32 on: 4-CTA clusters of 128-column groups,
+                # d = 4096 from M = 24 on: 4-CTA clusters of 128-column groups,
                 # the four K quarters of a group meet on chip
-                assert d == 4096 and M >= 32 and p["workspace"] == 0
+                assert d == 4096 and M >= 24 and p["workspace"] == 0
                 assert p["grid"] == -(-d // 128) * 4 and p["slices"] == 4
                 continue
             _, _, n_kb2, units2, grid2 = geometry(M, d_ff, d, 2, True, 152)
