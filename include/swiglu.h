@@ -291,10 +291,12 @@ SWIGLU_API int swiglu_mlp(const void* x, const void* w_gate, const void* w_up,
  *     it; make that first call before any stream capture.
  *   - Limit: a call whose partial sums need more than
  *     SWIGLU_NOALLOC_SCRATCH_BYTES returns SWIGLU_ERR_WORKSPACE and enqueues
- *     nothing.  The need is slices x M x 2 x d_ff x 4 bytes, i.e. the
- *     `workspace` that swiglu_plan reports for SWIGLU_PATH_SIMT; on a
- *     152-SM GB300 the d = 4096, d_ff = 14336 decode calls need at most
- *     7.3 MB (M = 16).
+ *     nothing.  The need is slices x M x 2 x d_ff x 4 bytes, slices being
+ *     the split-K kernel's K slices (swiglu_plan reports them and this
+ *     `workspace` for SWIGLU_PATH_SIMT, except for the one-row calls that
+ *     swiglu_up serves with the SIMT path's cluster form, which this entry
+ *     point does not use); on a 152-SM GB300 the d = 4096, d_ff = 14336
+ *     decode calls need at most 7.3 MB (M = 16).
  *   - Sharing: every call on a device uses the same array, which keeps the
  *     last call's contents.  Nothing in it needs to start at zero (each call
  *     writes every partial it later reads), but calls that may overlap on
