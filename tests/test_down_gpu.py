@@ -181,3 +181,14 @@ def test_bulk_staged_final_sums_equal_l2_sums(shape, monkeypatch):
                                  raw(r[rows].contiguous()))
     assert compare(to64(outs[0])[rows], y64, s, "bf16", d_ff)["ok"]
     swg.check_device_status()
+
+
+def test_large_model_stream_k_with_bulk_final_sums():
+    # d_ff = 29568 -> d = 8192 at M = 64: stream-K mode (its 64 groups do not
+    # fit as 4-CTA clusters), 128-column groups, final sums staged in shared
+    # memory by bulk copies (the default above 16 rows); every column of
+    # rows from both halves of the call
+    M, d_ff, d = 64, 29568, 8192
+    p = swg.down_plan(M, d_ff, d)
+    assert p["path"] == "skinny" and p["cluster"] == 1 and p["workspace"] > 0
+    check(M, d_ff, d, "auto", seed=91, rows=np.array([0, 17, 40, 63]))
