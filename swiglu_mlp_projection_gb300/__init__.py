@@ -34,15 +34,32 @@ def _path_code(path):
 
 
 _LIB = None
+_TORCH = None            # torch, imported on first use
+_RAW_STREAM = None       # torch._C._cuda_getCurrentRawStream, where it exists
+_CUR_DEVICE = None       # torch._C._cuda_getDevice, where it exists
+
+
+def _torch():
+    global _TORCH, _RAW_STREAM, _CUR_DEVICE
+    if _TORCH is None:
+        import torch
+        _RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        _CUR_DEVICE = getattr(torch._C, "_cuda_getDevice", None)
+        _TORCH = torch
+    return _TORCH
 
 
 def _raw_stream(index):
     """torch's current stream on device `index`, as a raw cudaStream_t value."""
-    import torch
-    get = getattr(torch._C, "_cuda_getCurrentRawStream", None)
-    if get is not None:
-        return get(index)
+    torch = _TORCH or _torch()
+    if _RAW_STREAM is not None:
+        return _RAW_STREAM(index)
     return torch.cuda.current_stream(index).cuda_stream
+
+
+def _current_device():
+    torch = _TORCH or _torch()
+    return _CUR_DEVICE() if _CUR_DEVICE is not None else torch.cuda.current_device()
 
 
 def swiglu_up(x, w_gate, w_up, out=None, path="auto", workspace=None, stream=None,
@@ -58,8 +75,9 @@ def swiglu_up(x, w_gate, w_up, out=None, path="auto", workspace=None, stream=Non
     torch's current stream on x's device).
     """
     global _LIB
-    import torch
-    if not (x.is_cuda and w_gate.is_cuda and w_up.is_cuda):
+    torch = _TORCH or _torch()
+    index = x.get_device()
+    if index < 0 or w_gate.get_device() < 0 or w_up.get_device() < 0:
         raise ValueError("x, w_gate and w_up must be CUDA tensors")
     if not (x.is_contiguous() and w_gate.is_contiguous() and w_up.is_contiguous()):
         raise ValueError("x, w_gate and w_up must be contiguous")
@@ -79,7 +97,6 @@ def swiglu_up(x, w_gate, w_up, out=None, path="auto", workspace=None, stream=Non
         out = torch.empty((M, d_ff), dtype=x.dtype, device=x.device)
     elif out.shape != (M, d_ff) or out.dtype != x.dtype or not out.is_contiguous():
         raise ValueError("out must be a contiguous [M, d_ff] tensor of x's dtype")
-    index = x.device.index
     st = stream.cuda_stream if stream is not None else _raw_stream(index)
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
@@ -89,7 +106,7 @@ def swiglu_up(x, w_gate, w_up, out=None, path="auto", workspace=None, stream=Non
     args = (x.data_ptr(), w_gate.data_ptr(), w_up.data_ptr(), out.data_ptr(), M, d, d_ff, dt,
             _path_code(path), ws_ptr, ws_bytes, st)
     fn = _LIB.swiglu_up_ex if layout == "kn" else _LIB.swiglu_up_nk
-    if torch.cuda.current_device() != index:
+    if _current_device() != index:
         with torch.cuda.device(index):
             status = fn(*args)
     else:
@@ -100,8 +117,8 @@ def swiglu_up(x, w_gate, w_up, out=None, path="auto", workspace=None, stream=Non
 
 
 def _call(index, fn, *args):
-    import torch
-    if torch.cuda.current_device() != index:
+    torch = _TORCH or _torch()
+    if _current_device() != index:
         with torch.cuda.device(index):
             status = fn(*args)
     else:
