@@ -710,10 +710,11 @@ def other_configs(dev, peaks, l2, iters, oracle_leg=False, sampler=None):
             gbs = by / (ms * 1e-3) / 1e9
             tfs = fl / (ms * 1e-3) / 1e12
             key = "%s/M=%d" % (cfg.name, M)
+            dplan = swg.plan(M, cfg.d, cfg.d_ff, cfg.dtype, "auto", 0)   # as this GPU serves it
             entry = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "TFLOP/s": round(tfs, 2),
                      "graph_us": round(ms_graph * 1e3, 2),
                      "graph_GB/s": round(by / (ms_graph * 1e-3) / 1e9, 1),
-                     "path": swg.plan(M, cfg.d, cfg.d_ff, cfg.dtype, "auto")["path"]}
+                     "path": dplan["path"], "cluster": dplan["cluster"]}
             add_quantiles(entry, per)
             if sampler is not None:
                 # SM clock while this configuration ran (both timing passes):
@@ -881,7 +882,8 @@ def down_and_mlp(dev, peaks, l2, iters, sampler=None):
         fl = workload.down_flops(M, d_ff, d)
         e = {"us": round(ms * 1e3, 2), "GB/s": round(by / ms / 1e6, 1),
              "TFLOP/s": round(fl / ms / 1e9, 2),
-             "path": swg.down_plan(M, d_ff, d, "bf16", "auto")["path"]}
+             "path": swg.down_plan(M, d_ff, d, "bf16", "auto", 0)["path"],
+             "cluster": swg.down_plan(M, d_ff, d, "bf16", "auto", 0)["cluster"]}
         add_quantiles(e, per_call[-1])
         e["clocks"] = clocks_of(sampler, walls[-2], walls[-1])
         if e["path"] == "skinny":   # M FLOP per weight byte: below the ridge, HBM-bound

@@ -315,8 +315,14 @@ SWIGLU_API int swiglu_up_noalloc(const void* x, const void* w_gate, const void* 
 SWIGLU_API size_t swiglu_workspace_bytes(int64_t M, int64_t d, int64_t d_ff, int dtype,
                               int path);
 
-/* How a call would be served, for a device with `num_sms` SMs (host-only,
- * needs no GPU).  Pure function of its arguments. */
+/* How a call would be served.
+ *   num_sms > 0   for a device with `num_sms` SMs: host-only, needs no GPU,
+ *                 a pure function of its arguments (thread-block cluster
+ *                 capacities are estimated from the SM count).
+ *   num_sms == 0  on the current device, exactly as a call would be: its SM
+ *                 count and the cluster capacities it reports
+ *                 (cudaOccupancyMaxActiveClusters).  Needs a GPU; without
+ *                 one it returns SWIGLU_ERR_CUDA. */
 typedef struct {
   int path;              /* resolved swiglu_path                                */
   int64_t slices;        /* K slices of the split-K paths (1 for TC)            */
@@ -333,8 +339,9 @@ typedef struct {
   int64_t launches;      /* kernel launches one call enqueues                   */
   int64_t cluster;       /* CTAs per thread-block cluster of the main kernel
                             (1: none; 2-8: the skinny kernel's split-K
-                            clusters; 8: the SIMT path's cluster form;
-                            2: the TC path's CTA pairs)                      */
+                            clusters; 4-8: the SIMT path's cluster form, 8
+                            unless 8-CTA clusters would not all fit at once
+                            on the device; 2: the TC path's CTA pairs)       */
 } swiglu_plan_info;
 
 SWIGLU_API int swiglu_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, int path,

@@ -416,7 +416,8 @@ def down_workspace_bytes(M, d_ff, d, dtype="bf16", path="auto"):
 
 
 def down_plan(M, d_ff, d, dtype="bf16", path="auto", num_sms=152):
-    """How a down-projection call would be served (host-only)."""
+    """How a down-projection call would be served: host-only for a GPU with
+    ``num_sms`` SMs, or on the current device with ``num_sms=0``."""
     lib = _lib.load()
     info = _lib.PlanInfo()
     dt = BF16 if dtype in ("bf16", BF16) else F32
@@ -433,7 +434,8 @@ def workspace_bytes(M, d, d_ff, dtype="bf16", path="auto"):
 
 
 def plan(M, d, d_ff, dtype="bf16", path="auto", num_sms=152):
-    """How a call would be served on a GPU with ``num_sms`` SMs (host-only)."""
+    """How a call would be served: host-only for a GPU with ``num_sms`` SMs,
+    or on the current device with ``num_sms=0``."""
     lib = _lib.load()
     info = _lib.PlanInfo()
     dt = BF16 if dtype in ("bf16", BF16) else F32

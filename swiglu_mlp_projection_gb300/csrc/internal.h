@@ -60,14 +60,19 @@ cudaError_t launch_simt_partial(const void* x, const void* wg, const void* wu,
 // The cluster form of the SIMT path (M = 1, weights <= 32 MB, d <= 2048):
 // the K slices of a column block are one thread-block cluster that adds them
 // in distributed shared memory, in one launch with no workspace.  Returns the
-// cluster size (the K slices) for a call it serves, else 0.
-int simt_cluster_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, const Tuning& tn);
+// cluster size (the K slices, 4 ... 8) for a call it serves, else 0.
+// caps[S] (S = 4 ... 8): clusters of S CTAs of its 4-CTAs-per-SM form that
+// fit at once (simt_cluster_caps), or null to assume that 8-CTA clusters fit.
+constexpr int kSimtCapSlots = 9;
+int simt_cluster_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, const Tuning& tn,
+                      const int* caps = nullptr);
+cudaError_t simt_cluster_caps(int caps[kSimtCapSlots]);
 // Largest d for which AUTO prefers the cluster form for bf16 (at most 4 rows
 // of W per thread, so 4 CTAs fit per SM).
 constexpr int64_t kSimtClusterPreferMaxK = 1024;
 cudaError_t launch_simt_cluster(const void* x, const void* wg, const void* wu, void* h,
-                                int64_t M, int64_t d, int64_t d_ff, int dtype, bool packed,
-                                cudaStream_t st);
+                                int64_t M, int64_t d, int64_t d_ff, int dtype, int ks,
+                                bool packed, cudaStream_t st);
 
 // How the weights are stored:
 //   kWeightsKN      [K, n_out] row-major (the default);

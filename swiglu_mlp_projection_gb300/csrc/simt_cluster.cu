@@ -8,7 +8,8 @@
 // along the weights, and the K slices of a column block are added in a fixed
 // order), and applies SiLU * up only once they are complete, as that page's
 // slice-reduction pass does.  What changes is where the slices meet:
-//   * the S = 8 K slices of a column block are one thread-block cluster; each
+//   * the S K slices of a column block (S = 8, or 7 ... 4 where the S = 8
+//     clusters would not all fit at once) are one thread-block cluster; each
 //     CTA stores its partial sums into the shared memory of the cluster's
 //     rank 0 (distributed shared memory), and after one cluster barrier rank
 //     0 adds the S partials in rank (= k) order and applies the epilogue;
@@ -37,7 +38,8 @@ constexpr int kLanesPerRow = 8;                       // 8 x 16 B = one 128-byte
 constexpr int kGroups = kThreads / kLanesPerRow;      // 32 rows of W in flight per pass
 constexpr int kMaxRows = 8;                           // k rows per thread and matrix, at most
 constexpr int kMaxK = kGroups * kMaxRows;             // 256 k per CTA at most (d <= 2048)
-constexpr int kS = 8;                                 // CTAs per cluster (K slices)
+constexpr int kMaxS = 8;                              // CTAs per cluster (K slices), at most
+constexpr int kMinS = 4;
 constexpr int64_t kMaxWeightBytes = (int64_t)32 << 20;
 
 template <bool BF16>
@@ -53,11 +55,11 @@ __device__ __forceinline__ void unpack16(const uint4& v, float* f) {
   }
 }
 
-// grid.x = column blocks x kS (a cluster = the kS K slices of one column
+// grid.x = column blocks x KS (a cluster = the KS K slices of one column
 // block), grid.y = chunks of RC rows of x.  ROWS: k rows of W per thread
 // (kn <= 32 ROWS), all in flight at once.  One row of x keeps 4 CTAs (1024
 // threads) resident per SM, so that a call of 4 CTAs per SM runs in one wave.
-template <bool BF16, int RC, int ROWS>
+template <bool BF16, int RC, int ROWS, int KS>
 __global__ void __launch_bounds__(kThreads, (RC == 1 && ROWS <= 4) ? 4 : 2)
 simt_cluster_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
                     const void* __restrict__ wu_, void* __restrict__ h_, int M, int d,
@@ -68,12 +70,12 @@ simt_cluster_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
   __shared__ float red[kThreads / 32][RC][2][C];
   // rank 0 only: every slice's sums, written by their CTAs through
   // distributed shared memory
-  __shared__ __align__(16) float part[kS][RC][2][C];
+  __shared__ __align__(16) float part[KS][RC][2][C];
 
-  const int rank = (int)tc::cluster_ctarank();        // = blockIdx.x % kS
-  const int cb = blockIdx.x / kS;
+  const int rank = (int)tc::cluster_ctarank();        // = blockIdx.x % KS
+  const int cb = blockIdx.x / KS;
   const int row0 = blockIdx.y * RC;
-  const int k0 = (int)((int64_t)rank * d / kS), k1 = (int)((int64_t)(rank + 1) * d / kS);
+  const int k0 = (int)((int64_t)rank * d / KS), k1 = (int)((int64_t)(rank + 1) * d / KS);
   const int l8 = threadIdx.x & 7, grp = threadIdx.x >> 3;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int col = cb * C + l8 * VEC;
@@ -180,7 +182,7 @@ simt_cluster_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
   tc::cluster_sync_all();   // every slice's sums are in rank 0's shared memory
   if (rank != 0) return;    // nobody reads the other CTAs' shared memory
 
-  // Rank 0 adds the kS slices in rank (= k) order and applies the epilogue.
+  // Rank 0 adds the KS slices in rank (= k) order and applies the epilogue.
   constexpr int kChunks = RC * C / 4;
   for (int q = threadIdx.x; q < kChunks; q += kThreads) {
     const int r = q / (C / 4), c = (q - r * (C / 4)) * 4;
@@ -188,7 +190,7 @@ simt_cluster_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
     if (row >= M || j >= d_ff) continue;   // d_ff is a multiple of 4: chunks are whole
     float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
 #pragma unroll
-    for (int s = 0; s < kS; ++s) {
+    for (int s = 0; s < KS; ++s) {
       const float4 a = *reinterpret_cast<const float4*>(&part[s][r][0][c]);
       const float4 b = *reinterpret_cast<const float4*>(&part[s][r][1][c]);
       g.x += a.x; g.y += a.y; g.z += a.z; g.w += a.w;
@@ -207,41 +209,83 @@ simt_cluster_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
   }
 }
 
-template <bool BF16, int RC, int ROWS>
-cudaError_t launch_rows(const void* x, const void* wg, const void* wu, void* h, int64_t M,
-                        int64_t d, int64_t d_ff, bool packed, cudaStream_t st) {
+template <bool BF16, int RC, int ROWS, int KS>
+cudaLaunchConfig_t launch_config(int64_t M, int64_t d_ff, cudaLaunchAttribute* attr,
+                                 cudaStream_t st) {
   constexpr int C = kLanesPerRow * (BF16 ? 8 : 4);
   const int64_t n_cb = (d_ff + C - 1) / C;
-  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = kS;
+  attr[1].val.clusterDim.x = KS;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(n_cb * kS), (unsigned)((M + RC - 1) / RC));
+  cfg.gridDim = dim3((unsigned)(n_cb * KS), (unsigned)((M + RC - 1) / RC));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, simt_cluster_kernel<BF16, RC, ROWS>, x, wg, wu, h, (int)M,
+  return cfg;
+}
+
+template <bool BF16, int RC, int ROWS, int KS>
+cudaError_t launch_rows(const void* x, const void* wg, const void* wu, void* h, int64_t M,
+                        int64_t d, int64_t d_ff, bool packed, cudaStream_t st) {
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = launch_config<BF16, RC, ROWS, KS>(M, d_ff, attr, st);
+  return cudaLaunchKernelEx(&cfg, simt_cluster_kernel<BF16, RC, ROWS, KS>, x, wg, wu, h, (int)M,
                             (int)d, (int)d_ff, packed ? 1 : 0);
+}
+
+// ROWS from the largest slice's k.  Clusters of fewer than 8 slices are
+// planned only where a slice holds at most 4 rows per thread (slice_fits).
+template <bool BF16, int RC, int KS>
+cudaError_t launch_ks(const void* x, const void* wg, const void* wu, void* h, int64_t M,
+                      int64_t d, int64_t d_ff, bool packed, cudaStream_t st) {
+  const int64_t kn = (d + KS - 1) / KS;
+  if (kn <= 2 * kGroups) return launch_rows<BF16, RC, 2, KS>(x, wg, wu, h, M, d, d_ff, packed, st);
+  if (kn <= 4 * kGroups) return launch_rows<BF16, RC, 4, KS>(x, wg, wu, h, M, d, d_ff, packed, st);
+  if constexpr (KS == kMaxS)
+    return launch_rows<BF16, RC, 8, KS>(x, wg, wu, h, M, d, d_ff, packed, st);
+  return cudaErrorInvalidValue;
 }
 
 template <bool BF16, int RC>
 cudaError_t launch_rc(const void* x, const void* wg, const void* wu, void* h, int64_t M,
-                      int64_t d, int64_t d_ff, bool packed, cudaStream_t st) {
-  const int64_t kn = (d + kS - 1) / kS;    // k of the largest slice
-  if (kn <= 2 * kGroups) return launch_rows<BF16, RC, 2>(x, wg, wu, h, M, d, d_ff, packed, st);
-  if (kn <= 4 * kGroups) return launch_rows<BF16, RC, 4>(x, wg, wu, h, M, d, d_ff, packed, st);
-  return launch_rows<BF16, RC, 8>(x, wg, wu, h, M, d, d_ff, packed, st);
+                      int64_t d, int64_t d_ff, int ks, bool packed, cudaStream_t st) {
+  switch (ks) {
+    case 8: return launch_ks<BF16, RC, 8>(x, wg, wu, h, M, d, d_ff, packed, st);
+    case 7: return launch_ks<BF16, RC, 7>(x, wg, wu, h, M, d, d_ff, packed, st);
+    case 6: return launch_ks<BF16, RC, 6>(x, wg, wu, h, M, d, d_ff, packed, st);
+    case 5: return launch_ks<BF16, RC, 5>(x, wg, wu, h, M, d, d_ff, packed, st);
+    case 4: return launch_ks<BF16, RC, 4>(x, wg, wu, h, M, d, d_ff, packed, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Can a cluster of ks slices serve a d-deep sum?  8 slices take up to 8 rows
+// of W per thread (kMaxK = 256 k per slice); fewer slices only up to 4 rows,
+// so that 4 CTAs still fit per SM.
+bool slice_fits(int64_t d, int ks) {
+  if (ks < kMinS || ks > kMaxS || d < ks) return false;
+  const int64_t kn = (d + ks - 1) / ks;
+  return ks == kMaxS ? kn <= kMaxK : kn <= 4 * kGroups;
+}
+
+template <int KS>
+cudaError_t cap_of(int* n) {
+  cudaLaunchAttribute attr[2];
+  // one cluster's grid: the occupancy query asks how many such clusters fit
+  cudaLaunchConfig_t cfg = launch_config<true, 1, 4, KS>(1, (int64_t)kLanesPerRow * 8, attr, 0);
+  return cudaOccupancyMaxActiveClusters(n, simt_cluster_kernel<true, 1, 4, KS>, &cfg);
 }
 
 }  // namespace
 
-int simt_cluster_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, const Tuning& tn) {
+int simt_cluster_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, const Tuning& tn,
+                      const int* caps) {
   if (tn.simt_cluster == 0) return 0;
   const int64_t e = dtype == 1 ? 2 : 4;
   const int C = kLanesPerRow * (dtype == 1 ? 8 : 4);
@@ -250,19 +294,39 @@ int simt_cluster_plan(int64_t M, int64_t d, int64_t d_ff, int dtype, const Tunin
   // four rows double or quadruple the accumulators, which halves the CTAs an
   // SM holds, and the call then needs two waves (bf16 d = 896: 12.4 / 15.4
   // us at M = 2 / 4 against 8.1 at M = 1).
-  const bool fits = M == 1 && d >= kS && (d + kS - 1) / kS <= kMaxK && d_ff > 0 &&
-                    2 * d * d_ff * e <= kMaxWeightBytes &&
-                    (d_ff + C - 1) / C * kS <= (int64_t)INT32_MAX;
-  return fits ? kS : 0;
+  if (M != 1 || d_ff <= 0 || 2 * d * d_ff * e > kMaxWeightBytes) return 0;
+  const int64_t n_cb = (d_ff + C - 1) / C;
+  if (n_cb * kMaxS > (int64_t)INT32_MAX) return 0;
+  if (tn.simt_cluster >= kMinS && tn.simt_cluster <= kMaxS)
+    return slice_fits(d, tn.simt_cluster) ? tn.simt_cluster : 0;
+  // The largest cluster whose n_cb clusters all run at once, 4 CTAs per SM
+  // (caps[S]: clusters of S CTAs that fit).  A cluster of 8 must find 8 free
+  // CTA slots in one GPC, and 4 per SM do not pack into whole 8-CTA clusters
+  // on every GPC: e.g. the d = 896 model's 76 column blocks.
+  if (caps)
+    for (int ks = kMaxS; ks >= kMinS; --ks)
+      if (slice_fits(d, ks) && (d + ks - 1) / ks <= 4 * kGroups && n_cb <= caps[ks]) return ks;
+  return slice_fits(d, kMaxS) ? kMaxS : 0;
+}
+
+cudaError_t simt_cluster_caps(int caps[kSimtCapSlots]) {
+  for (int i = 0; i < kSimtCapSlots; ++i) caps[i] = 0;
+  cudaError_t e;
+  if ((e = cap_of<8>(&caps[8])) != cudaSuccess) return e;
+  if ((e = cap_of<7>(&caps[7])) != cudaSuccess) return e;
+  if ((e = cap_of<6>(&caps[6])) != cudaSuccess) return e;
+  if ((e = cap_of<5>(&caps[5])) != cudaSuccess) return e;
+  return cap_of<4>(&caps[4]);
 }
 
 cudaError_t launch_simt_cluster(const void* x, const void* wg, const void* wu, void* h,
-                                int64_t M, int64_t d, int64_t d_ff, int dtype, bool packed,
-                                cudaStream_t st) {
+                                int64_t M, int64_t d, int64_t d_ff, int dtype, int ks,
+                                bool packed, cudaStream_t st) {
   if (M == 0 || d_ff == 0) return cudaSuccess;
   if (M != 1) return cudaErrorInvalidValue;   // simt_cluster_plan serves one row
-  return dtype == 1 ? launch_rc<true, 1>(x, wg, wu, h, M, d, d_ff, packed, st)
-                    : launch_rc<false, 1>(x, wg, wu, h, M, d, d_ff, packed, st);
+  if (!slice_fits(d, ks)) return cudaErrorInvalidValue;
+  return dtype == 1 ? launch_rc<true, 1>(x, wg, wu, h, M, d, d_ff, ks, packed, st)
+                    : launch_rc<false, 1>(x, wg, wu, h, M, d, d_ff, ks, packed, st);
 }
 
 }  // namespace swg

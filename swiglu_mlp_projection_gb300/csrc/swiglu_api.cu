@@ -45,6 +45,7 @@ struct DeviceInfo {
   int num_sms = 0;
   int max_pairs = 0;            // 2-CTA clusters of the tile kernel that fit at once
   int sk_caps[4] = {0, 0, 0, 0};   // clusters of 2, 4, 8 skinny CTAs that fit at once
+  int simt_caps[kSimtCapSlots] = {};   // clusters of S SIMT-cluster CTAs that fit at once
   int cc_major = 0, cc_minor = 0;
   cudaMemPool_t pool = nullptr;
   unsigned* status = nullptr;   // device address of g_device_status
@@ -77,6 +78,8 @@ int current_device(int* dev_out, DeviceInfo* out) {
         return cuda_fail(e, "cudaOccupancyMaxActiveClusters(tile kernel)");
       if ((e = skinny_cluster_caps(di.sk_caps)) != cudaSuccess)
         return cuda_fail(e, "cudaOccupancyMaxActiveClusters(skinny kernel)");
+      if ((e = simt_cluster_caps(di.simt_caps)) != cudaSuccess)
+        return cuda_fail(e, "cudaOccupancyMaxActiveClusters(SIMT cluster kernel)");
     }
     di.ready = true;
   }
@@ -489,7 +492,7 @@ struct Plan {
 // nk: the weights are [n_out, K] (served by the tensor-core paths only).
 int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, int num_sms,
               int max_pairs, Plan* p, bool fp8 = false, const int* sk_caps = nullptr,
-              bool nk = false) {
+              bool nk = false, const int* simt_caps = nullptr) {
   int rp = 0;
   int st = resolve_path(op, M, K, n_out, dtype, path, &rp, num_sms, sk_caps);
   if (st != SWIGLU_OK) return st;
@@ -499,7 +502,7 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
   // 896 / 1024 at M = 1: 3.2 / 6.6 / 4.6 us against 4.2 / 7.0 / 6.4 us; at
   // d = 2048 it trails, 10.2 against 9.8 us).
   if (path == SWIGLU_PATH_AUTO && op == kOpUp && dtype == SWIGLU_BF16 && !fp8 && !nk &&
-      simt_cluster_plan(M, K, n_out, dtype, tn) && K <= kSimtClusterPreferMaxK)
+      simt_cluster_plan(M, K, n_out, dtype, tn, simt_caps) && K <= kSimtClusterPreferMaxK)
     rp = SWIGLU_PATH_SIMT;
   *p = Plan{};
   p->path = rp;
@@ -510,7 +513,7 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
     p->simt = plan_simt(M, K, n_out, dtype, num_sms, tn);
     if (p->simt.slices > kMaxGridYZ || p->simt.row_chunks > kMaxGridYZ)
       return fail(SWIGLU_ERR_UNSUPPORTED, "shape exceeds the grid limits of the SIMT path");
-    p->simt.cluster = simt_cluster_plan(M, K, n_out, dtype, tn);
+    p->simt.cluster = simt_cluster_plan(M, K, n_out, dtype, tn, simt_caps);
     if (p->simt.cluster) {
       // one launch: K slices in clusters of CTAs, no workspace
       const int64_t cols = dtype == SWIGLU_BF16 ? 64 : 32;
@@ -581,7 +584,7 @@ int run(const Call& c) {
   // FP8: the GEMM kernels see each row of e4m3 codes as K / 2 byte pairs
   const int64_t Kg = c.fp8 ? c.K / 2 : c.K;
   if ((v = make_plan(c.op, c.M, Kg, c.n_out, c.dtype, c.path, di.num_sms, di.max_pairs, &p,
-                     c.fp8, di.sk_caps, c.wlayout == kWeightsNK)) != SWIGLU_OK)
+                     c.fp8, di.sk_caps, c.wlayout == kWeightsNK, di.simt_caps)) != SWIGLU_OK)
     return v;
   if (c.fp8 && p.path == SWIGLU_PATH_SIMT && c.K > 0)
     return fail(SWIGLU_ERR_UNSUPPORTED, "FP8 weights are served by the tensor-core paths only");
@@ -704,7 +707,7 @@ int run(const Call& c) {
   }
   const Fp8Scales* fsp = fp8_prefix ? &fs : nullptr;
   if (p.path == SWIGLU_PATH_SIMT && p.simt.cluster) {
-    e = launch_simt_cluster(c.x, c.wa, c.wb, c.out, c.M, c.K, c.n_out, c.dtype,
+    e = launch_simt_cluster(c.x, c.wa, c.wb, c.out, c.M, c.K, c.n_out, c.dtype, p.simt.cluster,
                             c.wlayout == kWeightsPacked, st);
   } else if (p.path == SWIGLU_PATH_SIMT && p.simt.fused) {
     e = launch_simt_partial(c.x, c.wa, c.wb, part, c.M, c.K, c.n_out, c.dtype, p.simt, st,
@@ -1086,7 +1089,7 @@ size_t swiglu_workspace_bytes(int64_t M, int64_t d, int64_t d_ff, int dtype, int
   if (current_device(&dev, &di) != SWIGLU_OK) return 0;
   Plan p;
   if (make_plan(kOpUp, M, d, d_ff, dtype, path, di.num_sms, di.max_pairs, &p, false,
-                di.sk_caps) != SWIGLU_OK)
+                di.sk_caps, false, di.simt_caps) != SWIGLU_OK)
     return 0;
   return p.workspace;
 }
@@ -1103,20 +1106,35 @@ size_t swiglu_down_workspace_bytes(int64_t M, int64_t d_ff, int64_t d, int dtype
   return p.workspace;
 }
 
+// num_sms > 0: host-only, for a device with that many SMs (cluster
+// capacities estimated from it).  num_sms == 0: the current device, with the
+// SM count and cluster capacities a call would use.
 static int plan_common(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path,
                        int num_sms, swiglu_plan_info* out) {
   if (!out) return fail(SWIGLU_ERR_INVALID_ARG, "null output");
   if (dtype != SWIGLU_F32 && dtype != SWIGLU_BF16) return fail(SWIGLU_ERR_INVALID_ARG, "unknown dtype %d", dtype);
-  if (M < 0 || K < 0 || n_out < 0 || num_sms <= 0) return fail(SWIGLU_ERR_INVALID_ARG, "negative size or SM count");
+  if (M < 0 || K < 0 || n_out < 0 || num_sms < 0) return fail(SWIGLU_ERR_INVALID_ARG, "negative size or SM count");
   Plan p;
-  int v = make_plan(op, M, K, n_out, dtype, path, num_sms, num_sms / 2, &p);
+  int v;
+  const int* sk_caps = nullptr;
+  DeviceInfo di;
+  if (num_sms == 0) {
+    int dev = 0;
+    if ((v = current_device(&dev, &di)) != SWIGLU_OK) return v;
+    num_sms = di.num_sms;
+    sk_caps = di.sk_caps;
+    v = make_plan(op, M, K, n_out, dtype, path, di.num_sms, di.max_pairs, &p, false, sk_caps,
+                  false, di.simt_caps);
+  } else {
+    v = make_plan(op, M, K, n_out, dtype, path, num_sms, num_sms / 2, &p);
+  }
   if (v != SWIGLU_OK) return v;
   out->path = p.path;
   out->slices = p.slices;
   out->grid = p.grid;
   out->row_chunk = p.path == SWIGLU_PATH_SIMT ? p.simt.row_chunk : 0;
   out->workspace = (int64_t)p.workspace;
-  out->skinny_max_m = skinny_max_m(op, K, n_out, num_sms, nullptr);
+  out->skinny_max_m = skinny_max_m(op, K, n_out, num_sms, sk_caps);
   out->launches = p.launches;
   out->cluster = p.cluster;
   return SWIGLU_OK;

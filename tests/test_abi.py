@@ -71,8 +71,8 @@ def test_plan_covers_all_columns_rows_and_k(cuda_lib, dtype):
         vec = 8 if dtype == "bf16" else 4
         e = 2 if dtype == "bf16" else 4
         if p["cluster"] > 1:
-            # the cluster form: 8 K slices per cluster, 128-byte column
-            # blocks, one launch, no workspace
+            # the cluster form: 8 K slices per cluster on the host plan,
+            # 128-byte column blocks, one launch, no workspace
             assert M == 1 and 8 <= d <= 2048 and 2 * d * d_ff * e <= 32 << 20
             assert p["slices"] == p["cluster"] == 8
             assert p["grid"] == -(-d_ff // (8 * vec)) * 8
@@ -100,6 +100,26 @@ def test_simt_cluster_form_selection(cuda_lib, monkeypatch):
     monkeypatch.setenv("SWIGLU_SIMT_CLUSTER", "0")
     p = swg.plan(1, 512, 2048, "f32", "simt", 152)
     assert p["cluster"] == 1 and p["workspace"] > 0
+
+
+@pytest.mark.parametrize("ks", [4, 5, 6, 7, 8])
+def test_simt_cluster_sizes(cuda_lib, monkeypatch, ks):
+    # SWIGLU_SIMT_CLUSTER=S forces clusters of S K slices.  Fewer than 8 are
+    # served only where a slice holds at most 4 rows of W per thread (128 k);
+    # 8 slices up to 256 k.  Otherwise the call keeps the split-K kernel.
+    monkeypatch.setenv("SWIGLU_SIMT_CLUSTER", str(ks))
+    for (d, d_ff, dtype) in [(512, 2048, "f32"), (896, 4864, "bf16"), (520, 264, "bf16"),
+                             (2048, 1024, "bf16"), (8, 8, "f32"), (5, 8, "f32")]:
+        kn = -(-d // ks)
+        fits = d >= ks and (kn <= 256 if ks == 8 else kn <= 128)
+        p = swg.plan(1, d, d_ff, dtype, "simt", 152)
+        vec = 8 if dtype == "bf16" else 4
+        if fits:
+            assert p["cluster"] == p["slices"] == ks, (d, d_ff, dtype, p)
+            assert p["grid"] == -(-d_ff // (8 * vec)) * ks
+            assert p["workspace"] == 0 and p["launches"] == 1
+        else:
+            assert p["cluster"] == 1 and p["workspace"] > 0, (d, d_ff, dtype, p)
 
 
 def test_plan_reports_cluster_size(cuda_lib):
@@ -201,7 +221,16 @@ def test_plan_rejects_bad_arguments(cuda_lib):
     with pytest.raises(swg.SwiGLUError):
         swg.plan(1, 8, 8, "bf16", 17, 152)
     with pytest.raises(swg.SwiGLUError):
-        swg.plan(1, 8, 8, "bf16", "auto", 0)
+        swg.plan(1, 8, 8, "bf16", "auto", -1)
+
+
+def test_device_plan_needs_a_device(cuda_lib):
+    # num_sms = 0 plans on the current device; without a GPU that is an error
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(swg.SwiGLUError):
+        swg.plan(1, 896, 4864, "bf16", "auto", 0)
 
 
 def test_entry_point_validates_before_touching_the_device(cuda_lib):

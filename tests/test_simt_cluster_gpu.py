@@ -39,11 +39,47 @@ def test_cluster_form_matches_oracle(dtype, seed, shape):
     M = 1
     d, d_ff = shape
     assert swg.plan(M, d, d_ff, dtype, "simt")["cluster"] == 8
+    # on the device: 8 slices, or fewer where 8-CTA clusters would not all fit
+    assert swg.plan(M, d, d_ff, dtype, "simt", 0)["cluster"] in (4, 5, 6, 7, 8)
     x, wg, wu = inputs.make_inputs(M, d, d_ff, dtype, seed=seed * 7 + d)
     h = run(x, wg, wu)
     h64, _, s = oracle_h(x, wg, wu, dtype)
     res = compare(h.cpu().double().numpy(), h64, s, dtype, d)
     assert res["ok"], (dtype, M, shape, res)
+
+
+@pytest.mark.parametrize("ks", [4, 5, 6, 7, 8])
+@pytest.mark.parametrize("dtype,shape", [("f32", (512, 2048)), ("bf16", (512, 2048)),
+                                         ("bf16", (520, 264)), ("bf16", (896, 4864)),
+                                         ("f32", (24, 40))])
+def test_every_cluster_size_matches_oracle(dtype, shape, ks, monkeypatch):
+    # SWIGLU_SIMT_CLUSTER=S forces S K slices per cluster where a slice holds
+    # at most 4 rows of W per thread (8 slices: 8 rows)
+    d, d_ff = shape
+    monkeypatch.setenv("SWIGLU_SIMT_CLUSTER", str(ks))
+    kn = -(-d // ks)
+    if not (kn <= 256 if ks == 8 else kn <= 128):
+        assert swg.plan(1, d, d_ff, dtype, "simt", 0)["cluster"] == 1
+        return
+    p = swg.plan(1, d, d_ff, dtype, "simt", 0)
+    assert p["cluster"] == p["slices"] == ks and p["workspace"] == 0
+    x, wg, wu = inputs.make_inputs(1, d, d_ff, dtype, seed=ks + d)
+    h = run(x, wg, wu)
+    h64, _, s = oracle_h(x, wg, wu, dtype)
+    res = compare(h.cpu().double().numpy(), h64, s, dtype, d)
+    assert res["ok"], (dtype, shape, ks, res)
+    h2 = run(x, wg, wu)
+    view = torch.int16 if dtype == "bf16" else torch.int32
+    assert torch.equal(h.view(view), h2.view(view))      # same bits every run
+
+
+def test_small_model_clusters_fit_at_once():
+    # the d = 896 model's 76 column blocks: the device plan takes the largest
+    # cluster whose 76 clusters all run at once (on GB300, 4 CTAs per SM hold
+    # 74 clusters of 8 but 81 of 7)
+    p = swg.plan(1, 896, 4864, "bf16", "auto", 0)
+    assert p["path"] == "simt" and p["cluster"] in (7, 8)
+    assert p["grid"] == 76 * p["cluster"] and p["workspace"] == 0
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
