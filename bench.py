@@ -566,7 +566,7 @@ def run_ours(args):
         xs_sampler.start()
         extra = other_configs(dev, peaks, l2, args.extra_iters, oracle_leg, xs_sampler)
         next_rows = down_and_mlp(dev, peaks, l2, args.extra_iters, xs_sampler)
-        fp8_rows = fp8_configs(dev, peaks, args.extra_iters, xs_sampler)
+        fp8_rows = fp8_configs(dev, peaks, l2, args.extra_iters, xs_sampler)
         xs_sampler.stop()
 
     if rank == 0:
@@ -750,10 +750,16 @@ def clocks_of(sampler, w0, w1):
     return {"sm_mhz": cs["sm_mhz"], "reasons": cs["reasons"], "samples": cs.get("samples", 0)}
 
 
-def fp8_configs(dev, peaks, iters, sampler=None):
+def copies_for(l2, nbytes):
+    """Weight copies rotated per call so that a call's weights were last read
+    at least 3 L2 capacities ago."""
+    return max(2, math.ceil(3 * l2 / nbytes))
+
+
+def fp8_configs(dev, peaks, l2, iters, sampler=None):
     """The FP8 (e4m3) up projection at d=4096, d_ff=14336: the decode sweep
-    and the prefill call, back to back with 2 weight copies (117 MB each,
-    larger than L2); then the FP8 down projection and the FP8 MLP (both
+    and the prefill call, back to back with weight copies rotated per call
+    (copies_for); then the FP8 down projection and the FP8 MLP (both
     projections, with the residual) at M = 1, 16, 4096.  GB/s counts fp8_bytes; TFLOP/s is against the FP8
     dense peak taken as 2x the measured bf16 peak (the nominal FP8 : BF16
     ratio, 4.5 : 2.25 PFLOP/s)."""
@@ -763,7 +769,8 @@ def fp8_configs(dev, peaks, iters, sampler=None):
     d, d_ff = D, D_FF
     _, wg, wu = inputs.make_inputs(1, d, d_ff, "bf16", seed=0)
     wgd, wud = wg.to(dev), wu.to(dev)
-    qs = [swg.quantize_weights_fp8(wgd, wud) for _ in range(2)]
+    nq = copies_for(l2, 2 * d * d_ff)
+    qs = [swg.quantize_weights_fp8(wgd, wud) for _ in range(nq)]
     del wg, wu, wgd, wud
     torch.cuda.synchronize(dev)
     out = {}
@@ -772,17 +779,17 @@ def fp8_configs(dev, peaks, iters, sampler=None):
         x = inputs.make_inputs(M, d, 8, "bf16", seed=M, x_only=True)[0].to(dev)
         h = torch.empty(M, d_ff, dtype=torch.bfloat16, device=dev)
         for i in range(3):
-            swg.swiglu_up_fp8(x, qs[i % 2], out=h)
+            swg.swiglu_up_fp8(x, qs[i % nq], out=h)
         torch.cuda.synchronize(dev)
         w0 = time.time()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for i in range(iters):
-            swg.swiglu_up_fp8(x, qs[i % 2], out=h)
+            swg.swiglu_up_fp8(x, qs[i % nq], out=h)
         e1.record()
         torch.cuda.synchronize(dev)
         ms = e0.elapsed_time(e1) / iters
-        per = timed_reps(lambda i: swg.swiglu_up_fp8(x, qs[i % 2], out=h), iters)
+        per = timed_reps(lambda i: swg.swiglu_up_fp8(x, qs[i % nq], out=h), iters)
         w1 = time.time()
         by = workload.fp8_bytes(M, d, d_ff)
         fl = workload.flops(M, d, d_ff)
@@ -800,7 +807,8 @@ def fp8_configs(dev, peaks, iters, sampler=None):
     # the FP8 down projection and the whole FP8 MLP (both projections e4m3)
     _, wd, _ = inputs.make_inputs(1, d_ff, d, "bf16", seed=1)
     wdd = wd.to(dev)
-    qds = [swg.quantize_weight_fp8(wdd) for _ in range(2)]
+    nqd = copies_for(l2, d * d_ff)
+    qds = [swg.quantize_weight_fp8(wdd) for _ in range(nqd)]
     del wd, wdd
     for M in (1, 16, 4096):
         x = inputs.make_inputs(M, d, 8, "bf16", seed=M, x_only=True)[0].to(dev)
@@ -808,10 +816,10 @@ def fp8_configs(dev, peaks, iters, sampler=None):
         y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
         swg.swiglu_up_fp8(x, qs[0], out=hb)
         for name, fn, by, fl in (
-                ("fp8_down_d4096", lambda i: swg.swiglu_down_fp8(hb, qds[i % 2], residual=x, out=y),
+                ("fp8_down_d4096", lambda i: swg.swiglu_down_fp8(hb, qds[i % nqd], residual=x, out=y),
                  workload.fp8_down_bytes(M, d_ff, d), workload.down_flops(M, d_ff, d)),
-                ("fp8_mlp_d4096", lambda i: (swg.swiglu_up_fp8(x, qs[i % 2], out=hb),
-                                             swg.swiglu_down_fp8(hb, qds[i % 2], residual=x, out=y)),
+                ("fp8_mlp_d4096", lambda i: (swg.swiglu_up_fp8(x, qs[i % nq], out=hb),
+                                             swg.swiglu_down_fp8(hb, qds[i % nqd], residual=x, out=y)),
                  workload.fp8_bytes(M, d, d_ff) + workload.fp8_down_bytes(M, d_ff, d),
                  workload.flops(M, d, d_ff) + workload.down_flops(M, d_ff, d))):
             for i in range(3):
@@ -849,7 +857,7 @@ def down_and_mlp(dev, peaks, l2, iters, sampler=None):
     d, d_ff = D, D_FF
     _, wd, _ = inputs.make_inputs(1, d_ff, d, "bf16", seed=1)
     _, wg, wu = inputs.make_inputs(1, d, d_ff, "bf16", seed=0)
-    n_copies = 2
+    n_copies = copies_for(l2, 2 * d * d_ff)   # the down projection's weights alone
     wds = [wd.to(dev) for _ in range(n_copies)]
     wgs = [(wg.to(dev), wu.to(dev)) for _ in range(n_copies)]
     del wd, wg, wu

@@ -864,17 +864,20 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   p.l2_promo = tn.sk_promo >= 0 ? tn.sk_promo : 128;
   p.hint = tn.sk_hint >= 0 ? tn.sk_hint : 1;
   // Bulk-staged final sums (measured, calls back to back): the down
-  // projection at M > 16 gains 1-4 % (d = 4096, M = 128: 44.4 -> 42.4 us;
-  // d = 8192, M = 32: 82.1 -> 80.1 us); at M <= 16 and for the up projection,
-  // whose final sums are short, it is within noise or up to 2 % slower.
-  p.bulk = tn.sk_bulk >= 0 ? (tn.sk_bulk != 0) : (plain && M > 16);
-  // L2 prefetch budget per CTA (measured): 512 KB for SwiGLU; 256 KB for the
-  // down projection, whose column groups collect ~10 partial sums each (K is
-  // long), so the previous call's final reductions run longer and a larger
-  // prefetch slows them (512 KB measured ~5 % slower, none ~13 % slower);
-  // 256 KB for FP8 weights, where 512 KB is most of a CTA's share of the
-  // call (d = 4096, M = 1: 26.8 us at 256 KB, 29.4 us at 512 KB).
-  const uint32_t pf_bytes = (plain || fp8) ? kPrefetchBytes / 2 : kPrefetchBytes;
+  // projection from M = 16 gains 1-4 % (d = 4096, M = 16: 25.5 -> 24.8 us;
+  // M = 128: 44.4 -> 42.4 us; d = 8192, M = 32: 82.1 -> 80.1 us); at
+  // M <= 8 and for the up projection, whose final sums are short, it is
+  // within noise or up to 3 % slower.
+  p.bulk = tn.sk_bulk >= 0 ? (tn.sk_bulk != 0) : (plain && M >= 16);
+  // L2 prefetch budget per CTA (measured, d = 4096, calls back to back):
+  // 512 KB for bf16 SwiGLU; 256 KB for the down projection, whose column
+  // groups collect ~10 partial sums each (K is long), so the previous
+  // call's final reductions run longer and a larger prefetch slows them
+  // (M = 1: 21.5 us at 256 KB, 23.2 at 512 KB, 22.0 at 128 KB); 384 KB for
+  // the FP8 up projection (M = 1 / 16: 21.9 / 23.2 us against 22.6 / 24.0
+  // at 256 KB and 22.0 / 23.1 at 512 KB).
+  const uint32_t pf_bytes = plain ? kPrefetchBytes / 2
+                                  : (fp8 ? kPrefetchBytes / 4 * 3 : kPrefetchBytes);
   p.prefetch_units = tn.sk_prefetch_units >= 0 ? tn.sk_prefetch_units
                                                : (int)(pf_bytes / ((uint32_t)nb * kSubBytes));
   const int64_t sub_cols = plain ? 2 * kCB : kCB;
