@@ -126,8 +126,10 @@ SWIGLU_API int swiglu_up_ex(const void* x, const void* w_gate, const void* w_up,
  * Sums in f32 over k, the residual added to the f32 sum, one rounding to the
  * output type.  bf16 only (f32 returns SWIGLU_ERR_UNSUPPORTED), on the
  * tensor-core paths: M up to the skinny limit that swiglu_down_plan reports
- * (128 for weights above 32 MB, 256 for smaller ones) -> split-K skinny
- * kernel, larger M -> tile kernel (SWIGLU_PATH_SIMT is rejected).
+ * (256) -> split-K skinny kernel, larger M -> tile kernel (SWIGLU_PATH_SIMT
+ * is rejected).  Above 32 MB of weights the skinny kernel's stream-K form
+ * enqueues two kernels: one writes partial sums, the second adds them (in
+ * k order, the same bits as one kernel would give) and the residual.
  * d_ff == 0 gives y = residual (or 0).
  * Workspace, streams, determinism and errors as for swiglu_up.
  */
@@ -333,9 +335,7 @@ typedef struct {
                             weight sizes.  Up projection: 32, or 128 for
                             weights of 32 MB or less (where one row may take
                             the SIMT path's cluster form instead).  Down
-                            projection: 128, or 256 for weights of 32 MB or
-                            less and where 128-column groups fit as 4-CTA
-                            clusters                                         */
+                            projection: 256                                  */
   int64_t launches;      /* kernel launches one call enqueues                   */
   int64_t cluster;       /* CTAs per thread-block cluster of the main kernel
                             (1: none; 2-8: the skinny kernel's split-K

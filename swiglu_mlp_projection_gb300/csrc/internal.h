@@ -35,6 +35,8 @@ struct Tuning {
   int tile_pair = -1, tile_sk = -1, tile_sk_split = -1, tile_seq = -1, tile_band = -1;
   int simt_fused = -1;
   int sk_bulk = -1;   // skinny stream-K final sums staged by bulk copies (default on)
+  int sk_split = -1;  // skinny stream-K final sums in a second kernel (1) or by the
+                      // group's last CTA (0)
   int simt_cluster = -1;   // 0: never use the cluster form of the SIMT path
   // Test hook (SWIGLU_INJECT_OOM=1): every workspace the library would take
   // from its pool or its per-stream cache fails to allocate, so the call
@@ -121,6 +123,8 @@ struct SkinnyPlan {
   int prefetch_units;      // units each CTA prefetches into L2 before its dependency wait
   int cluster;             // cluster mode: CTAs per column group (0: stream-K)
   int bulk;                // stream-K: stage the final sums by bulk copies when possible
+  int split;               // stream-K: the kernel only writes partial sums; a second
+                           // kernel (launched with programmatic serialisation) adds them
   int64_t n_cb, n_kb;      // units: (nb x 64)-column groups, 64-deep k blocks
   int64_t units;           // n_cb * n_kb
   int grid;                // CTAs (<= SM count)

@@ -317,7 +317,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 // most 16 rows with its skinny kernel; the tcgen05 skinny kernel pays longer.
 constexpr int64_t kSkinnyMaxM = 32;
 constexpr int64_t kSkinnyMaxMSmall = 128;
-constexpr int64_t kSkinnyMaxMDown = 128;
+constexpr int64_t kSkinnyMaxMDown = 256;
 constexpr int64_t kSkinnyMaxMDownSmall = 256;
 constexpr int64_t kSkinnyMaxMDownCluster4 = 256;
 
@@ -340,9 +340,9 @@ enum Op { kOpUp = 0, kOpDown = 1 };
 
 // The measured crossovers (both paths forced, calls back to back, residual
 // included).  Stream-K mode: up projection 32 at d = 4096 and 8192 (d =
-// 4096: 39.4 vs 40.2 us at M = 32, 42.8 vs 40.4 at 48); down projection 128
-// (d = 4096: 44.6 vs 48.9 us at M = 128, 58.3 vs 49.4 at 192; d = 8192:
-// 94.9 vs 109 at 128).  Cluster mode, d = 896 (graph replay; 64-column
+// 4096: 39.4 vs 40.2 us at M = 32, 42.8 vs 40.4 at 48); down projection,
+// with its sums in a second kernel, all the 256 rows the kernel serves (d =
+// 8192: 83.3 vs 111.3 us at M = 128, 100.7 vs 143.9 at 256).  Cluster mode, d = 896 (graph replay; 64-column
 // groups from 16 rows): up projection 128 (9.97 vs 10.67 us at M = 128,
 // 11.84 vs 10.39 at 192); down projection all M the kernel
 // serves (13.9 vs 27.3 us at M = 256).  Down projection in 4-CTA clusters of
@@ -384,6 +384,7 @@ Tuning read_tuning() {
                           {"TILE_BAND", &t.tile_band},
                           {"SIMT_FUSED", &t.simt_fused},
                           {"SK_BULK", &t.sk_bulk},
+                          {"SK_SPLIT", &t.sk_split},
                           {"SIMT_CLUSTER", &t.simt_cluster},
                           {"INJECT_OOM", &t.inject_oom}};
     for (const Knob& k : knobs)
@@ -536,7 +537,7 @@ int make_plan(int op, int64_t M, int64_t K, int64_t n_out, int dtype, int path, 
     p->slices = p->skinny.cluster ? p->skinny.cluster : p->skinny.maxq;
     p->grid = p->skinny.grid;
     p->workspace = p->skinny.counters_bytes + p->skinny.part_bytes;
-    p->launches = 1;
+    p->launches = p->skinny.split ? 2 : 1;
     p->cluster = p->skinny.cluster ? p->skinny.cluster : 1;
   } else {
     p->tile = plan_tile(M, K, n_out, num_sms, plain, max_pairs, tn);

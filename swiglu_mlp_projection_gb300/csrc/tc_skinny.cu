@@ -73,8 +73,9 @@ constexpr uint32_t kChunkBytes = kCB * kBK * 2;       // one 64 x 64 bf16 weight
 constexpr uint32_t kSubBytes = 2 * kChunkBytes;       // gate box + up box = one MMA A tile
 constexpr uint32_t kPrefetchBytes = 512u * 1024u;     // weight bytes per CTA prefetched before the wait
 constexpr uint32_t kRingBudget = 200u * 1024u;        // shared memory for the stage ring
-constexpr int64_t kPlainCluster4MinM = 24;            // see plan_skinny
-constexpr int64_t kPlainCluster4MinMFp8 = 16;
+// Rows for which the down projection takes 4-CTA clusters (see plan_skinny)
+constexpr int64_t kPlainCluster4MinM = 33, kPlainCluster4MaxM = 64;
+constexpr int64_t kPlainCluster4MinMFp8 = 16, kPlainCluster4MaxMFp8 = 128;
 
 constexpr uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
   uint32_t r = lo;
@@ -113,6 +114,8 @@ struct SkArgs {
   int prefetch_units;   // units each CTA prefetches into L2 before the dependency wait
   int cluster;          // cluster mode: CTAs per column group (0: stream-K mode)
   int bulk;             // stream-K: final sums staged by bulk copies when the ring is idle
+  int split;            // stream-K: write the partial sums only (skinny_sum_kernel adds them)
+  int nb;               // 64-column blocks per unit (the sum kernel's slot layout)
   float* part;          // [n_cg][maxq][NB][2][M][64]
   unsigned* counters;   // [n_cg], zero on entry, zero again on exit
   uint16_t* out;        // [M][n_out] bf16
@@ -464,6 +467,12 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         acc = 0;
         acc_phase ^= 1u;
       }
+      // Two-kernel form: the sums are added by skinny_sum_kernel, which the
+      // end of this grid releases.
+      if (a.split) {
+        t = seg_end;
+        continue;
+      }
       // The CTA that completes column group cg last reduces it.
       __syncwarp();
       named_bar_sync(1, kEpiThreads);
@@ -730,6 +739,100 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
   }
 }
 
+// Second kernel of the two-kernel form (stream-K mode): one thread per
+// output chunk (4 adjacent columns of one row) adds the chunk's partial sums
+// from every CTA of its column group in slot (= k) order -- the order of the
+// one-kernel form's last CTA, so the bits are the same -- and applies the
+// epilogue.  A thread issues all of its loads before the first add, so the
+// sums take one or two L2 round trips on a grid as wide as the output,
+// instead of one CTA per column group walking its slots while the rest of
+// the GPU idles.  This is the slice-reduction pass of "Ou part le temps d'un
+// token" (section "Un kernel pour les matrices etroites") on this kernel's
+// partial-sum layout.
+constexpr int kSumThreads = 256;
+
+template <int MODE, bool FP8>
+__global__ void __launch_bounds__(kSumThreads) skinny_sum_kernel(const SkArgs a) {
+  // Launched with programmatic serialisation behind the GEMM: its partial
+  // sums are complete and visible once that grid is (the dependency wait).
+  pdl_wait();
+  pdl_launch_dependents();
+  constexpr int kSubCols = MODE == kSwiGLU ? kCB : 2 * kCB;
+  constexpr int kBatch = MODE == kSwiGLU ? 6 : 12;   // slots loaded per round
+  const int64_t group_cols = (int64_t)a.nb * kSubCols;
+  const int64_t cpr = a.n_out / 4;                    // chunks per row (n_out % 8 == 0)
+  const int64_t idx = (int64_t)blockIdx.x * kSumThreads + threadIdx.x;
+  if (idx >= (int64_t)a.M * cpr) return;
+  const int m = (int)(idx / cpr);
+  const int64_t col = (idx - (int64_t)m * cpr) * 4;
+  const int64_t cg = col / group_cols;
+  const int ch = (int)((col - cg * group_cols) / 4);
+  const int64_t U = a.units, G = a.grid;
+  const int64_t c_lo = cta_of(cg * a.n_kb, U, G);
+  const int n_contrib = (int)(cta_of((cg + 1) * a.n_kb - 1, U, G) - c_lo + 1);
+  const int64_t Mrow = (int64_t)a.M * kCB;            // floats of one [M][64] block
+  const int64_t q_stride = (int64_t)a.nb * 2 * Mrow;  // floats of one slot
+  // the chunk's [M][64] block in [NB][2] order: SwiGLU -> sub-block ch/16,
+  // gate half (up at + Mrow); plain -> sub-block ch/32, half (ch/16) & 1
+  const int blk = MODE == kSwiGLU ? (ch >> 4) * 2 : (ch >> 4);
+  const float* p0 = a.part + cg * a.maxq * q_stride + blk * Mrow + (int64_t)m * kCB + (ch & 15) * 4;
+  const int64_t o = (int64_t)m * a.n_out + col;
+  uint2 rv = make_uint2(0u, 0u);
+  if (MODE == kPlain && a.resid) rv = __ldg(reinterpret_cast<const uint2*>(a.resid + o));
+  float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+  for (int q0 = 0; q0 < n_contrib; q0 += kBatch) {
+    float4 vg[kBatch], vu[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const bool have = q0 + j < n_contrib;
+      const float* pq = p0 + (int64_t)(q0 + j) * q_stride;
+      vg[j] = have ? __ldcg(reinterpret_cast<const float4*>(pq)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if constexpr (MODE == kSwiGLU)
+        vu[j] = have ? __ldcg(reinterpret_cast<const float4*>(pq + Mrow))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (q0 + j < n_contrib) {
+        g.x += vg[j].x; g.y += vg[j].y; g.z += vg[j].z; g.w += vg[j].w;
+        if constexpr (MODE == kSwiGLU) {
+          u.x += vu[j].x; u.y += vu[j].y; u.z += vu[j].z; u.w += vu[j].w;
+        }
+      }
+    }
+  }
+  if constexpr (MODE == kSwiGLU) {
+    store_chunk<MODE, FP8>(a, g, u, m, col);
+  } else {
+    // store_chunk's plain epilogue, with the residual loaded up front
+    if constexpr (FP8) fp8_scale1(g, a, m, col);
+    if (a.resid) {
+      g.x += bf16_lo(rv.x); g.y += bf16_hi(rv.x);
+      g.z += bf16_lo(rv.y); g.w += bf16_hi(rv.y);
+    }
+    uint2 ov;
+    ov.x = pack_bf16x2(g.x, g.y);
+    ov.y = pack_bf16x2(g.z, g.w);
+    *reinterpret_cast<uint2*>(a.out + o) = ov;
+  }
+}
+
+template <int MODE, bool FP8>
+cudaError_t launch_sum(const SkArgs& a, cudaStream_t st) {
+  const int64_t chunks = (int64_t)a.M * (a.n_out / 4);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((chunks + kSumThreads - 1) / kSumThreads));
+  cfg.blockDim = dim3(kSumThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, skinny_sum_kernel<MODE, FP8>, a);
+}
+
 template <int N, int NB, int MODE, bool FP8>
 cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mu,
                      const SkArgs& a, cudaStream_t st) {
@@ -827,19 +930,21 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
     const int64_t limit = fp8 ? (int64_t)128 << 10 : (int64_t)256 << 10;
     if (slots2 * 4 * kCB * 4 * M > limit) nb = 1;
   }
-  // Large down projections from kPlainCluster4MinM rows on (FP8: 16): 4-CTA
+  // Large down projections in a band of rows (bf16 33-64, FP8 16-128): 4-CTA
   // clusters of 128-column groups, when all the groups' clusters fit at once
   // (n_out up to 36 x 128 on GB300).  The group's four K quarters then meet
-  // in distributed shared memory instead of ~5 partial slots in L2 that one
-  // CTA adds after everyone else is done, a tail that grows with M.
-  // Measured, d_ff = 14336 -> d = 4096, calls back to back, stream-K vs
-  // 4-CTA clusters (without the pre-wait prefetch, below): M = 16: 25.3 /
-  // 25.4 us; 24: 28.2 / 25.9; 32: 29.1 / 26.1; 64: 33.5 / 27.3; 128: 42.4 /
-  // 29.7; 256: 62.7 / 35.8.  FP8: M = 16: 18.8 / 17.8; 64: 26.6 / 20.4.
-  // (d = 8192 needs 64 groups, more than fit: stream-K.)
+  // in distributed shared memory; 128 CTAs stream the weights.  Elsewhere
+  // stream-K on every SM with its sums in a second kernel leads.  Measured,
+  // d_ff = 14336 -> d = 4096, calls back to back, 4-CTA clusters against
+  // stream-K with the two-kernel sums: M = 16: 25.3 / 21.0 us; 32: 26.0 /
+  // 25.1; 48: 26.7 / 28.0; 64: 27.2 / 28.3; 96: 28.7 / 28.9; 128: 29.9 /
+  // 29.2; 256: 36.2 / 34.0.  FP8: M = 16: 17.9 / 21.1; 64: 20.4 / 21.7; 128:
+  // 23.8 / 24.0; 256: 30.6 / 28.5.  (d = 8192 needs 64 groups, more than
+  // fit: stream-K.)
   bool plain_cluster4 = false;
   if (plain && weight_bytes > kSkinnyClusterMaxWeightBytes &&
-      M >= (fp8 ? kPlainCluster4MinMFp8 : kPlainCluster4MinM) && tn.sk_nb < 0 &&
+      M >= (fp8 ? kPlainCluster4MinMFp8 : kPlainCluster4MinM) &&
+      M <= (fp8 ? kPlainCluster4MaxMFp8 : kPlainCluster4MaxM) && tn.sk_nb < 0 &&
       tn.sk_cluster < 0 && skinny_plain_cluster4_fits(K, n_out, num_sms, cluster_caps)) {
     nb = 1;
     plain_cluster4 = true;
@@ -927,6 +1032,16 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   p.part_bytes = (size_t)p.n_cb * p.maxq * nb * 2 * (size_t)M * kCB * sizeof(float);
   p.part_bytes = (p.part_bytes + 255) / 256 * 256;
   if (p.cluster) p.counters_bytes = p.part_bytes = 0;   // the reduction stays on chip
+  // Two-kernel form (stream-K only; skinny_sum_kernel).  Measured, calls back
+  // to back, one kernel / two kernels: the bf16 down projection d = 4096 at
+  // M = 1 / 8 / 16: 21.9 / 22.9 / 25.2 us against 20.7 / 20.7 / 20.9 us;
+  // d = 8192 at M = 16 / 128 / 256: 73.8 / 93.8 / 119.9 against 70.7 / 83.3
+  // / 100.7 us; FP8, d = 4096, M = 256: 61.4 against 28.5 us.  Where the
+  // group sums are short it loses the second launch's cost: the up
+  // projection (d = 4096, M = 1: 35.9 against 37.1 us) and the FP8 down
+  // projection at M <= 8 (M = 1: 16.8 against 18.4 us).
+  const bool split_default = plain && (!fp8 || M >= 16);
+  p.split = !p.cluster && (tn.sk_split >= 0 ? tn.sk_split > 0 : split_default) ? 1 : 0;
   return p;
 }
 
@@ -994,6 +1109,8 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   a.sw_b = fp8 ? fp8->sw_b : nullptr;
   a.prefetch_units = p.prefetch_units;
   a.bulk = p.bulk;
+  a.split = p.split;
+  a.nb = p.nb;
   a.cluster = p.cluster;
   a.part = part;
   a.counters = counters;
@@ -1002,10 +1119,14 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   a.status = status;
   a.timeout_ns = timeout_ns;
   if (p.plain)
-    return fp8 ? launch_mode<kPlain, true>(p.n_pad, p.nb, mx, mg, mu, a, st)
-               : launch_mode<kPlain, false>(p.n_pad, p.nb, mx, mg, mu, a, st);
-  return fp8 ? launch_mode<kSwiGLU, true>(p.n_pad, p.nb, mx, mg, mu, a, st)
-             : launch_mode<kSwiGLU, false>(p.n_pad, p.nb, mx, mg, mu, a, st);
+    e = fp8 ? launch_mode<kPlain, true>(p.n_pad, p.nb, mx, mg, mu, a, st)
+            : launch_mode<kPlain, false>(p.n_pad, p.nb, mx, mg, mu, a, st);
+  else
+    e = fp8 ? launch_mode<kSwiGLU, true>(p.n_pad, p.nb, mx, mg, mu, a, st)
+            : launch_mode<kSwiGLU, false>(p.n_pad, p.nb, mx, mg, mu, a, st);
+  if (e != cudaSuccess || !a.split) return e;
+  if (p.plain) return fp8 ? launch_sum<kPlain, true>(a, st) : launch_sum<kPlain, false>(a, st);
+  return fp8 ? launch_sum<kSwiGLU, true>(a, st) : launch_sum<kSwiGLU, false>(a, st);
 }
 
 }  // namespace swg

@@ -140,9 +140,9 @@ def test_plan_reports_cluster_size(cuda_lib):
 
 def test_dispatch_rule(cuda_lib):
     # measured thresholds, weights above 32 MB (stream-K mode): skinny up to
-    # M = 32 (up) and 128 (down); smaller weights (cluster mode): 128 (up) and
-    # every M the skinny kernel serves (down); a down projection whose
-    # 128-column groups fit as 4-CTA clusters (d = 4096): every M it serves
+    # M = 32 (up) and every M the skinny kernel serves (down, its sums in a
+    # second kernel); smaller weights (cluster mode): 128 (up) and every M
+    # the skinny kernel serves (down)
     for M, path in [(1, "skinny"), (16, "skinny"), (32, "skinny"), (33, "tc"), (4096, "tc")]:
         assert swg.plan(M, 4096, 14336, "bf16", "auto", 152)["path"] == path
     # (one row on small weights with d <= 1024: the SIMT path's cluster form)
@@ -152,20 +152,27 @@ def test_dispatch_rule(cuda_lib):
     assert swg.plan(1, 2048, 3584, "bf16", "auto", 152)["path"] == "skinny"
     for M, path in [(1, "skinny"), (64, "skinny"), (256, "skinny"), (257, "tc"), (4096, "tc")]:
         assert swg.down_plan(M, 14336, 4096, "bf16", "auto", 152)["path"] == path
-    for M, path in [(1, "skinny"), (128, "skinny"), (129, "tc"), (4096, "tc")]:
+    for M, path in [(1, "skinny"), (128, "skinny"), (256, "skinny"), (257, "tc"), (4096, "tc")]:
         assert swg.down_plan(M, 29568, 8192, "bf16", "auto", 152)["path"] == path
     for M, path in [(1, "skinny"), (256, "skinny"), (257, "tc")]:
         assert swg.down_plan(M, 4864, 896, "bf16", "auto", 152)["path"] == path
     assert swg.plan(1, 4096, 14336, "bf16", "auto", 152)["skinny_max_m"] == 32
     assert swg.plan(1, 896, 4864, "bf16", "auto", 152)["skinny_max_m"] == 128
     assert swg.down_plan(1, 14336, 4096, "bf16", "auto", 152)["skinny_max_m"] == 256
-    assert swg.down_plan(1, 29568, 8192, "bf16", "auto", 152)["skinny_max_m"] == 128
+    assert swg.down_plan(1, 29568, 8192, "bf16", "auto", 152)["skinny_max_m"] == 256
     assert swg.down_plan(1, 4864, 896, "bf16", "auto", 152)["skinny_max_m"] == 256
-    # the down projection at d = 4096: stream-K up to 23 rows, 4-CTA clusters
-    # of 128-column groups from 24 on
-    for M, cl in [(16, 1), (23, 1), (24, 4), (256, 4)]:
+    # the down projection at d = 4096: 4-CTA clusters of 128-column groups for
+    # 33-64 rows, stream-K with its sums in a second kernel otherwise
+    for M, cl in [(1, 1), (16, 1), (32, 1), (33, 4), (64, 4), (65, 1), (256, 1)]:
         p = swg.down_plan(M, 14336, 4096, "bf16", "auto", 152)
         assert p["cluster"] == cl and (cl == 1) == (p["workspace"] > 0), (M, p)
+        assert p["launches"] == (2 if cl == 1 else 1), (M, p)
+    # d = 8192 (64 groups, more than fit as 4-CTA clusters): stream-K, two kernels
+    for M in (1, 16, 128, 256):
+        p = swg.down_plan(M, 29568, 8192, "bf16", "auto", 152)
+        assert p["cluster"] == 1 and p["launches"] == 2, (M, p)
+    # the up projection keeps its final sums in one kernel
+    assert swg.plan(16, 4096, 14336, "bf16", "auto", 152)["launches"] == 1
     assert swg.plan(1, 512, 2048, "f32", "auto", 152)["path"] == "simt"
     assert swg.plan(3, 0, 64, "bf16", "auto", 152)["path"] == "simt"
     with pytest.raises(swg.SwiGLUError):

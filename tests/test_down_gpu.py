@@ -74,13 +74,54 @@ def test_small_model_full(M):
     check(M, 4864, 896, "auto", seed=M + 5)
 
 
-@pytest.mark.parametrize("M", [32, 128, 256])
+@pytest.mark.parametrize("M", [33, 48, 64])
 def test_skinny_cluster4_rows(M):
-    # AUTO serves M = 32 .. 256 at d = 4096 on the skinny kernel in 4-CTA
+    # AUTO serves M = 33 .. 64 at d = 4096 on the skinny kernel in 4-CTA
     # clusters of 128-column groups (the K quarters meet on chip)
     p = swg.down_plan(M, 14336, 4096)
     assert p["path"] == "skinny" and p["cluster"] == 4 and p["workspace"] == 0
     check(M, 14336, 4096, "auto", seed=M, rows=tile_rows(M, seed=M))
+
+
+@pytest.mark.parametrize("M", [1, 16, 32, 65, 128, 256])
+def test_skinny_two_kernel_rows(M):
+    # Outside that band AUTO runs the skinny kernel's stream-K form on every
+    # SM and adds the partial sums in a second kernel; every column of rows
+    # of every 128-row block against the oracle
+    p = swg.down_plan(M, 14336, 4096, "bf16", "auto", 0)
+    assert p["path"] == "skinny" and p["cluster"] == 1 and p["launches"] == 2
+    rows = np.arange(M) if M <= 32 else tile_rows(M, seed=M)
+    check(M, 14336, 4096, "auto", seed=M + 3, rows=rows)
+    swg.check_device_status()
+
+
+@pytest.mark.parametrize("shape", [(1, 14336, 4096), (16, 14336, 4096), (200, 14336, 4096),
+                                   (40, 4104, 1032), (7, 29568, 8192)])
+def test_two_kernel_sums_equal_one_kernel_sums(shape, monkeypatch):
+    # Stream-K mode: the second kernel (SWIGLU_SK_SPLIT=1) adds each column
+    # group's partial sums in the order the group's last CTA does in the
+    # one-kernel form (SWIGLU_SK_SPLIT=0, sums staged by bulk copies or read
+    # from L2): the bits must agree, and match the oracle
+    M, d_ff, d = shape
+    h, wd, r = make(M, d_ff, d, seed=M + 11)
+    monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")
+    outs = []
+    for split, bulk in (("1", "1"), ("0", "1"), ("0", "0")):
+        monkeypatch.setenv("SWIGLU_SK_SPLIT", split)
+        monkeypatch.setenv("SWIGLU_SK_BULK", bulk)
+        p = swg.down_plan(M, d_ff, d, "bf16", "skinny", 0)
+        assert p["cluster"] == 1 and p["launches"] == (2 if split == "1" else 1)
+        y = swg.swiglu_down(h.to(DEV), wd.to(DEV), r.to(DEV), path="skinny")
+        torch.cuda.synchronize()
+        outs.append(y)
+    for y in outs[1:]:
+        assert torch.equal(outs[0].view(torch.int16), y.view(torch.int16))
+    raw = inputs.raw_bits
+    rows = np.unique(np.linspace(0, M - 1, min(M, 6)).astype(int))
+    y64, _, s = oracle.down_proj(raw(h[rows].contiguous()), raw(wd), oracle.BF16,
+                                 raw(r[rows].contiguous()))
+    assert compare(to64(outs[0])[rows], y64, s, "bf16", d_ff)["ok"]
+    swg.check_device_status()
 
 
 def test_cluster4_and_stream_k_agree(monkeypatch):
@@ -168,6 +209,7 @@ def test_bulk_staged_final_sums_equal_l2_sums(shape, monkeypatch):
     M, d_ff, d = shape
     h, wd, r = make(M, d_ff, d, seed=M + 1)
     outs = []
+    monkeypatch.setenv("SWIGLU_SK_SPLIT", "0")     # the one-kernel form's final sums
     for bulk in ("1", "0"):
         monkeypatch.setenv("SWIGLU_SK_BULK", bulk)
         monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")
@@ -185,10 +227,10 @@ def test_bulk_staged_final_sums_equal_l2_sums(shape, monkeypatch):
 
 def test_large_model_stream_k_with_bulk_final_sums():
     # d_ff = 29568 -> d = 8192 at M = 64: stream-K mode (its 64 groups do not
-    # fit as 4-CTA clusters), 128-column groups, final sums staged in shared
-    # memory by bulk copies (the default above 16 rows); every column of
-    # rows from both halves of the call
+    # fit as 4-CTA clusters), 128-column groups, the sums added by the second
+    # kernel; every column of rows from both halves of the call
     M, d_ff, d = 64, 29568, 8192
     p = swg.down_plan(M, d_ff, d)
     assert p["path"] == "skinny" and p["cluster"] == 1 and p["workspace"] > 0
+    assert p["launches"] == 2
     check(M, d_ff, d, "auto", seed=91, rows=np.array([0, 17, 40, 63]))

@@ -217,26 +217,32 @@ def test_fp8_down_full_size_rows():
     swg.check_device_status()
 
 
-@pytest.mark.parametrize("M", [16, 64])
-def test_fp8_down_bulk_staged_final_sums(M, monkeypatch):
-    # FP8 down projection (stream-K at d = 4096): both final-sum routes agree
+@pytest.mark.parametrize("M", [1, 16, 64, 256])
+def test_fp8_down_final_sum_routes(M, monkeypatch):
+    # FP8 down projection in stream-K mode at d = 4096: the second kernel's
+    # sums and the one-kernel form's (bulk-staged or read from L2) agree bit
+    # for bit and match the oracle
     h = inputs.make_inputs(M, 14336, 8, "bf16", seed=M, x_only=True)[0]
     _, wd, _ = inputs.make_inputs(1, 14336, 4096, "bf16", seed=M + 1)
     r = inputs.make_inputs(M, 4096, 8, "bf16", seed=M + 2, x_only=True)[0]
     w8 = swg.quantize_weight_fp8(wd.to(DEV))
+    monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")
     outs = []
-    for bulk in ("1", "0"):
+    for split, bulk in (("1", "1"), ("0", "1"), ("0", "0")):
+        monkeypatch.setenv("SWIGLU_SK_SPLIT", split)
         monkeypatch.setenv("SWIGLU_SK_BULK", bulk)
         outs.append(swg.swiglu_down_fp8(h.to(DEV), w8, residual=r.to(DEV), path="skinny"))
         torch.cuda.synchronize()
-    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    for y in outs[1:]:
+        assert torch.equal(outs[0].view(torch.int16), y.view(torch.int16))
     rows = [0, M - 1]
     y64, sens = oracle.down_proj_fp8(RAW(h[rows].contiguous()), RAW(wd), RAW(r[rows].contiguous()))
     assert compare(to64(outs[0])[rows], y64, sens, "bf16", 14336)["ok"]
 
 
-@pytest.mark.parametrize("M", [16, 64, 256])
+@pytest.mark.parametrize("M", [16, 64, 128, 256])
 def test_fp8_down_cluster4(M):
     # FP8 down projection at d = 4096: 4-CTA clusters of 128-column groups
-    # from M = 16 on; every column of rows of every 128-row block
+    # for M = 16 .. 128, stream-K with the second kernel's sums above; every
+    # column of rows of every 128-row block
     down_check(M, 14336, 4096, "auto", seed=M + 9, rows=tile_rows(M, seed=M))

@@ -336,14 +336,19 @@ def test_simt_single_launch_matches_two_launches(dtype, shape, monkeypatch):
 @pytest.mark.parametrize("M,d,d_ff", [(16, 4096, 14336), (32, 4096, 14336), (130, 640, 1032),
                                       (7, 1024, 4104)])
 def test_skinny_bulk_staged_final_sums_equal_l2_sums(M, d, d_ff, monkeypatch):
-    # the up projection's final sums by either route: identical bits
+    # the up projection's final sums by every route (the group's last CTA
+    # with bulk-staged or L2 loads, or the second kernel that
+    # SWIGLU_SK_SPLIT=1 adds): identical bits
     x, wg, wu = inputs.make_inputs(M, d, d_ff, "bf16", seed=M + 2)
     outs = []
-    for bulk in ("1", "0"):
+    monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")
+    for split, bulk in (("0", "1"), ("0", "0"), ("1", "0")):
+        monkeypatch.setenv("SWIGLU_SK_SPLIT", split)
         monkeypatch.setenv("SWIGLU_SK_BULK", bulk)
-        monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")
+        assert swg.plan(M, d, d_ff, "bf16", "skinny", 0)["launches"] == (2 if split == "1" else 1)
         outs.append(gpu_run(x, wg, wu, "skinny"))
-    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    for h in outs[1:]:
+        assert torch.equal(outs[0].view(torch.int16), h.view(torch.int16))
     raw = inputs.raw_bits
     h64, _, sens = oracle.swiglu_up(raw(x), raw(wg), raw(wu), oracle.BF16)
     assert compare(to64(outs[0]), h64, sens, "bf16", d)["ok"]
