@@ -116,6 +116,7 @@ struct SkArgs {
   int bulk;             // stream-K: final sums staged by bulk copies when the ring is idle
   int split;            // stream-K: write the partial sums only (skinny_sum_kernel adds them)
   int nb;               // 64-column blocks per unit (the sum kernel's slot layout)
+  int release_early;    // the sum kernel releases the next kernel before its wait
   float* part;          // [n_cg][maxq][NB][2][M][64]
   unsigned* counters;   // [n_cg], zero on entry, zero again on exit
   uint16_t* out;        // [M][n_out] bf16
@@ -755,6 +756,14 @@ template <int MODE, bool FP8>
 __global__ void __launch_bounds__(kSumThreads) skinny_sum_kernel(const SkArgs a) {
   // Launched with programmatic serialisation behind the GEMM: its partial
   // sums are complete and visible once that grid is (the dependency wait).
+  // With release_early the next kernel in the stream may launch at once (its
+  // own dependency wait still covers this grid's completion): an FP8 call
+  // starts with its activation quantizer, and releasing it early lets the
+  // next call's GEMM take the SMs this call's GEMM frees, and prefetch its
+  // weights, one launch sooner.  Measured, FP8 down projection d = 4096,
+  // M = 4 / 8: 16.9 / 17.0 us against 18.7 / 18.8 without (one-kernel form
+  // 17.4 / 18.0); for bf16 it measured 0.1-0.7 us slower.
+  if (a.release_early) pdl_launch_dependents();
   pdl_wait();
   pdl_launch_dependents();
   constexpr int kSubCols = MODE == kSwiGLU ? kCB : 2 * kCB;
@@ -1036,11 +1045,11 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   // to back, one kernel / two kernels: the bf16 down projection d = 4096 at
   // M = 1 / 8 / 16: 21.9 / 22.9 / 25.2 us against 20.7 / 20.7 / 20.9 us;
   // d = 8192 at M = 16 / 128 / 256: 73.8 / 93.8 / 119.9 against 70.7 / 83.3
-  // / 100.7 us; FP8, d = 4096, M = 256: 61.4 against 28.5 us.  Where the
-  // group sums are short it loses the second launch's cost: the up
-  // projection (d = 4096, M = 1: 35.9 against 37.1 us) and the FP8 down
-  // projection at M <= 8 (M = 1: 16.8 against 18.4 us).
-  const bool split_default = plain && (!fp8 || M >= 16);
+  // / 100.7 us; FP8, d = 4096, M = 1 / 8 / 256: 16.9 / 17.0 / 28.3 against
+  // 16.9 / 18.0 / 60.5 us.  Where the group sums are short it loses the
+  // second launch's cost: the up projection (d = 4096, M = 1: 35.9 against
+  // 37.1 us).
+  const bool split_default = plain;
   p.split = !p.cluster && (tn.sk_split >= 0 ? tn.sk_split > 0 : split_default) ? 1 : 0;
   return p;
 }
@@ -1111,6 +1120,7 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   a.bulk = p.bulk;
   a.split = p.split;
   a.nb = p.nb;
+  a.release_early = fp8 ? 1 : 0;
   a.cluster = p.cluster;
   a.part = part;
   a.counters = counters;
