@@ -311,15 +311,12 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 // Largest bf16 M that AUTO sends to the skinny kernel, by operation and by
-// the skinny kernel's mode for the weights: cluster mode (at most 32 MB),
-// stream-K, or, for the down projection above 32 MB whose 128-column groups
-// fit as 4-CTA clusters, that cluster mode.  The decode article serves at
-// most 16 rows with its skinny kernel; the tcgen05 skinny kernel pays longer.
+// the skinny kernel's mode for the weights: cluster mode (at most 32 MB) or
+// stream-K.  The decode article serves at most 16 rows with its skinny
+// kernel; the tcgen05 skinny kernel pays longer.
 constexpr int64_t kSkinnyMaxM = 32;
 constexpr int64_t kSkinnyMaxMSmall = 128;
 constexpr int64_t kSkinnyMaxMDown = 256;
-constexpr int64_t kSkinnyMaxMDownSmall = 256;
-constexpr int64_t kSkinnyMaxMDownCluster4 = 256;
 
 // Grid-dimension limits of the SIMT path (gridDim.y/z are 16-bit).
 constexpr int64_t kMaxGridYZ = kSimtMaxGridYZ;
@@ -342,20 +339,17 @@ enum Op { kOpUp = 0, kOpDown = 1 };
 // included).  Stream-K mode: up projection 32 at d = 4096 and 8192 (d =
 // 4096: 39.4 vs 40.2 us at M = 32, 42.8 vs 40.4 at 48); down projection,
 // with its sums in a second kernel, all the 256 rows the kernel serves (d =
-// 8192: 83.3 vs 111.3 us at M = 128, 100.7 vs 143.9 at 256).  Cluster mode, d = 896 (graph replay; 64-column
-// groups from 16 rows): up projection 128 (9.97 vs 10.67 us at M = 128,
-// 11.84 vs 10.39 at 192); down projection all M the kernel
-// serves (13.9 vs 27.3 us at M = 256).  Down projection in 4-CTA clusters of
-// 128-column groups (d_ff = 14336 -> d = 4096): the skinny kernel leads up to
-// the 256 rows it serves (37.3 vs 49.6 us at M = 256; FP8 32.4 vs 46.7).
-// FP8 calls measure alike otherwise.
+// 4096: 32.3 vs 50.3 us at M = 256; d = 8192: 83.3 vs 111.3 at 128, 100.7
+// vs 143.9 at 256; FP8 d = 4096: 27.2 vs 45.6 at 256).  Cluster mode, d =
+// 896 (graph replay; 64-column groups from 16 rows): up projection 128
+// (9.97 vs 10.67 us at M = 128, 11.84 vs 10.39 at 192); down projection
+// all M the kernel serves (13.9 vs 27.3 us at M = 256).  FP8 calls measure
+// alike otherwise.
 int64_t skinny_max_m(int op, int64_t K, int64_t n_out, int num_sms, const int* sk_caps) {
   const bool small = (op == kOpDown ? 1 : 2) * K * n_out * 2 <= kSkinnyClusterMaxWeightBytes;
-  if (op == kOpDown) {
-    if (small) return kSkinnyMaxMDownSmall;
-    return skinny_plain_cluster4_fits(K, n_out, num_sms, sk_caps) ? kSkinnyMaxMDownCluster4
-                                                                  : kSkinnyMaxMDown;
-  }
+  (void)num_sms;
+  (void)sk_caps;
+  if (op == kOpDown) return kSkinnyMaxMDown;
   return small ? kSkinnyMaxMSmall : kSkinnyMaxM;
 }
 

@@ -73,9 +73,8 @@ constexpr uint32_t kChunkBytes = kCB * kBK * 2;       // one 64 x 64 bf16 weight
 constexpr uint32_t kSubBytes = 2 * kChunkBytes;       // gate box + up box = one MMA A tile
 constexpr uint32_t kPrefetchBytes = 512u * 1024u;     // weight bytes per CTA prefetched before the wait
 constexpr uint32_t kRingBudget = 200u * 1024u;        // shared memory for the stage ring
-// Rows for which the down projection takes 4-CTA clusters (see plan_skinny)
-constexpr int64_t kPlainCluster4MinM = 33, kPlainCluster4MaxM = 64;
-constexpr int64_t kPlainCluster4MinMFp8 = 16, kPlainCluster4MaxMFp8 = 128;
+// Rows for which the FP8 down projection takes 4-CTA clusters (see plan_skinny)
+constexpr int64_t kPlainCluster4MinMFp8 = 16, kPlainCluster4MaxMFp8 = 64;
 
 constexpr uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
   uint32_t r = lo;
@@ -939,21 +938,20 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
     const int64_t limit = fp8 ? (int64_t)128 << 10 : (int64_t)256 << 10;
     if (slots2 * 4 * kCB * 4 * M > limit) nb = 1;
   }
-  // Large down projections in a band of rows (bf16 33-64, FP8 16-128): 4-CTA
-  // clusters of 128-column groups, when all the groups' clusters fit at once
-  // (n_out up to 36 x 128 on GB300).  The group's four K quarters then meet
-  // in distributed shared memory; 128 CTAs stream the weights.  Elsewhere
-  // stream-K on every SM with its sums in a second kernel leads.  Measured,
-  // d_ff = 14336 -> d = 4096, calls back to back, 4-CTA clusters against
-  // stream-K with the two-kernel sums: M = 16: 25.3 / 21.0 us; 32: 26.0 /
-  // 25.1; 48: 26.7 / 28.0; 64: 27.2 / 28.3; 96: 28.7 / 28.9; 128: 29.9 /
-  // 29.2; 256: 36.2 / 34.0.  FP8: M = 16: 17.9 / 21.1; 64: 20.4 / 21.7; 128:
-  // 23.8 / 24.0; 256: 30.6 / 28.5.  (d = 8192 needs 64 groups, more than
-  // fit: stream-K.)
+  // FP8 down projections of 16-64 rows: 4-CTA clusters of 128-column groups,
+  // when all the groups' clusters fit at once (n_out up to 36 x 128 on
+  // GB300).  The group's four K quarters then meet in distributed shared
+  // memory; 128 CTAs stream the weights.  Elsewhere, and for bf16 at every
+  // M, stream-K on every SM with its sums in a second kernel leads.
+  // Measured, d_ff = 14336 -> d = 4096, calls back to back, 4-CTA clusters
+  // against stream-K with the two-kernel sums: bf16 M = 16: 25.3 / 21.1 us;
+  // 33: 26.4 / 24.1; 48: 26.8 / 26.0; 64: 27.3 / 26.1; 80: 26.7 / 26.6; 128:
+  // 29.9 / 27.1; 256: 36.2 / 32.3.  FP8 M = 16: 18.0 / 18.7; 32: 18.9 /
+  // 20.0; 64: 20.6 / 20.7; 96: 22.3 / 21.4; 128: 23.6 / 22.3.  (d = 8192
+  // needs 64 groups, more than fit.)
   bool plain_cluster4 = false;
-  if (plain && weight_bytes > kSkinnyClusterMaxWeightBytes &&
-      M >= (fp8 ? kPlainCluster4MinMFp8 : kPlainCluster4MinM) &&
-      M <= (fp8 ? kPlainCluster4MaxMFp8 : kPlainCluster4MaxM) && tn.sk_nb < 0 &&
+  if (plain && fp8 && weight_bytes > kSkinnyClusterMaxWeightBytes &&
+      M >= kPlainCluster4MinMFp8 && M <= kPlainCluster4MaxMFp8 && tn.sk_nb < 0 &&
       tn.sk_cluster < 0 && skinny_plain_cluster4_fits(K, n_out, num_sms, cluster_caps)) {
     nb = 1;
     plain_cluster4 = true;
@@ -983,14 +981,16 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   // M <= 8 and for the up projection, whose final sums are short, it is
   // within noise or up to 3 % slower.
   p.bulk = tn.sk_bulk >= 0 ? (tn.sk_bulk != 0) : (plain && M >= 16);
-  // L2 prefetch budget per CTA (measured, d = 4096, calls back to back):
-  // 512 KB for bf16 SwiGLU; 256 KB for the down projection, whose column
-  // groups collect ~10 partial sums each (K is long), so the previous
-  // call's final reductions run longer and a larger prefetch slows them
-  // (M = 1: 21.5 us at 256 KB, 23.2 at 512 KB, 22.0 at 128 KB); 384 KB for
-  // the FP8 up projection (M = 1 / 16: 21.9 / 23.2 us against 22.6 / 24.0
-  // at 256 KB and 22.0 / 23.1 at 512 KB).
-  const uint32_t pf_bytes = plain ? kPrefetchBytes / 2
+  // L2 prefetch budget per CTA (measured, calls back to back): 512 KB for
+  // bf16 SwiGLU; 384 KB for the FP8 up projection (d = 4096, M = 1 / 16:
+  // 21.9 / 23.2 us against 22.6 / 24.0 at 256 KB and 22.0 / 23.1 at 512
+  // KB).  Down projection: 256 KB with 256-column groups (d = 4096, M = 1 /
+  // 16 / 24: 21.0 / 21.1 / 23.9 us, against 21.7 / 22.3 / 24.0 at 128 KB
+  // and 22.5 / 22.8 / 25.0 at 512 KB; d = 8192 M = 32: 74.6 against 76.3
+  // at 64 KB), 64 KB with the 128-column groups of larger M (d = 4096, M =
+  // 96 / 128 / 256: 26.9 / 27.1 / 32.3 us against 28.7 / 29.0 / 34.0 at 256
+  // KB; FP8 M = 256: 26.9 against 28.1).
+  const uint32_t pf_bytes = plain ? (nb == 1 ? kPrefetchBytes / 8 : kPrefetchBytes / 2)
                                   : (fp8 ? kPrefetchBytes / 4 * 3 : kPrefetchBytes);
   p.prefetch_units = tn.sk_prefetch_units >= 0 ? tn.sk_prefetch_units
                                                : (int)(pf_bytes / ((uint32_t)nb * kSubBytes));

@@ -161,13 +161,11 @@ def test_dispatch_rule(cuda_lib):
     assert swg.down_plan(1, 14336, 4096, "bf16", "auto", 152)["skinny_max_m"] == 256
     assert swg.down_plan(1, 29568, 8192, "bf16", "auto", 152)["skinny_max_m"] == 256
     assert swg.down_plan(1, 4864, 896, "bf16", "auto", 152)["skinny_max_m"] == 256
-    # the down projection at d = 4096: 4-CTA clusters of 128-column groups for
-    # 33-64 rows, stream-K with its sums in a second kernel otherwise
-    for M, cl in [(1, 1), (16, 1), (32, 1), (33, 4), (64, 4), (65, 1), (256, 1)]:
+    # the bf16 down projection above 32 MB: stream-K with its sums in a
+    # second kernel at every M (4-CTA clusters serve FP8 at 16-64 rows)
+    for M in (1, 16, 32, 33, 64, 65, 256):
         p = swg.down_plan(M, 14336, 4096, "bf16", "auto", 152)
-        assert p["cluster"] == cl and (cl == 1) == (p["workspace"] > 0), (M, p)
-        assert p["launches"] == (2 if cl == 1 else 1), (M, p)
-    # d = 8192 (64 groups, more than fit as 4-CTA clusters): stream-K, two kernels
+        assert p["cluster"] == 1 and p["workspace"] > 0 and p["launches"] == 2, (M, p)
     for M in (1, 16, 128, 256):
         p = swg.down_plan(M, 29568, 8192, "bf16", "auto", 152)
         assert p["cluster"] == 1 and p["launches"] == 2, (M, p)

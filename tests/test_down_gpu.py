@@ -74,20 +74,22 @@ def test_small_model_full(M):
     check(M, 4864, 896, "auto", seed=M + 5)
 
 
-@pytest.mark.parametrize("M", [33, 48, 64])
-def test_skinny_cluster4_rows(M):
-    # AUTO serves M = 33 .. 64 at d = 4096 on the skinny kernel in 4-CTA
-    # clusters of 128-column groups (the K quarters meet on chip)
+@pytest.mark.parametrize("M", [33, 48, 64, 256])
+def test_skinny_cluster4_rows(M, monkeypatch):
+    # the skinny kernel in 4-CTA clusters of 128-column groups (the K quarters
+    # meet on chip; AUTO takes it for FP8 at 16-64 rows), forced for bf16
+    monkeypatch.setenv("SWIGLU_SK_CLUSTER", "4")
+    monkeypatch.setenv("SWIGLU_SK_NB", "1")
     p = swg.down_plan(M, 14336, 4096)
     assert p["path"] == "skinny" and p["cluster"] == 4 and p["workspace"] == 0
     check(M, 14336, 4096, "auto", seed=M, rows=tile_rows(M, seed=M))
 
 
-@pytest.mark.parametrize("M", [1, 16, 32, 65, 128, 256])
+@pytest.mark.parametrize("M", [1, 16, 32, 48, 65, 128, 256])
 def test_skinny_two_kernel_rows(M):
-    # Outside that band AUTO runs the skinny kernel's stream-K form on every
-    # SM and adds the partial sums in a second kernel; every column of rows
-    # of every 128-row block against the oracle
+    # AUTO runs the bf16 down projection on the skinny kernel's stream-K
+    # form on every SM and adds the partial sums in a second kernel; every
+    # column of rows of every 128-row block against the oracle
     p = swg.down_plan(M, 14336, 4096, "bf16", "auto", 0)
     assert p["path"] == "skinny" and p["cluster"] == 1 and p["launches"] == 2
     rows = np.arange(M) if M <= 32 else tile_rows(M, seed=M)

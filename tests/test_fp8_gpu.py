@@ -243,6 +243,6 @@ def test_fp8_down_final_sum_routes(M, monkeypatch):
 @pytest.mark.parametrize("M", [16, 64, 128, 256])
 def test_fp8_down_cluster4(M):
     # FP8 down projection at d = 4096: 4-CTA clusters of 128-column groups
-    # for M = 16 .. 128, stream-K with the second kernel's sums above; every
+    # for M = 16 .. 64, stream-K with the second kernel's sums above; every
     # column of rows of every 128-row block
     down_check(M, 14336, 4096, "auto", seed=M + 9, rows=tile_rows(M, seed=M))
