@@ -74,8 +74,9 @@ def bench_config():
     """The `config` both arms print (identical, so the two lines describe the
     same workload)."""
     return {"workload": WORKLOAD, "weights": "N(0,1/d) bf16, seed 0",
-            "l2": "inputs larger than L2: 235 MB of weights per call, and distinct weight "
-                  "copies rotated per call"}
+            "l2": "inputs larger than L2: 235 MB of weights per call, distinct weight "
+                  "copies rotated per call, at least 2 GiB of them (no call finds an "
+                  "earlier call's weights in L2)"}
 
 
 def torchrun_argv(args, argv):
@@ -107,6 +108,24 @@ def dist_env():
 
 
 TRAFFIC_FILE = os.path.join("profiles", "skinny_decode_traffic.json")
+
+
+# Distinct weight bytes rotated through in every timed loop.  Weights are
+# streamed with an L2 evict-first hint, and on GB300 a part of a weight set
+# read two calls earlier was measured to still hit in L2 when fewer than
+# about 1 GB of other weights came in between (the decode call at d = 4096,
+# M = 1: 36.2 us with 2 copies of 235 MB, 38.4 us from 8 copies on; plain
+# loads show no such effect).  A model's layers each read their own weights
+# once per token, so the timed loops rotate at least 2 GiB of copies.
+WEIGHT_FOOTPRINT = 2 << 30
+
+
+def copies_for(l2, nbytes):
+    """Weight copies rotated per call: at least 3 L2 capacities and
+    WEIGHT_FOOTPRINT bytes of distinct weights, so that no call finds the
+    weights of an earlier one in L2."""
+    nbytes = max(int(nbytes), 1)
+    return max(2, math.ceil(3 * l2 / nbytes), math.ceil(WEIGHT_FOOTPRINT / nbytes))
 
 
 def profiled_traffic():
@@ -360,10 +379,10 @@ def run_ours(args):
     # the sweep per rank), or its 64-aligned share (--split columns)
     c0, c1 = (0, D_FF) if args.split == "replicas" else sharding.column_range(D_FF, rank, world)
     n_cols = c1 - c0
-    # weights: enough distinct copies that no call finds the previous call's
-    # weights in L2 (each copy of the full matrices, 235 MB, is already larger)
+    # weights: enough distinct copies that no call finds an earlier call's
+    # weights in L2 (copies_for)
     w_bytes = 2 * D * max(n_cols, 1) * 2
-    n_copies = max(2, math.ceil(3 * l2 / w_bytes))
+    n_copies = copies_for(l2, w_bytes)
     _, wg_h, wu_h = inputs.make_inputs(1, D, D_FF, "bf16", seed=0)
     wg_s, wu_s = wg_h[:, c0:c1].contiguous(), wu_h[:, c0:c1].contiguous()
     copies = [(wg_s.to(dev), wu_s.to(dev)) for _ in range(n_copies)]
@@ -666,7 +685,7 @@ def other_configs(dev, peaks, l2, iters, oracle_leg=False, sampler=None):
             continue
         _, wg, wu = inputs.make_inputs(1, cfg.d, cfg.d_ff, cfg.dtype, seed=0)
         w_bytes = 2 * wg.numel() * wg.element_size()
-        n_copies = max(2, math.ceil(3 * l2 / w_bytes))
+        n_copies = copies_for(l2, w_bytes)
         copies = [(wg.to(dev), wu.to(dev)) for _ in range(n_copies)]
         for M in cfg.Ms:
             x_h = inputs.make_inputs(M, cfg.d, cfg.d_ff, cfg.dtype, seed=0, x_only=True)[0]
@@ -750,10 +769,6 @@ def clocks_of(sampler, w0, w1):
     return {"sm_mhz": cs["sm_mhz"], "reasons": cs["reasons"], "samples": cs.get("samples", 0)}
 
 
-def copies_for(l2, nbytes):
-    """Weight copies rotated per call so that a call's weights were last read
-    at least 3 L2 capacities ago."""
-    return max(2, math.ceil(3 * l2 / nbytes))
 
 
 def fp8_configs(dev, peaks, l2, iters, sampler=None):

@@ -84,3 +84,14 @@ def test_gpus_must_match_world_size(monkeypatch, capsys):
     monkeypatch.setattr("sys.argv", ["bench.py", "--gpus", "3", "--impl", "reference"])
     assert bench.main() == 2
     assert "WORLD_SIZE=2" in capsys.readouterr().err
+
+
+def test_weight_copies_cover_the_footprint():
+    # every timed loop rotates at least 3 L2 capacities and 2 GiB of distinct
+    # weights (the headline's 235 MB copies, FP8's 117 MB, d = 8192's 969 MB)
+    l2 = 129 << 20
+    for nbytes in (8 << 20, 17_432_576, 117_440_512, 234_881_024, 968_884_224, 4 << 30):
+        n = bench.copies_for(l2, nbytes)
+        assert n >= 2
+        assert n * nbytes >= 3 * l2 and n * nbytes >= bench.WEIGHT_FOOTPRINT
+        assert (n - 1) * nbytes < max(3 * l2, bench.WEIGHT_FOOTPRINT) or n == 2
