@@ -26,10 +26,12 @@ struct SimtPlan {
 };
 
 // Tuning overrides from the environment (SWIGLU_SK_NB, SWIGLU_SK_PROMO,
-// SWIGLU_SK_HINT, SWIGLU_SK_PREFETCH_UNITS, SWIGLU_SK_CLUSTER, SWIGLU_TILE_PAIR,
-// SWIGLU_TILE_SK, SWIGLU_TILE_SK_SPLIT, SWIGLU_TILE_SEQ, SWIGLU_SIMT_FUSED),
-// read in one pass over the environment for every planned call, so a process
-// may change them between calls.  -1: not set (the measured default applies).
+// SWIGLU_SK_HINT, SWIGLU_SK_PREFETCH_UNITS, SWIGLU_SK_CLUSTER, SWIGLU_SK_BULK,
+// SWIGLU_SK_SPLIT, SWIGLU_TILE_PAIR, SWIGLU_TILE_SK, SWIGLU_TILE_SK_SPLIT,
+// SWIGLU_TILE_SEQ, SWIGLU_TILE_BAND, SWIGLU_SIMT_FUSED, SWIGLU_SIMT_CLUSTER,
+// SWIGLU_INJECT_OOM), read in one pass over the environment for every planned
+// call, so a process may change them between calls.  -1: not set (the
+// measured default applies).
 struct Tuning {
   int sk_nb = -1, sk_promo = -1, sk_hint = -1, sk_prefetch_units = -1, sk_cluster = -1;
   int tile_pair = -1, tile_sk = -1, tile_sk_split = -1, tile_seq = -1, tile_band = -1;
@@ -37,7 +39,8 @@ struct Tuning {
   int sk_bulk = -1;   // skinny stream-K final sums staged by bulk copies (default on)
   int sk_split = -1;  // skinny stream-K final sums in a second kernel (1) or by the
                       // group's last CTA (0)
-  int simt_cluster = -1;   // 0: never use the cluster form of the SIMT path
+  int simt_cluster = -1;   // 0: never use the cluster form of the SIMT path;
+                           // 4..8: that many K slices per cluster
   // Test hook (SWIGLU_INJECT_OOM=1): every workspace the library would take
   // from its pool or its per-stream cache fails to allocate, so the call
   // returns SWIGLU_ERR_OOM having enqueued nothing.  Caller workspaces and
