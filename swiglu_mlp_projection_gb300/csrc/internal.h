@@ -27,7 +27,7 @@ struct SimtPlan {
 
 // Tuning overrides from the environment (SWIGLU_SK_NB, SWIGLU_SK_PROMO,
 // SWIGLU_SK_HINT, SWIGLU_SK_PREFETCH_UNITS, SWIGLU_SK_CLUSTER, SWIGLU_SK_BULK,
-// SWIGLU_SK_SPLIT, SWIGLU_TILE_PAIR, SWIGLU_TILE_SK, SWIGLU_TILE_SK_SPLIT,
+// SWIGLU_SK_SPLIT, SWIGLU_SK_KB, SWIGLU_TILE_PAIR, SWIGLU_TILE_SK, SWIGLU_TILE_SK_SPLIT,
 // SWIGLU_TILE_SEQ, SWIGLU_TILE_BAND, SWIGLU_SIMT_FUSED, SWIGLU_SIMT_CLUSTER,
 // SWIGLU_INJECT_OOM), read in one pass over the environment for every planned
 // call, so a process may change them between calls.  -1: not set (the
@@ -37,6 +37,7 @@ struct Tuning {
   int tile_pair = -1, tile_sk = -1, tile_sk_split = -1, tile_seq = -1, tile_band = -1;
   int simt_fused = -1;
   int sk_bulk = -1;   // skinny stream-K final sums staged by bulk copies (default on)
+  int sk_kb = -1;     // skinny FP8: 64-deep k blocks per unit (1 or 2)
   int sk_split = -1;  // skinny stream-K final sums in a second kernel (1) or by the
                       // group's last CTA (0)
   int simt_cluster = -1;   // 0: never use the cluster form of the SIMT path;
@@ -120,6 +121,7 @@ cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, 
 struct SkinnyPlan {
   int n_pad;               // M rounded up to the MMA N granule (16..256)
   int nb;                  // 64-column blocks per unit (1, 2 or 4)
+  int kb;                  // 64-deep k blocks per unit (1, or 2 for FP8)
   int l2_promo;            // L2 promotion of the weight loads (bytes, 0 = none)
   int hint;                // weight-load L2 hint: 0 none, 1 evict_first
   bool plain;              // plain epilogue (down projection) instead of SwiGLU

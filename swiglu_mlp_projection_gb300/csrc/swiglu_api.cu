@@ -379,6 +379,7 @@ Tuning read_tuning() {
                           {"SIMT_FUSED", &t.simt_fused},
                           {"SK_BULK", &t.sk_bulk},
                           {"SK_SPLIT", &t.sk_split},
+                          {"SK_KB", &t.sk_kb},
                           {"SIMT_CLUSTER", &t.simt_cluster},
                           {"INJECT_OOM", &t.inject_oom}};
     for (const Knob& k : knobs)

@@ -84,10 +84,13 @@ constexpr uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
 
 // N: MMA N (M of the call rounded up); NB: adjacent 64-column blocks per unit,
 // so every weight row is read in NB x 128-byte contiguous runs per matrix.
-template <int N, int NB>
+// KB: 64-deep k blocks per unit (and stage); with [n_out, K] weights a unit
+// then reads KB x 128 contiguous bytes of every weight row it covers.
+template <int N, int NB, int KB = 1>
 struct SkCfg {
   static constexpr uint32_t kBTileBytes = (uint32_t)N * kBK * 2;
-  static constexpr uint32_t kStageBytes = NB * kSubBytes + kBTileBytes;
+  static constexpr uint32_t kKBlockBytes = NB * kSubBytes + kBTileBytes;   // one k block
+  static constexpr uint32_t kStageBytes = KB * kKBlockBytes;
   static constexpr int kFit = (int)(kRingBudget / kStageBytes);
   static constexpr int kStages = kFit > 12 ? 12 : kFit;
   static constexpr uint32_t kAccCols = (uint32_t)NB * N;          // one accumulator buffer
@@ -116,6 +119,7 @@ struct SkArgs {
   int split;            // stream-K: write the partial sums only (skinny_sum_kernel adds them)
   int nb;               // 64-column blocks per unit (the sum kernel's slot layout)
   int release_early;    // the sum kernel releases the next kernel before its wait
+  int k64;              // 64-deep k blocks of K (a unit's k blocks past it are skipped)
   float* part;          // [n_cg][maxq][NB][2][M][64]
   unsigned* counters;   // [n_cg], zero on entry, zero again on exit
   uint16_t* out;        // [M][n_out] bf16
@@ -188,12 +192,12 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, unsig
 // FP8: e4m3 operands (kind::f8f6f4) and scaled sums.  A compile-time choice:
 // one kernel issuing MMAs of two kinds behind a runtime branch measured
 // 20-40 % slower on its bf16 work.
-template <int N, int NB, int MODE, bool FP8>
+template <int N, int NB, int MODE, bool FP8, int KB>
 __global__ void __launch_bounds__(kThreads, 1)
 skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                  const __grid_constant__ CUtensorMap tm_wg,
                  const __grid_constant__ CUtensorMap tm_wu, const SkArgs a) {
-  using C = SkCfg<N, NB>;
+  using C = SkCfg<N, NB, KB>;
   // Weight columns of one unit's sub-block, and where its two 64-column
   // boxes come from: (tm_wg, col) and (tm_wu, col) for SwiGLU, (tm_wg, col)
   // and (tm_wg, col + 64) for the plain mode.
@@ -265,16 +269,21 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
   if (warp == 0 && lane == 0) {
     const int64_t pend = min(u1, u0 + (int64_t)a.prefetch_units);
     for (int64_t t = u0; t < pend; ++t) {
-      const int cg = (int)(t / a.n_kb), kb = (int)(t - (int64_t)cg * a.n_kb);
+      const int cg = (int)(t / a.n_kb), kbu = (int)(t - (int64_t)cg * a.n_kb);
 #pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        const int col = (cg * NB + b) * kSubCols * col_mul;
-        if (a.kmajor) {
-          tma_prefetch_l2_2d(&tm_wg, kb * kBK, col);
-          tma_prefetch_l2_2d(hi_map, kb * kBK, col + kHiOff);
-        } else {
-          tma_prefetch_l2_2d(&tm_wg, col, kb * kBK);
-          tma_prefetch_l2_2d(hi_map, col + kHiOff, kb * kBK);
+      for (int j = 0; j < KB; ++j) {
+        const int kb = kbu * KB + j;
+        if (KB > 1 && kb >= a.k64) break;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const int col = (cg * NB + b) * kSubCols * col_mul;
+          if (a.kmajor) {
+            tma_prefetch_l2_2d(&tm_wg, kb * kBK, col);
+            tma_prefetch_l2_2d(hi_map, kb * kBK, col + kHiOff);
+          } else {
+            tma_prefetch_l2_2d(&tm_wg, col, kb * kBK);
+            tma_prefetch_l2_2d(hi_map, col + kHiOff, kb * kBK);
+          }
         }
       }
     }
@@ -291,29 +300,37 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
       int64_t issued = 0;
       bool ok = true;
       for (int64_t t = u0; t < u1; ++t) {
-        const int cg = (int)(t / a.n_kb), kb = (int)(t - (int64_t)cg * a.n_kb);
+        const int cg = (int)(t / a.n_kb), kbu = (int)(t - (int64_t)cg * a.n_kb);
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.status, a.timeout_ns)) {
           ok = false;
           break;
         }
         uint8_t* st = stages + (size_t)stage * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+        // k blocks of this unit inside K (a unit of KB > 1 blocks may end past it)
+        const int nkb = KB > 1 ? min(KB, a.k64 - kbu * KB) : 1;
+        mbar_arrive_expect_tx(&full[stage], (uint32_t)nkb * C::kKBlockBytes);
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          const int col = (cg * NB + b) * kSubCols * col_mul;
-          uint8_t* sb = st + b * kSubBytes;
-          // [K, n_out] weights: box (col, k); [n_out, K] weights: box (k, col).
-          const int c0 = a.kmajor ? kb * kBK : col, c1 = a.kmajor ? col : kb * kBK;
-          const int h0 = a.kmajor ? kb * kBK : col + kHiOff, h1 = a.kmajor ? col + kHiOff : kb * kBK;
-          if (a.hint) {
-            tma_load_2d_hint(sb, &tm_wg, &full[stage], c0, c1, evict_first);
-            tma_load_2d_hint(sb + kChunkBytes, hi_map, &full[stage], h0, h1, evict_first);
-          } else {
-            tma_load_2d(sb, &tm_wg, &full[stage], c0, c1);
-            tma_load_2d(sb + kChunkBytes, hi_map, &full[stage], h0, h1);
+        for (int j = 0; j < KB; ++j) {
+          if (j >= nkb) break;
+          const int kb = kbu * KB + j;
+          uint8_t* sk = st + j * C::kKBlockBytes;
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            const int col = (cg * NB + b) * kSubCols * col_mul;
+            uint8_t* sb = sk + b * kSubBytes;
+            // [K, n_out] weights: box (col, k); [n_out, K] weights: box (k, col).
+            const int c0 = a.kmajor ? kb * kBK : col, c1 = a.kmajor ? col : kb * kBK;
+            const int h0 = a.kmajor ? kb * kBK : col + kHiOff, h1 = a.kmajor ? col + kHiOff : kb * kBK;
+            if (a.hint) {
+              tma_load_2d_hint(sb, &tm_wg, &full[stage], c0, c1, evict_first);
+              tma_load_2d_hint(sb + kChunkBytes, hi_map, &full[stage], h0, h1, evict_first);
+            } else {
+              tma_load_2d(sb, &tm_wg, &full[stage], c0, c1);
+              tma_load_2d(sb + kChunkBytes, hi_map, &full[stage], h0, h1);
+            }
           }
+          tma_load_2d(sk + NB * kSubBytes, &tm_x, &full[stage], kb * kBK, 0);
         }
-        tma_load_2d(st + NB * kSubBytes, &tm_x, &full[stage], kb * kBK, 0);
         ++issued;
         if (++stage == C::kStages) {
           stage = 0;
@@ -363,23 +380,29 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             break;
           }
           tc_fence_after();
-          const uint32_t s_addr = smem_u32(stages + (size_t)stage * C::kStageBytes);
-          const uint32_t b_addr = s_addr + NB * kSubBytes;
+          const int nkb = KB > 1 ? min(KB, a.k64 - (int)(tt - cg * a.n_kb) * KB) : 1;
 #pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            const uint32_t d_tmem = tmem + (uint32_t)(acc * C::kAccCols + b * N);
+          for (int j = 0; j < KB; ++j) {
+            if (j >= nkb) break;
+            const uint32_t s_addr =
+                smem_u32(stages + (size_t)stage * C::kStageBytes + j * C::kKBlockBytes);
+            const uint32_t b_addr = s_addr + NB * kSubBytes;
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              // A: 16 k-rows further down the MN-major tile (2 swizzle atoms);
-              // B: 32 bytes further along the K-major 128-byte rows.
-              const uint64_t ad =
-                  smem_desc_sw128(s_addr + b * kSubBytes + kk * a_step, a_lbo, 1024u);
-              const uint64_t bd = smem_desc_sw128(b_addr + kk * 32u, 16u, 1024u);
-              const uint32_t accum = (tt != t || kk != 0) ? 1u : 0u;
-              if constexpr (FP8)
-                mma_e4m3(d_tmem, ad, bd, idesc, accum);
-              else
-                mma_bf16(d_tmem, ad, bd, idesc, accum);
+            for (int b = 0; b < NB; ++b) {
+              const uint32_t d_tmem = tmem + (uint32_t)(acc * C::kAccCols + b * N);
+#pragma unroll
+              for (int kk = 0; kk < kBK / 16; ++kk) {
+                // A: 16 k-rows further down the MN-major tile (2 swizzle atoms);
+                // B: 32 bytes further along the K-major 128-byte rows.
+                const uint64_t ad =
+                    smem_desc_sw128(s_addr + b * kSubBytes + kk * a_step, a_lbo, 1024u);
+                const uint64_t bd = smem_desc_sw128(b_addr + kk * 32u, 16u, 1024u);
+                const uint32_t accum = (tt != t || j != 0 || kk != 0) ? 1u : 0u;
+                if constexpr (FP8)
+                  mma_e4m3(d_tmem, ad, bd, idesc, accum);
+                else
+                  mma_bf16(d_tmem, ad, bd, idesc, accum);
+              }
             }
           }
           mma_commit(&empty[stage]);
@@ -841,11 +864,11 @@ cudaError_t launch_sum(const SkArgs& a, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, skinny_sum_kernel<MODE, FP8>, a);
 }
 
-template <int N, int NB, int MODE, bool FP8>
+template <int N, int NB, int MODE, bool FP8, int KB = 1>
 cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mg, const CUtensorMap& mu,
                      const SkArgs& a, cudaStream_t st) {
-  using C = SkCfg<N, NB>;
-  auto kern = skinny_tc_kernel<N, NB, MODE, FP8>;
+  using C = SkCfg<N, NB, KB>;
+  auto kern = skinny_tc_kernel<N, NB, MODE, FP8, KB>;
   static std::atomic<int> configured[64];   // zero: not yet set on that device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -874,8 +897,14 @@ cudaError_t launch_n(const CUtensorMap& mx, const CUtensorMap& mg, const CUtenso
 }
 
 template <int N, int MODE, bool FP8>
-cudaError_t launch_nb(int nb, const CUtensorMap& mx, const CUtensorMap& mg,
+cudaError_t launch_nb(int nb, int kb, const CUtensorMap& mx, const CUtensorMap& mg,
                       const CUtensorMap& mu, const SkArgs& a, cudaStream_t st) {
+  // two k blocks per unit: FP8 ([n_out, K] codes), one column block, N <= 64
+  if constexpr (FP8 && N <= 64) {
+    if (kb == 2) return nb == 1 ? launch_n<N, 1, MODE, FP8, 2>(mx, mg, mu, a, st)
+                                : cudaErrorInvalidValue;
+  }
+  if (kb != 1) return cudaErrorInvalidValue;
   if constexpr (N <= 64) {
     if (nb == 4) return launch_n<N, 4, MODE, FP8>(mx, mg, mu, a, st);
   }
@@ -887,14 +916,14 @@ cudaError_t launch_nb(int nb, const CUtensorMap& mx, const CUtensorMap& mg,
 }
 
 template <int MODE, bool FP8>
-cudaError_t launch_mode(int n_pad, int nb, const CUtensorMap& mx, const CUtensorMap& mg,
+cudaError_t launch_mode(int n_pad, int nb, int kb, const CUtensorMap& mx, const CUtensorMap& mg,
                         const CUtensorMap& mu, const SkArgs& a, cudaStream_t st) {
   switch (n_pad) {
-    case 16: return launch_nb<16, MODE, FP8>(nb, mx, mg, mu, a, st);
-    case 32: return launch_nb<32, MODE, FP8>(nb, mx, mg, mu, a, st);
-    case 64: return launch_nb<64, MODE, FP8>(nb, mx, mg, mu, a, st);
-    case 128: return launch_nb<128, MODE, FP8>(nb, mx, mg, mu, a, st);
-    case 256: return launch_nb<256, MODE, FP8>(nb, mx, mg, mu, a, st);
+    case 16: return launch_nb<16, MODE, FP8>(nb, kb, mx, mg, mu, a, st);
+    case 32: return launch_nb<32, MODE, FP8>(nb, kb, mx, mg, mu, a, st);
+    case 64: return launch_nb<64, MODE, FP8>(nb, kb, mx, mg, mu, a, st);
+    case 128: return launch_nb<128, MODE, FP8>(nb, kb, mx, mg, mu, a, st);
+    case 256: return launch_nb<256, MODE, FP8>(nb, kb, mx, mg, mu, a, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -972,6 +1001,19 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
     if (groups1 <= cap2 && (K + kBK - 1) / kBK >= 2) nb = 1;
   }
   while (nb > 1 && nb * n > 256) nb /= 2;
+  // FP8 ([n_out, K] codes) in 4-CTA clusters: two 64-deep k blocks of one
+  // column block per unit, so every weight row is read 256 contiguous bytes
+  // at a time instead of 128 (SWIGLU_SK_KB forces 1 or 2).  Measured with 2
+  // GiB of weights rotating, the FP8 down projection at d = 4096, M = 16 /
+  // 64: 16.5 / 18.9 us against 17.7 / 20.4; in stream-K mode it measured
+  // slower (up projection M = 1 / 16: 26.9 / 29.0 against 25.4 / 27.4 us;
+  // down M = 1: 17.8 against 17.2).
+  p.kb = 1;
+  const bool kb2 = tn.sk_kb >= 0 ? tn.sk_kb == 2 : plain_cluster4;
+  if (fp8 && n <= 64 && kb2) {
+    p.kb = 2;
+    nb = 1;
+  }
   p.nb = nb;
   p.l2_promo = tn.sk_promo >= 0 ? tn.sk_promo : 128;
   p.hint = tn.sk_hint >= 0 ? tn.sk_hint : 1;
@@ -982,22 +1024,22 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   // within noise or up to 3 % slower.
   p.bulk = tn.sk_bulk >= 0 ? (tn.sk_bulk != 0) : (plain && M >= 16);
   // L2 prefetch budget per CTA (measured, calls back to back): 512 KB for
-  // bf16 SwiGLU; 384 KB for the FP8 up projection (d = 4096, M = 1 / 16:
-  // 21.9 / 23.2 us against 22.6 / 24.0 at 256 KB and 22.0 / 23.1 at 512
-  // KB).  Down projection: 256 KB with 256-column groups (d = 4096, M = 1 /
+  // the up projection (FP8 with 2 GiB of weights rotating, d = 4096, M = 1 /
+  // 16 / 32: 24.4 / 26.1 / 28.8 us against 25.4 / 27.4 / 30.5 at 384 KB).
+  // Down projection: 256 KB with 256-column groups (d = 4096, M = 1 /
   // 16 / 24: 21.0 / 21.1 / 23.9 us, against 21.7 / 22.3 / 24.0 at 128 KB
   // and 22.5 / 22.8 / 25.0 at 512 KB; d = 8192 M = 32: 74.6 against 76.3
   // at 64 KB), 64 KB with the 128-column groups of larger M (d = 4096, M =
   // 96 / 128 / 256: 26.9 / 27.1 / 32.3 us against 28.7 / 29.0 / 34.0 at 256
   // KB; FP8 M = 256: 26.9 against 28.1).
   const uint32_t pf_bytes = plain ? (nb == 1 ? kPrefetchBytes / 8 : kPrefetchBytes / 2)
-                                  : (fp8 ? kPrefetchBytes / 4 * 3 : kPrefetchBytes);
+                                  : kPrefetchBytes;
   p.prefetch_units = tn.sk_prefetch_units >= 0 ? tn.sk_prefetch_units
-                                               : (int)(pf_bytes / ((uint32_t)nb * kSubBytes));
+                                               : (int)(pf_bytes / ((uint32_t)(nb * p.kb) * kSubBytes));
   const int64_t sub_cols = plain ? 2 * kCB : kCB;
   const int64_t subs = (n_out + sub_cols - 1) / sub_cols;
   p.n_cb = (subs + nb - 1) / nb;
-  p.n_kb = (K + kBK - 1) / kBK;
+  p.n_kb = (K + kBK * p.kb - 1) / (kBK * p.kb);
   p.units = p.n_cb * p.n_kb;
   p.grid = (int)(p.units < num_sms ? p.units : num_sms);
   if (p.grid < 1) p.grid = 1;
@@ -1056,7 +1098,7 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
 
 cudaError_t skinny_cluster_caps(int caps[4]) {
   using C = SkCfg<16, 2>;
-  auto kern = skinny_tc_kernel<16, 2, kSwiGLU, false>;
+  auto kern = skinny_tc_kernel<16, 2, kSwiGLU, false, 1>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -1121,6 +1163,7 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   a.split = p.split;
   a.nb = p.nb;
   a.release_early = fp8 ? 1 : 0;
+  a.k64 = (int)((K + kBK - 1) / kBK);
   a.cluster = p.cluster;
   a.part = part;
   a.counters = counters;
@@ -1129,11 +1172,11 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   a.status = status;
   a.timeout_ns = timeout_ns;
   if (p.plain)
-    e = fp8 ? launch_mode<kPlain, true>(p.n_pad, p.nb, mx, mg, mu, a, st)
-            : launch_mode<kPlain, false>(p.n_pad, p.nb, mx, mg, mu, a, st);
+    e = fp8 ? launch_mode<kPlain, true>(p.n_pad, p.nb, p.kb, mx, mg, mu, a, st)
+            : launch_mode<kPlain, false>(p.n_pad, p.nb, p.kb, mx, mg, mu, a, st);
   else
-    e = fp8 ? launch_mode<kSwiGLU, true>(p.n_pad, p.nb, mx, mg, mu, a, st)
-            : launch_mode<kSwiGLU, false>(p.n_pad, p.nb, mx, mg, mu, a, st);
+    e = fp8 ? launch_mode<kSwiGLU, true>(p.n_pad, p.nb, p.kb, mx, mg, mu, a, st)
+            : launch_mode<kSwiGLU, false>(p.n_pad, p.nb, p.kb, mx, mg, mu, a, st);
   if (e != cudaSuccess || !a.split) return e;
   if (p.plain) return fp8 ? launch_sum<kPlain, true>(a, st) : launch_sum<kPlain, false>(a, st);
   return fp8 ? launch_sum<kSwiGLU, true>(a, st) : launch_sum<kSwiGLU, false>(a, st);

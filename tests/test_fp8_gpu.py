@@ -246,3 +246,20 @@ def test_fp8_down_cluster4(M):
     # for M = 16 .. 64, stream-K with the second kernel's sums above; every
     # column of rows of every 128-row block
     down_check(M, 14336, 4096, "auto", seed=M + 9, rows=tile_rows(M, seed=M))
+
+
+@pytest.mark.parametrize("op,mode,shape", [
+    ("up", "0", (5, 1040, 1032)), ("up", "0", (16, 4096, 1040)), ("up", "2", (3, 1040, 264)),
+    ("down", "0", (7, 1040, 520)), ("down", "4", (33, 14336, 4096)), ("down", "4", (16, 1040, 264))])
+def test_fp8_two_k_blocks_per_unit(op, mode, shape, monkeypatch):
+    # Units of two 64-deep k blocks (256 code bytes of every weight row), the
+    # 4-CTA cluster form's default and SWIGLU_SK_KB=2 elsewhere, in stream-K
+    # (mode 0) and cluster modes.  K = 1040 codes (520 pairs, 9 blocks) leaves
+    # the last unit's second block past K, which the kernel skips.
+    monkeypatch.setenv("SWIGLU_SK_KB", "2")
+    monkeypatch.setenv("SWIGLU_SK_CLUSTER", mode)
+    if op == "up":
+        check(*shape, "skinny", seed=sum(shape))
+    else:
+        down_check(*shape, "skinny", seed=sum(shape))
+    swg.check_device_status()
