@@ -965,7 +965,12 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
     const int64_t per2 = grid2 > 0 ? units2 / grid2 : 1;
     const int64_t slots2 = per2 > 0 ? (n_kb2 + per2 - 1) / per2 + 1 : 1;
     const int64_t limit = fp8 ? (int64_t)128 << 10 : (int64_t)256 << 10;
-    if (slots2 * 4 * kCB * 4 * M > limit) nb = 1;
+    // With the bf16 sums in a second kernel (the default, below) no single
+    // CTA reads a group's partials, and 256-column groups lead up to 48 rows
+    // (measured, 2 GiB of weights rotating, d = 4096, M = 32 / 48 / 64 / 128:
+    // 22.8 / 25.6 / 26.0 / 27.3 us against 23.6 / 25.8 / 26.0 / 27.0).
+    const bool two_kernels = !fp8 && tn.sk_split != 0;
+    if (two_kernels ? M > 48 : slots2 * 4 * kCB * 4 * M > limit) nb = 1;
   }
   // FP8 down projections of 16-64 rows: 4-CTA clusters of 128-column groups,
   // when all the groups' clusters fit at once (n_out up to 36 x 128 on

@@ -83,21 +83,25 @@ def slots(units, grid, n_kb):
     return -(-n_kb // per) + 1
 
 
-def test_down_projection_column_group_rule(cuda_lib):
-    # No override: 128-column groups once 256-column groups would collect
-    # more than 256 KB of partial sums per group (slots x 256 columns x M x
-    # 4 B); either way every group has enough slots.
-    for M in (1, 8, 16, 24, 32, 48, 64, 96, 128, 256):
+@pytest.mark.parametrize("split", ["default", "0"])
+def test_down_projection_column_group_rule(cuda_lib, split, monkeypatch):
+    # No override, sums in a second kernel (the bf16 default): 256-column
+    # groups up to 48 rows, 128-column groups above.  With the group's last
+    # CTA adding the sums (SWIGLU_SK_SPLIT=0): 128-column groups once
+    # 256-column groups would collect more than 256 KB of partial sums per
+    # group (slots x 256 columns x M x 4 B).  Either way every group has
+    # enough slots.
+    if split == "0":
+        monkeypatch.setenv("SWIGLU_SK_SPLIT", "0")
+    for M in (1, 8, 16, 24, 32, 48, 49, 64, 96, 128, 256):
         for d, d_ff in ((4096, 14336), (8192, 29568)):
             p = swg.down_plan(M, d_ff, d, "bf16", "skinny", 152)
-            if p["cluster"] == 4:
-                # d = 4096 from M = 24 on: 4-CTA clusters of 128-column groups,
-                # the four K quarters of a group meet on chip
-                assert d == 4096 and M >= 24 and p["workspace"] == 0
-                assert p["grid"] == -(-d // 128) * 4 and p["slices"] == 4
-                continue
+            assert p["cluster"] == 1 and p["launches"] == (1 if split == "0" else 2)
             _, _, n_kb2, units2, grid2 = geometry(M, d_ff, d, 2, True, 152)
-            nb = 1 if slots(units2, grid2, n_kb2) * 256 * 4 * M > 256 * 1024 else 2
+            if split == "0":
+                nb = 1 if slots(units2, grid2, n_kb2) * 256 * 4 * M > 256 * 1024 else 2
+            else:
+                nb = 1 if M > 48 else 2
             _, n_cb, n_kb, units, grid = geometry(M, d_ff, d, nb, True, 152)
             assert p["slices"] == slots(units, grid, n_kb), (M, d, nb)
             assert p["slices"] >= max_contributors(units, grid, n_kb, n_cb)
