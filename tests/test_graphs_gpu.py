@@ -148,3 +148,43 @@ def test_down_projection_in_a_graph(M):
     torch.cuda.synchronize()
     assert torch.equal(ref.view(torch.int16), y.view(torch.int16))
     swg.check_device_status()
+
+
+@pytest.mark.parametrize("M", [1, 16])
+def test_fp8_down_chain_in_a_graph(M):
+    # The FP8 down projection, d_ff = 14336 -> d = 4096: M = 1 runs three
+    # kernels (quantize h, partial sums, their sum, which releases the next
+    # kernel early), M = 16 two (quantize, 4-CTA clusters).  Three calls
+    # captured back to back, each on its own h and output: replays match the
+    # oracle and the direct calls bit for bit.
+    d_ff, d = 14336, 4096
+    dev = torch.device("cuda", 0)
+    _, wd, _ = inputs.make_inputs(1, d_ff, d, "bf16", seed=91)
+    w8 = swg.quantize_weight_fp8(wd.to(dev))
+    hs = [inputs.make_inputs(M, d_ff, 8, "bf16", seed=92 + i, x_only=True)[0].to(dev)
+          for i in range(3)]
+    r = inputs.make_inputs(M, d, 8, "bf16", seed=95, x_only=True)[0]
+    rs = r.to(dev)
+    ys = [torch.empty(M, d, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    for i in range(3):
+        swg.swiglu_down_fp8(hs[i], w8, residual=rs, out=ys[i])
+    torch.cuda.synchronize()
+    direct = [y.clone() for y in ys]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(3):
+            swg.swiglu_down_fp8(hs[i], w8, residual=rs, out=ys[i])
+    for y in ys:
+        y.fill_(float("nan"))
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    raw = inputs.raw_bits
+    for i in range(3):
+        assert torch.equal(direct[i].view(torch.int16), ys[i].view(torch.int16)), i
+    h_host = hs[2].cpu()
+    rows = np.unique(np.linspace(0, M - 1, 4).astype(int))
+    y64, sens = oracle.down_proj_fp8(raw(h_host[rows].contiguous()), raw(wd), raw(r[rows].contiguous()))
+    res = compare(ys[2].to("cpu", torch.float64).numpy()[rows], y64, sens, "bf16", d_ff)
+    assert res["ok"], (M, res)
+    swg.check_device_status()
