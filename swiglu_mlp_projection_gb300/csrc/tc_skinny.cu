@@ -73,6 +73,13 @@ constexpr uint32_t kChunkBytes = kCB * kBK * 2;       // one 64 x 64 bf16 weight
 constexpr uint32_t kSubBytes = 2 * kChunkBytes;       // gate box + up box = one MMA A tile
 constexpr uint32_t kPrefetchBytes = 512u * 1024u;     // weight bytes per CTA prefetched before the wait
 constexpr uint32_t kRingBudget = 200u * 1024u;        // shared memory for the stage ring
+// The decode rows' configuration (N = 16, two 64-column blocks per unit)
+// streams best with 4 stages of 34 KB in flight per SM rather than 5 or 6
+// (measured, 2 GiB of weights rotating, d = 4096: the up projection at
+// M = 1 / 16 takes 38.5 / 39.0 us with 4 stages, 39.0 / 39.4 with 5, 41.0 /
+// 41.2 with 6; the down projection M = 1 / 16: 22.3 / 22.5 against 22.7 /
+// 22.9); at N = 32 five stages lead (40.9 against 41.4 us with 3).
+constexpr uint32_t kRingBudgetN16 = 140u * 1024u;
 // Rows for which the FP8 down projection takes 4-CTA clusters (see plan_skinny)
 constexpr int64_t kPlainCluster4MinMFp8 = 16, kPlainCluster4MaxMFp8 = 64;
 
@@ -91,7 +98,8 @@ struct SkCfg {
   static constexpr uint32_t kBTileBytes = (uint32_t)N * kBK * 2;
   static constexpr uint32_t kKBlockBytes = NB * kSubBytes + kBTileBytes;   // one k block
   static constexpr uint32_t kStageBytes = KB * kKBlockBytes;
-  static constexpr int kFit = (int)(kRingBudget / kStageBytes);
+  static constexpr int kFit =
+      (int)(((N == 16 && NB == 2 && KB == 1) ? kRingBudgetN16 : kRingBudget) / kStageBytes);
   static constexpr int kStages = kFit > 12 ? 12 : kFit;
   static constexpr uint32_t kAccCols = (uint32_t)NB * N;          // one accumulator buffer
   static constexpr uint32_t kTmemCols = pow2_at_least(2 * kAccCols, 32);
