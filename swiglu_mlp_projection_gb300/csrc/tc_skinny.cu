@@ -1013,6 +1013,16 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
     const int64_t cap2 = cluster_caps ? cluster_caps[1] : (int64_t)(num_sms / 2);
     if (groups1 <= cap2 && (K + kBK - 1) / kBK >= 2) nb = 1;
   }
+  // Up projection above 32 MB of weights, up to 4 rows: units of four
+  // 64-column blocks, i.e. 512-byte runs of every weight row (1 KB with
+  // packed weights).  Measured with 2 GiB of weights rotating, d = 4096,
+  // M = 1 / 2 / 4 / 8: 38.0 / 38.0 / 38.1 / 38.7 us against 38.4 / 38.4 /
+  // 38.4 / 38.6 with two blocks; packed weights 36.9 / 37.0 / 37.3 / 37.9
+  // against 38.1 / 38.1 / 38.2 / 38.3.  At M = 16 four blocks are slower
+  // (40.0 against 38.7 us, packed).  Both layouts keep one rule, so that
+  // swiglu_workspace_bytes serves both.
+  if (!plain && !fp8 && tn.sk_nb < 0 && weight_bytes > kSkinnyClusterMaxWeightBytes && M <= 4)
+    nb = 4;
   while (nb > 1 && nb * n > 256) nb /= 2;
   // FP8 ([n_out, K] codes) in 4-CTA clusters: two 64-deep k blocks of one
   // column block per unit, so every weight row is read 256 contiguous bytes
