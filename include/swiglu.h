@@ -88,10 +88,22 @@ typedef enum {
  * cudaFreeAsync on `stream`), so calls on different streams never share it.
  * The buffer is cached per stream (up to 256 streams, 256 MB of partial sums
  * each) and reused by the stream's later calls; swiglu_release_stream_workspace
- * and swiglu_release_workspaces give it back.  The first call on a device
- * that uses arrival counters outside a CUDA-graph capture also creates a
- * 4 MB region of zeroed counters for captured calls, and waits for `stream`
- * once to do so.
+ * and swiglu_release_workspaces give it back.
+ * A call captured into a CUDA graph takes its workspace from memory the
+ * library allocates outside the graph. It switches the calling thread to
+ * relaxed capture mode for a cudaMalloc and a clearing memset on a private
+ * stream, then restores the mode. There is one zeroed slice per capture
+ * sequence and capturing stream, shared by that capture's calls on that
+ * stream, which run one after another.
+ *   - These slices are kept until the process exits, because the graph may be
+ *     replayed at any time; the release calls do not free them.
+ *   - Two instances (graph execs) of one captured graph must not run at the
+ *     same time.
+ *   - Past 8 GB of slices on a device, captures allocate inside the graph
+ *     instead (allocation and free nodes), taking their arrival counters from
+ *     a 4 MB zeroed region.  The first call on a device that uses arrival
+ *     counters outside a capture creates that region, and waits for `stream`
+ *     once to do so.
  * Errors: SWIGLU_ERR_INVALID_ARG, _ALIGNMENT, _ARCH, _OOM, _CUDA.
  */
 SWIGLU_API int swiglu_up(const void* x, const void* w_gate, const void* w_up, void* h,
@@ -378,7 +390,8 @@ SWIGLU_API int64_t swiglu_split_k_slices(int64_t K, int64_t col_blocks,
  *   those of streams already destroyed, and returns the library pool's unused
  *   memory to the driver.  Returns SWIGLU_OK or SWIGLU_ERR_CUDA.
  * swiglu_cached_workspace_bytes: bytes the cache holds on the current
- *   device (0 when no device is current).
+ *   device (0 when no device is current); the workspaces of captured calls
+ *   (see swiglu_up) are not part of the cache.
  * Neither release call may run while another thread enqueues calls of this
  * library on the same stream (release_stream) or device (release).
  */

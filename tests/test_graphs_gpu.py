@@ -188,3 +188,72 @@ def test_fp8_down_chain_in_a_graph(M):
     res = compare(ys[2].to("cpu", torch.float64).numpy()[rows], y64, sens, "bf16", d_ff)
     assert res["ok"], (M, res)
     swg.check_device_status()
+
+
+def _graph_node_types(graph):
+    # node types of a captured CUDA graph, through the driver API
+    import ctypes
+    cu = ctypes.CDLL("libcuda.so.1")
+    raw = graph.raw_cuda_graph()
+    count = ctypes.c_size_t(0)
+    assert cu.cuGraphGetNodes(ctypes.c_void_p(raw), None, ctypes.byref(count)) == 0
+    nodes = (ctypes.c_void_p * count.value)()
+    assert cu.cuGraphGetNodes(ctypes.c_void_p(raw), nodes, ctypes.byref(count)) == 0
+    types = []
+    for i in range(count.value):
+        t = ctypes.c_int(-1)
+        assert cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) == 0
+        types.append(t.value)
+    return types
+
+
+@pytest.mark.parametrize("op", ["up", "down"])
+def test_captured_calls_hold_only_kernel_nodes(op, monkeypatch):
+    # Calls captured into a graph take their workspace from a slice allocated
+    # outside the graph, so the graph holds kernel nodes only (no allocation,
+    # free or memset nodes between them, which would cut the programmatic
+    # overlap of consecutive calls); three calls share their capture's slice
+    # and replay to the direct calls' bits.
+    monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")     # stream-K: partial sums and counters
+    dev = torch.device("cuda", 0)
+    if op == "up":
+        M, K, N = 4, 1024, 4104
+        x, wg, wu = inputs.make_inputs(M, K, N, "bf16", seed=60)
+        xs = [inputs.make_inputs(M, K, 8, "bf16", seed=61 + i, x_only=True)[0].to(dev) for i in range(3)]
+        wgd, wud = wg.to(dev), wu.to(dev)
+        run = lambda i, out: swg.swiglu_up(xs[i], wgd, wud, out=out)
+    else:
+        M, K, N = 8, 4104, 1032
+        _, wd, _ = inputs.make_inputs(1, K, N, "bf16", seed=64)
+        xs = [inputs.make_inputs(M, K, 8, "bf16", seed=65 + i, x_only=True)[0].to(dev) for i in range(3)]
+        r = inputs.make_inputs(M, N, 8, "bf16", seed=68, x_only=True)[0].to(dev)
+        wdd = wd.to(dev)
+        run = lambda i, out: swg.swiglu_down(xs[i], wdd, residual=r, out=out)
+    assert swg.plan(M, K, N, "bf16", "auto", 0)["workspace"] > 0 if op == "up" else \
+        swg.down_plan(M, K, N, "bf16", "auto", 0)["workspace"] > 0
+    outs = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(3):
+            run(i, outs[i])
+    torch.cuda.synchronize()
+    direct = [o.clone() for o in outs]
+    try:
+        g = torch.cuda.CUDAGraph(keep_graph=True)
+    except TypeError:
+        pytest.skip("this PyTorch cannot keep the captured graph")
+    with torch.cuda.graph(g, stream=s):
+        for i in range(3):
+            run(i, outs[i])
+    types = _graph_node_types(g)
+    kernel = 0   # CU_GRAPH_NODE_TYPE_KERNEL
+    assert types and all(t == kernel for t in types), types
+    for o in outs:
+        o.fill_(float("nan"))
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for i in range(3):
+        assert torch.equal(direct[i].view(torch.int16), outs[i].view(torch.int16)), i
+    swg.check_device_status()
