@@ -257,3 +257,41 @@ def test_captured_calls_hold_only_kernel_nodes(op, monkeypatch):
     for i in range(3):
         assert torch.equal(direct[i].view(torch.int16), outs[i].view(torch.int16)), i
     swg.check_device_status()
+
+
+def test_forked_capture_gives_each_stream_its_own_workspace(monkeypatch):
+    # A capture forked onto two streams runs their calls concurrently on
+    # replay; each capturing stream takes its own workspace slice, so the
+    # stream-K partial sums of the two never mix: replays equal the direct
+    # calls bit for bit.
+    monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")
+    dev = torch.device("cuda", 0)
+    M, K, N = 8, 1024, 4104
+    _, wg, wu = inputs.make_inputs(1, K, N, "bf16", seed=70)
+    wgd, wud = wg.to(dev), wu.to(dev)
+    xs = [inputs.make_inputs(M, K, 8, "bf16", seed=71 + i, x_only=True)[0].to(dev) for i in range(6)]
+    outs = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(6)]
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    for s in (s1, s2):
+        s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s1):
+        for i in range(6):
+            swg.swiglu_up(xs[i], wgd, wud, out=outs[i])
+    torch.cuda.synchronize()
+    direct = [o.clone() for o in outs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s1):
+        s2.wait_stream(s1)
+        for i in range(3):
+            swg.swiglu_up(xs[i], wgd, wud, out=outs[i])                 # on s1
+            with torch.cuda.stream(s2):
+                swg.swiglu_up(xs[3 + i], wgd, wud, out=outs[3 + i])     # on s2, concurrently
+        s1.wait_stream(s2)
+    for o in outs:
+        o.fill_(float("nan"))
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for i in range(6):
+        assert torch.equal(direct[i].view(torch.int16), outs[i].view(torch.int16)), i
+    swg.check_device_status()
