@@ -42,10 +42,6 @@ constexpr int kMaxS = 8;                              // CTAs per cluster (K sli
 constexpr int kMinS = 4;
 constexpr int64_t kMaxWeightBytes = (int64_t)32 << 20;
 
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 template <bool BF16>
 __device__ __forceinline__ void unpack16(const uint4& v, float* f) {
   if constexpr (BF16) {
@@ -102,8 +98,8 @@ simt_cluster_kernel(const void* __restrict__ x_, const void* __restrict__ wg_,
     for (int i = 0; i < ROWS; ++i) {
       const int kk = k0 + grp + kGroups * i;
       if (kk < k1) {
-        prefetch_l2(wg + (size_t)kk * row_bytes);
-        prefetch_l2(wu + (size_t)kk * row_bytes);
+        tc::prefetch_l2(wg + (size_t)kk * row_bytes);
+        tc::prefetch_l2(wu + (size_t)kk * row_bytes);
       }
     }
   }

@@ -69,6 +69,14 @@ constexpr int kBK = 64;                               // k per stage (128-byte r
 constexpr int kCB = 64;                               // columns of one weight box
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
+// Warp whose lane 0 issues the L2 prefetch before the dependency wait: the
+// first epilogue warp, idle until the first accumulator is full.  Issued by
+// the TMA producer instead, the prefetch held it back from the wait for up
+// to 5 us when the TMA unit was busy (per-CTA %globaltimer trace), and the
+// main loop started late.  Measured, calls back to back, 2 GiB of weights
+// rotating: d = 4096 up projection, packed, M = 1 / 2 / 4: 36.9 / 37.1 /
+// 36.9 us against 38.4 / 38.4 / 38.1.
+constexpr int kPrefetchWarp = 2;
 constexpr uint32_t kChunkBytes = kCB * kBK * 2;       // one 64 x 64 bf16 weight box
 constexpr uint32_t kSubBytes = 2 * kChunkBytes;       // gate box + up box = one MMA A tile
 constexpr uint32_t kPrefetchBytes = 512u * 1024u;     // weight bytes per CTA prefetched before the wait
@@ -270,11 +278,12 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // Everything above overlaps the previous kernel's tail.  So does an L2
-  // prefetch of this CTA's first weight boxes: a prefetch only reads, and L2
-  // is where every later write lands, so it is safe before the wait.  From
+  // prefetch of this CTA's first weight boxes and of the x boxes they meet: a
+  // prefetch only reads, and L2 is where every later write lands, so it is
+  // safe before the wait.  From
   // the wait on, the kernel reads x and the workspace, which the previous
   // kernel may still be writing.
-  if (warp == 0 && lane == 0) {
+  if (warp == kPrefetchWarp && lane == 0) {
     const int64_t pend = min(u1, u0 + (int64_t)a.prefetch_units);
     for (int64_t t = u0; t < pend; ++t) {
       const int cg = (int)(t / a.n_kb), kbu = (int)(t - (int64_t)cg * a.n_kb);
@@ -282,6 +291,11 @@ skinny_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
       for (int j = 0; j < KB; ++j) {
         const int kb = kbu * KB + j;
         if (KB > 1 && kb >= a.k64) break;
+        // x too: the same argument holds, and a call whose x was evicted
+        // since it was written would otherwise wait a DRAM round trip for
+        // its first stage (the d = 4096 decode sweep, M = 1 ... 16 in turn:
+        // 0.4-0.6 % per step)
+        tma_prefetch_l2_2d(&tm_x, kb * kBK, 0);
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
           const int col = (cg * NB + b) * kSubCols * col_mul;
@@ -792,10 +806,14 @@ __global__ void __launch_bounds__(kSumThreads) skinny_sum_kernel(const SkArgs a)
   // next call's GEMM take the SMs this call's GEMM frees, and prefetch its
   // weights, one launch sooner.  Measured, FP8 down projection d = 4096,
   // M = 4 / 8: 16.9 / 17.0 us against 18.7 / 18.8 without (one-kernel form
-  // 17.4 / 18.0); for bf16 it measured 0.1-0.7 us slower.
+  // 17.4 / 18.0).  The bf16 down projection with 256-column groups gains
+  // too once the next GEMM prefetches more (see plan_skinny).
   if (a.release_early) pdl_launch_dependents();
-  pdl_wait();
-  pdl_launch_dependents();
+  // Everything up to the wait reads only the kernel's parameters: the
+  // chunk's index arithmetic (64-bit divisions, long enough to matter here:
+  // a per-CTA %globaltimer trace put this kernel at 1.8-3.4 us from its wait
+  // to its stores at M = 1) and an L2 prefetch of the residual and the
+  // column scales, which are inputs of the call like the weights.
   constexpr int kSubCols = MODE == kSwiGLU ? kCB : 2 * kCB;
   constexpr int kBatch = MODE == kSwiGLU ? 6 : 12;   // slots loaded per round
   const int64_t group_cols = (int64_t)a.nb * kSubCols;
@@ -816,8 +834,23 @@ __global__ void __launch_bounds__(kSumThreads) skinny_sum_kernel(const SkArgs a)
   const int blk = MODE == kSwiGLU ? (ch >> 4) * 2 : (ch >> 4);
   const float* p0 = a.part + cg * a.maxq * q_stride + blk * Mrow + (int64_t)m * kCB + (ch & 15) * 4;
   const int64_t o = (int64_t)m * a.n_out + col;
+  if (MODE == kPlain && (threadIdx.x & 7) == 0) {   // 8 chunks: 64 B of residual, 128 B of scales
+    if (a.resid) prefetch_l2(a.resid + o);
+    if (FP8) prefetch_l2(a.sw_a + col);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  // The residual and (FP8) the scales load with the partial sums, not after
+  // them.  Measured with the changes above, FP8 down projection d = 4096,
+  // calls back to back, M = 1 / 8: 15.9 / 16.5 us against 17.3 / 17.6.
   uint2 rv = make_uint2(0u, 0u);
   if (MODE == kPlain && a.resid) rv = __ldg(reinterpret_cast<const uint2*>(a.resid + o));
+  float sxm = 1.f;
+  float4 swv = make_float4(1.f, 1.f, 1.f, 1.f);
+  if (FP8 && MODE == kPlain) {
+    sxm = __ldcg(a.sx + m);
+    swv = __ldcg(reinterpret_cast<const float4*>(a.sw_a + col));
+  }
   float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
   for (int q0 = 0; q0 < n_contrib; q0 += kBatch) {
     float4 vg[kBatch], vu[kBatch];
@@ -843,8 +876,11 @@ __global__ void __launch_bounds__(kSumThreads) skinny_sum_kernel(const SkArgs a)
   if constexpr (MODE == kSwiGLU) {
     store_chunk<MODE, FP8>(a, g, u, m, col);
   } else {
-    // store_chunk's plain epilogue, with the residual loaded up front
-    if constexpr (FP8) fp8_scale1(g, a, m, col);
+    // store_chunk's plain epilogue (fp8_scale1's arithmetic), with the
+    // residual and the scales loaded up front
+    if constexpr (FP8) {
+      g.x *= sxm * swv.x; g.y *= sxm * swv.y; g.z *= sxm * swv.z; g.w *= sxm * swv.w;
+    }
     if (a.resid) {
       g.x += bf16_lo(rv.x); g.y += bf16_hi(rv.x);
       g.z += bf16_lo(rv.y); g.w += bf16_hi(rv.y);
@@ -1013,15 +1049,15 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
     const int64_t cap2 = cluster_caps ? cluster_caps[1] : (int64_t)(num_sms / 2);
     if (groups1 <= cap2 && (K + kBK - 1) / kBK >= 2) nb = 1;
   }
-  // Up projection above 32 MB of weights, up to 4 rows: units of four
+  // Up projection above 32 MB of weights, up to 8 rows: units of four
   // 64-column blocks, i.e. 512-byte runs of every weight row (1 KB with
   // packed weights).  Measured with 2 GiB of weights rotating, d = 4096,
-  // M = 1 / 2 / 4 / 8: 38.0 / 38.0 / 38.1 / 38.7 us against 38.4 / 38.4 /
-  // 38.4 / 38.6 with two blocks; packed weights 36.9 / 37.0 / 37.3 / 37.9
-  // against 38.1 / 38.1 / 38.2 / 38.3.  At M = 16 four blocks are slower
-  // (40.0 against 38.7 us, packed).  Both layouts keep one rule, so that
-  // swiglu_workspace_bytes serves both.
-  if (!plain && !fp8 && tn.sk_nb < 0 && weight_bytes > kSkinnyClusterMaxWeightBytes && M <= 4)
+  // packed weights, calls back to back: M = 1 / 4 / 8 / 16: 37.0 / 37.2 /
+  // 37.6 / 39.4 us against 37.0 / 37.2 / 38.5 / 38.9 with two blocks.  (Four
+  // blocks issue twice the prefetches per unit; before an epilogue warp
+  // issued them, M = 8 measured 38.7 against 38.6.)  Both layouts keep one
+  // rule, so that swiglu_workspace_bytes serves both.
+  if (!plain && !fp8 && tn.sk_nb < 0 && weight_bytes > kSkinnyClusterMaxWeightBytes && M <= 8)
     nb = 4;
   while (nb > 1 && nb * n > 256) nb /= 2;
   // FP8 ([n_out, K] codes) in 4-CTA clusters: two 64-deep k blocks of one
@@ -1046,17 +1082,26 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   // M <= 8 and for the up projection, whose final sums are short, it is
   // within noise or up to 3 % slower.
   p.bulk = tn.sk_bulk >= 0 ? (tn.sk_bulk != 0) : (plain && M >= 16);
-  // L2 prefetch budget per CTA (measured, calls back to back): 512 KB for
-  // the up projection (FP8 with 2 GiB of weights rotating, d = 4096, M = 1 /
-  // 16 / 32: 24.4 / 26.1 / 28.8 us against 25.4 / 27.4 / 30.5 at 384 KB).
-  // Down projection: 256 KB with 256-column groups (d = 4096, M = 1 /
-  // 16 / 24: 21.0 / 21.1 / 23.9 us, against 21.7 / 22.3 / 24.0 at 128 KB
-  // and 22.5 / 22.8 / 25.0 at 512 KB; d = 8192 M = 32: 74.6 against 76.3
-  // at 64 KB), 64 KB with the 128-column groups of larger M (d = 4096, M =
-  // 96 / 128 / 256: 26.9 / 27.1 / 32.3 us against 28.7 / 29.0 / 34.0 at 256
-  // KB; FP8 M = 256: 26.9 against 28.1).
-  const uint32_t pf_bytes = plain ? (nb == 1 ? kPrefetchBytes / 8 : kPrefetchBytes / 2)
-                                  : kPrefetchBytes;
+  // L2 prefetch budget per CTA, issued by an epilogue warp (measured, calls
+  // back to back, 2 GiB of weights rotating, d = 4096):
+  // - up projection: 512 KB with four-block units (packed, M = 1 / 4: 36.9
+  //   / 36.9 us against 37.4 / 37.3 at 384 KB and 38.9 / 39.4 at 1 MB; M = 8:
+  //   37.6 against 38.0 at 768 KB), 384 KB with two-block units (M = 16: 38.7
+  //   against 39.1 at 512 KB); FP8: 512 KB (M = 1 / 16: 23.8 / 25.7 us
+  //   against 24.9 / 26.0 at 768 KB).
+  // - down projection with 256-column groups, whose sum kernel releases the
+  //   next GEMM early (launch_skinny): 512 KB for bf16 (M = 1 / 16 / 48:
+  //   20.9 / 21.5 / 23.7 us against 22.0 / 22.9 / 25.7 at 384 KB; the 256 KB
+  //   of the one-kernel form, without the early release: 22.6 / 22.8 / 26.2),
+  //   384 KB for FP8 (M = 1 / 8: 15.6 / 16.2 against 15.9 / 16.4 at 256 KB);
+  //   64 KB with the 128-column groups of larger M (M = 96 / 128 / 256: 26.9
+  //   / 27.1 / 32.3 us against 28.7 / 29.0 / 34.0 at 256 KB; FP8 M = 256:
+  //   26.9 against 28.1).
+  uint32_t pf_bytes = kPrefetchBytes;
+  if (plain)
+    pf_bytes = nb == 1 ? kPrefetchBytes / 8 : (fp8 ? kPrefetchBytes / 4 * 3 : kPrefetchBytes);
+  else if (!fp8 && nb < 4)
+    pf_bytes = kPrefetchBytes / 4 * 3;
   p.prefetch_units = tn.sk_prefetch_units >= 0 ? tn.sk_prefetch_units
                                                : (int)(pf_bytes / ((uint32_t)(nb * p.kb) * kSubBytes));
   const int64_t sub_cols = plain ? 2 * kCB : kCB;
@@ -1185,7 +1230,11 @@ cudaError_t launch_skinny_tc(const void* x, const void* wa, const void* wb, void
   a.bulk = p.bulk;
   a.split = p.split;
   a.nb = p.nb;
-  a.release_early = fp8 ? 1 : 0;
+  // The sum kernel releases the next kernel before its own wait for FP8
+  // calls (the next one starts with the activation quantizer) and for the
+  // down projection's 256-column groups, whose next GEMM then prefetches 512
+  // KB while this call's sums run (see plan_skinny's prefetch budgets).
+  a.release_early = (fp8 || (p.plain && p.nb >= 2)) ? 1 : 0;
   a.k64 = (int)((K + kBK - 1) / kBK);
   a.cluster = p.cluster;
   a.part = part;
