@@ -1097,11 +1097,15 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   //   64 KB with the 128-column groups of larger M (M = 96 / 128 / 256: 26.9
   //   / 27.1 / 32.3 us against 28.7 / 29.0 / 34.0 at 256 KB; FP8 M = 256:
   //   26.9 against 28.1).
+  // - FP8 down projection in 4-CTA clusters: 384 KB too (M = 16 / 32 / 64:
+  //   15.8 / 16.8 / 18.5 us against 16.3 / 17.2 / 18.6 without; 64 or 128 KB
+  //   measured slower than none, and all 448 KB of a CTA's range no faster).
   uint32_t pf_bytes = kPrefetchBytes;
   if (plain)
     pf_bytes = nb == 1 ? kPrefetchBytes / 8 : (fp8 ? kPrefetchBytes / 4 * 3 : kPrefetchBytes);
   else if (!fp8 && nb < 4)
     pf_bytes = kPrefetchBytes / 4 * 3;
+  if (plain_cluster4) pf_bytes = kPrefetchBytes / 4 * 3;
   p.prefetch_units = tn.sk_prefetch_units >= 0 ? tn.sk_prefetch_units
                                                : (int)(pf_bytes / ((uint32_t)(nb * p.kb) * kSubBytes));
   const int64_t sub_cols = plain ? 2 * kCB : kCB;
@@ -1139,12 +1143,12 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   if (forced == 1 || forced == 2 || forced == 4 || forced == 8)
     p.cluster = p.n_kb >= forced ? forced : 0;
   if (p.cluster) p.grid = (int)(p.n_cb * p.cluster);
-  // Cluster mode: no L2 prefetch before the dependency wait (measured: the
-  // d = 896 up projection, graph replay, 6.8 / 9.7 us at M = 1 / 64 without
-  // it, 7.1 / 9.8 us with it; the d = 4096 down projection in 4-CTA
-  // clusters, back to back, 27.3 / 29.7 us at M = 64 / 128 without it, 29.8 /
-  // 31.9 us with it).
-  if (p.cluster && tn.sk_prefetch_units < 0) p.prefetch_units = 0;
+  // Cluster mode (small weights): no L2 prefetch before the dependency wait
+  // (measured, graph replay, d = 896: up projection M = 16 / 64: 6.9 / 8.1 us
+  // with or without it; down projection M = 1 / 16 / 64: 6.8 / 7.2 / 8.0 us
+  // without, 6.9 / 7.3 / 8.2 with 64 KB).  The FP8 down projection's 4-CTA
+  // clusters keep their budget (above).
+  if (p.cluster && !plain_cluster4 && tn.sk_prefetch_units < 0) p.prefetch_units = 0;
   const int64_t per = p.units > 0 ? p.units / p.grid : 1;   // fewest units a CTA gets
   p.maxq = (int)((p.n_kb + per - 1) / (per > 0 ? per : 1) + 1);
   p.counters_bytes = ((size_t)p.n_cb * sizeof(unsigned) + 255) / 256 * 256;
