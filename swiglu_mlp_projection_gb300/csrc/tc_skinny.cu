@@ -1060,15 +1060,18 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   if (!plain && !fp8 && tn.sk_nb < 0 && weight_bytes > kSkinnyClusterMaxWeightBytes && M <= 8)
     nb = 4;
   while (nb > 1 && nb * n > 256) nb /= 2;
-  // FP8 ([n_out, K] codes) in 4-CTA clusters: two 64-deep k blocks of one
-  // column block per unit, so every weight row is read 256 contiguous bytes
-  // at a time instead of 128 (SWIGLU_SK_KB forces 1 or 2).  Measured with 2
-  // GiB of weights rotating, the FP8 down projection at d = 4096, M = 16 /
-  // 64: 16.5 / 18.9 us against 17.7 / 20.4; in stream-K mode it measured
-  // slower (up projection M = 1 / 16: 26.9 / 29.0 against 25.4 / 27.4 us;
-  // down M = 1: 17.8 against 17.2).
+  // FP8 down projection ([n_out, K] codes) above 32 MB of weights: two
+  // 64-deep k blocks of one column block per unit, so every weight row is
+  // read 256 contiguous bytes at a time instead of 128 (SWIGLU_SK_KB forces
+  // 1 or 2).  Measured with 2 GiB of weights rotating, d = 4096: in 4-CTA
+  // clusters M = 16 / 64 take 16.5 / 18.9 us against 17.7 / 20.4; in
+  // stream-K mode, with the 384 KB prefetch below, M = 1 / 4 / 8 / 12 take
+  // 15.0 / 15.2 / 15.5 / 15.6 us against 15.5 / 15.8 / 16.0 / 17.8.  The FP8
+  // up projection measured slower this way (M = 1 / 16: 26.1 / 27.5 against
+  // 24.1 / 25.9 us).
   p.kb = 1;
-  const bool kb2 = tn.sk_kb >= 0 ? tn.sk_kb == 2 : plain_cluster4;
+  const bool kb2 = tn.sk_kb >= 0 ? tn.sk_kb == 2
+                                 : (plain && fp8 && weight_bytes > kSkinnyClusterMaxWeightBytes);
   if (fp8 && n <= 64 && kb2) {
     p.kb = 2;
     nb = 1;
@@ -1097,15 +1100,16 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   //   64 KB with the 128-column groups of larger M (M = 96 / 128 / 256: 26.9
   //   / 27.1 / 32.3 us against 28.7 / 29.0 / 34.0 at 256 KB; FP8 M = 256:
   //   26.9 against 28.1).
-  // - FP8 down projection in 4-CTA clusters: 384 KB too (M = 16 / 32 / 64:
-  //   15.8 / 16.8 / 18.5 us against 16.3 / 17.2 / 18.6 without; 64 or 128 KB
-  //   measured slower than none, and all 448 KB of a CTA's range no faster).
+  // - FP8 down projection with units of two k blocks (stream-K, or 4-CTA
+  //   clusters): 384 KB too (clusters, M = 16 / 32 / 64: 15.8 / 16.8 / 18.5
+  //   us against 16.3 / 17.2 / 18.6 without; 64 or 128 KB measured slower
+  //   than none, and all 448 KB of a CTA's range no faster).
   uint32_t pf_bytes = kPrefetchBytes;
   if (plain)
     pf_bytes = nb == 1 ? kPrefetchBytes / 8 : (fp8 ? kPrefetchBytes / 4 * 3 : kPrefetchBytes);
   else if (!fp8 && nb < 4)
     pf_bytes = kPrefetchBytes / 4 * 3;
-  if (plain_cluster4) pf_bytes = kPrefetchBytes / 4 * 3;
+  if (plain && fp8 && p.kb == 2) pf_bytes = kPrefetchBytes / 4 * 3;
   p.prefetch_units = tn.sk_prefetch_units >= 0 ? tn.sk_prefetch_units
                                                : (int)(pf_bytes / ((uint32_t)(nb * p.kb) * kSubBytes));
   const int64_t sub_cols = plain ? 2 * kCB : kCB;

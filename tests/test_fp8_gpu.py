@@ -263,3 +263,14 @@ def test_fp8_two_k_blocks_per_unit(op, mode, shape, monkeypatch):
     else:
         down_check(*shape, "skinny", seed=sum(shape))
     swg.check_device_status()
+
+
+@pytest.mark.parametrize("shape", [(7, 1040, 520), (12, 14336, 4096)])
+def test_fp8_down_one_k_block_per_unit(shape, monkeypatch):
+    # The FP8 down projection's stream-K units default to two k blocks above
+    # 32 MB of weights; one block per unit (SWIGLU_SK_KB=1) stays a valid
+    # form, and is the default for small weights and above 64 rows
+    monkeypatch.setenv("SWIGLU_SK_KB", "1")
+    monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")
+    down_check(*shape, "skinny", seed=sum(shape), rows=[0, shape[0] - 1])
+    swg.check_device_status()
