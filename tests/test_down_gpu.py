@@ -236,3 +236,37 @@ def test_large_model_stream_k_with_bulk_final_sums():
     assert p["path"] == "skinny" and p["cluster"] == 1 and p["workspace"] > 0
     assert p["launches"] == 2
     check(M, d_ff, d, "auto", seed=91, rows=np.array([0, 17, 40, 63]))
+
+
+@pytest.mark.parametrize("M", [1, 16, 48])
+def test_back_to_back_calls_on_two_weight_sets(M):
+    # d_ff = 14336 -> d = 4096, two kernels per call, whose sum kernel lets
+    # the next call's GEMM start (and prefetch its weights) before the sums
+    # are done: six calls back to back, alternating two weight matrices and
+    # each with its own h and output, equal the same calls made one at a
+    # time bit for bit, and match the oracle
+    d_ff, d = 14336, 4096
+    ws = [inputs.make_inputs(1, d_ff, d, "bf16", seed=300 + j)[1] for j in range(2)]
+    wds = [w.to(DEV) for w in ws]
+    hs = [inputs.make_inputs(M, d_ff, 8, "bf16", seed=310 + i, x_only=True)[0] for i in range(6)]
+    r = inputs.make_inputs(M, d, 8, "bf16", seed=320, x_only=True)[0]
+    hd, rd = [h.to(DEV) for h in hs], r.to(DEV)
+    assert swg.down_plan(M, d_ff, d)["launches"] == 2
+    alone = []
+    for i in range(6):
+        alone.append(swg.swiglu_down(hd[i], wds[i % 2], residual=rd))
+        torch.cuda.synchronize()
+    ys = [torch.full((M, d), float("nan"), dtype=torch.bfloat16, device=DEV) for _ in range(6)]
+    for i in range(6):
+        swg.swiglu_down(hd[i], wds[i % 2], residual=rd, out=ys[i])
+    torch.cuda.synchronize()
+    for i in range(6):
+        assert torch.equal(alone[i].view(torch.int16), ys[i].view(torch.int16)), (M, i)
+    raw = inputs.raw_bits
+    rows = np.unique(np.linspace(0, M - 1, 3).astype(int))
+    for i in (0, 5):
+        y64, _, s = oracle.down_proj(raw(hs[i][rows].contiguous()), raw(ws[i % 2]), oracle.BF16,
+                                     raw(r[rows].contiguous()))
+        res = compare(to64(ys[i])[rows], y64, s, "bf16", d_ff)
+        assert res["ok"], (M, i, res)
+    swg.check_device_status()

@@ -151,6 +151,46 @@ def test_down_projection_in_a_graph(M):
 
 
 @pytest.mark.parametrize("M", [1, 16])
+def test_down_chain_in_a_graph(M):
+    # Three bf16 down projections (d_ff = 14336 -> d = 4096) captured back to
+    # back, each on its own h and output: every call's sum kernel releases
+    # the next call's GEMM early.  Replays equal the direct calls bit for bit
+    # and match the oracle.
+    d_ff, d = 14336, 4096
+    dev = torch.device("cuda", 0)
+    _, wd, _ = inputs.make_inputs(1, d_ff, d, "bf16", seed=191)
+    wds = wd.to(dev)
+    hs = [inputs.make_inputs(M, d_ff, 8, "bf16", seed=192 + i, x_only=True)[0].to(dev)
+          for i in range(3)]
+    r = inputs.make_inputs(M, d, 8, "bf16", seed=195, x_only=True)[0]
+    rs = r.to(dev)
+    ys = [torch.empty(M, d, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    for i in range(3):
+        swg.swiglu_down(hs[i], wds, residual=rs, out=ys[i])
+        torch.cuda.synchronize()
+    direct = [y.clone() for y in ys]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(3):
+            swg.swiglu_down(hs[i], wds, residual=rs, out=ys[i])
+    for y in ys:
+        y.fill_(float("nan"))
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for i in range(3):
+        assert torch.equal(direct[i].view(torch.int16), ys[i].view(torch.int16)), i
+    raw = inputs.raw_bits
+    h_host = hs[1].cpu()
+    rows = np.unique(np.linspace(0, M - 1, 4).astype(int))
+    y64, _, s = oracle.down_proj(raw(h_host[rows].contiguous()), raw(wd), oracle.BF16,
+                                 raw(r[rows].contiguous()))
+    res = compare(ys[1].to("cpu", torch.float64).numpy()[rows], y64, s, "bf16", d_ff)
+    assert res["ok"], (M, res)
+    swg.check_device_status()
+
+
+@pytest.mark.parametrize("M", [1, 16])
 def test_fp8_down_chain_in_a_graph(M):
     # The FP8 down projection, d_ff = 14336 -> d = 4096: M = 1 runs three
     # kernels (quantize h, partial sums, their sum, which releases the next
