@@ -1010,11 +1010,16 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
     const int64_t slots2 = per2 > 0 ? (n_kb2 + per2 - 1) / per2 + 1 : 1;
     const int64_t limit = fp8 ? (int64_t)128 << 10 : (int64_t)256 << 10;
     // With the bf16 sums in a second kernel (the default, below) no single
-    // CTA reads a group's partials, and 256-column groups lead up to 48 rows
-    // (measured, 2 GiB of weights rotating, d = 4096, M = 32 / 48 / 64 / 128:
-    // 22.8 / 25.6 / 26.0 / 27.3 us against 23.6 / 25.8 / 26.0 / 27.0).
+    // CTA reads a group's partials, and 256-column groups, whose sum kernel
+    // releases the next GEMM early, lead up to 128 rows where the sums are a
+    // large share of the call (measured, 2 GiB of weights rotating, d = 4096,
+    // 117 MB: M = 32 / 64 / 96 / 128 take 21.7 / 23.6 / 23.5 / 24.7 us
+    // against 22.7 / 24.4 / 24.9 / 25.3 with 128-column groups), and up to 64
+    // rows above 256 MB (d = 8192, 484 MB: M = 64 / 128 take 76.2 / 81.8 us
+    // against 77.5 / 80.1).
     const bool two_kernels = !fp8 && tn.sk_split != 0;
-    if (two_kernels ? M > 48 : slots2 * 4 * kCB * 4 * M > limit) nb = 1;
+    const int64_t max_m2 = weight_bytes > ((int64_t)256 << 20) ? 64 : 128;
+    if (two_kernels ? M > max_m2 : slots2 * 4 * kCB * 4 * M > limit) nb = 1;
   }
   // FP8 down projections of 16-64 rows: 4-CTA clusters of 128-column groups,
   // when all the groups' clusters fit at once (n_out up to 36 x 128 on
@@ -1096,7 +1101,9 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   //   next GEMM early (launch_skinny): 512 KB for bf16 (M = 1 / 16 / 48:
   //   20.9 / 21.5 / 23.7 us against 22.0 / 22.9 / 25.7 at 384 KB; the 256 KB
   //   of the one-kernel form, without the early release: 22.6 / 22.8 / 26.2),
-  //   384 KB for FP8 (M = 1 / 8: 15.6 / 16.2 against 15.9 / 16.4 at 256 KB);
+  //   384 KB above 64 rows (M = 96 / 128: 23.7 / 24.7 us against 24.2 / 25.8
+  //   at 512 KB), 384 KB for FP8 with one k block per unit (M = 1 / 8: 15.6
+  //   / 16.2 against 15.9 / 16.4 at 256 KB);
   //   64 KB with the 128-column groups of larger M (M = 96 / 128 / 256: 26.9
   //   / 27.1 / 32.3 us against 28.7 / 29.0 / 34.0 at 256 KB; FP8 M = 256:
   //   26.9 against 28.1).
@@ -1106,7 +1113,8 @@ SkinnyPlan plan_skinny(int64_t M, int64_t K, int64_t n_out, int num_sms, bool pl
   //   than none, and all 448 KB of a CTA's range no faster).
   uint32_t pf_bytes = kPrefetchBytes;
   if (plain)
-    pf_bytes = nb == 1 ? kPrefetchBytes / 8 : (fp8 ? kPrefetchBytes / 4 * 3 : kPrefetchBytes);
+    pf_bytes = nb == 1 ? kPrefetchBytes / 8
+                       : (fp8 || M > 64 ? kPrefetchBytes / 4 * 3 : kPrefetchBytes);
   else if (!fp8 && nb < 4)
     pf_bytes = kPrefetchBytes / 4 * 3;
   if (plain && fp8 && p.kb == 2) pf_bytes = kPrefetchBytes / 4 * 3;

@@ -180,16 +180,16 @@ def test_dispatch_rule(cuda_lib):
 
 
 def test_down_projection_column_groups(cuda_lib, monkeypatch):
-    # 256-column groups (11 partial slots at d = 4096) until their partial
-    # sums pass 256 KB per group, then 128-column groups (6 slots)
-    # (stream-K mode forced: at d = 4096 the down projection takes 4-CTA
-    # clusters from M = 24 on)
+    # 256-column groups (11 partial slots at d = 4096) up to 128 rows, then
+    # 128-column groups (6 slots); stream-K mode forced at d = 4096
     monkeypatch.setenv("SWIGLU_SK_CLUSTER", "0")
     assert swg.down_plan(16, 14336, 4096, "bf16", "skinny", 152)["slices"] == 11
-    assert swg.down_plan(64, 14336, 4096, "bf16", "skinny", 152)["slices"] == 6
+    assert swg.down_plan(128, 14336, 4096, "bf16", "skinny", 152)["slices"] == 11
+    assert swg.down_plan(129, 14336, 4096, "bf16", "skinny", 152)["slices"] == 6
     monkeypatch.delenv("SWIGLU_SK_CLUSTER")
-    assert swg.down_plan(32, 29568, 8192, "bf16", "skinny", 152)["slices"] == 6
-    assert swg.down_plan(64, 29568, 8192, "bf16", "skinny", 152)["slices"] == 4
+    # above 256 MB of weights, 256-column groups up to 64 rows
+    assert swg.down_plan(64, 29568, 8192, "bf16", "skinny", 152)["slices"] == 6
+    assert swg.down_plan(65, 29568, 8192, "bf16", "skinny", 152)["slices"] == 4
     # small weights stay in cluster mode; the up projection keeps its groups
     assert swg.down_plan(256, 4864, 896, "bf16", "skinny", 152)["cluster"] == 8
     assert swg.plan(32, 4096, 14336, "bf16", "skinny", 152)["slices"] == 3

@@ -86,7 +86,8 @@ def slots(units, grid, n_kb):
 @pytest.mark.parametrize("split", ["default", "0"])
 def test_down_projection_column_group_rule(cuda_lib, split, monkeypatch):
     # No override, sums in a second kernel (the bf16 default): 256-column
-    # groups up to 48 rows, 128-column groups above.  With the group's last
+    # groups up to 128 rows (64 above 256 MB of weights), 128-column groups
+    # above.  With the group's last
     # CTA adding the sums (SWIGLU_SK_SPLIT=0): 128-column groups once
     # 256-column groups would collect more than 256 KB of partial sums per
     # group (slots x 256 columns x M x 4 B).  Either way every group has
@@ -101,7 +102,7 @@ def test_down_projection_column_group_rule(cuda_lib, split, monkeypatch):
             if split == "0":
                 nb = 1 if slots(units2, grid2, n_kb2) * 256 * 4 * M > 256 * 1024 else 2
             else:
-                nb = 1 if M > 48 else 2
+                nb = 1 if M > (64 if d_ff * d * 2 > 256 << 20 else 128) else 2
             _, n_cb, n_kb, units, grid = geometry(M, d_ff, d, nb, True, 152)
             assert p["slices"] == slots(units, grid, n_kb), (M, d, nb)
             assert p["slices"] >= max_contributors(units, grid, n_kb, n_cb)
