@@ -179,6 +179,20 @@ def test_dispatch_rule(cuda_lib):
         swg.plan(4, 64, 64, "f32", "tc", 152)
 
 
+def test_up_projection_unit_width_rule(cuda_lib):
+    # Above 32 MB of weights the up projection's units hold four 64-column
+    # blocks up to 8 rows and two from 9 rows on; at d = 4096, d_ff = 14336
+    # on 152 SMs that is 4 partial slots per column group against 3, and one
+    # launch either way (the final sums stay in the kernel)
+    for M in range(1, 17):
+        p = swg.plan(M, 4096, 14336, "bf16", "auto", 152)
+        assert p["path"] == "skinny" and p["cluster"] == 1 and p["launches"] == 1
+        assert p["slices"] == (4 if M <= 8 else 3), (M, p)
+    assert [swg.plan(M, 8192, 29568, "bf16", "auto", 152)["slices"] for M in (8, 9)] == [3, 2]
+    # small weights keep cluster mode (the SIMT cluster form at one row)
+    assert swg.plan(8, 896, 4864, "bf16", "auto", 152)["cluster"] == 2
+
+
 def test_down_projection_column_groups(cuda_lib, monkeypatch):
     # 256-column groups (11 partial slots at d = 4096) up to 128 rows, then
     # 128-column groups (6 slots); stream-K mode forced at d = 4096
