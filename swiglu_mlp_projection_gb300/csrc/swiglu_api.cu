@@ -144,9 +144,9 @@ int stream_workspace(int dev, cudaStream_t st, size_t part_bytes, float** part,
   *part = nullptr;
   *counters = nullptr;
   if (st == cudaStreamPerThread || part_bytes > kMaxCachedPartBytes) return SWIGLU_OK;
-  // A call being captured into a CUDA graph gets its own allocation (alloc
-  // and free nodes inside the graph): a replay may run on another stream,
-  // unordered with later calls that would share this stream's buffer.
+  // A call being captured into a CUDA graph does not use this stream's
+  // buffer: a replay may run on another stream, unordered with later calls
+  // that would share it.  It takes its capture's slice (graph_workspace).
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
     cudaGetLastError();
@@ -660,8 +660,10 @@ int run(const Call& c) {
     return fail(SWIGLU_ERR_UNSUPPORTED,
                 "[N, K] weights are served by the tensor-core paths (bf16) only");
   if (p.path == SWIGLU_PATH_SIMT && p.simt.fused) {
-    // Inside a CUDA graph the workspace is a fresh allocation per call whose
-    // counters would need a memset node; two kernel nodes cost less.
+    // Inside a CUDA graph the two-launch form is kept: it needs no arrival
+    // counters.  (It was chosen when a captured call's workspace needed a
+    // memset node; the zeroed slices of graph_workspace have not been
+    // measured with the single launch.)
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(c.st, &cs) != cudaSuccess) {
       cudaGetLastError();
